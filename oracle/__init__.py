@@ -1,0 +1,8 @@
+"""OSCAR CPU oracle (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` import this package.  It wraps ``oscar_oracle.cpp`` (plain fp64
+C++, single-threaded) through ctypes and shares nothing with the CUDA library.
+"""
+
+from .oracle import *  # noqa: F401,F403

@@ -1,0 +1,77 @@
+"""Planted-mistake check of the oracle pins (CPU only).
+
+Each mutant is a copy of the oracle source with one plausible mistake (a
+dropped term, a wrong sign or index, a transposed operand, a wrong rounding).
+It is compiled into a temporary library and every pin is run against it; at
+least one pin must fail, otherwise the pins would not notice that mistake.
+"""
+
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle_pins
+from oracle import oracle as O
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "oscar_oracle.cpp")
+
+# (name, text in the oracle, replacement, expected number of occurrences)
+MUTANTS = [
+    ("rotation_transposed",
+     "orc_bf16_to_f64(x_bf16[i]) * static_cast<double>(R[static_cast<size_t>(i) * D + j])",
+     "orc_bf16_to_f64(x_bf16[i]) * static_cast<double>(R[static_cast<size_t>(j) * D + i])", 1),
+    ("clip_lower_bound_dropped", "    if (x[j] < -c) x[j] = -c;\n", "", 1),
+    ("scale_divisor_4", "(mx - mn) / 3.0", "(mx - mn) / 4.0", 1),
+    ("zero_is_max", "const float z32 = static_cast<float>(mn);", "const float z32 = static_cast<float>(mx);", 1),
+    ("code_floor_not_rint", "double c = std::nearbyint(u);", "double c = std::floor(u);", 1),
+    ("packing_reversed_in_byte", "(c << (2 * (j % 4)))", "(c << (2 * (3 - j % 4)))", 1),
+    ("unrotation_not_transposed",
+     "acc_rot[j] * static_cast<double>(R_v[static_cast<size_t>(c) * D + j])",
+     "acc_rot[j] * static_cast<double>(R_v[static_cast<size_t>(j) * D + c])", 1),
+    ("window_ring_index", "* W + (p % W);", "* W + (p - win_begin);", 2),
+    ("gqa_mapping_modulo", "const int h = hq / gqa;", "const int h = hq % H;", 2),
+    ("dequant_drops_zero", "x[j] = c * s + z;", "x[j] = c * s;", 1),
+    ("f16_truncates", "std::nearbyint(a / quantum) * quantum", "std::trunc(a / quantum) * quantum", 1),
+    ("default_scale_1_over_D", "sm_scale = 1.0 / std::sqrt(static_cast<double>(D));", "sm_scale = 1.0 / D;", 2),
+    ("key_reads_value_codes", "page, h, 0, p % P, kk);", "page, h, 1, p % P, kk);", 1),
+    ("softmax_denominator_counts_tokens", "    denom += w;\n", "    denom += 1.0;\n", 1),
+    ("query_rotation_transposed",
+     "qv[i] * static_cast<double>(Rk[static_cast<size_t>(i) * D + j])",
+     "qv[i] * static_cast<double>(Rk[static_cast<size_t>(j) * D + i])", 1),
+    ("all_groups_use_group0", "orc_group_params(G, y.data() + g * G, &s_bits, &z_bits);",
+     "orc_group_params(G, y.data(), &s_bits, &z_bits);", 1),
+    ("scale_zero_swapped", "sz[2 * g + 0] = s_bits;\n          sz[2 * g + 1] = z_bits;",
+     "sz[2 * g + 0] = z_bits;\n          sz[2 * g + 1] = s_bits;", 1),
+    ("bulk_offset_uses_page_index", "orc_dequant_row(d, int2_pages, scale_zero_pages, page, h, 1, p % P, vv);",
+     "orc_dequant_row(d, int2_pages, scale_zero_pages, page, h, 1, (p / P) % P, vv);", 1),
+]
+
+
+@pytest.fixture(scope="module")
+def workdir():
+    with tempfile.TemporaryDirectory(prefix="oracle_mutants_") as d:
+        yield d
+
+
+@pytest.mark.parametrize("name,old,new,count", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, count, workdir):
+    with open(SRC) as f:
+        src = f.read()
+    assert src.count(old) == count, f"mutation site for {name} not found {count} time(s)"
+    path = os.path.join(workdir, f"{name}.cpp")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    lib_path = os.path.join(workdir, f"lib{name}.so")
+    subprocess.run(["g++", "-O1", "-std=c++17", "-ffp-contract=off", "-shared", "-fPIC", path, "-o", lib_path],
+                   check=True)
+    lib = O.load(lib_path)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError):
+            caught.append(pin.__name__)
+            break
+    assert caught, f"no pin catches the planted mistake '{name}'"
