@@ -1,0 +1,507 @@
+#!/usr/bin/env python
+"""Benchmark of the OSCAR decode step (INT2 rotated KV append + mixed-precision
+paged decode) on one GB300, printing one JSON line.
+
+A step is one decode step of a batch: oscar_append of each sequence's current
+token, then oscar_decode over the whole cache.  The default workload is the
+batch-1 long decode (32 query / 8 KV heads, head_dim 128, context 32768, sink
+64 + window 128 in BF16, group 64, shuffled pages).  Its cache (21.7 MB) fits
+in L2, so the benchmark builds enough independent cache replicas (disjoint
+pages of one pool) that the replicas together exceed 3x the L2 size and
+cycles through them, one replica per step.
+
+The K timed steps are captured in CUDA graphs and timed with CUDA events on
+the launching stream; W warm-up steps run first.  Also reported: the decode
+alone (roofline of the dominant kernel), the in-repo BF16 paged decode over
+the same tokens (speedup reference), an end-to-end figure through the public
+API with host buffers, and the fp64 CPU oracle on a bounded sample.
+
+--impl reference times that oracle instead (the slow CPU restatement of the
+same computation), on the same workload and metric.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+import types
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "oscar_decode HBM GB/s (% of peak) & tokens/s; INT2 vs BF16 decode speedup"
+
+
+# --------------------------------------------------------------------------- helpers
+
+def algorithmic_bytes_decode(w, batch_lens, n_q_heads=None, n_kv_heads=None):
+    """Bytes a decode step must move: INT2 codes + scale/zero of bulk tokens, BF16
+    sink/window tokens, q in and fp32 out (rotations and page tables not counted).
+    ``w`` is anything with num_q_heads, num_kv_heads, head_dim, group_size,
+    sink_len and window_len attributes."""
+    H = w.num_kv_heads if n_kv_heads is None else n_kv_heads
+    Hq = w.num_q_heads if n_q_heads is None else n_q_heads
+    D, G, S, W = w.head_dim, w.group_size, w.sink_len, w.window_len
+    per_bulk = 2 * (D // 4) + 2 * (D // G) * 2 * 2
+    per_bf16 = 2 * D * 2
+    total = 0
+    for L in batch_lens:
+        n_bf16 = min(S, L) + max(0, L - max(S, L - W))
+        n_bulk = L - n_bf16
+        total += H * (n_bulk * per_bulk + n_bf16 * per_bf16)
+    total += len(batch_lens) * Hq * D * (2 + 4)
+    return total
+
+
+def algorithmic_bytes_append(w, n_tokens):
+    D, G, H = w.head_dim, w.group_size, w.num_kv_heads
+    return n_tokens * (H * 2 * D * 2 + 8 + H * (2 * (D // 4) + 2 * (D // G) * 2 * 2))
+
+
+def algorithmic_bytes_bf16(w, batch_lens):
+    return sum(w.num_kv_heads * L * 2 * w.head_dim * 2 for L in batch_lens) + \
+        len(batch_lens) * w.num_q_heads * w.head_dim * (2 + 4)
+
+
+class ClockSampler:
+    """Background nvidia-smi sampler of SM clocks and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.interval = interval_ms
+        self._thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.interval)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.perf_counter(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        used = inside
+        where = "timed_region"
+        if not inside:  # region shorter than the sampling interval: nearest samples
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            used = [p for (_, p) in near]
+            where = "adjacent_to_timed_region"
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in used if num(p[1]) is not None]
+        mx = [num(p[2]) for p in used if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in used for i in range(4) if p[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(used), "where": where}
+
+
+def measured_peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle timed on the host cores, one rank only."""
+    if rank != 0:
+        return
+    import concurrent.futures
+    import numpy as np
+    import torch
+
+    from int2_rotated_kv_append_gb300 import synth
+    from int2_rotated_kv_append_gb300.synth import bits16
+    from oracle import oracle as O
+
+    O.build_oracle()
+    w = synth.make_config(args.config)
+    # The oracle's own append builds the cache it then decodes (host memory).
+    codes = np.zeros(w.num_pages * w.num_kv_heads * 2 * 16 * w.head_dim // 4, np.uint8)
+    sz = np.zeros(w.num_pages * w.num_kv_heads * 2 * 16 * (w.head_dim // w.group_size) * 2, np.uint16)
+    kb, vb = bits16(w.k), bits16(w.v)
+    Rk, Rv, ck, cv = (t.cpu().numpy() for t in (w.R_k, w.R_v, w.clip_k, w.clip_v))
+    slots = w.slot_mapping.numpy()
+    threads = min(os.cpu_count() or 1, 32)
+    chunks = np.array_split(np.arange(w.num_tokens), threads)
+
+    def app(ix):
+        O.append(w.dims, kb[ix], vb[ix], Rk, Rv, ck, cv, slots[ix], codes, sz)
+    with concurrent.futures.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(app, chunks))
+    sink, win = w.sink_window()
+    sinkb, winb, qb = bits16(sink), bits16(win), bits16(w.q)
+    pt, lens = w.page_table.numpy(), w.seq_lens.numpy()
+    gqa = w.num_q_heads // w.num_kv_heads
+
+    def sample_step(i, L):
+        # one KV head's query group over the first L tokens of sequence 0, GQA heads in parallel threads
+        h = i % w.num_kv_heads
+        lens_s = lens.copy()
+        lens_s[0] = L
+        pairs = [[(0, h * gqa + j)] for j in range(gqa)]
+        with concurrent.futures.ThreadPoolExecutor(gqa) as ex:
+            list(ex.map(lambda pr: O.decode(w.dims, w.batch, qb, Rk, Rv, codes, sz, sinkb, winb, pt, lens_s,
+                                            w.sink_len, w.window_len, 0.0, pairs=pr), pairs))
+    # Calibrate the sample length so the whole run stays within ~2 minutes.
+    L_full = int(lens[0])
+    t = time.perf_counter()
+    sample_step(0, L_full)
+    t_full = time.perf_counter() - t
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    frac = min(1.0, budget / max(t_full, 1e-6))
+    L = max(w.sink_len + w.window_len + 16, int(L_full * frac))
+    for i in range(args.warmup):
+        sample_step(i, L)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        sample_step(i, L)
+    el = time.perf_counter() - t
+    step_bytes = algorithmic_bytes_decode(w, [L], n_q_heads=gqa, n_kv_heads=1)
+    value = step_bytes * args.steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": synth.CONFIG_NAMES[args.config], "batch": 1, "seq_len": L_full},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": gqa, "kind": "oracle",
+                         "sample": f"per step: the {gqa} query heads of one KV head of sequence 0 over its first "
+                                   f"{L} of {L_full} tokens (fp64 oracle, one thread per query head)"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import int2_rotated_kv_append_gb300 as ok
+    from int2_rotated_kv_append_gb300 import build as okbuild
+    from int2_rotated_kv_append_gb300 import synth
+    from int2_rotated_kv_append_gb300.cache import Bf16Cache, Int2Cache
+
+    okbuild.build()
+    ok.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    base_lens = synth.config_seq_lens(args.config)
+    B = len(base_lens)
+    # Number of replicas so that the cycled caches exceed 3x L2 (shape of one replica from a tiny draw).
+    one = types.SimpleNamespace(num_q_heads=64 if args.config == 3 else 32, num_kv_heads=8, head_dim=128,
+                                group_size=64, sink_len=64, window_len=256 if args.config == 3 else 128)
+    w0_bytes = algorithmic_bytes_decode(one, base_lens)
+    NR = max(1, math.ceil(3 * l2 / w0_bytes)) if args.replicas <= 0 else args.replicas
+    w = synth.make_config(args.config, device=dev, replicas=NR)
+    cache = Int2Cache(w, device=dev)
+    cache.prefill()
+    bf = Bf16Cache(w, device=dev)
+    bf.prefill()
+    torch.cuda.synchronize()
+
+    H, Hq, D = w.num_kv_heads, w.num_q_heads, w.head_dim
+    lens_all = w.seq_lens.tolist()
+    msl = max(lens_all)
+    # Current token (position L-1) of every sequence: the K/V appended by each step.
+    starts = np.cumsum([0] + lens_all)[:-1]
+    cur = torch.as_tensor(starts + np.array(lens_all) - 1, dtype=torch.long)
+    k_cur = w.k[cur.to(dev)].contiguous()
+    v_cur = w.v[cur.to(dev)].contiguous()
+    s_cur = w.slot_mapping[cur].to(dev).contiguous()
+    q = w.q.contiguous()
+    out = torch.empty((w.batch, Hq, D), dtype=torch.float32, device=dev)
+    out_bf = torch.empty_like(out)
+    ws = cache.workspace(msl)
+    ws_bf = bf.workspace()
+
+    def views(r):
+        sl = slice(r * B, (r + 1) * B)
+        return dict(k=k_cur[sl], v=v_cur[sl], slots=s_cur[sl], q=q[sl], pt=cache.page_table[sl],
+                    lens=cache.seq_lens[sl], sink=cache.sink[sl], win=cache.window[sl], out=out[sl],
+                    out_bf=out_bf[sl], bpt=bf.page_table[sl], blens=bf.seq_lens[sl])
+    V = [views(r) for r in range(NR)]
+    msl_r = [max(lens_all[r * B:(r + 1) * B]) for r in range(NR)]
+
+    def append_r(r):
+        x = V[r]
+        ok.oscar_append(w.dims, x["k"], x["v"], cache.R_k, cache.R_v, cache.clip_k, cache.clip_v, x["pt"],
+                        x["slots"], cache.int2_pages, cache.scale_zero)
+
+    def decode_r(r):
+        x = V[r]
+        ok.oscar_decode(w.dims, B, msl_r[r], cache.pps, x["q"], cache.R_k, cache.R_v, cache.int2_pages,
+                        cache.scale_zero, x["sink"], x["win"], x["pt"], x["lens"], w.sink_len, w.window_len, 0.0,
+                        x["out"], ws)
+
+    def bf16_r(r):
+        x = V[r]
+        ok.oscar_bf16_decode(w.dims, B, msl_r[r], 0, x["q"], bf.pages, x["bpt"], x["blens"], 0.0, x["out_bf"],
+                             ws_bf)
+
+    def step(i):
+        r = i % NR
+        append_r(r)
+        decode_r(r)
+
+    def capture(fn, n):
+        """CUDA graph of a chunk of calls fn(0..per-1), replayed n // per times (per | n, per <= 1000)."""
+        per = n if n <= 1000 else next(d for d in range(1000, 0, -1) if n % d == 0)
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(min(3, n)):
+                fn(i)
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(per):
+                fn(i)
+        return g, n // per
+
+    def timed(fn, n, warm):
+        g, reps = capture(fn, n)
+        if warm > 0:
+            gw, rw = capture(fn, warm)
+            for _ in range(rw):
+                gw.replay()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        e1.synchronize()
+        t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            tt = torch.tensor([ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms = float(tt.item())
+        return ms, (t0, t1)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.1)
+    K, Wm = args.steps, args.warmup
+    ms, (t0, t1) = timed(step, K, Wm)
+    clocks = sampler.summary(t0, t1)
+    # Decode alone and the BF16 reference decode over the same tokens.
+    ms_dec, _ = timed(lambda i: decode_r(i % NR), K, Wm)
+    ms_bf, _ = timed(lambda i: bf16_r(i % NR), K, Wm)
+    ms_app, _ = timed(lambda i: append_r(i % NR), K, Wm)
+    sampler.stop()
+
+    step_bytes_dec = algorithmic_bytes_decode(w, lens_all[:B])
+    step_bytes_app = algorithmic_bytes_append(w, B)
+    step_bytes = step_bytes_dec + step_bytes_app
+    ms_step = ms / K
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    dec_us = ms_dec / K * 1e3
+    achieved = step_bytes_dec / (dec_us * 1e-6) / 1e9
+    peak, peak_kind = measured_peak_hbm()
+    bf_us = ms_bf / K * 1e3
+
+    # End to end through the public API with pinned host buffers.
+    E = min(K, 2000)
+    q_h = q.cpu().pin_memory()
+    k_h, v_h, s_h = k_cur.cpu().pin_memory(), v_cur.cpu().pin_memory(), s_cur.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def e2e_step(i):
+        r = i % NR
+        sl = slice(r * B, (r + 1) * B)
+        x = V[r]
+        x["q"].copy_(q_h[sl], non_blocking=True)
+        x["k"].copy_(k_h[sl], non_blocking=True)
+        x["v"].copy_(v_h[sl], non_blocking=True)
+        x["slots"].copy_(s_h[sl], non_blocking=True)
+        append_r(r)
+        decode_r(r)
+        out_h[sl].copy_(x["out"], non_blocking=True)
+        stream.synchronize()
+    for i in range(min(50, E)):
+        e2e_step(i)
+    barrier()
+    te = time.perf_counter()
+    for i in range(E):
+        e2e_step(i)
+    te = time.perf_counter() - te
+    e2e_ms = te / E * 1e3
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    h2d = B * (Hq * D * 2 + 2 * H * D * 2 + 8)
+    d2h = B * Hq * D * 4
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, cache, B, step_bytes)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": Wm,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": synth.CONFIG_NAMES[args.config] + ": decode step = append current token + "
+                                   "mixed-precision paged decode",
+                       "batch": B, "seq_len": msl, "num_q_heads": Hq, "num_kv_heads": H, "head_dim": D,
+                       "sink": w.sink_len, "window": w.window_len, "group": w.group_size, "page_size": 16,
+                       "pages_per_split": "auto" if cache.pps == 0 else cache.pps,
+                       "l2_policy": f"inputs larger than L2: {NR} cache replicas in disjoint pages, "
+                                    f"{NR * step_bytes_dec / 1e6:.0f} MB cycled (L2 {l2 / 1e6:.0f} MB)"},
+            "tokens_per_s": world * B / (ms_step * 1e-3),
+            "us_per_step": ms_step * 1e3,
+            "decode_us": dec_us, "append_us": ms_app / K * 1e3, "bf16_decode_us": bf_us,
+            "speedup_vs_bf16": bf_us / dec_us,
+            "bf16_decode_GBps": algorithmic_bytes_bf16(w, lens_all[:B]) / (bf_us * 1e-6) / 1e9,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "kernel": "oscar_decode (q-rotate + split + merge) per launch",
+                         "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_launch": step_bytes_dec},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": K * 4,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(w, cache, B, step_bytes):
+    """The oracle, as it stands, on one full step of replica 0 (append + decode),
+    repeated up to ~10 s; one thread per (sequence, query head)."""
+    import concurrent.futures
+
+    import numpy as np
+    import torch
+
+    from int2_rotated_kv_append_gb300.synth import bits16
+    from oracle import oracle as O
+
+    O.build_oracle()
+    codes = cache.int2_pages.cpu().numpy()
+    sz = cache.scale_zero.view(torch.int16).cpu().numpy().view(np.uint16)
+    sinkb, winb = bits16(cache.sink), bits16(cache.window)
+    qb = bits16(w.q)
+    Rk, Rv, ck, cv = (t.cpu().numpy() for t in (w.R_k, w.R_v, w.clip_k, w.clip_v))
+    pt, lens = w.page_table.numpy(), w.seq_lens.numpy()
+    lens_all = lens.tolist()
+    starts = np.cumsum([0] + lens_all)[:-1]
+    cur = starts[:B] + np.array(lens_all[:B]) - 1
+    kb, vb = bits16(w.k[torch.as_tensor(cur, device=w.k.device)]), bits16(w.v[torch.as_tensor(cur, device=w.k.device)])
+    slots = w.slot_mapping.numpy()[cur]
+    pairs = [(b, h) for b in range(B) for h in range(w.num_q_heads)]
+    threads = max(1, min(os.cpu_count() or 1, len(pairs)))
+
+    def one_step():
+        O.append(w.dims, kb, vb, Rk, Rv, ck, cv, slots, codes, sz)
+        with concurrent.futures.ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda pr: O.decode(w.dims, w.batch, qb, Rk, Rv, codes, sz, sinkb, winb, pt, lens,
+                                            w.sink_len, w.window_len, 0.0, pairs=[pr]), pairs))
+    n, t = 0, time.perf_counter()
+    while True:
+        one_step()
+        n += 1
+        el = time.perf_counter() - t
+        if el > 10.0 or n >= 20:
+            break
+    return {"value": step_bytes * n / el / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} full step(s) of one replica (append of {B} token(s) + decode of {len(pairs)} "
+                      f"(sequence, query head) pairs), fp64 oracle, {threads} threads",
+            "s_per_step": el / n}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3],
+                    help="workload: 1 batch-1 32K (default), 2 batch-64 mixed lengths, 3 batch-4 131K")
+    ap.add_argument("--replicas", type=int, default=0, help="cache replicas (0: enough to exceed 3x L2)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,189 @@
+/*
+ * oscar.h -- C ABI of the OSCAR INT2 rotated KV-cache library (GB300, sm_103a).
+ *
+ * The method ("OSCAR: Offline Spectral Covariance-Aware Rotation for 2-bit KV
+ * Cache Quantization"; strixaai.com summary, agentlenshq.com project card and
+ * the paper abstract at thelatestinai.com/papers/2605.17757):
+ *   - new K/V head vectors are multiplied by a fixed orthogonal rotation R and
+ *     clipped to fixed per-channel thresholds, both found offline
+ *     (summary "Practical Summary"; project card "How it works");
+ *   - the bulk of the KV cache is stored in 2 bits, inside a paged KV cache
+ *     (abstract: "custom INT2 attention kernel ... compatible with paged
+ *     KV-cache serving");
+ *   - a small sink of initial tokens and a recent window stay in BF16 and are
+ *     attended together with the INT2 bulk (project card "How it works").
+ * The pages print no formulas; the readings below are stated at each call.
+ *
+ * Conventions shared by every call
+ *   - Pointers named as device buffers must point to device memory (or
+ *     managed memory) of the current CUDA device.  The caller owns every
+ *     buffer; the library keeps no pointer after a call returns and allocates
+ *     no device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls are asynchronous and stream-ordered; they never
+ *     synchronise the device.
+ *   - Errors: arguments are checked on the host before anything is launched;
+ *     a failed check returns OSCAR_ERR_INVALID_ARG / _UNSUPPORTED / _WORKSPACE
+ *     and launches nothing.  A launch failure returns OSCAR_ERR_CUDA.  Kernels
+ *     never trap: a bad page id, slot or sequence length met on the device is
+ *     skipped and recorded in a device error word (oscar_device_errors).
+ *   - Outputs never alias inputs.
+ *   - Supported shapes: head_dim 64 or 128; page_size 16; group_size 32, 64
+ *     or 128 dividing head_dim; num_q_heads / num_kv_heads (GQA) 1..8.
+ */
+#ifndef OSCAR_H_
+#define OSCAR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  OSCAR_OK = 0,
+  OSCAR_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size      */
+  OSCAR_ERR_UNSUPPORTED = 2, /* valid but not implemented (head_dim 96, ...)     */
+  OSCAR_ERR_WORKSPACE = 3,   /* workspace smaller than the *_workspace_bytes call */
+  OSCAR_ERR_CUDA = 4         /* a CUDA call or launch failed                     */
+} oscar_status_t;
+
+/* Device error bits recorded by kernels (read with oscar_device_errors). */
+#define OSCAR_DEVERR_SLOT 0x1u      /* append: slot >= num_pages * page_size (token skipped)  */
+#define OSCAR_DEVERR_PAGE_ID 0x2u   /* decode: page id outside [0, num_pages) (page skipped)  */
+#define OSCAR_DEVERR_SEQ_LEN 0x4u   /* decode: seq_len < 0 or > max_seq_len (clamped)         */
+#define OSCAR_DEVERR_TIMEOUT 0x8u   /* a bounded wait on an async copy ran out (work skipped) */
+
+/* Cache geometry. */
+typedef struct {
+  int32_t num_q_heads;       /* Hq, a multiple of num_kv_heads                          */
+  int32_t num_kv_heads;      /* Hkv                                                     */
+  int32_t head_dim;          /* D                                                       */
+  int32_t page_size;         /* P: tokens per page                                      */
+  int32_t group_size;        /* G: channels sharing one fp16 (scale, zero) pair         */
+  int32_t num_pages;         /* pages in the pool                                       */
+  int32_t max_pages_per_seq; /* row stride of page_table                                */
+} oscar_dims_t;
+
+/*
+ * oscar_append -- rotate, clip, quantise to INT2 and store new K/V vectors.
+ *
+ * Defined by: summary "Practical Summary" (fixed rotations and clipping
+ * thresholds, 2-bit KV cache) and abstract (paged KV cache).  For every token
+ * t with slot_mapping[t] >= 0, every KV head h, and separately for K (R_k,
+ * clip_k) and V (R_v, clip_v):
+ *   y = x . R[h]                      row vector times fp32 [D][D] row-major R
+ *   y_j = min(max(y_j, -clip[h][j]), +clip[h][j])      (+inf = no clipping)
+ *   per group g of G consecutive channels: mn, mx = min, max of the group;
+ *     scale = fp16(fp32((mx - mn) / 3)), zero = fp16(fp32(mn));
+ *     code_j = clamp(rint((y_j - zero) / scale), 0, 3), ties to even, computed
+ *     from the stored fp16 scale and zero (code 0 when scale == 0);
+ *   the codes and pairs are written to page slot / P at offset slot % P.
+ * Arguments
+ *   k, v          device bf16 [num_tokens][Hkv][D]
+ *   R_k, R_v      device fp32 [Hkv][D][D]
+ *   clip_k/_v     device fp32 [Hkv][D]
+ *   page_table    unused (may be NULL): placement is by slot_mapping only
+ *   slot_mapping  device int64 [num_tokens]; page * P + offset; < 0 skips the token
+ *   int2_pages    device uint8 [num_pages][Hkv][2 = K,V][P][D/4]; channel j of a
+ *                 row is byte j/4, bits 2*(j%4)..2*(j%4)+1
+ *   scale_zero_pages device fp16 [num_pages][Hkv][2][P][D/G][2 = scale, zero]
+ * Only the rows of the given slots are written.  A slot past the pool is
+ * skipped and flagged OSCAR_DEVERR_SLOT.  num_tokens == 0 is a no-op.
+ */
+oscar_status_t oscar_append(const oscar_dims_t* dims, int64_t num_tokens, const void* k, const void* v,
+                            const float* R_k, const float* R_v, const float* clip_k, const float* clip_v,
+                            const int32_t* page_table, const int64_t* slot_mapping, uint8_t* int2_pages,
+                            void* scale_zero_pages, void* stream);
+
+/*
+ * Workspace (device bytes) oscar_decode needs for `batch` sequences of at most
+ * max_seq_len tokens, splits of pages_per_split pages (0 = automatic) and the
+ * given BF16 sink/window lengths.  Returns 0 when the arguments are invalid.
+ */
+size_t oscar_decode_workspace_bytes(const oscar_dims_t* dims, int32_t batch, int32_t max_seq_len,
+                                    int32_t pages_per_split, int32_t sink_len, int32_t window_len);
+
+/*
+ * oscar_decode -- one decode step of mixed-precision paged GQA attention.
+ *
+ * Defined by: project card "How it works" (a BF16 sink of initial tokens and a
+ * BF16 recent window, the bulk in INT2, fused mixed-precision attention) and
+ * abstract (INT2 attention kernel over a paged KV cache).  For each sequence b
+ * and query head hq (KV head h = hq / (Hq/Hkv)), with L = seq_lens[b]:
+ *   sink   positions [0, min(S, L))          bf16_sink[b][K|V][h][p]
+ *   window positions [max(S, L-W), L)        bf16_window[b][K|V][h][p % W]
+ *   bulk   positions [S, L-W)                INT2 pool, page page_table[b][p/P],
+ *                                            offset p % P
+ *   logits: sm_scale * q.k for sink/window tokens (original space);
+ *           sm_scale * (q.R_k[h]).(c*scale + zero) for bulk tokens (rotated
+ *           space, so stored keys are never un-rotated);
+ *   out = ( sum_bf16 w_p v_p + (sum_bulk w_p (c*scale+zero)_v) . R_v[h]^T ) / sum_p w_p
+ *   with w_p = exp(logit_p - max logit).  A sequence with L == 0 gets zeros.
+ * The bulk is cut into splits of pages_per_split pages (flash-decoding); each
+ * split keeps (max, sum, partial output) and a merge combines them by
+ * log-sum-exp before the single un-rotation.
+ * Arguments
+ *   max_seq_len   host bound on every seq_lens[b] (<= max_pages_per_seq * P);
+ *                 larger device values are clamped and flagged
+ *   pages_per_split  0 = chosen from the grid size; else >= 1
+ *   q             device bf16 [batch][Hq][D]
+ *   R_k, R_v      device fp32 [Hkv][D][D] (the rotations used at append time)
+ *   int2_pages, scale_zero_pages   the pools written by oscar_append
+ *   bf16_sink     device bf16 [batch][2][Hkv][S][D] (NULL allowed when S == 0)
+ *   bf16_window   device bf16 [batch][2][Hkv][W][D] ring (NULL allowed when W == 0)
+ *   page_table    device int32 [batch][max_pages_per_seq]
+ *   seq_lens      device int32 [batch], tokens in the cache including the current one
+ *   sm_scale      softmax scale; <= 0 selects 1/sqrt(D)
+ *   out           device fp32 [batch][Hq][D]
+ *   workspace     device scratch of at least oscar_decode_workspace_bytes(...)
+ *                 bytes, 256-byte aligned; its contents need no initialisation
+ */
+oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, int32_t max_seq_len, int32_t pages_per_split,
+                            const void* q, const float* R_k, const float* R_v, const uint8_t* int2_pages,
+                            const void* scale_zero_pages, const void* bf16_sink, const void* bf16_window,
+                            const int32_t* page_table, const int32_t* seq_lens, int32_t sink_len,
+                            int32_t window_len, float sm_scale, float* out, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
+ * oscar_bf16_append -- store K/V vectors unchanged into a BF16 paged pool (the
+ * speedup reference's cache; the pages compare OSCAR against BF16 decoding,
+ * summary "Practical Summary").
+ *   k, v          device bf16 [num_tokens][Hkv][D]
+ *   slot_mapping  device int64 [num_tokens]; < 0 skips; past the pool is flagged
+ *   bf16_pages    device bf16 [num_pages][Hkv][2][P][D]
+ */
+oscar_status_t oscar_bf16_append(const oscar_dims_t* dims, int64_t num_tokens, const void* k, const void* v,
+                                 const int64_t* slot_mapping, void* bf16_pages, void* stream);
+
+size_t oscar_bf16_decode_workspace_bytes(const oscar_dims_t* dims, int32_t batch, int32_t max_seq_len,
+                                         int32_t pages_per_split);
+
+/*
+ * oscar_bf16_decode -- paged GQA decode attention over an all-BF16 cache (the
+ * speedup reference).  Every position [0, L) is read from
+ * bf16_pages[page_table[b][p/P]][h][K|V][p % P]; out = softmax(sm_scale q.k) v
+ * in fp32.  Split-KV with a log-sum-exp merge, as oscar_decode.
+ */
+oscar_status_t oscar_bf16_decode(const oscar_dims_t* dims, int32_t batch, int32_t max_seq_len,
+                                 int32_t pages_per_split, const void* q, const void* bf16_pages,
+                                 const int32_t* page_table, const int32_t* seq_lens, float sm_scale, float* out,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* oscar_status_string(oscar_status_t status);
+
+/*
+ * Reads the device error word (OSCAR_DEVERR_* bits) of the current device,
+ * OR-ed over all kernels since the last reset; clears it when reset != 0.
+ * Synchronises the device.  Returns OSCAR_ERR_CUDA if the read fails.
+ */
+oscar_status_t oscar_device_errors(uint32_t* flags, int32_t reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSCAR_H_ */

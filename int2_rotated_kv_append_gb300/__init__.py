@@ -1,0 +1,169 @@
+"""OSCAR INT2 rotated KV append + mixed-precision paged decode for GB300.
+
+Thin ctypes binding over ``liboscar.so`` (the C ABI declared in
+``include/oscar.h``).  The functions carry the C names and only marshal
+torch tensors to pointers; every step of the path runs in the CUDA kernels.
+The library must have been built (``int2_rotated_kv_append_gb300.build``):
+it is loaded on first use, and any call without it raises ImportError --
+there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liboscar.so")
+
+OSCAR_OK = 0
+OSCAR_ERR_INVALID_ARG = 1
+OSCAR_ERR_UNSUPPORTED = 2
+OSCAR_ERR_WORKSPACE = 3
+OSCAR_ERR_CUDA = 4
+
+OSCAR_DEVERR_SLOT = 0x1
+OSCAR_DEVERR_PAGE_ID = 0x2
+OSCAR_DEVERR_SEQ_LEN = 0x4
+OSCAR_DEVERR_TIMEOUT = 0x8
+
+
+class OscarError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)}")
+        self.status = status
+
+
+class oscar_dims_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_q_heads", "num_kv_heads", "head_dim", "page_size", "group_size", "num_pages",
+        "max_pages_per_seq")]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"OSCAR CUDA library not built ({LIB_PATH} missing); run "
+                          "int2_rotated_kv_append_gb300.build.build() -- there is no CPU fallback")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    D = ctypes.POINTER(oscar_dims_t)
+    sigs = {
+        "oscar_append": (I32, [D, I64, P, P, P, P, P, P, P, P, P, P, P]),
+        "oscar_decode_workspace_bytes": (SZ, [D, I32, I32, I32, I32, I32]),
+        "oscar_decode": (I32, [D, I32, I32, I32, P, P, P, P, P, P, P, P, P, I32, I32, F32, P, P, SZ, P]),
+        "oscar_bf16_append": (I32, [D, I64, P, P, P, P, P]),
+        "oscar_bf16_decode_workspace_bytes": (SZ, [D, I32, I32, I32]),
+        "oscar_bf16_decode": (I32, [D, I32, I32, I32, P, P, P, P, F32, P, P, SZ, P]),
+        "oscar_status_string": (ctypes.c_char_p, [I32]),
+        "oscar_device_errors": (I32, [ctypes.POINTER(ctypes.c_uint32), I32]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+class _LazyLib:
+    """Loads liboscar.so on first attribute access (raises ImportError if absent)."""
+
+    _handle = None
+
+    def __getattr__(self, name):
+        if _LazyLib._handle is None:
+            _LazyLib._handle = _load()
+        return getattr(_LazyLib._handle, name)
+
+
+lib = _LazyLib()
+
+
+def load_library():
+    """Load the CUDA library now; returns the ctypes handle."""
+    lib.oscar_status_string  # noqa: B018 -- forces the load
+    return _LazyLib._handle
+
+
+def status_string(status: int) -> str:
+    return lib.oscar_status_string(int(status)).decode()
+
+
+def make_dims(num_q_heads, num_kv_heads, head_dim, page_size, group_size, num_pages, max_pages_per_seq):
+    return oscar_dims_t(int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size), int(group_size),
+                        int(num_pages), int(max_pages_per_seq))
+
+
+def _dims(d) -> oscar_dims_t:
+    if isinstance(d, oscar_dims_t):
+        return d
+    return make_dims(**d)
+
+
+def _ptr(t) -> ctypes.c_void_p | None:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("OSCAR tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(status: int, where: str):
+    if status != OSCAR_OK:
+        raise OscarError(status, where)
+
+
+def oscar_append(dims, k, v, R_k, R_v, clip_k, clip_v, page_table, slot_mapping, int2_pages, scale_zero_pages,
+                 stream=None):
+    """Rotate, clip, INT2-quantise and store k/v (bf16 [T][Hkv][D]) at slot_mapping."""
+    _check(lib.oscar_append(ctypes.byref(_dims(dims)), int(k.shape[0]), _ptr(k), _ptr(v), _ptr(R_k), _ptr(R_v),
+                            _ptr(clip_k), _ptr(clip_v), _ptr(page_table), _ptr(slot_mapping), _ptr(int2_pages),
+                            _ptr(scale_zero_pages), _stream(stream)), "oscar_append")
+
+
+def oscar_decode_workspace_bytes(dims, batch, max_seq_len, pages_per_split, sink_len, window_len) -> int:
+    return int(lib.oscar_decode_workspace_bytes(ctypes.byref(_dims(dims)), int(batch), int(max_seq_len),
+                                                int(pages_per_split), int(sink_len), int(window_len)))
+
+
+def oscar_decode(dims, batch, max_seq_len, pages_per_split, q, R_k, R_v, int2_pages, scale_zero_pages, bf16_sink,
+                 bf16_window, page_table, seq_lens, sink_len, window_len, sm_scale, out, workspace, stream=None):
+    """One mixed-precision decode step; writes fp32 out [B][Hq][D]."""
+    _check(lib.oscar_decode(ctypes.byref(_dims(dims)), int(batch), int(max_seq_len), int(pages_per_split), _ptr(q),
+                            _ptr(R_k), _ptr(R_v), _ptr(int2_pages), _ptr(scale_zero_pages), _ptr(bf16_sink),
+                            _ptr(bf16_window), _ptr(page_table), _ptr(seq_lens), int(sink_len), int(window_len),
+                            float(sm_scale), _ptr(out), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream)), "oscar_decode")
+
+
+def oscar_bf16_append(dims, k, v, slot_mapping, bf16_pages, stream=None):
+    _check(lib.oscar_bf16_append(ctypes.byref(_dims(dims)), int(k.shape[0]), _ptr(k), _ptr(v), _ptr(slot_mapping),
+                                 _ptr(bf16_pages), _stream(stream)), "oscar_bf16_append")
+
+
+def oscar_bf16_decode_workspace_bytes(dims, batch, max_seq_len, pages_per_split) -> int:
+    return int(lib.oscar_bf16_decode_workspace_bytes(ctypes.byref(_dims(dims)), int(batch), int(max_seq_len),
+                                                     int(pages_per_split)))
+
+
+def oscar_bf16_decode(dims, batch, max_seq_len, pages_per_split, q, bf16_pages, page_table, seq_lens, sm_scale, out,
+                      workspace, stream=None):
+    _check(lib.oscar_bf16_decode(ctypes.byref(_dims(dims)), int(batch), int(max_seq_len), int(pages_per_split),
+                                 _ptr(q), _ptr(bf16_pages), _ptr(page_table), _ptr(seq_lens), float(sm_scale),
+                                 _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream)), "oscar_bf16_decode")
+
+
+def oscar_device_errors(reset: bool = False) -> int:
+    flags = ctypes.c_uint32(0)
+    _check(lib.oscar_device_errors(ctypes.byref(flags), int(bool(reset))), "oscar_device_errors")
+    return int(flags.value)

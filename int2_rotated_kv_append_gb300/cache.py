@@ -1,0 +1,103 @@
+"""Device-side paged caches driven through the C ABI.
+
+``Int2Cache`` owns the INT2 code pool, the fp16 scale/zero pool and the BF16
+sink/window buffers of a workload; ``Bf16Cache`` owns the all-BF16 pool of the
+speedup reference.  Both only allocate torch memory and call the library.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import (oscar_append, oscar_bf16_append, oscar_bf16_decode, oscar_bf16_decode_workspace_bytes,
+               oscar_decode, oscar_decode_workspace_bytes)
+from .synth import Workload
+
+SENTINEL = 0xA5
+
+
+class Int2Cache:
+    def __init__(self, w: Workload, device="cuda", pages_per_split: int | None = None, fill: int = SENTINEL):
+        self.w = w
+        self.device = torch.device(device)
+        H, D, P, G = w.num_kv_heads, w.head_dim, w.page_size, w.group_size
+        self.dims = w.dims
+        self.int2_pages = torch.full((w.num_pages * H * 2 * P * D // 4,), fill, dtype=torch.uint8,
+                                     device=self.device)
+        fill16 = fill * 0x101
+        fill16 = fill16 - 0x10000 if fill16 >= 0x8000 else fill16
+        self.scale_zero = torch.full((w.num_pages * H * 2 * P * (D // G) * 2,), fill16, dtype=torch.int16,
+                                     device=self.device).view(torch.float16)
+        self.page_table = w.page_table.to(self.device)
+        self.seq_lens = w.seq_lens.to(self.device)
+        self.R_k, self.R_v = w.R_k.to(self.device), w.R_v.to(self.device)
+        self.clip_k, self.clip_v = w.clip_k.to(self.device), w.clip_v.to(self.device)
+        self.pps = w.pages_per_split if pages_per_split is None else pages_per_split
+        self.sink = None
+        self.window = None
+        self._ws = None
+
+    def append(self, k, v, slot_mapping, stream=None):
+        oscar_append(self.dims, k, v, self.R_k, self.R_v, self.clip_k, self.clip_v, self.page_table, slot_mapping,
+                     self.int2_pages, self.scale_zero, stream)
+
+    def prefill(self, stream=None):
+        """Append every token of the workload and fill the BF16 sink/window buffers."""
+        w = self.w
+        self.append(w.k.to(self.device), w.v.to(self.device), w.slot_mapping.to(self.device), stream)
+        sink, win = w.sink_window()
+        self.sink, self.window = sink.to(self.device), win.to(self.device)
+
+    def workspace(self, max_seq_len=None):
+        w = self.w
+        msl = w.max_seq_len if max_seq_len is None else max_seq_len
+        nbytes = oscar_decode_workspace_bytes(self.dims, w.batch, msl, self.pps, w.sink_len, w.window_len)
+        if nbytes == 0:
+            raise ValueError("invalid decode arguments for workspace sizing")
+        if self._ws is None or self._ws.numel() < nbytes:
+            self._ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def decode(self, q, out=None, sm_scale=0.0, seq_lens=None, max_seq_len=None, stream=None):
+        w = self.w
+        msl = w.max_seq_len if max_seq_len is None else max_seq_len
+        if out is None:
+            out = torch.empty((w.batch, w.num_q_heads, w.head_dim), dtype=torch.float32, device=self.device)
+        ws = self.workspace(msl)
+        oscar_decode(self.dims, w.batch, msl, self.pps, q, self.R_k, self.R_v, self.int2_pages, self.scale_zero,
+                     self.sink, self.window, self.page_table, self.seq_lens if seq_lens is None else seq_lens,
+                     w.sink_len, w.window_len, sm_scale, out, ws, stream)
+        return out
+
+
+class Bf16Cache:
+    def __init__(self, w: Workload, device="cuda", pages_per_split: int | None = None):
+        self.w = w
+        self.device = torch.device(device)
+        self.dims = w.dims
+        self.pages = torch.zeros((w.num_pages * w.num_kv_heads * 2 * w.page_size * w.head_dim,),
+                                 dtype=torch.bfloat16, device=self.device)
+        self.page_table = w.page_table.to(self.device)
+        self.seq_lens = w.seq_lens.to(self.device)
+        self.pps = w.pages_per_split if pages_per_split is None else pages_per_split
+        self._ws = None
+
+    def prefill(self, stream=None):
+        w = self.w
+        oscar_bf16_append(self.dims, w.k.to(self.device), w.v.to(self.device), w.slot_mapping.to(self.device),
+                          self.pages, stream)
+
+    def workspace(self):
+        w = self.w
+        nbytes = oscar_bf16_decode_workspace_bytes(self.dims, w.batch, w.max_seq_len, self.pps)
+        if self._ws is None or self._ws.numel() < nbytes:
+            self._ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def decode(self, q, out=None, sm_scale=0.0, stream=None):
+        w = self.w
+        if out is None:
+            out = torch.empty((w.batch, w.num_q_heads, w.head_dim), dtype=torch.float32, device=self.device)
+        oscar_bf16_decode(self.dims, w.batch, w.max_seq_len, self.pps, q, self.pages, self.page_table,
+                          self.seq_lens, sm_scale, out, self.workspace(), stream)
+        return out

@@ -1,0 +1,219 @@
+// KV append: rotate by the fixed per-head R, clip per channel, quantise per
+// group to asymmetric INT2 with fp16 scale/zero, pack 4 codes per byte and
+// scatter the rows into the paged pool ("OSCAR: Offline Spectral
+// Covariance-Aware Rotation for 2-bit KV Cache Quantization": summary
+// "Practical Summary" -- fixed rotations and clipping thresholds, 2-bit KV
+// cache; abstract -- paged KV cache).
+//
+// One CTA owns a tile of 32 tokens of one (KV head, K|V) pair, so R (fp32,
+// 64 KB at D = 128) is staged once in shared memory and reused by all tokens of
+// the tile.  Each warp rotates 4 tokens; lane l owns channels [l*D/32,
+// (l+1)*D/32), so a group of G channels is G*32/D consecutive lanes and the
+// group min/max is a warp-shuffle reduction.
+#include "common.cuh"
+
+namespace {
+
+using namespace oscar;
+
+constexpr int kTokTile = 32;
+constexpr int kThreads = 256;  // 8 warps x 4 tokens each
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) append_kernel(
+    int64_t num_tokens, int H, int G, int num_pages, const __nv_bfloat16* __restrict__ k,
+    const __nv_bfloat16* __restrict__ v, const float* __restrict__ R_k, const float* __restrict__ R_v,
+    const float* __restrict__ clip_k, const float* __restrict__ clip_v, const int64_t* __restrict__ slots,
+    uint8_t* __restrict__ codes, __half* __restrict__ sz) {
+  constexpr int CPL = D / 32;  // channels per lane
+  extern __shared__ __align__(16) float smem[];
+  float* Rs = smem;           // [D][D]
+  float* xs = smem + D * D;   // [kTokTile][D]
+  const int h = blockIdx.y, kv = blockIdx.z;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTokTile;
+  const float* R = (kv ? R_v : R_k) + static_cast<size_t>(h) * D * D;
+  const float* clip = (kv ? clip_v : clip_k) + static_cast<size_t>(h) * D;
+  const __nv_bfloat16* x = kv ? v : k;
+
+  for (int i = threadIdx.x; i < D * D / 4; i += kThreads)
+    reinterpret_cast<float4*>(Rs)[i] = __ldg(reinterpret_cast<const float4*>(R) + i);
+  for (int i = threadIdx.x; i < kTokTile * D / 2; i += kThreads) {
+    const int tt = i / (D / 2), c2 = i % (D / 2);
+    const int64_t t = t0 + tt;
+    float2 val = make_float2(0.f, 0.f);
+    if (t < num_tokens)
+      val = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(x + (static_cast<size_t>(t) * H + h) * D)[c2]);
+    xs[tt * D + 2 * c2] = val.x;
+    xs[tt * D + 2 * c2 + 1] = val.y;
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  float acc[4][CPL];
+#pragma unroll
+  for (int m = 0; m < 4; ++m)
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[m][c] = 0.f;
+
+  // y_j = sum_i x_i R[i][j], accumulated in i order.
+#pragma unroll 4
+  for (int i = 0; i < D; ++i) {
+    float r[CPL];
+    if constexpr (CPL == 4) {
+      const float4 rv = *reinterpret_cast<const float4*>(Rs + i * D + 4 * lane);
+      r[0] = rv.x; r[1] = rv.y; r[2] = rv.z; r[3] = rv.w;
+    } else {
+      const float2 rv = *reinterpret_cast<const float2*>(Rs + i * D + 2 * lane);
+      r[0] = rv.x; r[1] = rv.y;
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float xv = xs[(warp + 8 * m) * D + i];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acc[m][c] = fmaf(xv, r[c], acc[m][c]);
+    }
+  }
+
+  float cl[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) cl[c] = __ldg(clip + CPL * lane + c);
+  const int lanes_per_group = G / CPL;
+
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int64_t t = t0 + warp + 8 * m;
+    if (t >= num_tokens) break;  // warp-uniform
+    const int64_t slot = __ldg(slots + t);
+    if (slot < 0) continue;
+    if (slot >= static_cast<int64_t>(num_pages) * kPageSize) {
+      if (lane == 0) record_error(OSCAR_DEVERR_SLOT);
+      continue;
+    }
+    float y[CPL];
+    float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      y[c] = fminf(fmaxf(acc[m][c], -cl[c]), cl[c]);
+      mn = fminf(mn, y[c]);
+      mx = fmaxf(mx, y[c]);
+    }
+    for (int off = 1; off < lanes_per_group; off <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    const __half sh = __float2half_rn((mx - mn) / 3.0f);
+    const __half zh = __float2half_rn(mn);
+    const float s = __half2float(sh), z = __half2float(zh);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      uint32_t code = 0;
+      if (s != 0.f) {
+        const float u = (y[c] - z) / s;
+        code = static_cast<uint32_t>(fminf(fmaxf(rintf(u), 0.f), 3.f));
+      }
+      packed |= code << (2 * c);
+    }
+    const int64_t page = slot / kPageSize;
+    const int off = static_cast<int>(slot % kPageSize);
+    const size_t row = ((static_cast<size_t>(page) * H + h) * 2 + kv) * kPageSize + off;
+    uint8_t* row_codes = codes + row * (D / 4);
+    if constexpr (CPL == 4) {
+      row_codes[lane] = static_cast<uint8_t>(packed);
+    } else {
+      const uint32_t hi = __shfl_down_sync(0xffffffffu, packed, 1);
+      if ((lane & 1) == 0) row_codes[lane / 2] = static_cast<uint8_t>(packed | (hi << 4));
+    }
+    if (lane % lanes_per_group == 0) {
+      const int g = lane / lanes_per_group;
+      reinterpret_cast<__half2*>(sz + row * (D / G) * 2)[g] = __halves2half2(sh, zh);
+    }
+  }
+}
+
+// Plain copy of bf16 rows into the BF16 paged pool, 16 bytes per thread.
+__global__ void bf16_append_kernel(int64_t num_tokens, int H, int D, int num_pages,
+                                   const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+                                   const int64_t* __restrict__ slots, __nv_bfloat16* __restrict__ pages) {
+  const int chunks = D / 8;  // 16-byte chunks per row
+  const int64_t total = num_tokens * H * 2 * chunks;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % chunks);
+    const int kv = static_cast<int>((i / chunks) % 2);
+    const int h = static_cast<int>((i / (2 * chunks)) % H);
+    const int64_t t = i / (2 * chunks * H);
+    const int64_t slot = __ldg(slots + t);
+    if (slot < 0) continue;
+    if (slot >= static_cast<int64_t>(num_pages) * kPageSize) {
+      record_error(OSCAR_DEVERR_SLOT);
+      continue;
+    }
+    const __nv_bfloat16* src = (kv ? v : k) + (static_cast<size_t>(t) * H + h) * D;
+    const int64_t page = slot / kPageSize;
+    const int off = static_cast<int>(slot % kPageSize);
+    __nv_bfloat16* dst = pages + (((static_cast<size_t>(page) * H + h) * 2 + kv) * kPageSize + off) * D;
+    reinterpret_cast<uint4*>(dst)[c] = __ldg(reinterpret_cast<const uint4*>(src) + c);
+  }
+}
+
+template <int D>
+cudaError_t launch_append(int64_t T, const oscar_dims_t* d, const void* k, const void* v, const float* R_k,
+                          const float* R_v, const float* clip_k, const float* clip_v, const int64_t* slots,
+                          uint8_t* codes, void* sz, cudaStream_t stream) {
+  const size_t smem = (static_cast<size_t>(D) * D + kTokTile * D) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(append_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>((T + kTokTile - 1) / kTokTile), d->num_kv_heads, 2);
+  append_kernel<D><<<grid, kThreads, smem, stream>>>(
+      T, d->num_kv_heads, d->group_size, d->num_pages, static_cast<const __nv_bfloat16*>(k),
+      static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz));
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" oscar_status_t oscar_append(const oscar_dims_t* dims, int64_t num_tokens, const void* k, const void* v,
+                                       const float* R_k, const float* R_v, const float* clip_k,
+                                       const float* clip_v, const int32_t* page_table,
+                                       const int64_t* slot_mapping, uint8_t* int2_pages, void* scale_zero_pages,
+                                       void* stream) {
+  (void)page_table;
+  oscar_status_t st = check_dims(dims);
+  if (st != OSCAR_OK) return st;
+  if (num_tokens < 0) return OSCAR_ERR_INVALID_ARG;
+  if (num_tokens == 0) return OSCAR_OK;
+  if (!k || !v || !R_k || !R_v || !clip_k || !clip_v || !slot_mapping || !int2_pages || !scale_zero_pages)
+    return OSCAR_ERR_INVALID_ARG;
+  if ((num_tokens + kTokTile - 1) / kTokTile > 0x7fffffffLL) return OSCAR_ERR_UNSUPPORTED;
+  cudaError_t e = dims->head_dim == 128
+                      ? launch_append<128>(num_tokens, dims, k, v, R_k, R_v, clip_k, clip_v, slot_mapping,
+                                           int2_pages, scale_zero_pages, as_stream(stream))
+                      : launch_append<64>(num_tokens, dims, k, v, R_k, R_v, clip_k, clip_v, slot_mapping,
+                                          int2_pages, scale_zero_pages, as_stream(stream));
+  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+extern "C" oscar_status_t oscar_bf16_append(const oscar_dims_t* dims, int64_t num_tokens, const void* k,
+                                            const void* v, const int64_t* slot_mapping, void* bf16_pages,
+                                            void* stream) {
+  oscar_status_t st = check_dims(dims);
+  if (st != OSCAR_OK) return st;
+  if (num_tokens < 0) return OSCAR_ERR_INVALID_ARG;
+  if (num_tokens == 0) return OSCAR_OK;
+  if (!k || !v || !slot_mapping || !bf16_pages) return OSCAR_ERR_INVALID_ARG;
+  const int64_t total = num_tokens * dims->num_kv_heads * 2 * (dims->head_dim / 8);
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
+  if (blocks > cap) blocks = cap;
+  bf16_append_kernel<<<static_cast<unsigned>(blocks), threads, 0, as_stream(stream)>>>(
+      num_tokens, dims->num_kv_heads, dims->head_dim, dims->num_pages, static_cast<const __nv_bfloat16*>(k),
+      static_cast<const __nv_bfloat16*>(v), slot_mapping, static_cast<__nv_bfloat16*>(bf16_pages));
+  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+oscar_status_t oscar_internal_append_errors(uint32_t* flags, int reset) {
+  return read_unit_errors(flags, reset) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}

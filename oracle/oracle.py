@@ -20,7 +20,7 @@ _LIB_PATH = os.path.join(_HERE, "liboscar_oracle.so")
 
 __all__ = [
     "OracleDims", "build_oracle", "load", "bf16_to_f64", "f16_to_f64", "f64_to_f16",
-    "rotate", "clip", "group_params", "quantize", "append", "append_prequant",
+    "rotate", "clip", "group_params", "quantize", "codes_given_params", "append", "append_prequant",
     "attend_mixed", "dequant_row", "decode", "bf16_decode",
 ]
 
@@ -61,6 +61,7 @@ def load(path: str | None = None):
         "orc_group_params": (None, [ctypes.c_int32, _P, _P, _P]),
         "orc_quantize": (ctypes.c_int32, [ctypes.c_double, ctypes.c_uint16, ctypes.c_uint16, _P]),
         "orc_append_prequant": (ctypes.c_int32, [_P, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P]),
+        "orc_codes_given_params": (None, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]),
         "orc_append": (ctypes.c_int32, [_P, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
         "orc_attend_mixed": (None, [ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P,
                                     ctypes.c_double, _P, _P]),
@@ -151,6 +152,18 @@ def quantize(x: float, s_bits: int, z_bits: int, lib=None) -> tuple[int, float]:
     u = ctypes.c_double(0.0)
     c = lib.orc_quantize(float(x), int(s_bits), int(z_bits), ctypes.byref(u))
     return int(c), float(u.value)
+
+
+def codes_given_params(x: np.ndarray, sz_bits: np.ndarray, group_size: int, lib=None):
+    """Codes and u of rows x [n][D] given stored (scale, zero) bits [n][D/G][2]."""
+    lib = lib or load()
+    xx = _c(x, np.float64)
+    n, D = xx.shape
+    s = _c(sz_bits, np.uint16).reshape(n, D // group_size, 2)
+    codes = np.empty((n, D), np.int32)
+    u = np.empty((n, D), np.float64)
+    lib.orc_codes_given_params(n, D, group_size, _ptr(xx), _ptr(s), _ptr(codes), _ptr(u))
+    return codes, u
 
 
 def append_prequant(dims, k_bits, v_bits, R_k, R_v, clip_k, clip_v, lib=None) -> np.ndarray:

@@ -155,6 +155,20 @@ int32_t orc_quantize(double x, uint16_t s_bits, uint16_t z_bits, double* u_out) 
   return static_cast<int32_t>(c);
 }
 
+// Step A5 over whole rows: codes of n rows of D pre-quantisation values x
+// ([n][D] fp64) given stored (scale, zero) bits sz ([n][D/G][2]), with u as in
+// orc_quantize.  codes: int32 [n][D]; u: fp64 [n][D].
+void orc_codes_given_params(int64_t n, int32_t D, int32_t G, const double* x, const uint16_t* sz,
+                            int32_t* codes, double* u) {
+  for (int64_t r = 0; r < n; ++r) {
+    for (int j = 0; j < D; ++j) {
+      const size_t e = static_cast<size_t>(r) * D + j;
+      const size_t g = (static_cast<size_t>(r) * (D / G) + j / G) * 2;
+      codes[e] = orc_quantize(x[e], sz[g], sz[g + 1], &u[e]);
+    }
+  }
+}
+
 // Byte offset of the packed code row of (page, kv head, K|V, offset): the INT2
 // pool is uint8 [num_pages][Hkv][2][P][D/4] (reading R17).
 static size_t code_row(const orc_dims_t* d, int64_t page, int h, int kv, int off) {
@@ -249,9 +263,14 @@ int32_t orc_append(const orc_dims_t* d, int64_t T, const uint16_t* k, const uint
 // (is_rot[i] == 1: logit = sm_scale * q_rot . key_i).  The output is
 //   ( sum_{unrotated} w_i v_i  +  (sum_{rotated} w_i v_i) . R_v^T ) / sum_i w_i
 // with w_i = exp(logit_i - max logit).  Keys/values are fp64 [n][D].
+// An empty token set (n == 0) attends to nothing; its output is zero.
 void orc_attend_mixed(int32_t D, int32_t n, const double* q, const double* q_rot,
                       const double* keys, const double* vals, const int32_t* is_rot,
                       double sm_scale, const float* R_v, double* out) {
+  if (n == 0) {
+    for (int c = 0; c < D; ++c) out[c] = 0.0;
+    return;
+  }
   std::vector<double> logit(n);
   double m = -HUGE_VAL;
   for (int i = 0; i < n; ++i) {

@@ -1,0 +1,99 @@
+"""The C-ABI library loads, exports every declared entry point, and rejects bad
+arguments on the host (no GPU needed: nothing is launched)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import int2_rotated_kv_append_gb300 as ok
+from int2_rotated_kv_append_gb300 import build
+
+HEADER = os.path.join(build.INCLUDE, "oscar.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ok.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(oscar_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("oscar_append", "oscar_decode", "oscar_decode_workspace_bytes", "oscar_bf16_decode"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def _dims(**kw):
+    d = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16, group_size=64, num_pages=100,
+             max_pages_per_seq=20)
+    d.update(kw)
+    return ok.make_dims(**d)
+
+
+P = ctypes.c_void_p(16)  # never dereferenced: validation fails before any launch
+
+
+def _append(lib, dims, T=4, ptr=P):
+    return lib.oscar_append(ctypes.byref(dims) if dims is not None else None, T, ptr, ptr, ptr, ptr, ptr, ptr,
+                            None, ptr, ptr, ptr, None)
+
+
+def test_append_validation(lib):
+    assert _append(lib, None) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append(lib, _dims(head_dim=96, group_size=32)) == ok.OSCAR_ERR_UNSUPPORTED
+    assert _append(lib, _dims(num_q_heads=30)) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append(lib, _dims(group_size=48)) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append(lib, _dims(group_size=16)) == ok.OSCAR_ERR_UNSUPPORTED
+    assert _append(lib, _dims(page_size=32)) == ok.OSCAR_ERR_UNSUPPORTED
+    assert _append(lib, _dims(num_q_heads=128)) == ok.OSCAR_ERR_UNSUPPORTED  # GQA 16
+    assert _append(lib, _dims(num_pages=0)) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append(lib, _dims(), T=-1) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append(lib, _dims(), T=0) == ok.OSCAR_OK  # no-op
+    assert _append(lib, _dims(), ptr=None) == ok.OSCAR_ERR_INVALID_ARG
+
+
+def _decode(lib, dims, batch=2, msl=100, pps=8, S=4, W=8, ws_bytes=1 << 30, ws=ctypes.c_void_p(256), sink=P):
+    return lib.oscar_decode(ctypes.byref(dims), batch, msl, pps, P, P, P, P, P, sink, P, P, P, S, W, 0.0, P, ws,
+                            ws_bytes, None)
+
+
+def test_decode_validation(lib):
+    d = _dims()
+    assert _decode(lib, d, batch=-1) == ok.OSCAR_ERR_INVALID_ARG
+    assert _decode(lib, d, batch=0) == ok.OSCAR_OK
+    assert _decode(lib, d, msl=20 * 16 + 1) == ok.OSCAR_ERR_INVALID_ARG  # beyond the page table
+    assert _decode(lib, d, S=-1) == ok.OSCAR_ERR_INVALID_ARG
+    assert _decode(lib, d, W=-2) == ok.OSCAR_ERR_INVALID_ARG
+    assert _decode(lib, d, pps=-1) == ok.OSCAR_ERR_INVALID_ARG
+    assert _decode(lib, d, sink=None) == ok.OSCAR_ERR_INVALID_ARG  # S > 0 needs a sink buffer
+    assert _decode(lib, d, ws=ctypes.c_void_p(260)) == ok.OSCAR_ERR_INVALID_ARG  # misaligned workspace
+    need = lib.oscar_decode_workspace_bytes(ctypes.byref(d), 2, 100, 8, 4, 8)
+    assert need > 0
+    assert _decode(lib, d, ws_bytes=need - 1) == ok.OSCAR_ERR_WORKSPACE
+
+
+def test_workspace_sizes(lib):
+    d = _dims(max_pages_per_seq=2048)
+    a = lib.oscar_decode_workspace_bytes(ctypes.byref(d), 1, 32768, 64, 64, 128)
+    b = lib.oscar_decode_workspace_bytes(ctypes.byref(d), 1, 32768, 16, 64, 128)
+    assert 0 < a < b and a % 256 == 0
+    assert lib.oscar_decode_workspace_bytes(ctypes.byref(d), 1, 2048 * 16 + 1, 64, 64, 128) == 0
+    assert lib.oscar_bf16_decode_workspace_bytes(ctypes.byref(d), 1, 32768, 64) > 0
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert ok.status_string(s).startswith("OSCAR")

@@ -1,0 +1,105 @@
+"""GPU parity of oscar_append against the oracle (bit-exact codes and layout)."""
+
+import numpy as np
+import pytest
+import torch
+
+from int2_rotated_kv_append_gb300 import synth
+from int2_rotated_kv_append_gb300.cache import Int2Cache
+from parity import check_append, pools_to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def _append_all(w, cache):
+    cache.append(w.k.cuda(), w.v.cuda(), w.slot_mapping.cuda())
+    torch.cuda.synchronize()
+    return pools_to_host(cache)
+
+
+def test_append_tiny_config():
+    w = synth.make_config(0)
+    cache = Int2Cache(w)
+    codes, sz = _append_all(w, cache)
+    stats = check_append(w, codes, sz, w.k, w.v, w.slot_mapping.numpy())
+    assert stats["elements"] == 512 * 2 * 64
+
+
+@pytest.mark.parametrize("D,G", [(64, 32), (64, 64), (128, 32), (128, 64), (128, 128)])
+@pytest.mark.parametrize("H", [1, 3])
+def test_append_sweep_random_slots(D, G, H):
+    # 70 tokens (3 tiles, ragged) into random distinct slots of a 12-page pool; some slots skipped.
+    w = synth.make_workload(num_q_heads=H, num_kv_heads=H, head_dim=D, group_size=G, sink_len=0, window_len=0,
+                            seq_lens=[70], seed=D + G + H, spare_pages=7)
+    g = torch.Generator().manual_seed(D * 7 + G + H)
+    slots = torch.randperm(w.num_pages * 16, generator=g)[:70].to(torch.int64)
+    slots[5] = -1
+    slots[40] = -7
+    cache = Int2Cache(w)
+    cache.append(w.k.cuda(), w.v.cuda(), slots.cuda())
+    torch.cuda.synchronize()
+    codes, sz = pools_to_host(cache)
+    check_append(w, codes, sz, w.k, w.v, slots.numpy())
+
+
+def test_append_unclipped_identity_rotation():
+    # R = I and infinite clip: the codes quantise the raw bf16 values.
+    w = synth.make_workload(num_q_heads=2, num_kv_heads=2, head_dim=128, group_size=64, sink_len=0, window_len=0,
+                            seq_lens=[45], seed=3, clip_frac=None)
+    w.R_k = torch.eye(128).expand(2, 128, 128).contiguous()
+    w.R_v = w.R_k.clone()
+    cache = Int2Cache(w)
+    codes, sz = _append_all(w, cache)
+    check_append(w, codes, sz, w.k, w.v, w.slot_mapping.numpy())
+
+
+def test_append_zero_clip_degenerate():
+    w = synth.make_workload(num_q_heads=1, num_kv_heads=1, head_dim=64, group_size=32, sink_len=0, window_len=0,
+                            seq_lens=[20], seed=4)
+    w.clip_k = torch.zeros_like(w.clip_k)
+    w.clip_v = torch.zeros_like(w.clip_v)
+    cache = Int2Cache(w)
+    codes, sz = _append_all(w, cache)
+    check_append(w, codes, sz, w.k, w.v, w.slot_mapping.numpy())
+    rows = codes.reshape(w.num_pages, 1, 2, 16, 16)
+    pt = w.page_table.numpy()[0]
+    assert np.all(rows[pt[0], :, :, :16] == 0) and np.all(rows[pt[1], :, :, :4] == 0)
+
+
+def test_append_prefill_config_sampled():
+    # Prefill append of 16384 tokens x 8 heads x D=128 at full size; the oracle checks a sample.
+    w = synth.make_config(4, device="cuda")
+    cache = Int2Cache(w)
+    codes, sz = _append_all(w, cache)
+    g = np.random.default_rng(0)
+    sample = np.sort(g.choice(w.num_tokens, 1024, replace=False))
+    sample = np.concatenate([sample, [0, w.num_tokens - 1]])
+    check_append(w, codes, sz, w.k, w.v, w.slot_mapping.numpy(), sample=sample)
+
+
+def test_append_decode_batch_random_slots():
+    # Decode append: 256 single tokens at random slots of a pool, every token checked.
+    w = synth.make_workload(num_q_heads=32, num_kv_heads=8, head_dim=128, group_size=64, sink_len=64,
+                            window_len=128, seq_lens=[4096], seed=4, device="cuda")
+    k, v, slots = synth.decode_append_batch(w, 256)
+    cache = Int2Cache(w)
+    cache.append(k, v, slots.cuda())
+    torch.cuda.synchronize()
+    codes, sz = pools_to_host(cache)
+    check_append(w, codes, sz, k, v, slots.numpy())
+
+
+def test_append_slot_past_pool_is_flagged():
+    import int2_rotated_kv_append_gb300 as ok
+    ok.oscar_device_errors(reset=True)
+    w = synth.make_workload(num_q_heads=1, num_kv_heads=1, head_dim=64, group_size=32, sink_len=0, window_len=0,
+                            seq_lens=[8], seed=6)
+    slots = w.slot_mapping.clone()
+    slots[3] = w.num_pages * 16 + 5
+    cache = Int2Cache(w)
+    cache.append(w.k.cuda(), w.v.cuda(), slots.cuda())
+    flags = ok.oscar_device_errors(reset=True)
+    assert flags & ok.OSCAR_DEVERR_SLOT
+    codes, sz = pools_to_host(cache)
+    keep = np.array([i for i in range(8) if i != 3])
+    check_append(w, codes, sz, w.k, w.v, slots.numpy(), sample=keep)

@@ -1,0 +1,127 @@
+"""GPU parity of oscar_decode: the oracle recomputes every checked output from
+the GPU's own codes and scale/zero (max-abs <= 2e-3, mean-abs <= 2e-4)."""
+
+import numpy as np
+import pytest
+import torch
+
+import int2_rotated_kv_append_gb300 as ok
+from int2_rotated_kv_append_gb300 import synth
+from int2_rotated_kv_append_gb300.cache import Int2Cache
+from parity import compare_decode, oracle_decode_on_gpu_cache
+
+pytestmark = pytest.mark.gpu
+
+
+def _built(w, pps=None):
+    cache = Int2Cache(w, pages_per_split=pps)
+    cache.prefill()
+    return cache
+
+
+def test_decode_tiny_config():
+    w = synth.make_config(0)
+    cache = _built(w)
+    out = cache.decode(w.q.cuda())
+    compare_decode(out, oracle_decode_on_gpu_cache(w, cache))
+
+
+def test_decode_batch1_32k_config_all_heads():
+    w = synth.make_config(1, device="cuda")
+    cache = _built(w)
+    out = cache.decode(w.q)
+    compare_decode(out, oracle_decode_on_gpu_cache(w, cache))
+
+
+def test_decode_batch64_config_sampled():
+    w = synth.make_config(2, device="cuda")
+    cache = _built(w)
+    out = cache.decode(w.q)
+    lens = w.seq_lens.numpy()
+    bs = [int(np.argmin(lens)), int(np.argmax(lens)), 7, 33]
+    pairs = [(b, h) for b in bs for h in (0, 13, 31)]
+    compare_decode(out, oracle_decode_on_gpu_cache(w, cache, pairs=pairs), pairs=pairs)
+
+
+def test_decode_131k_gqa8_config_sampled():
+    w = synth.make_config(3, device="cuda")
+    cache = _built(w)
+    out = cache.decode(w.q)
+    pairs = [(0, 0), (1, 9), (2, 40), (3, 63)]
+    compare_decode(out, oracle_decode_on_gpu_cache(w, cache, pairs=pairs), pairs=pairs)
+
+
+@pytest.mark.parametrize("D,G,Hq,H", [(64, 32, 1, 1), (64, 64, 4, 2), (128, 64, 8, 2), (128, 32, 6, 3),
+                                      (128, 128, 8, 1), (128, 64, 2, 2)])
+def test_decode_edge_lengths(D, G, Hq, H):
+    # Lengths around every boundary: empty, single token, inside the sink, at the
+    # sink/window edge, bulk starting mid-page, window ends mid-page, multi-split.
+    S, W = 5, 19
+    lens = [0, 1, S - 1, S, S + 1, S + W, S + W + 1, S + W + 16, 16 * 9 + 3, 700]
+    w = synth.make_workload(num_q_heads=Hq, num_kv_heads=H, head_dim=D, group_size=G, sink_len=S, window_len=W,
+                            seq_lens=lens, seed=D + Hq, spare_pages=5)
+    for pps in (0, 1, 3):
+        cache = _built(w, pps=pps)
+        out = cache.decode(w.q.cuda())
+        compare_decode(out, oracle_decode_on_gpu_cache(w, cache))
+
+
+@pytest.mark.parametrize("S,W", [(0, 0), (0, 32), (16, 0), (64, 256)])
+def test_decode_sink_window_extremes(S, W):
+    w = synth.make_workload(num_q_heads=8, num_kv_heads=2, head_dim=128, group_size=64, sink_len=S, window_len=W,
+                            seq_lens=[300, 1000, 77], seed=S + W)
+    cache = _built(w)
+    out = cache.decode(w.q.cuda())
+    compare_decode(out, oracle_decode_on_gpu_cache(w, cache))
+
+
+def test_decode_split_size_invariance():
+    w = synth.make_workload(num_q_heads=8, num_kv_heads=2, head_dim=128, group_size=64, sink_len=16, window_len=32,
+                            seq_lens=[3000, 1234], seed=11)
+    outs = []
+    for pps in (1, 2, 7, 64, 0):
+        cache = _built(w, pps=pps)
+        outs.append(cache.decode(w.q.cuda()).cpu())
+    for o in outs[1:]:
+        assert torch.max(torch.abs(o - outs[0])).item() <= 1e-5
+
+
+def test_decode_page_shuffle_bit_identical():
+    w = synth.make_workload(num_q_heads=4, num_kv_heads=1, head_dim=128, group_size=64, sink_len=8, window_len=16,
+                            seq_lens=[900], seed=12, spare_pages=10)
+    cache = _built(w)
+    out1 = cache.decode(w.q.cuda()).clone()
+    perm = torch.randperm(w.num_pages, generator=torch.Generator().manual_seed(1))
+    codes = cache.int2_pages.view(w.num_pages, -1)
+    sz = cache.scale_zero.view(w.num_pages, -1)
+    new_codes, new_sz = torch.empty_like(codes), torch.empty_like(sz)
+    new_codes[perm.cuda()] = codes
+    new_sz[perm.cuda()] = sz
+    cache.int2_pages.copy_(new_codes.view(-1))
+    cache.scale_zero.copy_(new_sz.view(-1))
+    cache.page_table = perm.to(torch.int32)[w.page_table.long().clamp(min=0)].cuda()
+    out2 = cache.decode(w.q.cuda())
+    assert torch.equal(out1, out2)
+
+
+def test_decode_bad_page_id_is_flagged_and_finite():
+    w = synth.make_workload(num_q_heads=4, num_kv_heads=1, head_dim=64, group_size=32, sink_len=4, window_len=8,
+                            seq_lens=[200], seed=13)
+    cache = _built(w)
+    ok.oscar_device_errors(reset=True)
+    pt = cache.page_table.clone()
+    pt[0, 3] = w.num_pages + 100
+    cache.page_table = pt
+    out = cache.decode(w.q.cuda())
+    flags = ok.oscar_device_errors(reset=True)
+    assert flags & ok.OSCAR_DEVERR_PAGE_ID
+    assert torch.isfinite(out).all()
+
+
+def test_decode_seq_len_over_bound_is_flagged():
+    w = synth.make_workload(num_q_heads=2, num_kv_heads=1, head_dim=64, group_size=32, sink_len=4, window_len=8,
+                            seq_lens=[100], seed=14)
+    cache = _built(w)
+    ok.oscar_device_errors(reset=True)
+    cache.decode(w.q.cuda(), seq_lens=torch.tensor([150], dtype=torch.int32, device="cuda"), max_seq_len=100)
+    assert ok.oscar_device_errors(reset=True) & ok.OSCAR_DEVERR_SEQ_LEN
