@@ -18,6 +18,62 @@ using namespace oscar;
 
 constexpr int kTokTile = 32;
 constexpr int kThreads = 256;  // 8 warps x 4 tokens each
+constexpr int64_t kSmallTokenLimit = 512;  // at most this many tokens use the few-token kernel
+
+// Clip, group min/max, fp16 scale/zero, codes, pack and store of one rotated
+// vector held by a warp (lane l owns channels [l*CPL, (l+1)*CPL)).  Called by
+// all 32 lanes of the warp with a warp-uniform slot.
+template <int D>
+__device__ __forceinline__ void quantize_store(const float (&acc)[D / 32], const float (&cl)[D / 32], int64_t slot,
+                                               int H, int G, int num_pages, int h, int kv, int lane,
+                                               uint8_t* __restrict__ codes, __half* __restrict__ sz) {
+  constexpr int CPL = D / 32;
+  if (slot < 0) return;
+  if (slot >= static_cast<int64_t>(num_pages) * kPageSize) {
+    if (lane == 0) record_error(OSCAR_DEVERR_SLOT);
+    return;
+  }
+  const int lanes_per_group = G / CPL;
+  float y[CPL];
+  float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    y[c] = fminf(fmaxf(acc[c], -cl[c]), cl[c]);
+    mn = fminf(mn, y[c]);
+    mx = fmaxf(mx, y[c]);
+  }
+  for (int off = 1; off < lanes_per_group; off <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  const __half sh = __float2half_rn((mx - mn) / 3.0f);
+  const __half zh = __float2half_rn(mn);
+  const float s = __half2float(sh), z = __half2float(zh);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    uint32_t code = 0;
+    if (s != 0.f) {
+      const float u = (y[c] - z) / s;
+      code = static_cast<uint32_t>(fminf(fmaxf(rintf(u), 0.f), 3.f));
+    }
+    packed |= code << (2 * c);
+  }
+  const int64_t page = slot / kPageSize;
+  const int off = static_cast<int>(slot % kPageSize);
+  const size_t row = ((static_cast<size_t>(page) * H + h) * 2 + kv) * kPageSize + off;
+  uint8_t* row_codes = codes + row * (D / 4);
+  if constexpr (CPL == 4) {
+    row_codes[lane] = static_cast<uint8_t>(packed);
+  } else {
+    const uint32_t hi = __shfl_down_sync(0xffffffffu, packed, 1);
+    if ((lane & 1) == 0) row_codes[lane / 2] = static_cast<uint8_t>(packed | (hi << 4));
+  }
+  if (lane % lanes_per_group == 0) {
+    const int g = lane / lanes_per_group;
+    reinterpret_cast<__half2*>(sz + row * (D / G) * 2)[g] = __halves2half2(sh, zh);
+  }
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) append_kernel(
@@ -77,58 +133,91 @@ __global__ void __launch_bounds__(kThreads) append_kernel(
   float cl[CPL];
 #pragma unroll
   for (int c = 0; c < CPL; ++c) cl[c] = __ldg(clip + CPL * lane + c);
-  const int lanes_per_group = G / CPL;
-
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const int64_t t = t0 + warp + 8 * m;
     if (t >= num_tokens) break;  // warp-uniform
-    const int64_t slot = __ldg(slots + t);
-    if (slot < 0) continue;
-    if (slot >= static_cast<int64_t>(num_pages) * kPageSize) {
-      if (lane == 0) record_error(OSCAR_DEVERR_SLOT);
-      continue;
-    }
-    float y[CPL];
-    float mn = INFINITY, mx = -INFINITY;
+    quantize_store<D>(acc[m], cl, __ldg(slots + t), H, G, num_pages, h, kv, lane, codes, sz);
+  }
+}
+
+// Few-token variant (decode-time append): the D rows of R are split over the 8
+// warps (D/8 rows each, read from L2 without staging all of R), each warp keeps
+// partial sums for up to kSmallTok tokens, and the partials are added in a
+// fixed warp order through shared memory before the same quantise/store step.
+constexpr int kSmallTok = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) append_small_kernel(
+    int64_t num_tokens, int H, int G, int num_pages, const __nv_bfloat16* __restrict__ k,
+    const __nv_bfloat16* __restrict__ v, const float* __restrict__ R_k, const float* __restrict__ R_v,
+    const float* __restrict__ clip_k, const float* __restrict__ clip_v, const int64_t* __restrict__ slots,
+    uint8_t* __restrict__ codes, __half* __restrict__ sz) {
+  constexpr int CPL = D / 32;
+  constexpr int kWarpsA = kThreads / 32;
+  constexpr int kRows = D / kWarpsA;
+  __shared__ __align__(16) float xs[kSmallTok * D];
+  __shared__ __align__(16) float part[kWarpsA * kSmallTok * D];
+  const int h = blockIdx.y, kv = blockIdx.z;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kSmallTok;
+  const float* R = (kv ? R_v : R_k) + static_cast<size_t>(h) * D * D;
+  const float* clip = (kv ? clip_v : clip_k) + static_cast<size_t>(h) * D;
+  const __nv_bfloat16* x = kv ? v : k;
+  for (int i = threadIdx.x; i < kSmallTok * D / 2; i += kThreads) {
+    const int tt = i / (D / 2), c2 = i % (D / 2);
+    const int64_t t = t0 + tt;
+    float2 val = make_float2(0.f, 0.f);
+    if (t < num_tokens)
+      val = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(x + (static_cast<size_t>(t) * H + h) * D)[c2]);
+    xs[tt * D + 2 * c2] = val.x;
+    xs[tt * D + 2 * c2 + 1] = val.y;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  float acc[kSmallTok][CPL];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-      y[c] = fminf(fmaxf(acc[m][c], -cl[c]), cl[c]);
-      mn = fminf(mn, y[c]);
-      mx = fmaxf(mx, y[c]);
-    }
-    for (int off = 1; off < lanes_per_group; off <<= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    }
-    const __half sh = __float2half_rn((mx - mn) / 3.0f);
-    const __half zh = __float2half_rn(mn);
-    const float s = __half2float(sh), z = __half2float(zh);
-    uint32_t packed = 0;
+  for (int m = 0; m < kSmallTok; ++m)
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-      uint32_t code = 0;
-      if (s != 0.f) {
-        const float u = (y[c] - z) / s;
-        code = static_cast<uint32_t>(fminf(fmaxf(rintf(u), 0.f), 3.f));
-      }
-      packed |= code << (2 * c);
-    }
-    const int64_t page = slot / kPageSize;
-    const int off = static_cast<int>(slot % kPageSize);
-    const size_t row = ((static_cast<size_t>(page) * H + h) * 2 + kv) * kPageSize + off;
-    uint8_t* row_codes = codes + row * (D / 4);
+    for (int c = 0; c < CPL; ++c) acc[m][c] = 0.f;
+#pragma unroll 4
+  for (int r = 0; r < kRows; ++r) {
+    const int i = warp * kRows + r;
+    float rv[CPL];
     if constexpr (CPL == 4) {
-      row_codes[lane] = static_cast<uint8_t>(packed);
+      const float4 q4 = __ldg(reinterpret_cast<const float4*>(R + static_cast<size_t>(i) * D) + lane);
+      rv[0] = q4.x; rv[1] = q4.y; rv[2] = q4.z; rv[3] = q4.w;
     } else {
-      const uint32_t hi = __shfl_down_sync(0xffffffffu, packed, 1);
-      if ((lane & 1) == 0) row_codes[lane / 2] = static_cast<uint8_t>(packed | (hi << 4));
+      const float2 q2 = __ldg(reinterpret_cast<const float2*>(R + static_cast<size_t>(i) * D) + lane);
+      rv[0] = q2.x; rv[1] = q2.y;
     }
-    if (lane % lanes_per_group == 0) {
-      const int g = lane / lanes_per_group;
-      reinterpret_cast<__half2*>(sz + row * (D / G) * 2)[g] = __halves2half2(sh, zh);
+#pragma unroll
+    for (int m = 0; m < kSmallTok; ++m) {
+      const float xv = xs[m * D + i];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acc[m][c] = fmaf(xv, rv[c], acc[m][c]);
     }
   }
+#pragma unroll
+  for (int m = 0; m < kSmallTok; ++m)
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) part[(warp * kSmallTok + m) * D + CPL * lane + c] = acc[m][c];
+  __syncthreads();
+  // warp m finishes token m
+  const int m = warp;
+  const int64_t t = t0 + m;
+  if (m >= kSmallTok || t >= num_tokens) return;
+  float tot[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    float a = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarpsA; ++w) a += part[(w * kSmallTok + m) * D + CPL * lane + c];
+    tot[c] = a;
+  }
+  float cl[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) cl[c] = __ldg(clip + CPL * lane + c);
+  quantize_store<D>(tot, cl, __ldg(slots + t), H, G, num_pages, h, kv, lane, codes, sz);
 }
 
 // Plain copy of bf16 rows into the BF16 paged pool, 16 bytes per thread.
@@ -161,6 +250,14 @@ template <int D>
 cudaError_t launch_append(int64_t T, const oscar_dims_t* d, const void* k, const void* v, const float* R_k,
                           const float* R_v, const float* clip_k, const float* clip_v, const int64_t* slots,
                           uint8_t* codes, void* sz, cudaStream_t stream) {
+  // Few tokens per (head, K|V): spread R's rows over warps instead of staging all of R.
+  if (T <= kSmallTokenLimit) {
+    const dim3 grid(static_cast<unsigned>((T + kSmallTok - 1) / kSmallTok), d->num_kv_heads, 2);
+    append_small_kernel<D><<<grid, kThreads, 0, stream>>>(
+        T, d->num_kv_heads, d->group_size, d->num_pages, static_cast<const __nv_bfloat16*>(k),
+        static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz));
+    return cudaGetLastError();
+  }
   const size_t smem = (static_cast<size_t>(D) * D + kTokTile * D) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(append_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));

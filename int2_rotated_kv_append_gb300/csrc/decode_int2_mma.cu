@@ -1,0 +1,553 @@
+// Tensor-core split kernel of the OSCAR decode for the INT2 bulk
+// ("OSCAR: Offline Spectral Covariance-Aware Rotation for 2-bit KV Cache
+// Quantization", abstract: INT2 attention kernel over a paged KV cache;
+// project card "How it works": fused mixed-precision attention).
+//
+// Shape covered: head_dim 128, group 64 or 128, GQA 1..8.  One CTA of 4 warps
+// owns one split (a run of pages) of one (sequence, KV head); BF16 sink/window
+// splits of the same grid run the CUDA-core body of decode_common.cuh.
+//
+// Per warp and page (16 tokens x 128 channels, K and V):
+//   * the page's 1024 code bytes and 128/256 scale-zero bytes arrive by two
+//     bulk async copies (cp.async.bulk + mbarrier) into a per-warp ring of
+//     kStages pages, so many pages per SM are in flight;
+//   * QK:  S^T[token][query] = C_k[token][ch] . Qs[ch][query] on mma.sync
+//     m16n8k16 (fp16 in, fp32 accumulate), one accumulator per group.  A is
+//     built from the packed codes with one AND per register: the 2-bit code at
+//     bit position k of an fp16 half is the subnormal c * 2^(k-24), exact.  B
+//     holds q.R_k (already in log2 units) times 2^(E_q - k) for that channel,
+//     split into fp16 hi + lo (about 22 significant bits), so the product
+//     c * q * 2^(E_q - 24) is exact for every channel;
+//   * logits: sum_g scale_g * 2^(24 - E_q) * acc_g + zero_g * sum_{ch in g} q;
+//     online softmax per query with warp shuffles;
+//   * PV:  O^T[ch][query] += C_v^T[ch][token] . P'[token][query] on the same
+//     MMA; A pairs two tokens of one channel (one byte-permute + one AND), B is
+//     p * scale_g * 2^sig split into fp16 hi + lo, with sig a per-warp power of
+//     two that keeps P' below 2^14; the zero term sum p * zero_g, the per-channel
+//     power of two and 2^-sig are applied once at the end.
+// The warps of a CTA are merged through shared memory by log-sum-exp and the
+// CTA writes one (max, sum, output) partial per query head.
+#include "decode_common.cuh"
+
+namespace oscar_dec {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kWarps = 4;
+constexpr int kStages = 6;               // pages in flight per warp
+constexpr int kCodeBytes = 2 * 16 * 32;  // K then V codes of one (page, KV head)
+constexpr int kMaxPps = 256;             // page ids of one split staged in shared memory
+constexpr long long kWaitCycles = 2000000000LL;  // bounded wait on an async copy (about 1 s)
+
+template <int NG>
+struct Geo {
+  static constexpr int kSzBytes = 2 * 16 * NG * 2 * 2;  // K then V fp16 (scale, zero) of 16 tokens
+  static constexpr int kStageBytes = kCodeBytes + kSzBytes;
+  static constexpr size_t kPagedSmem =
+      static_cast<size_t>(kWarps) * kStages * kStageBytes + kWarps * kStages * 8 + kMaxPps * 4;
+  static constexpr size_t kSmem = kPagedSmem > split_body_smem(kD) ? kPagedSmem : split_body_smem(kD);
+};
+
+// ---- PTX helpers -------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity; gives up after kWaitCycles.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long start = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - start > kWaitCycles) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 2^k as a float for -126 <= k <= 127 (exact).
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
+
+// Bit position, inside its fp16 half, of channel e (0..15) of a packed word
+// after the extraction below: e%8 <= 4 sit at 2*(e%8) of the raw word's half,
+// e%8 >= 5 at 2*(e%8) - 10 after a right shift by 10.
+__host__ __device__ constexpr int kpos(int e) { return (e & 7) <= 4 ? 2 * (e & 7) : 2 * (e & 7) - 10; }
+
+// fp16x2 register holding channels e and e+8 of packed word w (e in 0..7) as the
+// subnormals c_e * 2^(kpos(e) - 24) (low half) and c_{e+8} * 2^(kpos(e) - 24).
+template <int E>
+__device__ __forceinline__ uint32_t extract_pair(uint32_t w, uint32_t w_shr10) {
+  constexpr int k = kpos(E);
+  constexpr uint32_t mask = (3u << k) | (3u << (16 + k));
+  return ((E & 7) <= 4 ? w : w_shr10) & mask;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
+  return static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+}
+
+// ---- the kernel --------------------------------------------------------------
+
+template <int NT, int NG>
+__global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (s >= p.n_paged) {
+    split_body<kD, kMixed>(p, s, h, b, reinterpret_cast<float*>(smem));
+    return;
+  }
+  constexpr int kStageBytes = Geo<NG>::kStageBytes;
+  constexpr int kSzBytes = Geo<NG>::kSzBytes;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int gqa = p.gqa;
+  const int L = clamp_len(p, b);
+  const int win_begin = max(p.S, L - p.W);
+  const int lo_pos = s * p.pps * kPageSize;
+  const int r0 = max(lo_pos, p.S), r1 = min(lo_pos + p.pps * kPageSize, win_begin);
+  const size_t bh0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * gqa;
+
+  if (r1 <= r0) {  // nothing of the bulk falls in this split
+    grid_dep_launch_dependents();
+    for (int i = tid; i < gqa * kD; i += kWarps * 32)
+      p.part_o[((bh0 + i / kD) * p.ns + s) * kD + i % kD] = 0.f;
+    if (tid < gqa) {
+      p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 0] = -INFINITY;
+      p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 1] = 0.f;
+    }
+    return;
+  }
+  const int pg0 = r0 / kPageSize;
+  const int npg = (r1 - 1) / kPageSize + 1 - pg0;
+
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kStageBytes);
+  int* pid_s = reinterpret_cast<int*>(bars + kWarps * kStages);
+  for (int i = tid; i < npg; i += kWarps * 32) {
+    int pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg0 + i);
+    if (pid < 0 || pid >= p.num_pages) {
+      record_error(OSCAR_DEVERR_PAGE_ID);
+      pid = -1;
+    }
+    pid_s[i] = pid;
+  }
+  if (lane == 0)
+    for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp * kStages + i]), 1);
+  mbar_init_fence();
+  __syncthreads();
+
+  const int n_my = npg > warp ? (npg - warp + kWarps - 1) / kWarps : 0;
+  uint8_t* my_stages = stages + warp * kStages * kStageBytes;
+  uint64_t* my_bars = bars + warp * kStages;
+  auto issue = [&](int i) {  // lane 0: bring local page i of this warp into its stage
+    const int pid = pid_s[warp + i * kWarps];
+    const uint32_t bar = smem_u32(&my_bars[i % kStages]);
+    if (pid < 0) {
+      mbar_arrive(bar);
+      return;
+    }
+    uint8_t* st = my_stages + (i % kStages) * kStageBytes;
+    const size_t ph = static_cast<size_t>(pid) * p.H + h;
+    mbar_arrive_expect_tx(bar, kStageBytes);
+    bulk_g2s(smem_u32(st), p.codes + ph * kCodeBytes, kCodeBytes, bar);
+    bulk_g2s(smem_u32(st + kCodeBytes), reinterpret_cast<const uint8_t*>(p.sz) + ph * kSzBytes, kSzBytes, bar);
+  };
+  if (lane == 0)
+    for (int i = 0; i < n_my && i < kStages; ++i) issue(i);
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // q_rot comes from the preceding kernel; the page copies above do not need it
+
+  // ---- query side (overlaps the first copies) ----
+  // Per n-tile nt this thread's C columns belong to query 4*nt + t and its B
+  // column to query 4*nt + (g >> 1), part g & 1 (0 = hi, 1 = lo).
+  const float* qr = p.q_rot + bh0 * kD;
+  float F[NT], qs[NT][NG];
+  int Eb[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    F[nt] = 0.f;
+    Eb[nt] = 0;
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) qs[nt][gg] = 0.f;
+  }
+  for (int qi = 0; qi < gqa; ++qi) {  // warp-uniform loop
+    const float4 v4 = *reinterpret_cast<const float4*>(qr + qi * kD + 4 * lane);
+    const float a0 = v4.x * p.scale_log2, a1 = v4.y * p.scale_log2, a2 = v4.z * p.scale_log2,
+                a3 = v4.w * p.scale_log2;
+    float amax = fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3)));
+    float sum = (a0 + a1) + (a2 + a3);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    // group sums: G = 64 -> lanes 0..15 and 16..31; G = 128 -> all lanes
+#pragma unroll
+    for (int off = 1; off < 32 / NG; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    const float sum_lo = __shfl_sync(0xffffffffu, sum, 0);
+    const float sum_hi = __shfl_sync(0xffffffffu, sum, 31);
+    int e = 0;
+    if (amax > 0.f) frexpf(amax, &e);
+    const int E = min(max(15 - e, -100), 100);  // max |q| * 2^E < 2^15 (clamped far from fp32 limits)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      if (qi == 4 * nt + t) {
+        F[nt] = pow2i(24 - E);
+        qs[nt][0] = sum_lo;
+        if (NG == 2) qs[nt][NG - 1] = sum_hi;
+      }
+      if (qi == 4 * nt + (g >> 1)) Eb[nt] = E;
+    }
+  }
+  // B fragments of QK: k-step ks uses word w = t + 4 * (ks >= 4) of each token,
+  // channels 16w + j, 16w + j + 8 (rows 2t, 2t+1) and 16w + j + 1, 16w + j + 9
+  // (rows 2t + 8, 2t + 9), with j = 2 * (ks & 3).
+  uint32_t bq[NT][8][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int qb = 4 * nt + (g >> 1);
+    const bool use = qb < gqa;
+    const bool lo_part = (g & 1) != 0;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int w = t + 4 * (ks >> 2);
+      const int j = 2 * (ks & 3);
+      const int chs[4] = {16 * w + j, 16 * w + j + 8, 16 * w + j + 1, 16 * w + j + 9};
+      __half hv[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float x = 0.f;
+        if (use) x = __ldg(qr + qb * kD + chs[c]) * p.scale_log2 * pow2i(Eb[nt] - kpos(chs[c] & 15));
+        const __half hi = __float2half_rn(x);
+        hv[c] = lo_part ? __float2half_rn(x - __half2float(hi)) : hi;
+      }
+      bq[nt][ks][0] = pack_half2(hv[0], hv[1]);
+      bq[nt][ks][1] = pack_half2(hv[2], hv[3]);
+    }
+  }
+
+  // ---- main loop over this warp's pages ----
+  float m_run[NT], l_run[NT], zacc[NT][NG], O[NT][8][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m_run[nt] = -INFINITY;
+    l_run[nt] = 0.f;
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) O[nt][i][c] = 0.f;
+  }
+  // P' = p * scale_v is carried as P' * 2^sig with sig chosen from the running
+  // max of the V scales seen by this warp, so P' * 2^sig < 2^14: no fp16
+  // overflow, and the fp16 lo part stays normal for every weight that matters.
+  float smax_run = 0.f;
+  int sig = 0;
+  const uint32_t vsel = (2 * (g & 1)) | ((2 * (g & 1) + 1) << 4) | ((4 + 2 * (g & 1)) << 8) | ((5 + 2 * (g & 1)) << 12);
+  const int src1 = 4 * t + (g >> 1), src2 = src1 + 16;
+  bool aborted = false;
+  int i = 0;
+  for (; i < n_my; ++i) {
+    const uint32_t bar = smem_u32(&my_bars[i % kStages]);
+    const bool ok = mbar_wait_bounded(bar, (i / kStages) & 1);
+    if (__any_sync(0xffffffffu, !ok)) {
+      aborted = true;
+      break;
+    }
+    const uint8_t* st = my_stages + (i % kStages) * kStageBytes;
+    const int jpage = warp + i * kWarps;
+    const bool page_ok = pid_s[jpage] >= 0;
+    const int pos0 = (pg0 + jpage) * kPageSize + g;
+    const bool v0 = page_ok && pos0 >= r0 && pos0 < r1;
+    const bool v1 = page_ok && pos0 + 8 >= r0 && pos0 + 8 < r1;
+
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st);
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + 512);
+    const uint32_t kw0 = kc[g * 8 + t], kw1 = kc[g * 8 + t + 4];
+    const uint32_t kw2 = kc[(g + 8) * 8 + t], kw3 = kc[(g + 8) * 8 + t + 4];
+    const int vw = g >> 1;
+    uint32_t xa[2], xb[2];
+#pragma unroll
+    for (int hw = 0; hw < 2; ++hw) {
+      xa[hw] = __byte_perm(vc[t * 8 + 4 * hw + vw], vc[(t + 8) * 8 + 4 * hw + vw], vsel);
+      xb[hw] = __byte_perm(vc[(t + 4) * 8 + 4 * hw + vw], vc[(t + 12) * 8 + 4 * hw + vw], vsel);
+    }
+    const __half2* szk = reinterpret_cast<const __half2*>(st + kCodeBytes);
+    const __half2* szv = szk + 16 * NG;
+    float2 k0[NG], k1[NG], w0[NG], w1[NG];
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) {
+      k0[gg] = __half22float2(szk[g * NG + gg]);
+      k1[gg] = __half22float2(szk[(g + 8) * NG + gg]);
+      w0[gg] = __half22float2(szv[g * NG + gg]);
+      w1[gg] = __half22float2(szv[(g + 8) * NG + gg]);
+    }
+    {
+      float sm = 0.f;
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg) sm = fmaxf(sm, fmaxf(v0 ? w0[gg].x : 0.f, v1 ? w1[gg].x : 0.f));
+      sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 4));
+      sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 8));
+      sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 16));
+      if (sm > smax_run) {  // warp-uniform
+        int e = 0;
+        frexpf(sm, &e);  // sm < 2^e
+        const int sig_new = min(max(14 - e, -100), 100);
+        if (smax_run > 0.f && sig_new < sig) {
+          const float f = pow2i(sig_new - sig);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int mi = 0; mi < 8; ++mi)
+#pragma unroll
+              for (int c = 0; c < 4; ++c) O[nt][mi][c] *= f;
+        }
+        if (smax_run == 0.f || sig_new < sig) sig = sig_new;
+        smax_run = sm;
+      }
+    }
+    const float psc = pow2i(sig);
+
+    // QK
+    float acc[NT][NG][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[nt][gg][c] = 0.f;
+    {
+      const uint32_t kw0s = kw0 >> 10, kw1s = kw1 >> 10, kw2s = kw2 >> 10, kw3s = kw3 >> 10;
+#define OSCAR_QK_STEP(KS)                                                                         \
+  {                                                                                               \
+    constexpr int gg = (KS) * NG / 8;                                                             \
+    constexpr int j = 2 * ((KS) & 3);                                                             \
+    const uint32_t wa = (KS) < 4 ? kw0 : kw1, was = (KS) < 4 ? kw0s : kw1s;                       \
+    const uint32_t wb = (KS) < 4 ? kw2 : kw3, wbs = (KS) < 4 ? kw2s : kw3s;                       \
+    const uint32_t a0 = extract_pair<j>(wa, was), a1 = extract_pair<j>(wb, wbs);                  \
+    const uint32_t a2 = extract_pair<j + 1>(wa, was), a3 = extract_pair<j + 1>(wb, wbs);          \
+    _Pragma("unroll") for (int nt = 0; nt < NT; ++nt)                                             \
+        mma16816(acc[nt][gg], a0, a1, a2, a3, bq[nt][KS][0], bq[nt][KS][1]);                      \
+  }
+      OSCAR_QK_STEP(0) OSCAR_QK_STEP(1) OSCAR_QK_STEP(2) OSCAR_QK_STEP(3)
+      OSCAR_QK_STEP(4) OSCAR_QK_STEP(5) OSCAR_QK_STEP(6) OSCAR_QK_STEP(7)
+#undef OSCAR_QK_STEP
+    }
+
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float sc0 = 0.f, sc1 = 0.f;
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg) {
+        sc0 += k0[gg].x * F[nt] * (acc[nt][gg][0] + acc[nt][gg][1]) + k0[gg].y * qs[nt][gg];
+        sc1 += k1[gg].x * F[nt] * (acc[nt][gg][2] + acc[nt][gg][3]) + k1[gg].y * qs[nt][gg];
+      }
+      sc0 = v0 ? sc0 : -INFINITY;
+      sc1 = v1 ? sc1 : -INFINITY;
+      float mx = fmaxf(sc0, sc1);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(m_run[nt], mx);
+      if (__any_sync(0xffffffffu, m_new > m_run[nt])) {
+        const float alpha = m_run[nt] == -INFINITY ? 0.f : fast_exp2(m_run[nt] - m_new);
+        l_run[nt] *= alpha;
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] *= alpha;
+#pragma unroll
+        for (int mi = 0; mi < 8; ++mi)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) O[nt][mi][c] *= alpha;
+        m_run[nt] = m_new;
+      }
+      const float p0 = v0 ? fast_exp2(sc0 - m_new) : 0.f;
+      const float p1 = v1 ? fast_exp2(sc1 - m_new) : 0.f;
+      l_run[nt] += p0 + p1;
+      uint32_t bp[NG][2];
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg) {
+        const float q0 = v0 ? p0 * w0[gg].x * psc : 0.f;
+        const float q1 = v1 ? p1 * w1[gg].x * psc : 0.f;
+        zacc[nt][gg] += (v0 ? p0 * w0[gg].y : 0.f) + (v1 ? p1 * w1[gg].y : 0.f);
+        const __half h0 = __float2half_rn(q0), h1 = __float2half_rn(q1);
+        const __half e0 = __float2half_rn(q0 - __half2float(h0)), e1 = __float2half_rn(q1 - __half2float(h1));
+        const uint32_t xhi = pack_half2(h0, h1), xlo = pack_half2(e0, e1);
+        const uint32_t h_1 = __shfl_sync(0xffffffffu, xhi, src1), l_1 = __shfl_sync(0xffffffffu, xlo, src1);
+        const uint32_t h_2 = __shfl_sync(0xffffffffu, xhi, src2), l_2 = __shfl_sync(0xffffffffu, xlo, src2);
+        bp[gg][0] = (g & 1) ? l_1 : h_1;
+        bp[gg][1] = (g & 1) ? l_2 : h_2;
+      }
+      // PV: m-tile mi covers channels 16*word + 8*(g&1) + 2*(mi&3) + {0 (row g), 1 (row g+8)},
+      // word = g/2 for mi < 4 and 4 + g/2 for mi >= 4.
+      const uint32_t xas[2] = {xa[0] >> 10, xa[1] >> 10}, xbs[2] = {xb[0] >> 10, xb[1] >> 10};
+#define OSCAR_PV_TILE(MI)                                                                          \
+  {                                                                                                \
+    constexpr int hw = (MI) >> 2;                                                                  \
+    constexpr int gg = (MI) * NG / 8;                                                              \
+    constexpr int e = 2 * ((MI) & 3);                                                              \
+    mma16816(O[nt][MI], extract_pair<e>(xa[hw], xas[hw]), extract_pair<e + 1>(xa[hw], xas[hw]),    \
+             extract_pair<e>(xb[hw], xbs[hw]), extract_pair<e + 1>(xb[hw], xbs[hw]), bp[gg][0],     \
+             bp[gg][1]);                                                                           \
+  }
+      OSCAR_PV_TILE(0) OSCAR_PV_TILE(1) OSCAR_PV_TILE(2) OSCAR_PV_TILE(3)
+      OSCAR_PV_TILE(4) OSCAR_PV_TILE(5) OSCAR_PV_TILE(6) OSCAR_PV_TILE(7)
+#undef OSCAR_PV_TILE
+    }
+    __syncwarp();
+    if (lane == 0 && i + kStages < n_my) issue(i + kStages);
+  }
+  if (aborted) {
+    if (lane == 0) record_error(OSCAR_DEVERR_TIMEOUT);
+    // Let the copies already issued land (bounded) before the shared memory is reused.
+    const int issued = min(n_my, i + kStages);
+    for (int k = i; k < issued; ++k) mbar_wait_bounded(smem_u32(&my_bars[k % kStages]), (k / kStages) & 1);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m_run[nt] = -INFINITY;
+      l_run[nt] = 0.f;
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = 0.f;
+#pragma unroll
+      for (int mi = 0; mi < 8; ++mi)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) O[nt][mi][c] = 0.f;
+    }
+  }
+
+  // ---- warp totals, then a log-sum-exp merge of the 4 warps ----
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], off);
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] += __shfl_xor_sync(0xffffffffu, zacc[nt][gg], off);
+    }
+  }
+  __syncthreads();  // every stage consumed: the stage area becomes the merge buffer
+  float* mw = reinterpret_cast<float*>(smem);  // [kWarps][kMaxGqa]
+  float* lw = mw + kWarps * kMaxGqa;           // [kWarps][kMaxGqa]
+  float* ow = lw + kWarps * kMaxGqa;           // [kWarps][kMaxGqa][kD]
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int qi = 4 * nt + t;
+    if (qi < gqa) {
+      if (g == 0) {
+        mw[warp * kMaxGqa + qi] = m_run[nt];
+        lw[warp * kMaxGqa + qi] = l_run[nt];
+      }
+#pragma unroll
+      for (int mi = 0; mi < 8; ++mi) {
+        const int gg = mi * NG / 8;
+        const int word = (mi < 4 ? 0 : 4) + (g >> 1);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int e = 2 * (mi & 3) + r;
+          const int ch = 16 * word + 8 * (g & 1) + e;
+          ow[(warp * kMaxGqa + qi) * kD + ch] =
+              (O[nt][mi][2 * r] + O[nt][mi][2 * r + 1]) * pow2i(24 - kpos(e) - sig) + zacc[nt][gg];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < gqa * kD; idx += kWarps * 32) {
+    const int qi = idx / kD, ch = idx % kD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * kMaxGqa + qi]);
+    float o = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mwq = mw[w * kMaxGqa + qi];
+        if (mwq != -INFINITY) o += fast_exp2(mwq - M) * ow[(w * kMaxGqa + qi) * kD + ch];
+      }
+    }
+    p.part_o[((bh0 + qi) * p.ns + s) * kD + ch] = o;
+  }
+  if (tid < gqa) {
+    float M = -INFINITY, l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * kMaxGqa + tid]);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mwq = mw[w * kMaxGqa + tid];
+        if (mwq != -INFINITY) l += fast_exp2(mwq - M) * lw[w * kMaxGqa + tid];
+      }
+    }
+    p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 0] = M;
+    p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 1] = l;
+  }
+}
+
+template <int NT, int NG>
+cudaError_t launch_impl(const Params& p, cudaStream_t stream) {
+  constexpr size_t smem = Geo<NG>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(int2_mma_split_kernel<NT, NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(int2_mma_split_kernel<NT, NG>, dim3(p.ns, p.H, p.B), dim3(kWarps * 32), smem, stream, p);
+}
+
+}  // namespace
+
+bool int2_mma_supported(const Params& p) {
+  return p.D == kD && (p.G == 64 || p.G == 128) && p.gqa >= 1 && p.gqa <= 8 && p.pps <= kMaxPps;
+}
+
+cudaError_t int2_mma_split(const Params& p, cudaStream_t stream) {
+  const bool two = p.gqa > 4;
+  if (p.G == 64) return two ? launch_impl<2, 2>(p, stream) : launch_impl<1, 2>(p, stream);
+  return two ? launch_impl<2, 1>(p, stream) : launch_impl<1, 1>(p, stream);
+}
+
+}  // namespace oscar_dec
+
+oscar_status_t oscar_internal_decode_mma_errors(uint32_t* flags, int reset) {
+  return oscar::read_unit_errors(flags, reset) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}

@@ -50,7 +50,7 @@ def test_append_unclipped_identity_rotation():
     w.R_v = w.R_k.clone()
     cache = Int2Cache(w)
     codes, sz = _append_all(w, cache)
-    check_append(w, codes, sz, w.k, w.v, w.slot_mapping.numpy())
+    check_append(w, codes, sz, w.k, w.v, w.slot_mapping.numpy(), exact=True)
 
 
 def test_append_zero_clip_degenerate():

@@ -81,9 +81,13 @@ def test_decode_split_size_invariance():
     outs = []
     for pps in (1, 2, 7, 64, 0):
         cache = _built(w, pps=pps)
-        outs.append(cache.decode(w.q.cuda()).cpu())
+        out = cache.decode(w.q.cuda())
+        compare_decode(out, oracle_decode_on_gpu_cache(w, cache))
+        outs.append(out.cpu())
+    # fp16 hi+lo operands (about 22 bits) and tensor-core fp32 accumulation: split
+    # sizes agree to ~1e-5; the bound is 20x below the 2e-3 parity tolerance.
     for o in outs[1:]:
-        assert torch.max(torch.abs(o - outs[0])).item() <= 1e-5
+        assert torch.max(torch.abs(o - outs[0])).item() <= 1e-4
 
 
 def test_decode_page_shuffle_bit_identical():
