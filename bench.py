@@ -135,6 +135,14 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(used), "where": where}
 
 
+_T0 = time.perf_counter()
+
+
+def log(msg: str):
+    """Progress line on stderr (the JSON result goes to stdout)."""
+    print(f"[bench {time.perf_counter() - _T0:8.2f}s] {msg}", file=sys.stderr, flush=True)
+
+
 def measured_peak_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -255,7 +263,9 @@ def run_ours(args, world, rank, local):
                                 group_size=64, sink_len=64, window_len=256 if args.config == 3 else 128)
     w0_bytes = algorithmic_bytes_decode(one, base_lens)
     NR = max(1, math.ceil(3 * l2 / w0_bytes)) if args.replicas <= 0 else args.replicas
+    log(f"generating workload: config {args.config}, {NR} replicas")
     w = synth.make_config(args.config, device=dev, replicas=NR)
+    log("building INT2 and BF16 caches")
     cache = Int2Cache(w, device=dev)
     cache.prefill()
     bf = Bf16Cache(w, device=dev)
@@ -347,16 +357,21 @@ def run_ours(args, world, rank, local):
             ms = float(tt.item())
         return ms, (t0, t1)
 
+    log("caches built; timing")
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.1)
     K, Wm = args.steps, args.warmup
     ms, (t0, t1) = timed(step, K, Wm)
     clocks = sampler.summary(t0, t1)
+    log(f"step: {ms / K * 1e3:.2f} us")
     # Decode alone and the BF16 reference decode over the same tokens.
     ms_dec, _ = timed(lambda i: decode_r(i % NR), K, Wm)
+    log(f"decode: {ms_dec / K * 1e3:.2f} us")
     ms_bf, _ = timed(lambda i: bf16_r(i % NR), K, Wm)
+    log(f"bf16 decode: {ms_bf / K * 1e3:.2f} us")
     ms_app, _ = timed(lambda i: append_r(i % NR), K, Wm)
+    log(f"append: {ms_app / K * 1e3:.2f} us")
     sampler.stop()
 
     step_bytes_dec = algorithmic_bytes_decode(w, lens_all[:B])
@@ -371,6 +386,7 @@ def run_ours(args, world, rank, local):
 
     # End to end through the public API with pinned host buffers.
     E = min(K, 2000)
+    log("end-to-end loop")
     q_h = q.cpu().pin_memory()
     k_h, v_h, s_h = k_cur.cpu().pin_memory(), v_cur.cpu().pin_memory(), s_cur.cpu().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -403,8 +419,10 @@ def run_ours(args, world, rank, local):
     h2d = B * (Hq * D * 2 + 2 * H * D * 2 + 8)
     d2h = B * Hq * D * 4
 
+    log(f"e2e: {e2e_ms * 1e3:.2f} us/step")
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        log("cpu baseline (oracle)")
         cpu = cpu_baseline(w, cache, B, step_bytes)
 
     if rank == 0:

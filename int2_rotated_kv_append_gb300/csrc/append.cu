@@ -259,8 +259,7 @@ cudaError_t launch_append(int64_t T, const oscar_dims_t* d, const void* k, const
     return cudaGetLastError();
   }
   const size_t smem = (static_cast<size_t>(D) * D + kTokTile * D) * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(append_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(append_kernel<D>), smem);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>((T + kTokTile - 1) / kTokTile), d->num_kv_heads, 2);
   append_kernel<D><<<grid, kThreads, smem, stream>>>(

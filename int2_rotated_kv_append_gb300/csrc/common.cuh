@@ -6,6 +6,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "oscar.h"
 
 namespace oscar {
@@ -62,6 +66,21 @@ static inline int num_sms() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+// Sets a kernel's dynamic shared-memory limit once per (kernel, device), so
+// later launches (including ones recorded into a CUDA graph) only launch.
+static inline cudaError_t set_smem_limit_once(const void* func, size_t bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({func, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) done.insert({func, dev});
+  return e;
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }

@@ -21,8 +21,7 @@ using namespace oscar_dec;
 template <int D, Mode MODE>
 cudaError_t merge(const Params& p, cudaStream_t stream) {
   const size_t smem = MODE == kMixed ? static_cast<size_t>(D) * D * sizeof(float) : 0;
-  cudaError_t e = cudaFuncSetAttribute(merge_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(merge_kernel<D, MODE>), smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(merge_kernel<D, MODE>, dim3(p.B * p.Hq), dim3(kThreads), smem, stream, p);
 }
@@ -40,8 +39,7 @@ cudaError_t launch(const Params& p, cudaStream_t stream) {
     e = MODE == kMixed ? int2_mma_split(p, stream) : bf16_mma_split(p, stream);
   } else {
     constexpr size_t smem = split_body_smem(D);
-    e = cudaFuncSetAttribute(split_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    e = set_smem_limit_once(reinterpret_cast<const void*>(split_kernel<D, MODE>), smem);
     if (e == cudaSuccess) {
       if (MODE == kMixed) {
         e = launch_pdl(split_kernel<D, MODE>, dim3(p.ns, p.H, p.B), dim3(kThreads), smem, stream, p);

@@ -358,8 +358,7 @@ __global__ void __launch_bounds__(kWarps * 32) bf16_mma_split_kernel(Params p) {
 
 template <int NT>
 cudaError_t launch_impl(const Params& p, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(bf16_mma_split_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmem));
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(bf16_mma_split_kernel<NT>), kSmem);
   if (e != cudaSuccess) return e;
   bf16_mma_split_kernel<NT><<<dim3(p.ns, p.H, p.B), kWarps * 32, kSmem, stream>>>(p);
   return cudaGetLastError();

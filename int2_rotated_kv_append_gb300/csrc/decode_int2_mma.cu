@@ -528,8 +528,7 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
 template <int NT, int NG>
 cudaError_t launch_impl(const Params& p, cudaStream_t stream) {
   constexpr size_t smem = Geo<NG>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(int2_mma_split_kernel<NT, NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(int2_mma_split_kernel<NT, NG>), smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(int2_mma_split_kernel<NT, NG>, dim3(p.ns, p.H, p.B), dim3(kWarps * 32), smem, stream, p);
 }
