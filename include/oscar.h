@@ -148,6 +148,34 @@ oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, int32_t max
                             size_t workspace_bytes, void* stream);
 
 /*
+ * oscar_decode_noalloc -- oscar_decode without a caller workspace.
+ *
+ * The OSCAR pages have no counterpart for this call; it is a convenience of this
+ * library.  It exists for callers that cannot call cudaMalloc, for example a
+ * serving engine whose device memory is owned entirely by its own pool (an
+ * allocation behind the pool's back breaks its accounting), or a plugin
+ * interface that hands the kernel only its input and output buffers.
+ * Arguments and results are those of oscar_decode; the workspace is a static
+ * device array of OSCAR_NOALLOC_SCRATCH_BYTES inside the library, which every GPU
+ * that loads the library holds until the process exits.
+ *   - The first call on a device looks up that array's device address (a host
+ *     call made once per device, with that device current); make this first call
+ *     before any stream capture.
+ *   - A call whose plan (see oscar_decode_workspace_bytes) needs more than
+ *     OSCAR_NOALLOC_SCRATCH_BYTES returns OSCAR_ERR_WORKSPACE and launches nothing.
+ *   - Every call shares the one array and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero, but calls that overlap on the GPU
+ *     (several streams, or several host threads) race on it: serialise them.
+ *   - No memory is allocated, by this call or by anything it calls.
+ */
+#define OSCAR_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+oscar_status_t oscar_decode_noalloc(const oscar_dims_t* dims, int32_t batch, int32_t max_seq_len,
+                                    int32_t pages_per_split, const void* q, const float* R_k, const float* R_v,
+                                    const uint8_t* int2_pages, const void* scale_zero_pages, const void* bf16_sink,
+                                    const void* bf16_window, const int32_t* page_table, const int32_t* seq_lens,
+                                    int32_t sink_len, int32_t window_len, float sm_scale, float* out, void* stream);
+
+/*
  * oscar_bf16_append -- store K/V vectors unchanged into a BF16 paged pool (the
  * speedup reference's cache; the pages compare OSCAR against BF16 decoding,
  * summary "Practical Summary").

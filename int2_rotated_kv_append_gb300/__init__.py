@@ -53,6 +53,7 @@ def _load():
         "oscar_append": (I32, [D, I64, P, P, P, P, P, P, P, P, P, P, P]),
         "oscar_decode_workspace_bytes": (SZ, [D, I32, I32, I32, I32, I32]),
         "oscar_decode": (I32, [D, I32, I32, I32, P, P, P, P, P, P, P, P, P, I32, I32, F32, P, P, SZ, P]),
+        "oscar_decode_noalloc": (I32, [D, I32, I32, I32, P, P, P, P, P, P, P, P, P, I32, I32, F32, P, P]),
         "oscar_bf16_append": (I32, [D, I64, P, P, P, P, P]),
         "oscar_bf16_decode_workspace_bytes": (SZ, [D, I32, I32, I32]),
         "oscar_bf16_decode": (I32, [D, I32, I32, I32, P, P, P, P, F32, P, P, SZ, P]),
@@ -143,6 +144,22 @@ def oscar_decode(dims, batch, max_seq_len, pages_per_split, q, R_k, R_v, int2_pa
                             _ptr(bf16_window), _ptr(page_table), _ptr(seq_lens), int(sink_len), int(window_len),
                             float(sm_scale), _ptr(out), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream)), "oscar_decode")
+
+
+OSCAR_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def oscar_decode_noalloc(dims, batch, max_seq_len, pages_per_split, q, R_k, R_v, int2_pages, scale_zero_pages,
+                         bf16_sink, bf16_window, page_table, seq_lens, sink_len, window_len, sm_scale, out,
+                         stream=None):
+    """oscar_decode with the library's static device scratch instead of a caller
+    workspace (for callers that cannot allocate device memory; calls must not
+    overlap on the GPU)."""
+    _check(lib.oscar_decode_noalloc(ctypes.byref(_dims(dims)), int(batch), int(max_seq_len), int(pages_per_split),
+                                    _ptr(q), _ptr(R_k), _ptr(R_v), _ptr(int2_pages), _ptr(scale_zero_pages),
+                                    _ptr(bf16_sink), _ptr(bf16_window), _ptr(page_table), _ptr(seq_lens),
+                                    int(sink_len), int(window_len), float(sm_scale), _ptr(out), _stream(stream)),
+           "oscar_decode_noalloc")
 
 
 def oscar_bf16_append(dims, k, v, slot_mapping, bf16_pages, stream=None):

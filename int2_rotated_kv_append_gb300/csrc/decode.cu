@@ -11,6 +11,8 @@
 //   merge  one CTA per (sequence, query head): log-sum-exp merge of the splits,
 //          one un-rotation of the INT2 part by R_v^T, normalisation.
 // Logits are kept in log2 units (scale * log2 e folded into the query side).
+#include <mutex>
+
 #include "decode_common.cuh"
 
 namespace {
@@ -159,6 +161,56 @@ extern "C" oscar_status_t oscar_bf16_decode(const oscar_dims_t* dims, int32_t ba
   p.seq_lens = seq_lens;
   p.out = out;
   return run(p, kBf16Paged, stream);
+}
+
+// ---- decode without a caller workspace ----------------------------------------
+// Scratch of oscar_decode_noalloc: one file-scope device array, present on every
+// device that loads this library until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[OSCAR_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device.  The host-side name
+// is only a stand-in, so the address is looked up with cudaGetSymbolAddress once
+// per device (with that device current) and cached.
+static oscar_status_t noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* cached[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return OSCAR_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return OSCAR_ERR_CUDA;
+    cached[dev] = ptr;
+  }
+  *out = cached[dev];
+  return OSCAR_OK;
+}
+
+extern "C" oscar_status_t oscar_decode_noalloc(const oscar_dims_t* dims, int32_t batch, int32_t max_seq_len,
+                                               int32_t pages_per_split, const void* q, const float* R_k,
+                                               const float* R_v, const uint8_t* int2_pages,
+                                               const void* scale_zero_pages, const void* bf16_sink,
+                                               const void* bf16_window, const int32_t* page_table,
+                                               const int32_t* seq_lens, int32_t sink_len, int32_t window_len,
+                                               float sm_scale, float* out, void* stream) {
+  // Size check first, so an oversized request fails before any CUDA call.
+  if (check_dims(dims) == OSCAR_OK && batch > 0 && max_seq_len >= 0 && pages_per_split >= 0 && sink_len >= 0 &&
+      window_len >= 0) {
+    Plan plan;
+    if (make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, &plan) &&
+        plan.total > OSCAR_NOALLOC_SCRATCH_BYTES)
+      return OSCAR_ERR_WORKSPACE;
+  }
+  void* ws = nullptr;
+  if (batch > 0) {
+    const oscar_status_t st = noalloc_scratch(&ws);
+    if (st != OSCAR_OK) return st;
+  }
+  // The workspace of oscar_decode needs no initialisation: every byte it reads
+  // was written earlier in the same call.
+  return oscar_decode(dims, batch, max_seq_len, pages_per_split, q, R_k, R_v, int2_pages, scale_zero_pages,
+                      bf16_sink, bf16_window, page_table, seq_lens, sink_len, window_len, sm_scale, out, ws,
+                      OSCAR_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 oscar_status_t oscar_internal_decode_errors(uint32_t* flags, int reset) {
