@@ -51,6 +51,8 @@ static inline oscar_status_t check_dims(const oscar_dims_t* d) {
   return OSCAR_OK;
 }
 
+static inline bool misaligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
 static inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -22,8 +22,8 @@ using namespace oscar_dec;
 
 template <int D, Mode MODE>
 cudaError_t merge(const Params& p, cudaStream_t stream) {
-  const size_t smem = MODE == kMixed ? static_cast<size_t>(D) * D * sizeof(float) : 0;
-  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(merge_kernel<D, MODE>), smem);
+  const size_t smem = merge_smem(D, p.ns, MODE == kMixed, p.merge_stage != 0);
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(merge_kernel<D, MODE>), kMergeSmemLimit);
   if (e != cudaSuccess) return e;
   return launch_pdl(merge_kernel<D, MODE>, dim3(p.B * p.Hq), dim3(kThreads), smem, stream, p);
 }
@@ -31,8 +31,11 @@ cudaError_t merge(const Params& p, cudaStream_t stream) {
 template <int D, Mode MODE>
 cudaError_t launch(const Params& p, cudaStream_t stream) {
   if (MODE == kMixed) {
-    qrot_kernel<<<p.B * p.Hq, 128, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    constexpr size_t qsmem = qrot_smem(D);
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(qrot_kernel<D>), qsmem);
+    if (e != cudaSuccess) return e;
+    qrot_kernel<D><<<p.B * p.H, kThreads, qsmem, stream>>>(p);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   const bool mma = MODE == kMixed ? int2_mma_supported(p) : bf16_mma_supported(p);
@@ -77,6 +80,7 @@ Params base_params(const oscar_dims_t* d, int B, int max_seq_len, const Plan& pl
   p.n_paged = plan.n_paged;
   p.n_dense = plan.n_dense;
   p.ns = plan.ns;
+  p.merge_stage = static_cast<size_t>(plan.ns) * d->head_dim * 4 <= kMergeStageMax ? 1 : 0;
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(d->head_dim));
   p.scale_log2 = scale * 1.4426950408889634f;
   char* w = static_cast<char*>(ws);
@@ -112,10 +116,13 @@ extern "C" oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, 
     return OSCAR_ERR_INVALID_ARG;
   if ((sink_len > 0 && !bf16_sink) || (window_len > 0 && !bf16_window)) return OSCAR_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return OSCAR_ERR_INVALID_ARG;
+  if (misaligned16(R_k) || misaligned16(R_v) || misaligned16(int2_pages) || misaligned16(scale_zero_pages))
+    return OSCAR_ERR_INVALID_ARG;
   Plan plan;
   if (!make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, &plan))
     return OSCAR_ERR_INVALID_ARG;
   if (workspace_bytes < plan.total) return OSCAR_ERR_WORKSPACE;
+  if (merge_smem(dims->head_dim, plan.ns, true, false) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
   if (static_cast<long long>(batch) * dims->num_q_heads > 0x7fffffffLL || plan.ns > 0x7fffffff) return OSCAR_ERR_UNSUPPORTED;
   Params p = base_params(dims, batch, max_seq_len, plan, sm_scale, workspace);
   p.S = sink_len;
@@ -151,9 +158,11 @@ extern "C" oscar_status_t oscar_bf16_decode(const oscar_dims_t* dims, int32_t ba
   if (batch == 0) return OSCAR_OK;
   if (!q || !bf16_pages || !page_table || !seq_lens || !out || !workspace) return OSCAR_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return OSCAR_ERR_INVALID_ARG;
+  if (misaligned16(bf16_pages)) return OSCAR_ERR_INVALID_ARG;
   Plan plan;
   if (!make_plan(dims, batch, max_seq_len, pages_per_split, 0, 0, kBf16Paged, &plan)) return OSCAR_ERR_INVALID_ARG;
   if (workspace_bytes < plan.total) return OSCAR_ERR_WORKSPACE;
+  if (merge_smem(dims->head_dim, plan.ns, false, false) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
   Params p = base_params(dims, batch, max_seq_len, plan, sm_scale, workspace);
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.pages = static_cast<const __nv_bfloat16*>(bf16_pages);

@@ -7,6 +7,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace oscar_dec {
 
@@ -15,6 +16,8 @@ using namespace oscar;
 constexpr int kThreads = 128;
 constexpr int kTile = 32;        // positions per softmax tile (one per lane)
 constexpr int kBf16Chunk = 64;   // sink/window positions per split
+constexpr size_t kMergeStageMax = 96 * 1024;    // partials staged in the merge's shared memory up to this size
+constexpr size_t kMergeSmemLimit = 200 * 1024;  // dynamic shared-memory limit set for the merge kernel
 
 enum Mode { kMixed = 0, kBf16Paged = 1 };
 
@@ -30,6 +33,7 @@ struct Params {
   int B, Hq, H, D, G, gqa, num_pages, max_pages, max_seq_len;
   int S, W, pps, n_paged, n_dense, ns;
   float scale_log2;
+  int merge_stage;  // 1: the merge kernel stages the split partials in shared memory
   const __nv_bfloat16* q;
   const float* R_k;
   const float* R_v;
@@ -119,21 +123,47 @@ __device__ __forceinline__ int clamp_len(const Params& p, int b) {
   return L;
 }
 
-// q_rot[b][hq] = q[b][hq] . R_k[hq / gqa]; one CTA per (b, hq), one thread per column.
-__global__ void qrot_kernel(Params p) {
+// q_rot[b][hq] = q[b][hq] . R_k[h] for the GQA query heads hq of one (b, h):
+// R_k[h] arrives in shared memory by one bulk copy and thread j computes column
+// j for every query head.  Dynamic shared memory: qrot_smem(D) bytes.
+constexpr size_t qrot_smem(int D) { return static_cast<size_t>(D) * D * 4 + static_cast<size_t>(kMaxGqa) * D * 4 + 16; }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) qrot_kernel(Params p) {
+  extern __shared__ __align__(128) float qsm[];
+  float* Rs = qsm;                 // [D][D]
+  float* qs = Rs + D * D;          // [gqa][D]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(qs + kMaxGqa * D);
   grid_dep_launch_dependents();
-  __shared__ float qs[128];
-  const int bh = blockIdx.x;
-  const int h = (bh % p.Hq) / p.gqa;
-  const int j = threadIdx.x;
-  if (j < p.D) qs[j] = __bfloat162float(p.q[static_cast<size_t>(bh) * p.D + j]);
+  const int b = blockIdx.x / p.H, h = blockIdx.x % p.H;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_init(smem_u32(bar), 1);
+    mbar_init_fence();
+    mbar_arrive_expect_tx(smem_u32(bar), D * D * 4);
+    bulk_g2s(smem_u32(Rs), p.R_k + static_cast<size_t>(h) * D * D, D * D * 4, smem_u32(bar));
+  }
+  const size_t q0 = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * p.gqa) * D;
+  for (int i = tid; i < p.gqa * D; i += kThreads) qs[i] = __bfloat162float(p.q[q0 + i]);
   __syncthreads();
-  if (j >= p.D) return;
-  const float* R = p.R_k + static_cast<size_t>(h) * p.D * p.D;
-  float acc = 0.f;
-#pragma unroll 8
-  for (int i = 0; i < p.D; ++i) acc = fmaf(qs[i], __ldg(R + static_cast<size_t>(i) * p.D + j), acc);
-  p.q_rot[static_cast<size_t>(bh) * p.D + j] = acc;
+  if (!mbar_wait_bounded(smem_u32(bar), 0)) {
+    if (tid == 0) record_error(OSCAR_DEVERR_TIMEOUT);
+    mbar_wait_bounded(smem_u32(bar), 0);  // give a late copy one more bounded chance to land
+  }
+  if (tid >= D) return;
+  float acc[kMaxGqa];
+#pragma unroll
+  for (int qi = 0; qi < kMaxGqa; ++qi) acc[qi] = 0.f;
+#pragma unroll 4
+  for (int i = 0; i < D; ++i) {
+    const float r = Rs[i * D + tid];
+#pragma unroll
+    for (int qi = 0; qi < kMaxGqa; ++qi)
+      if (qi < p.gqa) acc[qi] = fmaf(qs[qi * D + i], r, acc[qi]);
+  }
+#pragma unroll
+  for (int qi = 0; qi < kMaxGqa; ++qi)
+    if (qi < p.gqa) p.q_rot[q0 + static_cast<size_t>(qi) * D + tid] = acc[qi];
 }
 
 // Shared memory (bytes) of split_body for head dimension D.
@@ -334,51 +364,94 @@ __global__ void __launch_bounds__(kThreads) split_kernel(Params p) {
 }
 
 // Log-sum-exp merge of the splits of one (b, hq), un-rotation of the INT2 part
-// by R_v^T and normalisation.
+// by R_v^T and normalisation.  R_v[h] (mixed mode) is staged by a bulk copy
+// before the wait for the split kernel, the partials by a second bulk copy
+// after it (when they fit, merge_stage).  Dynamic shared memory:
+// merge_smem(D, ns, mixed, stage) bytes.
+constexpr size_t merge_smem(int D, int ns, bool mixed, bool stage) {
+  return (mixed ? static_cast<size_t>(D) * D * 4 : 0) + (stage ? static_cast<size_t>(ns) * D * 4 : 0) +
+         static_cast<size_t>(ns + 2) * 4 + 32;
+}
+
 template <int D, Mode MODE>
 __global__ void __launch_bounds__(kThreads) merge_kernel(Params p) {
   __shared__ float o_rot[D];
   __shared__ float o_plain[D];
-  extern __shared__ __align__(16) float Rs[];  // R_v[h] (mixed mode), staged before the wait
+  __shared__ float red[kThreads / 32];
+  extern __shared__ __align__(128) float msm[];
+  constexpr bool kRot = MODE == kMixed;
+  const int ns = p.ns;
+  float* Rs = msm;                                      // [D][D] (mixed)
+  float* po_s = Rs + (kRot ? D * D : 0);                // [ns][D] (staged)
+  float* wts = po_s + (p.merge_stage ? ns * D : 0);     // [ns]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uintptr_t>(wts + ns + 2 + 1) & ~uintptr_t(7));
   const int bh = blockIdx.x;
   const int h = (bh % p.Hq) / p.gqa;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  if (MODE == kMixed) {
-    const float4* src = reinterpret_cast<const float4*>(p.R_v + static_cast<size_t>(h) * D * D);
-    for (int i = tid; i < D * D / 4; i += kThreads) reinterpret_cast<float4*>(Rs)[i] = __ldg(src + i);
-  }
-  grid_dep_wait();  // the split partials come from the preceding kernel
-  const float* ml = p.part_ml + static_cast<size_t>(bh) * p.ns * 2;
-  const float* po = p.part_o + static_cast<size_t>(bh) * p.ns * D;
-  float M = -INFINITY;
-  for (int s = 0; s < p.ns; ++s) M = fmaxf(M, ml[2 * s]);
-  float denom = 0.f;
-  if (tid < D) {
-    float a_rot = 0.f, a_plain = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < p.ns; ++s) {
-        const float m = ml[2 * s];
-        if (m == -INFINITY) continue;
-        const float w = exp2f(m - M);
-        const float o = po[static_cast<size_t>(s) * D + tid];
-        if (MODE == kMixed && s < p.n_paged) a_rot = fmaf(w, o, a_rot);
-        else a_plain = fmaf(w, o, a_plain);
-      }
-    }
-    o_rot[tid] = a_rot;
-    o_plain[tid] = a_plain;
-  }
-  if (M != -INFINITY) {
-    for (int s = 0; s < p.ns; ++s) {
-      const float m = ml[2 * s];
-      if (m != -INFINITY) denom = fmaf(exp2f(m - M), ml[2 * s + 1], denom);
+  if (tid == 0) {
+    mbar_init(smem_u32(&bars[0]), 1);
+    mbar_init(smem_u32(&bars[1]), 1);
+    mbar_init_fence();
+    if (kRot) {
+      mbar_arrive_expect_tx(smem_u32(&bars[0]), D * D * 4);
+      bulk_g2s(smem_u32(Rs), p.R_v + static_cast<size_t>(h) * D * D, D * D * 4, smem_u32(&bars[0]));
     }
   }
   __syncthreads();
-  const float inv = denom > 0.f ? 1.f / denom : 0.f;
+  grid_dep_wait();  // the split partials come from the preceding kernel
+  const float* ml = p.part_ml + static_cast<size_t>(bh) * ns * 2;
+  const float* po = p.part_o + static_cast<size_t>(bh) * ns * D;
+  if (tid == 0 && p.merge_stage) {
+    mbar_arrive_expect_tx(smem_u32(&bars[1]), ns * D * 4);
+    bulk_g2s(smem_u32(po_s), po, ns * D * 4, smem_u32(&bars[1]));
+  }
+  // M = max_s m_s, weights w_s = 2^(m_s - M), denominator sum_s w_s l_s.
+  float M = -INFINITY;
+  for (int s = tid; s < ns; s += kThreads) M = fmaxf(M, ml[2 * s]);
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = red[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
+  float den = 0.f;
+  for (int s = tid; s < ns; s += kThreads) {
+    const float m = ml[2 * s];
+    const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(m - M);
+    wts[s] = w;
+    den = fmaf(w, ml[2 * s + 1], den);
+  }
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  if (lane == 0) red[warp] = den;
+  __syncthreads();
+  den = 0.f;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) den += red[w];
+  bool ok = true;
+  if (p.merge_stage) ok = mbar_wait_bounded(smem_u32(&bars[1]), 0);
+  if (!ok && tid == 0) record_error(OSCAR_DEVERR_TIMEOUT);
+  const float* src = p.merge_stage ? po_s : po;
+  if (tid < D) {
+    float a_rot = 0.f, a_plain = 0.f;
+    const int n_rot = kRot ? p.n_paged : 0;
+#pragma unroll 4
+    for (int s = 0; s < n_rot; ++s) a_rot = fmaf(wts[s], src[static_cast<size_t>(s) * D + tid], a_rot);
+#pragma unroll 4
+    for (int s = n_rot; s < ns; ++s) a_plain = fmaf(wts[s], src[static_cast<size_t>(s) * D + tid], a_plain);
+    o_rot[tid] = a_rot;
+    o_plain[tid] = a_plain;
+  }
+  __syncthreads();
+  const float inv = (ok && den > 0.f) ? 1.f / den : 0.f;
   float* out = p.out + static_cast<size_t>(bh) * D;
-  if (MODE == kBf16Paged) {
+  if (!kRot) {
     if (tid < D) out[tid] = o_plain[tid] * inv;
+    return;
+  }
+  if (!mbar_wait_bounded(smem_u32(&bars[0]), 0)) {
+    if (tid == 0) record_error(OSCAR_DEVERR_TIMEOUT);
+    if (tid < D) out[tid] = 0.f;
     return;
   }
   // out[c] = (o_plain[c] + sum_j o_rot[j] R_v[h][c][j]) * inv, one warp per row c.

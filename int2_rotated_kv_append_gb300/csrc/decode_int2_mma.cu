@@ -37,65 +37,17 @@ constexpr int kWarps = 4;
 constexpr int kStages = 6;               // pages in flight per warp
 constexpr int kCodeBytes = 2 * 16 * 32;  // K then V codes of one (page, KV head)
 constexpr int kMaxPps = 256;             // page ids of one split staged in shared memory
-constexpr long long kWaitCycles = 2000000000LL;  // bounded wait on an async copy (about 1 s)
 
 template <int NG>
 struct Geo {
   static constexpr int kSzBytes = 2 * 16 * NG * 2 * 2;  // K then V fp16 (scale, zero) of 16 tokens
   static constexpr int kStageBytes = kCodeBytes + kSzBytes;
-  static constexpr size_t kPagedSmem =
-      static_cast<size_t>(kWarps) * kStages * kStageBytes + kWarps * kStages * 8 + kMaxPps * 4;
+  // stages | q_rot rows of the CTA's query heads | mbarriers (stages + q) | page ids
+  static constexpr size_t kPagedSmem = static_cast<size_t>(kWarps) * kStages * kStageBytes +
+                                       static_cast<size_t>(kMaxGqa) * kD * 4 + (kWarps * kStages + 1) * 8 +
+                                       kMaxPps * 4;
   static constexpr size_t kSmem = kPagedSmem > split_body_smem(kD) ? kPagedSmem : split_body_smem(kD);
 };
-
-// ---- PTX helpers -------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_init_fence() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Waits for the phase with the given parity; gives up after kWaitCycles.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long start = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - start > kWaitCycles) return false;
-  }
-  return true;
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -104,15 +56,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// 2^k as a float for -126 <= k <= 127 (exact).
-__device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
 
 // Bit position, inside its fp16 half, of channel e (0..15) of a packed word
 // after the extraction below: e%8 <= 4 sit at 2*(e%8) of the raw word's half,
@@ -166,8 +109,10 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
   const int npg = (r1 - 1) / kPageSize + 1 - pg0;
 
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kStageBytes);
-  int* pid_s = reinterpret_cast<int*>(bars + kWarps * kStages);
+  float* qbuf = reinterpret_cast<float*>(smem + kWarps * kStages * kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qbuf + kMaxGqa * kD);
+  uint64_t* qbar = bars + kWarps * kStages;
+  int* pid_s = reinterpret_cast<int*>(qbar + 1);
   for (int i = tid; i < npg; i += kWarps * 32) {
     int pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg0 + i);
     if (pid < 0 || pid >= p.num_pages) {
@@ -178,6 +123,7 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
   }
   if (lane == 0)
     for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp * kStages + i]), 1);
+  if (tid == 0) mbar_init(smem_u32(qbar), 1);
   mbar_init_fence();
   __syncthreads();
 
@@ -201,11 +147,16 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
     for (int i = 0; i < n_my && i < kStages; ++i) issue(i);
   grid_dep_launch_dependents();
   grid_dep_wait();  // q_rot comes from the preceding kernel; the page copies above do not need it
+  if (tid == 0) {
+    mbar_arrive_expect_tx(smem_u32(qbar), gqa * kD * 4);
+    bulk_g2s(smem_u32(qbuf), p.q_rot + bh0 * kD, gqa * kD * 4, smem_u32(qbar));
+  }
+  bool aborted = __any_sync(0xffffffffu, !mbar_wait_bounded(smem_u32(qbar), 0));
 
   // ---- query side (overlaps the first copies) ----
   // Per n-tile nt this thread's C columns belong to query 4*nt + t and its B
   // column to query 4*nt + (g >> 1), part g & 1 (0 = hi, 1 = lo).
-  const float* qr = p.q_rot + bh0 * kD;
+  const float* qr = qbuf;
   float F[NT], qs[NT][NG];
   int Eb[NT];
 #pragma unroll
@@ -259,7 +210,7 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float x = 0.f;
-        if (use) x = __ldg(qr + qb * kD + chs[c]) * p.scale_log2 * pow2i(Eb[nt] - kpos(chs[c] & 15));
+        if (use) x = qr[qb * kD + chs[c]] * p.scale_log2 * pow2i(Eb[nt] - kpos(chs[c] & 15));
         const __half hi = __float2half_rn(x);
         hv[c] = lo_part ? __float2half_rn(x - __half2float(hi)) : hi;
       }
@@ -288,9 +239,8 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
   int sig = 0;
   const uint32_t vsel = (2 * (g & 1)) | ((2 * (g & 1) + 1) << 4) | ((4 + 2 * (g & 1)) << 8) | ((5 + 2 * (g & 1)) << 12);
   const int src1 = 4 * t + (g >> 1), src2 = src1 + 16;
-  bool aborted = false;
   int i = 0;
-  for (; i < n_my; ++i) {
+  for (; i < n_my && !aborted; ++i) {
     const uint32_t bar = smem_u32(&my_bars[i % kStages]);
     const bool ok = mbar_wait_bounded(bar, (i / kStages) & 1);
     if (__any_sync(0xffffffffu, !ok)) {
