@@ -34,7 +34,7 @@ cudaError_t launch(const Params& p, cudaStream_t stream) {
     constexpr size_t qsmem = qrot_smem(D);
     cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(qrot_kernel<D>), qsmem);
     if (e != cudaSuccess) return e;
-    qrot_kernel<D><<<p.B * p.H, kThreads, qsmem, stream>>>(p);
+    qrot_kernel<D><<<p.B * p.H, kQrotThreads, qsmem, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -15,7 +15,7 @@ using namespace oscar;
 
 constexpr int kThreads = 128;
 constexpr int kTile = 32;        // positions per softmax tile (one per lane)
-constexpr int kBf16Chunk = 64;   // sink/window positions per split
+constexpr int kBf16Chunk = 32;   // sink/window positions per split (one softmax tile)
 constexpr size_t kMergeStageMax = 96 * 1024;    // partials staged in the merge's shared memory up to this size
 constexpr size_t kMergeSmemLimit = 200 * 1024;  // dynamic shared-memory limit set for the merge kernel
 
@@ -128,8 +128,10 @@ __device__ __forceinline__ int clamp_len(const Params& p, int b) {
 // j for every query head.  Dynamic shared memory: qrot_smem(D) bytes.
 constexpr size_t qrot_smem(int D) { return static_cast<size_t>(D) * D * 4 + static_cast<size_t>(kMaxGqa) * D * 4 + 16; }
 
+constexpr int kQrotThreads = 512;  // 4 groups of 128 threads, each summing a quarter of the rows
+
 template <int D>
-__global__ void __launch_bounds__(kThreads) qrot_kernel(Params p) {
+__global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
   extern __shared__ __align__(128) float qsm[];
   float* Rs = qsm;                 // [D][D]
   float* qs = Rs + D * D;          // [gqa][D]
@@ -144,26 +146,44 @@ __global__ void __launch_bounds__(kThreads) qrot_kernel(Params p) {
     bulk_g2s(smem_u32(Rs), p.R_k + static_cast<size_t>(h) * D * D, D * D * 4, smem_u32(bar));
   }
   const size_t q0 = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * p.gqa) * D;
-  for (int i = tid; i < p.gqa * D; i += kThreads) qs[i] = __bfloat162float(p.q[q0 + i]);
+  for (int i = tid; i < p.gqa * D; i += kQrotThreads) qs[i] = __bfloat162float(p.q[q0 + i]);
   __syncthreads();
   if (!mbar_wait_bounded(smem_u32(bar), 0)) {
     if (tid == 0) record_error(OSCAR_DEVERR_TIMEOUT);
     mbar_wait_bounded(smem_u32(bar), 0);  // give a late copy one more bounded chance to land
   }
-  if (tid >= D) return;
+  // Thread (quarter qt, column j) sums rows [qt*D/4, (qt+1)*D/4); the quarters are
+  // then added in order through shared memory (the R_k area is no longer needed).
+  const int j = tid % D, qt = tid / D;
+  constexpr int kGroups = kQrotThreads / D;
   float acc[kMaxGqa];
 #pragma unroll
   for (int qi = 0; qi < kMaxGqa; ++qi) acc[qi] = 0.f;
+  if (qt < kGroups) {
+    const int i0 = qt * (D / kGroups);
 #pragma unroll 4
-  for (int i = 0; i < D; ++i) {
-    const float r = Rs[i * D + tid];
+    for (int i = i0; i < i0 + D / kGroups; ++i) {
+      const float r = Rs[i * D + j];
+#pragma unroll
+      for (int qi = 0; qi < kMaxGqa; ++qi)
+        if (qi < p.gqa) acc[qi] = fmaf(qs[qi * D + i], r, acc[qi]);
+    }
+  }
+  __syncthreads();
+  float* part = Rs;  // [kGroups][kMaxGqa][D]
+  if (qt < kGroups) {
 #pragma unroll
     for (int qi = 0; qi < kMaxGqa; ++qi)
-      if (qi < p.gqa) acc[qi] = fmaf(qs[qi * D + i], r, acc[qi]);
+      if (qi < p.gqa) part[(qt * kMaxGqa + qi) * D + j] = acc[qi];
   }
+  __syncthreads();
+  for (int idx = tid; idx < p.gqa * D; idx += kQrotThreads) {
+    const int qi = idx / D, jj = idx % D;
+    float tot = 0.f;
 #pragma unroll
-  for (int qi = 0; qi < kMaxGqa; ++qi)
-    if (qi < p.gqa) p.q_rot[q0 + static_cast<size_t>(qi) * D + tid] = acc[qi];
+    for (int g = 0; g < kGroups; ++g) tot += part[(g * kMaxGqa + qi) * D + jj];
+    p.q_rot[q0 + idx] = tot;
+  }
 }
 
 // Shared memory (bytes) of split_body for head dimension D.
@@ -251,41 +271,64 @@ __device__ __forceinline__ void split_body(const Params& p, int s, int h, int b,
       pos_s[tid] = pos;
     }
     __syncthreads();
-    // Load (and dequantise) K and V of the tile into shared memory, 16 channels per item.
-    for (int w = tid; w < 2 * kTile * (D / 16); w += kThreads) {
+    // Load (and dequantise) K and V of the tile into shared memory, 16 channels per
+    // item: all global loads of the thread are issued first, then converted.
+    constexpr int kItems = 2 * kTile * (D / 16);
+    constexpr int kPer = (kItems + kThreads - 1) / kThreads;
+    uint4 raw[kPer][2];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int w = tid + k * kThreads;
+      raw[k][0] = make_uint4(0u, 0u, 0u, 0u);
+      raw[k][1] = make_uint4(0u, 0u, 0u, 0u);
+      if (w >= kItems) continue;
+      const int kvsel = w / (kTile * (D / 16));
+      const int rem = w % (kTile * (D / 16));
+      const int tt = rem / (D / 16), word = rem % (D / 16);
+      const int pos = pos_s[tt];
+      if (pos < 0) continue;
+      if (MODE == kMixed && paged) {
+        const size_t row = ((static_cast<size_t>(page_s[tt]) * p.H + h) * 2 + kvsel) * kPageSize + pos % kPageSize;
+        const int g = word * 16 / p.G;
+        raw[k][0].x = __ldg(reinterpret_cast<const uint32_t*>(p.codes + row * (D / 4)) + word);
+        raw[k][0].y = __ldg(reinterpret_cast<const unsigned int*>(p.sz + row * (D / p.G) * 2) + g);
+      } else {
+        const __nv_bfloat16* src;
+        if (MODE == kBf16Paged) {
+          src = p.pages + (((static_cast<size_t>(page_s[tt]) * p.H + h) * 2 + kvsel) * kPageSize + pos % kPageSize) * D;
+        } else if (pos < sink_end) {
+          src = p.sink + (((static_cast<size_t>(b) * 2 + kvsel) * p.H + h) * p.S + pos) * D;
+        } else {
+          src = p.win + (((static_cast<size_t>(b) * 2 + kvsel) * p.H + h) * p.W + pos % p.W) * D;
+        }
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + word * 16);
+        raw[k][0] = __ldg(s4);
+        raw[k][1] = __ldg(s4 + 1);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int w = tid + k * kThreads;
+      if (w >= kItems) continue;
       const int kvsel = w / (kTile * (D / 16));
       const int rem = w % (kTile * (D / 16));
       const int tt = rem / (D / 16), word = rem % (D / 16);
       float vals[16];
+      if (MODE == kMixed && paged) {
+        const uint32_t bits = raw[k][0].x;
+        const uint32_t szb = raw[k][0].y;
+        const float sc = __half2float(__ushort_as_half(static_cast<unsigned short>(szb & 0xffffu)));
+        const float ze = __half2float(__ushort_as_half(static_cast<unsigned short>(szb >> 16)));
+        const bool ok = pos_s[tt] >= 0;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) vals[i] = 0.f;
-      const int pos = pos_s[tt];
-      if (pos >= 0) {
-        if (MODE == kMixed && paged) {
-          const size_t row = ((static_cast<size_t>(page_s[tt]) * p.H + h) * 2 + kvsel) * kPageSize + pos % kPageSize;
-          const uint32_t bits = reinterpret_cast<const uint32_t*>(p.codes + row * (D / 4))[word];
-          const int g = word * 16 / p.G;
-          const __half2 szv = reinterpret_cast<const __half2*>(p.sz + row * (D / p.G) * 2)[g];
-          const float sc = __low2float(szv), ze = __high2float(szv);
+        for (int i = 0; i < 16; ++i) vals[i] = ok ? fmaf(static_cast<float>((bits >> (2 * i)) & 3u), sc, ze) : 0.f;
+      } else {
+        const uint32_t wds[8] = {raw[k][0].x, raw[k][0].y, raw[k][0].z, raw[k][0].w,
+                                 raw[k][1].x, raw[k][1].y, raw[k][1].z, raw[k][1].w};
 #pragma unroll
-          for (int i = 0; i < 16; ++i) vals[i] = fmaf(static_cast<float>((bits >> (2 * i)) & 3u), sc, ze);
-        } else {
-          const __nv_bfloat16* src;
-          if (MODE == kBf16Paged) {
-            src = p.pages + (((static_cast<size_t>(page_s[tt]) * p.H + h) * 2 + kvsel) * kPageSize + pos % kPageSize) * D;
-          } else if (pos < sink_end) {
-            src = p.sink + (((static_cast<size_t>(b) * 2 + kvsel) * p.H + h) * p.S + pos) * D;
-          } else {
-            src = p.win + (((static_cast<size_t>(b) * 2 + kvsel) * p.H + h) * p.W + pos % p.W) * D;
-          }
-          const uint4* s4 = reinterpret_cast<const uint4*>(src + word * 16);
-          const uint4 a = __ldg(s4), c = __ldg(s4 + 1);
-          const uint32_t wds[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            vals[2 * i] = bf16_bits_to_float(wds[i] & 0xffffu);
-            vals[2 * i + 1] = bf16_bits_to_float(wds[i] >> 16);
-          }
+        for (int i = 0; i < 8; ++i) {
+          vals[2 * i] = bf16_bits_to_float(wds[i] & 0xffffu);
+          vals[2 * i + 1] = bf16_bits_to_float(wds[i] >> 16);
         }
       }
       float* dst = (kvsel ? vt : kt) + tt * DP + word * 16;
@@ -454,14 +497,18 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(Params p) {
     if (tid < D) out[tid] = 0.f;
     return;
   }
-  // out[c] = (o_plain[c] + sum_j o_rot[j] R_v[h][c][j]) * inv, one warp per row c.
-  constexpr int CPL = D / 32;
-  for (int c = warp; c < D; c += kThreads / 32) {
+  // out[c] = (o_plain[c] + sum_j o_rot[j] R_v[h][c][j]) * inv, thread c.  Thread c
+  // visits j in the order (c + k) mod D, so at every step the 32 lanes of a warp
+  // read 32 different banks of R_v's row-major rows and of o_rot.
+  if (tid < D) {
+    const int c = tid;
     float part = 0.f;
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) part = fmaf(o_rot[lane * CPL + i], Rs[c * D + lane * CPL + i], part);
-    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if (lane == 0) out[c] = (o_plain[c] + part) * inv;
+#pragma unroll 8
+    for (int k = 0; k < D; ++k) {
+      const int j = (c + k) & (D - 1);
+      part = fmaf(o_rot[j], Rs[c * D + j], part);
+    }
+    out[c] = (o_plain[c] + part) * inv;
   }
 }
 
