@@ -266,9 +266,9 @@ def run_ours(args, world, rank, local):
     log(f"generating workload: config {args.config}, {NR} replicas")
     w = synth.make_config(args.config, device=dev, replicas=NR)
     log("building INT2 and BF16 caches")
-    cache = Int2Cache(w, device=dev)
+    cache = Int2Cache(w, device=dev, pages_per_split=None if args.pps < 0 else args.pps)
     cache.prefill()
-    bf = Bf16Cache(w, device=dev)
+    bf = Bf16Cache(w, device=dev, pages_per_split=None if args.pps < 0 else args.pps)
     bf.prefill()
     torch.cuda.synchronize()
 
@@ -308,7 +308,7 @@ def run_ours(args, world, rank, local):
 
     def bf16_r(r):
         x = V[r]
-        ok.oscar_bf16_decode(w.dims, B, msl_r[r], 0, x["q"], bf.pages, x["bpt"], x["blens"], 0.0, x["out_bf"],
+        ok.oscar_bf16_decode(w.dims, B, msl_r[r], bf.pps, x["q"], bf.pages, x["bpt"], x["blens"], 0.0, x["out_bf"],
                              ws_bf)
 
     def step(i):
@@ -510,6 +510,7 @@ def main():
     ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3],
                     help="workload: 1 batch-1 32K (default), 2 batch-64 mixed lengths, 3 batch-4 131K")
     ap.add_argument("--replicas", type=int, default=0, help="cache replicas (0: enough to exceed 3x L2)")
+    ap.add_argument("--pps", type=int, default=-1, help="pages per split for both decodes (-1: the workload's, 0: auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -65,6 +65,16 @@ oscar_status_t run(Params p, Mode mode, void* stream) {
   return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
+// Resident CTAs per SM of the split kernel a shape will use (for split sizing).
+int split_ctas_per_sm(const oscar_dims_t* d, Mode mode) {
+  const int gqa = d->num_q_heads / d->num_kv_heads;
+  if (d->head_dim == 128) {
+    if (mode == kBf16Paged) return bf16_mma_ctas_per_sm(gqa);
+    if (d->group_size == 64 || d->group_size == 128) return int2_mma_ctas_per_sm(gqa, d->group_size);
+  }
+  return 4;
+}
+
 Params base_params(const oscar_dims_t* d, int B, int max_seq_len, const Plan& plan, float sm_scale, void* ws) {
   Params p{};
   p.B = B;
@@ -85,6 +95,7 @@ Params base_params(const oscar_dims_t* d, int B, int max_seq_len, const Plan& pl
   p.scale_log2 = scale * 1.4426950408889634f;
   char* w = static_cast<char*>(ws);
   p.q_rot = reinterpret_cast<float*>(w + plan.off_qrot);
+  p.qfrag = reinterpret_cast<uint32_t*>(w + plan.off_qfrag);
   p.part_o = reinterpret_cast<float*>(w + plan.off_po);
   p.part_ml = reinterpret_cast<float*>(w + plan.off_pml);
   return p;
@@ -96,7 +107,7 @@ extern "C" size_t oscar_decode_workspace_bytes(const oscar_dims_t* dims, int32_t
                                                int32_t pages_per_split, int32_t sink_len, int32_t window_len) {
   if (check_dims(dims) != OSCAR_OK) return 0;
   Plan plan;
-  if (!make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, &plan)) return 0;
+  if (!make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, split_ctas_per_sm(dims, kMixed), &plan)) return 0;
   return plan.total;
 }
 
@@ -119,7 +130,7 @@ extern "C" oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, 
   if (misaligned16(R_k) || misaligned16(R_v) || misaligned16(int2_pages) || misaligned16(scale_zero_pages))
     return OSCAR_ERR_INVALID_ARG;
   Plan plan;
-  if (!make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, &plan))
+  if (!make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, split_ctas_per_sm(dims, kMixed), &plan))
     return OSCAR_ERR_INVALID_ARG;
   if (workspace_bytes < plan.total) return OSCAR_ERR_WORKSPACE;
   if (merge_smem(dims->head_dim, plan.ns, true, false) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
@@ -137,6 +148,7 @@ extern "C" oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, 
   p.page_table = page_table;
   p.seq_lens = seq_lens;
   p.out = out;
+  if (!int2_mma_supported(p)) p.qfrag = nullptr;
   return run(p, kMixed, stream);
 }
 
@@ -144,7 +156,7 @@ extern "C" size_t oscar_bf16_decode_workspace_bytes(const oscar_dims_t* dims, in
                                                     int32_t pages_per_split) {
   if (check_dims(dims) != OSCAR_OK) return 0;
   Plan plan;
-  if (!make_plan(dims, batch, max_seq_len, pages_per_split, 0, 0, kBf16Paged, &plan)) return 0;
+  if (!make_plan(dims, batch, max_seq_len, pages_per_split, 0, 0, kBf16Paged, split_ctas_per_sm(dims, kBf16Paged), &plan)) return 0;
   return plan.total;
 }
 
@@ -160,7 +172,7 @@ extern "C" oscar_status_t oscar_bf16_decode(const oscar_dims_t* dims, int32_t ba
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return OSCAR_ERR_INVALID_ARG;
   if (misaligned16(bf16_pages)) return OSCAR_ERR_INVALID_ARG;
   Plan plan;
-  if (!make_plan(dims, batch, max_seq_len, pages_per_split, 0, 0, kBf16Paged, &plan)) return OSCAR_ERR_INVALID_ARG;
+  if (!make_plan(dims, batch, max_seq_len, pages_per_split, 0, 0, kBf16Paged, split_ctas_per_sm(dims, kBf16Paged), &plan)) return OSCAR_ERR_INVALID_ARG;
   if (workspace_bytes < plan.total) return OSCAR_ERR_WORKSPACE;
   if (merge_smem(dims->head_dim, plan.ns, false, false) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
   Params p = base_params(dims, batch, max_seq_len, plan, sm_scale, workspace);
@@ -169,6 +181,7 @@ extern "C" oscar_status_t oscar_bf16_decode(const oscar_dims_t* dims, int32_t ba
   p.page_table = page_table;
   p.seq_lens = seq_lens;
   p.out = out;
+  p.qfrag = nullptr;
   return run(p, kBf16Paged, stream);
 }
 
@@ -206,7 +219,7 @@ extern "C" oscar_status_t oscar_decode_noalloc(const oscar_dims_t* dims, int32_t
   if (check_dims(dims) == OSCAR_OK && batch > 0 && max_seq_len >= 0 && pages_per_split >= 0 && sink_len >= 0 &&
       window_len >= 0) {
     Plan plan;
-    if (make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, &plan) &&
+    if (make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, split_ctas_per_sm(dims, kMixed), &plan) &&
         plan.total > OSCAR_NOALLOC_SCRATCH_BYTES)
       return OSCAR_ERR_WORKSPACE;
   }

@@ -15,6 +15,8 @@
 //   * PV:  O^T[ch][query] += V^T[ch][token] . P[token][query], A from
 //     ldmatrix.trans, B = p split into bf16 hi + lo;
 // then a log-sum-exp merge of the warps through shared memory.
+#include <mutex>
+
 #include "decode_common.cuh"
 
 namespace oscar_dec {
@@ -22,7 +24,7 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kWarps = 4;
-constexpr int kStages = 3;
+constexpr int kStages = 2;  // 2 pages per warp: three 4-warp CTAs fit in shared memory
 constexpr int kRowBytes = kD * 2;            // one token row of K or V
 constexpr int kRowPitch = kRowBytes + 16;    // padded row in shared memory
 constexpr int kStageBytes = 32 * kRowPitch;  // 16 K rows then 16 V rows
@@ -312,6 +314,26 @@ cudaError_t launch_impl(const Params& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+int bf16_mma_ctas_per_sm(int gqa) {
+  static std::mutex mu;
+  static int cache[64][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 2;
+  const int two = gqa > 4 ? 1 : 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int& c = cache[dev][two];
+  if (c == 0) {
+    const void* k = two ? reinterpret_cast<const void*>(bf16_mma_split_kernel<2>)
+                        : reinterpret_cast<const void*>(bf16_mma_split_kernel<1>);
+    int n = 0;
+    if (set_smem_limit_once(k, kSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kWarps * 32, kSmem) != cudaSuccess || n <= 0)
+      n = 2;
+    c = n;
+  }
+  return c;
+}
 
 bool bf16_mma_supported(const Params& p) { return p.D == kD && p.gqa >= 1 && p.gqa <= 8 && p.pps <= kMaxPps; }
 

@@ -16,6 +16,11 @@ using namespace oscar;
 constexpr int kThreads = 128;
 constexpr int kTile = 32;        // positions per softmax tile (one per lane)
 constexpr int kBf16Chunk = 32;   // sink/window positions per split (one softmax tile)
+// Per (sequence, KV head): the QK B-fragments of the tensor-core INT2 kernel for
+// each of the 32 lanes (2 n-tiles x 8 k-steps x 2 words) and the lane's per-query
+// factors (2 n-tiles x (score factor + 2 group sums)), 40 words per lane.
+constexpr int kQfragWords = 40;
+constexpr int kQfragBytes = 32 * kQfragWords * 4;
 constexpr size_t kMergeStageMax = 96 * 1024;    // partials staged in the merge's shared memory up to this size
 constexpr size_t kMergeSmemLimit = 200 * 1024;  // dynamic shared-memory limit set for the merge kernel
 
@@ -26,7 +31,7 @@ struct Plan {
   int n_paged = 0;     // splits over the paged pool
   int n_dense = 0;     // splits over the BF16 sink/window buffers
   int ns = 0;          // n_paged + n_dense
-  size_t off_qrot = 0, off_po = 0, off_pml = 0, total = 0;
+  size_t off_qrot = 0, off_qfrag = 0, off_po = 0, off_pml = 0, total = 0;
 };
 
 struct Params {
@@ -46,6 +51,7 @@ struct Params {
   const int32_t* seq_lens;
   float* out;
   float* q_rot;
+  uint32_t* qfrag;  // kQfragBytes per (sequence, KV head); null when not needed
   float* part_o;
   float* part_ml;
 };
@@ -53,6 +59,8 @@ struct Params {
 // Tensor-core split kernels for the shapes they cover (decode_int2_mma.cu,
 // decode_bf16_mma.cu).
 bool int2_mma_supported(const Params& p);
+int int2_mma_ctas_per_sm(int gqa, int G);  // resident CTAs per SM of the INT2 kernel
+int bf16_mma_ctas_per_sm(int gqa);         // resident CTAs per SM of the BF16 kernel
 cudaError_t int2_mma_split(const Params& p, cudaStream_t stream);
 bool bf16_mma_supported(const Params& p);
 cudaError_t bf16_mma_split(const Params& p, cudaStream_t stream);
@@ -84,28 +92,37 @@ __device__ __forceinline__ void grid_dep_launch_dependents() { asm volatile("gri
 
 namespace {  // internal linkage in every unit that includes this header
 
-bool make_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req, int S, int W, Mode mode, Plan* p) {
+// Split plan.  With pages_per_split == 0 the split size is chosen so that the
+// paged splits of the whole batch fill about one wave of resident CTAs
+// (ctas_per_sm x SMs, the sink/window splits counted), 4..64 pages per split.
+bool make_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req, int S, int W, Mode mode, int ctas_per_sm,
+               Plan* p) {
   if (B < 0 || max_seq_len < 0 || pps_req < 0 || S < 0 || W < 0) return false;
   if (max_seq_len > d->max_pages_per_seq * kPageSize) return false;
   const int max_pages = (max_seq_len + kPageSize - 1) / kPageSize;
+  const int dense = mode == kMixed ? (S + W < max_seq_len ? S + W : max_seq_len) : 0;
+  p->n_dense = (dense + kBf16Chunk - 1) / kBf16Chunk;
   int pps = pps_req;
   if (pps == 0) {
     const long long units = static_cast<long long>(B) * d->num_kv_heads;
-    long long want = (static_cast<long long>(max_pages) * units + 2LL * num_sms() - 1) / (2LL * num_sms());
-    if (want < 8) want = 8;
+    long long slots = static_cast<long long>(ctas_per_sm > 0 ? ctas_per_sm : 2) * num_sms() - units * p->n_dense;
+    if (slots < units) slots = units;
+    const long long splits = (slots + units - 1) / units;
+    long long want = (max_pages + splits - 1) / splits;
+    if (want < 4) want = 4;
     if (want > 64) want = 64;
     pps = static_cast<int>(want);
   }
   p->pps = pps;
   p->n_paged = max_pages == 0 ? 0 : (max_pages + pps - 1) / pps;
-  const int dense = mode == kMixed ? (S + W < max_seq_len ? S + W : max_seq_len) : 0;
-  p->n_dense = (dense + kBf16Chunk - 1) / kBf16Chunk;
   p->ns = p->n_paged + p->n_dense;
   if (p->ns == 0) p->ns = 1;
   const size_t bh = static_cast<size_t>(B) * d->num_q_heads;
   size_t off = 0;
   p->off_qrot = off;
   if (mode == kMixed) off += align_up(bh * d->head_dim * sizeof(float), 256);
+  p->off_qfrag = off;
+  if (mode == kMixed) off += align_up(static_cast<size_t>(B) * d->num_kv_heads * kQfragBytes, 256);
   p->off_po = off;
   off += align_up(bh * p->ns * d->head_dim * sizeof(float), 256);
   p->off_pml = off;
@@ -129,6 +146,84 @@ __device__ __forceinline__ int clamp_len(const Params& p, int b) {
 constexpr size_t qrot_smem(int D) { return static_cast<size_t>(D) * D * 4 + static_cast<size_t>(kMaxGqa) * D * 4 + 16; }
 
 constexpr int kQrotThreads = 512;  // 4 groups of 128 threads, each summing a quarter of the rows
+
+// Bit position, inside its fp16 half, at which the tensor-core INT2 kernel
+// extracts channel e (0..15) of a packed 16-channel word (see decode_int2_mma.cu).
+__host__ __device__ constexpr int code_kpos(int e) { return (e & 7) <= 4 ? 2 * (e & 7) : 2 * (e & 7) - 10; }
+
+// Builds the per-lane QK operands of the tensor-core INT2 kernel for (b, h) from
+// q_rot (qr: [gqa][128] fp32 in shared memory), with `tmp` 64 floats of shared
+// scratch, into p.qfrag.  For query qi: E = 15 - ceil-exponent of max |q|, so
+// that q * 2^(E - k) fits fp16 for every code position k; the lane's B words hold
+// fp16 hi or lo parts of q * scale * log2(e) * 2^(E - kpos(ch)), and its factors
+// are F = 2^(24 - E) and the per-group sums of q * scale * log2(e).
+__device__ __forceinline__ void qfrag_build(const Params& p, int b, int h, const float* qr, float* tmp) {
+  constexpr int D = 128;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int NG = D / p.G;
+  int* E_s = reinterpret_cast<int*>(tmp);   // [8]
+  float* F_s = tmp + kMaxGqa;               // [8]
+  float* qs_s = tmp + 2 * kMaxGqa;          // [8][2]
+  __syncthreads();
+  if (warp < p.gqa) {
+    const int qi = warp;
+    const float a0 = qr[qi * D + 4 * lane] * p.scale_log2, a1 = qr[qi * D + 4 * lane + 1] * p.scale_log2;
+    const float a2 = qr[qi * D + 4 * lane + 2] * p.scale_log2, a3 = qr[qi * D + 4 * lane + 3] * p.scale_log2;
+    float amax = fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3)));
+    float sum = (a0 + a1) + (a2 + a3);
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    for (int off = 1; off < 32 / NG; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    const float sum_lo = __shfl_sync(0xffffffffu, sum, 0), sum_hi = __shfl_sync(0xffffffffu, sum, 31);
+    if (lane == 0) {
+      int e = 0;
+      if (amax > 0.f) frexpf(amax, &e);
+      const int E = min(max(15 - e, -100), 100);
+      E_s[qi] = E;
+      F_s[qi] = pow2i(24 - E);
+      qs_s[2 * qi] = sum_lo;
+      qs_s[2 * qi + 1] = NG == 2 ? sum_hi : 0.f;
+    }
+  }
+  __syncthreads();
+  uint32_t* dst = p.qfrag + (static_cast<size_t>(b) * p.H + h) * (32 * kQfragWords);
+  // B words: lane L, n-tile nt, k-step ks, word c2 -> dst[L][nt*16 + ks*2 + c2]
+  for (int idx = tid; idx < 32 * 32; idx += blockDim.x) {
+    const int L = idx / 32, r = idx % 32;
+    const int nt = r / 16, ks = (r % 16) / 2, c2 = r % 2;
+    const int g = L >> 2, t = L & 3;
+    const int qb = 4 * nt + (g >> 1);
+    const int w = t + 4 * (ks >> 2), j = 2 * (ks & 3) + c2;
+    const int ch_lo = 16 * w + j, ch_hi = ch_lo + 8;
+    uint32_t word = 0;
+    if (qb < p.gqa) {
+      const int E = E_s[qb];
+      const float x0 = qr[qb * D + ch_lo] * p.scale_log2 * pow2i(E - code_kpos(ch_lo & 15));
+      const float x1 = qr[qb * D + ch_hi] * p.scale_log2 * pow2i(E - code_kpos(ch_hi & 15));
+      __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+      if (g & 1) {
+        h0 = __float2half_rn(x0 - __half2float(h0));
+        h1 = __float2half_rn(x1 - __half2float(h1));
+      }
+      word = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+    }
+    dst[L * kQfragWords + r] = word;
+  }
+  // factors: lane L, n-tile nt -> dst[L][32 + 3*nt + {0: F, 1: group-0 sum, 2: group-1 sum}]
+  for (int idx = tid; idx < 32 * 2; idx += blockDim.x) {
+    const int L = idx / 2, nt = idx % 2;
+    const int qi = 4 * nt + (L & 3);
+    float F = 0.f, s0 = 0.f, s1 = 0.f;
+    if (qi < p.gqa) {
+      F = F_s[qi];
+      s0 = qs_s[2 * qi];
+      s1 = qs_s[2 * qi + 1];
+    }
+    dst[L * kQfragWords + 32 + 3 * nt + 0] = __float_as_uint(F);
+    dst[L * kQfragWords + 32 + 3 * nt + 1] = __float_as_uint(s0);
+    dst[L * kQfragWords + 32 + 3 * nt + 2] = __float_as_uint(s1);
+  }
+  for (int idx = tid; idx < 32 * 2; idx += blockDim.x) dst[(idx / 2) * kQfragWords + 38 + idx % 2] = 0u;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
@@ -183,7 +278,9 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) tot += part[(g * kMaxGqa + qi) * D + jj];
     p.q_rot[q0 + idx] = tot;
+    qs[idx] = tot;  // q is no longer needed: keep q_rot for the fragments below
   }
+  if (D == 128 && p.qfrag != nullptr) qfrag_build(p, b, h, qs, reinterpret_cast<float*>(part + kGroups * kMaxGqa * D));
 }
 
 // Shared memory (bytes) of split_body for head dimension D.

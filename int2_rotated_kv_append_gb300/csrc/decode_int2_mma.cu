@@ -27,6 +27,8 @@
 //     power of two and 2^-sig are applied once at the end.
 // The warps of a CTA are merged through shared memory by log-sum-exp and the
 // CTA writes one (max, sum, output) partial per query head.
+#include <mutex>
+
 #include "decode_common.cuh"
 
 namespace oscar_dec {
@@ -42,10 +44,9 @@ template <int NG>
 struct Geo {
   static constexpr int kSzBytes = 2 * 16 * NG * 2 * 2;  // K then V fp16 (scale, zero) of 16 tokens
   static constexpr int kStageBytes = kCodeBytes + kSzBytes;
-  // stages | q_rot rows of the CTA's query heads | mbarriers (stages + q) | page ids
-  static constexpr size_t kPagedSmem = static_cast<size_t>(kWarps) * kStages * kStageBytes +
-                                       static_cast<size_t>(kMaxGqa) * kD * 4 + (kWarps * kStages + 1) * 8 +
-                                       kMaxPps * 4;
+  // stages | QK fragments of the 32 lanes | mbarriers (stages + fragments) | page ids
+  static constexpr size_t kPagedSmem = static_cast<size_t>(kWarps) * kStages * kStageBytes + kQfragBytes +
+                                       (kWarps * kStages + 1) * 8 + kMaxPps * 4;
   static constexpr size_t kSmem = kPagedSmem > split_body_smem(kD) ? kPagedSmem : split_body_smem(kD);
 };
 
@@ -109,8 +110,8 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
   const int npg = (r1 - 1) / kPageSize + 1 - pg0;
 
   uint8_t* stages = smem;
-  float* qbuf = reinterpret_cast<float*>(smem + kWarps * kStages * kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qbuf + kMaxGqa * kD);
+  uint32_t* qbuf = reinterpret_cast<uint32_t*>(smem + kWarps * kStages * kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qbuf + 32 * kQfragWords);
   uint64_t* qbar = bars + kWarps * kStages;
   int* pid_s = reinterpret_cast<int*>(qbar + 1);
   for (int i = tid; i < npg; i += kWarps * 32) {
@@ -148,75 +149,28 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
   grid_dep_launch_dependents();
   grid_dep_wait();  // q_rot comes from the preceding kernel; the page copies above do not need it
   if (tid == 0) {
-    mbar_arrive_expect_tx(smem_u32(qbar), gqa * kD * 4);
-    bulk_g2s(smem_u32(qbuf), p.q_rot + bh0 * kD, gqa * kD * 4, smem_u32(qbar));
+    mbar_arrive_expect_tx(smem_u32(qbar), kQfragBytes);
+    bulk_g2s(smem_u32(qbuf), p.qfrag + (static_cast<size_t>(b) * p.H + h) * (32 * kQfragWords), kQfragBytes,
+             smem_u32(qbar));
   }
   bool aborted = __any_sync(0xffffffffu, !mbar_wait_bounded(smem_u32(qbar), 0));
 
-  // ---- query side (overlaps the first copies) ----
-  // Per n-tile nt this thread's C columns belong to query 4*nt + t and its B
-  // column to query 4*nt + (g >> 1), part g & 1 (0 = hi, 1 = lo).
-  const float* qr = qbuf;
+  // ---- query side: this lane's QK B-fragments and per-query factors ----
+  // (built by the q-rotation kernel).  Per n-tile nt the lane's C columns belong
+  // to query 4*nt + t and its B column to query 4*nt + (g >> 1), part g & 1.
+  const uint32_t* qw = qbuf + lane * kQfragWords;
   float F[NT], qs[NT][NG];
-  int Eb[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    F[nt] = 0.f;
-    Eb[nt] = 0;
-#pragma unroll
-    for (int gg = 0; gg < NG; ++gg) qs[nt][gg] = 0.f;
-  }
-  for (int qi = 0; qi < gqa; ++qi) {  // warp-uniform loop
-    const float4 v4 = *reinterpret_cast<const float4*>(qr + qi * kD + 4 * lane);
-    const float a0 = v4.x * p.scale_log2, a1 = v4.y * p.scale_log2, a2 = v4.z * p.scale_log2,
-                a3 = v4.w * p.scale_log2;
-    float amax = fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3)));
-    float sum = (a0 + a1) + (a2 + a3);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    // group sums: G = 64 -> lanes 0..15 and 16..31; G = 128 -> all lanes
-#pragma unroll
-    for (int off = 1; off < 32 / NG; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    const float sum_lo = __shfl_sync(0xffffffffu, sum, 0);
-    const float sum_hi = __shfl_sync(0xffffffffu, sum, 31);
-    int e = 0;
-    if (amax > 0.f) frexpf(amax, &e);
-    const int E = min(max(15 - e, -100), 100);  // max |q| * 2^E < 2^15 (clamped far from fp32 limits)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      if (qi == 4 * nt + t) {
-        F[nt] = pow2i(24 - E);
-        qs[nt][0] = sum_lo;
-        if (NG == 2) qs[nt][NG - 1] = sum_hi;
-      }
-      if (qi == 4 * nt + (g >> 1)) Eb[nt] = E;
-    }
-  }
-  // B fragments of QK: k-step ks uses word w = t + 4 * (ks >= 4) of each token,
-  // channels 16w + j, 16w + j + 8 (rows 2t, 2t+1) and 16w + j + 1, 16w + j + 9
-  // (rows 2t + 8, 2t + 9), with j = 2 * (ks & 3).
   uint32_t bq[NT][8][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int qb = 4 * nt + (g >> 1);
-    const bool use = qb < gqa;
-    const bool lo_part = (g & 1) != 0;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      const int w = t + 4 * (ks >> 2);
-      const int j = 2 * (ks & 3);
-      const int chs[4] = {16 * w + j, 16 * w + j + 8, 16 * w + j + 1, 16 * w + j + 9};
-      __half hv[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float x = 0.f;
-        if (use) x = qr[qb * kD + chs[c]] * p.scale_log2 * pow2i(Eb[nt] - kpos(chs[c] & 15));
-        const __half hi = __float2half_rn(x);
-        hv[c] = lo_part ? __float2half_rn(x - __half2float(hi)) : hi;
-      }
-      bq[nt][ks][0] = pack_half2(hv[0], hv[1]);
-      bq[nt][ks][1] = pack_half2(hv[2], hv[3]);
+      bq[nt][ks][0] = qw[nt * 16 + ks * 2];
+      bq[nt][ks][1] = qw[nt * 16 + ks * 2 + 1];
     }
+    F[nt] = __uint_as_float(qw[32 + 3 * nt]);
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) qs[nt][gg] = __uint_as_float(qw[32 + 3 * nt + 1 + gg]);
   }
 
   // ---- main loop over this warp's pages ----
@@ -484,6 +438,29 @@ cudaError_t launch_impl(const Params& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+int int2_mma_ctas_per_sm(int gqa, int G) {
+  static std::mutex mu;
+  static int cache[64][2][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 2;
+  const int two = gqa > 4 ? 1 : 0, g64 = G == 64 ? 1 : 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int& c = cache[dev][two][g64];
+  if (c == 0) {
+    const void* k = two ? (g64 ? reinterpret_cast<const void*>(int2_mma_split_kernel<2, 2>)
+                               : reinterpret_cast<const void*>(int2_mma_split_kernel<2, 1>))
+                        : (g64 ? reinterpret_cast<const void*>(int2_mma_split_kernel<1, 2>)
+                               : reinterpret_cast<const void*>(int2_mma_split_kernel<1, 1>));
+    const size_t smem = g64 ? Geo<2>::kSmem : Geo<1>::kSmem;
+    int n = 0;
+    if (set_smem_limit_once(k, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kWarps * 32, smem) != cudaSuccess || n <= 0)
+      n = 2;
+    c = n;
+  }
+  return c;
+}
 
 bool int2_mma_supported(const Params& p) {
   return p.D == kD && (p.G == 64 || p.G == 128) && p.gqa >= 1 && p.gqa <= 8 && p.pps <= kMaxPps;
