@@ -545,9 +545,20 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(Params p) {
     mbar_arrive_expect_tx(smem_u32(&bars[1]), ns * D * 4);
     bulk_g2s(smem_u32(po_s), po, ns * D * 4, smem_u32(&bars[1]));
   }
-  // M = max_s m_s, weights w_s = 2^(m_s - M), denominator sum_s w_s l_s.
+  // M = max_s m_s, weights w_s = 2^(m_s - M), denominator sum_s w_s l_s.  Each
+  // thread loads its (m, l) pairs once (up to kMlPer of them; more splits reload).
+  constexpr int kMlPer = 4;
+  float mv[kMlPer], lv[kMlPer];
   float M = -INFINITY;
-  for (int s = tid; s < ns; s += kThreads) M = fmaxf(M, ml[2 * s]);
+#pragma unroll
+  for (int k = 0; k < kMlPer; ++k) {
+    const int s = tid + k * kThreads;
+    const float2 v = s < ns ? *reinterpret_cast<const float2*>(ml + 2 * s) : make_float2(-INFINITY, 0.f);
+    mv[k] = v.x;
+    lv[k] = v.y;
+    M = fmaxf(M, v.x);
+  }
+  for (int s = tid + kMlPer * kThreads; s < ns; s += kThreads) M = fmaxf(M, ml[2 * s]);
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   if (lane == 0) red[warp] = M;
   __syncthreads();
@@ -556,7 +567,16 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(Params p) {
   for (int w = 1; w < kThreads / 32; ++w) M = fmaxf(M, red[w]);
   __syncthreads();
   float den = 0.f;
-  for (int s = tid; s < ns; s += kThreads) {
+#pragma unroll
+  for (int k = 0; k < kMlPer; ++k) {
+    const int s = tid + k * kThreads;
+    if (s < ns) {
+      const float w = (mv[k] == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(mv[k] - M);
+      wts[s] = w;
+      den = fmaf(w, lv[k], den);
+    }
+  }
+  for (int s = tid + kMlPer * kThreads; s < ns; s += kThreads) {
     const float m = ml[2 * s];
     const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(m - M);
     wts[s] = w;
@@ -599,13 +619,13 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(Params p) {
   // read 32 different banks of R_v's row-major rows and of o_rot.
   if (tid < D) {
     const int c = tid;
-    float part = 0.f;
+    float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
     for (int k = 0; k < D; ++k) {
       const int j = (c + k) & (D - 1);
-      part = fmaf(o_rot[j], Rs[c * D + j], part);
+      part[k & 3] = fmaf(o_rot[j], Rs[c * D + j], part[k & 3]);
     }
-    out[c] = (o_plain[c] + part) * inv;
+    out[c] = (o_plain[c] + ((part[0] + part[1]) + (part[2] + part[3]))) * inv;
   }
 }
 

@@ -22,9 +22,12 @@
 //     online softmax per query with warp shuffles;
 //   * PV:  O^T[ch][query] += C_v^T[ch][token] . P'[token][query] on the same
 //     MMA; A pairs two tokens of one channel (one byte-permute + one AND), B is
-//     p * scale_g * 2^sig split into fp16 hi + lo, with sig a per-warp power of
-//     two that keeps P' below 2^14; the zero term sum p * zero_g, the per-channel
-//     power of two and 2^-sig are applied once at the end.
+//     P' = p * scale_g (p <= 1, so P' <= scale <= 65504 never overflows fp16)
+//     split into fp16 hi + lo; lo is subnormal for small weights, an absolute
+//     error of at most 2^-25 per weight.  The zero term sum p * zero_g and the
+//     per-channel power of two are applied once at the end;
+//   * pages entirely inside the split's range take a path without per-token
+//     masking.
 // The warps of a CTA are merged through shared memory by log-sum-exp and the
 // CTA writes one (max, sum, output) partial per query head.
 #include <mutex>
@@ -52,7 +55,7 @@ struct Geo {
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -72,8 +75,134 @@ __device__ __forceinline__ uint32_t extract_pair(uint32_t w, uint32_t w_shr10) {
   return ((E & 7) <= 4 ? w : w_shr10) & mask;
 }
 
-__device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
-  return static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// One 16-token page of one warp: QK on tensor cores, online softmax, PV on
+// tensor cores.  `st` is the page's stage in shared memory.  FULL: every token
+// of the page is in range (no per-token masking); otherwise v0 / v1 say whether
+// this thread's tokens g and g + 8 are.
+template <int NT, int NG, bool FULL>
+__device__ __forceinline__ void int2_page(const uint8_t* st, int g, int t, bool v0, bool v1, uint32_t vsel,
+                                          int src1, int src2, const uint32_t (&bq)[NT][8][2], const float (&F)[NT],
+                                          const float (&qs)[NT][NG], float (&m_run)[NT], float (&l_run)[NT],
+                                          float (&zacc)[NT][NG], float (&O)[NT][8][4]) {
+  if (FULL) v0 = v1 = true;
+  // K words t and t + 4 of tokens g and g + 8
+  const uint32_t* kp = reinterpret_cast<const uint32_t*>(st + g * 32 + 4 * t);
+  const uint32_t kw0 = kp[0], kw1 = kp[4], kw2 = kp[64], kw3 = kp[68];
+  // V words g/2 and 4 + g/2 of tokens t, t + 8 (xa) and t + 4, t + 12 (xb)
+  const uint32_t* vp = reinterpret_cast<const uint32_t*>(st + 512 + t * 32 + 4 * (g >> 1));
+  uint32_t xa[2], xb[2];
+  xa[0] = __byte_perm(vp[0], vp[64], vsel);
+  xa[1] = __byte_perm(vp[4], vp[68], vsel);
+  xb[0] = __byte_perm(vp[32], vp[96], vsel);
+  xb[1] = __byte_perm(vp[36], vp[100], vsel);
+  // (scale, zero) of K and V for tokens g and g + 8
+  const __half2* sp = reinterpret_cast<const __half2*>(st + kCodeBytes) + g * NG;
+  float2 k0[NG], k1[NG], w0[NG], w1[NG];
+#pragma unroll
+  for (int gg = 0; gg < NG; ++gg) {
+    k0[gg] = __half22float2(sp[gg]);
+    k1[gg] = __half22float2(sp[8 * NG + gg]);
+    w0[gg] = __half22float2(sp[16 * NG + gg]);
+    w1[gg] = __half22float2(sp[24 * NG + gg]);
+  }
+
+  float acc[NT][NG][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[nt][gg][c] = 0.f;
+  {
+    const uint32_t kw0s = kw0 >> 10, kw1s = kw1 >> 10, kw2s = kw2 >> 10, kw3s = kw3 >> 10;
+#define OSCAR_QK_STEP(KS)                                                                         \
+  {                                                                                               \
+    constexpr int gg = (KS) * NG / 8;                                                             \
+    constexpr int j = 2 * ((KS) & 3);                                                             \
+    const uint32_t wa = (KS) < 4 ? kw0 : kw1, was = (KS) < 4 ? kw0s : kw1s;                       \
+    const uint32_t wb = (KS) < 4 ? kw2 : kw3, wbs = (KS) < 4 ? kw2s : kw3s;                       \
+    const uint32_t a0 = extract_pair<j>(wa, was), a1 = extract_pair<j>(wb, wbs);                  \
+    const uint32_t a2 = extract_pair<j + 1>(wa, was), a3 = extract_pair<j + 1>(wb, wbs);          \
+    _Pragma("unroll") for (int nt = 0; nt < NT; ++nt)                                             \
+        mma16816(acc[nt][gg], a0, a1, a2, a3, bq[nt][KS][0], bq[nt][KS][1]);                      \
+  }
+    OSCAR_QK_STEP(0) OSCAR_QK_STEP(1) OSCAR_QK_STEP(2) OSCAR_QK_STEP(3)
+    OSCAR_QK_STEP(4) OSCAR_QK_STEP(5) OSCAR_QK_STEP(6) OSCAR_QK_STEP(7)
+#undef OSCAR_QK_STEP
+  }
+  const uint32_t xas[2] = {xa[0] >> 10, xa[1] >> 10}, xbs[2] = {xb[0] >> 10, xb[1] >> 10};
+
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    float sc0 = 0.f, sc1 = 0.f;
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) {
+      sc0 = fmaf(k0[gg].x * F[nt], acc[nt][gg][0] + acc[nt][gg][1], fmaf(k0[gg].y, qs[nt][gg], sc0));
+      sc1 = fmaf(k1[gg].x * F[nt], acc[nt][gg][2] + acc[nt][gg][3], fmaf(k1[gg].y, qs[nt][gg], sc1));
+    }
+    if (!FULL) {
+      sc0 = v0 ? sc0 : -INFINITY;
+      sc1 = v1 ? sc1 : -INFINITY;
+    }
+    float mx = fmaxf(sc0, sc1);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float m_new = fmaxf(m_run[nt], mx);
+    if (__any_sync(0xffffffffu, m_new > m_run[nt])) {
+      const float alpha = m_run[nt] == -INFINITY ? 0.f : fast_exp2(m_run[nt] - m_new);
+      l_run[nt] *= alpha;
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] *= alpha;
+#pragma unroll
+      for (int mi = 0; mi < 8; ++mi)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) O[nt][mi][c] *= alpha;
+      m_run[nt] = m_new;
+    }
+    float p0 = fast_exp2(sc0 - m_new), p1 = fast_exp2(sc1 - m_new);
+    if (!FULL) {
+      p0 = v0 ? p0 : 0.f;
+      p1 = v1 ? p1 : 0.f;
+    }
+    l_run[nt] += p0 + p1;
+    uint32_t bp[NG][2];
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) {
+      float q0 = p0 * w0[gg].x, q1 = p1 * w1[gg].x;
+      float z0 = p0 * w0[gg].y, z1 = p1 * w1[gg].y;
+      if (!FULL) {  // masked tokens may hold any bits: never multiply them in
+        q0 = v0 ? q0 : 0.f;
+        q1 = v1 ? q1 : 0.f;
+        z0 = v0 ? z0 : 0.f;
+        z1 = v1 ? z1 : 0.f;
+      }
+      zacc[nt][gg] += z0 + z1;
+      const __half2 hi = __floats2half2_rn(q0, q1);
+      const float2 hf = __half22float2(hi);
+      const uint32_t xhi = h2_bits(hi), xlo = h2_bits(__floats2half2_rn(q0 - hf.x, q1 - hf.y));
+      const uint32_t h_1 = __shfl_sync(0xffffffffu, xhi, src1), l_1 = __shfl_sync(0xffffffffu, xlo, src1);
+      const uint32_t h_2 = __shfl_sync(0xffffffffu, xhi, src2), l_2 = __shfl_sync(0xffffffffu, xlo, src2);
+      bp[gg][0] = (g & 1) ? l_1 : h_1;
+      bp[gg][1] = (g & 1) ? l_2 : h_2;
+    }
+    // PV: m-tile mi covers channels 16*word + 8*(g&1) + 2*(mi&3) + {0 (row g), 1 (row g+8)},
+    // word = g/2 for mi < 4 and 4 + g/2 for mi >= 4.
+#define OSCAR_PV_TILE(MI)                                                                          \
+  {                                                                                                \
+    constexpr int hw = (MI) >> 2;                                                                  \
+    constexpr int gg = (MI) * NG / 8;                                                              \
+    constexpr int e = 2 * ((MI) & 3);                                                              \
+    mma16816(O[nt][MI], extract_pair<e>(xa[hw], xas[hw]), extract_pair<e + 1>(xa[hw], xas[hw]),    \
+             extract_pair<e>(xb[hw], xbs[hw]), extract_pair<e + 1>(xb[hw], xbs[hw]), bp[gg][0],     \
+             bp[gg][1]);                                                                           \
+  }
+    OSCAR_PV_TILE(0) OSCAR_PV_TILE(1) OSCAR_PV_TILE(2) OSCAR_PV_TILE(3)
+    OSCAR_PV_TILE(4) OSCAR_PV_TILE(5) OSCAR_PV_TILE(6) OSCAR_PV_TILE(7)
+#undef OSCAR_PV_TILE
+  }
 }
 
 // ---- the kernel --------------------------------------------------------------
@@ -182,166 +311,38 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
 #pragma unroll
     for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int mi = 0; mi < 8; ++mi)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) O[nt][i][c] = 0.f;
+      for (int c = 0; c < 4; ++c) O[nt][mi][c] = 0.f;
   }
-  // P' = p * scale_v is carried as P' * 2^sig with sig chosen from the running
-  // max of the V scales seen by this warp, so P' * 2^sig < 2^14: no fp16
-  // overflow, and the fp16 lo part stays normal for every weight that matters.
-  float smax_run = 0.f;
-  int sig = 0;
   const uint32_t vsel = (2 * (g & 1)) | ((2 * (g & 1) + 1) << 4) | ((4 + 2 * (g & 1)) << 8) | ((5 + 2 * (g & 1)) << 12);
   const int src1 = 4 * t + (g >> 1), src2 = src1 + 16;
+  int stage = 0;
+  uint32_t phase = 0;
   int i = 0;
   for (; i < n_my && !aborted; ++i) {
-    const uint32_t bar = smem_u32(&my_bars[i % kStages]);
-    const bool ok = mbar_wait_bounded(bar, (i / kStages) & 1);
-    if (__any_sync(0xffffffffu, !ok)) {
+    if (__any_sync(0xffffffffu, !mbar_wait_bounded(smem_u32(&my_bars[stage]), phase))) {
       aborted = true;
       break;
     }
-    const uint8_t* st = my_stages + (i % kStages) * kStageBytes;
+    const uint8_t* st = my_stages + stage * kStageBytes;
     const int jpage = warp + i * kWarps;
+    const int pos_base = (pg0 + jpage) * kPageSize;
     const bool page_ok = pid_s[jpage] >= 0;
-    const int pos0 = (pg0 + jpage) * kPageSize + g;
-    const bool v0 = page_ok && pos0 >= r0 && pos0 < r1;
-    const bool v1 = page_ok && pos0 + 8 >= r0 && pos0 + 8 < r1;
-
-    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st);
-    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + 512);
-    const uint32_t kw0 = kc[g * 8 + t], kw1 = kc[g * 8 + t + 4];
-    const uint32_t kw2 = kc[(g + 8) * 8 + t], kw3 = kc[(g + 8) * 8 + t + 4];
-    const int vw = g >> 1;
-    uint32_t xa[2], xb[2];
-#pragma unroll
-    for (int hw = 0; hw < 2; ++hw) {
-      xa[hw] = __byte_perm(vc[t * 8 + 4 * hw + vw], vc[(t + 8) * 8 + 4 * hw + vw], vsel);
-      xb[hw] = __byte_perm(vc[(t + 4) * 8 + 4 * hw + vw], vc[(t + 12) * 8 + 4 * hw + vw], vsel);
-    }
-    const __half2* szk = reinterpret_cast<const __half2*>(st + kCodeBytes);
-    const __half2* szv = szk + 16 * NG;
-    float2 k0[NG], k1[NG], w0[NG], w1[NG];
-#pragma unroll
-    for (int gg = 0; gg < NG; ++gg) {
-      k0[gg] = __half22float2(szk[g * NG + gg]);
-      k1[gg] = __half22float2(szk[(g + 8) * NG + gg]);
-      w0[gg] = __half22float2(szv[g * NG + gg]);
-      w1[gg] = __half22float2(szv[(g + 8) * NG + gg]);
-    }
-    {
-      float sm = 0.f;
-#pragma unroll
-      for (int gg = 0; gg < NG; ++gg) sm = fmaxf(sm, fmaxf(v0 ? w0[gg].x : 0.f, v1 ? w1[gg].x : 0.f));
-      sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 4));
-      sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 8));
-      sm = fmaxf(sm, __shfl_xor_sync(0xffffffffu, sm, 16));
-      if (sm > smax_run) {  // warp-uniform
-        int e = 0;
-        frexpf(sm, &e);  // sm < 2^e
-        const int sig_new = min(max(14 - e, -100), 100);
-        if (smax_run > 0.f && sig_new < sig) {
-          const float f = pow2i(sig_new - sig);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int mi = 0; mi < 8; ++mi)
-#pragma unroll
-              for (int c = 0; c < 4; ++c) O[nt][mi][c] *= f;
-        }
-        if (smax_run == 0.f || sig_new < sig) sig = sig_new;
-        smax_run = sm;
-      }
-    }
-    const float psc = pow2i(sig);
-
-    // QK
-    float acc[NT][NG][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int gg = 0; gg < NG; ++gg)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[nt][gg][c] = 0.f;
-    {
-      const uint32_t kw0s = kw0 >> 10, kw1s = kw1 >> 10, kw2s = kw2 >> 10, kw3s = kw3 >> 10;
-#define OSCAR_QK_STEP(KS)                                                                         \
-  {                                                                                               \
-    constexpr int gg = (KS) * NG / 8;                                                             \
-    constexpr int j = 2 * ((KS) & 3);                                                             \
-    const uint32_t wa = (KS) < 4 ? kw0 : kw1, was = (KS) < 4 ? kw0s : kw1s;                       \
-    const uint32_t wb = (KS) < 4 ? kw2 : kw3, wbs = (KS) < 4 ? kw2s : kw3s;                       \
-    const uint32_t a0 = extract_pair<j>(wa, was), a1 = extract_pair<j>(wb, wbs);                  \
-    const uint32_t a2 = extract_pair<j + 1>(wa, was), a3 = extract_pair<j + 1>(wb, wbs);          \
-    _Pragma("unroll") for (int nt = 0; nt < NT; ++nt)                                             \
-        mma16816(acc[nt][gg], a0, a1, a2, a3, bq[nt][KS][0], bq[nt][KS][1]);                      \
-  }
-      OSCAR_QK_STEP(0) OSCAR_QK_STEP(1) OSCAR_QK_STEP(2) OSCAR_QK_STEP(3)
-      OSCAR_QK_STEP(4) OSCAR_QK_STEP(5) OSCAR_QK_STEP(6) OSCAR_QK_STEP(7)
-#undef OSCAR_QK_STEP
-    }
-
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float sc0 = 0.f, sc1 = 0.f;
-#pragma unroll
-      for (int gg = 0; gg < NG; ++gg) {
-        sc0 += k0[gg].x * F[nt] * (acc[nt][gg][0] + acc[nt][gg][1]) + k0[gg].y * qs[nt][gg];
-        sc1 += k1[gg].x * F[nt] * (acc[nt][gg][2] + acc[nt][gg][3]) + k1[gg].y * qs[nt][gg];
-      }
-      sc0 = v0 ? sc0 : -INFINITY;
-      sc1 = v1 ? sc1 : -INFINITY;
-      float mx = fmaxf(sc0, sc1);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      const float m_new = fmaxf(m_run[nt], mx);
-      if (__any_sync(0xffffffffu, m_new > m_run[nt])) {
-        const float alpha = m_run[nt] == -INFINITY ? 0.f : fast_exp2(m_run[nt] - m_new);
-        l_run[nt] *= alpha;
-#pragma unroll
-        for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] *= alpha;
-#pragma unroll
-        for (int mi = 0; mi < 8; ++mi)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) O[nt][mi][c] *= alpha;
-        m_run[nt] = m_new;
-      }
-      const float p0 = v0 ? fast_exp2(sc0 - m_new) : 0.f;
-      const float p1 = v1 ? fast_exp2(sc1 - m_new) : 0.f;
-      l_run[nt] += p0 + p1;
-      uint32_t bp[NG][2];
-#pragma unroll
-      for (int gg = 0; gg < NG; ++gg) {
-        const float q0 = v0 ? p0 * w0[gg].x * psc : 0.f;
-        const float q1 = v1 ? p1 * w1[gg].x * psc : 0.f;
-        zacc[nt][gg] += (v0 ? p0 * w0[gg].y : 0.f) + (v1 ? p1 * w1[gg].y : 0.f);
-        const __half h0 = __float2half_rn(q0), h1 = __float2half_rn(q1);
-        const __half e0 = __float2half_rn(q0 - __half2float(h0)), e1 = __float2half_rn(q1 - __half2float(h1));
-        const uint32_t xhi = pack_half2(h0, h1), xlo = pack_half2(e0, e1);
-        const uint32_t h_1 = __shfl_sync(0xffffffffu, xhi, src1), l_1 = __shfl_sync(0xffffffffu, xlo, src1);
-        const uint32_t h_2 = __shfl_sync(0xffffffffu, xhi, src2), l_2 = __shfl_sync(0xffffffffu, xlo, src2);
-        bp[gg][0] = (g & 1) ? l_1 : h_1;
-        bp[gg][1] = (g & 1) ? l_2 : h_2;
-      }
-      // PV: m-tile mi covers channels 16*word + 8*(g&1) + 2*(mi&3) + {0 (row g), 1 (row g+8)},
-      // word = g/2 for mi < 4 and 4 + g/2 for mi >= 4.
-      const uint32_t xas[2] = {xa[0] >> 10, xa[1] >> 10}, xbs[2] = {xb[0] >> 10, xb[1] >> 10};
-#define OSCAR_PV_TILE(MI)                                                                          \
-  {                                                                                                \
-    constexpr int hw = (MI) >> 2;                                                                  \
-    constexpr int gg = (MI) * NG / 8;                                                              \
-    constexpr int e = 2 * ((MI) & 3);                                                              \
-    mma16816(O[nt][MI], extract_pair<e>(xa[hw], xas[hw]), extract_pair<e + 1>(xa[hw], xas[hw]),    \
-             extract_pair<e>(xb[hw], xbs[hw]), extract_pair<e + 1>(xb[hw], xbs[hw]), bp[gg][0],     \
-             bp[gg][1]);                                                                           \
-  }
-      OSCAR_PV_TILE(0) OSCAR_PV_TILE(1) OSCAR_PV_TILE(2) OSCAR_PV_TILE(3)
-      OSCAR_PV_TILE(4) OSCAR_PV_TILE(5) OSCAR_PV_TILE(6) OSCAR_PV_TILE(7)
-#undef OSCAR_PV_TILE
+    if (page_ok && pos_base >= r0 && pos_base + kPageSize <= r1) {
+      int2_page<NT, NG, true>(st, g, t, true, true, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
+    } else {
+      const int pos0 = pos_base + g;
+      const bool v0 = page_ok && pos0 >= r0 && pos0 < r1;
+      const bool v1 = page_ok && pos0 + 8 >= r0 && pos0 + 8 < r1;
+      int2_page<NT, NG, false>(st, g, t, v0, v1, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
     }
     __syncwarp();
     if (lane == 0 && i + kStages < n_my) issue(i + kStages);
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
   }
   if (aborted) {
     if (lane == 0) record_error(OSCAR_DEVERR_TIMEOUT);
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
           const int e = 2 * (mi & 3) + r;
           const int ch = 16 * word + 8 * (g & 1) + e;
           ow[(warp * kMaxGqa + qi) * kD + ch] =
-              (O[nt][mi][2 * r] + O[nt][mi][2 * r + 1]) * pow2i(24 - kpos(e) - sig) + zacc[nt][gg];
+              (O[nt][mi][2 * r] + O[nt][mi][2 * r + 1]) * pow2i(24 - kpos(e)) + zacc[nt][gg];
         }
       }
     }
