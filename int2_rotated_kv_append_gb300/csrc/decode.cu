@@ -25,17 +25,14 @@ cudaError_t merge(const Params& p, cudaStream_t stream) {
   const size_t smem = merge_smem(D, p.ns, MODE == kMixed, p.merge_stage != 0);
   cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(merge_kernel<D, MODE>), kMergeSmemLimit);
   if (e != cudaSuccess) return e;
-  return launch_pdl(merge_kernel<D, MODE>, dim3(p.B * p.Hq), dim3(kThreads), smem, stream, p);
+  return launch_pdl(merge_kernel<D, MODE>, dim3(p.B * p.Hq), dim3(kMergeThreads), smem, stream, p);
 }
 
 template <int D, Mode MODE>
 cudaError_t launch(const Params& p, cudaStream_t stream) {
   if (MODE == kMixed) {
-    constexpr size_t qsmem = qrot_smem(D);
-    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(qrot_kernel<D>), qsmem);
-    if (e != cudaSuccess) return e;
-    qrot_kernel<D><<<p.B * p.H, kQrotThreads, qsmem, stream>>>(p);
-    e = cudaGetLastError();
+    qrot_kernel<D><<<dim3(p.B * p.H, D / 32), kQrotThreads, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   const bool mma = MODE == kMixed ? int2_mma_supported(p) : bf16_mma_supported(p);

@@ -18,11 +18,12 @@ constexpr int kTile = 32;        // positions per softmax tile (one per lane)
 constexpr int kBf16Chunk = 32;   // sink/window positions per split (one softmax tile)
 // Per (sequence, KV head): the QK B-fragments of the tensor-core INT2 kernel for
 // each of the 32 lanes (2 n-tiles x 8 k-steps x 2 words) and the lane's per-query
-// factors (2 n-tiles x (score factor + 2 group sums)), 40 words per lane.
-constexpr int kQfragWords = 40;
+// factors (2 n-tiles x (score factor + 4 column-block sums)), 44 words per lane.
+constexpr int kQfragWords = 44;
 constexpr int kQfragBytes = 32 * kQfragWords * 4;
 constexpr size_t kMergeStageMax = 96 * 1024;    // partials staged in the merge's shared memory up to this size
-constexpr size_t kMergeSmemLimit = 200 * 1024;  // dynamic shared-memory limit set for the merge kernel
+constexpr size_t kMergeSmemLimit = 180 * 1024;  // dynamic shared-memory limit set for the merge kernel
+constexpr int kMergeThreads = 512;
 
 enum Mode { kMixed = 0, kBf16Paged = 1 };
 
@@ -143,144 +144,118 @@ __device__ __forceinline__ int clamp_len(const Params& p, int b) {
 // q_rot[b][hq] = q[b][hq] . R_k[h] for the GQA query heads hq of one (b, h):
 // R_k[h] arrives in shared memory by one bulk copy and thread j computes column
 // j for every query head.  Dynamic shared memory: qrot_smem(D) bytes.
-constexpr size_t qrot_smem(int D) { return static_cast<size_t>(D) * D * 4 + static_cast<size_t>(kMaxGqa) * D * 4 + 16; }
-
-constexpr int kQrotThreads = 512;  // 4 groups of 128 threads, each summing a quarter of the rows
+constexpr int kQrotThreads = 128;  // 4 warps, each summing a quarter of the rows of R
 
 // Bit position, inside its fp16 half, at which the tensor-core INT2 kernel
 // extracts channel e (0..15) of a packed 16-channel word (see decode_int2_mma.cu).
 __host__ __device__ constexpr int code_kpos(int e) { return (e & 7) <= 4 ? 2 * (e & 7) : 2 * (e & 7) - 10; }
 
-// Builds the per-lane QK operands of the tensor-core INT2 kernel for (b, h) from
-// q_rot (qr: [gqa][128] fp32 in shared memory), with `tmp` 64 floats of shared
-// scratch, into p.qfrag.  For query qi: E = 15 - ceil-exponent of max |q|, so
-// that q * 2^(E - k) fits fp16 for every code position k; the lane's B words hold
-// fp16 hi or lo parts of q * scale * log2(e) * 2^(E - kpos(ch)), and its factors
-// are F = 2^(24 - E) and the per-group sums of q * scale * log2(e).
-__device__ __forceinline__ void qfrag_build(const Params& p, int b, int h, const float* qr, float* tmp) {
-  constexpr int D = 128;
+// q_rot[b][hq] = q[b][hq] . R_k[h] for the GQA query heads of one (b, h), one
+// CTA per block of 32 output columns (grid (B*Hkv, D/32)).  Warp w sums rows
+// [w*D/4, (w+1)*D/4) of the block's columns, read straight from global memory
+// (D/4 independent coalesced loads per lane); the warps' sums are added in
+// order through shared memory.
+//
+// For head_dim 128 the CTA also writes its share of the tensor-core INT2
+// kernel's per-lane QK operands (p.qfrag, kQfragWords words per lane):
+//   words [0, 32): B fragments, word nt*16 + ks*2 + c2 holds fp16 hi (lanes with
+//     g even) or lo (g odd) parts of q_rot * scale * log2(e) * 2^(E - kpos(ch))
+//     for channels (16w + j, 16w + j + 8), w = t + 4*(ks/4), j = 2*(ks%4) + c2,
+//     query 4*nt + g/2 (g = lane/4, t = lane%4); the 16-channel word w lives in
+//     column block w/2, so each CTA writes the words of its two w;
+//   words 32 + 5*nt + {0, 1..4}: for query 4*nt + t, F = 2^(24 - E) and the sums
+//     of q_rot * scale * log2(e) over each column block (the kernel adds the
+//     blocks of a group).
+// E = 15 - ceil(log2(||q|| * scale * log2(e) * (1 + 2^-10))): since R is
+// orthogonal every |q_rot[ch]| <= ||q||, so every B value fits fp16.
+template <int D>
+__global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
+  constexpr int kRows = D / 4;
+  __shared__ float qs[kMaxGqa * D];
+  __shared__ float part[4][kMaxGqa][32];
+  __shared__ float qrb[kMaxGqa][32];
+  __shared__ int E_s[kMaxGqa];
+  grid_dep_launch_dependents();
+  const int b = blockIdx.x / p.H, h = blockIdx.x % p.H, cb = blockIdx.y;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int NG = D / p.G;
-  int* E_s = reinterpret_cast<int*>(tmp);   // [8]
-  float* F_s = tmp + kMaxGqa;               // [8]
-  float* qs_s = tmp + 2 * kMaxGqa;          // [8][2]
+  const int gqa = p.gqa;
+  const size_t q0 = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * gqa) * D;
+  const float* R = p.R_k + static_cast<size_t>(h) * D * D + static_cast<size_t>(warp) * kRows * D + 32 * cb + lane;
+  float r[kRows];
+#pragma unroll
+  for (int rr = 0; rr < kRows; ++rr) r[rr] = __ldg(R + static_cast<size_t>(rr) * D);
+  for (int i = tid; i < gqa * D; i += kQrotThreads) qs[i] = __bfloat162float(p.q[q0 + i]);
   __syncthreads();
-  if (warp < p.gqa) {
-    const int qi = warp;
-    const float a0 = qr[qi * D + 4 * lane] * p.scale_log2, a1 = qr[qi * D + 4 * lane + 1] * p.scale_log2;
-    const float a2 = qr[qi * D + 4 * lane + 2] * p.scale_log2, a3 = qr[qi * D + 4 * lane + 3] * p.scale_log2;
-    float amax = fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3)));
-    float sum = (a0 + a1) + (a2 + a3);
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    for (int off = 1; off < 32 / NG; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    const float sum_lo = __shfl_sync(0xffffffffu, sum, 0), sum_hi = __shfl_sync(0xffffffffu, sum, 31);
+  for (int qi = 0; qi < gqa; ++qi) {
+    float acc = 0.f;
+#pragma unroll
+    for (int rr = 0; rr < kRows; ++rr) acc = fmaf(qs[qi * D + warp * kRows + rr], r[rr], acc);
+    part[warp][qi][lane] = acc;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < gqa * 32; idx += kQrotThreads) {
+    const int qi = idx / 32, c = idx % 32;
+    const float tot = ((part[0][qi][c] + part[1][qi][c]) + part[2][qi][c]) + part[3][qi][c];
+    p.q_rot[q0 + static_cast<size_t>(qi) * D + 32 * cb + c] = tot;
+    qrb[qi][c] = tot;
+  }
+  if (p.qfrag == nullptr) return;
+  if constexpr (D == 128) {
+  // exponents from ||q|| (one warp per query)
+  for (int qi = warp; qi < gqa; qi += kQrotThreads / 32) {
+    float ss = 0.f;
+    for (int i = lane; i < D; i += 32) ss = fmaf(qs[qi * D + i], qs[qi * D + i], ss);
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     if (lane == 0) {
+      const float bound = sqrtf(ss) * fabsf(p.scale_log2) * (1.f + 1.f / 1024.f);
       int e = 0;
-      if (amax > 0.f) frexpf(amax, &e);
-      const int E = min(max(15 - e, -100), 100);
-      E_s[qi] = E;
-      F_s[qi] = pow2i(24 - E);
-      qs_s[2 * qi] = sum_lo;
-      qs_s[2 * qi + 1] = NG == 2 ? sum_hi : 0.f;
+      if (bound > 0.f) frexpf(bound, &e);
+      E_s[qi] = min(max(15 - e, -100), 100);
     }
   }
   __syncthreads();
   uint32_t* dst = p.qfrag + (static_cast<size_t>(b) * p.H + h) * (32 * kQfragWords);
-  // B words: lane L, n-tile nt, k-step ks, word c2 -> dst[L][nt*16 + ks*2 + c2]
-  for (int idx = tid; idx < 32 * 32; idx += blockDim.x) {
-    const int L = idx / 32, r = idx % 32;
-    const int nt = r / 16, ks = (r % 16) / 2, c2 = r % 2;
-    const int g = L >> 2, t = L & 3;
-    const int qb = 4 * nt + (g >> 1);
-    const int w = t + 4 * (ks >> 2), j = 2 * (ks & 3) + c2;
+  // fragment words of this block's two 16-channel words w = 2*cb, 2*cb + 1:
+  // lanes with t = w % 4 (8 values of g), k-steps 4*(w/4) .. +3, c2 in {0,1}, nt in {0,1}
+  for (int idx = tid; idx < 2 * 8 * 4 * 2 * 2; idx += kQrotThreads) {
+    const int w = 2 * cb + (idx >> 7);
+    const int gg8 = (idx >> 4) & 7, kk = (idx >> 2) & 3, c2 = (idx >> 1) & 1, nt = idx & 1;
+    const int t = w & 3, L = 4 * gg8 + t, ks = 4 * (w >> 2) + kk;
+    const int qb = 4 * nt + (gg8 >> 1);
+    const int j = 2 * kk + c2;
     const int ch_lo = 16 * w + j, ch_hi = ch_lo + 8;
     uint32_t word = 0;
-    if (qb < p.gqa) {
+    if (qb < gqa) {
       const int E = E_s[qb];
-      const float x0 = qr[qb * D + ch_lo] * p.scale_log2 * pow2i(E - code_kpos(ch_lo & 15));
-      const float x1 = qr[qb * D + ch_hi] * p.scale_log2 * pow2i(E - code_kpos(ch_hi & 15));
+      const float x0 = qrb[qb][ch_lo - 32 * cb] * p.scale_log2 * pow2i(E - code_kpos(ch_lo & 15));
+      const float x1 = qrb[qb][ch_hi - 32 * cb] * p.scale_log2 * pow2i(E - code_kpos(ch_hi & 15));
       __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-      if (g & 1) {
+      if (gg8 & 1) {
         h0 = __float2half_rn(x0 - __half2float(h0));
         h1 = __float2half_rn(x1 - __half2float(h1));
       }
       word = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
     }
-    dst[L * kQfragWords + r] = word;
+    dst[L * kQfragWords + nt * 16 + ks * 2 + c2] = word;
   }
-  // factors: lane L, n-tile nt -> dst[L][32 + 3*nt + {0: F, 1: group-0 sum, 2: group-1 sum}]
-  for (int idx = tid; idx < 32 * 2; idx += blockDim.x) {
-    const int L = idx / 2, nt = idx % 2;
+  // factors: block sums of query 4*nt + t for the 32 lanes (and F from block 0)
+  if (tid < 64) {
+    const int L = tid / 2, nt = tid % 2;
     const int qi = 4 * nt + (L & 3);
-    float F = 0.f, s0 = 0.f, s1 = 0.f;
-    if (qi < p.gqa) {
-      F = F_s[qi];
-      s0 = qs_s[2 * qi];
-      s1 = qs_s[2 * qi + 1];
+    float sum = 0.f, F = 0.f;
+    if (qi < gqa) {
+      for (int c = 0; c < 32; ++c) sum += qrb[qi][c];
+      sum *= p.scale_log2;
+      F = pow2i(24 - E_s[qi]);
     }
-    dst[L * kQfragWords + 32 + 3 * nt + 0] = __float_as_uint(F);
-    dst[L * kQfragWords + 32 + 3 * nt + 1] = __float_as_uint(s0);
-    dst[L * kQfragWords + 32 + 3 * nt + 2] = __float_as_uint(s1);
-  }
-  for (int idx = tid; idx < 32 * 2; idx += blockDim.x) dst[(idx / 2) * kQfragWords + 38 + idx % 2] = 0u;
-}
-
-template <int D>
-__global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
-  extern __shared__ __align__(128) float qsm[];
-  float* Rs = qsm;                 // [D][D]
-  float* qs = Rs + D * D;          // [gqa][D]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(qs + kMaxGqa * D);
-  grid_dep_launch_dependents();
-  const int b = blockIdx.x / p.H, h = blockIdx.x % p.H;
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    mbar_init(smem_u32(bar), 1);
-    mbar_init_fence();
-    mbar_arrive_expect_tx(smem_u32(bar), D * D * 4);
-    bulk_g2s(smem_u32(Rs), p.R_k + static_cast<size_t>(h) * D * D, D * D * 4, smem_u32(bar));
-  }
-  const size_t q0 = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * p.gqa) * D;
-  for (int i = tid; i < p.gqa * D; i += kQrotThreads) qs[i] = __bfloat162float(p.q[q0 + i]);
-  __syncthreads();
-  if (!mbar_wait_bounded(smem_u32(bar), 0)) {
-    if (tid == 0) record_error(OSCAR_DEVERR_TIMEOUT);
-    mbar_wait_bounded(smem_u32(bar), 0);  // give a late copy one more bounded chance to land
-  }
-  // Thread (quarter qt, column j) sums rows [qt*D/4, (qt+1)*D/4); the quarters are
-  // then added in order through shared memory (the R_k area is no longer needed).
-  const int j = tid % D, qt = tid / D;
-  constexpr int kGroups = kQrotThreads / D;
-  float acc[kMaxGqa];
-#pragma unroll
-  for (int qi = 0; qi < kMaxGqa; ++qi) acc[qi] = 0.f;
-  if (qt < kGroups) {
-    const int i0 = qt * (D / kGroups);
-#pragma unroll 4
-    for (int i = i0; i < i0 + D / kGroups; ++i) {
-      const float r = Rs[i * D + j];
-#pragma unroll
-      for (int qi = 0; qi < kMaxGqa; ++qi)
-        if (qi < p.gqa) acc[qi] = fmaf(qs[qi * D + i], r, acc[qi]);
+    dst[L * kQfragWords + 32 + 5 * nt + 1 + cb] = __float_as_uint(sum);
+    if (cb == 0) {
+      dst[L * kQfragWords + 32 + 5 * nt] = __float_as_uint(F);
+      dst[L * kQfragWords + 42] = 0u;
+      dst[L * kQfragWords + 43] = 0u;
     }
   }
-  __syncthreads();
-  float* part = Rs;  // [kGroups][kMaxGqa][D]
-  if (qt < kGroups) {
-#pragma unroll
-    for (int qi = 0; qi < kMaxGqa; ++qi)
-      if (qi < p.gqa) part[(qt * kMaxGqa + qi) * D + j] = acc[qi];
-  }
-  __syncthreads();
-  for (int idx = tid; idx < p.gqa * D; idx += kQrotThreads) {
-    const int qi = idx / D, jj = idx % D;
-    float tot = 0.f;
-#pragma unroll
-    for (int g = 0; g < kGroups; ++g) tot += part[(g * kMaxGqa + qi) * D + jj];
-    p.q_rot[q0 + idx] = tot;
-    qs[idx] = tot;  // q is no longer needed: keep q_rot for the fragments below
-  }
-  if (D == 128 && p.qfrag != nullptr) qfrag_build(p, b, h, qs, reinterpret_cast<float*>(part + kGroups * kMaxGqa * D));
+  }  // D == 128
 }
 
 // Shared memory (bytes) of split_body for head dimension D.
@@ -514,10 +489,13 @@ constexpr size_t merge_smem(int D, int ns, bool mixed, bool stage) {
 }
 
 template <int D, Mode MODE>
-__global__ void __launch_bounds__(kThreads) merge_kernel(Params p) {
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
   __shared__ float o_rot[D];
   __shared__ float o_plain[D];
-  __shared__ float red[kThreads / 32];
+  constexpr int kMG = kMergeThreads / D;  // threads per output channel
+  __shared__ float red[kMergeThreads / 32];
+  __shared__ float red2[kMG][D];
+  __shared__ float red3[kMG][D];
   extern __shared__ __align__(128) float msm[];
   constexpr bool kRot = MODE == kMixed;
   const int ns = p.ns;
@@ -547,36 +525,36 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(Params p) {
   }
   // M = max_s m_s, weights w_s = 2^(m_s - M), denominator sum_s w_s l_s.  Each
   // thread loads its (m, l) pairs once (up to kMlPer of them; more splits reload).
-  constexpr int kMlPer = 4;
+  constexpr int kMlPer = 1;
   float mv[kMlPer], lv[kMlPer];
   float M = -INFINITY;
 #pragma unroll
   for (int k = 0; k < kMlPer; ++k) {
-    const int s = tid + k * kThreads;
+    const int s = tid + k * kMergeThreads;
     const float2 v = s < ns ? *reinterpret_cast<const float2*>(ml + 2 * s) : make_float2(-INFINITY, 0.f);
     mv[k] = v.x;
     lv[k] = v.y;
     M = fmaxf(M, v.x);
   }
-  for (int s = tid + kMlPer * kThreads; s < ns; s += kThreads) M = fmaxf(M, ml[2 * s]);
+  for (int s = tid + kMlPer * kMergeThreads; s < ns; s += kMergeThreads) M = fmaxf(M, ml[2 * s]);
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   if (lane == 0) red[warp] = M;
   __syncthreads();
   M = red[0];
 #pragma unroll
-  for (int w = 1; w < kThreads / 32; ++w) M = fmaxf(M, red[w]);
+  for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red[w]);
   __syncthreads();
   float den = 0.f;
 #pragma unroll
   for (int k = 0; k < kMlPer; ++k) {
-    const int s = tid + k * kThreads;
+    const int s = tid + k * kMergeThreads;
     if (s < ns) {
       const float w = (mv[k] == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(mv[k] - M);
       wts[s] = w;
       den = fmaf(w, lv[k], den);
     }
   }
-  for (int s = tid + kMlPer * kThreads; s < ns; s += kThreads) {
+  for (int s = tid + kMlPer * kMergeThreads; s < ns; s += kMergeThreads) {
     const float m = ml[2 * s];
     const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(m - M);
     wts[s] = w;
@@ -587,20 +565,31 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(Params p) {
   __syncthreads();
   den = 0.f;
 #pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) den += red[w];
+  for (int w = 0; w < kMergeThreads / 32; ++w) den += red[w];
   bool ok = true;
   if (p.merge_stage) ok = mbar_wait_bounded(smem_u32(&bars[1]), 0);
   if (!ok && tid == 0) record_error(OSCAR_DEVERR_TIMEOUT);
   const float* src = p.merge_stage ? po_s : po;
-  if (tid < D) {
-    float a_rot = 0.f, a_plain = 0.f;
+  {
+    // thread (channel c, group sg) sums the splits s = sg, sg + kMG, ...
+    const int c = tid % D, sg = tid / D;
     const int n_rot = kRot ? p.n_paged : 0;
-#pragma unroll 4
-    for (int s = 0; s < n_rot; ++s) a_rot = fmaf(wts[s], src[static_cast<size_t>(s) * D + tid], a_rot);
-#pragma unroll 4
-    for (int s = n_rot; s < ns; ++s) a_plain = fmaf(wts[s], src[static_cast<size_t>(s) * D + tid], a_plain);
-    o_rot[tid] = a_rot;
-    o_plain[tid] = a_plain;
+    float a_rot = 0.f, a_plain = 0.f;
+    for (int s = sg; s < n_rot; s += kMG) a_rot = fmaf(wts[s], src[static_cast<size_t>(s) * D + c], a_rot);
+    for (int s = n_rot + sg; s < ns; s += kMG) a_plain = fmaf(wts[s], src[static_cast<size_t>(s) * D + c], a_plain);
+    red2[sg][c] = a_rot;
+    red3[sg][c] = a_plain;
+  }
+  __syncthreads();
+  if (tid < D) {
+    float ar = 0.f, ap = 0.f;
+#pragma unroll
+    for (int g = 0; g < kMG; ++g) {
+      ar += red2[g][tid];
+      ap += red3[g][tid];
+    }
+    o_rot[tid] = ar;
+    o_plain[tid] = ap;
   }
   __syncthreads();
   const float inv = (ok && den > 0.f) ? 1.f / den : 0.f;
@@ -609,23 +598,32 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(Params p) {
     if (tid < D) out[tid] = o_plain[tid] * inv;
     return;
   }
-  if (!mbar_wait_bounded(smem_u32(&bars[0]), 0)) {
+  if (!__syncthreads_and(mbar_wait_bounded(smem_u32(&bars[0]), 0))) {
     if (tid == 0) record_error(OSCAR_DEVERR_TIMEOUT);
     if (tid < D) out[tid] = 0.f;
     return;
   }
-  // out[c] = (o_plain[c] + sum_j o_rot[j] R_v[h][c][j]) * inv, thread c.  Thread c
-  // visits j in the order (c + k) mod D, so at every step the 32 lanes of a warp
-  // read 32 different banks of R_v's row-major rows and of o_rot.
-  if (tid < D) {
-    const int c = tid;
+  // out[c] = (o_plain[c] + sum_j o_rot[j] R_v[h][c][j]) * inv.  Thread (c, jq) sums
+  // j over the jq-th block of D/kMG columns, visiting them in the order
+  // (c + k) mod (D/kMG) so a warp's lanes read different banks; the blocks are
+  // then added in order.
+  {
+    constexpr int kJ = D / kMG;
+    const int c = tid % D, jq = tid / D;
     float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-    for (int k = 0; k < D; ++k) {
-      const int j = (c + k) & (D - 1);
+    for (int k = 0; k < kJ; ++k) {
+      const int j = jq * kJ + ((c + k) & (kJ - 1));
       part[k & 3] = fmaf(o_rot[j], Rs[c * D + j], part[k & 3]);
     }
-    out[c] = (o_plain[c] + ((part[0] + part[1]) + (part[2] + part[3]))) * inv;
+    red2[jq][c] = (part[0] + part[1]) + (part[2] + part[3]);
+  }
+  __syncthreads();
+  if (tid < D) {
+    float u = 0.f;
+#pragma unroll
+    for (int g = 0; g < kMG; ++g) u += red2[g][tid];
+    out[tid] = (o_plain[tid] + u) * inv;
   }
 }
 

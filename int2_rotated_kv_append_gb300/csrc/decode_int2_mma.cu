@@ -219,6 +219,14 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
   constexpr int kSzBytes = Geo<NG>::kSzBytes;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int gqa = p.gqa;
+  // Page ids of the whole split are loaded together with the sequence length (they
+  // do not depend on it); only the pages in range are validated and used.
+  uint64_t* bars0 = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kStageBytes + kQfragBytes);
+  int* pid_all = reinterpret_cast<int*>(bars0 + kWarps * kStages + 1);
+  const int sp0 = s * p.pps;
+  const int spn = max(0, min(p.pps, p.max_pages - sp0));
+  for (int k = tid; k < spn; k += kWarps * 32)
+    pid_all[k] = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + sp0 + k);
   const int L = clamp_len(p, b);
   const int win_begin = max(p.S, L - p.W);
   const int lo_pos = s * p.pps * kPageSize;
@@ -240,17 +248,9 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
 
   uint8_t* stages = smem;
   uint32_t* qbuf = reinterpret_cast<uint32_t*>(smem + kWarps * kStages * kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qbuf + 32 * kQfragWords);
+  uint64_t* bars = bars0;
   uint64_t* qbar = bars + kWarps * kStages;
-  int* pid_s = reinterpret_cast<int*>(qbar + 1);
-  for (int i = tid; i < npg; i += kWarps * 32) {
-    int pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg0 + i);
-    if (pid < 0 || pid >= p.num_pages) {
-      record_error(OSCAR_DEVERR_PAGE_ID);
-      pid = -1;
-    }
-    pid_s[i] = pid;
-  }
+  const int* pid_s = pid_all + (pg0 - sp0);  // page ids from the split's first page in range
   if (lane == 0)
     for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp * kStages + i]), 1);
   if (tid == 0) mbar_init(smem_u32(qbar), 1);
@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
   auto issue = [&](int i) {  // lane 0: bring local page i of this warp into its stage
     const int pid = pid_s[warp + i * kWarps];
     const uint32_t bar = smem_u32(&my_bars[i % kStages]);
-    if (pid < 0) {
+    if (pid < 0 || pid >= p.num_pages) {
+      record_error(OSCAR_DEVERR_PAGE_ID);
       mbar_arrive(bar);
       return;
     }
@@ -297,9 +298,16 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
       bq[nt][ks][0] = qw[nt * 16 + ks * 2];
       bq[nt][ks][1] = qw[nt * 16 + ks * 2 + 1];
     }
-    F[nt] = __uint_as_float(qw[32 + 3 * nt]);
-#pragma unroll
-    for (int gg = 0; gg < NG; ++gg) qs[nt][gg] = __uint_as_float(qw[32 + 3 * nt + 1 + gg]);
+    F[nt] = __uint_as_float(qw[32 + 5 * nt]);
+    // group sums from the four 32-column block sums
+    const float c0 = __uint_as_float(qw[33 + 5 * nt]), c1 = __uint_as_float(qw[34 + 5 * nt]);
+    const float c2 = __uint_as_float(qw[35 + 5 * nt]), c3 = __uint_as_float(qw[36 + 5 * nt]);
+    if (NG == 2) {
+      qs[nt][0] = c0 + c1;
+      qs[nt][NG - 1] = c2 + c3;
+    } else {
+      qs[nt][0] = (c0 + c1) + (c2 + c3);
+    }
   }
 
   // ---- main loop over this warp's pages ----
@@ -328,7 +336,7 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
     const uint8_t* st = my_stages + stage * kStageBytes;
     const int jpage = warp + i * kWarps;
     const int pos_base = (pg0 + jpage) * kPageSize;
-    const bool page_ok = pid_s[jpage] >= 0;
+    const bool page_ok = pid_s[jpage] >= 0 && pid_s[jpage] < p.num_pages;
     if (page_ok && pos_base >= r0 && pos_base + kPageSize <= r1) {
       int2_page<NT, NG, true>(st, g, t, true, true, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
     } else {
