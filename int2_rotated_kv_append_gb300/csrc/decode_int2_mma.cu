@@ -77,35 +77,48 @@ __device__ __forceinline__ uint32_t extract_pair(uint32_t w, uint32_t w_shr10) {
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
+// Shared-memory load at a 32-bit shared address (the stage was filled by a bulk
+// copy whose mbarrier phase the caller has already observed).
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float2 lds_h2f(uint32_t addr) {
+  const uint32_t v = lds32(addr);
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
 // One 16-token page of one warp: QK on tensor cores, online softmax, PV on
 // tensor cores.  `st` is the page's stage in shared memory.  FULL: every token
 // of the page is in range (no per-token masking); otherwise v0 / v1 say whether
 // this thread's tokens g and g + 8 are.
 template <int NT, int NG, bool FULL>
-__device__ __forceinline__ void int2_page(const uint8_t* st, int g, int t, bool v0, bool v1, uint32_t vsel,
+__device__ __forceinline__ void int2_page(uint32_t st, int g, int t, bool v0, bool v1, uint32_t vsel,
                                           int src1, int src2, const uint32_t (&bq)[NT][8][2], const float (&F)[NT],
                                           const float (&qs)[NT][NG], float (&m_run)[NT], float (&l_run)[NT],
                                           float (&zacc)[NT][NG], float (&O)[NT][8][4]) {
   if (FULL) v0 = v1 = true;
   // K words t and t + 4 of tokens g and g + 8
-  const uint32_t* kp = reinterpret_cast<const uint32_t*>(st + g * 32 + 4 * t);
-  const uint32_t kw0 = kp[0], kw1 = kp[4], kw2 = kp[64], kw3 = kp[68];
+  const uint32_t kp = st + g * 32 + 4 * t;
+  const uint32_t kw0 = lds32(kp), kw1 = lds32(kp + 16), kw2 = lds32(kp + 256), kw3 = lds32(kp + 272);
   // V words g/2 and 4 + g/2 of tokens t, t + 8 (xa) and t + 4, t + 12 (xb)
-  const uint32_t* vp = reinterpret_cast<const uint32_t*>(st + 512 + t * 32 + 4 * (g >> 1));
+  const uint32_t vp = st + 512 + t * 32 + 4 * (g >> 1);
   uint32_t xa[2], xb[2];
-  xa[0] = __byte_perm(vp[0], vp[64], vsel);
-  xa[1] = __byte_perm(vp[4], vp[68], vsel);
-  xb[0] = __byte_perm(vp[32], vp[96], vsel);
-  xb[1] = __byte_perm(vp[36], vp[100], vsel);
+  xa[0] = __byte_perm(lds32(vp), lds32(vp + 256), vsel);
+  xa[1] = __byte_perm(lds32(vp + 16), lds32(vp + 272), vsel);
+  xb[0] = __byte_perm(lds32(vp + 128), lds32(vp + 384), vsel);
+  xb[1] = __byte_perm(lds32(vp + 144), lds32(vp + 400), vsel);
   // (scale, zero) of K and V for tokens g and g + 8
-  const __half2* sp = reinterpret_cast<const __half2*>(st + kCodeBytes) + g * NG;
+  const uint32_t sp = st + kCodeBytes + g * NG * 4;
   float2 k0[NG], k1[NG], w0[NG], w1[NG];
 #pragma unroll
   for (int gg = 0; gg < NG; ++gg) {
-    k0[gg] = __half22float2(sp[gg]);
-    k1[gg] = __half22float2(sp[8 * NG + gg]);
-    w0[gg] = __half22float2(sp[16 * NG + gg]);
-    w1[gg] = __half22float2(sp[24 * NG + gg]);
+    k0[gg] = lds_h2f(sp + 4 * gg);
+    k1[gg] = lds_h2f(sp + 32 * NG + 4 * gg);
+    w0[gg] = lds_h2f(sp + 64 * NG + 4 * gg);
+    w1[gg] = lds_h2f(sp + 96 * NG + 4 * gg);
   }
 
   float acc[NT][NG][4];
@@ -325,6 +338,7 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
   }
   const uint32_t vsel = (2 * (g & 1)) | ((2 * (g & 1) + 1) << 4) | ((4 + 2 * (g & 1)) << 8) | ((5 + 2 * (g & 1)) << 12);
   const int src1 = 4 * t + (g >> 1), src2 = src1 + 16;
+  const uint32_t stage_base = smem_u32(my_stages);
   int stage = 0;
   uint32_t phase = 0;
   int i = 0;
@@ -333,7 +347,7 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
       aborted = true;
       break;
     }
-    const uint8_t* st = my_stages + stage * kStageBytes;
+    const uint32_t st = stage_base + stage * kStageBytes;
     const int jpage = warp + i * kWarps;
     const int pos_base = (pg0 + jpage) * kPageSize;
     const bool page_ok = pid_s[jpage] >= 0 && pid_s[jpage] < p.num_pages;
