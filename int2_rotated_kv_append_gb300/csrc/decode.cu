@@ -87,6 +87,7 @@ Params base_params(const oscar_dims_t* d, int B, int max_seq_len, const Plan& pl
   p.n_paged = plan.n_paged;
   p.n_dense = plan.n_dense;
   p.ns = plan.ns;
+  p.mma = plan.mma;
   p.merge_stage = static_cast<size_t>(plan.ns) * d->head_dim * 4 <= kMergeStageMax ? 1 : 0;
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(d->head_dim));
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -124,7 +125,8 @@ extern "C" oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, 
     return OSCAR_ERR_INVALID_ARG;
   if ((sink_len > 0 && !bf16_sink) || (window_len > 0 && !bf16_window)) return OSCAR_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return OSCAR_ERR_INVALID_ARG;
-  if (misaligned16(R_k) || misaligned16(R_v) || misaligned16(int2_pages) || misaligned16(scale_zero_pages))
+  if (misaligned16(R_k) || misaligned16(R_v) || misaligned16(int2_pages) || misaligned16(scale_zero_pages) ||
+      misaligned16(bf16_sink) || misaligned16(bf16_window))
     return OSCAR_ERR_INVALID_ARG;
   Plan plan;
   if (!make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, split_ctas_per_sm(dims, kMixed), &plan))

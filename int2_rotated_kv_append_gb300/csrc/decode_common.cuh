@@ -27,11 +27,15 @@ constexpr int kMergeThreads = 512;
 
 enum Mode { kMixed = 0, kBf16Paged = 1 };
 
+constexpr int kDenseMmaPages = 8;  // 16-row sink/window pages per dense split of the tensor-core kernel
+constexpr int kMmaMaxPps = 256;    // largest split the tensor-core kernels stage page ids for
+
 struct Plan {
   int pps = 0;         // pages per INT2 (or BF16-paged) split
   int n_paged = 0;     // splits over the paged pool
   int n_dense = 0;     // splits over the BF16 sink/window buffers
   int ns = 0;          // n_paged + n_dense
+  int mma = 0;         // 1: the tensor-core split kernel runs (dense splits of kDenseMmaPages pages)
   size_t off_qrot = 0, off_qfrag = 0, off_po = 0, off_pml = 0, total = 0;
 };
 
@@ -40,6 +44,7 @@ struct Params {
   int S, W, pps, n_paged, n_dense, ns;
   float scale_log2;
   int merge_stage;  // 1: the merge kernel stages the split partials in shared memory
+  int mma;          // 1: tensor-core split kernel (INT2 mode: head_dim 128, group 64 or 128)
   const __nv_bfloat16* q;
   const float* R_k;
   const float* R_v;
@@ -93,16 +98,30 @@ __device__ __forceinline__ void grid_dep_launch_dependents() { asm volatile("gri
 
 namespace {  // internal linkage in every unit that includes this header
 
+// Number of sink/window splits: the tensor-core kernel takes kDenseMmaPages
+// 16-row pages per split (sink and window buffers paged separately), the
+// CUDA-core body kBf16Chunk positions.
+int dense_splits(int S, int W, int max_seq_len, bool mma) {
+  if (mma) {
+    const int pages = (S + kPageSize - 1) / kPageSize + (W + kPageSize - 1) / kPageSize;
+    return (pages + kDenseMmaPages - 1) / kDenseMmaPages;
+  }
+  const int dense = S + W < max_seq_len ? S + W : max_seq_len;
+  return (dense + kBf16Chunk - 1) / kBf16Chunk;
+}
+
 // Split plan.  With pages_per_split == 0 the split size is chosen so that the
 // paged splits of the whole batch fill about one wave of resident CTAs
 // (ctas_per_sm x SMs, the sink/window splits counted), 4..64 pages per split.
+// The tensor-core split kernels cover head_dim 128 (INT2: group 64 or 128) and
+// splits of at most kMmaMaxPps pages.
 bool make_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req, int S, int W, Mode mode, int ctas_per_sm,
                Plan* p) {
   if (B < 0 || max_seq_len < 0 || pps_req < 0 || S < 0 || W < 0) return false;
   if (max_seq_len > d->max_pages_per_seq * kPageSize) return false;
   const int max_pages = (max_seq_len + kPageSize - 1) / kPageSize;
-  const int dense = mode == kMixed ? (S + W < max_seq_len ? S + W : max_seq_len) : 0;
-  p->n_dense = (dense + kBf16Chunk - 1) / kBf16Chunk;
+  const bool shape_mma = d->head_dim == 128 && (mode == kBf16Paged || d->group_size == 64 || d->group_size == 128);
+  p->n_dense = mode == kMixed ? dense_splits(S, W, max_seq_len, shape_mma) : 0;
   int pps = pps_req;
   if (pps == 0) {
     const long long units = static_cast<long long>(B) * d->num_kv_heads;
@@ -114,6 +133,8 @@ bool make_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req, int S
     if (want > 64) want = 64;
     pps = static_cast<int>(want);
   }
+  p->mma = shape_mma && pps <= kMmaMaxPps ? 1 : 0;
+  if (mode == kMixed && !p->mma) p->n_dense = dense_splits(S, W, max_seq_len, false);
   p->pps = pps;
   p->n_paged = max_pages == 0 ? 0 : (max_pages + pps - 1) / pps;
   p->ns = p->n_paged + p->n_dense;
@@ -575,8 +596,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
     const int c = tid % D, sg = tid / D;
     const int n_rot = kRot ? p.n_paged : 0;
     float a_rot = 0.f, a_plain = 0.f;
-    for (int s = sg; s < n_rot; s += kMG) a_rot = fmaf(wts[s], src[static_cast<size_t>(s) * D + c], a_rot);
-    for (int s = n_rot + sg; s < ns; s += kMG) a_plain = fmaf(wts[s], src[static_cast<size_t>(s) * D + c], a_plain);
+    // empty splits (weight 0) wrote only (m, l): their outputs are never read
+    for (int s = sg; s < n_rot; s += kMG) {
+      const float w = wts[s];
+      if (w != 0.f) a_rot = fmaf(w, src[static_cast<size_t>(s) * D + c], a_rot);
+    }
+    for (int s = n_rot + sg; s < ns; s += kMG) {
+      const float w = wts[s];
+      if (w != 0.f) a_plain = fmaf(w, src[static_cast<size_t>(s) * D + c], a_plain);
+    }
     red2[sg][c] = a_rot;
     red3[sg][c] = a_plain;
   }

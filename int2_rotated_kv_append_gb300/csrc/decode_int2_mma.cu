@@ -32,7 +32,7 @@
 // CTA writes one (max, sum, output) partial per query head.
 #include <mutex>
 
-#include "decode_common.cuh"
+#include "bf16_page.cuh"
 
 namespace oscar_dec {
 namespace {
@@ -42,14 +42,17 @@ constexpr int kWarps = 4;
 constexpr int kStages = 6;               // pages in flight per warp
 constexpr int kCodeBytes = 2 * 16 * 32;  // K then V codes of one (page, KV head)
 constexpr int kMaxPps = 256;             // page ids of one split staged in shared memory
+constexpr int kDenseStage = bf16pg::kStageBytes;  // one BF16 sink/window page per warp
 
 template <int NG>
 struct Geo {
   static constexpr int kSzBytes = 2 * 16 * NG * 2 * 2;  // K then V fp16 (scale, zero) of 16 tokens
   static constexpr int kStageBytes = kCodeBytes + kSzBytes;
-  // stages | QK fragments of the 32 lanes | mbarriers (stages + fragments) | page ids
-  static constexpr size_t kPagedSmem = static_cast<size_t>(kWarps) * kStages * kStageBytes + kQfragBytes +
-                                       (kWarps * kStages + 1) * 8 + kMaxPps * 4;
+  // page stages (or one BF16 stage per warp) | mbarriers | page ids
+  static constexpr size_t kStageArea = static_cast<size_t>(kWarps) * kStages * kStageBytes > kWarps * kDenseStage
+                                           ? static_cast<size_t>(kWarps) * kStages * kStageBytes
+                                           : static_cast<size_t>(kWarps) * kDenseStage;
+  static constexpr size_t kPagedSmem = kStageArea + kWarps * kStages * 8 + kMaxPps * 4;
   static constexpr size_t kSmem = kPagedSmem > split_body_smem(kD) ? kPagedSmem : split_body_smem(kD);
 };
 
@@ -218,14 +221,142 @@ __device__ __forceinline__ void int2_page(uint32_t st, int g, int t, bool v0, bo
   }
 }
 
+// ---- BF16 sink / window splits -------------------------------------------------
+
+constexpr int kDensePagesPerCta = 8;  // 16-row sink/window pages per CTA (2 per warp)
+
+// Dense split d of (b, h): the BF16 sink and recent-window rows on tensor cores,
+// unrotated (the query is q itself).  The rows of (b, K|V, h) form 16-row pages:
+// sink pages cover positions [16k, 16k + 16), window pages ring slots
+// [16k', 16k' + 16); page k < ceil(S/16) is a sink page.  A sink row is attended
+// when its position is below min(S, L); window slot r holds position
+// L - 1 - ((L - 1 - r) mod W), attended when that position is at least S (the
+// sink wins on overlap).  Rows that are not attended are not read: the warp
+// zeroes them in shared memory so that p = 0 never meets stale bits.
+template <int NT>
+__device__ __forceinline__ void dense_split(const Params& p, int d, int h, int b, uint8_t* smem) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int gqa = p.gqa;
+  const int s = p.n_paged + d;
+  const size_t bh0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * gqa;
+  grid_dep_launch_dependents();
+  const int L = clamp_len(p, b);
+  const int nsp = (p.S + kPageSize - 1) / kPageSize, nwp = (p.W + kPageSize - 1) / kPageSize;
+  const int first = d * kDensePagesPerCta;
+  const int cnt = max(0, min(kDensePagesPerCta, nsp + nwp - first));
+  const int sink_end = min(p.S, L);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kDenseStage);
+  if (lane == 0) mbar_init(smem_u32(&bars[warp]), 1);
+  mbar_init_fence();
+  __syncthreads();
+
+  const int n_my = cnt > warp ? (cnt - warp + kWarps - 1) / kWarps : 0;
+  const uint32_t st = smem_u32(smem + warp * kDenseStage);
+  const uint32_t bar = smem_u32(&bars[warp]);
+  const int kv = lane >> 4, r = lane & 15;  // lane r: K row r (r < 16) or V row r - 16
+  const uint32_t dst = st + bf16pg::stage_row(lane) * bf16pg::kRowPitch;
+  // Whole warp: bring dense page `i` of this warp into the stage; returns the
+  // mask of attended rows (bit r for token r).
+  auto issue = [&](int i) -> uint32_t {
+    const int k = first + warp + i * kWarps;
+    const __nv_bfloat16* src = nullptr;
+    if (k < nsp) {
+      const int pos = k * kPageSize + r;
+      if (pos < sink_end)
+        src = p.sink + (((static_cast<size_t>(b) * 2 + kv) * p.H + h) * p.S + pos) * kD;
+    } else {
+      const int slot = (k - nsp) * kPageSize + r;
+      if (slot < p.W && L > 0) {
+        int back = (L - 1 - slot) % p.W;
+        if (back < 0) back += p.W;
+        if (L - 1 - back >= p.S) src = p.win + (((static_cast<size_t>(b) * 2 + kv) * p.H + h) * p.W + slot) * kD;
+      }
+    }
+    const uint32_t mask = __ballot_sync(0xffffffffu, src != nullptr);
+    if (src == nullptr) {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int c = 0; c < bf16pg::kRowBytes / 16; ++c)
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16 * c), "r"(z.x), "r"(z.y), "r"(z.z),
+                     "r"(z.w)
+                     : "memory");
+    }
+    // this lane's generic writes (zeros, earlier reads) before its next bulk copy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t bytes = static_cast<uint32_t>(__popc(mask)) * bf16pg::kRowBytes;
+      if (bytes) mbar_arrive_expect_tx(bar, bytes);
+      else mbar_arrive(bar);
+    }
+    __syncwarp();
+    if (src != nullptr) bulk_g2s(dst, src, bf16pg::kRowBytes, bar);
+    return mask & 0xffffu;  // K rows (lanes 0..15) and V rows share the mask
+  };
+  uint32_t mask = n_my > 0 ? issue(0) : 0u;
+
+  uint32_t bq[NT][8][2];
+  bf16pg::build_bq<NT>(p.q + bh0 * kD, p.scale_log2, gqa, g, t, bq);
+  float m_run[NT], l_run[NT], O[NT][8][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m_run[nt] = -INFINITY;
+    l_run[nt] = 0.f;
+#pragma unroll
+    for (int mi = 0; mi < 8; ++mi)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) O[nt][mi][c] = 0.f;
+  }
+  const bf16pg::LaneOffsets lo = bf16pg::lane_offsets(lane);
+  bool aborted = false;
+  int i = 0;
+  for (; i < n_my; ++i) {
+    if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar, i & 1))) {
+      aborted = true;
+      break;
+    }
+    __syncwarp();  // zeroed rows of other lanes are visible
+    bf16pg::page<NT>(st, lo, g, (mask >> g) & 1u, (mask >> (g + 8)) & 1u, bq, m_run, l_run, O);
+    __syncwarp();
+    if (i + 1 < n_my) mask = issue(i + 1);
+  }
+  if (aborted) {
+    if (lane == 0) record_error(OSCAR_DEVERR_TIMEOUT);
+    // the one copy in flight (page i) may still land: wait for it (bounded) before
+    // the stage area is reused
+    mbar_wait_bounded(bar, i & 1);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m_run[nt] = -INFINITY;
+      l_run[nt] = 0.f;
+#pragma unroll
+      for (int mi = 0; mi < 8; ++mi)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) O[nt][mi][c] = 0.f;
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], off);
+  __syncthreads();
+  float* mw = reinterpret_cast<float*>(smem);
+  float* lw = mw + kWarps * kMaxGqa;
+  float* ow = lw + kWarps * kMaxGqa;
+  bf16pg::store_warp<NT>(O, m_run, l_run, mw, lw, ow, warp, g, t, gqa);
+  __syncthreads();
+  merge_warps_store<kWarps, kD, kWarps * 32>(p, mw, lw, ow, s, bh0, tid);
+  grid_dep_wait();  // keeps completion ordered after the q-rotation kernel
+}
+
 // ---- the kernel --------------------------------------------------------------
 
 template <int NT, int NG>
-__global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
+__global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_kernel(Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   if (s >= p.n_paged) {
-    split_body<kD, kMixed>(p, s, h, b, reinterpret_cast<float*>(smem));
+    dense_split<NT>(p, s - p.n_paged, h, b, smem);
     return;
   }
   constexpr int kStageBytes = Geo<NG>::kStageBytes;
@@ -234,8 +365,8 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
   const int gqa = p.gqa;
   // Page ids of the whole split are loaded together with the sequence length (they
   // do not depend on it); only the pages in range are validated and used.
-  uint64_t* bars0 = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kStageBytes + kQfragBytes);
-  int* pid_all = reinterpret_cast<int*>(bars0 + kWarps * kStages + 1);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo<NG>::kStageArea);
+  int* pid_all = reinterpret_cast<int*>(bars + kWarps * kStages);
   const int sp0 = s * p.pps;
   const int spn = max(0, min(p.pps, p.max_pages - sp0));
   for (int k = tid; k < spn; k += kWarps * 32)
@@ -246,27 +377,22 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
   const int r0 = max(lo_pos, p.S), r1 = min(lo_pos + p.pps * kPageSize, win_begin);
   const size_t bh0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * gqa;
 
-  if (r1 <= r0) {  // nothing of the bulk falls in this split
+  if (r1 <= r0) {  // nothing of the bulk falls in this split: an empty partial (the merge skips it)
     grid_dep_launch_dependents();
-    for (int i = tid; i < gqa * kD; i += kWarps * 32)
-      p.part_o[((bh0 + i / kD) * p.ns + s) * kD + i % kD] = 0.f;
     if (tid < gqa) {
       p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 0] = -INFINITY;
       p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 1] = 0.f;
     }
+    grid_dep_wait();  // keeps completion ordered after the q-rotation kernel
     return;
   }
   const int pg0 = r0 / kPageSize;
   const int npg = (r1 - 1) / kPageSize + 1 - pg0;
 
   uint8_t* stages = smem;
-  uint32_t* qbuf = reinterpret_cast<uint32_t*>(smem + kWarps * kStages * kStageBytes);
-  uint64_t* bars = bars0;
-  uint64_t* qbar = bars + kWarps * kStages;
   const int* pid_s = pid_all + (pg0 - sp0);  // page ids from the split's first page in range
   if (lane == 0)
     for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp * kStages + i]), 1);
-  if (tid == 0) mbar_init(smem_u32(qbar), 1);
   mbar_init_fence();
   __syncthreads();
 
@@ -290,38 +416,47 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
   if (lane == 0)
     for (int i = 0; i < n_my && i < kStages; ++i) issue(i);
   grid_dep_launch_dependents();
-  grid_dep_wait();  // q_rot comes from the preceding kernel; the page copies above do not need it
-  if (tid == 0) {
-    mbar_arrive_expect_tx(smem_u32(qbar), kQfragBytes);
-    bulk_g2s(smem_u32(qbuf), p.qfrag + (static_cast<size_t>(b) * p.H + h) * (32 * kQfragWords), kQfragBytes,
-             smem_u32(qbar));
-  }
-  bool aborted = __any_sync(0xffffffffu, !mbar_wait_bounded(smem_u32(qbar), 0));
+  grid_dep_wait();  // the QK fragments come from the q-rotation kernel; the page copies above do not need them
 
   // ---- query side: this lane's QK B-fragments and per-query factors ----
-  // (built by the q-rotation kernel).  Per n-tile nt the lane's C columns belong
-  // to query 4*nt + t and its B column to query 4*nt + (g >> 1), part g & 1.
-  const uint32_t* qw = qbuf + lane * kQfragWords;
-  float F[NT], qs[NT][NG];
+  // (built by the q-rotation kernel, kQfragWords words per lane).  Per n-tile nt
+  // the lane's C columns belong to query 4*nt + t and its B column to query
+  // 4*nt + (g >> 1), part g & 1.
+  const uint4* qw4 = reinterpret_cast<const uint4*>(p.qfrag + ((static_cast<size_t>(b) * p.H + h) * 32 + lane) * kQfragWords);
   uint32_t bq[NT][8][2];
+  float F[NT], qs[NT][NG];
+  {
+    uint4 v[4 * NT], f[3];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+    for (int k = 0; k < 4 * NT; ++k) v[k] = __ldcg(qw4 + k);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      bq[nt][ks][0] = qw[nt * 16 + ks * 2];
-      bq[nt][ks][1] = qw[nt * 16 + ks * 2 + 1];
-    }
-    F[nt] = __uint_as_float(qw[32 + 5 * nt]);
-    // group sums from the four 32-column block sums
-    const float c0 = __uint_as_float(qw[33 + 5 * nt]), c1 = __uint_as_float(qw[34 + 5 * nt]);
-    const float c2 = __uint_as_float(qw[35 + 5 * nt]), c3 = __uint_as_float(qw[36 + 5 * nt]);
-    if (NG == 2) {
-      qs[nt][0] = c0 + c1;
-      qs[nt][NG - 1] = c2 + c3;
-    } else {
-      qs[nt][0] = (c0 + c1) + (c2 + c3);
+    for (int k = 0; k < 3; ++k) f[k] = __ldcg(qw4 + 8 + k);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        bq[nt][2 * k][0] = v[4 * nt + k].x;
+        bq[nt][2 * k][1] = v[4 * nt + k].y;
+        bq[nt][2 * k + 1][0] = v[4 * nt + k].z;
+        bq[nt][2 * k + 1][1] = v[4 * nt + k].w;
+      }
+    const uint32_t fw[12] = {f[0].x, f[0].y, f[0].z, f[0].w, f[1].x, f[1].y,
+                             f[1].z, f[1].w, f[2].x, f[2].y, f[2].z, f[2].w};
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      F[nt] = __uint_as_float(fw[5 * nt]);
+      // group sums from the four 32-column block sums
+      const float c0 = __uint_as_float(fw[5 * nt + 1]), c1 = __uint_as_float(fw[5 * nt + 2]);
+      const float c2 = __uint_as_float(fw[5 * nt + 3]), c3 = __uint_as_float(fw[5 * nt + 4]);
+      if (NG == 2) {
+        qs[nt][0] = c0 + c1;
+        qs[nt][NG - 1] = c2 + c3;
+      } else {
+        qs[nt][0] = (c0 + c1) + (c2 + c3);
+      }
     }
   }
+  bool aborted = false;
 
   // ---- main loop over this warp's pages ----
   float m_run[NT], l_run[NT], zacc[NT][NG], O[NT][8][4];
@@ -421,35 +556,7 @@ __global__ void __launch_bounds__(kWarps * 32) int2_mma_split_kernel(Params p) {
     }
   }
   __syncthreads();
-  for (int idx = tid; idx < gqa * kD; idx += kWarps * 32) {
-    const int qi = idx / kD, ch = idx % kD;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * kMaxGqa + qi]);
-    float o = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mwq = mw[w * kMaxGqa + qi];
-        if (mwq != -INFINITY) o += fast_exp2(mwq - M) * ow[(w * kMaxGqa + qi) * kD + ch];
-      }
-    }
-    p.part_o[((bh0 + qi) * p.ns + s) * kD + ch] = o;
-  }
-  if (tid < gqa) {
-    float M = -INFINITY, l = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * kMaxGqa + tid]);
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mwq = mw[w * kMaxGqa + tid];
-        if (mwq != -INFINITY) l += fast_exp2(mwq - M) * lw[w * kMaxGqa + tid];
-      }
-    }
-    p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 0] = M;
-    p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 1] = l;
-  }
+  merge_warps_store<kWarps, kD, kWarps * 32>(p, mw, lw, ow, s, bh0, tid);
 }
 
 template <int NT, int NG>
@@ -486,7 +593,7 @@ int int2_mma_ctas_per_sm(int gqa, int G) {
 }
 
 bool int2_mma_supported(const Params& p) {
-  return p.D == kD && (p.G == 64 || p.G == 128) && p.gqa >= 1 && p.gqa <= 8 && p.pps <= kMaxPps;
+  return p.mma != 0 && p.D == kD && (p.G == 64 || p.G == 128) && p.gqa >= 1 && p.gqa <= 8 && p.pps <= kMaxPps;
 }
 
 cudaError_t int2_mma_split(const Params& p, cudaStream_t stream) {

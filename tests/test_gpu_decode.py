@@ -129,3 +129,28 @@ def test_decode_seq_len_over_bound_is_flagged():
     ok.oscar_device_errors(reset=True)
     cache.decode(w.q.cuda(), seq_lens=torch.tensor([150], dtype=torch.int32, device="cuda"), max_seq_len=100)
     assert ok.oscar_device_errors(reset=True) & ok.OSCAR_DEVERR_SEQ_LEN
+
+
+def test_decode_unattended_bf16_rows_never_read():
+    # Sink rows at or past min(S, L) and window slots whose position is below S
+    # (or does not exist yet) hold NaN bits: they must not reach the output.
+    S, W = 24, 40
+    lens = [3, 30, 50, 64, 200]
+    w = synth.make_workload(num_q_heads=8, num_kv_heads=2, head_dim=128, group_size=64, sink_len=S, window_len=W,
+                            seq_lens=lens, seed=21)
+    cache = _built(w)
+    nan = torch.tensor(0x7FC0, dtype=torch.int16).view(torch.bfloat16)
+    sink, win = cache.sink.clone(), cache.window.clone()
+    for b, L in enumerate(lens):
+        for p in range(S):
+            if p >= min(S, L):
+                sink[b, :, :, p, :] = nan
+        for r in range(W):
+            back = (L - 1 - r) % W
+            pos = L - 1 - back
+            if L == 0 or pos < S:
+                win[b, :, :, r, :] = nan
+    cache.sink, cache.window = sink, win
+    out = cache.decode(w.q.cuda())
+    assert torch.isfinite(out).all()
+    compare_decode(out, oracle_decode_on_gpu_cache(w, cache))
