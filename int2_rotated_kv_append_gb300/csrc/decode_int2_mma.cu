@@ -93,45 +93,57 @@ __device__ __forceinline__ float2 lds_h2f(uint32_t addr) {
   return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
 
-// One 16-token page of one warp: QK on tensor cores, online softmax, PV on
-// tensor cores.  `st` is the page's stage in shared memory.  FULL: every token
-// of the page is in range (no per-token masking); otherwise v0 / v1 say whether
-// this thread's tokens g and g + 8 are.
-template <int NT, int NG, bool FULL>
-__device__ __forceinline__ void int2_page(uint32_t st, int g, int t, bool v0, bool v1, uint32_t vsel,
-                                          int src1, int src2, const uint32_t (&bq)[NT][8][2], const float (&F)[NT],
-                                          const float (&qs)[NT][NG], float (&m_run)[NT], float (&l_run)[NT],
-                                          float (&zacc)[NT][NG], float (&O)[NT][8][4]) {
-  if (FULL) v0 = v1 = true;
-  // K words t and t + 4 of tokens g and g + 8
-  const uint32_t kp = st + g * 32 + 4 * t;
-  const uint32_t kw0 = lds32(kp), kw1 = lds32(kp + 16), kw2 = lds32(kp + 256), kw3 = lds32(kp + 272);
-  // V words g/2 and 4 + g/2 of tokens t, t + 8 (xa) and t + 4, t + 12 (xb)
-  const uint32_t vp = st + 512 + t * 32 + 4 * (g >> 1);
-  uint32_t xa[2], xb[2];
-  xa[0] = __byte_perm(lds32(vp), lds32(vp + 256), vsel);
-  xa[1] = __byte_perm(lds32(vp + 16), lds32(vp + 272), vsel);
-  xb[0] = __byte_perm(lds32(vp + 128), lds32(vp + 384), vsel);
-  xb[1] = __byte_perm(lds32(vp + 144), lds32(vp + 400), vsel);
-  // (scale, zero) of K and V for tokens g and g + 8
-  const uint32_t sp = st + kCodeBytes + g * NG * 4;
-  float2 k0[NG], k1[NG], w0[NG], w1[NG];
+// NP (1 or 2) 16-token pages of one warp: QK on tensor cores, online softmax
+// (one running maximum update for all NP pages), PV on tensor cores.  With two
+// pages the two QK chains and the two PV chains are independent, which hides
+// tensor-core and shared-memory latency.  st[k] is page k's stage in shared
+// memory.  FULL: every token of the pages is in range (no per-token masking);
+// otherwise v0[k] / v1[k] say whether this thread's tokens g and g + 8 of page k
+// are.
+template <int NT, int NG, int NP, bool FULL>
+__device__ __forceinline__ void int2_pages(const uint32_t (&st)[NP], int g, int t, const bool (&v0)[NP],
+                                           const bool (&v1)[NP], uint32_t vsel, int src1, int src2,
+                                           const uint32_t (&bq)[NT][8][2], const float (&F)[NT],
+                                           const float (&qs)[NT][NG], float (&m_run)[NT], float (&l_run)[NT],
+                                           float (&zacc)[NT][NG], float (&O)[NT][8][4]) {
+  // K words t and t + 4 of tokens g and g + 8; V words g/2 and 4 + g/2 of tokens
+  // t, t + 8 (xa) and t + 4, t + 12 (xb); (scale, zero) of K and V for tokens g, g + 8
+  uint32_t kw[NP][4], xa[NP][2], xb[NP][2];
+  float2 k0[NP][NG], k1[NP][NG], w0[NP][NG], w1[NP][NG];
 #pragma unroll
-  for (int gg = 0; gg < NG; ++gg) {
-    k0[gg] = lds_h2f(sp + 4 * gg);
-    k1[gg] = lds_h2f(sp + 32 * NG + 4 * gg);
-    w0[gg] = lds_h2f(sp + 64 * NG + 4 * gg);
-    w1[gg] = lds_h2f(sp + 96 * NG + 4 * gg);
+  for (int pg = 0; pg < NP; ++pg) {
+    const uint32_t kp = st[pg] + g * 32 + 4 * t;
+    kw[pg][0] = lds32(kp);
+    kw[pg][1] = lds32(kp + 16);
+    kw[pg][2] = lds32(kp + 256);
+    kw[pg][3] = lds32(kp + 272);
+    const uint32_t vp = st[pg] + 512 + t * 32 + 4 * (g >> 1);
+    xa[pg][0] = __byte_perm(lds32(vp), lds32(vp + 256), vsel);
+    xa[pg][1] = __byte_perm(lds32(vp + 16), lds32(vp + 272), vsel);
+    xb[pg][0] = __byte_perm(lds32(vp + 128), lds32(vp + 384), vsel);
+    xb[pg][1] = __byte_perm(lds32(vp + 144), lds32(vp + 400), vsel);
+    const uint32_t sp = st[pg] + kCodeBytes + g * NG * 4;
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) {
+      k0[pg][gg] = lds_h2f(sp + 4 * gg);
+      k1[pg][gg] = lds_h2f(sp + 32 * NG + 4 * gg);
+      w0[pg][gg] = lds_h2f(sp + 64 * NG + 4 * gg);
+      w1[pg][gg] = lds_h2f(sp + 96 * NG + 4 * gg);
+    }
   }
 
-  float acc[NT][NG][4];
+  float acc[NP][NT][NG][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int pg = 0; pg < NP; ++pg)
 #pragma unroll
-    for (int gg = 0; gg < NG; ++gg)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) acc[nt][gg][c] = 0.f;
-  {
+      for (int gg = 0; gg < NG; ++gg)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[pg][nt][gg][c] = 0.f;
+#pragma unroll
+  for (int pg = 0; pg < NP; ++pg) {
+    const uint32_t kw0 = kw[pg][0], kw1 = kw[pg][1], kw2 = kw[pg][2], kw3 = kw[pg][3];
     const uint32_t kw0s = kw0 >> 10, kw1s = kw1 >> 10, kw2s = kw2 >> 10, kw3s = kw3 >> 10;
 #define OSCAR_QK_STEP(KS)                                                                         \
   {                                                                                               \
@@ -142,27 +154,33 @@ __device__ __forceinline__ void int2_page(uint32_t st, int g, int t, bool v0, bo
     const uint32_t a0 = extract_pair<j>(wa, was), a1 = extract_pair<j>(wb, wbs);                  \
     const uint32_t a2 = extract_pair<j + 1>(wa, was), a3 = extract_pair<j + 1>(wb, wbs);          \
     _Pragma("unroll") for (int nt = 0; nt < NT; ++nt)                                             \
-        mma16816(acc[nt][gg], a0, a1, a2, a3, bq[nt][KS][0], bq[nt][KS][1]);                      \
+        mma16816(acc[pg][nt][gg], a0, a1, a2, a3, bq[nt][KS][0], bq[nt][KS][1]);                  \
   }
     OSCAR_QK_STEP(0) OSCAR_QK_STEP(1) OSCAR_QK_STEP(2) OSCAR_QK_STEP(3)
     OSCAR_QK_STEP(4) OSCAR_QK_STEP(5) OSCAR_QK_STEP(6) OSCAR_QK_STEP(7)
 #undef OSCAR_QK_STEP
   }
-  const uint32_t xas[2] = {xa[0] >> 10, xa[1] >> 10}, xbs[2] = {xb[0] >> 10, xb[1] >> 10};
 
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    float sc0 = 0.f, sc1 = 0.f;
+    float sc0[NP], sc1[NP];
+    float mx = -INFINITY;
 #pragma unroll
-    for (int gg = 0; gg < NG; ++gg) {
-      sc0 = fmaf(k0[gg].x * F[nt], acc[nt][gg][0] + acc[nt][gg][1], fmaf(k0[gg].y, qs[nt][gg], sc0));
-      sc1 = fmaf(k1[gg].x * F[nt], acc[nt][gg][2] + acc[nt][gg][3], fmaf(k1[gg].y, qs[nt][gg], sc1));
+    for (int pg = 0; pg < NP; ++pg) {
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg) {
+        a0 = fmaf(k0[pg][gg].x * F[nt], acc[pg][nt][gg][0] + acc[pg][nt][gg][1], fmaf(k0[pg][gg].y, qs[nt][gg], a0));
+        a1 = fmaf(k1[pg][gg].x * F[nt], acc[pg][nt][gg][2] + acc[pg][nt][gg][3], fmaf(k1[pg][gg].y, qs[nt][gg], a1));
+      }
+      if (!FULL) {
+        a0 = v0[pg] ? a0 : -INFINITY;
+        a1 = v1[pg] ? a1 : -INFINITY;
+      }
+      sc0[pg] = a0;
+      sc1[pg] = a1;
+      mx = fmaxf(mx, fmaxf(a0, a1));
     }
-    if (!FULL) {
-      sc0 = v0 ? sc0 : -INFINITY;
-      sc1 = v1 ? sc1 : -INFINITY;
-    }
-    float mx = fmaxf(sc0, sc1);
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -178,46 +196,50 @@ __device__ __forceinline__ void int2_page(uint32_t st, int g, int t, bool v0, bo
         for (int c = 0; c < 4; ++c) O[nt][mi][c] *= alpha;
       m_run[nt] = m_new;
     }
-    float p0 = fast_exp2(sc0 - m_new), p1 = fast_exp2(sc1 - m_new);
-    if (!FULL) {
-      p0 = v0 ? p0 : 0.f;
-      p1 = v1 ? p1 : 0.f;
-    }
-    l_run[nt] += p0 + p1;
-    uint32_t bp[NG][2];
 #pragma unroll
-    for (int gg = 0; gg < NG; ++gg) {
-      float q0 = p0 * w0[gg].x, q1 = p1 * w1[gg].x;
-      float z0 = p0 * w0[gg].y, z1 = p1 * w1[gg].y;
-      if (!FULL) {  // masked tokens may hold any bits: never multiply them in
-        q0 = v0 ? q0 : 0.f;
-        q1 = v1 ? q1 : 0.f;
-        z0 = v0 ? z0 : 0.f;
-        z1 = v1 ? z1 : 0.f;
+    for (int pg = 0; pg < NP; ++pg) {
+      float p0 = fast_exp2(sc0[pg] - m_new), p1 = fast_exp2(sc1[pg] - m_new);
+      if (!FULL) {
+        p0 = v0[pg] ? p0 : 0.f;
+        p1 = v1[pg] ? p1 : 0.f;
       }
-      zacc[nt][gg] += z0 + z1;
-      const __half2 hi = __floats2half2_rn(q0, q1);
-      const float2 hf = __half22float2(hi);
-      const uint32_t xhi = h2_bits(hi), xlo = h2_bits(__floats2half2_rn(q0 - hf.x, q1 - hf.y));
-      const uint32_t h_1 = __shfl_sync(0xffffffffu, xhi, src1), l_1 = __shfl_sync(0xffffffffu, xlo, src1);
-      const uint32_t h_2 = __shfl_sync(0xffffffffu, xhi, src2), l_2 = __shfl_sync(0xffffffffu, xlo, src2);
-      bp[gg][0] = (g & 1) ? l_1 : h_1;
-      bp[gg][1] = (g & 1) ? l_2 : h_2;
-    }
-    // PV: m-tile mi covers channels 16*word + 8*(g&1) + 2*(mi&3) + {0 (row g), 1 (row g+8)},
-    // word = g/2 for mi < 4 and 4 + g/2 for mi >= 4.
+      l_run[nt] += p0 + p1;
+      uint32_t bp[NG][2];
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg) {
+        float q0 = p0 * w0[pg][gg].x, q1 = p1 * w1[pg][gg].x;
+        float z0 = p0 * w0[pg][gg].y, z1 = p1 * w1[pg][gg].y;
+        if (!FULL) {  // masked tokens may hold any bits: never multiply them in
+          q0 = v0[pg] ? q0 : 0.f;
+          q1 = v1[pg] ? q1 : 0.f;
+          z0 = v0[pg] ? z0 : 0.f;
+          z1 = v1[pg] ? z1 : 0.f;
+        }
+        zacc[nt][gg] += z0 + z1;
+        const __half2 hi = __floats2half2_rn(q0, q1);
+        const float2 hf = __half22float2(hi);
+        const uint32_t xhi = h2_bits(hi), xlo = h2_bits(__floats2half2_rn(q0 - hf.x, q1 - hf.y));
+        const uint32_t h_1 = __shfl_sync(0xffffffffu, xhi, src1), l_1 = __shfl_sync(0xffffffffu, xlo, src1);
+        const uint32_t h_2 = __shfl_sync(0xffffffffu, xhi, src2), l_2 = __shfl_sync(0xffffffffu, xlo, src2);
+        bp[gg][0] = (g & 1) ? l_1 : h_1;
+        bp[gg][1] = (g & 1) ? l_2 : h_2;
+      }
+      // PV: m-tile mi covers channels 16*word + 8*(g&1) + 2*(mi&3) + {0 (row g), 1 (row g+8)},
+      // word = g/2 for mi < 4 and 4 + g/2 for mi >= 4.
+      const uint32_t xas[2] = {xa[pg][0] >> 10, xa[pg][1] >> 10}, xbs[2] = {xb[pg][0] >> 10, xb[pg][1] >> 10};
 #define OSCAR_PV_TILE(MI)                                                                          \
   {                                                                                                \
     constexpr int hw = (MI) >> 2;                                                                  \
     constexpr int gg = (MI) * NG / 8;                                                              \
     constexpr int e = 2 * ((MI) & 3);                                                              \
-    mma16816(O[nt][MI], extract_pair<e>(xa[hw], xas[hw]), extract_pair<e + 1>(xa[hw], xas[hw]),    \
-             extract_pair<e>(xb[hw], xbs[hw]), extract_pair<e + 1>(xb[hw], xbs[hw]), bp[gg][0],     \
+    mma16816(O[nt][MI], extract_pair<e>(xa[pg][hw], xas[hw]), extract_pair<e + 1>(xa[pg][hw], xas[hw]), \
+             extract_pair<e>(xb[pg][hw], xbs[hw]), extract_pair<e + 1>(xb[pg][hw], xbs[hw]), bp[gg][0], \
              bp[gg][1]);                                                                           \
   }
-    OSCAR_PV_TILE(0) OSCAR_PV_TILE(1) OSCAR_PV_TILE(2) OSCAR_PV_TILE(3)
-    OSCAR_PV_TILE(4) OSCAR_PV_TILE(5) OSCAR_PV_TILE(6) OSCAR_PV_TILE(7)
+      OSCAR_PV_TILE(0) OSCAR_PV_TILE(1) OSCAR_PV_TILE(2) OSCAR_PV_TILE(3)
+      OSCAR_PV_TILE(4) OSCAR_PV_TILE(5) OSCAR_PV_TILE(6) OSCAR_PV_TILE(7)
 #undef OSCAR_PV_TILE
+    }
   }
 }
 
@@ -474,31 +496,51 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   const uint32_t vsel = (2 * (g & 1)) | ((2 * (g & 1) + 1) << 4) | ((4 + 2 * (g & 1)) << 8) | ((5 + 2 * (g & 1)) << 12);
   const int src1 = 4 * t + (g >> 1), src2 = src1 + 16;
   const uint32_t stage_base = smem_u32(my_stages);
-  int stage = 0;
-  uint32_t phase = 0;
   int i = 0;
-  for (; i < n_my && !aborted; ++i) {
-    if (__any_sync(0xffffffffu, !mbar_wait_bounded(smem_u32(&my_bars[stage]), phase))) {
+  // Stage of local page k: k % kStages (kStages even: a pair never wraps).
+  auto wait_page = [&](int k) {
+    return mbar_wait_bounded(smem_u32(&my_bars[k % kStages]), (k / kStages) & 1);
+  };
+  auto page_full = [&](int k) {
+    const int jpage = warp + k * kWarps;
+    const int pos_base = (pg0 + jpage) * kPageSize;
+    const int pid = pid_s[jpage];
+    return pid >= 0 && pid < p.num_pages && pos_base >= r0 && pos_base + kPageSize <= r1;
+  };
+  auto token_ok = [&](int k, int tok) {
+    const int jpage = warp + k * kWarps;
+    const int pid = pid_s[jpage];
+    const int pos = (pg0 + jpage) * kPageSize + tok;
+    return pid >= 0 && pid < p.num_pages && pos >= r0 && pos < r1;
+  };
+  for (; i + 1 < n_my; i += 2) {
+    if (__any_sync(0xffffffffu, !wait_page(i) || !wait_page(i + 1))) {
       aborted = true;
       break;
     }
-    const uint32_t st = stage_base + stage * kStageBytes;
-    const int jpage = warp + i * kWarps;
-    const int pos_base = (pg0 + jpage) * kPageSize;
-    const bool page_ok = pid_s[jpage] >= 0 && pid_s[jpage] < p.num_pages;
-    if (page_ok && pos_base >= r0 && pos_base + kPageSize <= r1) {
-      int2_page<NT, NG, true>(st, g, t, true, true, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
+    const uint32_t st2[2] = {stage_base + (i % kStages) * kStageBytes, stage_base + ((i + 1) % kStages) * kStageBytes};
+    if (page_full(i) && page_full(i + 1)) {
+      const bool t2[2] = {true, true};
+      int2_pages<NT, NG, 2, true>(st2, g, t, t2, t2, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
     } else {
-      const int pos0 = pos_base + g;
-      const bool v0 = page_ok && pos0 >= r0 && pos0 < r1;
-      const bool v1 = page_ok && pos0 + 8 >= r0 && pos0 + 8 < r1;
-      int2_page<NT, NG, false>(st, g, t, v0, v1, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
+      const bool a0[2] = {token_ok(i, g), token_ok(i + 1, g)};
+      const bool a1[2] = {token_ok(i, g + 8), token_ok(i + 1, g + 8)};
+      int2_pages<NT, NG, 2, false>(st2, g, t, a0, a1, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
     }
     __syncwarp();
-    if (lane == 0 && i + kStages < n_my) issue(i + kStages);
-    if (++stage == kStages) {
-      stage = 0;
-      phase ^= 1u;
+    if (lane == 0) {
+      if (i + kStages < n_my) issue(i + kStages);
+      if (i + 1 + kStages < n_my) issue(i + 1 + kStages);
+    }
+  }
+  if (!aborted && i < n_my) {  // odd last page
+    if (__any_sync(0xffffffffu, !wait_page(i))) {
+      aborted = true;
+    } else {
+      const uint32_t st1[1] = {stage_base + (i % kStages) * kStageBytes};
+      const bool a0[1] = {token_ok(i, g)}, a1[1] = {token_ok(i, g + 8)};
+      int2_pages<NT, NG, 1, false>(st1, g, t, a0, a1, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
+      ++i;
     }
   }
   if (aborted) {
