@@ -11,6 +11,7 @@
 // (l+1)*D/32), so a group of G channels is G*32/D consecutive lanes and the
 // group min/max is a warp-shuffle reduction.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace {
 
@@ -81,6 +82,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ R_k, const float* __restrict__ R_v,
     const float* __restrict__ clip_k, const float* __restrict__ clip_v, const int64_t* __restrict__ slots,
     uint8_t* __restrict__ codes, __half* __restrict__ sz) {
+  grid_dep_launch_dependents();  // a following q-rotation (reads neither output) may start
   constexpr int CPL = D / 32;  // channels per lane
   extern __shared__ __align__(16) float smem[];
   float* Rs = smem;           // [D][D]
@@ -153,6 +155,7 @@ __global__ void __launch_bounds__(kThreads) append_small_kernel(
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ R_k, const float* __restrict__ R_v,
     const float* __restrict__ clip_k, const float* __restrict__ clip_v, const int64_t* __restrict__ slots,
     uint8_t* __restrict__ codes, __half* __restrict__ sz) {
+  grid_dep_launch_dependents();  // a following q-rotation (reads neither output) may start
   constexpr int CPL = D / 32;
   constexpr int kWarpsA = kThreads / 32;
   constexpr int kRows = D / kWarpsA;
@@ -224,6 +227,7 @@ __global__ void __launch_bounds__(kThreads) append_small_kernel(
 __global__ void bf16_append_kernel(int64_t num_tokens, int H, int D, int num_pages,
                                    const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
                                    const int64_t* __restrict__ slots, __nv_bfloat16* __restrict__ pages) {
+  grid_dep_launch_dependents();  // a following q-rotation (reads neither output) may start
   const int chunks = D / 8;  // 16-byte chunks per row
   const int64_t total = num_tokens * H * 2 * chunks;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;

@@ -22,17 +22,37 @@ using namespace oscar_dec;
 
 template <int D, Mode MODE>
 cudaError_t merge(const Params& p, cudaStream_t stream) {
-  const size_t smem = merge_smem(D, p.ns, MODE == kMixed, p.merge_stage != 0);
+  const size_t smem = merge_smem(D, p.ns, p.merge_qpc, p.merge_stage);
   cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(merge_kernel<D, MODE>), kMergeSmemLimit);
   if (e != cudaSuccess) return e;
-  return launch_pdl(merge_kernel<D, MODE>, dim3(p.B * p.Hq), dim3(kMergeThreads), smem, stream, p);
+  const int grid = p.B * p.H * (p.gqa / p.merge_qpc);
+  // A grid of at most one CTA per SM is launched early (programmatic dependent
+  // launch) so that it is resident, with R_v staged, when the splits finish; a
+  // larger one would take SM slots from the last split CTAs and waits for them.
+  if (grid <= num_sms()) return launch_pdl(merge_kernel<D, MODE>, dim3(grid), dim3(kMergeThreads), smem, stream, p);
+  merge_kernel<D, MODE><<<grid, kMergeThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// Query heads per merge CTA and what the merge stages in shared memory (see
+// merge_kernel): all of a KV head's GQA group per CTA when the batch has at least
+// one (sequence, KV head) per SM, otherwise one query head per CTA (more CTAs),
+// with R_v and, when they fit, the partials staged.
+void merge_config(const oscar_dims_t* d, int B, int ns, Mode mode, int* qpc, int* stage) {
+  const int gqa = d->num_q_heads / d->num_kv_heads;
+  const long long units = static_cast<long long>(B) * d->num_kv_heads;
+  *qpc = units >= num_sms() && merge_smem(d->head_dim, ns, gqa, 0) <= kMergeSmemLimit ? gqa : 1;
+  *stage = 0;
+  if (units * (gqa / *qpc) <= num_sms()) {
+    if (mode == kMixed && merge_smem(d->head_dim, ns, *qpc, kStageRv) <= kMergeSmemLimit) *stage |= kStageRv;
+    if (merge_smem(d->head_dim, ns, *qpc, *stage | kStagePartials) <= kMergeSmemLimit) *stage |= kStagePartials;
+  }
 }
 
 template <int D, Mode MODE>
 cudaError_t launch(const Params& p, cudaStream_t stream) {
   if (MODE == kMixed) {
-    qrot_kernel<D><<<dim3(p.B * p.H, D / 32), kQrotThreads, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(qrot_kernel<D>, dim3(p.B * p.H, D / 32), dim3(kQrotThreads), 0, stream, p);
     if (e != cudaSuccess) return e;
   }
   const bool mma = MODE == kMixed ? int2_mma_supported(p) : bf16_mma_supported(p);
@@ -72,7 +92,8 @@ int split_ctas_per_sm(const oscar_dims_t* d, Mode mode) {
   return 4;
 }
 
-Params base_params(const oscar_dims_t* d, int B, int max_seq_len, const Plan& plan, float sm_scale, void* ws) {
+Params base_params(const oscar_dims_t* d, int B, int max_seq_len, const Plan& plan, Mode mode, float sm_scale,
+                   void* ws) {
   Params p{};
   p.B = B;
   p.Hq = d->num_q_heads;
@@ -87,8 +108,8 @@ Params base_params(const oscar_dims_t* d, int B, int max_seq_len, const Plan& pl
   p.n_paged = plan.n_paged;
   p.n_dense = plan.n_dense;
   p.ns = plan.ns;
+  merge_config(d, B, plan.ns, mode, &p.merge_qpc, &p.merge_stage);
   p.mma = plan.mma;
-  p.merge_stage = static_cast<size_t>(plan.ns) * d->head_dim * 4 <= kMergeStageMax ? 1 : 0;
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(d->head_dim));
   p.scale_log2 = scale * 1.4426950408889634f;
   char* w = static_cast<char*>(ws);
@@ -132,9 +153,9 @@ extern "C" oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, 
   if (!make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, split_ctas_per_sm(dims, kMixed), &plan))
     return OSCAR_ERR_INVALID_ARG;
   if (workspace_bytes < plan.total) return OSCAR_ERR_WORKSPACE;
-  if (merge_smem(dims->head_dim, plan.ns, true, false) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
+  if (merge_smem(dims->head_dim, plan.ns, 1, 0) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
   if (static_cast<long long>(batch) * dims->num_q_heads > 0x7fffffffLL || plan.ns > 0x7fffffff) return OSCAR_ERR_UNSUPPORTED;
-  Params p = base_params(dims, batch, max_seq_len, plan, sm_scale, workspace);
+  Params p = base_params(dims, batch, max_seq_len, plan, kMixed, sm_scale, workspace);
   p.S = sink_len;
   p.W = window_len;
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -173,8 +194,8 @@ extern "C" oscar_status_t oscar_bf16_decode(const oscar_dims_t* dims, int32_t ba
   Plan plan;
   if (!make_plan(dims, batch, max_seq_len, pages_per_split, 0, 0, kBf16Paged, split_ctas_per_sm(dims, kBf16Paged), &plan)) return OSCAR_ERR_INVALID_ARG;
   if (workspace_bytes < plan.total) return OSCAR_ERR_WORKSPACE;
-  if (merge_smem(dims->head_dim, plan.ns, false, false) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
-  Params p = base_params(dims, batch, max_seq_len, plan, sm_scale, workspace);
+  if (merge_smem(dims->head_dim, plan.ns, 1, 0) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
+  Params p = base_params(dims, batch, max_seq_len, plan, kBf16Paged, sm_scale, workspace);
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.pages = static_cast<const __nv_bfloat16*>(bf16_pages);
   p.page_table = page_table;

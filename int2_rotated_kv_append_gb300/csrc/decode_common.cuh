@@ -21,9 +21,7 @@ constexpr int kBf16Chunk = 32;   // sink/window positions per split (one softmax
 // factors (2 n-tiles x (score factor + 4 column-block sums)), 44 words per lane.
 constexpr int kQfragWords = 44;
 constexpr int kQfragBytes = 32 * kQfragWords * 4;
-constexpr size_t kMergeStageMax = 96 * 1024;    // partials staged in the merge's shared memory up to this size
-constexpr size_t kMergeSmemLimit = 180 * 1024;  // dynamic shared-memory limit set for the merge kernel
-constexpr int kMergeThreads = 512;
+constexpr size_t kMergeSmemLimit = 160 * 1024;  // dynamic shared-memory limit set for the merge kernel
 
 enum Mode { kMixed = 0, kBf16Paged = 1 };
 
@@ -43,7 +41,8 @@ struct Params {
   int B, Hq, H, D, G, gqa, num_pages, max_pages, max_seq_len;
   int S, W, pps, n_paged, n_dense, ns;
   float scale_log2;
-  int merge_stage;  // 1: the merge kernel stages the split partials in shared memory
+  int merge_qpc;    // query heads per merge CTA (divides gqa)
+  int merge_stage;  // merge kernel: kStageRv (R_v staged before the wait) | kStagePartials
   int mma;          // 1: tensor-core split kernel (INT2 mode: head_dim 128, group 64 or 128)
   const __nv_bfloat16* q;
   const float* R_k;
@@ -90,11 +89,6 @@ cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t sm
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// grid_dep_wait() blocks until the preceding kernel has completed and its
-// writes are visible (a no-op without a programmatic dependency);
-// grid_dep_launch_dependents() lets the following kernel start launching.
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 namespace {  // internal linkage in every unit that includes this header
 
@@ -220,7 +214,10 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
     p.q_rot[q0 + static_cast<size_t>(qi) * D + 32 * cb + c] = tot;
     qrb[qi][c] = tot;
   }
-  if (p.qfrag == nullptr) return;
+  if (p.qfrag == nullptr) {
+    grid_dep_wait();  // completion stays ordered after the preceding kernel
+    return;
+  }
   if constexpr (D == 128) {
   // exponents from ||q|| (one warp per query)
   for (int qi = warp; qi < gqa; qi += kQrotThreads / 32) {
@@ -277,6 +274,11 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
     }
   }
   }  // D == 128
+  // This kernel may start while the preceding kernel (for example the append of
+  // the current token) still runs: it reads only q and R_k.  It completes only
+  // after that kernel, so the split kernel, which waits for this one, sees the
+  // preceding kernel's writes.
+  grid_dep_wait();
 }
 
 // Shared memory (bytes) of split_body for head dimension D.
@@ -499,159 +501,199 @@ __global__ void __launch_bounds__(kThreads) split_kernel(Params p) {
   split_body<D, MODE>(p, blockIdx.x, blockIdx.y, blockIdx.z, dyn_smem);
 }
 
-// Log-sum-exp merge of the splits of one (b, hq), un-rotation of the INT2 part
-// by R_v^T and normalisation.  R_v[h] (mixed mode) is staged by a bulk copy
-// before the wait for the split kernel, the partials by a second bulk copy
-// after it (when they fit, merge_stage).  Dynamic shared memory:
-// merge_smem(D, ns, mixed, stage) bytes.
-constexpr size_t merge_smem(int D, int ns, bool mixed, bool stage) {
-  return (mixed ? static_cast<size_t>(D) * D * 4 : 0) + (stage ? static_cast<size_t>(ns) * D * 4 : 0) +
-         static_cast<size_t>(ns + 2) * 4 + 32;
+// Log-sum-exp merge of the split partials and, in INT2 mode, the single
+// un-rotation by R_v^T (OSCAR project card "How it works": rotate the query once,
+// un-rotate the output once):
+//   out[c] = (sum_plain w_s o_s[c] + sum_j (sum_rot w_s o_s[j]) R_v[h][c][j]) / sum_s w_s l_s,
+//   w_s = 2^(m_s - max_s m_s),
+// where the rotated partials are the INT2 splits (s < n_paged) and the plain ones
+// the BF16 sink/window splits; splits that attended nothing (m = -inf) have
+// weight 0 and their outputs are not read.  One CTA covers merge_qpc query heads
+// of one (sequence, KV head): grid B * Hkv * (gqa / merge_qpc).
+//   phase A  one warp per query: maximum, weights, denominator;
+//   phase B  thread (query, 4-channel quad, split group) sums a strided subset of
+//            the splits, then the split groups are added in order;
+//   phase C  thread (channel c, column part) dots the rotated sum with its part of
+//            row c of R_v, then the parts are added in order.
+// A small grid, launched while the splits still run, stages R_v in shared memory
+// before it waits for them (kStageRv) and the partials with one bulk copy after
+// (kStagePartials); a large grid reads both from L2.
+constexpr int kMergeThreads = 256;
+constexpr int kStageRv = 1, kStagePartials = 2;
+
+// Dynamic shared memory of the merge kernel: [R_v D x D] [partials qpc x ns x D]
+// weights [qpc][ns], denominators [8], phase B/C scratch (2 x kMergeThreads
+// float4), rotated and plain sums [qpc][D], two mbarriers.
+constexpr size_t merge_smem(int D, int ns, int qpc, int stage) {
+  return ((stage & kStageRv) ? static_cast<size_t>(D) * D * 4 : 0) +
+         ((stage & kStagePartials) ? static_cast<size_t>(qpc) * ns * D * 4 : 0) +
+         (static_cast<size_t>((qpc * ns + 3) & ~3) + 8) * 4 + 2 * kMergeThreads * 16 +
+         2 * static_cast<size_t>(qpc) * D * 4 + 16;
 }
 
 template <int D, Mode MODE>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
-  __shared__ float o_rot[D];
-  __shared__ float o_plain[D];
-  constexpr int kMG = kMergeThreads / D;  // threads per output channel
-  __shared__ float red[kMergeThreads / 32];
-  __shared__ float red2[kMG][D];
-  __shared__ float red3[kMG][D];
   extern __shared__ __align__(128) float msm[];
   constexpr bool kRot = MODE == kMixed;
-  const int ns = p.ns;
-  float* Rs = msm;                                      // [D][D] (mixed)
-  float* po_s = Rs + (kRot ? D * D : 0);                // [ns][D] (staged)
-  float* wts = po_s + (p.merge_stage ? ns * D : 0);     // [ns]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uintptr_t>(wts + ns + 2 + 1) & ~uintptr_t(7));
-  const int bh = blockIdx.x;
-  const int h = (bh % p.Hq) / p.gqa;
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  if (tid == 0) {
+  constexpr int kQuads = D / 4;
+  const int qpc = p.merge_qpc;
+  const int qch = p.gqa / qpc;
+  const int unit = blockIdx.x / qch, qc = blockIdx.x % qch;
+  const int b = unit / p.H, h = unit % p.H;
+  const size_t row0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * p.gqa + static_cast<size_t>(qc) * qpc;
+  const int ns = p.ns, np = kRot ? p.n_paged : 0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool st_rv = kRot && (p.merge_stage & kStageRv) != 0;
+  const bool st_po = (p.merge_stage & kStagePartials) != 0;
+  float* Rs = msm;                                                          // [D][D] (st_rv)
+  float* po_s = Rs + (st_rv ? D * D : 0);                                   // [qpc][ns][D] (st_po)
+  float* wts = po_s + (st_po ? static_cast<size_t>(qpc) * ns * D : 0);      // [qpc][ns]
+  float* den_s = wts + ((qpc * ns + 3) & ~3);                               // [8]
+  float4* red = reinterpret_cast<float4*>(den_s + 8);                       // [2][kMergeThreads]
+  float* o_rot = reinterpret_cast<float*>(red + 2 * kMergeThreads);         // [qpc][D]
+  float* o_plain = o_rot + qpc * D;                                         // [qpc][D]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(o_plain + qpc * D);         // [2]
+  if (tid == 0 && (st_rv || st_po)) {
     mbar_init(smem_u32(&bars[0]), 1);
     mbar_init(smem_u32(&bars[1]), 1);
     mbar_init_fence();
-    if (kRot) {
+    if (st_rv) {
       mbar_arrive_expect_tx(smem_u32(&bars[0]), D * D * 4);
       bulk_g2s(smem_u32(Rs), p.R_v + static_cast<size_t>(h) * D * D, D * D * 4, smem_u32(&bars[0]));
     }
   }
   __syncthreads();
   grid_dep_wait();  // the split partials come from the preceding kernel
-  const float* ml = p.part_ml + static_cast<size_t>(bh) * ns * 2;
-  const float* po = p.part_o + static_cast<size_t>(bh) * ns * D;
-  if (tid == 0 && p.merge_stage) {
-    mbar_arrive_expect_tx(smem_u32(&bars[1]), ns * D * 4);
-    bulk_g2s(smem_u32(po_s), po, ns * D * 4, smem_u32(&bars[1]));
+  if (tid == 0 && st_po) {
+    const uint32_t bytes = static_cast<uint32_t>(qpc) * ns * D * 4;
+    mbar_arrive_expect_tx(smem_u32(&bars[1]), bytes);
+    bulk_g2s(smem_u32(po_s), p.part_o + row0 * ns * D, bytes, smem_u32(&bars[1]));
   }
-  // M = max_s m_s, weights w_s = 2^(m_s - M), denominator sum_s w_s l_s.  Each
-  // thread loads its (m, l) pairs once (up to kMlPer of them; more splits reload).
-  constexpr int kMlPer = 1;
-  float mv[kMlPer], lv[kMlPer];
-  float M = -INFINITY;
-#pragma unroll
-  for (int k = 0; k < kMlPer; ++k) {
-    const int s = tid + k * kMergeThreads;
-    const float2 v = s < ns ? *reinterpret_cast<const float2*>(ml + 2 * s) : make_float2(-INFINITY, 0.f);
-    mv[k] = v.x;
-    lv[k] = v.y;
-    M = fmaxf(M, v.x);
-  }
-  for (int s = tid + kMlPer * kMergeThreads; s < ns; s += kMergeThreads) M = fmaxf(M, ml[2 * s]);
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if (lane == 0) red[warp] = M;
-  __syncthreads();
-  M = red[0];
-#pragma unroll
-  for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red[w]);
-  __syncthreads();
-  float den = 0.f;
-#pragma unroll
-  for (int k = 0; k < kMlPer; ++k) {
-    const int s = tid + k * kMergeThreads;
-    if (s < ns) {
-      const float w = (mv[k] == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(mv[k] - M);
-      wts[s] = w;
-      den = fmaf(w, lv[k], den);
+
+  // phase A
+  for (int qi = warp; qi < qpc; qi += kMergeThreads / 32) {
+    const float* ml = p.part_ml + (row0 + qi) * ns * 2;
+    float* wq = wts + qi * ns;
+    float M = -INFINITY;
+    for (int s = lane; s < ns; s += 32) {
+      const float m = ml[2 * s];
+      wq[s] = m;
+      M = fmaxf(M, m);
     }
-  }
-  for (int s = tid + kMlPer * kMergeThreads; s < ns; s += kMergeThreads) {
-    const float m = ml[2 * s];
-    const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(m - M);
-    wts[s] = w;
-    den = fmaf(w, ml[2 * s + 1], den);
-  }
-  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-  if (lane == 0) red[warp] = den;
-  __syncthreads();
-  den = 0.f;
 #pragma unroll
-  for (int w = 0; w < kMergeThreads / 32; ++w) den += red[w];
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float den = 0.f;
+    for (int s = lane; s < ns; s += 32) {
+      const float m = wq[s];
+      const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(m - M);
+      wq[s] = w;
+      if (w != 0.f) den = fmaf(w, ml[2 * s + 1], den);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    if (lane == 0) den_s[qi] = den;
+  }
   bool ok = true;
-  if (p.merge_stage) ok = mbar_wait_bounded(smem_u32(&bars[1]), 0);
+  if (st_po) ok = mbar_wait_bounded(smem_u32(&bars[1]), 0);
+  ok = __syncthreads_and(ok);
+
+  // phase B
+  const int items = qpc * kQuads;
+  const int sg = kMergeThreads / items;
+  if (tid < items * sg) {
+    const int item = tid % items, grp = tid / items;
+    const int qi = item / kQuads, cq = item % kQuads;
+    const float4* po = reinterpret_cast<const float4*>(st_po ? po_s + static_cast<size_t>(qi) * ns * D
+                                                             : p.part_o + (row0 + qi) * ns * D) + cq;
+    const float* wq = wts + qi * ns;
+    float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), ap = ar;
+    for (int s0 = grp; s0 < ns; s0 += 4 * sg) {
+      float w[4];
+      float4 v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int s = s0 + k * sg;
+        w[k] = s < ns ? wq[s] : 0.f;
+        v[k] = w[k] != 0.f ? po[static_cast<size_t>(s) * kQuads] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float wr = s0 + k * sg < np ? w[k] : 0.f, wp = w[k] - wr;
+        ar.x = fmaf(wr, v[k].x, ar.x); ar.y = fmaf(wr, v[k].y, ar.y);
+        ar.z = fmaf(wr, v[k].z, ar.z); ar.w = fmaf(wr, v[k].w, ar.w);
+        ap.x = fmaf(wp, v[k].x, ap.x); ap.y = fmaf(wp, v[k].y, ap.y);
+        ap.z = fmaf(wp, v[k].z, ap.z); ap.w = fmaf(wp, v[k].w, ap.w);
+      }
+    }
+    red[grp * items + item] = ar;
+    red[kMergeThreads + grp * items + item] = ap;
+  }
+  __syncthreads();
+  if (tid < items) {
+    float4 ar = red[tid], ap = red[kMergeThreads + tid];
+    for (int grp = 1; grp < sg; ++grp) {
+      const float4 x = red[grp * items + tid], y = red[kMergeThreads + grp * items + tid];
+      ar.x += x.x; ar.y += x.y; ar.z += x.z; ar.w += x.w;
+      ap.x += y.x; ap.y += y.y; ap.z += y.z; ap.w += y.w;
+    }
+    reinterpret_cast<float4*>(o_rot)[tid] = ar;  // item = qi * kQuads + cq
+    reinterpret_cast<float4*>(o_plain)[tid] = ap;
+  }
+  if (st_rv) ok = mbar_wait_bounded(smem_u32(&bars[0]), 0) && ok;
+  ok = __syncthreads_and(ok);
+
+  // phase C: thread (c, jp) visits the 4-column chunks of its part starting at
+  // chunk c mod (kJ/4), so 8 consecutive lanes read distinct shared-memory banks.
+  float* part = reinterpret_cast<float*>(red);  // [kParts][qpc][D]
+  constexpr int kParts = kMergeThreads / D;     // column parts per channel
+  constexpr int kJ = D / kParts;                // columns per part
+  constexpr int kChunks = kJ / 4;
+  if (kRot) {
+    const int c = tid % D, jp = tid / D;
+    const float4* Rrow = reinterpret_cast<const float4*>((st_rv ? Rs + static_cast<size_t>(c) * D
+                                                                 : p.R_v + (static_cast<size_t>(h) * D + c) * D) +
+                                                         jp * kJ);
+    const float4* orow = reinterpret_cast<const float4*>(o_rot + jp * kJ);
+    float acc[kMaxGqa];
+#pragma unroll
+    for (int qi = 0; qi < kMaxGqa; ++qi) acc[qi] = 0.f;
+#pragma unroll
+    for (int k0 = 0; k0 < kChunks; k0 += 8) {
+      float4 r[8];
+      int ch[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        ch[k] = (k0 + k + c) & (kChunks - 1);
+        r[k] = k0 + k < kChunks ? (st_rv ? Rrow[ch[k]] : __ldg(Rrow + ch[k])) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int qi = 0; qi < kMaxGqa; ++qi) {
+        if (qi < qpc) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            if (k0 + k < kChunks) {
+              const float4 o = orow[qi * kQuads + ch[k]];
+              acc[qi] = fmaf(o.x, r[k].x, fmaf(o.y, r[k].y, fmaf(o.z, r[k].z, fmaf(o.w, r[k].w, acc[qi]))));
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int qi = 0; qi < kMaxGqa; ++qi)
+      if (qi < qpc) part[(jp * qpc + qi) * D + c] = acc[qi];
+    __syncthreads();
+  }
   if (!ok && tid == 0) record_error(OSCAR_DEVERR_TIMEOUT);
-  const float* src = p.merge_stage ? po_s : po;
-  {
-    // thread (channel c, group sg) sums the splits s = sg, sg + kMG, ...
-    const int c = tid % D, sg = tid / D;
-    const int n_rot = kRot ? p.n_paged : 0;
-    float a_rot = 0.f, a_plain = 0.f;
-    // empty splits (weight 0) wrote only (m, l): their outputs are never read
-    for (int s = sg; s < n_rot; s += kMG) {
-      const float w = wts[s];
-      if (w != 0.f) a_rot = fmaf(w, src[static_cast<size_t>(s) * D + c], a_rot);
-    }
-    for (int s = n_rot + sg; s < ns; s += kMG) {
-      const float w = wts[s];
-      if (w != 0.f) a_plain = fmaf(w, src[static_cast<size_t>(s) * D + c], a_plain);
-    }
-    red2[sg][c] = a_rot;
-    red3[sg][c] = a_plain;
-  }
-  __syncthreads();
-  if (tid < D) {
-    float ar = 0.f, ap = 0.f;
+  for (int idx = tid; idx < qpc * D; idx += kMergeThreads) {
+    const int qi = idx / D, cc = idx % D;
+    float u = o_plain[idx];
+    if (kRot) {
 #pragma unroll
-    for (int g = 0; g < kMG; ++g) {
-      ar += red2[g][tid];
-      ap += red3[g][tid];
+      for (int jp = 0; jp < kParts; ++jp) u += part[(jp * qpc + qi) * D + cc];
     }
-    o_rot[tid] = ar;
-    o_plain[tid] = ap;
-  }
-  __syncthreads();
-  const float inv = (ok && den > 0.f) ? 1.f / den : 0.f;
-  float* out = p.out + static_cast<size_t>(bh) * D;
-  if (!kRot) {
-    if (tid < D) out[tid] = o_plain[tid] * inv;
-    return;
-  }
-  if (!__syncthreads_and(mbar_wait_bounded(smem_u32(&bars[0]), 0))) {
-    if (tid == 0) record_error(OSCAR_DEVERR_TIMEOUT);
-    if (tid < D) out[tid] = 0.f;
-    return;
-  }
-  // out[c] = (o_plain[c] + sum_j o_rot[j] R_v[h][c][j]) * inv.  Thread (c, jq) sums
-  // j over the jq-th block of D/kMG columns, visiting them in the order
-  // (c + k) mod (D/kMG) so a warp's lanes read different banks; the blocks are
-  // then added in order.
-  {
-    constexpr int kJ = D / kMG;
-    const int c = tid % D, jq = tid / D;
-    float part[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int k = 0; k < kJ; ++k) {
-      const int j = jq * kJ + ((c + k) & (kJ - 1));
-      part[k & 3] = fmaf(o_rot[j], Rs[c * D + j], part[k & 3]);
-    }
-    red2[jq][c] = (part[0] + part[1]) + (part[2] + part[3]);
-  }
-  __syncthreads();
-  if (tid < D) {
-    float u = 0.f;
-#pragma unroll
-    for (int g = 0; g < kMG; ++g) u += red2[g][tid];
-    out[tid] = (o_plain[tid] + u) * inv;
+    const float den = den_s[qi];
+    p.out[(row0 + qi) * D + cc] = (ok && den > 0.f) ? u / den : 0.f;
   }
 }
 

@@ -40,6 +40,7 @@ namespace {
 constexpr int kD = 128;
 constexpr int kWarps = 4;
 constexpr int kStages = 6;               // pages in flight per warp
+constexpr int kFirstIssue = 2;           // pages per warp requested before the query fragments
 constexpr int kCodeBytes = 2 * 16 * 32;  // K then V codes of one (page, KV head)
 constexpr int kMaxPps = 256;             // page ids of one split staged in shared memory
 constexpr int kDenseStage = bf16pg::kStageBytes;  // one BF16 sink/window page per warp
@@ -435,8 +436,11 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
     bulk_g2s(smem_u32(st), p.codes + ph * kCodeBytes, kCodeBytes, bar);
     bulk_g2s(smem_u32(st + kCodeBytes), reinterpret_cast<const uint8_t*>(p.sz) + ph * kSzBytes, kSzBytes, bar);
   };
+  // The first kFirstIssue pages of each warp are requested before the query
+  // fragments, the rest once the fragments have arrived: a request made behind
+  // every page of the grid would wait for most of the page traffic.
   if (lane == 0)
-    for (int i = 0; i < n_my && i < kStages; ++i) issue(i);
+    for (int i = 0; i < n_my && i < kFirstIssue; ++i) issue(i);
   grid_dep_launch_dependents();
   grid_dep_wait();  // the QK fragments come from the q-rotation kernel; the page copies above do not need them
 
@@ -453,6 +457,14 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
     for (int k = 0; k < 4 * NT; ++k) v[k] = __ldcg(qw4 + k);
 #pragma unroll
     for (int k = 0; k < 3; ++k) f[k] = __ldcg(qw4 + 8 + k);
+    {  // wait for the fragments, then request the remaining pages
+      uint32_t x = f[0].x ^ f[1].x ^ f[2].x;
+#pragma unroll
+      for (int k = 0; k < 4 * NT; ++k) x ^= v[k].x ^ v[k].w;
+      asm volatile("" ::"r"(x));
+      if (lane == 0)
+        for (int i = kFirstIssue; i < n_my && i < kStages; ++i) issue(i);
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll

@@ -61,6 +61,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                : "memory");
 }
 
+// Programmatic dependent launch: grid_dep_wait() blocks until the preceding
+// kernel has completed and its writes are visible (a no-op without a
+// programmatic dependency); grid_dep_launch_dependents() lets the following
+// kernel, if launched with programmatic stream serialisation, start launching.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
