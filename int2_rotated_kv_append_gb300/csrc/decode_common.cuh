@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(Params p) {
 // the BF16 sink/window splits; splits that attended nothing (m = -inf) have
 // weight 0 and their outputs are not read.  One CTA covers merge_qpc query heads
 // of one (sequence, KV head): grid B * Hkv * (gqa / merge_qpc).
-//   phase A  one warp per query: maximum, weights, denominator;
+//   phase A  one warp per query: maximum, denominator, weights;
 //   phase B  thread (query, 4-channel quad, split group) sums a strided subset of
 //            the splits, then the split groups are added in order;
 //   phase C  thread (channel c, column part) dots the rotated sum with its part of
@@ -570,27 +570,38 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
     bulk_g2s(smem_u32(po_s), p.part_o + row0 * ns * D, bytes, smem_u32(&bars[1]));
   }
 
-  // phase A
+  // phase A: one pass over (m, l) with a running maximum per lane, combined
+  // across the warp by log-sum-exp; then the weights from the staged maxima
   for (int qi = warp; qi < qpc; qi += kMergeThreads / 32) {
-    const float* ml = p.part_ml + (row0 + qi) * ns * 2;
+    const float2* ml = reinterpret_cast<const float2*>(p.part_ml + (row0 + qi) * ns * 2);
     float* wq = wts + qi * ns;
-    float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) {
-      const float m = ml[2 * s];
-      wq[s] = m;
-      M = fmaxf(M, m);
-    }
+    float M = -INFINITY, den = 0.f;
+    for (int s0 = lane; s0 < ns; s0 += 4 * 32) {
+      float2 v[4];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float den = 0.f;
-    for (int s = lane; s < ns; s += 32) {
-      const float m = wq[s];
-      const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(m - M);
-      wq[s] = w;
-      if (w != 0.f) den = fmaf(w, ml[2 * s + 1], den);
+      for (int k = 0; k < 4; ++k) v[k] = s0 + 32 * k < ns ? ml[s0 + 32 * k] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (s0 + 32 * k < ns) wq[s0 + 32 * k] = v[k].x;
+        if (v[k].x != -INFINITY) {
+          if (v[k].x > M) {
+            den = M == -INFINITY ? 0.f : den * fast_exp2(M - v[k].x);
+            M = v[k].x;
+          }
+          den = fmaf(fast_exp2(v[k].x - M), v[k].y, den);
+        }
+      }
     }
+    float Mw = M;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, off));
+    den = M == -INFINITY ? 0.f : den * fast_exp2(M - Mw);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    for (int s = lane; s < ns; s += 32) {
+      const float m = wq[s];
+      wq[s] = (m == -INFINITY || Mw == -INFINITY) ? 0.f : fast_exp2(m - Mw);
+    }
     if (lane == 0) den_s[qi] = den;
   }
   bool ok = true;
