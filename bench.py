@@ -152,6 +152,23 @@ def measured_peak_hbm():
         return 6800.0, "fallback"
 
 
+def workload_config(args, w, batch, seq_len, pps, l2_policy):
+    """The config object of the JSON line (the same for both arms)."""
+    from int2_rotated_kv_append_gb300 import synth
+    return {"workload": synth.CONFIG_NAMES[args.config] + ": decode step = append current token + "
+                        "mixed-precision paged decode",
+            "batch": batch, "seq_len": seq_len, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "sink": w.sink_len, "window": w.window_len, "group": w.group_size,
+            "page_size": 16, "pages_per_split": "auto" if pps == 0 else pps, "l2_policy": l2_policy}
+
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one oscar_decode
+# launch (q-rotation + split + merge kernels) on the batch-1 32K workload, from one
+# ncu capture of the three kernels (cold caches: the split partials are re-read
+# from DRAM there, from L2 in the timed loop).  None for other workloads.
+MEASURED_DECODE_TRAFFIC = {1: 548096 + 21762560 + 2092800}
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -222,7 +239,7 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": synth.CONFIG_NAMES[args.config], "batch": 1, "seq_len": L_full},
+        "config": workload_config(args, w, w.batch, int(lens.max()), 0, "host memory (fp64 CPU oracle)"),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": gqa, "kind": "oracle",
                          "sample": f"per step: the {gqa} query heads of one KV head of sequence 0 over its first "
                                    f"{L} of {L_full} tokens (fp64 oracle, one thread per query head)"},
@@ -430,20 +447,16 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": Wm,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": {"workload": synth.CONFIG_NAMES[args.config] + ": decode step = append current token + "
-                                   "mixed-precision paged decode",
-                       "batch": B, "seq_len": msl, "num_q_heads": Hq, "num_kv_heads": H, "head_dim": D,
-                       "sink": w.sink_len, "window": w.window_len, "group": w.group_size, "page_size": 16,
-                       "pages_per_split": "auto" if cache.pps == 0 else cache.pps,
-                       "l2_policy": f"inputs larger than L2: {NR} cache replicas in disjoint pages, "
-                                    f"{NR * step_bytes_dec / 1e6:.0f} MB cycled (L2 {l2 / 1e6:.0f} MB)"},
+            "config": workload_config(args, w, B, msl, cache.pps,
+                                      f"inputs larger than L2: {NR} cache replicas in disjoint pages, "
+                                      f"{NR * step_bytes_dec / 1e6:.0f} MB cycled (L2 {l2 / 1e6:.0f} MB)"),
             "tokens_per_s": world * B / (ms_step * 1e-3),
             "us_per_step": ms_step * 1e3,
             "decode_us": dec_us, "append_us": ms_app / K * 1e3, "bf16_decode_us": bf_us,
             "speedup_vs_bf16": bf_us / dec_us,
             "bf16_decode_GBps": algorithmic_bytes_bf16(w, lens_all[:B]) / (bf_us * 1e-6) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak, "traffic": MEASURED_DECODE_TRAFFIC.get(args.config),
                          "kernel": "oscar_decode (q-rotate + split + merge) per launch",
                          "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_launch": step_bytes_dec},
             "cpu_baseline": cpu,
