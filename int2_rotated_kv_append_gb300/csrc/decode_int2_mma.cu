@@ -53,7 +53,8 @@ struct Geo {
   static constexpr size_t kStageArea = static_cast<size_t>(kWarps) * kStages * kStageBytes > kWarps * kDenseStage
                                            ? static_cast<size_t>(kWarps) * kStages * kStageBytes
                                            : static_cast<size_t>(kWarps) * kDenseStage;
-  static constexpr size_t kPagedSmem = kStageArea + kWarps * kStages * 8 + kMaxPps * 4;
+  // | QK operand block (kQfragBytes) | its mbarrier
+  static constexpr size_t kPagedSmem = kStageArea + kWarps * kStages * 8 + kMaxPps * 4 + kQfragBytes + 16;
   static constexpr size_t kSmem = kPagedSmem > split_body_smem(kD) ? kPagedSmem : split_body_smem(kD);
 };
 
@@ -390,6 +391,8 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   // do not depend on it); only the pages in range are validated and used.
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo<NG>::kStageArea);
   int* pid_all = reinterpret_cast<int*>(bars + kWarps * kStages);
+  uint32_t* qbuf = reinterpret_cast<uint32_t*>(pid_all + kMaxPps);  // [32 lanes][kQfragWords]
+  uint64_t* qbar = reinterpret_cast<uint64_t*>(qbuf + 32 * kQfragWords);
   const int sp0 = s * p.pps;
   const int spn = max(0, min(p.pps, p.max_pages - sp0));
   for (int k = tid; k < spn; k += kWarps * 32)
@@ -416,31 +419,44 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   const int* pid_s = pid_all + (pg0 - sp0);  // page ids from the split's first page in range
   if (lane == 0)
     for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp * kStages + i]), 1);
+  if (tid == 0) mbar_init(smem_u32(qbar), 1);
   mbar_init_fence();
   __syncthreads();
 
   const int n_my = npg > warp ? (npg - warp + kWarps - 1) / kWarps : 0;
   uint8_t* my_stages = stages + warp * kStages * kStageBytes;
   uint64_t* my_bars = bars + warp * kStages;
-  auto issue = [&](int i) {  // lane 0: bring local page i of this warp into its stage
-    const int pid = pid_s[warp + i * kWarps];
+  const uint32_t stage_base = smem_u32(my_stages);
+  // Whole warp: bring local pages [i0, i1) of this warp (at most 16) into their
+  // stages.  Lane 2j handles page i0 + j's codes, lane 2j + 1 its scale/zero, so the
+  // whole batch is requested by one bulk-copy instruction: the issue of a bulk
+  // copy takes a few hundred cycles, and copies requested by one lane one after
+  // another would hold the warp that long for each of them.
+  auto issue = [&](int i0, int i1) {
+    const int i = i0 + (lane >> 1), part = lane & 1;
+    const bool active = i < i1;
+    const int pid = active ? pid_s[warp + i * kWarps] : 0;
+    const bool bad = pid < 0 || pid >= p.num_pages;
     const uint32_t bar = smem_u32(&my_bars[i % kStages]);
-    if (pid < 0 || pid >= p.num_pages) {
-      record_error(OSCAR_DEVERR_PAGE_ID);
-      mbar_arrive(bar);
-      return;
+    if (active && part == 0) {
+      if (bad) {
+        record_error(OSCAR_DEVERR_PAGE_ID);
+        mbar_arrive(bar);
+      } else {
+        mbar_arrive_expect_tx(bar, kStageBytes);
+      }
     }
-    uint8_t* st = my_stages + (i % kStages) * kStageBytes;
-    const size_t ph = static_cast<size_t>(pid) * p.H + h;
-    mbar_arrive_expect_tx(bar, kStageBytes);
-    bulk_g2s(smem_u32(st), p.codes + ph * kCodeBytes, kCodeBytes, bar);
-    bulk_g2s(smem_u32(st + kCodeBytes), reinterpret_cast<const uint8_t*>(p.sz) + ph * kSzBytes, kSzBytes, bar);
+    __syncwarp();
+    if (active && !bad) {
+      const size_t ph = static_cast<size_t>(pid) * p.H + h;
+      const uint8_t* src = part ? reinterpret_cast<const uint8_t*>(p.sz) + ph * kSzBytes : p.codes + ph * kCodeBytes;
+      bulk_g2s(stage_base + (i % kStages) * kStageBytes + (part ? kCodeBytes : 0), src, part ? kSzBytes : kCodeBytes, bar);
+    }
   };
   // The first kFirstIssue pages of each warp are requested before the query
   // fragments, the rest once the fragments have arrived: a request made behind
   // every page of the grid would wait for most of the page traffic.
-  if (lane == 0)
-    for (int i = 0; i < n_my && i < kFirstIssue; ++i) issue(i);
+  issue(0, min(n_my, kFirstIssue));
   grid_dep_launch_dependents();
   grid_dep_wait();  // the QK fragments come from the q-rotation kernel; the page copies above do not need them
 
@@ -448,23 +464,26 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   // (built by the q-rotation kernel, kQfragWords words per lane).  Per n-tile nt
   // the lane's C columns belong to query 4*nt + t and its B column to query
   // 4*nt + (g >> 1), part g & 1.
-  const uint4* qw4 = reinterpret_cast<const uint4*>(p.qfrag + ((static_cast<size_t>(b) * p.H + h) * 32 + lane) * kQfragWords);
+  // The block of the (sequence, KV head) arrives by one bulk copy: all the split
+  // CTAs of a head read it at the same time, and whole-line requests load the L2
+  // far less than per-lane 16-byte loads.  The remaining pages are requested once
+  // it has landed.
+  if (tid == 0) {
+    mbar_arrive_expect_tx(smem_u32(qbar), kQfragBytes);
+    bulk_g2s(smem_u32(qbuf), p.qfrag + (static_cast<size_t>(b) * p.H + h) * (32 * kQfragWords), kQfragBytes,
+             smem_u32(qbar));
+  }
+  bool aborted = __any_sync(0xffffffffu, !mbar_wait_bounded(smem_u32(qbar), 0));
+  issue(min(n_my, kFirstIssue), min(n_my, kStages));
+  const uint4* qw4 = reinterpret_cast<const uint4*>(qbuf + lane * kQfragWords);
   uint32_t bq[NT][8][2];
   float F[NT], qs[NT][NG];
   {
     uint4 v[4 * NT], f[3];
 #pragma unroll
-    for (int k = 0; k < 4 * NT; ++k) v[k] = __ldcg(qw4 + k);
+    for (int k = 0; k < 4 * NT; ++k) v[k] = qw4[k];
 #pragma unroll
-    for (int k = 0; k < 3; ++k) f[k] = __ldcg(qw4 + 8 + k);
-    {  // wait for the fragments, then request the remaining pages
-      uint32_t x = f[0].x ^ f[1].x ^ f[2].x;
-#pragma unroll
-      for (int k = 0; k < 4 * NT; ++k) x ^= v[k].x ^ v[k].w;
-      asm volatile("" ::"r"(x));
-      if (lane == 0)
-        for (int i = kFirstIssue; i < n_my && i < kStages; ++i) issue(i);
-    }
+    for (int k = 0; k < 3; ++k) f[k] = qw4[8 + k];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -490,8 +509,6 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
       }
     }
   }
-  bool aborted = false;
-
   // ---- main loop over this warp's pages ----
   float m_run[NT], l_run[NT], zacc[NT][NG], O[NT][8][4];
 #pragma unroll
@@ -507,7 +524,6 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   }
   const uint32_t vsel = (2 * (g & 1)) | ((2 * (g & 1) + 1) << 4) | ((4 + 2 * (g & 1)) << 8) | ((5 + 2 * (g & 1)) << 12);
   const int src1 = 4 * t + (g >> 1), src2 = src1 + 16;
-  const uint32_t stage_base = smem_u32(my_stages);
   int i = 0;
   // Stage of local page k: k % kStages (kStages even: a pair never wraps).
   auto wait_page = [&](int k) {
@@ -540,10 +556,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
       int2_pages<NT, NG, 2, false>(st2, g, t, a0, a1, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
     }
     __syncwarp();
-    if (lane == 0) {
-      if (i + kStages < n_my) issue(i + kStages);
-      if (i + 1 + kStages < n_my) issue(i + 1 + kStages);
-    }
+    issue(min(n_my, i + kStages), min(n_my, i + 2 + kStages));
   }
   if (!aborted && i < n_my) {  // odd last page
     if (__any_sync(0xffffffffu, !wait_page(i))) {
@@ -558,7 +571,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   if (aborted) {
     if (lane == 0) record_error(OSCAR_DEVERR_TIMEOUT);
     // Let the copies already issued land (bounded) before the shared memory is reused.
-    const int issued = min(n_my, i + kStages);
+    const int issued = min(n_my, i + kStages);  // pages requested so far
     for (int k = i; k < issued; ++k) mbar_wait_bounded(smem_u32(&my_bars[k % kStages]), (k / kStages) & 1);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
