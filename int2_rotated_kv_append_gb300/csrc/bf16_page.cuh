@@ -225,8 +225,8 @@ __device__ __forceinline__ void merge_warps_store(const Params& p, const float* 
         if (mwq != -INFINITY) l += fast_exp2(mwq - M) * lw[w * kMaxGqa + tid];
       }
     }
-    p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 0] = M;
-    p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 1] = l;
+    p.part_ml[((bh0 + tid) * p.ml_ns + s) * 2 + 0] = M;
+    p.part_ml[((bh0 + tid) * p.ml_ns + s) * 2 + 1] = l;
   }
 }
 

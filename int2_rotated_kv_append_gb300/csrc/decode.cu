@@ -22,15 +22,23 @@ using namespace oscar_dec;
 
 template <int D, Mode MODE>
 cudaError_t merge(const Params& p, cudaStream_t stream) {
-  const size_t smem = merge_smem(D, p.ns, p.merge_qpc, p.merge_stage);
-  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(merge_kernel<D, MODE>), kMergeSmemLimit);
-  if (e != cudaSuccess) return e;
   const int grid = p.B * p.H * (p.gqa / p.merge_qpc);
-  // A grid of at most one CTA per SM is launched early (programmatic dependent
-  // launch) so that it is resident, with R_v staged, when the splits finish; a
-  // larger one would take SM slots from the last split CTAs and waits for them.
-  if (grid <= num_sms()) return launch_pdl(merge_kernel<D, MODE>, dim3(grid), dim3(kMergeThreads), smem, stream, p);
-  merge_kernel<D, MODE><<<grid, kMergeThreads, smem, stream>>>(p);
+  // A grid of at most one CTA per SM (one query head per CTA) is launched early
+  // (programmatic dependent launch) so that it is resident, with R_v staged, when
+  // the splits finish, and runs a form compiled for one query head; a larger grid
+  // would take SM slots from the last split CTAs and waits for them.
+  if (grid <= num_sms() && p.merge_qpc == 1) {
+    const size_t smem = merge_smem(D, p.ns, p.merge_qpc, p.merge_stage, kMergeThreadsSmall);
+    auto k = merge_kernel<D, MODE, kMergeThreadsSmall, 1>;
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k), kMergeSmemLimit);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k, dim3(grid), dim3(kMergeThreadsSmall), smem, stream, p);
+  }
+  const size_t smem = merge_smem(D, p.ns, p.merge_qpc, p.merge_stage, kMergeThreadsLarge);
+  auto k = merge_kernel<D, MODE, kMergeThreadsLarge, kMaxGqa>;
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k), kMergeSmemLimit);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kMergeThreadsLarge, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -41,11 +49,12 @@ cudaError_t merge(const Params& p, cudaStream_t stream) {
 void merge_config(const oscar_dims_t* d, int B, int ns, Mode mode, int* qpc, int* stage) {
   const int gqa = d->num_q_heads / d->num_kv_heads;
   const long long units = static_cast<long long>(B) * d->num_kv_heads;
-  *qpc = units >= num_sms() && merge_smem(d->head_dim, ns, gqa, 0) <= kMergeSmemLimit ? gqa : 1;
+  *qpc = units >= num_sms() && merge_smem(d->head_dim, ns, gqa, 0, kMergeThreadsLarge) <= kMergeSmemLimit ? gqa : 1;
   *stage = 0;
   if (units * (gqa / *qpc) <= num_sms()) {
-    if (mode == kMixed && merge_smem(d->head_dim, ns, *qpc, kStageRv) <= kMergeSmemLimit) *stage |= kStageRv;
-    if (merge_smem(d->head_dim, ns, *qpc, *stage | kStagePartials) <= kMergeSmemLimit) *stage |= kStagePartials;
+    const int t = kMergeThreadsSmall;
+    if (mode == kMixed && merge_smem(d->head_dim, ns, *qpc, kStageRv, t) <= kMergeSmemLimit) *stage |= kStageRv;
+    if (merge_smem(d->head_dim, ns, *qpc, *stage | kStagePartials, t) <= kMergeSmemLimit) *stage |= kStagePartials;
   }
 }
 
@@ -108,6 +117,7 @@ Params base_params(const oscar_dims_t* d, int B, int max_seq_len, const Plan& pl
   p.n_paged = plan.n_paged;
   p.n_dense = plan.n_dense;
   p.ns = plan.ns;
+  p.ml_ns = plan.ml_ns;
   merge_config(d, B, plan.ns, mode, &p.merge_qpc, &p.merge_stage);
   p.mma = plan.mma;
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(d->head_dim));
@@ -153,7 +163,7 @@ extern "C" oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, 
   if (!make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, split_ctas_per_sm(dims, kMixed), &plan))
     return OSCAR_ERR_INVALID_ARG;
   if (workspace_bytes < plan.total) return OSCAR_ERR_WORKSPACE;
-  if (merge_smem(dims->head_dim, plan.ns, 1, 0) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
+  if (merge_smem(dims->head_dim, plan.ns, 1, 0, kMergeThreadsSmall) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
   if (static_cast<long long>(batch) * dims->num_q_heads > 0x7fffffffLL || plan.ns > 0x7fffffff) return OSCAR_ERR_UNSUPPORTED;
   Params p = base_params(dims, batch, max_seq_len, plan, kMixed, sm_scale, workspace);
   p.S = sink_len;
@@ -194,7 +204,7 @@ extern "C" oscar_status_t oscar_bf16_decode(const oscar_dims_t* dims, int32_t ba
   Plan plan;
   if (!make_plan(dims, batch, max_seq_len, pages_per_split, 0, 0, kBf16Paged, split_ctas_per_sm(dims, kBf16Paged), &plan)) return OSCAR_ERR_INVALID_ARG;
   if (workspace_bytes < plan.total) return OSCAR_ERR_WORKSPACE;
-  if (merge_smem(dims->head_dim, plan.ns, 1, 0) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
+  if (merge_smem(dims->head_dim, plan.ns, 1, 0, kMergeThreadsSmall) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
   Params p = base_params(dims, batch, max_seq_len, plan, kBf16Paged, sm_scale, workspace);
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.pages = static_cast<const __nv_bfloat16*>(bf16_pages);

@@ -43,8 +43,8 @@ __global__ void __launch_bounds__(kWarps * 32) bf16_mma_split_kernel(Params p) {
   grid_dep_launch_dependents();
   if (r1 <= r0) {  // nothing of the sequence in this split: an empty partial (the merge skips it)
     if (tid < gqa) {
-      p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 0] = -INFINITY;
-      p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 1] = 0.f;
+      p.part_ml[((bh0 + tid) * p.ml_ns + s) * 2 + 0] = -INFINITY;
+      p.part_ml[((bh0 + tid) * p.ml_ns + s) * 2 + 1] = 0.f;
     }
     return;
   }

@@ -33,13 +33,14 @@ struct Plan {
   int n_paged = 0;     // splits over the paged pool
   int n_dense = 0;     // splits over the BF16 sink/window buffers
   int ns = 0;          // n_paged + n_dense
+  int ml_ns = 0;       // row stride (splits) of the (m, l) partials: ns rounded up to even (16-byte rows)
   int mma = 0;         // 1: the tensor-core split kernel runs (dense splits of kDenseMmaPages pages)
   size_t off_qrot = 0, off_qfrag = 0, off_po = 0, off_pml = 0, total = 0;
 };
 
 struct Params {
   int B, Hq, H, D, G, gqa, num_pages, max_pages, max_seq_len;
-  int S, W, pps, n_paged, n_dense, ns;
+  int S, W, pps, n_paged, n_dense, ns, ml_ns;
   float scale_log2;
   int merge_qpc;    // query heads per merge CTA (divides gqa)
   int merge_stage;  // merge kernel: kStageRv (R_v staged before the wait) | kStagePartials
@@ -106,7 +107,7 @@ int dense_splits(int S, int W, int max_seq_len, bool mma) {
 
 // Split plan.  With pages_per_split == 0 the split size is chosen so that the
 // paged splits of the whole batch fill about one wave of resident CTAs
-// (ctas_per_sm x SMs, the sink/window splits counted), 4..64 pages per split.
+// (ctas_per_sm x SMs, the sink/window splits counted), 4..128 pages per split.
 // The tensor-core split kernels cover head_dim 128 (INT2: group 64 or 128) and
 // splits of at most kMmaMaxPps pages.
 bool make_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req, int S, int W, Mode mode, int ctas_per_sm,
@@ -124,7 +125,7 @@ bool make_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req, int S
     const long long splits = (slots + units - 1) / units;
     long long want = (max_pages + splits - 1) / splits;
     if (want < 4) want = 4;
-    if (want > 64) want = 64;
+    if (want > 128) want = 128;
     pps = static_cast<int>(want);
   }
   p->mma = shape_mma && pps <= kMmaMaxPps ? 1 : 0;
@@ -142,7 +143,8 @@ bool make_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req, int S
   p->off_po = off;
   off += align_up(bh * p->ns * d->head_dim * sizeof(float), 256);
   p->off_pml = off;
-  off += align_up(bh * p->ns * 2 * sizeof(float), 256);
+  p->ml_ns = (p->ns + 1) & ~1;
+  off += align_up(bh * p->ml_ns * 2 * sizeof(float), 256);
   p->total = off;
   return true;
 }
@@ -490,8 +492,8 @@ __device__ __forceinline__ void split_body(const Params& p, int s, int h, int b,
   }
   if (tid < gqa) {
     const size_t bh = static_cast<size_t>(b) * p.Hq + h * gqa + tid;
-    p.part_ml[(bh * p.ns + s) * 2 + 0] = m_s[tid];
-    p.part_ml[(bh * p.ns + s) * 2 + 1] = l_s[tid];
+    p.part_ml[(bh * p.ml_ns + s) * 2 + 0] = m_s[tid];
+    p.part_ml[(bh * p.ml_ns + s) * 2 + 1] = l_s[tid];
   }
 }
 
@@ -518,20 +520,24 @@ __global__ void __launch_bounds__(kThreads) split_kernel(Params p) {
 // A small grid, launched while the splits still run, stages R_v in shared memory
 // before it waits for them (kStageRv) and the partials with one bulk copy after
 // (kStagePartials); a large grid reads both from L2.
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreadsLarge = 256;  // threads per merge CTA, large grids
+constexpr int kMergeThreadsSmall = 256;  // threads per merge CTA, grids of at most one CTA per SM (one query head each)
 constexpr int kStageRv = 1, kStagePartials = 2;
 
-// Dynamic shared memory of the merge kernel: [R_v D x D] [partials qpc x ns x D]
-// weights [qpc][ns], denominators [8], phase B/C scratch (2 x kMergeThreads
-// float4), rotated and plain sums [qpc][D], two mbarriers.
-constexpr size_t merge_smem(int D, int ns, int qpc, int stage) {
+// Dynamic shared memory of the merge kernel: [R_v D x D] [partials qpc x ns x D,
+// (m, l) qpc x ml_ns x 2] weights [qpc][ns], denominators [8], phase B/C scratch
+// (2 x kMergeThreads float4), rotated and plain sums [qpc][D], two mbarriers.
+constexpr size_t merge_smem(int D, int ns, int qpc, int stage, int threads) {
   return ((stage & kStageRv) ? static_cast<size_t>(D) * D * 4 : 0) +
-         ((stage & kStagePartials) ? static_cast<size_t>(qpc) * ns * D * 4 : 0) +
-         (static_cast<size_t>((qpc * ns + 3) & ~3) + 8) * 4 + 2 * kMergeThreads * 16 +
+         ((stage & kStagePartials) ? static_cast<size_t>(qpc) * ns * D * 4 + static_cast<size_t>(qpc) * ((ns + 1) & ~1) * 8
+                                   : 0) +
+         (static_cast<size_t>((qpc * ns + 3) & ~3) + 8) * 4 + 2 * static_cast<size_t>(threads) * 16 +
          2 * static_cast<size_t>(qpc) * D * 4 + 16;
 }
 
-template <int D, Mode MODE>
+// kQMax: most query heads per CTA the kernel is compiled for (1 for the
+// small-grid form: less code, whose first run is not delayed by instruction fetch).
+template <int D, Mode MODE, int kMergeThreads, int kQMax>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
   extern __shared__ __align__(128) float msm[];
   constexpr bool kRot = MODE == kMixed;
@@ -547,7 +553,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
   const bool st_po = (p.merge_stage & kStagePartials) != 0;
   float* Rs = msm;                                                          // [D][D] (st_rv)
   float* po_s = Rs + (st_rv ? D * D : 0);                                   // [qpc][ns][D] (st_po)
-  float* wts = po_s + (st_po ? static_cast<size_t>(qpc) * ns * D : 0);      // [qpc][ns]
+  float* ml_s = po_s + (st_po ? static_cast<size_t>(qpc) * ns * D : 0);     // [qpc][ml_ns][2] (st_po)
+  float* wts = ml_s + (st_po ? static_cast<size_t>(qpc) * p.ml_ns * 2 : 0);  // [qpc][ns]
   float* den_s = wts + ((qpc * ns + 3) & ~3);                               // [8]
   float4* red = reinterpret_cast<float4*>(den_s + 8);                       // [2][kMergeThreads]
   float* o_rot = reinterpret_cast<float*>(red + 2 * kMergeThreads);         // [qpc][D]
@@ -564,16 +571,23 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
   }
   __syncthreads();
   grid_dep_wait();  // the split partials come from the preceding kernel
-  if (tid == 0 && st_po) {
-    const uint32_t bytes = static_cast<uint32_t>(qpc) * ns * D * 4;
-    mbar_arrive_expect_tx(smem_u32(&bars[1]), bytes);
-    bulk_g2s(smem_u32(po_s), p.part_o + row0 * ns * D, bytes, smem_u32(&bars[1]));
+  bool ok = true;
+  if (st_po) {  // the partials and their (m, l) in one phase of bars[1]
+    if (tid == 0) {
+      const uint32_t bytes = static_cast<uint32_t>(qpc) * ns * D * 4;
+      const uint32_t ml_bytes = static_cast<uint32_t>(qpc) * p.ml_ns * 8;
+      mbar_arrive_expect_tx(smem_u32(&bars[1]), bytes + ml_bytes);
+      bulk_g2s(smem_u32(po_s), p.part_o + row0 * ns * D, bytes, smem_u32(&bars[1]));
+      bulk_g2s(smem_u32(ml_s), p.part_ml + row0 * p.ml_ns * 2, ml_bytes, smem_u32(&bars[1]));
+    }
+    ok = mbar_wait_bounded(smem_u32(&bars[1]), 0);
   }
 
   // phase A: one pass over (m, l) with a running maximum per lane, combined
   // across the warp by log-sum-exp; then the weights from the staged maxima
   for (int qi = warp; qi < qpc; qi += kMergeThreads / 32) {
-    const float2* ml = reinterpret_cast<const float2*>(p.part_ml + (row0 + qi) * ns * 2);
+    const float2* ml = reinterpret_cast<const float2*>(st_po ? ml_s + static_cast<size_t>(qi) * p.ml_ns * 2
+                                                             : p.part_ml + (row0 + qi) * p.ml_ns * 2);
     float* wq = wts + qi * ns;
     float M = -INFINITY, den = 0.f;
     for (int s0 = lane; s0 < ns; s0 += 4 * 32) {
@@ -604,8 +618,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
     }
     if (lane == 0) den_s[qi] = den;
   }
-  bool ok = true;
-  if (st_po) ok = mbar_wait_bounded(smem_u32(&bars[1]), 0);
   ok = __syncthreads_and(ok);
 
   // phase B
@@ -665,9 +677,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
                                                                  : p.R_v + (static_cast<size_t>(h) * D + c) * D) +
                                                          jp * kJ);
     const float4* orow = reinterpret_cast<const float4*>(o_rot + jp * kJ);
-    float acc[kMaxGqa];
+    float acc[kQMax], acc2[kQMax];  // two chains per query (even and odd chunks)
 #pragma unroll
-    for (int qi = 0; qi < kMaxGqa; ++qi) acc[qi] = 0.f;
+    for (int qi = 0; qi < kQMax; ++qi) acc[qi] = acc2[qi] = 0.f;
 #pragma unroll
     for (int k0 = 0; k0 < kChunks; k0 += 8) {
       float4 r[8];
@@ -678,21 +690,22 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
         r[k] = k0 + k < kChunks ? (st_rv ? Rrow[ch[k]] : __ldg(Rrow + ch[k])) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int qi = 0; qi < kMaxGqa; ++qi) {
+      for (int qi = 0; qi < kQMax; ++qi) {
         if (qi < qpc) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             if (k0 + k < kChunks) {
               const float4 o = orow[qi * kQuads + ch[k]];
-              acc[qi] = fmaf(o.x, r[k].x, fmaf(o.y, r[k].y, fmaf(o.z, r[k].z, fmaf(o.w, r[k].w, acc[qi]))));
+              float& a = (k & 1) ? acc2[qi] : acc[qi];
+              a = fmaf(o.x, r[k].x, fmaf(o.y, r[k].y, fmaf(o.z, r[k].z, fmaf(o.w, r[k].w, a))));
             }
           }
         }
       }
     }
 #pragma unroll
-    for (int qi = 0; qi < kMaxGqa; ++qi)
-      if (qi < qpc) part[(jp * qpc + qi) * D + c] = acc[qi];
+    for (int qi = 0; qi < kQMax; ++qi)
+      if (qi < qpc) part[(jp * qpc + qi) * D + c] = acc[qi] + acc2[qi];
     __syncthreads();
   }
   if (!ok && tid == 0) record_error(OSCAR_DEVERR_TIMEOUT);

@@ -406,8 +406,8 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   if (r1 <= r0) {  // nothing of the bulk falls in this split: an empty partial (the merge skips it)
     grid_dep_launch_dependents();
     if (tid < gqa) {
-      p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 0] = -INFINITY;
-      p.part_ml[((bh0 + tid) * p.ns + s) * 2 + 1] = 0.f;
+      p.part_ml[((bh0 + tid) * p.ml_ns + s) * 2 + 0] = -INFINITY;
+      p.part_ml[((bh0 + tid) * p.ml_ns + s) * 2 + 1] = 0.f;
     }
     grid_dep_wait();  // keeps completion ordered after the q-rotation kernel
     return;
