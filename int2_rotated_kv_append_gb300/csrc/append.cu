@@ -166,6 +166,27 @@ __global__ void __launch_bounds__(kThreads) append_small_kernel(
   const float* R = (kv ? R_v : R_k) + static_cast<size_t>(h) * D * D;
   const float* clip = (kv ? clip_v : clip_k) + static_cast<size_t>(h) * D;
   const __nv_bfloat16* x = kv ? v : k;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // Every load is issued before any is used: this warp's kRows rows of R (one
+  // round trip instead of one per few rows), the clip thresholds and the slot of
+  // the token it finishes.
+  float rv[kRows][CPL];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const int i = warp * kRows + r;
+    if constexpr (CPL == 4) {
+      const float4 q4 = __ldg(reinterpret_cast<const float4*>(R + static_cast<size_t>(i) * D) + lane);
+      rv[r][0] = q4.x; rv[r][1] = q4.y; rv[r][2] = q4.z; rv[r][3] = q4.w;
+    } else {
+      const float2 q2 = __ldg(reinterpret_cast<const float2*>(R + static_cast<size_t>(i) * D) + lane);
+      rv[r][0] = q2.x; rv[r][1] = q2.y;
+    }
+  }
+  float cl[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) cl[c] = __ldg(clip + CPL * lane + c);
+  const int64_t t_mine = t0 + warp;  // the token this warp finishes (if any)
+  const int64_t slot_mine = warp < kSmallTok && t_mine < num_tokens ? __ldg(slots + t_mine) : -1;
   for (int i = threadIdx.x; i < kSmallTok * D / 2; i += kThreads) {
     const int tt = i / (D / 2), c2 = i % (D / 2);
     const int64_t t = t0 + tt;
@@ -176,28 +197,19 @@ __global__ void __launch_bounds__(kThreads) append_small_kernel(
     xs[tt * D + 2 * c2 + 1] = val.y;
   }
   __syncthreads();
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   float acc[kSmallTok][CPL];
 #pragma unroll
   for (int m = 0; m < kSmallTok; ++m)
 #pragma unroll
     for (int c = 0; c < CPL; ++c) acc[m][c] = 0.f;
-#pragma unroll 4
+#pragma unroll
   for (int r = 0; r < kRows; ++r) {
     const int i = warp * kRows + r;
-    float rv[CPL];
-    if constexpr (CPL == 4) {
-      const float4 q4 = __ldg(reinterpret_cast<const float4*>(R + static_cast<size_t>(i) * D) + lane);
-      rv[0] = q4.x; rv[1] = q4.y; rv[2] = q4.z; rv[3] = q4.w;
-    } else {
-      const float2 q2 = __ldg(reinterpret_cast<const float2*>(R + static_cast<size_t>(i) * D) + lane);
-      rv[0] = q2.x; rv[1] = q2.y;
-    }
 #pragma unroll
     for (int m = 0; m < kSmallTok; ++m) {
       const float xv = xs[m * D + i];
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) acc[m][c] = fmaf(xv, rv[c], acc[m][c]);
+      for (int c = 0; c < CPL; ++c) acc[m][c] = fmaf(xv, rv[r][c], acc[m][c]);
     }
   }
 #pragma unroll
@@ -217,10 +229,7 @@ __global__ void __launch_bounds__(kThreads) append_small_kernel(
     for (int w = 0; w < kWarpsA; ++w) a += part[(w * kSmallTok + m) * D + CPL * lane + c];
     tot[c] = a;
   }
-  float cl[CPL];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) cl[c] = __ldg(clip + CPL * lane + c);
-  quantize_store<D>(tot, cl, __ldg(slots + t), H, G, num_pages, h, kv, lane, codes, sz);
+  quantize_store<D>(tot, cl, slot_mine, H, G, num_pages, h, kv, lane, codes, sz);
 }
 
 // Plain copy of bf16 rows into the BF16 paged pool, 16 bytes per thread.
