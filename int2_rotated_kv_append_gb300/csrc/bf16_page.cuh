@@ -194,39 +194,41 @@ __device__ __forceinline__ void store_warp(const float (&O)[NT][8][4], const flo
 }  // namespace bf16pg
 
 // Log-sum-exp merge of the NW warps' states in shared memory (mw, lw:
-// [NW][kMaxGqa]; ow: [NW][kMaxGqa][D]) into the CTA's split partial s.
+// [NW][kMaxGqa]; ow: [NW][kMaxGqa][D]) into the CTA's split partial s.  Called
+// by every thread of the CTA (NTHREADS); mw is overwritten with the warps'
+// weights 2^(m_w - M).
 template <int NW, int D, int NTHREADS>
-__device__ __forceinline__ void merge_warps_store(const Params& p, const float* mw, const float* lw, const float* ow,
+__device__ __forceinline__ void merge_warps_store(const Params& p, float* mw, const float* lw, const float* ow,
                                                   int s, size_t bh0, int tid) {
   const int gqa = p.gqa;
-  for (int idx = tid; idx < gqa * D; idx += NTHREADS) {
-    const int qi = idx / D, ch = idx % D;
+  if (tid < gqa) {
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, mw[w * kMaxGqa + qi]);
-    float o = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float mwq = mw[w * kMaxGqa + qi];
-        if (mwq != -INFINITY) o += fast_exp2(mwq - M) * ow[(w * kMaxGqa + qi) * D + ch];
-      }
-    }
-    p.part_o[((bh0 + qi) * p.ns + s) * D + ch] = o;
-  }
-  if (tid < gqa) {
-    float M = -INFINITY, l = 0.f;
-#pragma unroll
     for (int w = 0; w < NW; ++w) M = fmaxf(M, mw[w * kMaxGqa + tid]);
-    if (M != -INFINITY) {
+    float l = 0.f;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float mwq = mw[w * kMaxGqa + tid];
-        if (mwq != -INFINITY) l += fast_exp2(mwq - M) * lw[w * kMaxGqa + tid];
-      }
+    for (int w = 0; w < NW; ++w) {
+      const float mwq = mw[w * kMaxGqa + tid];
+      const float wt = (M == -INFINITY || mwq == -INFINITY) ? 0.f : fast_exp2(mwq - M);
+      l = fmaf(wt, lw[w * kMaxGqa + tid], l);
+      mw[w * kMaxGqa + tid] = wt;
     }
     p.part_ml[((bh0 + tid) * p.ml_ns + s) * 2 + 0] = M;
     p.part_ml[((bh0 + tid) * p.ml_ns + s) * 2 + 1] = l;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < gqa * (D / 4); idx += NTHREADS) {
+    const int qi = idx / (D / 4), c4 = idx % (D / 4);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float wt = mw[w * kMaxGqa + qi];
+      if (wt != 0.f) {
+        const float4 v = reinterpret_cast<const float4*>(ow + (w * kMaxGqa + qi) * D)[c4];
+        o.x = fmaf(wt, v.x, o.x); o.y = fmaf(wt, v.y, o.y); o.z = fmaf(wt, v.z, o.z); o.w = fmaf(wt, v.w, o.w);
+      }
+    }
+    reinterpret_cast<float4*>(p.part_o + ((bh0 + qi) * p.ns + s) * D)[c4] = o;
   }
 }
 

@@ -203,6 +203,21 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
   for (int rr = 0; rr < kRows; ++rr) r[rr] = __ldg(R + static_cast<size_t>(rr) * D);
   for (int i = tid; i < gqa * D; i += kQrotThreads) qs[i] = __bfloat162float(p.q[q0 + i]);
   __syncthreads();
+  if (D == 128 && p.qfrag != nullptr) {
+    // fp16 exponents of the QK operands from ||q|| (one warp per query): since R
+    // is orthogonal every |q_rot[ch]| <= ||q||
+    for (int qi = warp; qi < gqa; qi += kQrotThreads / 32) {
+      float ss = 0.f;
+      for (int i = lane; i < D; i += 32) ss = fmaf(qs[qi * D + i], qs[qi * D + i], ss);
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      if (lane == 0) {
+        const float bound = sqrtf(ss) * fabsf(p.scale_log2) * (1.f + 1.f / 1024.f);
+        int e = 0;
+        if (bound > 0.f) frexpf(bound, &e);
+        E_s[qi] = min(max(15 - e, -100), 100);
+      }
+    }
+  }
   for (int qi = 0; qi < gqa; ++qi) {
     float acc = 0.f;
 #pragma unroll
@@ -221,19 +236,7 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
     return;
   }
   if constexpr (D == 128) {
-  // exponents from ||q|| (one warp per query)
-  for (int qi = warp; qi < gqa; qi += kQrotThreads / 32) {
-    float ss = 0.f;
-    for (int i = lane; i < D; i += 32) ss = fmaf(qs[qi * D + i], qs[qi * D + i], ss);
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    if (lane == 0) {
-      const float bound = sqrtf(ss) * fabsf(p.scale_log2) * (1.f + 1.f / 1024.f);
-      int e = 0;
-      if (bound > 0.f) frexpf(bound, &e);
-      E_s[qi] = min(max(15 - e, -100), 100);
-    }
-  }
-  __syncthreads();
+  __syncthreads();  // qrb (all columns of the block) complete
   uint32_t* dst = p.qfrag + (static_cast<size_t>(b) * p.H + h) * (32 * kQfragWords);
   // fragment words of this block's two 16-channel words w = 2*cb, 2*cb + 1:
   // lanes with t = w % 4 (8 values of g), k-steps 4*(w/4) .. +3, c2 in {0,1}, nt in {0,1}
