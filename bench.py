@@ -437,6 +437,7 @@ def run_ours(args, world, rank, local):
     d2h = B * Hq * D * 4
 
     log(f"e2e: {e2e_ms * 1e3:.2f} us/step")
+    append_line = append_workload(dev) if rank == 0 and not args.no_append else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         log("cpu baseline (oracle)")
@@ -463,11 +464,66 @@ def run_ours(args, world, rank, local):
             "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": K * 4,
+            "append_workload": append_line,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def append_workload(dev):
+    """The append throughput workload: a prefill append of 16384 tokens x 8 KV
+    heads (K and V) into the paged INT2 cache, and a decode append of 256 tokens
+    at random slots.  The prefill is bound by the FP32 rotation (2 * 2 * D^2 flop
+    per token and head, K and V): its roofline is the FP32 FFMA rate of the GPU."""
+    import torch
+
+    import int2_rotated_kv_append_gb300 as ok
+    from int2_rotated_kv_append_gb300 import synth
+    from int2_rotated_kv_append_gb300.cache import Int2Cache
+
+    w = synth.make_config(4, device=dev)
+    cache = Int2Cache(w, device=dev)
+    k, v, slots = w.k.contiguous(), w.v.contiguous(), w.slot_mapping.to(dev).contiguous()
+    kd, vd, sd = synth.decode_append_batch(w, 256, device=dev)
+    sd = sd.to(dev)
+
+    def prefill():
+        ok.oscar_append(w.dims, k, v, cache.R_k, cache.R_v, cache.clip_k, cache.clip_v, cache.page_table, slots,
+                        cache.int2_pages, cache.scale_zero)
+
+    def dec_append():
+        ok.oscar_append(w.dims, kd, vd, cache.R_k, cache.R_v, cache.clip_k, cache.clip_v, cache.page_table, sd,
+                        cache.int2_pages, cache.scale_zero)
+
+    def time_it(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1) / n * 1e3
+
+    pre_us = time_it(prefill, 20)
+    dec_us = time_it(dec_append, 200)
+    T, H, D = w.num_tokens, w.num_kv_heads, w.head_dim
+    flops = 2 * T * H * 2 * D * D  # K and V: 2 D^2 flop each per token and head
+    props = torch.cuda.get_device_properties(dev)
+    fp32_peak = props.multi_processor_count * 128 * 2 * 2.07e9 / 1e12  # FP32 lanes x FMA x max SM clock
+    return {"workload": "prefill append 16384 tokens x 8 KV heads (K and V), head_dim 128, group 64; "
+                        "decode append of 256 tokens at random slots",
+            "prefill_us": pre_us, "prefill_tokens_per_s": T / (pre_us * 1e-6),
+            "prefill_GBps": algorithmic_bytes_append(w, T) / (pre_us * 1e-6) / 1e9,
+            "prefill_roofline": {"bound": "alu", "achieved": flops / (pre_us * 1e-6) / 1e12, "peak": fp32_peak,
+                                 "unit": "TFLOP/s", "frac": flops / (pre_us * 1e-6) / 1e12 / fp32_peak,
+                                 "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz (nominal)"},
+            "decode_append_256_us": dec_us,
+            "note": "inputs resident in L2 between iterations (prefill reads 67 MB and is ALU-bound)"}
 
 
 def cpu_baseline(w, cache, B, step_bytes):
@@ -525,6 +581,7 @@ def main():
     ap.add_argument("--replicas", type=int, default=0, help="cache replicas (0: enough to exceed 3x L2)")
     ap.add_argument("--pps", type=int, default=-1, help="pages per split for both decodes (-1: the workload's, 0: auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-append", action="store_true", help="skip the append throughput workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -2,8 +2,9 @@
  * oscar.h -- C ABI of the OSCAR INT2 rotated KV-cache library (GB300, sm_103a).
  *
  * The method ("OSCAR: Offline Spectral Covariance-Aware Rotation for 2-bit KV
- * Cache Quantization"; strixaai.com summary, agentlenshq.com project card and
- * the paper abstract at thelatestinai.com/papers/2605.17757):
+ * Cache Quantization"; described by the summary "OSCAR: Cut LLM Inference Costs
+ * 8x with 2-bit KV Cache Quantization", the project card "FutureMLS-Lab/OSCAR"
+ * and the paper's abstract):
  *   - new K/V head vectors are multiplied by a fixed orthogonal rotation R and
  *     clipped to fixed per-channel thresholds, both found offline
  *     (summary "Practical Summary"; project card "How it works");

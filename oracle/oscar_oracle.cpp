@@ -5,16 +5,18 @@
 // baseline leg may load this library; the product path never does.  It shares
 // no code, header, table or helper with the CUDA library.
 //
-// Sources (pages on the subject "OSCAR: Offline Spectral Covariance-Aware
-// Rotation for 2-bit KV Cache Quantization"):
-//   [P1]  strixaai.com summary, "Practical Summary" / "How OSCAR Works":
-//         fixed rotations and clipping thresholds, 2-bit KV cache.
-//   [P2]  agentlenshq.com project card, "How it works": per-layer orthogonal
-//         rotations and clipping thresholds from offline calibration; a BF16
-//         "sink" of initial tokens and a BF16 recent window, INT2 bulk.
-//   [P3]  thelatestinai.com/papers/2605.17757, "Abstract": fixed rotations and
-//         clipping thresholds, INT2 attention kernel compatible with paged
-//         KV-cache serving.
+// Sources (three web pages on OSCAR), cited by title and section:
+//   [Summary]   "OSCAR: Cut LLM Inference Costs 8x with 2-bit KV Cache
+//               Quantization", sections "Practical Summary" and "How OSCAR Works":
+//               fixed rotations and clipping thresholds, 2-bit KV cache.
+//   [Card]      project card "FutureMLS-Lab/OSCAR", section "How it works":
+//               per-layer orthogonal rotations and clipping thresholds from
+//               offline calibration; a BF16 "sink" of initial tokens and a BF16
+//               recent window, INT2 bulk.
+//   [Abstract]  "OSCAR: Offline Spectral Covariance-Aware Rotation for 2-bit KV
+//               Cache Quantization", abstract: fixed rotations and clipping
+//               thresholds, INT2 attention kernel compatible with paged KV-cache
+//               serving.
 // The pages give no formulas; the arithmetic below is the plainest reading of
 // the words (rotate, clip, per-group asymmetric INT2 with fp16 scale/zero,
 // paged storage, softmax attention).  Each such reading carries a tag (R#) and
@@ -96,8 +98,8 @@ uint16_t orc_f64_to_f16(double v) {
 }
 
 // ---------------------------------------------------------------------------
-// Append: rotate, clip, quantise, pack, place   ([P1] summary, [P2] how it
-// works, [P3] abstract: fixed rotation R and fixed per-channel clip; INT2)
+// Append: rotate, clip, quantise, pack, place   ([Summary] Practical Summary,
+// [Card] How it works, [Abstract]: fixed rotation R and fixed per-channel clip; INT2)
 // ---------------------------------------------------------------------------
 
 // Step A2 (rotation, reading R7): row vector convention, x_rot = x . R, with
@@ -254,8 +256,8 @@ int32_t orc_append(const orc_dims_t* d, int64_t T, const uint16_t* k, const uint
 
 // ---------------------------------------------------------------------------
 // Decode: mixed-precision attention over BF16 sink + BF16 window + INT2 bulk
-// ([P2] "How it works": sink of initial tokens and recent window in BF16, the
-// bulk in INT2; [P3] abstract: paged KV cache)
+// ([Card] "How it works": sink of initial tokens and recent window in BF16, the
+// bulk in INT2; [Abstract]: paged KV cache)
 // ---------------------------------------------------------------------------
 
 // Softmax attention of one query over n tokens, some scored in original space
