@@ -63,6 +63,8 @@ def load(path: str | None = None):
         "orc_append_prequant": (ctypes.c_int32, [_P, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P]),
         "orc_codes_given_params": (None, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]),
         "orc_append": (ctypes.c_int32, [_P, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+        "orc_append_mixed": (ctypes.c_int32, [_P, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]),
         "orc_attend_mixed": (None, [ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P,
                                     ctypes.c_double, _P, _P]),
         "orc_dequant_row": (None, [_P, _P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
@@ -192,6 +194,26 @@ def append(dims, k_bits, v_bits, R_k, R_v, clip_k, clip_v, slot_mapping, int2_pa
     args = [_c(a, np.float32) for a in (R_k, R_v, clip_k, clip_v)]
     return lib.orc_append(ctypes.byref(d), k.shape[0], _ptr(k), _ptr(v), *[_ptr(a) for a in args],
                           _ptr(slots), _ptr(int2_pages), _ptr(scale_zero_pages))
+
+
+def append_mixed(dims, k_bits, v_bits, R_k, R_v, clip_k, clip_v, slot_mapping, seq_ids, positions, seq_lens,
+                 sink_len, window_len, int2_pages, scale_zero_pages, sink_bits, window_bits, lib=None) -> int:
+    """Append into the host INT2 pools and the BF16 sink/window (uint16 bf16 bits,
+    [B][2][Hkv][S|W][D]) in place."""
+    lib = lib or load()
+    d = _dims(dims)
+    k = _c(k_bits, np.uint16)
+    v = _c(v_bits, np.uint16)
+    slots = _c(slot_mapping, np.int64)
+    sid, pos, lens = (_c(a, np.int32) for a in (seq_ids, positions, seq_lens))
+    for a, t in ((int2_pages, np.uint8), (scale_zero_pages, np.uint16), (sink_bits, np.uint16),
+                 (window_bits, np.uint16)):
+        assert a.dtype == t and a.flags.c_contiguous
+    args = [_c(a, np.float32) for a in (R_k, R_v, clip_k, clip_v)]
+    return lib.orc_append_mixed(ctypes.byref(d), k.shape[0], _ptr(k), _ptr(v), *[_ptr(a) for a in args],
+                                _ptr(slots), _ptr(sid), _ptr(pos), _ptr(lens), lens.shape[0], int(sink_len),
+                                int(window_len), _ptr(int2_pages), _ptr(scale_zero_pages), _ptr(sink_bits),
+                                _ptr(window_bits))
 
 
 # --- decode -------------------------------------------------------------------

@@ -254,6 +254,52 @@ int32_t orc_append(const orc_dims_t* d, int64_t T, const uint16_t* k, const uint
   return status;
 }
 
+// Append with the BF16 parts ([Card] "How it works": a BF16 sink of the first
+// tokens and a BF16 window of the most recent ones next to the INT2 bulk).  Every
+// token t with slot_mapping[t] >= 0 is appended to the INT2 pool exactly as
+// orc_append does ("dual write", reading R13).  Its original bf16 K and V rows are
+// also stored, unrotated (reading R12), for sequence b = seq_ids[t] at position
+// p = positions[t], with L = seq_lens[b] the sequence length after this append
+// (reading R18):
+//   p < S                  -> sink[b][K|V][h][p][:]
+//   p >= max(S, L - W)     -> window[b][K|V][h][p mod W][:]  (reading R11)
+// Tokens in neither range are INT2 only: the decode never reads them from the
+// BF16 buffers, and a later token of the same append takes their ring slot.
+// sink: bf16 bits [B][2][Hkv][S][D]; window: bf16 bits [B][2][Hkv][W][D].
+// Returns orc_append's status, or -2 if a token's sequence id or position is out
+// of range (its BF16 rows are not written).
+int32_t orc_append_mixed(const orc_dims_t* d, int64_t T, const uint16_t* k, const uint16_t* v,
+                         const float* R_k, const float* R_v, const float* clip_k, const float* clip_v,
+                         const int64_t* slot_mapping, const int32_t* seq_ids, const int32_t* positions,
+                         const int32_t* seq_lens, int32_t B, int32_t S, int32_t W, uint8_t* int2_pages,
+                         uint16_t* scale_zero_pages, uint16_t* sink, uint16_t* window) {
+  int32_t status = orc_append(d, T, k, v, R_k, R_v, clip_k, clip_v, slot_mapping, int2_pages, scale_zero_pages);
+  const int H = d->num_kv_heads, D = d->head_dim;
+  for (int64_t t = 0; t < T; ++t) {
+    if (slot_mapping[t] < 0) continue;
+    const int32_t b = seq_ids[t], p = positions[t];
+    if (b < 0 || b >= B || p < 0 || p >= seq_lens[b]) {
+      status = -2;
+      continue;
+    }
+    const int32_t L = seq_lens[b];
+    const int32_t win_begin = (L - W > S) ? L - W : S;
+    for (int kv = 0; kv < 2; ++kv) {
+      for (int h = 0; h < H; ++h) {
+        const uint16_t* x = (kv ? v : k) + (static_cast<size_t>(t) * H + h) * D;
+        uint16_t* dst = nullptr;
+        if (p < S) {
+          dst = sink + (((static_cast<size_t>(b) * 2 + kv) * H + h) * S + p) * D;
+        } else if (W > 0 && p >= win_begin) {
+          dst = window + (((static_cast<size_t>(b) * 2 + kv) * H + h) * W + p % W) * D;
+        }
+        if (dst != nullptr) std::memcpy(dst, x, static_cast<size_t>(D) * sizeof(uint16_t));
+      }
+    }
+  }
+  return status;
+}
+
 // ---------------------------------------------------------------------------
 // Decode: mixed-precision attention over BF16 sink + BF16 window + INT2 bulk
 // ([Card] "How it works": sink of initial tokens and recent window in BF16, the

@@ -639,4 +639,94 @@ def pin_bf16_decode_dense(lib):
         assert np.allclose(out[hq], dense_attention(bf16_vals(qb[0, hq]), K, V, 1 / 8), rtol=0, atol=1e-12)
 
 
+def _mixed_inputs(seed=31, lens=(5, 40, 70), S=4, W=16, D=64, G=32, H=2, P=16):
+    """Tokens of several sequences in position order, random slots of one pool."""
+    rng = np.random.default_rng(seed)
+    T = sum(lens)
+    num_pages = (T + P - 1) // P + 3
+    dims = _dims(H, H, D, P, G, num_pages, (max(lens) + P - 1) // P)
+    kb = bf16_bits(rng.standard_normal((T, H, D)))
+    vb = bf16_bits(rng.standard_normal((T, H, D)))
+    Rk = np.stack([exact_orthogonal(D, seed + h) for h in range(H)])
+    Rv = np.stack([exact_orthogonal(D, seed + 50 + h) for h in range(H)])
+    ck = np.full((H, D), np.inf, np.float32)
+    cv = ck.copy()
+    slots = rng.permutation(num_pages * P)[:T].astype(np.int64)
+    seq = np.concatenate([np.full(L, b, np.int32) for b, L in enumerate(lens)])
+    pos = np.concatenate([np.arange(L, dtype=np.int32) for L in lens])
+    return dict(dims=dims, kb=kb, vb=vb, Rk=Rk, Rv=Rv, ck=ck, cv=cv, slots=slots, seq=seq, pos=pos,
+                lens=np.array(lens, np.int32), S=S, W=W, D=D, G=G, H=H, P=P, num_pages=num_pages)
+
+
+def _mixed_buffers(c):
+    B, H, D, P, G = len(c["lens"]), c["H"], c["D"], c["P"], c["G"]
+    pool = np.full(c["num_pages"] * H * 2 * P * (D // 4), 0xA5, np.uint8)
+    sz = np.full(c["num_pages"] * H * 2 * P * (D // G) * 2, 0xA5A5, np.uint16)
+    sink = np.full((B, 2, H, max(c["S"], 1), D), 0xFFFF, np.uint16)
+    win = np.full((B, 2, H, max(c["W"], 1), D), 0xFFFF, np.uint16)
+    return pool, sz, sink, win
+
+
+def _mixed_call(lib, c, idx, lens_now, bufs):
+    pool, sz, sink, win = bufs
+    return O.append_mixed(c["dims"], c["kb"][idx], c["vb"][idx], c["Rk"], c["Rv"], c["ck"], c["cv"],
+                          c["slots"][idx], c["seq"][idx], c["pos"][idx], lens_now, c["S"], c["W"],
+                          pool, sz, sink, win, lib=lib)
+
+
+def _attended_rows(L, S, W):
+    """(buffer, row, position) of every row the decode reads for length L."""
+    rows = [("sink", p, p) for p in range(min(S, L))]
+    rows += [("win", p % W, p) for p in range(max(S, L - W), L)] if W > 0 else []
+    return rows
+
+
+def pin_append_mixed_streaming_equals_batch(lib):
+    """One append of every token (final lengths) leaves the same INT2 pool and the
+    same attended sink/window rows as appending the tokens one at a time in
+    position order (each with its length at that time): the batch rule that skips
+    window rows a later token of the same append overwrites is the streaming ring."""
+    c = _mixed_inputs()
+    batch = _mixed_buffers(c)
+    assert _mixed_call(lib, c, np.arange(len(c["seq"])), c["lens"], batch) == 0
+    stream = _mixed_buffers(c)
+    order = sorted(range(len(c["seq"])), key=lambda t: (c["pos"][t], c["seq"][t]))
+    now = np.zeros_like(c["lens"])
+    for t in order:
+        now[c["seq"][t]] = c["pos"][t] + 1
+        assert _mixed_call(lib, c, np.array([t]), now.copy(), stream) == 0
+    assert np.array_equal(batch[0], stream[0]) and np.array_equal(batch[1], stream[1])
+    for b, L in enumerate(c["lens"]):
+        for buf, row, _ in _attended_rows(int(L), c["S"], c["W"]):
+            i = 2 if buf == "sink" else 3
+            assert np.array_equal(batch[i][b, :, :, row], stream[i][b, :, :, row]), (b, buf, row)
+
+
+def pin_append_mixed_bf16_rows_and_int2(lib):
+    """The attended sink/window rows hold the token's original bf16 K and V (read
+    straight from the inputs by position), rows the decode never reads are not
+    written, and the INT2 pool equals that of the plain append."""
+    c = _mixed_inputs(seed=33, lens=(3, 20, 37), S=8, W=12)
+    bufs = _mixed_buffers(c)
+    assert _mixed_call(lib, c, np.arange(len(c["seq"])), c["lens"], bufs) == 0
+    pool, sz, sink, win = bufs
+    ref_pool, ref_sz, _, _ = _mixed_buffers(c)
+    O.append(c["dims"], c["kb"], c["vb"], c["Rk"], c["Rv"], c["ck"], c["cv"], c["slots"], ref_pool, ref_sz, lib=lib)
+    assert np.array_equal(pool, ref_pool) and np.array_equal(sz, ref_sz)
+    start = np.concatenate([[0], np.cumsum(c["lens"])[:-1]])
+    for b, L in enumerate(c["lens"]):
+        seen_sink, seen_win = set(), set()
+        for buf, row, p in _attended_rows(int(L), c["S"], c["W"]):
+            t = start[b] + p
+            got = (sink if buf == "sink" else win)[b, :, :, row]
+            assert np.array_equal(got[0], c["kb"][t]) and np.array_equal(got[1], c["vb"][t]), (b, buf, p)
+            (seen_sink if buf == "sink" else seen_win).add(row)
+        for r in range(c["S"]):
+            if r not in seen_sink:
+                assert np.all(sink[b, :, :, r] == 0xFFFF)
+        for r in range(c["W"]):
+            if r not in seen_win:
+                assert np.all(win[b, :, :, r] == 0xFFFF)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

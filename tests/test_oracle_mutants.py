@@ -46,6 +46,9 @@ MUTANTS = [
      "sz[2 * g + 0] = z_bits;\n          sz[2 * g + 1] = s_bits;", 1),
     ("bulk_offset_uses_page_index", "orc_dequant_row(d, int2_pages, scale_zero_pages, page, h, 1, p % P, vv);",
      "orc_dequant_row(d, int2_pages, scale_zero_pages, page, h, 1, (p / P) % P, vv);", 1),
+    ("mixed_kv_swapped", "const uint16_t* x = (kv ? v : k) + (static_cast<size_t>(t) * H + h) * D;\n        uint16_t* dst",
+     "const uint16_t* x = (kv ? k : v) + (static_cast<size_t>(t) * H + h) * D;\n        uint16_t* dst", 1),
+    ("mixed_window_skips_oldest", "} else if (W > 0 && p >= win_begin) {", "} else if (W > 0 && p > win_begin) {", 1),
 ]
 
 
