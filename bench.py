@@ -2,8 +2,9 @@
 """Benchmark of the OSCAR decode step (INT2 rotated KV append + mixed-precision
 paged decode) on one GB300, printing one JSON line.
 
-A step is one decode step of a batch: oscar_append of each sequence's current
-token, then oscar_decode over the whole cache.  The default workload is the
+A step is one decode step of a batch: oscar_append_mixed of each sequence's
+current token (INT2 pool and its BF16 window row), then oscar_decode over the
+whole cache.  The default workload is the
 batch-1 long decode (32 query / 8 KV heads, head_dim 128, context 32768, sink
 64 + window 128 in BF16, group 64, shuffled pages).  Its cache (21.7 MB) fits
 in L2, so the benchmark builds enough independent cache replicas (disjoint
@@ -60,9 +61,12 @@ def algorithmic_bytes_decode(w, batch_lens, n_q_heads=None, n_kv_heads=None):
     return total
 
 
-def algorithmic_bytes_append(w, n_tokens):
+def algorithmic_bytes_append(w, n_tokens, bf16_rows=False):
+    """Bytes of an append: read K, V (bf16) and the slot; write the INT2 rows (codes
+    and fp16 scale/zero); with bf16_rows also the K and V rows of the sink/window."""
     D, G, H = w.head_dim, w.group_size, w.num_kv_heads
-    return n_tokens * (H * 2 * D * 2 + 8 + H * (2 * (D // 4) + 2 * (D // G) * 2 * 2))
+    rows = H * 2 * D * 2 + 12 if bf16_rows else 0  # + sequence id and position
+    return n_tokens * (H * 2 * D * 2 + 8 + H * (2 * (D // 4) + 2 * (D // G) * 2 * 2) + rows)
 
 
 def algorithmic_bytes_bf16(w, batch_lens):
@@ -155,7 +159,7 @@ def measured_peak_hbm():
 def workload_config(args, w, batch, seq_len, pps, l2_policy):
     """The config object of the JSON line (the same for both arms)."""
     from int2_rotated_kv_append_gb300 import synth
-    return {"workload": synth.CONFIG_NAMES[args.config] + ": decode step = append current token + "
+    return {"workload": synth.CONFIG_NAMES[args.config] + ": decode step = append current token (INT2 + BF16 window) + "
                         "mixed-precision paged decode",
             "batch": batch, "seq_len": seq_len, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "sink": w.sink_len, "window": w.window_len, "group": w.group_size,
@@ -298,6 +302,8 @@ def run_ours(args, world, rank, local):
     k_cur = w.k[cur.to(dev)].contiguous()
     v_cur = w.v[cur.to(dev)].contiguous()
     s_cur = w.slot_mapping[cur].to(dev).contiguous()
+    p_cur = w.tok_pos[cur].to(dev).contiguous()                  # position L - 1 of the current token
+    i_cur = torch.arange(B, dtype=torch.int32, device=dev)      # sequence index inside a replica
     q = w.q.contiguous()
     out = torch.empty((w.batch, Hq, D), dtype=torch.float32, device=dev)
     out_bf = torch.empty_like(out)
@@ -306,16 +312,18 @@ def run_ours(args, world, rank, local):
 
     def views(r):
         sl = slice(r * B, (r + 1) * B)
-        return dict(k=k_cur[sl], v=v_cur[sl], slots=s_cur[sl], q=q[sl], pt=cache.page_table[sl],
+        return dict(k=k_cur[sl], v=v_cur[sl], slots=s_cur[sl], pos=p_cur[sl], q=q[sl], pt=cache.page_table[sl],
                     lens=cache.seq_lens[sl], sink=cache.sink[sl], win=cache.window[sl], out=out[sl],
                     out_bf=out_bf[sl], bpt=bf.page_table[sl], blens=bf.seq_lens[sl])
     V = [views(r) for r in range(NR)]
     msl_r = [max(lens_all[r * B:(r + 1) * B]) for r in range(NR)]
 
     def append_r(r):
+        # the current token into the INT2 pool and its BF16 row into the window ring
         x = V[r]
-        ok.oscar_append(w.dims, x["k"], x["v"], cache.R_k, cache.R_v, cache.clip_k, cache.clip_v, x["pt"],
-                        x["slots"], cache.int2_pages, cache.scale_zero)
+        ok.oscar_append_mixed(w.dims, x["k"], x["v"], cache.R_k, cache.R_v, cache.clip_k, cache.clip_v, x["pt"],
+                              x["slots"], i_cur, x["pos"], x["lens"], w.sink_len, w.window_len, cache.int2_pages,
+                              cache.scale_zero, x["sink"], x["win"])
 
     def decode_r(r):
         x = V[r]
@@ -392,7 +400,7 @@ def run_ours(args, world, rank, local):
     sampler.stop()
 
     step_bytes_dec = algorithmic_bytes_decode(w, lens_all[:B])
-    step_bytes_app = algorithmic_bytes_append(w, B)
+    step_bytes_app = algorithmic_bytes_append(w, B, bf16_rows=True)
     step_bytes = step_bytes_dec + step_bytes_app
     ms_step = ms / K
     value = world * step_bytes / (ms_step * 1e-3) / 1e9

@@ -59,6 +59,7 @@ typedef enum {
 #define OSCAR_DEVERR_PAGE_ID 0x2u   /* decode: page id outside [0, num_pages) (page skipped)  */
 #define OSCAR_DEVERR_SEQ_LEN 0x4u   /* decode: seq_len < 0 or > max_seq_len (clamped)         */
 #define OSCAR_DEVERR_TIMEOUT 0x8u   /* a bounded wait on an async copy ran out (work skipped) */
+#define OSCAR_DEVERR_POSITION 0x10u /* append_mixed: sequence id or position out of range (BF16 row skipped) */
 
 /* Cache geometry. */
 typedef struct {
@@ -101,6 +102,35 @@ oscar_status_t oscar_append(const oscar_dims_t* dims, int64_t num_tokens, const 
                             const float* R_k, const float* R_v, const float* clip_k, const float* clip_v,
                             const int32_t* page_table, const int64_t* slot_mapping, uint8_t* int2_pages,
                             void* scale_zero_pages, void* stream);
+
+/*
+ * oscar_append_mixed -- oscar_append plus the BF16 rows of the sink and the
+ * recent window (project card "How it works": a BF16 sink of the first tokens
+ * and a BF16 window of the most recent ones), in the same pass over K/V.
+ * Every token with slot_mapping >= 0 is appended to the INT2 pool exactly as by
+ * oscar_append.  Its original (unrotated) bf16 K and V rows are also written,
+ * for sequence b = seq_ids[t] at position p = positions[t], with
+ * L = seq_lens[b] the sequence's length after this append:
+ *   p < sink_len                      -> bf16_sink[b][K|V][h][p][:]
+ *   p >= max(sink_len, L - window_len) -> bf16_window[b][K|V][h][p % window_len][:]
+ * Other positions are stored in INT2 only: the decode reads them from there, and
+ * a later token of the same call would take their ring slot.  The result is the
+ * same as appending the tokens one at a time in position order.
+ * Arguments (beyond oscar_append's)
+ *   seq_ids, positions  device int32 [num_tokens]
+ *   seq_lens            device int32 [batch], lengths after this append
+ *   bf16_sink           device bf16 [batch][2][Hkv][sink_len][D] (may be NULL if sink_len == 0)
+ *   bf16_window         device bf16 [batch][2][Hkv][window_len][D] (may be NULL if window_len == 0)
+ * Errors: OSCAR_ERR_INVALID_ARG for null or negative arguments.  A sequence id
+ * outside [0, batch) or a position outside [0, L) skips that token's BF16 rows
+ * and sets OSCAR_DEVERR_POSITION.  Rows the call does not write are untouched.
+ */
+oscar_status_t oscar_append_mixed(const oscar_dims_t* dims, int64_t num_tokens, const void* k, const void* v,
+                                  const float* R_k, const float* R_v, const float* clip_k, const float* clip_v,
+                                  const int32_t* page_table, const int64_t* slot_mapping, const int32_t* seq_ids,
+                                  const int32_t* positions, const int32_t* seq_lens, int32_t batch,
+                                  int32_t sink_len, int32_t window_len, uint8_t* int2_pages, void* scale_zero_pages,
+                                  void* bf16_sink, void* bf16_window, void* stream);
 
 /*
  * Workspace (device bytes) oscar_decode needs for `batch` sequences of at most

@@ -28,6 +28,7 @@ OSCAR_DEVERR_SLOT = 0x1
 OSCAR_DEVERR_PAGE_ID = 0x2
 OSCAR_DEVERR_SEQ_LEN = 0x4
 OSCAR_DEVERR_TIMEOUT = 0x8
+OSCAR_DEVERR_POSITION = 0x10
 
 
 class OscarError(RuntimeError):
@@ -51,6 +52,7 @@ def _load():
     D = ctypes.POINTER(oscar_dims_t)
     sigs = {
         "oscar_append": (I32, [D, I64, P, P, P, P, P, P, P, P, P, P, P]),
+        "oscar_append_mixed": (I32, [D, I64, P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, P, P, P, P, P]),
         "oscar_decode_workspace_bytes": (SZ, [D, I32, I32, I32, I32, I32]),
         "oscar_decode": (I32, [D, I32, I32, I32, P, P, P, P, P, P, P, P, P, I32, I32, F32, P, P, SZ, P]),
         "oscar_decode_noalloc": (I32, [D, I32, I32, I32, P, P, P, P, P, P, P, P, P, I32, I32, F32, P, P]),
@@ -129,6 +131,18 @@ def oscar_append(dims, k, v, R_k, R_v, clip_k, clip_v, page_table, slot_mapping,
     _check(lib.oscar_append(ctypes.byref(_dims(dims)), int(k.shape[0]), _ptr(k), _ptr(v), _ptr(R_k), _ptr(R_v),
                             _ptr(clip_k), _ptr(clip_v), _ptr(page_table), _ptr(slot_mapping), _ptr(int2_pages),
                             _ptr(scale_zero_pages), _stream(stream)), "oscar_append")
+
+
+def oscar_append_mixed(dims, k, v, R_k, R_v, clip_k, clip_v, page_table, slot_mapping, seq_ids, positions,
+                       seq_lens, sink_len, window_len, int2_pages, scale_zero_pages, bf16_sink, bf16_window,
+                       stream=None):
+    """oscar_append plus the tokens' bf16 rows in the sink (position < sink_len) and
+    the window ring (positions of the window after this append)."""
+    _check(lib.oscar_append_mixed(ctypes.byref(_dims(dims)), int(k.shape[0]), _ptr(k), _ptr(v), _ptr(R_k),
+                                  _ptr(R_v), _ptr(clip_k), _ptr(clip_v), _ptr(page_table), _ptr(slot_mapping),
+                                  _ptr(seq_ids), _ptr(positions), _ptr(seq_lens), int(seq_lens.shape[0]),
+                                  int(sink_len), int(window_len), _ptr(int2_pages), _ptr(scale_zero_pages),
+                                  _ptr(bf16_sink), _ptr(bf16_window), _stream(stream)), "oscar_append_mixed")
 
 
 def oscar_decode_workspace_bytes(dims, batch, max_seq_len, pages_per_split, sink_len, window_len) -> int:

@@ -21,6 +21,48 @@ constexpr int kTokTile = 32;
 constexpr int kThreads = 256;  // 8 warps x 4 tokens each
 constexpr int64_t kSmallTokenLimit = 512;  // at most this many tokens use the few-token kernel
 
+// Where the original bf16 rows of each appended token go besides the INT2 pool
+// (oscar_append_mixed; OSCAR project card "How it works": a BF16 sink of the
+// first tokens and a BF16 recent window).  Inactive (sink == win == nullptr) for
+// oscar_append.
+struct MixedDst {
+  const int32_t* seq_ids;    // [T]
+  const int32_t* positions;  // [T]
+  const int32_t* seq_lens;   // [B] lengths after this append
+  int B, S, W;
+  __nv_bfloat16* sink;       // [B][2][Hkv][S][D]
+  __nv_bfloat16* win;        // [B][2][Hkv][W][D], ring slot p mod W
+  __host__ __device__ bool active() const { return sink != nullptr || win != nullptr; }
+};
+
+// Element offset of token t's row (head h, K|V kv) in the sink (returned with
+// *which = 0) or the window ring (*which = 1), or -1: position p < S goes to the
+// sink, p >= max(S, L - W) to ring slot p mod W (L = the sequence's length after
+// this append), other positions are INT2 only.  Tokens with a negative slot are
+// skipped like the INT2 write; a sequence id or position out of range is skipped
+// and flagged.
+__device__ __forceinline__ int64_t mixed_row(const MixedDst& md, int64_t t, int64_t slot, int H, int D, int h,
+                                             int kv, int* which) {
+  *which = 0;
+  if (slot < 0) return -1;
+  const int b = __ldg(md.seq_ids + t), p = __ldg(md.positions + t);
+  if (b < 0 || b >= md.B || p < 0) {
+    record_error(OSCAR_DEVERR_POSITION);
+    return -1;
+  }
+  const int L = __ldg(md.seq_lens + b);
+  if (p >= L) {
+    record_error(OSCAR_DEVERR_POSITION);
+    return -1;
+  }
+  if (p < md.S) return ((((static_cast<int64_t>(b) * 2 + kv) * H + h) * md.S) + p) * D;
+  if (md.W > 0 && p >= max(md.S, L - md.W)) {
+    *which = 1;
+    return ((((static_cast<int64_t>(b) * 2 + kv) * H + h) * md.W) + p % md.W) * D;
+  }
+  return -1;
+}
+
 // Clip, group min/max, fp16 scale/zero, codes, pack and store of one rotated
 // vector held by a warp (lane l owns channels [l*CPL, (l+1)*CPL)).  Called by
 // all 32 lanes of the warp with a warp-uniform slot.
@@ -81,10 +123,12 @@ __global__ void __launch_bounds__(kThreads) append_kernel(
     int64_t num_tokens, int H, int G, int num_pages, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ R_k, const float* __restrict__ R_v,
     const float* __restrict__ clip_k, const float* __restrict__ clip_v, const int64_t* __restrict__ slots,
-    uint8_t* __restrict__ codes, __half* __restrict__ sz) {
+    uint8_t* __restrict__ codes, __half* __restrict__ sz, MixedDst md) {
   grid_dep_launch_dependents();  // a following q-rotation (reads neither output) may start
   constexpr int CPL = D / 32;  // channels per lane
   extern __shared__ __align__(16) float smem[];
+  __shared__ int64_t dst_row[kTokTile];
+  __shared__ int dst_buf[kTokTile];
   float* Rs = smem;           // [D][D]
   float* xs = smem + D * D;   // [kTokTile][D]
   const int h = blockIdx.y, kv = blockIdx.z;
@@ -95,12 +139,23 @@ __global__ void __launch_bounds__(kThreads) append_kernel(
 
   for (int i = threadIdx.x; i < D * D / 4; i += kThreads)
     reinterpret_cast<float4*>(Rs)[i] = __ldg(reinterpret_cast<const float4*>(R) + i);
+  if (md.active() && threadIdx.x < kTokTile) {
+    const int64_t t = t0 + threadIdx.x;
+    int which = 0;
+    dst_row[threadIdx.x] = t < num_tokens ? mixed_row(md, t, __ldg(slots + t), H, D, h, kv, &which) : -1;
+    dst_buf[threadIdx.x] = which;
+  }
+  if (md.active()) __syncthreads();
   for (int i = threadIdx.x; i < kTokTile * D / 2; i += kThreads) {
     const int tt = i / (D / 2), c2 = i % (D / 2);
     const int64_t t = t0 + tt;
     float2 val = make_float2(0.f, 0.f);
-    if (t < num_tokens)
-      val = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(x + (static_cast<size_t>(t) * H + h) * D)[c2]);
+    if (t < num_tokens) {
+      const __nv_bfloat162 raw = reinterpret_cast<const __nv_bfloat162*>(x + (static_cast<size_t>(t) * H + h) * D)[c2];
+      val = __bfloat1622float2(raw);
+      if (md.active() && dst_row[tt] >= 0)
+        reinterpret_cast<__nv_bfloat162*>((dst_buf[tt] ? md.win : md.sink) + dst_row[tt])[c2] = raw;
+    }
     xs[tt * D + 2 * c2] = val.x;
     xs[tt * D + 2 * c2 + 1] = val.y;
   }
@@ -154,10 +209,12 @@ __global__ void __launch_bounds__(kThreads) append_small_kernel(
     int64_t num_tokens, int H, int G, int num_pages, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ R_k, const float* __restrict__ R_v,
     const float* __restrict__ clip_k, const float* __restrict__ clip_v, const int64_t* __restrict__ slots,
-    uint8_t* __restrict__ codes, __half* __restrict__ sz) {
+    uint8_t* __restrict__ codes, __half* __restrict__ sz, MixedDst md) {
   grid_dep_launch_dependents();  // a following q-rotation (reads neither output) may start
   constexpr int CPL = D / 32;
   constexpr int kWarpsA = kThreads / 32;
+  __shared__ int64_t dst_row[kSmallTok];
+  __shared__ int dst_buf[kSmallTok];
   constexpr int kRows = D / kWarpsA;
   __shared__ __align__(16) float xs[kSmallTok * D];
   __shared__ __align__(16) float part[kWarpsA * kSmallTok * D];
@@ -187,12 +244,23 @@ __global__ void __launch_bounds__(kThreads) append_small_kernel(
   for (int c = 0; c < CPL; ++c) cl[c] = __ldg(clip + CPL * lane + c);
   const int64_t t_mine = t0 + warp;  // the token this warp finishes (if any)
   const int64_t slot_mine = warp < kSmallTok && t_mine < num_tokens ? __ldg(slots + t_mine) : -1;
+  if (md.active() && threadIdx.x < kSmallTok) {
+    const int64_t t = t0 + threadIdx.x;
+    int which = 0;
+    dst_row[threadIdx.x] = t < num_tokens ? mixed_row(md, t, __ldg(slots + t), H, D, h, kv, &which) : -1;
+    dst_buf[threadIdx.x] = which;
+  }
+  if (md.active()) __syncthreads();
   for (int i = threadIdx.x; i < kSmallTok * D / 2; i += kThreads) {
     const int tt = i / (D / 2), c2 = i % (D / 2);
     const int64_t t = t0 + tt;
     float2 val = make_float2(0.f, 0.f);
-    if (t < num_tokens)
-      val = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(x + (static_cast<size_t>(t) * H + h) * D)[c2]);
+    if (t < num_tokens) {
+      const __nv_bfloat162 raw = reinterpret_cast<const __nv_bfloat162*>(x + (static_cast<size_t>(t) * H + h) * D)[c2];
+      val = __bfloat1622float2(raw);
+      if (md.active() && dst_row[tt] >= 0)
+        reinterpret_cast<__nv_bfloat162*>((dst_buf[tt] ? md.win : md.sink) + dst_row[tt])[c2] = raw;
+    }
     xs[tt * D + 2 * c2] = val.x;
     xs[tt * D + 2 * c2 + 1] = val.y;
   }
@@ -262,13 +330,13 @@ __global__ void bf16_append_kernel(int64_t num_tokens, int H, int D, int num_pag
 template <int D>
 cudaError_t launch_append(int64_t T, const oscar_dims_t* d, const void* k, const void* v, const float* R_k,
                           const float* R_v, const float* clip_k, const float* clip_v, const int64_t* slots,
-                          uint8_t* codes, void* sz, cudaStream_t stream) {
+                          uint8_t* codes, void* sz, const MixedDst& md, cudaStream_t stream) {
   // Few tokens per (head, K|V): spread R's rows over warps instead of staging all of R.
   if (T <= kSmallTokenLimit) {
     const dim3 grid(static_cast<unsigned>((T + kSmallTok - 1) / kSmallTok), d->num_kv_heads, 2);
     append_small_kernel<D><<<grid, kThreads, 0, stream>>>(
         T, d->num_kv_heads, d->group_size, d->num_pages, static_cast<const __nv_bfloat16*>(k),
-        static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz));
+        static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz), md);
     return cudaGetLastError();
   }
   const size_t smem = (static_cast<size_t>(D) * D + kTokTile * D) * sizeof(float);
@@ -277,8 +345,31 @@ cudaError_t launch_append(int64_t T, const oscar_dims_t* d, const void* k, const
   const dim3 grid(static_cast<unsigned>((T + kTokTile - 1) / kTokTile), d->num_kv_heads, 2);
   append_kernel<D><<<grid, kThreads, smem, stream>>>(
       T, d->num_kv_heads, d->group_size, d->num_pages, static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz));
+      static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz), md);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace {
+
+oscar_status_t run_append(const oscar_dims_t* dims, int64_t num_tokens, const void* k, const void* v,
+                          const float* R_k, const float* R_v, const float* clip_k, const float* clip_v,
+                          const int64_t* slot_mapping, uint8_t* int2_pages, void* scale_zero_pages,
+                          const MixedDst& md, void* stream) {
+  oscar_status_t st = check_dims(dims);
+  if (st != OSCAR_OK) return st;
+  if (num_tokens < 0) return OSCAR_ERR_INVALID_ARG;
+  if (num_tokens == 0) return OSCAR_OK;
+  if (!k || !v || !R_k || !R_v || !clip_k || !clip_v || !slot_mapping || !int2_pages || !scale_zero_pages)
+    return OSCAR_ERR_INVALID_ARG;
+  if ((num_tokens + kTokTile - 1) / kTokTile > 0x7fffffffLL) return OSCAR_ERR_UNSUPPORTED;
+  cudaError_t e = dims->head_dim == 128
+                      ? launch_append<128>(num_tokens, dims, k, v, R_k, R_v, clip_k, clip_v, slot_mapping,
+                                           int2_pages, scale_zero_pages, md, as_stream(stream))
+                      : launch_append<64>(num_tokens, dims, k, v, R_k, R_v, clip_k, clip_v, slot_mapping,
+                                          int2_pages, scale_zero_pages, md, as_stream(stream));
+  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
 }  // namespace
@@ -289,19 +380,33 @@ extern "C" oscar_status_t oscar_append(const oscar_dims_t* dims, int64_t num_tok
                                        const int64_t* slot_mapping, uint8_t* int2_pages, void* scale_zero_pages,
                                        void* stream) {
   (void)page_table;
-  oscar_status_t st = check_dims(dims);
-  if (st != OSCAR_OK) return st;
-  if (num_tokens < 0) return OSCAR_ERR_INVALID_ARG;
-  if (num_tokens == 0) return OSCAR_OK;
-  if (!k || !v || !R_k || !R_v || !clip_k || !clip_v || !slot_mapping || !int2_pages || !scale_zero_pages)
-    return OSCAR_ERR_INVALID_ARG;
-  if ((num_tokens + kTokTile - 1) / kTokTile > 0x7fffffffLL) return OSCAR_ERR_UNSUPPORTED;
-  cudaError_t e = dims->head_dim == 128
-                      ? launch_append<128>(num_tokens, dims, k, v, R_k, R_v, clip_k, clip_v, slot_mapping,
-                                           int2_pages, scale_zero_pages, as_stream(stream))
-                      : launch_append<64>(num_tokens, dims, k, v, R_k, R_v, clip_k, clip_v, slot_mapping,
-                                          int2_pages, scale_zero_pages, as_stream(stream));
-  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+  return run_append(dims, num_tokens, k, v, R_k, R_v, clip_k, clip_v, slot_mapping, int2_pages, scale_zero_pages,
+                    MixedDst{}, stream);
+}
+
+extern "C" oscar_status_t oscar_append_mixed(const oscar_dims_t* dims, int64_t num_tokens, const void* k,
+                                             const void* v, const float* R_k, const float* R_v,
+                                             const float* clip_k, const float* clip_v, const int32_t* page_table,
+                                             const int64_t* slot_mapping, const int32_t* seq_ids,
+                                             const int32_t* positions, const int32_t* seq_lens, int32_t batch,
+                                             int32_t sink_len, int32_t window_len, uint8_t* int2_pages,
+                                             void* scale_zero_pages, void* bf16_sink, void* bf16_window,
+                                             void* stream) {
+  (void)page_table;
+  if (batch < 0 || sink_len < 0 || window_len < 0) return OSCAR_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (batch == 0 || !seq_ids || !positions || !seq_lens)) return OSCAR_ERR_INVALID_ARG;
+  if ((sink_len > 0 && !bf16_sink) || (window_len > 0 && !bf16_window)) return OSCAR_ERR_INVALID_ARG;
+  MixedDst md{};
+  md.seq_ids = seq_ids;
+  md.positions = positions;
+  md.seq_lens = seq_lens;
+  md.B = batch;
+  md.S = sink_len;
+  md.W = window_len;
+  md.sink = sink_len > 0 ? static_cast<__nv_bfloat16*>(bf16_sink) : nullptr;
+  md.win = window_len > 0 ? static_cast<__nv_bfloat16*>(bf16_window) : nullptr;
+  return run_append(dims, num_tokens, k, v, R_k, R_v, clip_k, clip_v, slot_mapping, int2_pages, scale_zero_pages,
+                    md, stream);
 }
 
 extern "C" oscar_status_t oscar_bf16_append(const oscar_dims_t* dims, int64_t num_tokens, const void* k,

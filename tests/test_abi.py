@@ -65,6 +65,24 @@ def test_append_validation(lib):
     assert _append(lib, _dims(), ptr=None) == ok.OSCAR_ERR_INVALID_ARG
 
 
+def _append_mixed(lib, dims, T=4, ptr=P, batch=2, S=4, W=8, sink=P, win=P, ids=P):
+    return lib.oscar_append_mixed(ctypes.byref(dims), T, ptr, ptr, ptr, ptr, ptr, ptr, None, ptr, ids, ids, ids,
+                                  batch, S, W, ptr, ptr, sink, win, None)
+
+
+def test_append_mixed_validation(lib):
+    assert _append_mixed(lib, _dims(), batch=-1) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append_mixed(lib, _dims(), S=-1) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append_mixed(lib, _dims(), W=-2) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append_mixed(lib, _dims(), batch=0) == ok.OSCAR_ERR_INVALID_ARG  # tokens but no sequences
+    assert _append_mixed(lib, _dims(), ids=None) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append_mixed(lib, _dims(), sink=None) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append_mixed(lib, _dims(), win=None) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append_mixed(lib, _dims(), S=0, sink=None, W=0, win=None, T=0) == ok.OSCAR_OK  # no-op
+    assert _append_mixed(lib, _dims(head_dim=96, group_size=32)) == ok.OSCAR_ERR_UNSUPPORTED
+    assert _append_mixed(lib, _dims(), ptr=None) == ok.OSCAR_ERR_INVALID_ARG
+
+
 def _decode(lib, dims, batch=2, msl=100, pps=8, S=4, W=8, ws_bytes=1 << 30, ws=ctypes.c_void_p(256), sink=P):
     return lib.oscar_decode(ctypes.byref(dims), batch, msl, pps, P, P, P, P, P, sink, P, P, P, S, W, 0.0, P, ws,
                             ws_bytes, None)

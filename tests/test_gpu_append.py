@@ -103,3 +103,66 @@ def test_append_slot_past_pool_is_flagged():
     codes, sz = pools_to_host(cache)
     keep = np.array([i for i in range(8) if i != 3])
     check_append(w, codes, sz, w.k, w.v, slots.numpy(), sample=keep)
+
+
+# --- oscar_append_mixed: INT2 append plus the BF16 sink/window rows ------------
+
+def _mixed_run(w, S, W, ids=None, fill=0xFFFF):
+    """GPU append_mixed of every token of w (one call) into sentinel-filled buffers;
+    returns the INT2 pools, sink and window (host), and the plain append's pools."""
+    import int2_rotated_kv_append_gb300 as ok
+    B, H, D = w.batch, w.num_kv_heads, w.head_dim
+    fill16 = fill - 0x10000 if fill >= 0x8000 else fill
+    sink = torch.full((B, 2, H, max(S, 1), D), fill16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    win = torch.full((B, 2, H, max(W, 1), D), fill16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    cache = Int2Cache(w)
+    ids = w.tok_seq if ids is None else ids
+    ok.oscar_append_mixed(w.dims, w.k.cuda(), w.v.cuda(), cache.R_k, cache.R_v, cache.clip_k, cache.clip_v, None,
+                          w.slot_mapping.cuda(), ids.cuda(), w.tok_pos.cuda(), w.seq_lens.cuda(), S, W,
+                          cache.int2_pages, cache.scale_zero, sink, win)
+    torch.cuda.synchronize()
+    plain = Int2Cache(w)
+    plain.append(w.k.cuda(), w.v.cuda(), w.slot_mapping.cuda())
+    torch.cuda.synchronize()
+    return pools_to_host(cache), pools_to_host(plain), synth.bits16(sink), synth.bits16(win)
+
+
+def _oracle_mixed(w, S, W, fill=0xFFFF):
+    from oracle import oracle as O
+    B, H, D, G = w.batch, w.num_kv_heads, w.head_dim, w.group_size
+    pool = np.zeros(w.num_pages * H * 2 * 16 * D // 4, np.uint8)
+    sz = np.zeros(w.num_pages * H * 2 * 16 * (D // G) * 2, np.uint16)
+    sink = np.full((B, 2, H, max(S, 1), D), fill, np.uint16)
+    win = np.full((B, 2, H, max(W, 1), D), fill, np.uint16)
+    O.append_mixed(w.dims, synth.bits16(w.k), synth.bits16(w.v), w.R_k.cpu().numpy(), w.R_v.cpu().numpy(),
+                   w.clip_k.cpu().numpy(), w.clip_v.cpu().numpy(), w.slot_mapping.numpy(), w.tok_seq.numpy(),
+                   w.tok_pos.numpy(), w.seq_lens.numpy(), S, W, pool, sz, sink, win)
+    return sink, win
+
+
+@pytest.mark.parametrize("lens,S,W", [([5, 40, 70, 300], 8, 24), ([700, 300], 64, 128), ([3, 17], 0, 16),
+                                      ([33], 16, 0)])
+def test_append_mixed_matches_oracle(lens, S, W):
+    # few tokens (the small kernel) and > 512 tokens (the tiled kernel); sink or window absent
+    w = synth.make_workload(num_q_heads=4, num_kv_heads=2, head_dim=128, group_size=64, sink_len=S, window_len=W,
+                            seq_lens=lens, seed=sum(lens) + S + W)
+    (codes, sz), (codes_p, sz_p), sink, win = _mixed_run(w, S, W)
+    assert np.array_equal(codes, codes_p) and np.array_equal(sz, sz_p)  # INT2 part = plain append
+    o_sink, o_win = _oracle_mixed(w, S, W)
+    if S > 0:
+        assert np.array_equal(sink, o_sink)
+    if W > 0:
+        assert np.array_equal(win, o_win)
+
+
+def test_append_mixed_bad_sequence_id_is_flagged():
+    import int2_rotated_kv_append_gb300 as ok
+    w = synth.make_workload(num_q_heads=2, num_kv_heads=1, head_dim=64, group_size=32, sink_len=4, window_len=8,
+                            seq_lens=[12], seed=5)
+    ids = w.tok_seq.clone()
+    ids[2] = 7  # no such sequence: its BF16 rows are skipped (position 2 of the sink stays untouched)
+    ok.oscar_device_errors(reset=True)
+    _, _, sink, win = _mixed_run(w, 4, 8, ids=ids)
+    assert ok.oscar_device_errors(reset=True) & ok.OSCAR_DEVERR_POSITION
+    assert np.all(sink[0, :, :, 2] == 0xFFFF)
+    assert not np.all(sink[0, :, :, 1] == 0xFFFF)

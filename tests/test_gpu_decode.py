@@ -154,3 +154,22 @@ def test_decode_unattended_bf16_rows_never_read():
     out = cache.decode(w.q.cuda())
     assert torch.isfinite(out).all()
     compare_decode(out, oracle_decode_on_gpu_cache(w, cache))
+
+
+def test_decode_after_append_mixed_equals_generator_buffers():
+    # sink/window written by oscar_append_mixed give the same decode, bit for bit,
+    # as the generator's sink/window of the same tokens
+    import int2_rotated_kv_append_gb300 as ok
+    S, W = 16, 48
+    w = synth.make_workload(num_q_heads=8, num_kv_heads=2, head_dim=128, group_size=64, sink_len=S, window_len=W,
+                            seq_lens=[10, 60, 600], seed=23)
+    cache = _built(w)
+    out_ref = cache.decode(w.q.cuda()).clone()
+    sink = torch.zeros_like(cache.sink)
+    win = torch.zeros_like(cache.window)
+    ok.oscar_append_mixed(w.dims, w.k.cuda(), w.v.cuda(), cache.R_k, cache.R_v, cache.clip_k, cache.clip_v, None,
+                          w.slot_mapping.cuda(), w.tok_seq.cuda(), w.tok_pos.cuda(), w.seq_lens.cuda(), S, W,
+                          cache.int2_pages, cache.scale_zero, sink, win)
+    cache.sink, cache.window = sink, win
+    out = cache.decode(w.q.cuda())
+    assert torch.equal(out, out_ref)
