@@ -29,8 +29,8 @@
  *     never trap: a bad page id, slot or sequence length met on the device is
  *     skipped and recorded in a device error word (oscar_device_errors).
  *   - Outputs never alias inputs.
- *   - R_k, R_v, the page pools and the BF16 sink/window buffers are read with
- *     bulk async copies and must be 16-byte aligned (any cudaMalloc or torch
+ *   - q, R_k, R_v, the page pools and the BF16 sink/window buffers are read with
+ *     bulk async copies or 16-byte loads and must be 16-byte aligned (any cudaMalloc or torch
  *     allocation is); a misaligned pointer is rejected with
  *     OSCAR_ERR_INVALID_ARG.
  *   - Supported shapes: head_dim 64 or 128; page_size 16; group_size 32, 64

@@ -156,8 +156,8 @@ extern "C" oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, 
     return OSCAR_ERR_INVALID_ARG;
   if ((sink_len > 0 && !bf16_sink) || (window_len > 0 && !bf16_window)) return OSCAR_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return OSCAR_ERR_INVALID_ARG;
-  if (misaligned16(R_k) || misaligned16(R_v) || misaligned16(int2_pages) || misaligned16(scale_zero_pages) ||
-      misaligned16(bf16_sink) || misaligned16(bf16_window))
+  if (misaligned16(q) || misaligned16(R_k) || misaligned16(R_v) || misaligned16(int2_pages) ||
+      misaligned16(scale_zero_pages) || misaligned16(bf16_sink) || misaligned16(bf16_window))
     return OSCAR_ERR_INVALID_ARG;
   Plan plan;
   if (!make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, split_ctas_per_sm(dims, kMixed), &plan))

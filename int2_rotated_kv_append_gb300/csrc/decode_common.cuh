@@ -167,6 +167,31 @@ constexpr int kQrotThreads = 128;  // 4 warps, each summing a quarter of the row
 // extracts channel e (0..15) of a packed 16-channel word (see decode_int2_mma.cu).
 __host__ __device__ constexpr int code_kpos(int e) { return (e & 7) <= 4 ? 2 * (e & 7) : 2 * (e & 7) - 10; }
 
+// Exponent E of a query's tensor-core QK operands: E = 15 - ceil(log2(||q_rot|| *
+// |scale_log2| * (1 + 2^-10))), so that every operand q_rot[ch] * scale_log2 *
+// 2^(E - kpos) is below 2^15 in magnitude (|q_rot[ch]| <= ||q_rot||).
+__device__ __forceinline__ int qk_exponent(float norm, float scale_log2) {
+  const float bound = norm * fabsf(scale_log2) * (1.f + 1.f / 1024.f);
+  int e = 0;
+  if (bound > 0.f) frexpf(bound, &e);
+  return min(max(15 - e, -100), 100);
+}
+
+// One 32-bit B-operand word of the INT2 kernel's QK product: channels ch_lo and
+// ch_lo + 8 of a query (rotated values v_lo, v_hi), scaled by scale_log2 *
+// 2^(E - kpos(channel)), as the fp16 high part or (lo_part) the fp16 remainder.
+__device__ __forceinline__ uint32_t qk_word(float v_lo, float v_hi, float scale_log2, int E, int ch_lo,
+                                            bool lo_part) {
+  const float x0 = v_lo * scale_log2 * pow2i(E - code_kpos(ch_lo & 15));
+  const float x1 = v_hi * scale_log2 * pow2i(E - code_kpos((ch_lo + 8) & 15));
+  __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+  if (lo_part) {
+    h0 = __float2half_rn(x0 - __half2float(h0));
+    h1 = __float2half_rn(x1 - __half2float(h1));
+  }
+  return static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+}
+
 // q_rot[b][hq] = q[b][hq] . R_k[h] for the GQA query heads of one (b, h), one
 // CTA per block of 32 output columns (grid (B*Hkv, D/32)).  Warp w sums rows
 // [w*D/4, (w+1)*D/4) of the block's columns, read straight from global memory
@@ -210,12 +235,7 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
       float ss = 0.f;
       for (int i = lane; i < D; i += 32) ss = fmaf(qs[qi * D + i], qs[qi * D + i], ss);
       for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-      if (lane == 0) {
-        const float bound = sqrtf(ss) * fabsf(p.scale_log2) * (1.f + 1.f / 1024.f);
-        int e = 0;
-        if (bound > 0.f) frexpf(bound, &e);
-        E_s[qi] = min(max(15 - e, -100), 100);
-      }
+      if (lane == 0) E_s[qi] = qk_exponent(sqrtf(ss), p.scale_log2);
     }
   }
   for (int qi = 0; qi < gqa; ++qi) {
@@ -248,17 +268,8 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
     const int j = 2 * kk + c2;
     const int ch_lo = 16 * w + j, ch_hi = ch_lo + 8;
     uint32_t word = 0;
-    if (qb < gqa) {
-      const int E = E_s[qb];
-      const float x0 = qrb[qb][ch_lo - 32 * cb] * p.scale_log2 * pow2i(E - code_kpos(ch_lo & 15));
-      const float x1 = qrb[qb][ch_hi - 32 * cb] * p.scale_log2 * pow2i(E - code_kpos(ch_hi & 15));
-      __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-      if (gg8 & 1) {
-        h0 = __float2half_rn(x0 - __half2float(h0));
-        h1 = __float2half_rn(x1 - __half2float(h1));
-      }
-      word = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
-    }
+    if (qb < gqa)
+      word = qk_word(qrb[qb][ch_lo - 32 * cb], qrb[qb][ch_hi - 32 * cb], p.scale_log2, E_s[qb], ch_lo, gg8 & 1);
     dst[L * kQfragWords + nt * 16 + ks * 2 + c2] = word;
   }
   // factors: block sums of query 4*nt + t for the 32 lanes (and F from block 0)

@@ -264,6 +264,7 @@ __device__ __forceinline__ void dense_split(const Params& p, int d, int h, int b
   const int s = p.n_paged + d;
   const size_t bh0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * gqa;
   grid_dep_launch_dependents();
+  grid_dep_wait();  // the sink/window rows may come from the preceding kernel (an append)
   const int L = clamp_len(p, b);
   const int nsp = (p.S + kPageSize - 1) / kPageSize, nwp = (p.W + kPageSize - 1) / kPageSize;
   const int first = d * kDensePagesPerCta;
@@ -370,7 +371,6 @@ __device__ __forceinline__ void dense_split(const Params& p, int d, int h, int b
   bf16pg::store_warp<NT>(O, m_run, l_run, mw, lw, ow, warp, g, t, gqa);
   __syncthreads();
   merge_warps_store<kWarps, kD, kWarps * 32>(p, mw, lw, ow, s, bh0, tid);
-  grid_dep_wait();  // keeps completion ordered after the q-rotation kernel
 }
 
 // ---- the kernel --------------------------------------------------------------
@@ -453,12 +453,14 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
       bulk_g2s(stage_base + (i % kStages) * kStageBytes + (part ? kCodeBytes : 0), src, part ? kSzBytes : kCodeBytes, bar);
     }
   };
-  // The first kFirstIssue pages of each warp are requested before the query
-  // fragments, the rest once the fragments have arrived: a request made behind
-  // every page of the grid would wait for most of the page traffic.
-  issue(0, min(n_my, kFirstIssue));
   grid_dep_launch_dependents();
-  grid_dep_wait();  // the QK fragments come from the q-rotation kernel; the page copies above do not need them
+  uint32_t bq[NT][8][2];
+  float F[NT], qs[NT][NG];
+  bool aborted = false;
+  // Pages are read only after the preceding kernels have completed (an append may
+  // have written them): the preceding kernel is the q-rotation, which completes
+  // after the kernel before it.
+  grid_dep_wait();
 
   // ---- query side: this lane's QK B-fragments and per-query factors ----
   // (built by the q-rotation kernel, kQfragWords words per lane).  Per n-tile nt
@@ -468,16 +470,18 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   // CTAs of a head read it at the same time, and whole-line requests load the L2
   // far less than per-lane 16-byte loads.  The remaining pages are requested once
   // it has landed.
+  // The first kFirstIssue pages of each warp are requested before the operand
+  // block, the rest once it has landed: a request made behind every page of the
+  // grid would wait for most of the page traffic.
+  issue(0, min(n_my, kFirstIssue));
   if (tid == 0) {
     mbar_arrive_expect_tx(smem_u32(qbar), kQfragBytes);
     bulk_g2s(smem_u32(qbuf), p.qfrag + (static_cast<size_t>(b) * p.H + h) * (32 * kQfragWords), kQfragBytes,
              smem_u32(qbar));
   }
-  bool aborted = __any_sync(0xffffffffu, !mbar_wait_bounded(smem_u32(qbar), 0));
+  aborted = __any_sync(0xffffffffu, !mbar_wait_bounded(smem_u32(qbar), 0));
   issue(min(n_my, kFirstIssue), min(n_my, kStages));
   const uint4* qw4 = reinterpret_cast<const uint4*>(qbuf + lane * kQfragWords);
-  uint32_t bq[NT][8][2];
-  float F[NT], qs[NT][NG];
   {
     uint4 v[4 * NT], f[3];
 #pragma unroll
