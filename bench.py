@@ -170,7 +170,7 @@ def workload_config(args, w, batch, seq_len, pps, l2_policy):
 # launch (q-rotation + split + merge kernels) on the batch-1 32K workload, from one
 # ncu capture of the three kernels (cold caches: the split partials are re-read
 # from DRAM there, from L2 in the timed loop).  None for other workloads.
-MEASURED_DECODE_TRAFFIC = {1: 548096 + 21762560 + 2092800}
+MEASURED_DECODE_TRAFFIC = {1: 548608 + 21765888 + 2084096}
 
 
 def dist_setup():
