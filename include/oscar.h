@@ -29,9 +29,9 @@
  *     never trap: a bad page id, slot or sequence length met on the device is
  *     skipped and recorded in a device error word (oscar_device_errors).
  *   - Outputs never alias inputs.
- *   - q, R_k, R_v, the page pools and the BF16 sink/window buffers are read with
- *     bulk async copies or 16-byte loads and must be 16-byte aligned (any cudaMalloc or torch
- *     allocation is); a misaligned pointer is rejected with
+ *   - q, k, v, R_k, R_v, the page pools and the BF16 sink/window buffers are moved with
+ *     bulk async copies or 16-byte loads and stores and must be 16-byte aligned (any
+ *     cudaMalloc or torch allocation is); a misaligned pointer is rejected with
  *     OSCAR_ERR_INVALID_ARG.
  *   - Supported shapes: head_dim 64 or 128; page_size 16; group_size 32, 64
  *     or 128 dividing head_dim; num_q_heads / num_kv_heads (GQA) 1..8.
@@ -97,6 +97,11 @@ typedef struct {
  *   scale_zero_pages device fp16 [num_pages][Hkv][2][P][D/G][2 = scale, zero]
  * Only the rows of the given slots are written.  A slot past the pool is
  * skipped and flagged OSCAR_DEVERR_SLOT.  num_tokens == 0 is a no-op.
+ * Arithmetic: y is accumulated in fp32.  Calls of more than 512 tokens at D = 128
+ * multiply on tensor cores with R split into three
+ * bf16 terms (about 24 significant bits), so y may differ from a sequential fp32
+ * sum by rounding, and a value within rounding of a code boundary may take the
+ * neighbouring code.
  */
 oscar_status_t oscar_append(const oscar_dims_t* dims, int64_t num_tokens, const void* k, const void* v,
                             const float* R_k, const float* R_v, const float* clip_k, const float* clip_v,
@@ -214,9 +219,10 @@ oscar_status_t oscar_decode_noalloc(const oscar_dims_t* dims, int32_t batch, int
  * oscar_bf16_append -- store K/V vectors unchanged into a BF16 paged pool (the
  * speedup reference's cache; the pages compare OSCAR against BF16 decoding,
  * summary "Practical Summary").
- *   k, v          device bf16 [num_tokens][Hkv][D]
+ *   k, v          device bf16 [num_tokens][Hkv][D], 16-byte aligned
  *   slot_mapping  device int64 [num_tokens]; < 0 skips; past the pool is flagged
- *   bf16_pages    device bf16 [num_pages][Hkv][2][P][D]
+ *   bf16_pages    device bf16 [num_pages][Hkv][2][P][D], 16-byte aligned
+ * Misaligned k, v or bf16_pages return OSCAR_ERR_INVALID_ARG.
  */
 oscar_status_t oscar_bf16_append(const oscar_dims_t* dims, int64_t num_tokens, const void* k, const void* v,
                                  const int64_t* slot_mapping, void* bf16_pages, void* stream);

@@ -204,6 +204,260 @@ __global__ void __launch_bounds__(kThreads) append_kernel(
 // fixed warp order through shared memory before the same quantise/store step.
 constexpr int kSmallTok = 8;
 
+// ---- prefill append with the rotation on tensor cores (head_dim 128) -----------
+//
+// y = x . R for tiles of kTcTok tokens of one (KV head, K|V) on mma.sync m16n8k16
+// (bf16 in, fp32 accumulate).  x is bf16 and exact as an operand; R (fp32) is split
+// into three bf16 terms hi + mid + lo (about 24 significant bits), each multiplied
+// in and accumulated in fp32, so y carries fp32-level rounding like the FFMA
+// rotation.  Each CTA serves one (head, K|V) and loops over every gridDim.x-th
+// token tile: R^T's three parts stay in shared memory (split once per CTA), the
+// next tile's x is loaded into registers while the current one is multiplied, and
+// the clip / group min-max / fp16 scale-zero / codes / pack step runs on the
+// accumulators in registers (a quad of lanes holds a token row).  Shared rows are
+// 256 bytes with their 16-byte chunks XOR-swizzled by row, so ldmatrix reads are
+// conflict free.  Each of the 4 warps computes 16 tokens x 128 outputs.
+constexpr int kTcTok = 64;
+constexpr int kTcThreads = 128;
+constexpr int kTcLoads = kTcTok * 16 / kTcThreads;     // 16-byte chunks of x per thread per tile
+constexpr size_t kTcSmem = (3 * 128 + kTcTok) * 256;  // R^T parts, x tile: two CTAs fit an SM
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk) { return row * 256 + ((chunk ^ (row & 7)) << 4); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t bf16_pair(__nv_bfloat16 lo, __nv_bfloat16 hi) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) | (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
+}
+
+// x rows of token tile `tile` (zeros past the end), chunk u*kTcThreads + tid.
+__device__ __forceinline__ void tc_load_x(const __nv_bfloat16* __restrict__ x, int64_t num_tokens, int H, int h,
+                                          int64_t tile, int tid, uint4 (&raw)[kTcLoads]) {
+#pragma unroll
+  for (int u = 0; u < kTcLoads; ++u) {
+    const int it = u * kTcThreads + tid, tt = it >> 4, c = it & 15;
+    const int64_t t = tile * kTcTok + tt;
+    raw[u] = t < num_tokens ? __ldg(reinterpret_cast<const uint4*>(x + (static_cast<size_t>(t) * H + h) * 128) + c)
+                            : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kTcThreads, 2) append_tc_kernel(
+    int64_t num_tokens, int H, int num_pages, const __nv_bfloat16* __restrict__ k,
+    const __nv_bfloat16* __restrict__ v, const float* __restrict__ R_k, const float* __restrict__ R_v,
+    const float* __restrict__ clip_k, const float* __restrict__ clip_v, const int64_t* __restrict__ slots,
+    uint8_t* __restrict__ codes, __half* __restrict__ sz, MixedDst md) {
+  grid_dep_launch_dependents();  // a following q-rotation (reads neither output) may start
+  constexpr int D = 128, NPG = G / 8, NGRP = D / G;  // n-tiles per group, groups per row
+  extern __shared__ __align__(128) uint8_t tsm[];
+  __shared__ int64_t dst_row[kTcTok];
+  __shared__ int dst_buf[kTcTok];
+  const int h = blockIdx.y, kv = blockIdx.z;
+  const float* R = (kv ? R_v : R_k) + static_cast<size_t>(h) * D * D;
+  const __nv_bfloat16* x = kv ? v : k;
+  const uint32_t rt = smem_u32(tsm);       // R^T part p: rows n at rt + p * 128 * 256
+  const uint32_t xt = rt + 3 * 128 * 256;  // x tile: token rows
+  const float* clip = (kv ? clip_v : clip_k) + static_cast<size_t>(h) * D;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t ntiles = (num_tokens + kTcTok - 1) / kTcTok;
+
+  uint4 raw[kTcLoads];
+  tc_load_x(x, num_tokens, H, h, blockIdx.x, tid, raw);  // the first tile's x is in flight during the split
+  // R^T in three bf16 parts.  Thread: k pair kp = tid % 64 (rows 2kp, 2kp + 1 of R),
+  // 4 consecutive n per item; a warp's stores fall on 32 distinct banks.
+  {
+    const int kp = tid & 63;
+#pragma unroll 1
+    for (int b = 0; b < 2; ++b) {
+      float4 r0[8], r1[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int n4 = 2 * (8 * b + u) + (tid >> 6);
+        r0[u] = __ldg(reinterpret_cast<const float4*>(R + static_cast<size_t>(2 * kp) * D) + n4);
+        r1[u] = __ldg(reinterpret_cast<const float4*>(R + static_cast<size_t>(2 * kp + 1) * D) + n4);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int n4 = 2 * (8 * b + u) + (tid >> 6);
+        const float a0[4] = {r0[u].x, r0[u].y, r0[u].z, r0[u].w}, a1[4] = {r1[u].x, r1[u].y, r1[u].z, r1[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(a0[i]), h1 = __float2bfloat16_rn(a1[i]);
+          const float e0 = a0[i] - __bfloat162float(h0), e1 = a1[i] - __bfloat162float(h1);
+          const __nv_bfloat16 m0 = __float2bfloat16_rn(e0), m1 = __float2bfloat16_rn(e1);
+          const __nv_bfloat16 l0 = __float2bfloat16_rn(e0 - __bfloat162float(m0));
+          const __nv_bfloat16 l1 = __float2bfloat16_rn(e1 - __bfloat162float(m1));
+          const uint32_t off = rt + swz(4 * n4 + i, kp >> 2) + (kp & 3) * 4;
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(off), "r"(bf16_pair(h0, h1)) : "memory");
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(off + 128 * 256), "r"(bf16_pair(m0, m1)) : "memory");
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(off + 2 * 128 * 256), "r"(bf16_pair(l0, l1)) : "memory");
+        }
+      }
+    }
+  }
+
+  const int a_row = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1), a_hi = lane >> 4;
+  const int b_row = (lane & 7) + 8 * (lane >> 4), b_hi = (lane >> 3) & 1;
+  const int g = lane >> 2, tq = lane & 3;
+#pragma unroll 1
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int64_t t0 = tile * kTcTok;
+    __syncthreads();  // the previous tile's x reads are done (first pass: R^T is stored)
+    if (md.active()) {
+      if (tid < kTcTok) {
+        const int64_t t = t0 + tid;
+        int which = 0;
+        dst_row[tid] = t < num_tokens ? mixed_row(md, t, __ldg(slots + t), H, D, h, kv, &which) : -1;
+        dst_buf[tid] = which;
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int u = 0; u < kTcLoads; ++u) {
+      const int it = u * kTcThreads + tid, tt = it >> 4, c = it & 15;
+      if (md.active() && t0 + tt < num_tokens && dst_row[tt] >= 0)  // oscar_append_mixed: the bf16 row
+        reinterpret_cast<uint4*>((dst_buf[tt] ? md.win : md.sink) + dst_row[tt])[c] = raw[u];
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(xt + swz(tt, c)), "r"(raw[u].x), "r"(raw[u].y),
+                   "r"(raw[u].z), "r"(raw[u].w)
+                   : "memory");
+    }
+    __syncthreads();
+    tc_load_x(x, num_tokens, H, h, tile + gridDim.x, tid, raw);  // next tile (zeros past the end)
+
+    // y[16 tokens of this warp][128] = x . (R_hi + R_mid + R_lo)
+    float acc[16][4];
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[n][c] = 0.f;
+#pragma unroll 1
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(xt + swz(a_row, 2 * ks + a_hi), a0, a1, a2, a3);
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {  // n-tiles 2np, 2np + 1
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(rt + part * 128 * 256 + swz(16 * np + b_row, 2 * ks + b_hi), b0, b1, b2, b3);
+          mma_bf16_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+          mma_bf16_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+    }
+
+    // Quantise from the accumulators.  Quad g of the warp holds tokens 16w + g (elements
+    // 0, 1) and 16w + g + 8 (elements 2, 3); lane tq holds channels 8n + 2tq, 8n + 2tq + 1.
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int64_t t = t0 + 16 * warp + g + 8 * hf;
+      int64_t slot = t < num_tokens ? __ldg(slots + t) : -1;
+      if (slot >= static_cast<int64_t>(num_pages) * kPageSize) {
+        if (tq == 0) record_error(OSCAR_DEVERR_SLOT);
+        slot = -1;
+      }
+      uint32_t szw[NGRP];  // (scale, zero) of each group as stored: scale in the low half
+      uint32_t nib[16];
+#pragma unroll
+      for (int j = 0; j < NGRP; ++j) {
+        float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+        for (int n = j * NPG; n < (j + 1) * NPG; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float cl = __ldg(clip + 8 * n + 2 * tq + e);
+            const float y = fminf(fmaxf(acc[n][2 * hf + e], -cl), cl);
+            acc[n][2 * hf + e] = y;
+            mn = fminf(mn, y);
+            mx = fmaxf(mx, y);
+          }
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const __half sh = __float2half_rn((mx - mn) / 3.0f);
+        const __half zh = __float2half_rn(mn);
+        szw[j] = static_cast<uint32_t>(__half_as_ushort(sh)) | (static_cast<uint32_t>(__half_as_ushort(zh)) << 16);
+        const float s = __half2float(sh), z = __half2float(zh);
+#pragma unroll
+        for (int n = j * NPG; n < (j + 1) * NPG; ++n) {
+          uint32_t c2 = 0;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            uint32_t code = 0;
+            if (s != 0.f) {
+              const float uq = (acc[n][2 * hf + e] - z) / s;
+              code = static_cast<uint32_t>(fminf(fmaxf(rintf(uq), 0.f), 3.f));
+            }
+            c2 |= code << (2 * e);
+          }
+          nib[n] = c2;
+        }
+      }
+      // Channel 8n + 2tq + e is byte 2n + tq / 2, bits 4 (tq & 1) + 2e: the quad's four
+      // nibbles of n-tile n form 16 bits; n-tiles 2w, 2w + 1 form the row's word w.
+      uint32_t word[8];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        uint32_t vw = (nib[2 * w] | (nib[2 * w + 1] << 16)) << (4 * tq);
+        vw |= __shfl_xor_sync(0xffffffffu, vw, 1);
+        vw |= __shfl_xor_sync(0xffffffffu, vw, 2);
+        word[w] = vw;
+      }
+      if (slot >= 0) {
+        const int64_t page = slot / kPageSize;
+        const int off = static_cast<int>(slot % kPageSize);
+        const size_t row = ((static_cast<size_t>(page) * H + h) * 2 + kv) * kPageSize + off;
+        uint32_t lo = word[0], hi = word[1];
+#pragma unroll
+        for (int q = 1; q < 4; ++q)
+          if (tq == q) {
+            lo = word[2 * q];
+            hi = word[2 * q + 1];
+          }
+        reinterpret_cast<uint2*>(codes + row * (D / 4))[tq] = make_uint2(lo, hi);
+        if (tq == 0) {  // the row's NGRP pairs in one store
+          void* dst = sz + row * NGRP * 2;
+          if constexpr (NGRP == 4) *static_cast<uint4*>(dst) = make_uint4(szw[0], szw[1], szw[2], szw[3]);
+          if constexpr (NGRP == 2) *static_cast<uint2*>(dst) = make_uint2(szw[0], szw[1]);
+          if constexpr (NGRP == 1) *static_cast<uint32_t*>(dst) = szw[0];
+        }
+      }
+    }
+  }
+}
+
+template <int G>
+cudaError_t launch_append_tc(int64_t T, const oscar_dims_t* d, const void* k, const void* v, const float* R_k,
+                             const float* R_v, const float* clip_k, const float* clip_v, const int64_t* slots,
+                             uint8_t* codes, void* sz, const MixedDst& md, cudaStream_t stream) {
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(append_tc_kernel<G>), kTcSmem);
+  if (e != cudaSuccess) return e;
+  // Two CTAs per SM over all (head, K|V); each loops over its share of the token tiles.
+  const int64_t ntiles = (T + kTcTok - 1) / kTcTok;
+  const int hkv = 2 * d->num_kv_heads;
+  int64_t per = (2 * static_cast<int64_t>(num_sms()) + hkv - 1) / hkv;
+  if (per > ntiles) per = ntiles;
+  const dim3 grid(static_cast<unsigned>(per), d->num_kv_heads, 2);
+  append_tc_kernel<G><<<grid, kTcThreads, kTcSmem, stream>>>(
+      T, d->num_kv_heads, d->num_pages, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
+      R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz), md);
+  return cudaGetLastError();
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) append_small_kernel(
     int64_t num_tokens, int H, int G, int num_pages, const __nv_bfloat16* __restrict__ k,
@@ -339,6 +593,13 @@ cudaError_t launch_append(int64_t T, const oscar_dims_t* d, const void* k, const
         static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz), md);
     return cudaGetLastError();
   }
+  if constexpr (D == 128) {  // the rotation on tensor cores
+    switch (d->group_size) {
+      case 32: return launch_append_tc<32>(T, d, k, v, R_k, R_v, clip_k, clip_v, slots, codes, sz, md, stream);
+      case 64: return launch_append_tc<64>(T, d, k, v, R_k, R_v, clip_k, clip_v, slots, codes, sz, md, stream);
+      default: return launch_append_tc<128>(T, d, k, v, R_k, R_v, clip_k, clip_v, slots, codes, sz, md, stream);
+    }
+  }
   const size_t smem = (static_cast<size_t>(D) * D + kTokTile * D) * sizeof(float);
   cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(append_kernel<D>), smem);
   if (e != cudaSuccess) return e;
@@ -362,6 +623,9 @@ oscar_status_t run_append(const oscar_dims_t* dims, int64_t num_tokens, const vo
   if (num_tokens < 0) return OSCAR_ERR_INVALID_ARG;
   if (num_tokens == 0) return OSCAR_OK;
   if (!k || !v || !R_k || !R_v || !clip_k || !clip_v || !slot_mapping || !int2_pages || !scale_zero_pages)
+    return OSCAR_ERR_INVALID_ARG;
+  if (misaligned16(k) || misaligned16(v) || misaligned16(R_k) || misaligned16(R_v) || misaligned16(int2_pages) ||
+      misaligned16(scale_zero_pages) || misaligned16(md.sink) || misaligned16(md.win))
     return OSCAR_ERR_INVALID_ARG;
   if ((num_tokens + kTokTile - 1) / kTokTile > 0x7fffffffLL) return OSCAR_ERR_UNSUPPORTED;
   cudaError_t e = dims->head_dim == 128
@@ -417,6 +681,7 @@ extern "C" oscar_status_t oscar_bf16_append(const oscar_dims_t* dims, int64_t nu
   if (num_tokens < 0) return OSCAR_ERR_INVALID_ARG;
   if (num_tokens == 0) return OSCAR_OK;
   if (!k || !v || !slot_mapping || !bf16_pages) return OSCAR_ERR_INVALID_ARG;
+  if (misaligned16(k) || misaligned16(v) || misaligned16(bf16_pages)) return OSCAR_ERR_INVALID_ARG;
   const int64_t total = num_tokens * dims->num_kv_heads * 2 * (dims->head_dim / 8);
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;

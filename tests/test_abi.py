@@ -63,6 +63,21 @@ def test_append_validation(lib):
     assert _append(lib, _dims(), T=-1) == ok.OSCAR_ERR_INVALID_ARG
     assert _append(lib, _dims(), T=0) == ok.OSCAR_OK  # no-op
     assert _append(lib, _dims(), ptr=None) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append(lib, _dims(), ptr=ctypes.c_void_p(18)) == ok.OSCAR_ERR_INVALID_ARG  # misaligned
+
+
+def test_append_rejects_each_misaligned_buffer(lib):
+    # k, v, R_k, R_v and both pools: each one 2 bytes off a 16-byte boundary is refused.
+    bad = ctypes.c_void_p(18)
+    for i in (0, 1, 2, 3, 7, 8):
+        a = [P] * 9
+        a[i] = bad
+        rc = lib.oscar_append(ctypes.byref(_dims()), 4, a[0], a[1], a[2], a[3], a[4], a[5], None, a[6], a[7], a[8],
+                              None)
+        assert rc == ok.OSCAR_ERR_INVALID_ARG, i
+    d = _dims(); bd = ok.OSCAR_ERR_INVALID_ARG
+    assert lib.oscar_bf16_append(ctypes.byref(d), 4, bad, P, P, P, None) == bd
+    assert lib.oscar_bf16_append(ctypes.byref(d), 4, P, P, P, bad, None) == bd
 
 
 def _append_mixed(lib, dims, T=4, ptr=P, batch=2, S=4, W=8, sink=P, win=P, ids=P):
@@ -81,6 +96,8 @@ def test_append_mixed_validation(lib):
     assert _append_mixed(lib, _dims(), S=0, sink=None, W=0, win=None, T=0) == ok.OSCAR_OK  # no-op
     assert _append_mixed(lib, _dims(head_dim=96, group_size=32)) == ok.OSCAR_ERR_UNSUPPORTED
     assert _append_mixed(lib, _dims(), ptr=None) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append_mixed(lib, _dims(), sink=ctypes.c_void_p(20)) == ok.OSCAR_ERR_INVALID_ARG  # misaligned
+    assert _append_mixed(lib, _dims(), win=ctypes.c_void_p(24)) == ok.OSCAR_ERR_INVALID_ARG
 
 
 def _decode(lib, dims, batch=2, msl=100, pps=8, S=4, W=8, ws_bytes=1 << 30, ws=ctypes.c_void_p(256), sink=P):

@@ -77,6 +77,37 @@ def test_append_prefill_config_sampled():
     check_append(w, codes, sz, w.k, w.v, w.slot_mapping.numpy(), sample=sample)
 
 
+@pytest.mark.parametrize("G", [32, 64, 128])
+@pytest.mark.parametrize("H", [1, 3])
+def test_append_tensor_core_rotation_sweep(G, H):
+    # > 512 tokens at D = 128: the tensor-core rotation (64-token tiles; 1000 = 15 tiles + a
+    # ragged 40) into random distinct slots, some skipped.
+    T = 1000
+    w = synth.make_workload(num_q_heads=H, num_kv_heads=H, head_dim=128, group_size=G, sink_len=0, window_len=0,
+                            seq_lens=[T], seed=G + 11 * H, spare_pages=9)
+    g = torch.Generator().manual_seed(G * 5 + H)
+    slots = torch.randperm(w.num_pages * 16, generator=g)[:T].to(torch.int64)
+    slots[0] = -1
+    slots[999] = -1
+    slots[517] = -3
+    cache = Int2Cache(w)
+    cache.append(w.k.cuda(), w.v.cuda(), slots.cuda())
+    torch.cuda.synchronize()
+    codes, sz = pools_to_host(cache)
+    check_append(w, codes, sz, w.k, w.v, slots.numpy())
+
+
+def test_append_tensor_core_identity_rotation_exact():
+    # R = I splits into (1, 0, 0) exactly, so the tensor-core path quantises the raw bf16 values.
+    w = synth.make_workload(num_q_heads=2, num_kv_heads=2, head_dim=128, group_size=64, sink_len=0, window_len=0,
+                            seq_lens=[600], seed=5, clip_frac=None)
+    w.R_k = torch.eye(128).expand(2, 128, 128).contiguous()
+    w.R_v = w.R_k.clone()
+    cache = Int2Cache(w)
+    codes, sz = _append_all(w, cache)
+    check_append(w, codes, sz, w.k, w.v, w.slot_mapping.numpy(), exact=True)
+
+
 def test_append_decode_batch_random_slots():
     # Decode append: 256 single tokens at random slots of a pool, every token checked.
     w = synth.make_workload(num_q_heads=32, num_kv_heads=8, head_dim=128, group_size=64, sink_len=64,
