@@ -12,6 +12,7 @@
 // group min/max is a warp-shuffle reduction.
 #include "common.cuh"
 #include "ptx.cuh"
+#include "umma.cuh"
 
 namespace {
 
@@ -204,257 +205,409 @@ __global__ void __launch_bounds__(kThreads) append_kernel(
 // fixed warp order through shared memory before the same quantise/store step.
 constexpr int kSmallTok = 8;
 
-// ---- prefill append with the rotation on tensor cores (head_dim 128) -----------
-//
-// y = x . R for tiles of kTcTok tokens of one (KV head, K|V) on mma.sync m16n8k16
-// (bf16 in, fp32 accumulate).  x is bf16 and exact as an operand; R (fp32) is split
-// into three bf16 terms hi + mid + lo (about 24 significant bits), each multiplied
-// in and accumulated in fp32, so y carries fp32-level rounding like the FFMA
-// rotation.  Each CTA serves one (head, K|V) and loops over every gridDim.x-th
-// token tile: R^T's three parts stay in shared memory (split once per CTA), the
-// next tile's x is loaded into registers while the current one is multiplied, and
-// the clip / group min-max / fp16 scale-zero / codes / pack step runs on the
-// accumulators in registers (a quad of lanes holds a token row).  Shared rows are
-// 256 bytes with their 16-byte chunks XOR-swizzled by row, so ldmatrix reads are
-// conflict free.  Each of the 4 warps computes 16 tokens x 128 outputs.
-constexpr int kTcTok = 64;
-constexpr int kTcThreads = 128;
-constexpr int kTcLoads = kTcTok * 16 / kTcThreads;     // 16-byte chunks of x per thread per tile
-constexpr size_t kTcSmem = (3 * 128 + kTcTok) * 256;  // R^T parts, x tile: two CTAs fit an SM
-
-__device__ __forceinline__ uint32_t swz(int row, int chunk) { return row * 256 + ((chunk ^ (row & 7)) << 4); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
+// Two bf16 values as one 32-bit word (lo in the low half).
 __device__ __forceinline__ uint32_t bf16_pair(__nv_bfloat16 lo, __nv_bfloat16 hi) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) | (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
 }
 
-// x rows of token tile `tile` (zeros past the end), chunk u*kTcThreads + tid.
-__device__ __forceinline__ void tc_load_x(const __nv_bfloat16* __restrict__ x, int64_t num_tokens, int H, int h,
-                                          int64_t tile, int tid, uint4 (&raw)[kTcLoads]) {
-#pragma unroll
-  for (int u = 0; u < kTcLoads; ++u) {
-    const int it = u * kTcThreads + tid, tt = it >> 4, c = it & 15;
-    const int64_t t = tile * kTcTok + tt;
-    raw[u] = t < num_tokens ? __ldg(reinterpret_cast<const uint4*>(x + (static_cast<size_t>(t) * H + h) * 128) + c)
-                            : make_uint4(0u, 0u, 0u, 0u);
-  }
+// ---- prefill append on tcgen05 (head_dim 128) ---------------------------------------
+//
+// One CTA per SM serves a share of the 128-token tiles of one (KV head, K|V):
+//   * y = x . R for a tile is one UMMA chain of M = 128 tokens, N = 128 outputs and
+//     K = 3 x 128: R (fp32) is split into three bf16 terms hi + mid + lo (about 24
+//     significant bits), stored once as R^T in shared memory, and the same x tile
+//     multiplies each term, accumulating in fp32 in TMEM;
+//   * warp 0 streams x tiles by TMA (3-D map: channel, head, token; 128-byte swizzle)
+//     into a 3-stage ring; warp 1 owns the TMEM allocation and issues the MMAs;
+//   * kUmGroups groups of 4 epilogue warps take tiles in turn (one TMEM accumulator
+//     each); a thread owns one token row: a first pass over its 128 outputs clips
+//     and takes the group min/max, a second pass forms the codes and packs them.
+// Codes: u = (y - zero) / scale is formed as (y - zero) * (1 / scale), whose
+// rounding to an integer equals that of the correctly rounded quotient unless u
+// lies within 2^-18 of a half-integer; a 32-channel chunk with such an element is
+// recomputed with the quotient itself.
+constexpr int kUmTok = 128;
+constexpr int kUmStages = 3;
+constexpr int kUmGroups = 4;
+constexpr int kUmThreads = 64 + 128 * kUmGroups;
+constexpr uint32_t kUmXBytes = kUmTok * 128 * 2;  // one x tile (two K blocks of 16 KB)
+constexpr uint32_t kUmRPart = 128 * 128 * 2;      // one bf16 term of R^T
+constexpr uint32_t kUmTmemCols = 128 * kUmGroups; // one 128-column fp32 accumulator per group
+static_assert(kUmTmemCols == 512 || kUmTmemCols == 256, "TMEM allocation must be a power of two");
+// barriers: x_full, x_empty per stage; acc_full, acc_empty per group
+constexpr int kUmBars = 2 * kUmStages + 2 * kUmGroups;
+// R^T terms | x stages | clip | mbarriers | TMEM address, counters; +1 KB to align to 1024
+constexpr size_t kUmSmem = 1024 + 3 * kUmRPart + kUmStages * kUmXBytes + 128 * 4 + kUmBars * 8 + 16;
+
+// Exact code of one value (the quotient path of the append's rule).
+__device__ __forceinline__ uint32_t exact_code(float y, float z, float s) {
+  return s != 0.f ? static_cast<uint32_t>(fminf(fmaxf(rintf((y - z) / s), 0.f), 3.f)) : 0u;
 }
 
 template <int G>
-__global__ void __launch_bounds__(kTcThreads, 2) append_tc_kernel(
-    int64_t num_tokens, int H, int num_pages, const __nv_bfloat16* __restrict__ k,
-    const __nv_bfloat16* __restrict__ v, const float* __restrict__ R_k, const float* __restrict__ R_v,
-    const float* __restrict__ clip_k, const float* __restrict__ clip_v, const int64_t* __restrict__ slots,
-    uint8_t* __restrict__ codes, __half* __restrict__ sz, MixedDst md) {
+__global__ void __launch_bounds__(kUmThreads, 1) append_umma_kernel(
+    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v, int64_t num_tokens, int H,
+    int num_pages, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+    const float* __restrict__ R_k, const float* __restrict__ R_v, const float* __restrict__ clip_k,
+    const float* __restrict__ clip_v, const int64_t* __restrict__ slots, uint8_t* __restrict__ codes,
+    __half* __restrict__ sz, MixedDst md) {
   grid_dep_launch_dependents();  // a following q-rotation (reads neither output) may start
-  constexpr int D = 128, NPG = G / 8, NGRP = D / G;  // n-tiles per group, groups per row
-  extern __shared__ __align__(128) uint8_t tsm[];
-  __shared__ int64_t dst_row[kTcTok];
-  __shared__ int dst_buf[kTcTok];
+  constexpr int D = 128, NGRP = D / G;
+  extern __shared__ uint8_t usm_raw[];
+  uint8_t* usm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(usm_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t r_s = smem_u32(usm);       // 3 terms of R^T, K-major, swizzled
+  const uint32_t x_s = r_s + 3 * kUmRPart;  // x stages
+  float* clip_s = reinterpret_cast<float*>(usm + 3 * kUmRPart + kUmStages * kUmXBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(clip_s + 128);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kUmBars);
+  uint32_t* flags = tmem_slot + 1;  // [0]: x tiles requested, [1]: x tiles consumed, [2]: MMA chains committed
+  auto x_full = [&](int st) { return smem_u32(&bars[st]); };
+  auto x_empty = [&](int st) { return smem_u32(&bars[kUmStages + st]); };
+  auto acc_full = [&](int g) { return smem_u32(&bars[2 * kUmStages + g]); };
+  auto acc_empty = [&](int g) { return smem_u32(&bars[2 * kUmStages + kUmGroups + g]); };
   const int h = blockIdx.y, kv = blockIdx.z;
-  const float* R = (kv ? R_v : R_k) + static_cast<size_t>(h) * D * D;
-  const __nv_bfloat16* x = kv ? v : k;
-  const uint32_t rt = smem_u32(tsm);       // R^T part p: rows n at rt + p * 128 * 256
-  const uint32_t xt = rt + 3 * 128 * 256;  // x tile: token rows
-  const float* clip = (kv ? clip_v : clip_k) + static_cast<size_t>(h) * D;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t ntiles = (num_tokens + kTcTok - 1) / kTcTok;
+  const int64_t ntiles = (num_tokens + kUmTok - 1) / kUmTok;
+  const int per = gridDim.x, j0 = blockIdx.x;
+  const int n_my = static_cast<int>((ntiles - j0 + per - 1) / per);  // tiles j0, j0 + per, ...
+  const float* R = (kv ? R_v : R_k) + static_cast<size_t>(h) * D * D;
+  const CUtensorMap* map = kv ? &map_v : &map_k;
 
-  uint4 raw[kTcLoads];
-  tc_load_x(x, num_tokens, H, h, blockIdx.x, tid, raw);  // the first tile's x is in flight during the split
-  // R^T in three bf16 parts.  Thread: k pair kp = tid % 64 (rows 2kp, 2kp + 1 of R),
-  // 4 consecutive n per item; a warp's stores fall on 32 distinct banks.
-  {
-    const int kp = tid & 63;
-#pragma unroll 1
-    for (int b = 0; b < 2; ++b) {
-      float4 r0[8], r1[8];
+  if (tid == 0) {
+    for (int i = 0; i < kUmStages; ++i) {
+      mbar_init(x_full(i), 1);
+      mbar_init(x_empty(i), 1);
+    }
+    for (int g = 0; g < kUmGroups; ++g) {
+      mbar_init(acc_full(g), 1);
+      mbar_init(acc_empty(g), 4);
+    }
+    flags[0] = flags[1] = flags[2] = 0;
+    umma::prefetch_map(map);
+    mbar_init_fence();
+  }
+  if (warp == 1) umma::tmem_alloc(smem_u32(tmem_slot), kUmTmemCols);
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  // The first x tiles are requested before R^T is built (they do not depend on it).
+  const int first_issue = n_my < kUmStages ? n_my : kUmStages;
+  if (tid == 0) {
+    for (int i = 0; i < first_issue; ++i) {
+      const int t0 = static_cast<int>((j0 + static_cast<int64_t>(i) * per) * kUmTok);
+      mbar_arrive_expect_tx(x_full(i), kUmXBytes);
+      umma::tma_load_3d(x_s + i * kUmXBytes, map, 0, h, t0, x_full(i));
+      umma::tma_load_3d(x_s + i * kUmXBytes + kUmXBytes / 2, map, 64, h, t0, x_full(i));
+    }
+    flags[0] = first_issue;
+  }
+  // R^T terms: thread item (k pair kp, 4 outputs n4) reads R[2kp][4n4 ..] and
+  // R[2kp + 1][4n4 ..]; a warp's 32 consecutive kp store 32 distinct banks.
+  for (int it0 = 0; it0 < 64 * 32; it0 += kUmThreads * 2) {
+    float4 a0[2], a1[2];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int n4 = 2 * (8 * b + u) + (tid >> 6);
-        r0[u] = __ldg(reinterpret_cast<const float4*>(R + static_cast<size_t>(2 * kp) * D) + n4);
-        r1[u] = __ldg(reinterpret_cast<const float4*>(R + static_cast<size_t>(2 * kp + 1) * D) + n4);
+    for (int u = 0; u < 2; ++u) {
+      const int it = it0 + u * kUmThreads + tid;
+      if (it < 64 * 32) {
+        const int kp = it & 63, n4 = it >> 6;
+        a0[u] = __ldg(reinterpret_cast<const float4*>(R + static_cast<size_t>(2 * kp) * D) + n4);
+        a1[u] = __ldg(reinterpret_cast<const float4*>(R + static_cast<size_t>(2 * kp + 1) * D) + n4);
       }
+    }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int n4 = 2 * (8 * b + u) + (tid >> 6);
-        const float a0[4] = {r0[u].x, r0[u].y, r0[u].z, r0[u].w}, a1[4] = {r1[u].x, r1[u].y, r1[u].z, r1[u].w};
+    for (int u = 0; u < 2; ++u) {
+      const int it = it0 + u * kUmThreads + tid;
+      if (it < 64 * 32) {
+        const int kp = it & 63, n4 = it >> 6;
+        const float e0[4] = {a0[u].x, a0[u].y, a0[u].z, a0[u].w}, e1[4] = {a1[u].x, a1[u].y, a1[u].z, a1[u].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const __nv_bfloat16 h0 = __float2bfloat16_rn(a0[i]), h1 = __float2bfloat16_rn(a1[i]);
-          const float e0 = a0[i] - __bfloat162float(h0), e1 = a1[i] - __bfloat162float(h1);
-          const __nv_bfloat16 m0 = __float2bfloat16_rn(e0), m1 = __float2bfloat16_rn(e1);
-          const __nv_bfloat16 l0 = __float2bfloat16_rn(e0 - __bfloat162float(m0));
-          const __nv_bfloat16 l1 = __float2bfloat16_rn(e1 - __bfloat162float(m1));
-          const uint32_t off = rt + swz(4 * n4 + i, kp >> 2) + (kp & 3) * 4;
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(e0[i]), h1 = __float2bfloat16_rn(e1[i]);
+          const float d0 = e0[i] - __bfloat162float(h0), d1 = e1[i] - __bfloat162float(h1);
+          const __nv_bfloat16 m0 = __float2bfloat16_rn(d0), m1 = __float2bfloat16_rn(d1);
+          const __nv_bfloat16 l0 = __float2bfloat16_rn(d0 - __bfloat162float(m0));
+          const __nv_bfloat16 l1 = __float2bfloat16_rn(d1 - __bfloat162float(m1));
+          const uint32_t off = r_s + umma::sw128_offset(4 * n4 + i, 2 * kp, 128);
           asm volatile("st.shared.b32 [%0], %1;" ::"r"(off), "r"(bf16_pair(h0, h1)) : "memory");
-          asm volatile("st.shared.b32 [%0], %1;" ::"r"(off + 128 * 256), "r"(bf16_pair(m0, m1)) : "memory");
-          asm volatile("st.shared.b32 [%0], %1;" ::"r"(off + 2 * 128 * 256), "r"(bf16_pair(l0, l1)) : "memory");
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(off + kUmRPart), "r"(bf16_pair(m0, m1)) : "memory");
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(off + 2 * kUmRPart), "r"(bf16_pair(l0, l1)) : "memory");
         }
       }
     }
   }
+  if (tid < D) clip_s[tid] = __ldg((kv ? clip_v : clip_k) + static_cast<size_t>(h) * D + tid);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // R^T visible to the tensor cores
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
 
-  const int a_row = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1), a_hi = lane >> 4;
-  const int b_row = (lane & 7) + 8 * (lane >> 4), b_hi = (lane >> 3) & 1;
-  const int g = lane >> 2, tq = lane & 3;
+  if (warp == 0) {
+    // ---- TMA producer ----
+    if (lane == 0) {
+      int i = first_issue;
+      for (; i < n_my; ++i) {
+        const int st = i % kUmStages;
+        if (!mbar_wait_bounded(x_empty(st), ((i / kUmStages) - 1) & 1)) break;
+        const int t0 = static_cast<int>((j0 + static_cast<int64_t>(i) * per) * kUmTok);
+        mbar_arrive_expect_tx(x_full(st), kUmXBytes);
+        umma::tma_load_3d(x_s + st * kUmXBytes, map, 0, h, t0, x_full(st));
+        umma::tma_load_3d(x_s + st * kUmXBytes + kUmXBytes / 2, map, 64, h, t0, x_full(st));
+        flags[0] = i + 1;
+      }
+      if (i < n_my) record_error(OSCAR_DEVERR_TIMEOUT);
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer: tile i accumulates in TMEM columns 128 (i % kUmGroups) ----
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma::idesc_bf16_f32(128, 128);
+      int i = 0;
+      for (; i < n_my; ++i) {
+        const int st = i % kUmStages, b = i % kUmGroups;
+        if (!mbar_wait_bounded(x_full(st), (i / kUmStages) & 1)) break;
+        flags[1] = i + 1;
+        if (i >= kUmGroups && !mbar_wait_bounded(acc_empty(b), ((i / kUmGroups) - 1) & 1)) break;
+        umma::fence_after_sync();
+        const uint32_t d = tmem + b * 128;
 #pragma unroll 1
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const int64_t t0 = tile * kTcTok;
-    __syncthreads();  // the previous tile's x reads are done (first pass: R^T is stored)
-    if (md.active()) {
-      if (tid < kTcTok) {
-        const int64_t t = t0 + tid;
+        for (int part = 0; part < 3; ++part)
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t koff = (ks >> 2) * (kUmXBytes / 2) + (ks & 3) * 32;
+            umma::mma_bf16(d, umma::desc_k_sw128(x_s + st * kUmXBytes + koff),
+                           umma::desc_k_sw128(r_s + part * kUmRPart + koff), idesc, (part | ks) != 0);
+          }
+        umma::commit(x_empty(st));  // the x stage may be refilled
+        umma::commit(acc_full(b));  // the accumulator is ready
+        flags[2] = i + 1;
+      }
+      if (i < n_my) record_error(OSCAR_DEVERR_TIMEOUT);
+    }
+  } else {
+    // ---- epilogue: group e takes local tiles e, e + kUmGroups, ...; thread = token row ----
+    const int e = (warp - 2) >> 2, q = warp & 3;  // TMEM lanes 32q .. 32q + 31
+    const int row = 32 * q + lane;
+    const float4* clip4 = reinterpret_cast<const float4*>(clip_s);
+    for (int i = e; i < n_my; i += kUmGroups) {
+      const int64_t t = (j0 + static_cast<int64_t>(i) * per) * kUmTok + row;
+      const int64_t slot = t < num_tokens ? __ldg(slots + t) : -1;  // in flight during the wait
+      const bool ok = mbar_wait_bounded(acc_full(e), (i / kUmGroups) & 1);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) record_error(OSCAR_DEVERR_TIMEOUT);
+        break;
+      }
+      umma::fence_after_sync();
+      const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + e * 128;
+      // pass 1: clip (written back to TMEM), group min / max (four independent chains per chunk)
+      float mn[NGRP], mx[NGRP];
+#pragma unroll
+      for (int gi = 0; gi < NGRP; ++gi) {
+        mn[gi] = INFINITY;
+        mx[gi] = -INFINITY;
+      }
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t vb[32];
+        umma::tmem_ld32(ta + 32 * c, vb);
+        umma::tmem_ld_wait();
+        float lo[4] = {INFINITY, INFINITY, INFINITY, INFINITY}, hi[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 cl = clip4[8 * c + i4];
+          const float cv[4] = {cl.x, cl.y, cl.z, cl.w};
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const float y = fminf(fmaxf(__uint_as_float(vb[4 * i4 + r]), -cv[r]), cv[r]);
+            vb[4 * i4 + r] = __float_as_uint(y);
+            lo[r] = fminf(lo[r], y);
+            hi[r] = fmaxf(hi[r], y);
+          }
+        }
+        umma::tmem_st32(ta + 32 * c, vb);
+        const float cmn = fminf(fminf(lo[0], lo[1]), fminf(lo[2], lo[3]));
+        const float cmx = fmaxf(fmaxf(hi[0], hi[1]), fmaxf(hi[2], hi[3]));
+#pragma unroll
+        for (int gi = 0; gi < NGRP; ++gi) {
+          const bool hit = gi == 32 * c / G;
+          mn[gi] = hit ? fminf(mn[gi], cmn) : mn[gi];
+          mx[gi] = hit ? fmaxf(mx[gi], cmx) : mx[gi];
+        }
+      }
+      umma::tmem_st_wait();
+      float zg[NGRP], sg[NGRP], ig[NGRP];
+      bool fastg[NGRP];
+      uint32_t szw[NGRP];
+#pragma unroll
+      for (int gi = 0; gi < NGRP; ++gi) {
+        const __half sh = __float2half_rn((mx[gi] - mn[gi]) / 3.0f);
+        const __half zh = __float2half_rn(mn[gi]);
+        szw[gi] = static_cast<uint32_t>(__half_as_ushort(sh)) | (static_cast<uint32_t>(__half_as_ushort(zh)) << 16);
+        sg[gi] = __half2float(sh);
+        zg[gi] = __half2float(zh);
+        ig[gi] = sg[gi] != 0.f ? 1.0f / sg[gi] : 0.f;  // scale 0: every code is 0
+        // u = (y - zero) * (1 / scale) is monotone in y: when it spans [-0.5, 3.5) at the
+        // group's extremes, rint(u) is a code 0..3 without clamping.
+        fastg[gi] = (mn[gi] - zg[gi]) * ig[gi] >= -0.5f && (mx[gi] - zg[gi]) * ig[gi] < 3.5f;
+      }
+      const bool store = slot >= 0 && slot < static_cast<int64_t>(num_pages) * kPageSize;
+      const size_t rrow = store ? ((static_cast<size_t>(slot / kPageSize) * H + h) * 2 + kv) * kPageSize +
+                                      static_cast<size_t>(slot % kPageSize)
+                                : 0;
+      uint2* crow = reinterpret_cast<uint2*>(codes + rrow * (D / 4));
+      // pass 2: codes, two packed words (8 bytes of the row) per 32-channel chunk.
+      // m = u + 1.5 * 2^23 rounds u to an integer (ties to even) whose value is the low
+      // bits of m, so bits(m) = bits(1.5 * 2^23) + code; the 16 codes of a word are
+      // summed as bits(m_j) * 4^j and the constant part is taken off once.
+      constexpr float kRound = 12582912.0f;
+      constexpr uint32_t kWordBias = 0x4B400000u * 0x55555555u;  // bits(kRound) * sum_j 4^j (mod 2^32)
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float z = zg[0], inv = ig[0], s = sg[0];
+        bool fast = fastg[0];
+#pragma unroll
+        for (int gi = 1; gi < NGRP; ++gi) {
+          const bool hit = gi == 32 * c / G;
+          z = hit ? zg[gi] : z;
+          inv = hit ? ig[gi] : inv;
+          s = hit ? sg[gi] : s;
+          fast = hit ? fastg[gi] : fast;
+        }
+        uint32_t vb[32];
+        umma::tmem_ld32(ta + 32 * c, vb);
+        umma::tmem_ld_wait();
+        const uint64_t z2 = umma::f2_pack(z, z), inv2 = umma::f2_pack(inv, inv), kr2 = umma::f2_pack(kRound, kRound);
+        uint32_t w[2] = {0u - kWordBias, 0u - kWordBias};
+        float emax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const uint64_t y2 = umma::f2_pack(__uint_as_float(vb[j]), __uint_as_float(vb[j + 1]));
+          const uint64_t u2 = umma::f2_mul(umma::f2_sub(y2, z2), inv2);
+          const uint64_t m2 = umma::f2_add(u2, kr2);
+          const uint64_t r2 = umma::f2_sub(u2, umma::f2_sub(m2, kr2));  // u - rint(u), exact
+          float m0, m1, e0, e1;
+          umma::f2_unpack(m2, m0, m1);
+          umma::f2_unpack(r2, e0, e1);
+          emax = fmaxf(emax, fmaxf(fabsf(e0), fabsf(e1)));
+          w[j >> 4] += __float_as_uint(m0) * (1u << (2 * (j & 15)));
+          w[j >> 4] += __float_as_uint(m1) * (1u << (2 * ((j + 1) & 15)));
+        }
+        if (__any_sync(0xffffffffu, !fast || emax > 0.5f - 0x1p-18f)) {
+          // out-of-range values or one near a rounding boundary in the warp's chunk: the
+          // quotient itself, clamped (the clipped values are in TMEM)
+          w[0] = w[1] = 0u;
+#pragma unroll 1
+          for (int j = 0; j < 32; ++j) {
+            uint32_t one;
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(one) : "r"(ta + 32 * c + j) : "memory");
+            umma::tmem_ld_wait();
+            const uint32_t code = exact_code(__uint_as_float(one), z, s);
+            if (j < 16) w[0] |= code << (2 * j);
+            else w[1] |= code << (2 * (j - 16));
+          }
+        }
+        if (store) crow[c] = make_uint2(w[0], w[1]);
+      }
+      umma::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(e));  // the accumulator may be overwritten
+
+      if (t >= num_tokens) continue;
+      if (md.active()) {  // oscar_append_mixed: the token's bf16 row (sink or window)
         int which = 0;
-        dst_row[tid] = t < num_tokens ? mixed_row(md, t, __ldg(slots + t), H, D, h, kv, &which) : -1;
-        dst_buf[tid] = which;
-      }
-      __syncthreads();
-    }
-#pragma unroll
-    for (int u = 0; u < kTcLoads; ++u) {
-      const int it = u * kTcThreads + tid, tt = it >> 4, c = it & 15;
-      if (md.active() && t0 + tt < num_tokens && dst_row[tt] >= 0)  // oscar_append_mixed: the bf16 row
-        reinterpret_cast<uint4*>((dst_buf[tt] ? md.win : md.sink) + dst_row[tt])[c] = raw[u];
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(xt + swz(tt, c)), "r"(raw[u].x), "r"(raw[u].y),
-                   "r"(raw[u].z), "r"(raw[u].w)
-                   : "memory");
-    }
-    __syncthreads();
-    tc_load_x(x, num_tokens, H, h, tile + gridDim.x, tid, raw);  // next tile (zeros past the end)
-
-    // y[16 tokens of this warp][128] = x . (R_hi + R_mid + R_lo)
-    float acc[16][4];
-#pragma unroll
-    for (int n = 0; n < 16; ++n)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[n][c] = 0.f;
-#pragma unroll 1
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(xt + swz(a_row, 2 * ks + a_hi), a0, a1, a2, a3);
-#pragma unroll
-      for (int part = 0; part < 3; ++part) {
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {  // n-tiles 2np, 2np + 1
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(rt + part * 128 * 256 + swz(16 * np + b_row, 2 * ks + b_hi), b0, b1, b2, b3);
-          mma_bf16_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
-          mma_bf16_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+        const int64_t dst = mixed_row(md, t, slot, H, D, h, kv, &which);
+        if (dst >= 0) {
+          const uint4* src = reinterpret_cast<const uint4*>((kv ? v : k) + (static_cast<size_t>(t) * H + h) * D);
+          uint4* out = reinterpret_cast<uint4*>((which ? md.win : md.sink) + dst);
+#pragma unroll 4
+          for (int c = 0; c < D / 8; ++c) out[c] = __ldg(src + c);
         }
       }
-    }
-
-    // Quantise from the accumulators.  Quad g of the warp holds tokens 16w + g (elements
-    // 0, 1) and 16w + g + 8 (elements 2, 3); lane tq holds channels 8n + 2tq, 8n + 2tq + 1.
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int64_t t = t0 + 16 * warp + g + 8 * hf;
-      int64_t slot = t < num_tokens ? __ldg(slots + t) : -1;
       if (slot >= static_cast<int64_t>(num_pages) * kPageSize) {
-        if (tq == 0) record_error(OSCAR_DEVERR_SLOT);
-        slot = -1;
+        record_error(OSCAR_DEVERR_SLOT);
+        continue;
       }
-      uint32_t szw[NGRP];  // (scale, zero) of each group as stored: scale in the low half
-      uint32_t nib[16];
-#pragma unroll
-      for (int j = 0; j < NGRP; ++j) {
-        float mn = INFINITY, mx = -INFINITY;
-#pragma unroll
-        for (int n = j * NPG; n < (j + 1) * NPG; ++n)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float cl = __ldg(clip + 8 * n + 2 * tq + e);
-            const float y = fminf(fmaxf(acc[n][2 * hf + e], -cl), cl);
-            acc[n][2 * hf + e] = y;
-            mn = fminf(mn, y);
-            mx = fmaxf(mx, y);
-          }
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const __half sh = __float2half_rn((mx - mn) / 3.0f);
-        const __half zh = __float2half_rn(mn);
-        szw[j] = static_cast<uint32_t>(__half_as_ushort(sh)) | (static_cast<uint32_t>(__half_as_ushort(zh)) << 16);
-        const float s = __half2float(sh), z = __half2float(zh);
-#pragma unroll
-        for (int n = j * NPG; n < (j + 1) * NPG; ++n) {
-          uint32_t c2 = 0;
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            uint32_t code = 0;
-            if (s != 0.f) {
-              const float uq = (acc[n][2 * hf + e] - z) / s;
-              code = static_cast<uint32_t>(fminf(fmaxf(rintf(uq), 0.f), 3.f));
-            }
-            c2 |= code << (2 * e);
-          }
-          nib[n] = c2;
-        }
-      }
-      // Channel 8n + 2tq + e is byte 2n + tq / 2, bits 4 (tq & 1) + 2e: the quad's four
-      // nibbles of n-tile n form 16 bits; n-tiles 2w, 2w + 1 form the row's word w.
-      uint32_t word[8];
-#pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        uint32_t vw = (nib[2 * w] | (nib[2 * w + 1] << 16)) << (4 * tq);
-        vw |= __shfl_xor_sync(0xffffffffu, vw, 1);
-        vw |= __shfl_xor_sync(0xffffffffu, vw, 2);
-        word[w] = vw;
-      }
-      if (slot >= 0) {
-        const int64_t page = slot / kPageSize;
-        const int off = static_cast<int>(slot % kPageSize);
-        const size_t row = ((static_cast<size_t>(page) * H + h) * 2 + kv) * kPageSize + off;
-        uint32_t lo = word[0], hi = word[1];
-#pragma unroll
-        for (int q = 1; q < 4; ++q)
-          if (tq == q) {
-            lo = word[2 * q];
-            hi = word[2 * q + 1];
-          }
-        reinterpret_cast<uint2*>(codes + row * (D / 4))[tq] = make_uint2(lo, hi);
-        if (tq == 0) {  // the row's NGRP pairs in one store
-          void* dst = sz + row * NGRP * 2;
-          if constexpr (NGRP == 4) *static_cast<uint4*>(dst) = make_uint4(szw[0], szw[1], szw[2], szw[3]);
-          if constexpr (NGRP == 2) *static_cast<uint2*>(dst) = make_uint2(szw[0], szw[1]);
-          if constexpr (NGRP == 1) *static_cast<uint32_t*>(dst) = szw[0];
-        }
-      }
+      if (!store) continue;
+      void* zdst = sz + rrow * NGRP * 2;
+      if constexpr (NGRP == 4) *static_cast<uint4*>(zdst) = make_uint4(szw[0], szw[1], szw[2], szw[3]);
+      if constexpr (NGRP == 2) *static_cast<uint2*>(zdst) = make_uint2(szw[0], szw[1]);
+      if constexpr (NGRP == 1) *static_cast<uint32_t*>(zdst) = szw[0];
     }
+  }
+
+  // ---- teardown: nothing of this CTA may still be in flight ----
+  __syncthreads();
+  if (tid == 0) {
+    // x tiles requested but never consumed (only after a timeout)
+    for (uint32_t i = flags[1]; i < flags[0]; ++i) mbar_wait_bounded(x_full(i % kUmStages), (i / kUmStages) & 1);
+    // the last committed MMA chain (both of its completion barriers)
+    if (flags[2] > 0) {
+      const uint32_t i = flags[2] - 1;
+      mbar_wait_bounded(acc_full(i % kUmGroups), (i / kUmGroups) & 1);
+      mbar_wait_bounded(x_empty(i % kUmStages), (i / kUmStages) & 1);
+    }
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    umma::fence_after_sync();
+    umma::tmem_dealloc(tmem, kUmTmemCols);
   }
 }
 
+// cuTensorMapEncodeTiled, taken from the driver through the runtime (no link
+// against the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Map of x [T][H][128] bf16 as (channel, head, token) with a 64 x 1 x 128 box:
+// one K block (64 channels) of 128 tokens of one head, 128-byte swizzled.
+bool x_tensor_map(CUtensorMap* m, const void* x, int64_t T, int H) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+  const cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(H) * 256};
+  const cuuint32_t box[3] = {64, 1, kUmTok};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int G>
-cudaError_t launch_append_tc(int64_t T, const oscar_dims_t* d, const void* k, const void* v, const float* R_k,
-                             const float* R_v, const float* clip_k, const float* clip_v, const int64_t* slots,
-                             uint8_t* codes, void* sz, const MixedDst& md, cudaStream_t stream) {
-  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(append_tc_kernel<G>), kTcSmem);
+cudaError_t launch_append_umma(int64_t T, const oscar_dims_t* d, const void* k, const void* v, const float* R_k,
+                               const float* R_v, const float* clip_k, const float* clip_v, const int64_t* slots,
+                               uint8_t* codes, void* sz, const MixedDst& md, cudaStream_t stream) {
+  CUtensorMap mk, mv;
+  if (!x_tensor_map(&mk, k, T, d->num_kv_heads) || !x_tensor_map(&mv, v, T, d->num_kv_heads))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(append_umma_kernel<G>), kUmSmem);
   if (e != cudaSuccess) return e;
-  // Two CTAs per SM over all (head, K|V); each loops over its share of the token tiles.
-  const int64_t ntiles = (T + kTcTok - 1) / kTcTok;
+  // One CTA per SM: the (KV head, K|V) pairs share the SMs evenly, each CTA takes
+  // every per-th tile of its pair.
+  const int64_t ntiles = (T + kUmTok - 1) / kUmTok;
   const int hkv = 2 * d->num_kv_heads;
-  int64_t per = (2 * static_cast<int64_t>(num_sms()) + hkv - 1) / hkv;
+  int64_t per = num_sms() / hkv;
+  if (per < 1) per = 1;
   if (per > ntiles) per = ntiles;
   const dim3 grid(static_cast<unsigned>(per), d->num_kv_heads, 2);
-  append_tc_kernel<G><<<grid, kTcThreads, kTcSmem, stream>>>(
-      T, d->num_kv_heads, d->num_pages, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
-      R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz), md);
+  append_umma_kernel<G><<<grid, kUmThreads, kUmSmem, stream>>>(
+      mk, mv, T, d->num_kv_heads, d->num_pages, static_cast<const __nv_bfloat16*>(k),
+      static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz), md);
   return cudaGetLastError();
 }
 
@@ -593,11 +746,11 @@ cudaError_t launch_append(int64_t T, const oscar_dims_t* d, const void* k, const
         static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz), md);
     return cudaGetLastError();
   }
-  if constexpr (D == 128) {  // the rotation on tensor cores
+  if (D == 128 && T < 0x7fffffffLL - kUmTok) {  // the rotation on tcgen05 tensor cores
     switch (d->group_size) {
-      case 32: return launch_append_tc<32>(T, d, k, v, R_k, R_v, clip_k, clip_v, slots, codes, sz, md, stream);
-      case 64: return launch_append_tc<64>(T, d, k, v, R_k, R_v, clip_k, clip_v, slots, codes, sz, md, stream);
-      default: return launch_append_tc<128>(T, d, k, v, R_k, R_v, clip_k, clip_v, slots, codes, sz, md, stream);
+      case 32: return launch_append_umma<32>(T, d, k, v, R_k, R_v, clip_k, clip_v, slots, codes, sz, md, stream);
+      case 64: return launch_append_umma<64>(T, d, k, v, R_k, R_v, clip_k, clip_v, slots, codes, sz, md, stream);
+      default: return launch_append_umma<128>(T, d, k, v, R_k, R_v, clip_k, clip_v, slots, codes, sz, md, stream);
     }
   }
   const size_t smem = (static_cast<size_t>(D) * D + kTokTile * D) * sizeof(float);

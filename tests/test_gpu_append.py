@@ -97,6 +97,41 @@ def test_append_tensor_core_rotation_sweep(G, H):
     check_append(w, codes, sz, w.k, w.v, slots.numpy())
 
 
+def test_append_tensor_core_many_tiles_per_cta():
+    # 8 KV heads, 4685 tokens = 36 full 128-token tiles + a ragged 77: the CTAs of a
+    # (head, K|V) take 4-5 tiles each, so the x ring wraps and both accumulators are used.
+    w = synth.make_workload(num_q_heads=8, num_kv_heads=8, head_dim=128, group_size=64, sink_len=0, window_len=0,
+                            seq_lens=[4685], seed=21, device="cuda")
+    cache = Int2Cache(w)
+    codes, sz = _append_all(w, cache)
+    check_append(w, codes, sz, w.k, w.v, w.slot_mapping.numpy())
+
+
+def test_append_tensor_core_groups_outside_the_code_range():
+    # R = I, no clip, x ~ 1e-6: scale and zero fall in the fp16 subnormal range, where the
+    # rounding of the zero is comparable to the scale, so (y - zero) / scale leaves
+    # [-0.5, 3.5) in some groups and the kernel's clamped quotient path runs there.
+    w = synth.make_workload(num_q_heads=2, num_kv_heads=2, head_dim=128, group_size=64, sink_len=0, window_len=0,
+                            seq_lens=[600], seed=8, clip_frac=None)
+    w.R_k = torch.eye(128).expand(2, 128, 128).contiguous()
+    w.R_v = w.R_k.clone()
+    g = torch.Generator().manual_seed(9)
+    w.k = (1e-6 * (1 + 0.2 * torch.rand(w.k.shape, generator=g))).to(torch.bfloat16)
+    w.v = (-3e-6 * (1 + 0.1 * torch.rand(w.v.shape, generator=g))).to(torch.bfloat16)
+    # the case is present: groups whose extreme values map outside [-0.5, 3.5)
+    y = torch.cat([w.k, w.v]).float().numpy().reshape(-1, 64)
+    mn, mx = y.min(1), y.max(1)
+    sc = ((mx - mn) / np.float32(3)).astype(np.float16).astype(np.float32)
+    z = mn.astype(np.float16).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        inv = np.where(sc != 0, np.float32(1) / sc, np.float32(0)).astype(np.float32)
+    out = ((mn - z) * inv < -0.5) | ((mx - z) * inv >= 3.5)
+    assert out.sum() > 0
+    cache = Int2Cache(w)
+    codes, sz = _append_all(w, cache)
+    check_append(w, codes, sz, w.k, w.v, w.slot_mapping.numpy(), exact=True)
+
+
 def test_append_tensor_core_identity_rotation_exact():
     # R = I splits into (1, 0, 0) exactly, so the tensor-core path quantises the raw bf16 values.
     w = synth.make_workload(num_q_heads=2, num_kv_heads=2, head_dim=128, group_size=64, sink_len=0, window_len=0,
