@@ -21,7 +21,7 @@ _LIB_PATH = os.path.join(_HERE, "liboscar_oracle.so")
 __all__ = [
     "OracleDims", "build_oracle", "load", "bf16_to_f64", "f16_to_f64", "f64_to_f16",
     "rotate", "clip", "group_params", "quantize", "codes_given_params", "append", "append_prequant",
-    "attend_mixed", "dequant_row", "decode", "bf16_decode",
+    "attend_mixed", "dequant_row", "decode", "bf16_decode", "extend",
 ]
 
 
@@ -74,6 +74,9 @@ def load(path: str | None = None):
                                         ctypes.c_int32, _P, _P]),
         "orc_bf16_decode": (ctypes.c_int32, [_P, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_double,
                                              ctypes.c_int32, _P, _P]),
+        "orc_extend": (ctypes.c_int32, [_P, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                        _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                        ctypes.c_int32, _P, _P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -265,6 +268,36 @@ def decode(dims, batch, q_bits, R_k, R_v, int2_pages, scale_zero_pages, sink_bit
                         float(sm_scale), pr.shape[0], _ptr(pr), _ptr(out))
     if rc != 0:
         raise ValueError("oracle decode: page id or length outside the pool / page table")
+    return out
+
+
+def extend(dims, batch, q_bits, row_seq, row_pos, R_k, R_v, int2_pages, scale_zero_pages, sink_bits, window_bits,
+           page_table, seq_lens, sink_len, window_len, sm_scale, pairs=None, lib=None) -> np.ndarray:
+    """Extend attention, fp64 output [n_pairs][D] for (query row, query head) pairs
+    (all pairs in order when ``pairs`` is None); q_bits is [num_rows][Hq][D]."""
+    lib = lib or load()
+    d = _dims(dims)
+    q = _c(q_bits, np.uint16)
+    num_rows = q.shape[0]
+    if pairs is None:
+        pairs = [(r, h) for r in range(num_rows) for h in range(d.num_q_heads)]
+    pr = _c(np.asarray(pairs, dtype=np.int32).reshape(-1, 2), np.int32)
+    rs = _c(row_seq, np.int32)
+    rp = _c(row_pos, np.int32)
+    Rk = _c(R_k, np.float32)
+    Rv = _c(R_v, np.float32)
+    codes = _c(int2_pages, np.uint8)
+    sz = _c(scale_zero_pages, np.uint16)
+    sink = None if sink_bits is None else _c(sink_bits, np.uint16)
+    win = None if window_bits is None else _c(window_bits, np.uint16)
+    pt = _c(page_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    out = np.empty((pr.shape[0], d.head_dim), np.float64)
+    rc = lib.orc_extend(ctypes.byref(d), int(batch), int(num_rows), _ptr(q), _ptr(rs), _ptr(rp), _ptr(Rk), _ptr(Rv),
+                        _ptr(codes), _ptr(sz), _ptr(sink), _ptr(win), _ptr(pt), _ptr(sl), int(sink_len),
+                        int(window_len), float(sm_scale), pr.shape[0], _ptr(pr), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle extend: sequence, position, page id or length out of range")
     return out
 
 

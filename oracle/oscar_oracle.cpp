@@ -363,73 +363,122 @@ void orc_dequant_row(const orc_dims_t* d, const uint8_t* int2_pages, const uint1
   }
 }
 
-// Decode for a list of (batch index, query head) pairs.  For pair (b, hq):
-// kv head h = hq / (Hq / Hkv) (reading R10); L = seq_lens[b] (reading R18);
+// Attention of one query (bf16 bits q_row, head hq) of sequence b over the
+// cache of length L, restricted to positions p < A (A <= L).  The cache split
+// is the one of length L (readings R11-R13):
 //   sink   p in [0, min(S, L))                 from bf16_sink[b][K|V][h][p]
 //   window p in [max(S, L - W), L)              from bf16_window[b][K|V][h][p % W]
 //   bulk   p in [S, L - W)                      from the INT2 pool at page
 //          page_table[b][p / P], offset p % P, scored with q_rot = q . R_k[h]
-// (readings R11-R13), softmax with scale sm_scale (<= 0 means 1/sqrt(D),
-// reading R9), bulk output un-rotated by R_v[h]^T.  out: fp64 [n_pairs][D].
+// softmax with scale sm_scale, bulk output un-rotated by R_v[h]^T.  Returns 0,
+// or -1 when a page id is outside the pool.
+static int32_t attend_query(const orc_dims_t* d, const uint16_t* q_row, int hq, int b, int L, int A,
+                            const float* R_k, const float* R_v, const uint8_t* int2_pages,
+                            const uint16_t* scale_zero_pages, const uint16_t* bf16_sink,
+                            const uint16_t* bf16_window, const int32_t* page_table, int S, int W,
+                            double sm_scale, double* out) {
+  const int Hq = d->num_q_heads, H = d->num_kv_heads, D = d->head_dim, P = d->page_size;
+  const int gqa = Hq / H;
+  const int h = hq / gqa;
+  std::vector<double> qv(D), qr(D);
+  for (int j = 0; j < D; ++j) qv[j] = orc_bf16_to_f64(q_row[j]);
+  // q_rot = q . R_k[h]
+  const float* Rk = R_k + static_cast<size_t>(h) * D * D;
+  for (int j = 0; j < D; ++j) {
+    double acc = 0.0;
+    for (int i = 0; i < D; ++i) acc += qv[i] * static_cast<double>(Rk[static_cast<size_t>(i) * D + j]);
+    qr[j] = acc;
+  }
+  std::vector<double> keys(static_cast<size_t>(A) * D), vals(static_cast<size_t>(A) * D);
+  std::vector<int32_t> is_rot(A, 0);
+  int n = 0;
+  const int sink_end = L < S ? L : S;
+  const int win_begin = (L - W > S) ? L - W : S;
+  for (int p = 0; p < A; ++p) {
+    double* kk = keys.data() + static_cast<size_t>(n) * D;
+    double* vv = vals.data() + static_cast<size_t>(n) * D;
+    if (p < sink_end) {
+      const size_t kb = ((static_cast<size_t>(b) * 2 + 0) * H + h) * S + p;
+      const size_t vb = ((static_cast<size_t>(b) * 2 + 1) * H + h) * S + p;
+      for (int j = 0; j < D; ++j) {
+        kk[j] = orc_bf16_to_f64(bf16_sink[kb * D + j]);
+        vv[j] = orc_bf16_to_f64(bf16_sink[vb * D + j]);
+      }
+      is_rot[n] = 0;
+    } else if (p >= win_begin) {
+      const size_t kb = ((static_cast<size_t>(b) * 2 + 0) * H + h) * W + (p % W);
+      const size_t vb = ((static_cast<size_t>(b) * 2 + 1) * H + h) * W + (p % W);
+      for (int j = 0; j < D; ++j) {
+        kk[j] = orc_bf16_to_f64(bf16_window[kb * D + j]);
+        vv[j] = orc_bf16_to_f64(bf16_window[vb * D + j]);
+      }
+      is_rot[n] = 0;
+    } else {
+      const int64_t page = page_table[static_cast<size_t>(b) * d->max_pages_per_seq + p / P];
+      if (page < 0 || page >= d->num_pages) return -1;
+      orc_dequant_row(d, int2_pages, scale_zero_pages, page, h, 0, p % P, kk);
+      orc_dequant_row(d, int2_pages, scale_zero_pages, page, h, 1, p % P, vv);
+      is_rot[n] = 1;
+    }
+    ++n;
+  }
+  orc_attend_mixed(D, n, qv.data(), qr.data(), keys.data(), vals.data(), is_rot.data(), sm_scale,
+                   R_v + static_cast<size_t>(h) * D * D, out);
+  return 0;
+}
+
+// Decode for a list of (batch index, query head) pairs.  For pair (b, hq):
+// kv head h = hq / (Hq / Hkv) (reading R10); L = seq_lens[b] (reading R18); the
+// query attends every position [0, L) of the cache (attend_query).  sm_scale
+// <= 0 means 1/sqrt(D) (reading R9).  out: fp64 [n_pairs][D].
 // Returns 0, or -1 when a page id is outside the pool or L exceeds the table.
 int32_t orc_decode(const orc_dims_t* d, int32_t batch, const uint16_t* q, const float* R_k,
                    const float* R_v, const uint8_t* int2_pages, const uint16_t* scale_zero_pages,
                    const uint16_t* bf16_sink, const uint16_t* bf16_window, const int32_t* page_table,
                    const int32_t* seq_lens, int32_t sink_len, int32_t window_len, double sm_scale,
                    int32_t n_pairs, const int32_t* pairs, double* out) {
-  const int Hq = d->num_q_heads, H = d->num_kv_heads, D = d->head_dim, P = d->page_size;
-  const int S = sink_len, W = window_len;
-  const int gqa = Hq / H;
+  const int Hq = d->num_q_heads, D = d->head_dim, P = d->page_size;
   if (sm_scale <= 0.0) sm_scale = 1.0 / std::sqrt(static_cast<double>(D));
   for (int pi = 0; pi < n_pairs; ++pi) {
     const int b = pairs[2 * pi], hq = pairs[2 * pi + 1];
-    const int h = hq / gqa;
     const int L = seq_lens[b];
     if (L > d->max_pages_per_seq * P || b >= batch) return -1;
-    std::vector<double> qv(D), qr(D);
-    for (int j = 0; j < D; ++j) qv[j] = orc_bf16_to_f64(q[(static_cast<size_t>(b) * Hq + hq) * D + j]);
-    // q_rot = q . R_k[h]
-    const float* Rk = R_k + static_cast<size_t>(h) * D * D;
-    for (int j = 0; j < D; ++j) {
-      double acc = 0.0;
-      for (int i = 0; i < D; ++i) acc += qv[i] * static_cast<double>(Rk[static_cast<size_t>(i) * D + j]);
-      qr[j] = acc;
-    }
-    std::vector<double> keys(static_cast<size_t>(L) * D), vals(static_cast<size_t>(L) * D);
-    std::vector<int32_t> is_rot(L, 0);
-    int n = 0;
-    const int sink_end = L < S ? L : S;
-    const int win_begin = (L - W > S) ? L - W : S;
-    for (int p = 0; p < L; ++p) {
-      double* kk = keys.data() + static_cast<size_t>(n) * D;
-      double* vv = vals.data() + static_cast<size_t>(n) * D;
-      if (p < sink_end) {
-        const size_t kb = ((static_cast<size_t>(b) * 2 + 0) * H + h) * S + p;
-        const size_t vb = ((static_cast<size_t>(b) * 2 + 1) * H + h) * S + p;
-        for (int j = 0; j < D; ++j) {
-          kk[j] = orc_bf16_to_f64(bf16_sink[kb * D + j]);
-          vv[j] = orc_bf16_to_f64(bf16_sink[vb * D + j]);
-        }
-        is_rot[n] = 0;
-      } else if (p >= win_begin) {
-        const size_t kb = ((static_cast<size_t>(b) * 2 + 0) * H + h) * W + (p % W);
-        const size_t vb = ((static_cast<size_t>(b) * 2 + 1) * H + h) * W + (p % W);
-        for (int j = 0; j < D; ++j) {
-          kk[j] = orc_bf16_to_f64(bf16_window[kb * D + j]);
-          vv[j] = orc_bf16_to_f64(bf16_window[vb * D + j]);
-        }
-        is_rot[n] = 0;
-      } else {
-        const int64_t page = page_table[static_cast<size_t>(b) * d->max_pages_per_seq + p / P];
-        if (page < 0 || page >= d->num_pages) return -1;
-        orc_dequant_row(d, int2_pages, scale_zero_pages, page, h, 0, p % P, kk);
-        orc_dequant_row(d, int2_pages, scale_zero_pages, page, h, 1, p % P, vv);
-        is_rot[n] = 1;
-      }
-      ++n;
-    }
-    orc_attend_mixed(D, n, qv.data(), qr.data(), keys.data(), vals.data(), is_rot.data(), sm_scale,
-                     R_v + static_cast<size_t>(h) * D * D, out + static_cast<size_t>(pi) * D);
+    if (attend_query(d, q + (static_cast<size_t>(b) * Hq + hq) * D, hq, b, L, L, R_k, R_v, int2_pages,
+                     scale_zero_pages, bf16_sink, bf16_window, page_table, sink_len, window_len, sm_scale,
+                     out + static_cast<size_t>(pi) * D) != 0)
+      return -1;
+  }
+  return 0;
+}
+
+// Extend (chunked prefill) attention for a list of (query row, query head)
+// pairs: query row r belongs to sequence b = row_seq[r] at position
+// row_pos[r] and attends, causally, the positions [0, row_pos[r]] of that
+// sequence's cache of length L = seq_lens[b] (the new tokens are already in the
+// cache; the sink/window/bulk split is the one of length L; reading R24).  A
+// row at position L - 1 is exactly a decode query.  out: fp64 [n_pairs][D].
+// Returns 0, or -1 for a sequence or position out of range or a bad page id.
+int32_t orc_extend(const orc_dims_t* d, int32_t batch, int32_t num_rows, const uint16_t* q,
+                   const int32_t* row_seq, const int32_t* row_pos, const float* R_k, const float* R_v,
+                   const uint8_t* int2_pages, const uint16_t* scale_zero_pages, const uint16_t* bf16_sink,
+                   const uint16_t* bf16_window, const int32_t* page_table, const int32_t* seq_lens,
+                   int32_t sink_len, int32_t window_len, double sm_scale, int32_t n_pairs, const int32_t* pairs,
+                   double* out) {
+  const int Hq = d->num_q_heads, D = d->head_dim, P = d->page_size;
+  if (sm_scale <= 0.0) sm_scale = 1.0 / std::sqrt(static_cast<double>(D));
+  for (int pi = 0; pi < n_pairs; ++pi) {
+    const int r = pairs[2 * pi], hq = pairs[2 * pi + 1];
+    if (r < 0 || r >= num_rows) return -1;
+    const int b = row_seq[r];
+    if (b < 0 || b >= batch) return -1;
+    const int L = seq_lens[b];
+    if (L > d->max_pages_per_seq * P) return -1;
+    const int pos = row_pos[r];
+    if (pos < 0 || pos >= L) return -1;
+    if (attend_query(d, q + (static_cast<size_t>(r) * Hq + hq) * D, hq, b, L, pos + 1, R_k, R_v, int2_pages,
+                     scale_zero_pages, bf16_sink, bf16_window, page_table, sink_len, window_len, sm_scale,
+                     out + static_cast<size_t>(pi) * D) != 0)
+      return -1;
   }
   return 0;
 }

@@ -729,4 +729,88 @@ def pin_append_mixed_bf16_rows_and_int2(lib):
                 assert np.all(win[b, :, :, r] == 0xFFFF)
 
 
+def _extend_rows(lib, c, rows_pos, seed=41, row_seq=None):
+    """Extend output [rows][Hq][D] over the single-sequence cache of case ``c`` for query rows
+    at the given positions (fresh queries)."""
+    d = c["dims"]
+    rng = np.random.default_rng(seed)
+    nr = len(rows_pos)
+    qb = bf16_bits(rng.standard_normal((nr, d["num_q_heads"], d["head_dim"])))
+    rs = np.zeros(nr, np.int32) if row_seq is None else np.asarray(row_seq, np.int32)
+    out = O.extend(d, 1, qb, rs, np.asarray(rows_pos, np.int32), c["Rk"], c["Rv"], c["pool"], c["sz"], c["sink"],
+                   c["win"], c["page_table"], np.array([c["L"]], np.int32), c["S"], c["W"], 0.0, lib=lib)
+    return qb, out.reshape(nr, d["num_q_heads"], d["head_dim"])
+
+
+def pin_extend_last_row_is_decode(lib):
+    """A query row at the last position L - 1 is the decode query: identical output."""
+    for L, S, W in ((70, 4, 16), (33, 0, 0), (50, 8, 64)):
+        c = _decode_case(lib, L=L, S=S, W=W, exact_R=False, seed=43)
+        d = c["dims"]
+        out = O.extend(d, 1, c["qb"], np.zeros(1, np.int32), np.array([L - 1], np.int32), c["Rk"], c["Rv"],
+                       c["pool"], c["sz"], c["sink"], c["win"], c["page_table"], np.array([L], np.int32), S, W,
+                       0.0, lib=lib)
+        assert np.array_equal(out, c["out"]), (L, S, W)
+
+
+def pin_extend_all_bf16_is_causal_dense(lib):
+    """sink + window hold the whole cache: the row at position p is textbook dense
+    softmax attention over the bf16 K/V of positions 0..p."""
+    for L, S, W in ((40, 8, 32), (30, 0, 40), (25, 25, 0)):
+        c = _decode_case(lib, L=L, S=S, W=W, seed=44)
+        d = c["dims"]
+        gqa = d["num_q_heads"] // d["num_kv_heads"]
+        rows = [0, 3, L // 2, L - 2, L - 1]
+        qb, out = _extend_rows(lib, c, rows, seed=45)
+        for i, p in enumerate(rows):
+            for hq in range(d["num_q_heads"]):
+                h = hq // gqa
+                want = dense_attention(bf16_vals(qb[i, hq]), bf16_vals(c["kb"][: p + 1, h]),
+                                       bf16_vals(c["vb"][: p + 1, h]), 1 / math.sqrt(d["head_dim"]))
+                assert np.allclose(out[i, hq], want, rtol=0, atol=1e-12), (L, S, W, p)
+
+
+def pin_extend_causal_brute_force(lib):
+    """Mixed cache (sink, INT2 bulk, window ring of the final length L): each row at
+    position p, by a plain loop over positions 0..p with the split of length L."""
+    L, S, W = 60, 4, 16
+    c = _decode_case(lib, L=L, S=S, W=W, exact_R=False, seed=46)
+    d = c["dims"]
+    D, gqa = d["head_dim"], d["num_q_heads"] // d["num_kv_heads"]
+    rows = [0, 2, 3, 5, 20, 43, 44, 50, 59]
+    qb, out = _extend_rows(lib, c, rows, seed=47)
+    scale = 1 / math.sqrt(D)
+    for i, p in enumerate(rows):
+        for hq in range(d["num_q_heads"]):
+            h = hq // gqa
+            q = bf16_vals(qb[i, hq])
+            qr = q @ c["Rk"][h].astype(np.float64)
+            logits, vals, rot = [], [], []
+            for t in range(p + 1):
+                if t < S or t >= max(S, L - W):
+                    logits.append(scale * float(q @ bf16_vals(c["kb"][t, h])))
+                    vals.append(bf16_vals(c["vb"][t, h]))
+                    rot.append(False)
+                else:
+                    logits.append(scale * float(qr @ _bulk_dequant(c, t, 0)[h]))
+                    vals.append(_bulk_dequant(c, t, 1)[h])
+                    rot.append(True)
+            w = np.exp(np.array(logits) - max(logits))
+            plain = sum(w[k] * vals[k] for k in range(p + 1) if not rot[k])
+            rotd = sum(w[k] * vals[k] for k in range(p + 1) if rot[k])
+            want = (plain + (rotd @ c["Rv"][h].astype(np.float64).T if any(rot) else 0)) / w.sum()
+            assert np.allclose(out[i, hq], want, rtol=0, atol=1e-11), (p, hq)
+
+
+def pin_extend_rejects_out_of_range_rows(lib):
+    """A row at a position >= L or of a sequence outside the batch is refused."""
+    c = _decode_case(lib, L=20, S=2, W=4, seed=48)
+    for pos, seq in ((20, 0), (-1, 0), (3, 1), (3, -1)):
+        try:
+            _extend_rows(lib, c, [pos], row_seq=[seq])
+        except ValueError:
+            continue
+        raise AssertionError(f"row at position {pos} of sequence {seq} was accepted")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

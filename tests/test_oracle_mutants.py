@@ -34,7 +34,7 @@ MUTANTS = [
     ("gqa_mapping_modulo", "const int h = hq / gqa;", "const int h = hq % H;", 2),
     ("dequant_drops_zero", "x[j] = c * s + z;", "x[j] = c * s;", 1),
     ("f16_truncates", "std::nearbyint(a / quantum) * quantum", "std::trunc(a / quantum) * quantum", 1),
-    ("default_scale_1_over_D", "sm_scale = 1.0 / std::sqrt(static_cast<double>(D));", "sm_scale = 1.0 / D;", 2),
+    ("default_scale_1_over_D", "sm_scale = 1.0 / std::sqrt(static_cast<double>(D));", "sm_scale = 1.0 / D;", 3),
     ("key_reads_value_codes", "page, h, 0, p % P, kk);", "page, h, 1, p % P, kk);", 1),
     ("softmax_denominator_counts_tokens", "    denom += w;\n", "    denom += 1.0;\n", 1),
     ("query_rotation_transposed",
@@ -49,6 +49,11 @@ MUTANTS = [
     ("mixed_kv_swapped", "const uint16_t* x = (kv ? v : k) + (static_cast<size_t>(t) * H + h) * D;\n        uint16_t* dst",
      "const uint16_t* x = (kv ? k : v) + (static_cast<size_t>(t) * H + h) * D;\n        uint16_t* dst", 1),
     ("mixed_window_skips_oldest", "} else if (W > 0 && p >= win_begin) {", "} else if (W > 0 && p > win_begin) {", 1),
+    ("extend_not_causal", "hq, b, L, pos + 1, R_k", "hq, b, L, L, R_k", 1),
+    ("extend_excludes_own_position", "hq, b, L, pos + 1, R_k", "hq, b, L, pos, R_k", 1),
+    ("extend_window_of_prefix_length", "const int win_begin = (L - W > S) ? L - W : S;\n  for (int p = 0; p < A; ++p)",
+     "const int win_begin = (A - W > S) ? A - W : S;\n  for (int p = 0; p < A; ++p)", 1),
+    ("extend_row_as_sequence", "const int b = row_seq[r];", "const int b = r < batch ? r : row_seq[r];", 1),
 ]
 
 
