@@ -456,6 +456,7 @@ def run_ours(args, world, rank, local):
 
     log(f"e2e: {e2e_ms * 1e3:.2f} us/step")
     append_line = append_workload(dev) if rank == 0 and not args.no_append else None
+    extend_line = extend_workload(dev) if rank == 0 and not args.no_extend else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         log("cpu baseline (oracle)")
@@ -483,11 +484,65 @@ def run_ours(args, world, rank, local):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": K * 4,
             "append_workload": append_line,
+            "extend_workload": extend_line,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def extend_workload(dev):
+    """The extend (chunked prefill) workload: 32 sequences of 8192 cached tokens
+    (the last 16 of each are the new chunk), 32 query / 8 KV heads, head_dim 128,
+    group 64, sink 64, window 128; one oscar_extend over the 512 query rows.  Its
+    algorithmic bytes count each sequence's cache once (rows of a sequence share
+    its pages through L2) plus q in and fp32 out; the cache (168 MB) exceeds L2."""
+    import torch
+
+    from int2_rotated_kv_append_gb300 import synth
+    from int2_rotated_kv_append_gb300.cache import Int2Cache
+
+    B, L, chunk = 32, 8192, 16
+    w = synth.make_workload(num_q_heads=32, num_kv_heads=8, head_dim=128, group_size=64, sink_len=64,
+                            window_len=128, seq_lens=[L] * B, seed=11, device=dev)
+    cache = Int2Cache(w, device=dev)
+    cache.prefill()
+    rs = torch.arange(B, dtype=torch.int32, device=dev).repeat_interleave(chunk)
+    rp = (torch.arange(L - chunk, L, dtype=torch.int32, device=dev)).repeat(B)
+    g = torch.Generator(device=dev).manual_seed(3)
+    q = torch.randn((B * chunk, w.num_q_heads, w.head_dim), generator=g, device=dev).to(torch.bfloat16)
+    out = torch.empty((B * chunk, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+
+    def run():
+        cache.extend(q, rs, rp, out=out)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(10):
+        flush.zero_()  # evict the cache from L2 between runs
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    ts.sort()
+    us = ts[len(ts) // 2]
+    nbytes = algorithmic_bytes_decode(w, [L] * B) - B * w.num_q_heads * w.head_dim * 6 + \
+        B * chunk * w.num_q_heads * w.head_dim * 6
+    peak, peak_kind = measured_peak_hbm()
+    achieved = nbytes / (us * 1e-6) / 1e9
+    return {"workload": f"extend: {B} sequences x {L} cached tokens, last {chunk} are new (causal query rows), "
+                        "Hq 32 / Hkv 8, D 128, G 64, sink 64, window 128; L2 flushed between runs",
+            "us": us, "query_tokens_per_s": B * chunk / (us * 1e-6),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "bytes_per_launch": nbytes,
+                         "peak_source": f"{peak_kind} hbm_gbs"},
+            "note": "every query row reads its sequence's pages itself; rows of a sequence share them in L2"}
 
 
 def append_workload(dev):
@@ -603,6 +658,7 @@ def main():
     ap.add_argument("--pps", type=int, default=-1, help="pages per split for both decodes (-1: the workload's, 0: auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-append", action="store_true", help="skip the append throughput workload")
+    ap.add_argument("--no-extend", action="store_true", help="skip the extend (chunked prefill) workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -188,6 +188,42 @@ oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, int32_t max
                             size_t workspace_bytes, void* stream);
 
 /*
+ * oscar_extend -- mixed-precision paged attention of many query tokens per
+ * sequence (chunked prefill / extend) over the same INT2 + BF16 cache.
+ *
+ * The decode of oscar_decode generalised to query rows at earlier positions
+ * (a reading: the pages describe the fused mixed-precision attention kernels
+ * of the serving stack, project card "How it works", abstract "fused kernel
+ * pipelines", without fixing the multi-token case).  Query row r belongs to
+ * sequence b = row_seq[r] and sits at position p = row_pos[r]; it attends, causally,
+ * the positions [0, p] of sequence b's cache of length L = seq_lens[b] (the new
+ * tokens are appended first, e.g. by oscar_append_mixed).  Which positions are
+ * BF16 (sink, window) and which INT2 is the split of length L, exactly as in
+ * oscar_decode; a row at p = L - 1 is a decode query and gives the same output.
+ * Arguments (beyond oscar_decode's, whose pools, buffers and tables they share)
+ *   batch         number of sequences (rows of page_table, seq_lens, sink, window)
+ *   num_rows      number of query rows
+ *   max_seq_len   host bound on seq_lens (as oscar_decode)
+ *   q             device bf16 [num_rows][Hq][D]
+ *   row_seq       device int32 [num_rows], in [0, batch)
+ *   row_pos       device int32 [num_rows], in [0, seq_lens[row_seq[r]])
+ *   out           device fp32 [num_rows][Hq][D]
+ *   workspace     at least oscar_extend_workspace_bytes(dims, num_rows, ...) bytes
+ * A row with a sequence or position out of range attends nothing (zeros) and
+ * sets OSCAR_DEVERR_POSITION.  Every row reads its pages itself (rows of one
+ * sequence share them through L2).
+ */
+size_t oscar_extend_workspace_bytes(const oscar_dims_t* dims, int32_t num_rows, int32_t max_seq_len,
+                                    int32_t pages_per_split, int32_t sink_len, int32_t window_len);
+oscar_status_t oscar_extend(const oscar_dims_t* dims, int32_t batch, int32_t num_rows, int32_t max_seq_len,
+                            int32_t pages_per_split, const void* q, const int32_t* row_seq, const int32_t* row_pos,
+                            const float* R_k, const float* R_v, const uint8_t* int2_pages,
+                            const void* scale_zero_pages, const void* bf16_sink, const void* bf16_window,
+                            const int32_t* page_table, const int32_t* seq_lens, int32_t sink_len,
+                            int32_t window_len, float sm_scale, float* out, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
  * oscar_decode_noalloc -- oscar_decode without a caller workspace.
  *
  * The OSCAR pages have no counterpart for this call; it is a convenience of this

@@ -9,8 +9,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (oscar_append, oscar_bf16_append, oscar_bf16_decode, oscar_bf16_decode_workspace_bytes,
-               oscar_decode, oscar_decode_workspace_bytes)
+from . import (oscar_append, oscar_bf16_append, oscar_bf16_decode, oscar_bf16_decode_workspace_bytes, oscar_decode,
+               oscar_decode_workspace_bytes, oscar_extend, oscar_extend_workspace_bytes)
 from .synth import Workload
 
 SENTINEL = 0xA5
@@ -67,6 +67,25 @@ class Int2Cache:
         oscar_decode(self.dims, w.batch, msl, self.pps, q, self.R_k, self.R_v, self.int2_pages, self.scale_zero,
                      self.sink, self.window, self.page_table, self.seq_lens if seq_lens is None else seq_lens,
                      w.sink_len, w.window_len, sm_scale, out, ws, stream)
+        return out
+
+
+    def extend(self, q, row_seq, row_pos, out=None, sm_scale=0.0, max_seq_len=None, stream=None):
+        """Causal attention of query rows q [rows][Hq][D]; row r belongs to sequence
+        row_seq[r] at position row_pos[r] (int32 device tensors)."""
+        w = self.w
+        msl = w.max_seq_len if max_seq_len is None else max_seq_len
+        rows = q.shape[0]
+        if out is None:
+            out = torch.empty((rows, w.num_q_heads, w.head_dim), dtype=torch.float32, device=self.device)
+        nbytes = oscar_extend_workspace_bytes(self.dims, rows, msl, self.pps, w.sink_len, w.window_len)
+        if nbytes == 0:
+            raise ValueError("invalid extend arguments for workspace sizing")
+        if self._ws is None or self._ws.numel() < nbytes:
+            self._ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        oscar_extend(self.dims, w.batch, msl, self.pps, q, row_seq, row_pos, self.R_k, self.R_v, self.int2_pages,
+                     self.scale_zero, self.sink, self.window, self.page_table, self.seq_lens, w.sink_len,
+                     w.window_len, sm_scale, out, self._ws, stream)
         return out
 
 

@@ -140,18 +140,23 @@ extern "C" size_t oscar_decode_workspace_bytes(const oscar_dims_t* dims, int32_t
   return plan.total;
 }
 
-extern "C" oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, int32_t max_seq_len,
-                                       int32_t pages_per_split, const void* q, const float* R_k, const float* R_v,
-                                       const uint8_t* int2_pages, const void* scale_zero_pages,
-                                       const void* bf16_sink, const void* bf16_window, const int32_t* page_table,
-                                       const int32_t* seq_lens, int32_t sink_len, int32_t window_len,
-                                       float sm_scale, float* out, void* workspace, size_t workspace_bytes,
-                                       void* stream) {
+namespace {
+
+// The mixed-precision attention of `rows` query rows: a decode (row_seq null,
+// row b is sequence b and attends its whole cache) or an extend (row b attends
+// positions 0 .. row_pos[b] of sequence row_seq[b] < num_seqs).
+oscar_status_t mixed_attention(const oscar_dims_t* dims, int32_t rows, int32_t num_seqs, const int32_t* row_seq,
+                               const int32_t* row_pos, int32_t max_seq_len, int32_t pages_per_split, const void* q,
+                               const float* R_k, const float* R_v, const uint8_t* int2_pages,
+                               const void* scale_zero_pages, const void* bf16_sink, const void* bf16_window,
+                               const int32_t* page_table, const int32_t* seq_lens, int32_t sink_len,
+                               int32_t window_len, float sm_scale, float* out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   oscar_status_t st = check_dims(dims);
   if (st != OSCAR_OK) return st;
-  if (batch < 0 || max_seq_len < 0 || pages_per_split < 0 || sink_len < 0 || window_len < 0)
+  if (rows < 0 || num_seqs < 0 || max_seq_len < 0 || pages_per_split < 0 || sink_len < 0 || window_len < 0)
     return OSCAR_ERR_INVALID_ARG;
-  if (batch == 0) return OSCAR_OK;
+  if (rows == 0) return OSCAR_OK;
   if (!q || !R_k || !R_v || !int2_pages || !scale_zero_pages || !page_table || !seq_lens || !out || !workspace)
     return OSCAR_ERR_INVALID_ARG;
   if ((sink_len > 0 && !bf16_sink) || (window_len > 0 && !bf16_window)) return OSCAR_ERR_INVALID_ARG;
@@ -160,12 +165,12 @@ extern "C" oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, 
       misaligned16(scale_zero_pages) || misaligned16(bf16_sink) || misaligned16(bf16_window))
     return OSCAR_ERR_INVALID_ARG;
   Plan plan;
-  if (!make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, split_ctas_per_sm(dims, kMixed), &plan))
+  if (!make_plan(dims, rows, max_seq_len, pages_per_split, sink_len, window_len, kMixed, split_ctas_per_sm(dims, kMixed), &plan))
     return OSCAR_ERR_INVALID_ARG;
   if (workspace_bytes < plan.total) return OSCAR_ERR_WORKSPACE;
   if (merge_smem(dims->head_dim, plan.ns, 1, 0, kMergeThreadsSmall) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
-  if (static_cast<long long>(batch) * dims->num_q_heads > 0x7fffffffLL || plan.ns > 0x7fffffff) return OSCAR_ERR_UNSUPPORTED;
-  Params p = base_params(dims, batch, max_seq_len, plan, kMixed, sm_scale, workspace);
+  if (static_cast<long long>(rows) * dims->num_q_heads > 0x7fffffffLL || plan.ns > 0x7fffffff) return OSCAR_ERR_UNSUPPORTED;
+  Params p = base_params(dims, rows, max_seq_len, plan, kMixed, sm_scale, workspace);
   p.S = sink_len;
   p.W = window_len;
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -177,9 +182,46 @@ extern "C" oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, 
   p.win = static_cast<const __nv_bfloat16*>(bf16_window);
   p.page_table = page_table;
   p.seq_lens = seq_lens;
+  p.row_seq = row_seq;
+  p.row_pos = row_pos;
+  p.num_seqs = num_seqs;
   p.out = out;
   if (!int2_mma_supported(p)) p.qfrag = nullptr;
   return run(p, kMixed, stream);
+}
+
+}  // namespace
+
+extern "C" oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, int32_t max_seq_len,
+                                       int32_t pages_per_split, const void* q, const float* R_k, const float* R_v,
+                                       const uint8_t* int2_pages, const void* scale_zero_pages,
+                                       const void* bf16_sink, const void* bf16_window, const int32_t* page_table,
+                                       const int32_t* seq_lens, int32_t sink_len, int32_t window_len,
+                                       float sm_scale, float* out, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  return mixed_attention(dims, batch, batch, nullptr, nullptr, max_seq_len, pages_per_split, q, R_k, R_v,
+                         int2_pages, scale_zero_pages, bf16_sink, bf16_window, page_table, seq_lens, sink_len,
+                         window_len, sm_scale, out, workspace, workspace_bytes, stream);
+}
+
+extern "C" size_t oscar_extend_workspace_bytes(const oscar_dims_t* dims, int32_t num_rows, int32_t max_seq_len,
+                                               int32_t pages_per_split, int32_t sink_len, int32_t window_len) {
+  return oscar_decode_workspace_bytes(dims, num_rows, max_seq_len, pages_per_split, sink_len, window_len);
+}
+
+extern "C" oscar_status_t oscar_extend(const oscar_dims_t* dims, int32_t batch, int32_t num_rows,
+                                       int32_t max_seq_len, int32_t pages_per_split, const void* q,
+                                       const int32_t* row_seq, const int32_t* row_pos, const float* R_k,
+                                       const float* R_v, const uint8_t* int2_pages, const void* scale_zero_pages,
+                                       const void* bf16_sink, const void* bf16_window, const int32_t* page_table,
+                                       const int32_t* seq_lens, int32_t sink_len, int32_t window_len,
+                                       float sm_scale, float* out, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  if (batch < 0 || num_rows < 0) return OSCAR_ERR_INVALID_ARG;
+  if (num_rows > 0 && (batch == 0 || !row_seq || !row_pos)) return OSCAR_ERR_INVALID_ARG;
+  return mixed_attention(dims, num_rows, batch, row_seq, row_pos, max_seq_len, pages_per_split, q, R_k, R_v,
+                         int2_pages, scale_zero_pages, bf16_sink, bf16_window, page_table, seq_lens, sink_len,
+                         window_len, sm_scale, out, workspace, workspace_bytes, stream);
 }
 
 extern "C" size_t oscar_bf16_decode_workspace_bytes(const oscar_dims_t* dims, int32_t batch, int32_t max_seq_len,

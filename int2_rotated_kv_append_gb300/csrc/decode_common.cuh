@@ -55,6 +55,11 @@ struct Params {
   const __nv_bfloat16* pages; // BF16 pool (BF16 mode)
   const int32_t* page_table;
   const int32_t* seq_lens;
+  // Extend rows (null for a decode): query row b belongs to sequence row_seq[b]
+  // (< num_seqs) and attends positions 0 .. row_pos[b] of it.
+  const int32_t* row_seq;
+  const int32_t* row_pos;
+  int num_seqs;
   float* out;
   float* q_rot;
   uint32_t* qfrag;  // kQfragBytes per (sequence, KV head); null when not needed
@@ -156,6 +161,33 @@ __device__ __forceinline__ int clamp_len(const Params& p, int b) {
     L = L < 0 ? 0 : p.max_seq_len;
   }
   return L;
+}
+
+// The cache a query row reads: sequence `seq` of length L (which fixes the
+// sink / window / bulk split), positions [0, A) attended.  A decode row b is
+// sequence b with A = L; an extend row attends 0 .. row_pos[b] of sequence
+// row_seq[b].  A row naming a sequence or position out of range is flagged and
+// attends nothing.
+struct RowView {
+  int seq, L, A;
+};
+__device__ __forceinline__ RowView row_view(const Params& p, int b) {
+  if (p.row_seq == nullptr) {
+    const int L = clamp_len(p, b);
+    return {b, L, L};
+  }
+  const int seq = __ldg(p.row_seq + b);
+  if (seq < 0 || seq >= p.num_seqs) {
+    record_error(OSCAR_DEVERR_POSITION);
+    return {0, 0, 0};
+  }
+  const int L = clamp_len(p, seq);
+  const int pos = __ldg(p.row_pos + b);
+  if (pos < 0 || pos >= L) {
+    record_error(OSCAR_DEVERR_POSITION);
+    return {seq, L, 0};
+  }
+  return {seq, L, pos + 1};
 }
 
 // q_rot[b][hq] = q[b][hq] . R_k[h] for the GQA query heads hq of one (b, h):
@@ -323,24 +355,27 @@ __device__ __forceinline__ void split_body(const Params& p, int s, int h, int b,
   const int gqa = p.gqa;
   grid_dep_launch_dependents();
   grid_dep_wait();  // q_rot comes from the preceding kernel
-  const int L = clamp_len(p, b);
+  const RowView rv = row_view(p, b);
+  const int L = rv.L, A = rv.A, bs = rv.seq;
 
-  // Position range of this split.
+  // Position range of this split (positions below A only).
+  int sink_att = 0;
   const bool paged = s < p.n_paged;
   int begin = 0, count = 0;         // paged: absolute positions [begin, begin+count)
   int sink_end = 0, win_begin = 0;  // dense: enumerated sink then window
   if (MODE == kMixed) {
     sink_end = min(p.S, L);
     win_begin = max(p.S, L - p.W);
+    sink_att = min(sink_end, A);
   }
   if (paged) {
     const int lo = s * p.pps * kPageSize, hi = lo + p.pps * kPageSize;
     const int r0 = MODE == kMixed ? max(lo, p.S) : lo;
-    const int r1 = MODE == kMixed ? min(hi, win_begin) : min(hi, L);
+    const int r1 = MODE == kMixed ? min(hi, min(win_begin, A)) : min(hi, A);
     begin = r0;
     count = max(0, r1 - r0);
   } else {
-    const int n_dense = sink_end + max(0, L - win_begin);
+    const int n_dense = sink_att + max(0, A - win_begin);
     begin = (s - p.n_paged) * kBf16Chunk;
     count = max(0, min(kBf16Chunk, n_dense - begin));
   }
@@ -367,7 +402,7 @@ __device__ __forceinline__ void split_body(const Params& p, int s, int h, int b,
       if (e < count) {
         if (paged) {
           pos = begin + e;
-          page = p.page_table[static_cast<size_t>(b) * p.max_pages + pos / kPageSize];
+          page = p.page_table[static_cast<size_t>(bs) * p.max_pages + pos / kPageSize];
           if (page < 0 || page >= p.num_pages) {
             record_error(OSCAR_DEVERR_PAGE_ID);
             page = -1;
@@ -375,7 +410,7 @@ __device__ __forceinline__ void split_body(const Params& p, int s, int h, int b,
           }
         } else {
           const int idx = begin + e;
-          pos = idx < sink_end ? idx : win_begin + (idx - sink_end);
+          pos = idx < sink_att ? idx : win_begin + (idx - sink_att);
         }
       }
       page_s[tid] = page;
@@ -408,9 +443,9 @@ __device__ __forceinline__ void split_body(const Params& p, int s, int h, int b,
         if (MODE == kBf16Paged) {
           src = p.pages + (((static_cast<size_t>(page_s[tt]) * p.H + h) * 2 + kvsel) * kPageSize + pos % kPageSize) * D;
         } else if (pos < sink_end) {
-          src = p.sink + (((static_cast<size_t>(b) * 2 + kvsel) * p.H + h) * p.S + pos) * D;
+          src = p.sink + (((static_cast<size_t>(bs) * 2 + kvsel) * p.H + h) * p.S + pos) * D;
         } else {
-          src = p.win + (((static_cast<size_t>(b) * 2 + kvsel) * p.H + h) * p.W + pos % p.W) * D;
+          src = p.win + (((static_cast<size_t>(bs) * 2 + kvsel) * p.H + h) * p.W + pos % p.W) * D;
         }
         const uint4* s4 = reinterpret_cast<const uint4*>(src + word * 16);
         raw[k][0] = __ldg(s4);

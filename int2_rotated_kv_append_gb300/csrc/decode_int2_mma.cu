@@ -265,11 +265,12 @@ __device__ __forceinline__ void dense_split(const Params& p, int d, int h, int b
   const size_t bh0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * gqa;
   grid_dep_launch_dependents();
   grid_dep_wait();  // the sink/window rows may come from the preceding kernel (an append)
-  const int L = clamp_len(p, b);
+  const RowView rv = row_view(p, b);
+  const int L = rv.L, A = rv.A, bs = rv.seq;
   const int nsp = (p.S + kPageSize - 1) / kPageSize, nwp = (p.W + kPageSize - 1) / kPageSize;
   const int first = d * kDensePagesPerCta;
   const int cnt = max(0, min(kDensePagesPerCta, nsp + nwp - first));
-  const int sink_end = min(p.S, L);
+  const int sink_end = min(min(p.S, L), A);  // attended sink positions
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kDenseStage);
   if (lane == 0) mbar_init(smem_u32(&bars[warp]), 1);
   mbar_init_fence();
@@ -288,13 +289,15 @@ __device__ __forceinline__ void dense_split(const Params& p, int d, int h, int b
     if (k < nsp) {
       const int pos = k * kPageSize + r;
       if (pos < sink_end)
-        src = p.sink + (((static_cast<size_t>(b) * 2 + kv) * p.H + h) * p.S + pos) * kD;
+        src = p.sink + (((static_cast<size_t>(bs) * 2 + kv) * p.H + h) * p.S + pos) * kD;
     } else {
       const int slot = (k - nsp) * kPageSize + r;
       if (slot < p.W && L > 0) {
         int back = (L - 1 - slot) % p.W;
         if (back < 0) back += p.W;
-        if (L - 1 - back >= p.S) src = p.win + (((static_cast<size_t>(b) * 2 + kv) * p.H + h) * p.W + slot) * kD;
+        const int wpos = L - 1 - back;  // the position the ring slot holds
+        if (wpos >= p.S && wpos < A)
+          src = p.win + (((static_cast<size_t>(bs) * 2 + kv) * p.H + h) * p.W + slot) * kD;
       }
     }
     const uint32_t mask = __ballot_sync(0xffffffffu, src != nullptr);
@@ -395,12 +398,13 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   uint64_t* qbar = reinterpret_cast<uint64_t*>(qbuf + 32 * kQfragWords);
   const int sp0 = s * p.pps;
   const int spn = max(0, min(p.pps, p.max_pages - sp0));
+  const RowView rv = row_view(p, b);
   for (int k = tid; k < spn; k += kWarps * 32)
-    pid_all[k] = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + sp0 + k);
-  const int L = clamp_len(p, b);
+    pid_all[k] = __ldg(p.page_table + static_cast<size_t>(rv.seq) * p.max_pages + sp0 + k);
+  const int L = rv.L;
   const int win_begin = max(p.S, L - p.W);
   const int lo_pos = s * p.pps * kPageSize;
-  const int r0 = max(lo_pos, p.S), r1 = min(lo_pos + p.pps * kPageSize, win_begin);
+  const int r0 = max(lo_pos, p.S), r1 = min(lo_pos + p.pps * kPageSize, min(win_begin, rv.A));
   const size_t bh0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * gqa;
 
   if (r1 <= r0) {  // nothing of the bulk falls in this split: an empty partial (the merge skips it)

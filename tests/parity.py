@@ -123,6 +123,16 @@ def oracle_decode_on_gpu_cache(w: Workload, cache, pairs=None, q=None, seq_lens=
                     w.page_table.numpy(), sl, w.sink_len, w.window_len, sm_scale, pairs=pairs)
 
 
+def oracle_extend_on_gpu_cache(w: Workload, cache, q: torch.Tensor, row_seq: np.ndarray, row_pos: np.ndarray,
+                               pairs=None, sm_scale=0.0) -> np.ndarray:
+    codes, sz = pools_to_host(cache)
+    sink = bits16(cache.sink) if cache.sink is not None else None
+    win = bits16(cache.window) if cache.window is not None else None
+    return O.extend(w.dims, w.batch, bits16(q), row_seq, row_pos, w.R_k.cpu().numpy(), w.R_v.cpu().numpy(), codes,
+                    sz, sink, win, w.page_table.numpy(), cache.seq_lens.cpu().numpy(), w.sink_len, w.window_len,
+                    sm_scale, pairs=pairs)
+
+
 def compare_decode(gpu_out: torch.Tensor, ref: np.ndarray, pairs=None) -> dict:
     g = gpu_out.detach().cpu().numpy().astype(np.float64)
     if pairs is not None:

@@ -100,6 +100,21 @@ def test_append_mixed_validation(lib):
     assert _append_mixed(lib, _dims(), win=ctypes.c_void_p(24)) == ok.OSCAR_ERR_INVALID_ARG
 
 
+def test_extend_validation(lib):
+    d = _dims()
+    def ext(batch=2, rows=3, rs=P, rp=P, ws_bytes=1 << 30):
+        return lib.oscar_extend(ctypes.byref(d), batch, rows, 100, 8, P, rs, rp, P, P, P, P, P, P, P, P, 4, 8, 0.0, P,
+                                ctypes.c_void_p(256), ws_bytes, None)
+    assert ext(rows=0) == ok.OSCAR_OK  # nothing to attend
+    assert ext(rs=None) == ok.OSCAR_ERR_INVALID_ARG
+    assert ext(rp=None) == ok.OSCAR_ERR_INVALID_ARG
+    assert ext(batch=0) == ok.OSCAR_ERR_INVALID_ARG  # rows but no sequences
+    assert ext(rows=-1) == ok.OSCAR_ERR_INVALID_ARG
+    need = lib.oscar_extend_workspace_bytes(ctypes.byref(d), 3, 100, 8, 4, 8)
+    assert need == lib.oscar_decode_workspace_bytes(ctypes.byref(d), 3, 100, 8, 4, 8) > 0
+    assert ext(ws_bytes=need - 1) == ok.OSCAR_ERR_WORKSPACE
+
+
 def _decode(lib, dims, batch=2, msl=100, pps=8, S=4, W=8, ws_bytes=1 << 30, ws=ctypes.c_void_p(256), sink=P):
     return lib.oscar_decode(ctypes.byref(dims), batch, msl, pps, P, P, P, P, P, sink, P, P, P, S, W, 0.0, P, ws,
                             ws_bytes, None)

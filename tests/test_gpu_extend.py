@@ -1,0 +1,84 @@
+"""GPU parity of oscar_extend (chunked prefill / extend attention): the oracle
+recomputes every output from the GPU's own codes and scale/zero (decode
+tolerances: max-abs <= 2e-3, mean-abs <= 2e-4)."""
+
+import numpy as np
+import pytest
+import torch
+
+import int2_rotated_kv_append_gb300 as ok
+from int2_rotated_kv_append_gb300 import synth
+from int2_rotated_kv_append_gb300.cache import Int2Cache
+from parity import compare_decode, oracle_extend_on_gpu_cache
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows(lens, S, W, chunk, seed):
+    """For each sequence: the last `chunk` positions (the new tokens), plus one row in
+    the sink, one in the INT2 bulk and one at the first window position when they exist."""
+    g = np.random.default_rng(seed)
+    seqs, pos = [], []
+    for b, L in enumerate(lens):
+        ps = set(range(max(0, L - chunk), L))
+        if L > 0:
+            ps.add(int(min(S, L) // 2))
+        if L > S + W + 2:
+            ps.add(int(g.integers(S, L - W)))
+            if W > 0:
+                ps.add(L - W)
+        for p in sorted(ps):
+            seqs.append(b)
+            pos.append(p)
+    return np.array(seqs, np.int32), np.array(pos, np.int32)
+
+
+@pytest.mark.parametrize("D,G,Hq,H,lens,S,W,chunk", [
+    (128, 64, 8, 2, [70, 300, 45, 1200], 8, 24, 5),      # tensor-core INT2 kernel, GQA 4
+    (128, 128, 8, 1, [33, 517], 16, 32, 17),             # GQA 8, chunk longer than a page
+    (64, 32, 4, 2, [90, 400], 4, 16, 9),                 # CUDA-core split body
+    (128, 64, 2, 2, [260, 20], 0, 0, 6),                 # no sink, no window: all INT2
+])
+def test_extend_matches_oracle(D, G, Hq, H, lens, S, W, chunk):
+    w = synth.make_workload(num_q_heads=Hq, num_kv_heads=H, head_dim=D, group_size=G, sink_len=S, window_len=W,
+                            seq_lens=lens, seed=D + G + len(lens) + chunk)
+    cache = Int2Cache(w)
+    cache.prefill()
+    rs, rp = _rows(lens, S, W, chunk, seed=chunk)
+    g = torch.Generator().manual_seed(7)
+    q = torch.randn((len(rs), Hq, D), generator=g).to(torch.bfloat16).cuda()
+    out = cache.extend(q, torch.as_tensor(rs).cuda(), torch.as_tensor(rp).cuda())
+    torch.cuda.synchronize()
+    compare_decode(out, oracle_extend_on_gpu_cache(w, cache, q, rs, rp))
+
+
+def test_extend_last_rows_equal_decode():
+    # one row per sequence at position L - 1 with the decode's queries: the same
+    # plan and kernels, so the same outputs bit for bit
+    w = synth.make_workload(num_q_heads=8, num_kv_heads=2, head_dim=128, group_size=64, sink_len=8, window_len=24,
+                            seq_lens=[70, 300, 45, 1200], seed=5)
+    cache = Int2Cache(w)
+    cache.prefill()
+    dec = cache.decode(w.q.cuda())
+    rs = torch.arange(w.batch, dtype=torch.int32).cuda()
+    rp = (w.seq_lens - 1).to(torch.int32).cuda()
+    ext = cache.extend(w.q.cuda(), rs, rp)
+    torch.cuda.synchronize()
+    assert torch.equal(dec, ext)
+
+
+def test_extend_bad_rows_attend_nothing_and_are_flagged():
+    w = synth.make_workload(num_q_heads=4, num_kv_heads=1, head_dim=128, group_size=64, sink_len=4, window_len=8,
+                            seq_lens=[40, 60], seed=6)
+    cache = Int2Cache(w)
+    cache.prefill()
+    ok.oscar_device_errors(reset=True)
+    rs = torch.tensor([0, 2, 1, -1, 1], dtype=torch.int32).cuda()
+    rp = torch.tensor([39, 0, 60, 3, 10], dtype=torch.int32).cuda()
+    q = torch.randn((5, 4, 128)).to(torch.bfloat16).cuda()
+    out = cache.extend(q, rs, rp)
+    torch.cuda.synchronize()
+    flags = ok.oscar_device_errors(reset=True)
+    assert flags & ok.OSCAR_DEVERR_POSITION
+    assert torch.all(out[1:4] == 0)
+    assert torch.any(out[0] != 0) and torch.all(torch.isfinite(out[4]))
