@@ -22,6 +22,15 @@ using namespace oscar_dec;
 
 template <int D, Mode MODE>
 cudaError_t merge(const Params& p, cudaStream_t stream) {
+  if (p.merge_spc > 1) {  // large batch: several sequences per CTA, R_v staged once per CTA
+    const int grid = (p.B + p.merge_spc - 1) / p.merge_spc * p.H;
+    const size_t smem = merge_smem(D, p.ns, p.merge_qpc, p.merge_stage, kMergeThreadsBatch);
+    auto k = merge_kernel<D, MODE, kMergeThreadsBatch, kMergeQBatch>;
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k), kMergeSmemLimit);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kMergeThreadsBatch, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
   const int grid = p.B * p.H * (p.gqa / p.merge_qpc);
   // A grid of at most one CTA per SM (one query head per CTA) is launched early
   // (programmatic dependent launch) so that it is resident, with R_v staged, when
@@ -43,12 +52,21 @@ cudaError_t merge(const Params& p, cudaStream_t stream) {
 }
 
 // Query heads per merge CTA and what the merge stages in shared memory (see
-// merge_kernel): all of a KV head's GQA group per CTA when the batch has at least
-// one (sequence, KV head) per SM, otherwise one query head per CTA (more CTAs),
-// with R_v and, when they fit, the partials staged.
-void merge_config(const oscar_dims_t* d, int B, int ns, Mode mode, int* qpc, int* stage) {
+// merge_kernel): with at least two (sequence, KV head) units per SM (INT2 mode),
+// the GQA groups of several sequences per CTA with R_v staged once; with at least
+// one, a KV head's GQA group per CTA; otherwise one query head per CTA (more
+// CTAs), with R_v and, when they fit, the partials staged.
+void merge_config(const oscar_dims_t* d, int B, int ns, Mode mode, int* qpc, int* stage, int* spc) {
   const int gqa = d->num_q_heads / d->num_kv_heads;
   const long long units = static_cast<long long>(B) * d->num_kv_heads;
+  *spc = 1;
+  if (mode == kMixed && units >= 2LL * num_sms() &&
+      merge_smem(d->head_dim, ns, kMergeQBatch, kStageRv, kMergeThreadsBatch) <= kMergeSmemLimit) {
+    *spc = kMergeQBatch / gqa;
+    *qpc = *spc * gqa;
+    *stage = kStageRv;
+    return;
+  }
   *qpc = units >= num_sms() && merge_smem(d->head_dim, ns, gqa, 0, kMergeThreadsLarge) <= kMergeSmemLimit ? gqa : 1;
   *stage = 0;
   if (units * (gqa / *qpc) <= num_sms()) {
@@ -61,7 +79,8 @@ void merge_config(const oscar_dims_t* d, int B, int ns, Mode mode, int* qpc, int
 template <int D, Mode MODE>
 cudaError_t launch(const Params& p, cudaStream_t stream) {
   if (MODE == kMixed) {
-    cudaError_t e = launch_pdl(qrot_kernel<D>, dim3(p.B * p.H, D / 32), dim3(kQrotThreads), 0, stream, p);
+    const int chunks = (p.B + p.qrot_spc - 1) / p.qrot_spc;
+    cudaError_t e = launch_pdl(qrot_kernel<D>, dim3(chunks * p.H, D / 32), dim3(kQrotThreads), 0, stream, p);
     if (e != cudaSuccess) return e;
   }
   const bool mma = MODE == kMixed ? int2_mma_supported(p) : bf16_mma_supported(p);
@@ -118,7 +137,17 @@ Params base_params(const oscar_dims_t* d, int B, int max_seq_len, const Plan& pl
   p.n_dense = plan.n_dense;
   p.ns = plan.ns;
   p.ml_ns = plan.ml_ns;
-  merge_config(d, B, plan.ns, mode, &p.merge_qpc, &p.merge_stage);
+  merge_config(d, B, plan.ns, mode, &p.merge_qpc, &p.merge_stage, &p.merge_spc);
+  // q-rotation: about four CTAs per SM; a CTA takes up to kQrotMaxQ query heads
+  // (several sequences of one KV head) so that R_k is read once for all of them.
+  {
+    const long long ctas = static_cast<long long>(B) * d->num_kv_heads * (d->head_dim / 32);
+    long long spc = (ctas + 4LL * num_sms() - 1) / (4LL * num_sms());
+    const int cap = kQrotMaxQ / p.gqa;
+    if (spc > cap) spc = cap;
+    if (spc < 1) spc = 1;
+    p.qrot_spc = static_cast<int>(spc);
+  }
   p.mma = plan.mma;
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(d->head_dim));
   p.scale_log2 = scale * 1.4426950408889634f;

@@ -42,7 +42,9 @@ struct Params {
   int B, Hq, H, D, G, gqa, num_pages, max_pages, max_seq_len;
   int S, W, pps, n_paged, n_dense, ns, ml_ns;
   float scale_log2;
-  int merge_qpc;    // query heads per merge CTA (divides gqa)
+  int merge_qpc;    // query heads per merge CTA (divides gqa, or merge_spc * gqa)
+  int merge_spc;    // sequences per merge CTA: 1, or > 1 for the large-batch form (merge_qpc = spc * gqa)
+  int qrot_spc;     // sequences per q-rotation CTA (qrot_spc * gqa <= kQrotMaxQ)
   int merge_stage;  // merge kernel: kStageRv (R_v staged before the wait) | kStagePartials
   int mma;          // 1: tensor-core split kernel (INT2 mode: head_dim 128, group 64 or 128)
   const __nv_bfloat16* q;
@@ -224,64 +226,97 @@ __device__ __forceinline__ uint32_t qk_word(float v_lo, float v_hi, float scale_
   return static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
 }
 
-// q_rot[b][hq] = q[b][hq] . R_k[h] for the GQA query heads of one (b, h), one
-// CTA per block of 32 output columns (grid (B*Hkv, D/32)).  Warp w sums rows
-// [w*D/4, (w+1)*D/4) of the block's columns, read straight from global memory
-// (D/4 independent coalesced loads per lane); the warps' sums are added in
-// order through shared memory.
-//
-// For head_dim 128 the CTA also writes its share of the tensor-core INT2
-// kernel's per-lane QK operands (p.qfrag, kQfragWords words per lane):
-//   words [0, 32): B fragments, word nt*16 + ks*2 + c2 holds fp16 hi (lanes with
-//     g even) or lo (g odd) parts of q_rot * scale * log2(e) * 2^(E - kpos(ch))
-//     for channels (16w + j, 16w + j + 8), w = t + 4*(ks/4), j = 2*(ks%4) + c2,
-//     query 4*nt + g/2 (g = lane/4, t = lane%4); the 16-channel word w lives in
-//     column block w/2, so each CTA writes the words of its two w;
-//   words 32 + 5*nt + {0, 1..4}: for query 4*nt + t, F = 2^(24 - E) and the sums
-//     of q_rot * scale * log2(e) over each column block (the kernel adds the
-//     blocks of a group).
+// q_rot[b][hq] = q[b][hq] . R_k[h] for the GQA query heads of qrot_spc
+// consecutive sequences b of one KV head h, one CTA per block of 32 output
+// columns (grid (ceil(B / spc) * Hkv, D/32)): the CTA reads its block of R_k
+// once for all of them.  Warp w sums rows [w*D/4, (w+1)*D/4) of the block's
+// columns, read straight from global memory (D/4 independent coalesced loads per
+// lane); the warps' sums are added in order through shared memory.
+// For the tensor-core INT2 kernel (D = 128, qfrag non-null) the CTA also writes
+// the per-lane QK B-fragments of its two 16-channel words for each (b, h) and,
+// per query of every n-tile,
+//   * F = 2^(24 - E) (the exact power of two the codes' subnormal scale undoes),
+//   * the block sum of q_rot * scale * log2(e) (the kernel adds the blocks of a
+//     group).
 // E = 15 - ceil(log2(||q|| * scale * log2(e) * (1 + 2^-10))): since R is
 // orthogonal every |q_rot[ch]| <= ||q||, so every B value fits fp16.
+constexpr int kQrotMaxQ = 32;  // query heads per q-rotation CTA (qrot_spc * gqa)
+
 template <int D>
 __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
   constexpr int kRows = D / 4;
-  __shared__ float qs[kMaxGqa * D];
-  __shared__ float part[4][kMaxGqa][32];
-  __shared__ float qrb[kMaxGqa][32];
-  __shared__ int E_s[kMaxGqa];
+  __shared__ __align__(16) float qs[kQrotMaxQ * D];
+  __shared__ float part[4][kQrotMaxQ][32];
+  __shared__ float qrb[kQrotMaxQ][32];
+  __shared__ int E_s[kQrotMaxQ];
   grid_dep_launch_dependents();
-  const int b = blockIdx.x / p.H, h = blockIdx.x % p.H, cb = blockIdx.y;
+  const int spc = p.qrot_spc;
+  const int h = blockIdx.x % p.H, b0 = (blockIdx.x / p.H) * spc, cb = blockIdx.y;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int gqa = p.gqa;
-  const size_t q0 = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * gqa) * D;
+  const int nb = min(spc, p.B - b0);  // sequences of this CTA
+  const int nq = nb * gqa;            // query j * gqa + qi: head h * gqa + qi of sequence b0 + j
   const float* R = p.R_k + static_cast<size_t>(h) * D * D + static_cast<size_t>(warp) * kRows * D + 32 * cb + lane;
   float r[kRows];
 #pragma unroll
   for (int rr = 0; rr < kRows; ++rr) r[rr] = __ldg(R + static_cast<size_t>(rr) * D);
-  for (int i = tid; i < gqa * D; i += kQrotThreads) qs[i] = __bfloat162float(p.q[q0 + i]);
+  {  // q of the CTA's queries: 16-byte loads, all issued before any is used
+    constexpr int kQv = kQrotMaxQ * D / 8 / kQrotThreads;
+    uint4 qv[kQv];
+#pragma unroll
+    for (int u = 0; u < kQv; ++u) {
+      const int i = u * kQrotThreads + tid;  // 8-element chunk
+      if (i < nq * D / 8) {
+        const int j = (8 * i) / (gqa * D), rem = (8 * i) % (gqa * D);
+        qv[u] = __ldg(reinterpret_cast<const uint4*>(
+            p.q + (static_cast<size_t>(b0 + j) * p.Hq + static_cast<size_t>(h) * gqa) * D + rem));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kQv; ++u) {
+      const int i = u * kQrotThreads + tid;
+      if (i < nq * D / 8) {
+        const uint32_t wv[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          qs[8 * i + 2 * e] = __uint_as_float(wv[e] << 16);
+          qs[8 * i + 2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
+        }
+      }
+    }
+  }
   __syncthreads();
   if (D == 128 && p.qfrag != nullptr) {
     // fp16 exponents of the QK operands from ||q|| (one warp per query): since R
     // is orthogonal every |q_rot[ch]| <= ||q||
-    for (int qi = warp; qi < gqa; qi += kQrotThreads / 32) {
+    for (int qq = warp; qq < nq; qq += kQrotThreads / 32) {
       float ss = 0.f;
-      for (int i = lane; i < D; i += 32) ss = fmaf(qs[qi * D + i], qs[qi * D + i], ss);
+      for (int i = lane; i < D; i += 32) ss = fmaf(qs[qq * D + i], qs[qq * D + i], ss);
       for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-      if (lane == 0) E_s[qi] = qk_exponent(sqrtf(ss), p.scale_log2);
+      if (lane == 0) E_s[qq] = qk_exponent(sqrtf(ss), p.scale_log2);
     }
   }
-  for (int qi = 0; qi < gqa; ++qi) {
-    float acc = 0.f;
+  for (int q0 = 0; q0 < nq; q0 += 4) {  // four independent chains; q read 4 rows at a time
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int rr = 0; rr < kRows; ++rr) acc = fmaf(qs[qi * D + warp * kRows + rr], r[rr], acc);
-    part[warp][qi][lane] = acc;
+    for (int r4 = 0; r4 < kRows; r4 += 4)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (q0 + k < nq) {
+          const float4 qv = *reinterpret_cast<const float4*>(&qs[(q0 + k) * D + warp * kRows + r4]);
+          acc[k] = fmaf(qv.w, r[r4 + 3], fmaf(qv.z, r[r4 + 2], fmaf(qv.y, r[r4 + 1], fmaf(qv.x, r[r4], acc[k]))));
+        }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (q0 + k < nq) part[warp][q0 + k][lane] = acc[k];
   }
   __syncthreads();
-  for (int idx = tid; idx < gqa * 32; idx += kQrotThreads) {
-    const int qi = idx / 32, c = idx % 32;
-    const float tot = ((part[0][qi][c] + part[1][qi][c]) + part[2][qi][c]) + part[3][qi][c];
-    p.q_rot[q0 + static_cast<size_t>(qi) * D + 32 * cb + c] = tot;
-    qrb[qi][c] = tot;
+  for (int idx = tid; idx < nq * 32; idx += kQrotThreads) {
+    const int qq = idx / 32, c = idx % 32;
+    const float tot = ((part[0][qq][c] + part[1][qq][c]) + part[2][qq][c]) + part[3][qq][c];
+    const int j = qq / gqa, qi = qq % gqa;
+    p.q_rot[((static_cast<size_t>(b0 + j) * p.Hq + static_cast<size_t>(h) * gqa + qi)) * D + 32 * cb + c] = tot;
+    qrb[qq][c] = tot;
   }
   if (p.qfrag == nullptr) {
     grid_dep_wait();  // completion stays ordered after the preceding kernel
@@ -289,30 +324,34 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
   }
   if constexpr (D == 128) {
   __syncthreads();  // qrb (all columns of the block) complete
-  uint32_t* dst = p.qfrag + (static_cast<size_t>(b) * p.H + h) * (32 * kQfragWords);
-  // fragment words of this block's two 16-channel words w = 2*cb, 2*cb + 1:
-  // lanes with t = w % 4 (8 values of g), k-steps 4*(w/4) .. +3, c2 in {0,1}, nt in {0,1}
-  for (int idx = tid; idx < 2 * 8 * 4 * 2 * 2; idx += kQrotThreads) {
-    const int w = 2 * cb + (idx >> 7);
-    const int gg8 = (idx >> 4) & 7, kk = (idx >> 2) & 3, c2 = (idx >> 1) & 1, nt = idx & 1;
+  // fragment words of this block's two 16-channel words w = 2*cb, 2*cb + 1, for
+  // each sequence: lanes with t = w % 4 (8 values of g), k-steps 4*(w/4) .. +3,
+  // c2 in {0,1}, nt in {0,1}
+  for (int idx = tid; idx < nb * 256; idx += kQrotThreads) {
+    const int j = idx >> 8, it = idx & 255;
+    uint32_t* dst = p.qfrag + (static_cast<size_t>(b0 + j) * p.H + h) * (32 * kQfragWords);
+    const int w = 2 * cb + (it >> 7);
+    const int gg8 = (it >> 4) & 7, kk = (it >> 2) & 3, c2 = (it >> 1) & 1, nt = it & 1;
     const int t = w & 3, L = 4 * gg8 + t, ks = 4 * (w >> 2) + kk;
     const int qb = 4 * nt + (gg8 >> 1);
-    const int j = 2 * kk + c2;
-    const int ch_lo = 16 * w + j, ch_hi = ch_lo + 8;
+    const int jw = 2 * kk + c2;
+    const int ch_lo = 16 * w + jw, ch_hi = ch_lo + 8;
     uint32_t word = 0;
     if (qb < gqa)
-      word = qk_word(qrb[qb][ch_lo - 32 * cb], qrb[qb][ch_hi - 32 * cb], p.scale_log2, E_s[qb], ch_lo, gg8 & 1);
+      word = qk_word(qrb[j * gqa + qb][ch_lo - 32 * cb], qrb[j * gqa + qb][ch_hi - 32 * cb], p.scale_log2,
+                     E_s[j * gqa + qb], ch_lo, gg8 & 1);
     dst[L * kQfragWords + nt * 16 + ks * 2 + c2] = word;
   }
   // factors: block sums of query 4*nt + t for the 32 lanes (and F from block 0)
-  if (tid < 64) {
-    const int L = tid / 2, nt = tid % 2;
+  for (int idx = tid; idx < nb * 64; idx += kQrotThreads) {
+    const int j = idx >> 6, L = (idx & 63) / 2, nt = idx & 1;
+    uint32_t* dst = p.qfrag + (static_cast<size_t>(b0 + j) * p.H + h) * (32 * kQfragWords);
     const int qi = 4 * nt + (L & 3);
     float sum = 0.f, F = 0.f;
     if (qi < gqa) {
-      for (int c = 0; c < 32; ++c) sum += qrb[qi][c];
+      for (int c = 0; c < 32; ++c) sum += qrb[j * gqa + qi][c];
       sum *= p.scale_log2;
-      F = pow2i(24 - E_s[qi]);
+      F = pow2i(24 - E_s[j * gqa + qi]);
     }
     dst[L * kQfragWords + 32 + 5 * nt + 1 + cb] = __float_as_uint(sum);
     if (cb == 0) {
@@ -560,7 +599,9 @@ __global__ void __launch_bounds__(kThreads) split_kernel(Params p) {
 // where the rotated partials are the INT2 splits (s < n_paged) and the plain ones
 // the BF16 sink/window splits; splits that attended nothing (m = -inf) have
 // weight 0 and their outputs are not read.  One CTA covers merge_qpc query heads
-// of one (sequence, KV head): grid B * Hkv * (gqa / merge_qpc).
+// of one (sequence, KV head): grid B * Hkv * (gqa / merge_qpc); or, for large
+// batches, the gqa query heads of one KV head in merge_spc consecutive sequences
+// (grid ceil(B / spc) * Hkv), so that R_v is read once for all of them.
 //   phase A  one warp per query: maximum, denominator, weights;
 //   phase B  thread (query, 4-channel quad, split group) sums a strided subset of
 //            the splits, then the split groups are added in order;
@@ -570,17 +611,19 @@ __global__ void __launch_bounds__(kThreads) split_kernel(Params p) {
 // before it waits for them (kStageRv) and the partials with one bulk copy after
 // (kStagePartials); a large grid reads both from L2.
 constexpr int kMergeThreadsLarge = 256;  // threads per merge CTA, large grids
+constexpr int kMergeThreadsBatch = 512;  // threads per merge CTA, several sequences per CTA
+constexpr int kMergeQBatch = 16;         // query heads per CTA of that form
 constexpr int kMergeThreadsSmall = 256;  // threads per merge CTA, grids of at most one CTA per SM (one query head each)
 constexpr int kStageRv = 1, kStagePartials = 2;
 
 // Dynamic shared memory of the merge kernel: [R_v D x D] [partials qpc x ns x D,
-// (m, l) qpc x ml_ns x 2] weights [qpc][ns], denominators [8], phase B/C scratch
-// (2 x kMergeThreads float4), rotated and plain sums [qpc][D], two mbarriers.
+// (m, l) qpc x ml_ns x 2] weights [qpc][ns], denominators [16], phase B/C scratch
+// (max(8, qpc) x kMergeThreads floats), rotated and plain sums [qpc][D], two mbarriers.
 constexpr size_t merge_smem(int D, int ns, int qpc, int stage, int threads) {
   return ((stage & kStageRv) ? static_cast<size_t>(D) * D * 4 : 0) +
          ((stage & kStagePartials) ? static_cast<size_t>(qpc) * ns * D * 4 + static_cast<size_t>(qpc) * ((ns + 1) & ~1) * 8
                                    : 0) +
-         (static_cast<size_t>((qpc * ns + 3) & ~3) + 8) * 4 + 2 * static_cast<size_t>(threads) * 16 +
+         (static_cast<size_t>((qpc * ns + 3) & ~3) + 16) * 4 + static_cast<size_t>(qpc > 8 ? qpc : 8) * threads * 4 +
          2 * static_cast<size_t>(qpc) * D * 4 + 16;
 }
 
@@ -591,11 +634,25 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
   extern __shared__ __align__(128) float msm[];
   constexpr bool kRot = MODE == kMixed;
   constexpr int kQuads = D / 4;
-  const int qpc = p.merge_qpc;
-  const int qch = p.gqa / qpc;
-  const int unit = blockIdx.x / qch, qc = blockIdx.x % qch;
-  const int b = unit / p.H, h = unit % p.H;
-  const size_t row0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * p.gqa + static_cast<size_t>(qc) * qpc;
+  const int qpc = p.merge_qpc, spc = p.merge_spc;
+  int h, b0;
+  size_t row0 = 0;
+  if (spc > 1) {  // query heads qi of sequences b0 + qi / gqa, KV head h
+    h = blockIdx.x % p.H;
+    b0 = (blockIdx.x / p.H) * spc;
+  } else {
+    const int qch = p.gqa / qpc;
+    const int unit = blockIdx.x / qch, qc = blockIdx.x % qch;
+    b0 = unit / p.H;
+    h = unit % p.H;
+    row0 = static_cast<size_t>(b0) * p.Hq + static_cast<size_t>(h) * p.gqa + static_cast<size_t>(qc) * qpc;
+  }
+  // (sequence, query head) row of query qi, and how many queries of the CTA exist
+  auto row_of = [&](int qi) -> size_t {
+    return spc > 1 ? static_cast<size_t>(b0 + qi / p.gqa) * p.Hq + static_cast<size_t>(h) * p.gqa + qi % p.gqa
+                   : row0 + qi;
+  };
+  const int q_valid = spc > 1 ? min(qpc, (p.B - b0) * p.gqa) : qpc;
   const int ns = p.ns, np = kRot ? p.n_paged : 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool st_rv = kRot && (p.merge_stage & kStageRv) != 0;
@@ -604,9 +661,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
   float* po_s = Rs + (st_rv ? D * D : 0);                                   // [qpc][ns][D] (st_po)
   float* ml_s = po_s + (st_po ? static_cast<size_t>(qpc) * ns * D : 0);     // [qpc][ml_ns][2] (st_po)
   float* wts = ml_s + (st_po ? static_cast<size_t>(qpc) * p.ml_ns * 2 : 0);  // [qpc][ns]
-  float* den_s = wts + ((qpc * ns + 3) & ~3);                               // [8]
-  float4* red = reinterpret_cast<float4*>(den_s + 8);                       // [2][kMergeThreads]
-  float* o_rot = reinterpret_cast<float*>(red + 2 * kMergeThreads);         // [qpc][D]
+  float* den_s = wts + ((qpc * ns + 3) & ~3);                               // [16]
+  float4* red = reinterpret_cast<float4*>(den_s + 16);                      // [2][kMergeThreads]; phase C parts
+  float* o_rot = reinterpret_cast<float*>(red) + (qpc > 8 ? qpc : 8) * kMergeThreads;  // [qpc][D]
   float* o_plain = o_rot + qpc * D;                                         // [qpc][D]
   uint64_t* bars = reinterpret_cast<uint64_t*>(o_plain + qpc * D);         // [2]
   if (tid == 0 && (st_rv || st_po)) {
@@ -635,9 +692,14 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
   // phase A: one pass over (m, l) with a running maximum per lane, combined
   // across the warp by log-sum-exp; then the weights from the staged maxima
   for (int qi = warp; qi < qpc; qi += kMergeThreads / 32) {
-    const float2* ml = reinterpret_cast<const float2*>(st_po ? ml_s + static_cast<size_t>(qi) * p.ml_ns * 2
-                                                             : p.part_ml + (row0 + qi) * p.ml_ns * 2);
     float* wq = wts + qi * ns;
+    if (qi >= q_valid) {  // past the last sequence: no partials, weight 0
+      for (int s = lane; s < ns; s += 32) wq[s] = 0.f;
+      if (lane == 0) den_s[qi] = 0.f;
+      continue;
+    }
+    const float2* ml = reinterpret_cast<const float2*>(st_po ? ml_s + static_cast<size_t>(qi) * p.ml_ns * 2
+                                                             : p.part_ml + row_of(qi) * p.ml_ns * 2);
     float M = -INFINITY, den = 0.f;
     for (int s0 = lane; s0 < ns; s0 += 4 * 32) {
       float2 v[4];
@@ -676,7 +738,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
     const int item = tid % items, grp = tid / items;
     const int qi = item / kQuads, cq = item % kQuads;
     const float4* po = reinterpret_cast<const float4*>(st_po ? po_s + static_cast<size_t>(qi) * ns * D
-                                                             : p.part_o + (row0 + qi) * ns * D) + cq;
+                                                             : p.part_o + row_of(qi) * ns * D) + cq;
     const float* wq = wts + qi * ns;
     float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), ap = ar;
     for (int s0 = grp; s0 < ns; s0 += 4 * sg) {
@@ -766,7 +828,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
       for (int jp = 0; jp < kParts; ++jp) u += part[(jp * qpc + qi) * D + cc];
     }
     const float den = den_s[qi];
-    p.out[(row0 + qi) * D + cc] = (ok && den > 0.f) ? u / den : 0.f;
+    if (qi < q_valid) p.out[row_of(qi) * D + cc] = (ok && den > 0.f) ? u / den : 0.f;
   }
 }
 

@@ -51,6 +51,19 @@ def test_decode_131k_gqa8_config_sampled():
     compare_decode(out, oracle_decode_on_gpu_cache(w, cache, pairs=pairs), pairs=pairs)
 
 
+@pytest.mark.parametrize("Hq,H,B", [(6, 1, 311), (4, 2, 157), (8, 8, 40)])
+def test_decode_large_batch_merge(Hq, H, B):
+    # At least two (sequence, KV head) units per SM: the merge takes the GQA groups
+    # of several sequences per CTA (16 query heads; 12 for GQA 6), the last CTA ragged.
+    g = np.random.default_rng(B + Hq)
+    lens = g.integers(1, 200, B).tolist()
+    w = synth.make_workload(num_q_heads=Hq, num_kv_heads=H, head_dim=128, group_size=64, sink_len=8, window_len=16,
+                            seq_lens=lens, seed=B, device="cuda")
+    cache = _built(w)
+    out = cache.decode(w.q)
+    compare_decode(out, oracle_decode_on_gpu_cache(w, cache))
+
+
 @pytest.mark.parametrize("D,G,Hq,H", [(64, 32, 1, 1), (64, 64, 4, 2), (128, 64, 8, 2), (128, 32, 6, 3),
                                       (128, 128, 8, 1), (128, 64, 2, 2)])
 def test_decode_edge_lengths(D, G, Hq, H):
