@@ -177,10 +177,11 @@ def workload_config(args, w, batch, seq_len, pps, l2_policy):
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one oscar_decode
-# launch (q-rotation + split + merge kernels) on the batch-1 32K workload, from one
-# ncu capture of the three kernels (cold caches: the split partials are re-read
-# from DRAM there, from L2 in the timed loop).  None for other workloads.
-MEASURED_DECODE_TRAFFIC = {1: 548608 + 21765888 + 2084096}
+# launch (q-rotation + split + merge kernels) on the batch-1 32K and batch-64
+# workloads, from one ncu capture of the three kernels each (cold caches: the
+# split partials are re-read from DRAM there, from L2 in the timed loop).
+MEASURED_DECODE_TRAFFIC = {1: 554240 + 21765888 + 2091008,
+                           2: 1070848 + (424401152 + 5219584) + 8040960}
 
 
 def dist_setup():
