@@ -741,17 +741,18 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
                                                              : p.part_o + row_of(qi) * ns * D) + cq;
     const float* wq = wts + qi * ns;
     float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), ap = ar;
-    for (int s0 = grp; s0 < ns; s0 += 4 * sg) {
-      float w[4];
-      float4 v[4];
+    constexpr int kU = kQMax >= 16 ? 8 : 4;  // partials in flight per thread
+    for (int s0 = grp; s0 < ns; s0 += kU * sg) {
+      float w[kU];
+      float4 v[kU];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kU; ++k) {
         const int s = s0 + k * sg;
         w[k] = s < ns ? wq[s] : 0.f;
         v[k] = w[k] != 0.f ? po[static_cast<size_t>(s) * kQuads] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kU; ++k) {
         const float wr = s0 + k * sg < np ? w[k] : 0.f, wp = w[k] - wr;
         ar.x = fmaf(wr, v[k].x, ar.x); ar.y = fmaf(wr, v[k].y, ar.y);
         ar.z = fmaf(wr, v[k].z, ar.z); ar.w = fmaf(wr, v[k].w, ar.w);
