@@ -554,8 +554,8 @@ __global__ void __launch_bounds__(kUmThreads, 1) append_umma_kernel(
   }
 }
 
-// cuTensorMapEncodeTiled, taken from the driver through the runtime (no link
-// against the driver library).
+// cuTensorMapEncodeTiled, taken from the CUDA driver API through the runtime (no link
+// against libcuda).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);

@@ -617,13 +617,13 @@ constexpr int kMergeThreadsSmall = 256;  // threads per merge CTA, grids of at m
 constexpr int kStageRv = 1, kStagePartials = 2;
 
 // Dynamic shared memory of the merge kernel: [R_v D x D] [partials qpc x ns x D,
-// (m, l) qpc x ml_ns x 2] weights [qpc][ns], denominators [16], phase B/C scratch
+// (m, l) qpc x ml_ns x 2] weights [qpc][ns], denominators [16] and group maxima/sums [48], phase B/C scratch
 // (max(8, qpc) x kMergeThreads floats), rotated and plain sums [qpc][D], two mbarriers.
 constexpr size_t merge_smem(int D, int ns, int qpc, int stage, int threads) {
   return ((stage & kStageRv) ? static_cast<size_t>(D) * D * 4 : 0) +
          ((stage & kStagePartials) ? static_cast<size_t>(qpc) * ns * D * 4 + static_cast<size_t>(qpc) * ((ns + 1) & ~1) * 8
                                    : 0) +
-         (static_cast<size_t>((qpc * ns + 3) & ~3) + 16) * 4 + static_cast<size_t>(qpc > 8 ? qpc : 8) * threads * 4 +
+         (static_cast<size_t>((qpc * ns + 3) & ~3) + 64) * 4 + static_cast<size_t>(qpc > 8 ? qpc : 8) * threads * 4 +
          2 * static_cast<size_t>(qpc) * D * 4 + 16;
 }
 
@@ -661,8 +661,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
   float* po_s = Rs + (st_rv ? D * D : 0);                                   // [qpc][ns][D] (st_po)
   float* ml_s = po_s + (st_po ? static_cast<size_t>(qpc) * ns * D : 0);     // [qpc][ml_ns][2] (st_po)
   float* wts = ml_s + (st_po ? static_cast<size_t>(qpc) * p.ml_ns * 2 : 0);  // [qpc][ns]
-  float* den_s = wts + ((qpc * ns + 3) & ~3);                               // [16]
-  float4* red = reinterpret_cast<float4*>(den_s + 16);                      // [2][kMergeThreads]; phase C parts
+  float* den_s = wts + ((qpc * ns + 3) & ~3);                               // [16] (+ group maxima, sums)
+  float4* red = reinterpret_cast<float4*>(den_s + 64);                      // [2][kMergeThreads]; phase C parts
   float* o_rot = reinterpret_cast<float*>(red) + (qpc > 8 ? qpc : 8) * kMergeThreads;  // [qpc][D]
   float* o_plain = o_rot + qpc * D;                                         // [qpc][D]
   uint64_t* bars = reinterpret_cast<uint64_t*>(o_plain + qpc * D);         // [2]
@@ -689,90 +689,148 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(Params p) {
     ok = mbar_wait_bounded(smem_u32(&bars[1]), 0);
   }
 
-  // phase A: one pass over (m, l) with a running maximum per lane, combined
-  // across the warp by log-sum-exp; then the weights from the staged maxima
-  for (int qi = warp; qi < qpc; qi += kMergeThreads / 32) {
-    float* wq = wts + qi * ns;
-    if (qi >= q_valid) {  // past the last sequence: no partials, weight 0
-      for (int s = lane; s < ns; s += 32) wq[s] = 0.f;
-      if (lane == 0) den_s[qi] = 0.f;
-      continue;
+  if constexpr (kQMax == 1) {
+    // One query head per CTA: phases A and B in one pass.  Thread (quad cq, group
+    // grp) runs an online log-sum-exp over its splits grp, grp + sg, ... (rotated
+    // and plain sums kept apart); the groups are then combined in order.
+    constexpr int items = kQuads;
+    constexpr int sg = kMergeThreads / items;
+    static_assert(sg <= 24, "group maxima and sums are staged for at most 24 groups");
+    float* gm = den_s + 16;  // [sg] group maxima
+    float* gl = den_s + 40;  // [sg] group denominators
+    const int cq = tid % items, grp = tid / items;
+    const float2* ml = reinterpret_cast<const float2*>(st_po ? ml_s : p.part_ml + row0 * p.ml_ns * 2);
+    const float4* po = reinterpret_cast<const float4*>(st_po ? po_s : p.part_o + row0 * ns * D) + cq;
+    float m = -INFINITY, l = 0.f;
+    float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), ap = ar;
+    for (int sp = grp; sp < ns; sp += sg) {
+      const float2 v = ml[sp];
+      if (v.x == -INFINITY) continue;  // the split attended nothing: its output is not read
+      if (v.x > m) {
+        const float f = m == -INFINITY ? 0.f : fast_exp2(m - v.x);
+        l *= f;
+        ar.x *= f; ar.y *= f; ar.z *= f; ar.w *= f;
+        ap.x *= f; ap.y *= f; ap.z *= f; ap.w *= f;
+        m = v.x;
+      }
+      const float wgt = fast_exp2(v.x - m);
+      const float4 o = po[static_cast<size_t>(sp) * kQuads];
+      l = fmaf(wgt, v.y, l);
+      float4& acc = sp < np ? ar : ap;
+      acc.x = fmaf(wgt, o.x, acc.x); acc.y = fmaf(wgt, o.y, acc.y);
+      acc.z = fmaf(wgt, o.z, acc.z); acc.w = fmaf(wgt, o.w, acc.w);
     }
-    const float2* ml = reinterpret_cast<const float2*>(st_po ? ml_s + static_cast<size_t>(qi) * p.ml_ns * 2
-                                                             : p.part_ml + row_of(qi) * p.ml_ns * 2);
-    float M = -INFINITY, den = 0.f;
-    for (int s0 = lane; s0 < ns; s0 += 4 * 32) {
-      float2 v[4];
+    red[grp * items + cq] = ar;
+    red[kMergeThreads + grp * items + cq] = ap;
+    if (cq == 0) {
+      gm[grp] = m;
+      gl[grp] = l;
+    }
+    ok = __syncthreads_and(ok);
+    if (tid < items) {
+      float M = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = s0 + 32 * k < ns ? ml[s0 + 32 * k] : make_float2(-INFINITY, 0.f);
+      for (int g = 0; g < sg; ++g) M = fmaxf(M, gm[g]);
+      float4 sr = make_float4(0.f, 0.f, 0.f, 0.f), sp4 = sr;
+      float den = 0.f;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (s0 + 32 * k < ns) wq[s0 + 32 * k] = v[k].x;
-        if (v[k].x != -INFINITY) {
-          if (v[k].x > M) {
-            den = M == -INFINITY ? 0.f : den * fast_exp2(M - v[k].x);
-            M = v[k].x;
+      for (int g = 0; g < sg; ++g) {
+        const float f = gm[g] == -INFINITY ? 0.f : fast_exp2(gm[g] - M);
+        const float4 x = red[g * items + tid], y = red[kMergeThreads + g * items + tid];
+        sr.x = fmaf(f, x.x, sr.x); sr.y = fmaf(f, x.y, sr.y); sr.z = fmaf(f, x.z, sr.z); sr.w = fmaf(f, x.w, sr.w);
+        sp4.x = fmaf(f, y.x, sp4.x); sp4.y = fmaf(f, y.y, sp4.y); sp4.z = fmaf(f, y.z, sp4.z); sp4.w = fmaf(f, y.w, sp4.w);
+        den = fmaf(f, gl[g], den);
+      }
+      reinterpret_cast<float4*>(o_rot)[tid] = sr;
+      reinterpret_cast<float4*>(o_plain)[tid] = sp4;
+      if (tid == 0) den_s[0] = den;
+    }
+  } else {
+    // phase A: one pass over (m, l) with a running maximum per lane, combined
+    // across the warp by log-sum-exp; then the weights from the staged maxima
+    for (int qi = warp; qi < qpc; qi += kMergeThreads / 32) {
+      float* wq = wts + qi * ns;
+      if (qi >= q_valid) {  // past the last sequence: no partials, weight 0
+        for (int s = lane; s < ns; s += 32) wq[s] = 0.f;
+        if (lane == 0) den_s[qi] = 0.f;
+        continue;
+      }
+      const float2* ml = reinterpret_cast<const float2*>(st_po ? ml_s + static_cast<size_t>(qi) * p.ml_ns * 2
+                                                               : p.part_ml + row_of(qi) * p.ml_ns * 2);
+      float M = -INFINITY, den = 0.f;
+      for (int s0 = lane; s0 < ns; s0 += 4 * 32) {
+        float2 v[4];
+  #pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = s0 + 32 * k < ns ? ml[s0 + 32 * k] : make_float2(-INFINITY, 0.f);
+  #pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (s0 + 32 * k < ns) wq[s0 + 32 * k] = v[k].x;
+          if (v[k].x != -INFINITY) {
+            if (v[k].x > M) {
+              den = M == -INFINITY ? 0.f : den * fast_exp2(M - v[k].x);
+              M = v[k].x;
+            }
+            den = fmaf(fast_exp2(v[k].x - M), v[k].y, den);
           }
-          den = fmaf(fast_exp2(v[k].x - M), v[k].y, den);
         }
       }
+      float Mw = M;
+  #pragma unroll
+      for (int off = 16; off > 0; off >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, off));
+      den = M == -INFINITY ? 0.f : den * fast_exp2(M - Mw);
+  #pragma unroll
+      for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+      for (int s = lane; s < ns; s += 32) {
+        const float m = wq[s];
+        wq[s] = (m == -INFINITY || Mw == -INFINITY) ? 0.f : fast_exp2(m - Mw);
+      }
+      if (lane == 0) den_s[qi] = den;
     }
-    float Mw = M;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, off));
-    den = M == -INFINITY ? 0.f : den * fast_exp2(M - Mw);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-    for (int s = lane; s < ns; s += 32) {
-      const float m = wq[s];
-      wq[s] = (m == -INFINITY || Mw == -INFINITY) ? 0.f : fast_exp2(m - Mw);
-    }
-    if (lane == 0) den_s[qi] = den;
-  }
-  ok = __syncthreads_and(ok);
+    ok = __syncthreads_and(ok);
 
-  // phase B
-  const int items = qpc * kQuads;
-  const int sg = kMergeThreads / items;
-  if (tid < items * sg) {
-    const int item = tid % items, grp = tid / items;
-    const int qi = item / kQuads, cq = item % kQuads;
-    const float4* po = reinterpret_cast<const float4*>(st_po ? po_s + static_cast<size_t>(qi) * ns * D
-                                                             : p.part_o + row_of(qi) * ns * D) + cq;
-    const float* wq = wts + qi * ns;
-    float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), ap = ar;
-    constexpr int kU = kQMax >= 16 ? 8 : 4;  // partials in flight per thread
-    for (int s0 = grp; s0 < ns; s0 += kU * sg) {
-      float w[kU];
-      float4 v[kU];
-#pragma unroll
-      for (int k = 0; k < kU; ++k) {
-        const int s = s0 + k * sg;
-        w[k] = s < ns ? wq[s] : 0.f;
-        v[k] = w[k] != 0.f ? po[static_cast<size_t>(s) * kQuads] : make_float4(0.f, 0.f, 0.f, 0.f);
+    // phase B
+    const int items = qpc * kQuads;
+    const int sg = kMergeThreads / items;
+    if (tid < items * sg) {
+      const int item = tid % items, grp = tid / items;
+      const int qi = item / kQuads, cq = item % kQuads;
+      const float4* po = reinterpret_cast<const float4*>(st_po ? po_s + static_cast<size_t>(qi) * ns * D
+                                                               : p.part_o + row_of(qi) * ns * D) + cq;
+      const float* wq = wts + qi * ns;
+      float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), ap = ar;
+      constexpr int kU = kQMax >= 16 ? 8 : 4;  // partials in flight per thread
+      for (int s0 = grp; s0 < ns; s0 += kU * sg) {
+        float w[kU];
+        float4 v[kU];
+  #pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int s = s0 + k * sg;
+          w[k] = s < ns ? wq[s] : 0.f;
+          v[k] = w[k] != 0.f ? po[static_cast<size_t>(s) * kQuads] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+  #pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const float wr = s0 + k * sg < np ? w[k] : 0.f, wp = w[k] - wr;
+          ar.x = fmaf(wr, v[k].x, ar.x); ar.y = fmaf(wr, v[k].y, ar.y);
+          ar.z = fmaf(wr, v[k].z, ar.z); ar.w = fmaf(wr, v[k].w, ar.w);
+          ap.x = fmaf(wp, v[k].x, ap.x); ap.y = fmaf(wp, v[k].y, ap.y);
+          ap.z = fmaf(wp, v[k].z, ap.z); ap.w = fmaf(wp, v[k].w, ap.w);
+        }
       }
-#pragma unroll
-      for (int k = 0; k < kU; ++k) {
-        const float wr = s0 + k * sg < np ? w[k] : 0.f, wp = w[k] - wr;
-        ar.x = fmaf(wr, v[k].x, ar.x); ar.y = fmaf(wr, v[k].y, ar.y);
-        ar.z = fmaf(wr, v[k].z, ar.z); ar.w = fmaf(wr, v[k].w, ar.w);
-        ap.x = fmaf(wp, v[k].x, ap.x); ap.y = fmaf(wp, v[k].y, ap.y);
-        ap.z = fmaf(wp, v[k].z, ap.z); ap.w = fmaf(wp, v[k].w, ap.w);
+      red[grp * items + item] = ar;
+      red[kMergeThreads + grp * items + item] = ap;
+    }
+    __syncthreads();
+    if (tid < items) {
+      float4 ar = red[tid], ap = red[kMergeThreads + tid];
+      for (int grp = 1; grp < sg; ++grp) {
+        const float4 x = red[grp * items + tid], y = red[kMergeThreads + grp * items + tid];
+        ar.x += x.x; ar.y += x.y; ar.z += x.z; ar.w += x.w;
+        ap.x += y.x; ap.y += y.y; ap.z += y.z; ap.w += y.w;
       }
+      reinterpret_cast<float4*>(o_rot)[tid] = ar;  // item = qi * kQuads + cq
+      reinterpret_cast<float4*>(o_plain)[tid] = ap;
     }
-    red[grp * items + item] = ar;
-    red[kMergeThreads + grp * items + item] = ap;
-  }
-  __syncthreads();
-  if (tid < items) {
-    float4 ar = red[tid], ap = red[kMergeThreads + tid];
-    for (int grp = 1; grp < sg; ++grp) {
-      const float4 x = red[grp * items + tid], y = red[kMergeThreads + grp * items + tid];
-      ar.x += x.x; ar.y += x.y; ar.z += x.z; ar.w += x.w;
-      ap.x += y.x; ap.y += y.y; ap.z += y.z; ap.w += y.w;
-    }
-    reinterpret_cast<float4*>(o_rot)[tid] = ar;  // item = qi * kQuads + cq
-    reinterpret_cast<float4*>(o_plain)[tid] = ap;
   }
   if (st_rv) ok = mbar_wait_bounded(smem_u32(&bars[0]), 0) && ok;
   ok = __syncthreads_and(ok);

@@ -82,3 +82,37 @@ def test_extend_bad_rows_attend_nothing_and_are_flagged():
     assert flags & ok.OSCAR_DEVERR_POSITION
     assert torch.all(out[1:4] == 0)
     assert torch.any(out[0] != 0) and torch.all(torch.isfinite(out[4]))
+
+
+def test_chunked_prefill_flow_append_mixed_then_extend():
+    # The serving flow: the cached prefix, then a chunk of new tokens, both appended
+    # with oscar_append_mixed (INT2 + sink/window rows); the chunk's query rows then
+    # attend causally.  The ring after the two appends equals the one-shot buffers.
+    S, W, chunk = 16, 48, 12
+    lens = [300, 700, 40]
+    w = synth.make_workload(num_q_heads=8, num_kv_heads=2, head_dim=128, group_size=64, sink_len=S, window_len=W,
+                            seq_lens=lens, seed=31)
+    cache = Int2Cache(w)
+    sink = torch.zeros_like(w.sink_window()[0]).cuda()
+    win = torch.zeros_like(w.sink_window()[1]).cuda()
+    pos = w.tok_pos.numpy()
+    seq = w.tok_seq.numpy()
+    final = np.array(lens)
+    new = pos >= final[seq] - chunk
+    for part, seq_lens in ((~new, final - chunk), (new, final)):
+        idx = torch.as_tensor(np.nonzero(part)[0])
+        ok.oscar_append_mixed(w.dims, w.k[idx].cuda(), w.v[idx].cuda(), cache.R_k, cache.R_v, cache.clip_k,
+                              cache.clip_v, None, w.slot_mapping[idx].cuda(), w.tok_seq[idx].cuda(),
+                              w.tok_pos[idx].cuda(), torch.as_tensor(seq_lens, dtype=torch.int32).cuda(), S, W,
+                              cache.int2_pages, cache.scale_zero, sink, win)
+    torch.cuda.synchronize()
+    ref_sink, ref_win = w.sink_window()
+    assert torch.equal(sink.cpu(), ref_sink) and torch.equal(win.cpu(), ref_win)
+    cache.sink, cache.window = sink, win
+    rs = np.repeat(np.arange(len(lens), dtype=np.int32), chunk)
+    rp = np.concatenate([np.arange(L - chunk, L, dtype=np.int32) for L in lens])
+    g = torch.Generator().manual_seed(8)
+    q = torch.randn((len(rs), 8, 128), generator=g).to(torch.bfloat16).cuda()
+    out = cache.extend(q, torch.as_tensor(rs).cuda(), torch.as_tensor(rp).cuda())
+    torch.cuda.synchronize()
+    compare_decode(out, oracle_extend_on_gpu_cache(w, cache, q, rs, rp))
