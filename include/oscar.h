@@ -224,6 +224,33 @@ oscar_status_t oscar_extend(const oscar_dims_t* dims, int32_t batch, int32_t num
                             size_t workspace_bytes, void* stream);
 
 /*
+ * oscar_extend_varlen -- oscar_extend for the common layout of chunked prefill: the
+ * query rows of sequence b are rows q_start[b] .. q_start[b+1]-1 and sit at the
+ * last n_b = q_start[b+1] - q_start[b] positions of that sequence (the tokens just
+ * appended), in order.  Same result as oscar_extend with those rows.  For head_dim
+ * 128, group 64 or 128 and GQA 4 or 8, the INT2 part runs in tiles of 64 / GQA rows
+ * of one sequence: every page is fetched and its codes turned into tensor-core
+ * operands once per tile instead of once per row.
+ * Arguments (beyond oscar_extend's)
+ *   num_rows          q_start[batch]; q and out have num_rows rows
+ *   max_rows_per_seq  host bound on every n_b (sizes the grid)
+ *   q_start           device int32 [batch + 1], non-decreasing, q_start[0] = 0,
+ *                     q_start[batch] = num_rows; n_b <= seq_lens[b]
+ *   workspace         at least oscar_extend_varlen_workspace_bytes(...) bytes
+ * A row beyond a sequence's tokens (n_b > seq_lens[b]) attends nothing and sets
+ * OSCAR_DEVERR_POSITION.
+ */
+size_t oscar_extend_varlen_workspace_bytes(const oscar_dims_t* dims, int32_t num_rows, int32_t max_seq_len,
+                                           int32_t pages_per_split, int32_t sink_len, int32_t window_len);
+oscar_status_t oscar_extend_varlen(const oscar_dims_t* dims, int32_t batch, int32_t num_rows, int32_t max_seq_len,
+                                   int32_t max_rows_per_seq, int32_t pages_per_split, const void* q,
+                                   const int32_t* q_start, const float* R_k, const float* R_v,
+                                   const uint8_t* int2_pages, const void* scale_zero_pages, const void* bf16_sink,
+                                   const void* bf16_window, const int32_t* page_table, const int32_t* seq_lens,
+                                   int32_t sink_len, int32_t window_len, float sm_scale, float* out, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/*
  * oscar_decode_noalloc -- oscar_decode without a caller workspace.
  *
  * The OSCAR pages have no counterpart for this call; it is a convenience of this

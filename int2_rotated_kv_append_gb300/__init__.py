@@ -58,6 +58,9 @@ def _load():
         "oscar_decode_noalloc": (I32, [D, I32, I32, I32, P, P, P, P, P, P, P, P, P, I32, I32, F32, P, P]),
         "oscar_extend_workspace_bytes": (SZ, [D, I32, I32, I32, I32, I32]),
         "oscar_extend": (I32, [D, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, I32, I32, F32, P, P, SZ, P]),
+        "oscar_extend_varlen_workspace_bytes": (SZ, [D, I32, I32, I32, I32, I32]),
+        "oscar_extend_varlen": (I32, [D, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, I32, I32, F32, P, P, SZ,
+                                      P]),
         "oscar_bf16_append": (I32, [D, I64, P, P, P, P, P]),
         "oscar_bf16_decode_workspace_bytes": (SZ, [D, I32, I32, I32]),
         "oscar_bf16_decode": (I32, [D, I32, I32, I32, P, P, P, P, F32, P, P, SZ, P]),
@@ -178,6 +181,25 @@ def oscar_extend(dims, batch, max_seq_len, pages_per_split, q, row_seq, row_pos,
                             _ptr(page_table), _ptr(seq_lens), int(sink_len), int(window_len), float(sm_scale),
                             _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                             _stream(stream)), "oscar_extend")
+
+
+def oscar_extend_varlen_workspace_bytes(dims, num_rows, max_seq_len, pages_per_split, sink_len, window_len) -> int:
+    return int(lib.oscar_extend_varlen_workspace_bytes(ctypes.byref(_dims(dims)), int(num_rows), int(max_seq_len),
+                                                       int(pages_per_split), int(sink_len), int(window_len)))
+
+
+def oscar_extend_varlen(dims, batch, max_seq_len, max_rows_per_seq, pages_per_split, q, q_start, R_k, R_v, int2_pages,
+                        scale_zero_pages, bf16_sink, bf16_window, page_table, seq_lens, sink_len, window_len, sm_scale,
+                        out, workspace, stream=None):
+    """Causal attention of the rows q [rows][Hq][D]: rows q_start[b] .. q_start[b+1]-1 are
+    the last positions of sequence b; writes fp32 out [rows][Hq][D]."""
+    _check(lib.oscar_extend_varlen(ctypes.byref(_dims(dims)), int(batch), int(q.shape[0]), int(max_seq_len),
+                                   int(max_rows_per_seq), int(pages_per_split), _ptr(q), _ptr(q_start), _ptr(R_k),
+                                   _ptr(R_v), _ptr(int2_pages), _ptr(scale_zero_pages), _ptr(bf16_sink),
+                                   _ptr(bf16_window), _ptr(page_table), _ptr(seq_lens), int(sink_len),
+                                   int(window_len), float(sm_scale), _ptr(out), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "oscar_extend_varlen")
 
 
 OSCAR_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024

@@ -10,7 +10,8 @@ from __future__ import annotations
 import torch
 
 from . import (oscar_append, oscar_bf16_append, oscar_bf16_decode, oscar_bf16_decode_workspace_bytes, oscar_decode,
-               oscar_decode_workspace_bytes, oscar_extend, oscar_extend_workspace_bytes)
+               oscar_decode_workspace_bytes, oscar_extend, oscar_extend_varlen, oscar_extend_varlen_workspace_bytes,
+               oscar_extend_workspace_bytes)
 from .synth import Workload
 
 SENTINEL = 0xA5
@@ -86,6 +87,25 @@ class Int2Cache:
         oscar_extend(self.dims, w.batch, msl, self.pps, q, row_seq, row_pos, self.R_k, self.R_v, self.int2_pages,
                      self.scale_zero, self.sink, self.window, self.page_table, self.seq_lens, w.sink_len,
                      w.window_len, sm_scale, out, self._ws, stream)
+        return out
+
+
+    def extend_varlen(self, q, q_start, max_rows_per_seq, out=None, sm_scale=0.0, max_seq_len=None, stream=None):
+        """Causal attention of the rows q [rows][Hq][D], rows q_start[b] .. q_start[b+1]-1
+        being the last positions of sequence b (int32 device q_start [B+1])."""
+        w = self.w
+        msl = w.max_seq_len if max_seq_len is None else max_seq_len
+        rows = q.shape[0]
+        if out is None:
+            out = torch.empty((rows, w.num_q_heads, w.head_dim), dtype=torch.float32, device=self.device)
+        nbytes = oscar_extend_varlen_workspace_bytes(self.dims, rows, msl, self.pps, w.sink_len, w.window_len)
+        if nbytes == 0:
+            raise ValueError("invalid extend arguments for workspace sizing")
+        if self._ws is None or self._ws.numel() < nbytes:
+            self._ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        oscar_extend_varlen(self.dims, w.batch, msl, max_rows_per_seq, self.pps, q, q_start, self.R_k, self.R_v,
+                            self.int2_pages, self.scale_zero, self.sink, self.window, self.page_table, self.seq_lens,
+                            w.sink_len, w.window_len, sm_scale, out, self._ws, stream)
         return out
 
 

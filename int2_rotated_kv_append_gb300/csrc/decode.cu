@@ -233,6 +233,132 @@ extern "C" oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, 
                          window_len, sm_scale, out, workspace, workspace_bytes, stream);
 }
 
+namespace oscar_extend_rows {
+
+using namespace oscar;
+using namespace oscar_dec;
+
+// Rows of sequence b: q_start[b] .. q_start[b + 1) - 1, the last n_b = q_start[b + 1]
+// - q_start[b] positions of the sequence (the tokens just appended), in order.
+__global__ void extend_rows_kernel(const int32_t* q_start, const int32_t* seq_lens, int rows, int max_seq_len,
+                                   int32_t* row_seq, int32_t* row_pos) {
+  grid_dep_launch_dependents();
+  const int b = blockIdx.x;
+  const int q0 = q_start[b], q1 = q_start[b + 1];
+  int L = seq_lens[b];
+  if (L < 0 || L > max_seq_len) L = L < 0 ? 0 : max_seq_len;  // the attention kernels flag it
+  for (int j = threadIdx.x; q0 + j < q1; j += blockDim.x) {
+    const int r = q0 + j;
+    if (r < 0 || r >= rows) {
+      record_error(OSCAR_DEVERR_POSITION);
+      continue;
+    }
+    row_seq[r] = b;
+    row_pos[r] = L - (q1 - q0) + j;  // negative when the rows outnumber the tokens: flagged later
+  }
+}
+
+// Extend in tiles: the rows' (sequence, position), the BF16 sink/window splits per
+// row, the q-rotation, the INT2 splits in tiles of rows, the merge per row.
+template <int D>
+cudaError_t launch_extend_tiles(Params p, int batch, cudaStream_t stream) {
+  extend_rows_kernel<<<batch, 128, 0, stream>>>(p.q_start, p.seq_lens, p.B, p.max_seq_len,
+                                                const_cast<int32_t*>(p.row_seq), const_cast<int32_t*>(p.row_pos));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.n_dense > 0) {
+    Params pd = p;
+    pd.split_base = p.n_paged;
+    e = int2_mma_split(pd, stream);
+    if (e != cudaSuccess) return e;
+  }
+  const int chunks = (p.B + p.qrot_spc - 1) / p.qrot_spc;
+  e = launch_pdl(qrot_kernel<D>, dim3(chunks * p.H, D / 32), dim3(kQrotThreads), 0, stream, p);
+  if (e != cudaSuccess) return e;
+  if (p.n_paged > 0) {
+    e = int2_tile_split(p, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return ::merge<D, kMixed>(p, stream);
+}
+
+}  // namespace oscar_extend_rows
+
+extern "C" size_t oscar_extend_varlen_workspace_bytes(const oscar_dims_t* dims, int32_t num_rows,
+                                                      int32_t max_seq_len, int32_t pages_per_split,
+                                                      int32_t sink_len, int32_t window_len) {
+  const size_t base = oscar_decode_workspace_bytes(dims, num_rows, max_seq_len, pages_per_split, sink_len, window_len);
+  if (base == 0) return 0;
+  return base + 2 * align_up(static_cast<size_t>(num_rows) * 4, 256);
+}
+
+extern "C" oscar_status_t oscar_extend_varlen(const oscar_dims_t* dims, int32_t batch, int32_t num_rows,
+                                              int32_t max_seq_len, int32_t max_rows_per_seq, int32_t pages_per_split,
+                                              const void* q, const int32_t* q_start, const float* R_k,
+                                              const float* R_v, const uint8_t* int2_pages,
+                                              const void* scale_zero_pages, const void* bf16_sink,
+                                              const void* bf16_window, const int32_t* page_table,
+                                              const int32_t* seq_lens, int32_t sink_len, int32_t window_len,
+                                              float sm_scale, float* out, void* workspace, size_t workspace_bytes,
+                                              void* stream) {
+  oscar_status_t st = check_dims(dims);
+  if (st != OSCAR_OK) return st;
+  if (batch < 0 || num_rows < 0 || max_seq_len < 0 || max_rows_per_seq < 0 || pages_per_split < 0 || sink_len < 0 ||
+      window_len < 0)
+    return OSCAR_ERR_INVALID_ARG;
+  if (num_rows == 0) return OSCAR_OK;
+  if (batch == 0 || max_rows_per_seq == 0 || !q_start || !q || !R_k || !R_v || !int2_pages || !scale_zero_pages ||
+      !page_table || !seq_lens || !out || !workspace)
+    return OSCAR_ERR_INVALID_ARG;
+  if ((sink_len > 0 && !bf16_sink) || (window_len > 0 && !bf16_window)) return OSCAR_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return OSCAR_ERR_INVALID_ARG;
+  if (misaligned16(q) || misaligned16(R_k) || misaligned16(R_v) || misaligned16(int2_pages) ||
+      misaligned16(scale_zero_pages) || misaligned16(bf16_sink) || misaligned16(bf16_window))
+    return OSCAR_ERR_INVALID_ARG;
+  Plan plan;
+  if (!make_plan(dims, num_rows, max_seq_len, pages_per_split, sink_len, window_len, kMixed,
+                 split_ctas_per_sm(dims, kMixed), &plan))
+    return OSCAR_ERR_INVALID_ARG;
+  const size_t need = plan.total + 2 * align_up(static_cast<size_t>(num_rows) * 4, 256);
+  if (workspace_bytes < need) return OSCAR_ERR_WORKSPACE;
+  if (merge_smem(dims->head_dim, plan.ns, 1, 0, kMergeThreadsSmall) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_rows) * dims->num_q_heads > 0x7fffffffLL) return OSCAR_ERR_UNSUPPORTED;
+  Params p = base_params(dims, num_rows, max_seq_len, plan, kMixed, sm_scale, workspace);
+  p.S = sink_len;
+  p.W = window_len;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.R_k = R_k;
+  p.R_v = R_v;
+  p.codes = int2_pages;
+  p.sz = static_cast<const __half*>(scale_zero_pages);
+  p.sink = static_cast<const __nv_bfloat16*>(bf16_sink);
+  p.win = static_cast<const __nv_bfloat16*>(bf16_window);
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.num_seqs = batch;
+  p.q_start = q_start;
+  char* w = static_cast<char*>(workspace);
+  p.row_seq = reinterpret_cast<const int32_t*>(w + plan.total);
+  p.row_pos = reinterpret_cast<const int32_t*>(w + plan.total + align_up(static_cast<size_t>(num_rows) * 4, 256));
+  if (!int2_mma_supported(p)) p.qfrag = nullptr;
+  const bool tiles = p.qfrag != nullptr && int2_tile_supported(p);
+  if (tiles) {
+    const int rpt = 64 / p.gqa;
+    const long long t = (static_cast<long long>(max_rows_per_seq) + rpt - 1) / rpt;
+    if (t * batch > 65535) return OSCAR_ERR_UNSUPPORTED;
+    p.tiles = static_cast<int>(t);
+    const cudaError_t e = oscar_extend_rows::launch_extend_tiles<128>(p, batch, as_stream(stream));
+    return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+  }
+  // other shapes: one decode row per query row
+  oscar_extend_rows::extend_rows_kernel<<<batch, 128, 0, as_stream(stream)>>>(q_start, seq_lens, num_rows, max_seq_len,
+                                                           const_cast<int32_t*>(p.row_seq),
+                                                           const_cast<int32_t*>(p.row_pos));
+  if (cudaGetLastError() != cudaSuccess) return OSCAR_ERR_CUDA;
+  return run(p, kMixed, stream);
+}
+
 extern "C" size_t oscar_extend_workspace_bytes(const oscar_dims_t* dims, int32_t num_rows, int32_t max_seq_len,
                                                int32_t pages_per_split, int32_t sink_len, int32_t window_len) {
   return oscar_decode_workspace_bytes(dims, num_rows, max_seq_len, pages_per_split, sink_len, window_len);

@@ -62,6 +62,11 @@ struct Params {
   const int32_t* row_seq;
   const int32_t* row_pos;
   int num_seqs;
+  int split_base;             // first split index of the launch (the grid's x covers splits split_base ..)
+  // Extend in tiles (int2_tile_split): the rows of sequence b are q_start[b] .. q_start[b + 1) - 1,
+  // in tiles of 64 / gqa rows, `tiles` per sequence.
+  const int32_t* q_start;
+  int tiles;
   float* out;
   float* q_rot;
   uint32_t* qfrag;  // kQfragBytes per (sequence, KV head); null when not needed
@@ -75,6 +80,9 @@ bool int2_mma_supported(const Params& p);
 int int2_mma_ctas_per_sm(int gqa, int G);  // resident CTAs per SM of the INT2 kernel
 int bf16_mma_ctas_per_sm(int gqa);         // resident CTAs per SM of the BF16 kernel
 cudaError_t int2_mma_split(const Params& p, cudaStream_t stream);
+// Extend in tiles of query rows (decode_int2_mma.cu): the INT2 splits only.
+bool int2_tile_supported(const Params& p);
+cudaError_t int2_tile_split(const Params& p, cudaStream_t stream);
 bool bf16_mma_supported(const Params& p);
 cudaError_t bf16_mma_split(const Params& p, cudaStream_t stream);
 
@@ -588,7 +596,7 @@ __device__ __forceinline__ void split_body(const Params& p, int s, int h, int b,
 template <int D, Mode MODE>
 __global__ void __launch_bounds__(kThreads) split_kernel(Params p) {
   extern __shared__ __align__(16) float dyn_smem[];
-  split_body<D, MODE>(p, blockIdx.x, blockIdx.y, blockIdx.z, dyn_smem);
+  split_body<D, MODE>(p, blockIdx.x + p.split_base, blockIdx.y, blockIdx.z, dyn_smem);
 }
 
 // Log-sum-exp merge of the split partials and, in INT2 mode, the single

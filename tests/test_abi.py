@@ -115,6 +115,21 @@ def test_extend_validation(lib):
     assert ext(ws_bytes=need - 1) == ok.OSCAR_ERR_WORKSPACE
 
 
+def test_extend_varlen_validation(lib):
+    d = _dims()
+    def ext(batch=2, rows=3, mr=2, qs=P, ws_bytes=1 << 30):
+        return lib.oscar_extend_varlen(ctypes.byref(d), batch, rows, 100, mr, 8, P, qs, P, P, P, P, P, P, P, P, 4, 8,
+                                       0.0, P, ctypes.c_void_p(256), ws_bytes, None)
+    assert ext(rows=0) == ok.OSCAR_OK
+    assert ext(qs=None) == ok.OSCAR_ERR_INVALID_ARG
+    assert ext(batch=0) == ok.OSCAR_ERR_INVALID_ARG
+    assert ext(mr=0) == ok.OSCAR_ERR_INVALID_ARG
+    assert ext(rows=-1) == ok.OSCAR_ERR_INVALID_ARG
+    need = lib.oscar_extend_varlen_workspace_bytes(ctypes.byref(d), 3, 100, 8, 4, 8)
+    assert need > lib.oscar_decode_workspace_bytes(ctypes.byref(d), 3, 100, 8, 4, 8) > 0
+    assert ext(ws_bytes=need - 1) == ok.OSCAR_ERR_WORKSPACE
+
+
 def _decode(lib, dims, batch=2, msl=100, pps=8, S=4, W=8, ws_bytes=1 << 30, ws=ctypes.c_void_p(256), sink=P):
     return lib.oscar_decode(ctypes.byref(dims), batch, msl, pps, P, P, P, P, P, sink, P, P, P, S, W, 0.0, P, ws,
                             ws_bytes, None)

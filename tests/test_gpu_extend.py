@@ -116,3 +116,40 @@ def test_chunked_prefill_flow_append_mixed_then_extend():
     out = cache.extend(q, torch.as_tensor(rs).cuda(), torch.as_tensor(rp).cuda())
     torch.cuda.synchronize()
     compare_decode(out, oracle_extend_on_gpu_cache(w, cache, q, rs, rp))
+
+
+@pytest.mark.parametrize("D,G,Hq,H,lens,S,W,chunks", [
+    (128, 64, 8, 2, [300, 700, 40, 1200], 16, 48, [5, 17, 0, 40]),   # tiles of 16 rows (GQA 4), ragged, empty
+    (128, 128, 16, 2, [500, 90], 8, 24, [9, 1]),                    # tiles of 8 rows (GQA 8)
+    (128, 64, 4, 2, [260, 33], 0, 0, [3, 33]),                       # no sink, no window; a whole sequence as rows
+    (64, 32, 4, 2, [90, 400], 4, 16, [9, 2]),                        # other shapes: one decode row per query row
+])
+def test_extend_varlen_matches_oracle(D, G, Hq, H, lens, S, W, chunks):
+    w = synth.make_workload(num_q_heads=Hq, num_kv_heads=H, head_dim=D, group_size=G, sink_len=S, window_len=W,
+                            seq_lens=lens, seed=sum(chunks) + D + Hq)
+    cache = Int2Cache(w)
+    cache.prefill()
+    q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    rs = np.repeat(np.arange(len(lens), dtype=np.int32), chunks)
+    rp = np.concatenate([np.arange(L - n, L, dtype=np.int32) for L, n in zip(lens, chunks)])
+    g = torch.Generator().manual_seed(9)
+    q = torch.randn((len(rs), Hq, D), generator=g).to(torch.bfloat16).cuda()
+    out = cache.extend_varlen(q, torch.as_tensor(q_start).cuda(), max(chunks))
+    torch.cuda.synchronize()
+    assert ok.oscar_device_errors(reset=True) == 0
+    compare_decode(out, oracle_extend_on_gpu_cache(w, cache, q, rs, rp))
+
+
+def test_extend_varlen_rows_beyond_the_tokens_are_flagged():
+    w = synth.make_workload(num_q_heads=8, num_kv_heads=2, head_dim=128, group_size=64, sink_len=4, window_len=8,
+                            seq_lens=[5, 60], seed=12)
+    cache = Int2Cache(w)
+    cache.prefill()
+    ok.oscar_device_errors(reset=True)
+    q = torch.randn((9, 8, 128)).to(torch.bfloat16).cuda()
+    q_start = torch.tensor([0, 7, 9], dtype=torch.int32).cuda()  # 7 rows for a 5-token sequence
+    out = cache.extend_varlen(q, q_start, 7)
+    torch.cuda.synchronize()
+    assert ok.oscar_device_errors(reset=True) & ok.OSCAR_DEVERR_POSITION
+    assert torch.all(out[:2] == 0)            # positions -2 and -1: nothing attended
+    assert torch.all(torch.isfinite(out))
