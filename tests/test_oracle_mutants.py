@@ -6,16 +6,19 @@ It is compiled into a temporary library and every pin is run against it; at
 least one pin must fail, otherwise the pins would not notice that mistake.
 """
 
+import importlib.util
 import os
 import subprocess
 import tempfile
 
 import pytest
 
+import calib_pins
 import oracle_pins
 from oracle import oracle as O
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "oscar_oracle.cpp")
+CALIB_SRC = os.path.join(os.path.dirname(SRC), "calibration.py")
 
 # (name, text in the oracle, replacement, expected number of occurrences)
 MUTANTS = [
@@ -80,6 +83,47 @@ def test_mutant_is_caught(name, old, new, count, workdir):
         try:
             pin(lib)
         except (AssertionError, ValueError):
+            caught.append(pin.__name__)
+            break
+    assert caught, f"no pin catches the planted mistake '{name}'"
+
+
+# Planted mistakes in the calibration oracle (numpy source); same rule: some pin must fail.
+CALIB_MUTANTS = [
+    ("mean_not_subtracted", "            xh = xh - mu\n", "            xh = xh\n", 1),
+    ("divides_by_n_minus_1", "C[h] = (xh.T @ xh) / N", "C[h] = (xh.T @ xh) / (N - 1)", 1),
+    ("heads_mixed", "xh = x[:, h, :]", "xh = x[:, 0, :]", 1),
+    ("ascending_eigenvalues", 'order = np.argsort(-w, kind="stable")', 'order = np.argsort(w, kind="stable")', 1),
+    ("eigenvectors_reordered_by_row", "w, V = w[order], V[:, order]", "w, V = w[order], V[order, :]", 1),
+    ("rotation_rows_not_columns", "R[h] = V\n", "R[h] = V.T\n", 1),
+    ("sign_rule_negative", "if col[i_big] < 0:", "if col[i_big] > 0:", 1),
+    ("sign_rule_last_index", "i_big = int(np.argmax(np.abs(col)))",
+     "i_big = int(len(col) - 1 - np.argmax(np.abs(col[::-1])))", 1),
+    ("quantile_floor", "k = int(math.ceil(float(q) * float(N)))", "k = int(math.floor(float(q) * float(N)))", 1),
+    ("quantile_one_rank_high", "clip[h] = np.sort(y, axis=0)[k - 1]", "clip[h] = np.sort(y, axis=0)[min(k, N - 1)]", 1),
+    ("clip_without_magnitude", "y = np.abs(x[:, h, :] @ np.asarray(R[h], dtype=np.float64))",
+     "y = (x[:, h, :] @ np.asarray(R[h], dtype=np.float64))", 1),
+    ("clip_of_unrotated_samples", "y = np.abs(x[:, h, :] @ np.asarray(R[h], dtype=np.float64))",
+     "y = np.abs(x[:, h, :])", 1),
+]
+
+
+@pytest.mark.parametrize("name,old,new,count", CALIB_MUTANTS, ids=[m[0] for m in CALIB_MUTANTS])
+def test_calibration_mutant_is_caught(name, old, new, count, workdir):
+    with open(CALIB_SRC) as f:
+        src = f.read()
+    assert src.count(old) == count, f"mutation site for {name} not found {count} time(s)"
+    path = os.path.join(workdir, f"calib_{name}.py")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    spec = importlib.util.spec_from_file_location(f"calib_{name}", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    caught = []
+    for pin in calib_pins.ALL_PINS:
+        try:
+            pin(mod)
+        except (AssertionError, ValueError, IndexError):
             caught.append(pin.__name__)
             break
     assert caught, f"no pin catches the planted mistake '{name}'"
