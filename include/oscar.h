@@ -304,6 +304,67 @@ oscar_status_t oscar_bf16_decode(const oscar_dims_t* dims, int32_t batch, int32_
                                  const int32_t* page_table, const int32_t* seq_lens, float sm_scale, float* out,
                                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * oscar_calibrate -- the offline calibration that produces R and the clipping
+ * thresholds consumed by oscar_append, computed on the GPU from calibration
+ * samples of the keys and/or values (summary "How OSCAR Works": an offline
+ * analysis of the KV covariance designs the rotations, fixed clipping thresholds
+ * follow; project card "How it works": covariance structures of keys and values
+ * from a small calibration set give the orthogonal rotations and thresholds;
+ * abstract).  The pages give no formulas; the readings, per KV head h:
+ *   C_h    = (1/N) sum_t (x_t - mu)(x_t - mu)^T, mu = (1/N) sum_t x_t
+ *            (centered = 1), or the second moment (1/N) sum_t x_t x_t^T
+ *            (centered = 0); the "attention-aware" weighting is not defined on the
+ *            pages and is not applied;
+ *   R_h    = orthonormal eigenvectors of C_h as columns, eigenvalues descending
+ *            (ties by index), each column signed so that its entry of largest
+ *            magnitude (lowest row on a tie) is positive; x_rot = x . R_h;
+ *   clip_h[j] = the k-th smallest |x_t . R_h[:, j]| over the N samples, with
+ *            k = ceil(q N) evaluated in double and kept within [1, N].
+ * Arithmetic: the sums of x x^T and x are taken on the tensor cores from the bf16
+ * samples with fp32 accumulation (products exact), partial sums per chunk of
+ * samples are added in a fixed order and centred in fp64; the eigenvectors come
+ * from cyclic Jacobi in fp32 (a pair is left alone once |a_pq| <= 2^-21
+ * sqrt(|a_pp a_qq|); at most 40 sweeps); |x . R| is formed on the tensor cores
+ * with R split into three bf16 terms (about 24 bits) and fp32 accumulation, and the
+ * k-th smallest of those fp32 values is selected exactly.  The centred covariance
+ * loses relative accuracy in proportion to |mu|^2 / variance (fp32 sums).  Where
+ * eigenvalues coincide (or nearly, relative to fp32 rounding) the basis of their
+ * eigenspace is not unique and the columns there may differ from another solver's.
+ * Arguments
+ *   num_samples   N, 1 .. 2^31 - 257
+ *   k, v          device bf16 [N][Hkv][D] (the layout oscar_append takes), 16-byte
+ *                 aligned; either may be NULL (then its out_* must be NULL too)
+ *   centered      1: covariance about the sample mean; 0: second moment
+ *   clip_quantile q in (0, 1]; 1 gives the largest magnitude seen
+ *   out_k, out_v  outputs for the keys / values (fields below; device buffers):
+ *                   R            fp32 [Hkv][D][D] row-major, 16-byte aligned
+ *                   clip         fp32 [Hkv][D]
+ *                   eigenvalues  fp32 [Hkv][D], descending (may be NULL)
+ *                   cov          fp32 [Hkv][D][D], C_h as used (may be NULL)
+ *                   sweeps       int32 [Hkv], Jacobi sweeps taken (may be NULL)
+ *   workspace     at least oscar_calibrate_workspace_bytes(dims, N) bytes, 16-byte
+ *                 aligned; holds per-chunk partial sums and |x . R| for every sample
+ *                 (about 4 N Hkv D bytes per side)
+ * Only head_dim, num_kv_heads and the general shape checks of dims matter here.
+ * Invalid arguments (null R or clip, q outside (0, 1], centered not 0/1, N out of
+ * range, k and out_k not both given or both NULL, nothing to calibrate, misaligned
+ * pointers) return OSCAR_ERR_INVALID_ARG; a short workspace OSCAR_ERR_WORKSPACE.
+ */
+typedef struct {
+  float* R;
+  float* clip;
+  float* eigenvalues;
+  float* cov;
+  int32_t* sweeps;
+} oscar_calib_out_t;
+
+size_t oscar_calibrate_workspace_bytes(const oscar_dims_t* dims, int64_t num_samples);
+oscar_status_t oscar_calibrate(const oscar_dims_t* dims, int64_t num_samples, const void* k, const void* v,
+                               int32_t centered, double clip_quantile, const oscar_calib_out_t* out_k,
+                               const oscar_calib_out_t* out_v, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* oscar_status_string(oscar_status_t status);
 

@@ -43,6 +43,10 @@ class oscar_dims_t(ctypes.Structure):
         "max_pages_per_seq")]
 
 
+class oscar_calib_out_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("R", "clip", "eigenvalues", "cov", "sweeps")]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"OSCAR CUDA library not built ({LIB_PATH} missing); run "
@@ -64,6 +68,9 @@ def _load():
         "oscar_bf16_append": (I32, [D, I64, P, P, P, P, P]),
         "oscar_bf16_decode_workspace_bytes": (SZ, [D, I32, I32, I32]),
         "oscar_bf16_decode": (I32, [D, I32, I32, I32, P, P, P, P, F32, P, P, SZ, P]),
+        "oscar_calibrate_workspace_bytes": (SZ, [D, I64]),
+        "oscar_calibrate": (I32, [D, I64, P, P, I32, ctypes.c_double, ctypes.POINTER(oscar_calib_out_t),
+                                  ctypes.POINTER(oscar_calib_out_t), P, SZ, P]),
         "oscar_status_string": (ctypes.c_char_p, [I32]),
         "oscar_device_errors": (I32, [ctypes.POINTER(ctypes.c_uint32), I32]),
     }
@@ -234,6 +241,25 @@ def oscar_bf16_decode(dims, batch, max_seq_len, pages_per_split, q, bf16_pages, 
                                  _ptr(q), _ptr(bf16_pages), _ptr(page_table), _ptr(seq_lens), float(sm_scale),
                                  _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream(stream)), "oscar_bf16_decode")
+
+
+def oscar_calibrate_workspace_bytes(dims, num_samples) -> int:
+    return int(lib.oscar_calibrate_workspace_bytes(ctypes.byref(_dims(dims)), int(num_samples)))
+
+
+def _calib_out(o):
+    if o is None:
+        return None
+    return ctypes.byref(oscar_calib_out_t(*(_ptr(o.get(n)) for n in ("R", "clip", "eigenvalues", "cov", "sweeps"))))
+
+
+def oscar_calibrate(dims, num_samples, k, v, centered, clip_quantile, out_k, out_v, workspace, stream=None):
+    """Covariance, spectral rotation and quantile clipping thresholds per KV head from
+    bf16 samples [N][Hkv][D]; ``out_k`` / ``out_v``: dicts of output tensors (keys R,
+    clip and optionally eigenvalues, cov, sweeps) or None with ``k`` / ``v`` None."""
+    _check(lib.oscar_calibrate(ctypes.byref(_dims(dims)), int(num_samples), _ptr(k), _ptr(v), int(centered),
+                               float(clip_quantile), _calib_out(out_k), _calib_out(out_v), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream)), "oscar_calibrate")
 
 
 def oscar_device_errors(reset: bool = False) -> int:

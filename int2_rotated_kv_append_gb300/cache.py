@@ -2,16 +2,17 @@
 
 ``Int2Cache`` owns the INT2 code pool, the fp16 scale/zero pool and the BF16
 sink/window buffers of a workload; ``Bf16Cache`` owns the all-BF16 pool of the
-speedup reference.  Both only allocate torch memory and call the library.
+speedup reference.  Both only allocate torch memory and call the library, as does
+``calibrate`` (the offline step that produces R and the clipping thresholds).
 """
 
 from __future__ import annotations
 
 import torch
 
-from . import (oscar_append, oscar_bf16_append, oscar_bf16_decode, oscar_bf16_decode_workspace_bytes, oscar_decode,
-               oscar_decode_workspace_bytes, oscar_extend, oscar_extend_varlen, oscar_extend_varlen_workspace_bytes,
-               oscar_extend_workspace_bytes)
+from . import (make_dims, oscar_append, oscar_bf16_append, oscar_bf16_decode, oscar_bf16_decode_workspace_bytes,
+               oscar_calibrate, oscar_calibrate_workspace_bytes, oscar_decode, oscar_decode_workspace_bytes,
+               oscar_extend, oscar_extend_varlen, oscar_extend_varlen_workspace_bytes, oscar_extend_workspace_bytes)
 from .synth import Workload
 
 SENTINEL = 0xA5
@@ -140,3 +141,38 @@ class Bf16Cache:
         oscar_bf16_decode(self.dims, w.batch, w.max_seq_len, self.pps, q, self.pages, self.page_table,
                           self.seq_lens, sm_scale, out, self.workspace(), stream)
         return out
+
+
+def calibrate(k=None, v=None, centered: bool = True, clip_quantile: float = 1.0, with_cov: bool = False,
+              workspace=None, stream=None) -> dict:
+    """R, clipping thresholds and eigenvalues per KV head from calibration samples
+    (device bf16 [N][Hkv][D]); returns {"k": {...}, "v": {...}} for the sides given,
+    each with R [Hkv][D][D], clip [Hkv][D], eigenvalues [Hkv][D], sweeps [Hkv] and,
+    with ``with_cov``, cov [Hkv][D][D]."""
+    x = k if k is not None else v
+    if x is None:
+        raise ValueError("calibrate needs k or v samples")
+    N, H, D = x.shape
+    dims = make_dims(H, H, D, 16, D, 1, 1)
+    dev = x.device
+
+    def outputs():
+        o = {"R": torch.empty(H, D, D, dtype=torch.float32, device=dev),
+             "clip": torch.empty(H, D, dtype=torch.float32, device=dev),
+             "eigenvalues": torch.empty(H, D, dtype=torch.float32, device=dev),
+             "sweeps": torch.empty(H, dtype=torch.int32, device=dev)}
+        if with_cov:
+            o["cov"] = torch.empty(H, D, D, dtype=torch.float32, device=dev)
+        return o
+
+    out_k = outputs() if k is not None else None
+    out_v = outputs() if v is not None else None
+    if workspace is None:
+        workspace = torch.empty(oscar_calibrate_workspace_bytes(dims, N), dtype=torch.uint8, device=dev)
+    oscar_calibrate(dims, N, k, v, int(centered), clip_quantile, out_k, out_v, workspace, stream)
+    res = {}
+    if out_k is not None:
+        res["k"] = out_k
+    if out_v is not None:
+        res["v"] = out_v
+    return res

@@ -554,25 +554,8 @@ __global__ void __launch_bounds__(kUmThreads, 1) append_umma_kernel(
   }
 }
 
-// cuTensorMapEncodeTiled, taken from the CUDA driver API through the runtime (no link
-// against libcuda).
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
+using umma::encode_tiled;
+using umma::EncodeTiledFn;
 
 // Map of x [T][H][128] bf16 as (channel, head, token) with a 64 x 1 x 128 box:
 // one K block (64 channels) of 128 tokens of one head, 128-byte swizzled.

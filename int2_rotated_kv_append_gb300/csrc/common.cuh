@@ -94,3 +94,4 @@ oscar_status_t oscar_internal_append_errors(uint32_t* flags, int reset);
 oscar_status_t oscar_internal_decode_errors(uint32_t* flags, int reset);
 oscar_status_t oscar_internal_decode_mma_errors(uint32_t* flags, int reset);
 oscar_status_t oscar_internal_decode_bf16_errors(uint32_t* flags, int reset);
+oscar_status_t oscar_internal_calib_errors(uint32_t* flags, int reset);

@@ -5,7 +5,10 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <mutex>
 
 namespace oscar {
 namespace umma {
@@ -37,6 +40,18 @@ __host__ __device__ constexpr uint32_t sw128_offset(int row, int k, int rows) {
                                (k & 7) * 2);
 }
 
+// MN-major operand with the 128-byte swizzle: a 128-byte row holds 64 consecutive
+// M/N elements of one K index, 8 consecutive K rows form a 1024-byte atom (16-byte
+// chunk c of row r at chunk c ^ r), the next 8 K indices follow 1024 bytes later
+// (stride byte offset) and the next 64 M/N elements `mn_block_bytes` later
+// (leading byte offset).  A TMA box of 64 elements x rows with the 128-byte swizzle
+// lands in exactly this layout when its rows are read as K.
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t smem_addr, uint32_t mn_block_bytes) {
+  return static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(mn_block_bytes >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
 // K-major, dense, M x N.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
@@ -44,6 +59,11 @@ __host__ __device__ constexpr uint32_t sw128_offset(int row, int k, int rows) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The same with both A and B MN-major (bits 15 and 16 set).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int M, int N) {
+  return idesc_bf16_f32(M, N) | (1u << 15) | (1u << 16);
 }
 
 // ---- TMEM ------------------------------------------------------------------------
@@ -156,6 +176,28 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- host: tensor-map encoding ---------------------------------------------------------
+
+// cuTensorMapEncodeTiled, taken from the CUDA driver API through the runtime (no link
+// against libcuda); null if the driver does not provide it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
 }
 
 }  // namespace umma

@@ -262,6 +262,30 @@ def decode_append_batch(w: Workload, n_tokens: int = 256, seed: int = 4, device=
     return k, v, slots
 
 
+def calibration_samples(N: int, H: int, D: int, seed: int, kind: str = "spectrum", device="cpu") -> torch.Tensor:
+    """Calibration vectors bf16 [N][H][D] for the offline calibration.
+    kind 'spectrum': per head a planted covariance Q diag(lam) Q^T with Q Haar and
+      lam geometric from 100 down to 0.1 (distinct, well separated eigenvalues),
+      plus channel means ~N(0, 2^2): x = (z sqrt(lam)) Q^T + mu, z ~ N(0, 1);
+    kind 'qwen': the K distribution of the workloads (channel means, outlier channels);
+    kind 'normal': N(0, 1) (the V distribution; an isotropic covariance)."""
+    gen_cpu = torch.Generator(device="cpu").manual_seed(seed)
+    gen_dev = torch.Generator(device=device).manual_seed(seed + 2_000_029)
+    if kind == "qwen":
+        return _draw_k(N, H, D, gen_cpu, gen_dev, device, "qwen")
+    if kind == "normal":
+        return _normal_bf16((N, H, D), gen_dev, device)
+    if kind != "spectrum":
+        raise ValueError(kind)
+    Q = haar_orthogonal(H, D, gen_cpu)
+    lam = torch.logspace(2.0, -1.0, D, dtype=torch.float64)
+    mu = 2.0 * torch.randn((H, D), dtype=torch.float64, generator=gen_cpu)
+    A = (lam.sqrt().view(1, D, 1) * Q.transpose(-1, -2)).to(torch.float32).to(device)  # [H][D][D]: row j = sqrt(lam_j) q_j
+    z = torch.randn((H, N, D), dtype=torch.float32, generator=gen_dev, device=device)
+    x = torch.bmm(z, A) + mu.to(torch.float32).to(device).unsqueeze(1)
+    return x.transpose(0, 1).contiguous().to(torch.bfloat16)
+
+
 def bits16(t: torch.Tensor) -> np.ndarray:
     """uint16 bit patterns of a bf16/fp16 tensor as a numpy array (host copy)."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)

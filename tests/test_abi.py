@@ -162,3 +162,37 @@ def test_workspace_sizes(lib):
 def test_status_strings(lib):
     for s in range(5):
         assert ok.status_string(s).startswith("OSCAR")
+
+
+def test_calibrate_validation(lib):
+    d = _dims()
+    out = ok.oscar_calib_out_t(P, P, None, None, None)
+    bad_R = ok.oscar_calib_out_t(ctypes.c_void_p(24), P, None, None, None)
+    no_clip = ok.oscar_calib_out_t(P, None, None, None, None)
+    need = lib.oscar_calibrate_workspace_bytes(ctypes.byref(d), 1000)
+    assert need > 0
+    assert lib.oscar_calibrate_workspace_bytes(ctypes.byref(d), 0) == 0
+    assert lib.oscar_calibrate_workspace_bytes(ctypes.byref(d), 2000) > need
+
+    def cal(N=1000, k=P, v=P, centered=1, q=0.99, ok_=ctypes.byref(out), ov=ctypes.byref(out),
+            ws=ctypes.c_void_p(256), ws_bytes=1 << 40, dims=d):
+        return lib.oscar_calibrate(ctypes.byref(dims), N, k, v, centered, q, ok_, ov, ws, ws_bytes, None)
+
+    E = ok.OSCAR_ERR_INVALID_ARG
+    assert cal(N=0) == E
+    assert cal(N=-5) == E
+    assert cal(N=1 << 31) == E
+    assert cal(k=None) == E                       # k missing but out_k given
+    assert cal(ov=None) == E                      # v given but out_v missing
+    assert cal(k=None, v=None, ok_=None, ov=None) == E  # nothing to calibrate
+    assert cal(q=0.0) == E
+    assert cal(q=1.5) == E
+    assert cal(q=float("nan")) == E
+    assert cal(centered=2) == E
+    assert cal(ok_=ctypes.byref(bad_R)) == E      # misaligned R
+    assert cal(ov=ctypes.byref(no_clip)) == E
+    assert cal(k=ctypes.c_void_p(40)) == E        # misaligned samples
+    assert cal(ws=None) == E
+    assert cal(ws=ctypes.c_void_p(264)) == E      # misaligned workspace
+    assert cal(dims=_dims(head_dim=96, group_size=32)) == ok.OSCAR_ERR_UNSUPPORTED
+    assert cal(ws_bytes=need - 1) == ok.OSCAR_ERR_WORKSPACE
