@@ -492,10 +492,14 @@ def run_ours(args, world, rank, local):
     log(f"e2e: {e2e_ms * 1e3:.2f} us/step")
     append_line = append_workload(dev) if rank == 0 and not args.no_append else None
     extend_line = extend_workload(dev) if rank == 0 and not args.no_extend else None
+    calib_line = calibrate_workload(dev) if rank == 0 and not args.no_calibrate else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         log("cpu baseline (oracle)")
         cpu = cpu_baseline(w, cache, B, step_bytes)
+        if calib_line is not None:
+            calib_line["cpu_oracle"] = cpu_calibration_baseline()
+            calib_line["gpu_vs_cpu_oracle"] = calib_line["cpu_oracle"]["us_per_matrix"] * 16 / calib_line["us"]
 
     if rank == 0:
         line = {
@@ -521,6 +525,7 @@ def run_ours(args, world, rank, local):
             "gpu_launches": K * 4,
             "append_workload": append_line,
             "extend_workload": extend_line,
+            "calibrate_workload": calib_line,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -581,6 +586,57 @@ def extend_workload(dev):
                     "sequence; the BF16 sink/window once per row"}
 
 
+def calibrate_workload(dev):
+    """The offline calibration workload: 16384 calibration vectors x 8 KV heads of
+    head_dim 128 for keys (the workloads' K distribution) and values (N(0, 1)); one
+    oscar_calibrate call (covariance, Jacobi eigenvectors, |x.R|, 0.999 quantile) per
+    run, L2 flushed between runs.  Its bytes: the samples read twice (moments and
+    rotation), |x.R| written and read once (fp32)."""
+    import torch
+
+    import int2_rotated_kv_append_gb300 as ok
+    from int2_rotated_kv_append_gb300 import synth
+
+    N, H, D = 16384, 8, 128
+    k = synth.calibration_samples(N, H, D, 4, "qwen", device=dev)
+    v = synth.calibration_samples(N, H, D, 5, "normal", device=dev)
+    dims = ok.make_dims(H, H, D, 16, D, 1, 1)
+    ws = torch.empty(ok.oscar_calibrate_workspace_bytes(dims, N), dtype=torch.uint8, device=dev)
+
+    def outputs():
+        return {"R": torch.empty(H, D, D, device=dev), "clip": torch.empty(H, D, device=dev),
+                "eigenvalues": torch.empty(H, D, device=dev), "sweeps": torch.empty(H, dtype=torch.int32, device=dev)}
+
+    out_k, out_v = outputs(), outputs()
+
+    def run():
+        ok.oscar_calibrate(dims, N, k, v, 1, 0.999, out_k, out_v, ws)
+
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(10):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    ts.sort()
+    us = ts[len(ts) // 2]
+    nbytes = 2 * (2 * N * H * D * 2) + 2 * (2 * N * H * D * 4)
+    sweeps = out_k["sweeps"].tolist() + out_v["sweeps"].tolist()
+    return {"workload": f"calibration: {N} samples x {H} KV heads x D {D}, keys and values, centred covariance, "
+                        "clip at the 0.999 quantile; L2 flushed between runs",
+            "us": us, "matrices_per_s": 2 * H / (us * 1e-6), "samples_per_s": N / (us * 1e-6),
+            "GBps_samples_and_rotated": nbytes / (us * 1e-6) / 1e9, "jacobi_sweeps": sweeps,
+            "note": "one oscar_calibrate call (5 kernels) per run; the Jacobi eigensolver (about 9 sweeps x "
+                    "127 rounds, 2 barriers each, 8 CTAs per matrix) takes most of it"}
+
+
 def append_workload(dev):
     """The append throughput workload: a prefill append of 16384 tokens x 8 KV
     heads (K and V) into the paged INT2 cache, and a decode append of 256 tokens
@@ -633,7 +689,7 @@ def append_workload(dev):
             "prefill_roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
                                  "frac": achieved / bf16_peak, "peak_source": bf16_src + " bf16_tflops (burst)",
                                  "executed_tflops": 3 * achieved,
-                                 "note": "mma.sync bf16 with R as three bf16 terms: 3x the algorithmic flops"},
+                                 "note": "tcgen05 bf16 MMAs with R as three bf16 terms: 3x the algorithmic flops"},
             "decode_append_256_us": dec_us,
             "note": "inputs resident in L2 between iterations (prefill reads 67 MB; tensor and shared-memory bound)"}
 
@@ -682,6 +738,28 @@ def cpu_baseline(w, cache, B, step_bytes):
             "s_per_step": el / n}
 
 
+def cpu_calibration_baseline():
+    """The calibration oracle, as it stands (fp64 numpy), on one matrix of the
+    calibration workload (16384 key samples of one KV head, D 128), repeated up to ~5 s."""
+    import numpy as np
+
+    from int2_rotated_kv_append_gb300 import synth
+    from int2_rotated_kv_append_gb300.synth import bits16
+    from oracle import calibration as CAL
+
+    x = bits16(synth.calibration_samples(16384, 8, 128, 4, "qwen", device="cpu"))[:, :1, :]
+    x = np.ascontiguousarray(x)
+    n, t = 0, time.perf_counter()
+    while True:
+        CAL.calibrate(x, centered=True, q=0.999)
+        n += 1
+        el = time.perf_counter() - t
+        if el > 5.0 or n >= 20:
+            break
+    return {"us_per_matrix": el / n * 1e6, "kind": "oracle", "cores": os.cpu_count(),
+            "sample": f"{n} run(s) of one matrix (16384 samples x D 128), numpy fp64 (BLAS threads as installed)"}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -695,6 +773,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-append", action="store_true", help="skip the append throughput workload")
     ap.add_argument("--no-extend", action="store_true", help="skip the extend (chunked prefill) workload")
+    ap.add_argument("--no-calibrate", action="store_true", help="skip the offline calibration workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -15,8 +15,9 @@
 //   calib_moments_kernel  sum_t x_t x_t^T and sum_t x_t per chunk of samples on the
 //                         tensor cores (the sample tile is the MN-major operand on
 //                         both sides; a constant column of ones yields the sums);
-//   calib_eig_kernel      one CTA per matrix: chunk partials summed, centred,
-//                         cyclic Jacobi in shared memory, ordering and signs;
+//   calib_eig_kernel      chunk partials summed and centred, cyclic Jacobi in shared
+//                         memory (several CTAs per matrix, each with its rows of V);
+//   calib_finalize_kernel re-orthogonalisation, eigenvalue order, column signs;
 //   calib_rotate_kernel   |x . R| for every sample on the tensor cores (R split into
 //                         three bf16 terms), stored per channel;
 //   calib_select_kernel   one CTA per (matrix, channel): radix selection of the
@@ -202,42 +203,53 @@ __global__ void __launch_bounds__(kMoThreads, 1) calib_moments_kernel(
 
 // ---- eigendecomposition ------------------------------------------------------------------
 //
-// One CTA per (KV head, K|V).  The chunk partials are summed in a fixed order,
-// symmetrised and (if asked) centred in fp64, then cyclic Jacobi runs in fp32 in
-// shared memory: a sweep is D - 1 rounds of the round-robin pairing (position
-// D - 1 fixed, the others turning), each round rotating D / 2 disjoint pairs at once.
-// A pair is rotated when |a_pq| > kJacobiTol sqrt(|a_pp a_qq|); the sweeps stop
-// after one without rotations (or at kMaxSweeps).  Each 2 x 2 block of A between
-// two pairs is updated once by J1^T A J2 and mirrored, so A stays exactly
-// symmetric; a pair's own block takes the stable form a_pp - t a_pq, a_qq + t a_pq, 0.
+// Cyclic Jacobi in fp32 over (KV head, K|V) matrices.  kSlices CTAs serve one
+// matrix: each sums the chunk partials in a fixed order, symmetrises and (if asked)
+// centres them in fp64, and runs the same sweeps on A (so all of them hold the
+// same A, bit for bit), while accumulating only its own D / kSlices rows of
+// V = J_1 J_2 ...; the rotations need no exchange between the CTAs.
+//   * A is kept as its upper triangle (element (i, j) at min/max), in shared memory;
+//   * a sweep is D - 1 rounds of the round-robin pairing (position D - 1 fixed, the
+//     others turning), each round rotating D / 2 disjoint pairs at once;
+//   * a pair is rotated when |a_pq| > kJacobiTol sqrt(|a_pp a_qq|); the sweeps stop
+//     after one without rotations (or at kMaxSweeps);
+//   * each 2 x 2 block of A between two pairs is updated once by J1^T A J2; a pair's
+//     own block takes the stable form a_pp - t a_pq, a_qq + t a_pq, 0.
+// The V rows and the eigenvalues go to the workspace; calib_finalize_kernel
+// re-orthogonalises V, orders and signs the columns.
 constexpr int kEigThreads = 512;
+constexpr int kFinThreads = 512;
+constexpr int kSlices = 8;
 constexpr float kJacobiTol = 0x1p-21f;
 constexpr int kMaxSweeps = 40;
 
 template <int D>
 constexpr size_t eig_smem() {
-  return static_cast<size_t>(2 * D * (D + 1)) * 4 + (D / 2) * 16 + (D / 2) * 8 + D * 8 + D * 4 * 4 + 16;
+  return static_cast<size_t>(D * (D + 1) + (D / kSlices) * (D + 1)) * 4 + (D / 2) * 16 + (D / 2) * 8 + D * 8 + 16;
+}
+
+// Index of element (i, j) of the symmetric matrix in its upper-triangle storage.
+template <int LD>
+__device__ __forceinline__ int sym_at(int i, int j) {
+  return i < j ? i * LD + j : j * LD + i;
 }
 
 template <int D>
 __global__ void __launch_bounds__(kEigThreads, 1) calib_eig_kernel(const float* __restrict__ part_m,
                                                                     const float* __restrict__ part_s, int per,
                                                                     int64_t num_samples, int centered, int H,
-                                                                    int kv_base, CalibIO io) {
-  constexpr int NP = D / 2, LD = D + 1;
+                                                                    int kv_base, CalibIO io, float* __restrict__ v_ws,
+                                                                    float* __restrict__ lam_ws) {
+  constexpr int NP = D / 2, LD = D + 1, RS = D / kSlices;
   extern __shared__ __align__(16) uint8_t esm_raw[];
-  float* A = reinterpret_cast<float*>(esm_raw);   // [D][LD]
-  float* V = A + D * LD;                          // [D][LD]
-  float4* rot = reinterpret_cast<float4*>(V + D * LD);  // (c, s, t, active) per pair
-  int2* pr = reinterpret_cast<int2*>(rot + NP);         // (p, q) per pair
-  double* mu = reinterpret_cast<double*>(pr + NP);      // [D]
-  float* lam = reinterpret_cast<float*>(mu + D);        // [D]
-  float* sgn = lam + D;                                 // [D]
-  int* rank = reinterpret_cast<int*>(sgn + D);          // [D]
-  int* inv = rank + D;                                  // [D]
-  int* cnt = inv + D;  // [2]
-  const int h = blockIdx.x, kv = kv_base + blockIdx.y, mat = kv * H + h;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* A = reinterpret_cast<float*>(esm_raw);         // [D][LD], upper triangle
+  float* V = A + D * LD;                                // [RS][LD]: rows s RS .. s RS + RS - 1
+  float4* rot = reinterpret_cast<float4*>(V + RS * LD);  // (c, s, t, active) per pair
+  int2* pr = reinterpret_cast<int2*>(rot + NP);          // (p, q) per pair
+  double* mu = reinterpret_cast<double*>(pr + NP);       // [D]
+  int* cnt = reinterpret_cast<int*>(mu + D);             // [2]
+  const int h = blockIdx.x, kv = kv_base + blockIdx.y, mat = kv * H + h, slice = blockIdx.z;
+  const int tid = threadIdx.x;
   const float* pm = part_m + static_cast<size_t>(mat) * per * D * D;
   const float* ps = part_s + static_cast<size_t>(mat) * per * D;
   const double n = static_cast<double>(num_samples);
@@ -253,12 +265,12 @@ __global__ void __launch_bounds__(kEigThreads, 1) calib_eig_kernel(const float* 
     for (int c = 0; c < per; ++c) s += pm[static_cast<size_t>(c) * D * D + e];
     A[(e / D) * LD + (e % D)] = s;
   }
-  for (int e = tid; e < D * D; e += kEigThreads) {
+  for (int e = tid; e < RS * D; e += kEigThreads) {
     const int i = e / D, j = e % D;
-    V[i * LD + j] = (i == j) ? 1.f : 0.f;
+    V[i * LD + j] = (slice * RS + i == j) ? 1.f : 0.f;
   }
   __syncthreads();
-  float* cov = io.cov[kv] ? io.cov[kv] + static_cast<size_t>(h) * D * D : nullptr;
+  float* cov = (io.cov[kv] && slice == 0) ? io.cov[kv] + static_cast<size_t>(h) * D * D : nullptr;
   float cij[(D * D + kEigThreads - 1) / kEigThreads];
 #pragma unroll
   for (int u = 0; u < (D * D + kEigThreads - 1) / kEigThreads; ++u) {
@@ -294,9 +306,10 @@ __global__ void __launch_bounds__(kEigThreads, 1) calib_eig_kernel(const float* 
           p = (r + tid) % (D - 1);
           q = (r - tid + (D - 1)) % (D - 1);
         }
-        const float app = A[p * LD + p], aqq = A[q * LD + q], apq = A[p * LD + q];
+        const float app = A[p * LD + p], aqq = A[q * LD + q], apq = A[sym_at<LD>(p, q)];
         float c = 1.f, s = 0.f, t = 0.f, act = 0.f;
         if (apq != 0.f && fabsf(apq) > kJacobiTol * sqrtf(fabsf(app) * fabsf(aqq))) {
+          // tan of the rotation angle (the root of t^2 + 2 theta t - 1 of magnitude <= 1)
           const float theta = (aqq - app) / (2.f * apq);
           const float at = fabsf(theta);
           t = at > 1e18f ? 0.5f / theta : copysignf(1.f / (at + sqrtf(theta * theta + 1.f)), theta);
@@ -326,31 +339,26 @@ __global__ void __launch_bounds__(kEigThreads, 1) calib_eig_kernel(const float* 
         if (r1.w == 0.f && r2.w == 0.f) continue;
         const int2 P1 = pr[k1], P2 = pr[k2];
         if (k1 == k2) {
-          const float apq = A[P1.x * LD + P1.y];
+          const int o = sym_at<LD>(P1.x, P1.y);
+          const float apq = A[o];
           A[P1.x * LD + P1.x] -= r1.z * apq;
           A[P1.y * LD + P1.y] += r1.z * apq;
-          A[P1.x * LD + P1.y] = 0.f;
-          A[P1.y * LD + P1.x] = 0.f;
+          A[o] = 0.f;
           continue;
         }
-        const float a11 = A[P1.x * LD + P2.x], a12 = A[P1.x * LD + P2.y];
-        const float a21 = A[P1.y * LD + P2.x], a22 = A[P1.y * LD + P2.y];
+        const int o11 = sym_at<LD>(P1.x, P2.x), o12 = sym_at<LD>(P1.x, P2.y);
+        const int o21 = sym_at<LD>(P1.y, P2.x), o22 = sym_at<LD>(P1.y, P2.y);
+        const float a11 = A[o11], a12 = A[o12], a21 = A[o21], a22 = A[o22];
         const float r11 = r1.x * a11 - r1.y * a21, r21 = r1.y * a11 + r1.x * a21;
         const float r12 = r1.x * a12 - r1.y * a22, r22 = r1.y * a12 + r1.x * a22;
-        const float b11 = r2.x * r11 - r2.y * r12, b12 = r2.y * r11 + r2.x * r12;
-        const float b21 = r2.x * r21 - r2.y * r22, b22 = r2.y * r21 + r2.x * r22;
-        A[P1.x * LD + P2.x] = b11;
-        A[P1.x * LD + P2.y] = b12;
-        A[P1.y * LD + P2.x] = b21;
-        A[P1.y * LD + P2.y] = b22;
-        A[P2.x * LD + P1.x] = b11;
-        A[P2.y * LD + P1.x] = b12;
-        A[P2.x * LD + P1.y] = b21;
-        A[P2.y * LD + P1.y] = b22;
+        A[o11] = r2.x * r11 - r2.y * r12;
+        A[o12] = r2.y * r11 + r2.x * r12;
+        A[o21] = r2.x * r21 - r2.y * r22;
+        A[o22] = r2.y * r21 + r2.x * r22;
       }
-      // V <- V J: columns p, q of every row
-      for (int e = tid; e < D * NP; e += kEigThreads) {
-        const int k = e / D, i = e % D;
+      // V <- V J on this CTA's rows: columns p, q
+      for (int e = tid; e < RS * NP; e += kEigThreads) {
+        const int k = e / RS, i = e % RS;
         const float4 rr = rot[k];
         if (rr.w == 0.f) continue;
         const int2 P = pr[k];
@@ -363,11 +371,42 @@ __global__ void __launch_bounds__(kEigThreads, 1) calib_eig_kernel(const float* 
     if (cnt[sweep & 1] == 0) break;
   }
 
-  // eigenvalues; then one Newton-Schulz step V <- V (3 I - V^T V) / 2 brings the
-  // columns, which lose orthogonality by rounding over the sweeps' rotations, back to
-  // orthonormal within fp32 rounding (A's storage holds V^T V, then the new V)
+  float* vw = v_ws + static_cast<size_t>(mat) * D * D;
+  for (int e = tid; e < RS * D; e += kEigThreads) vw[static_cast<size_t>(slice * RS + e / D) * D + e % D] = V[(e / D) * LD + e % D];
+  if (slice == 0) {
+    if (tid < D) lam_ws[static_cast<size_t>(mat) * D + tid] = A[tid * LD + tid];
+    if (io.sweeps[kv] && tid == 0) io.sweeps[kv][h] = sweep < kMaxSweeps ? sweep + 1 : kMaxSweeps;
+  }
+}
+
+// One CTA per matrix: one Newton-Schulz step V <- V (3 I - V^T V) / 2 (the columns
+// lose orthogonality by rounding over the sweeps' rotations; the step brings them
+// back within fp32 rounding), then the eigenvalues in descending order (ties by
+// index) and each column signed so that its entry of largest magnitude (lowest row
+// on a tie) is positive.
+template <int D>
+constexpr size_t fin_smem() {
+  return static_cast<size_t>(2 * D * (D + 1)) * 4 + D * 4 * 4;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFinThreads, 1) calib_finalize_kernel(const float* __restrict__ v_ws,
+                                                                         const float* __restrict__ lam_ws, int H,
+                                                                         int kv_base, CalibIO io) {
+  constexpr int LD = D + 1;
+  extern __shared__ __align__(16) uint8_t fsm_raw[];
+  float* V = reinterpret_cast<float*>(fsm_raw);  // [D][LD]
+  float* W = V + D * LD;                          // [D][LD]
+  float* lam = W + D * LD;                        // [D]
+  float* sgn = lam + D;                           // [D]
+  int* rank = reinterpret_cast<int*>(sgn + D);    // [D]
+  int* inv = rank + D;                            // [D]
+  const int h = blockIdx.x, kv = kv_base + blockIdx.y, mat = kv * H + h;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float* vw = v_ws + static_cast<size_t>(mat) * D * D;
+  for (int e = tid; e < D * D; e += kFinThreads) V[(e / D) * LD + e % D] = vw[e];
   if (tid < D) {
-    lam[tid] = A[tid * LD + tid];
+    lam[tid] = lam_ws[static_cast<size_t>(mat) * D + tid];
     inv[tid] = tid;
   }
   __syncthreads();
@@ -379,7 +418,7 @@ __global__ void __launch_bounds__(kEigThreads, 1) calib_eig_kernel(const float* 
     for (int a = 0; a < TI; ++a)
 #pragma unroll
       for (int b = 0; b < TJ; ++b) acc[a][b] = 0.f;
-    for (int r = 0; r < D; ++r) {  // W = V^T V
+    for (int r = 0; r < D; ++r) {  // V^T V
       float va[TI], vb[TJ];
 #pragma unroll
       for (int a = 0; a < TI; ++a) va[a] = V[r * LD + ti + 32 * a];
@@ -395,19 +434,19 @@ __global__ void __launch_bounds__(kEigThreads, 1) calib_eig_kernel(const float* 
 #pragma unroll
       for (int b = 0; b < TJ; ++b) {
         const int i = ti + 32 * a, j = tj + 16 * b;
-        A[i * LD + j] = (i == j ? 1.5f : 0.f) - 0.5f * acc[a][b];
+        W[i * LD + j] = (i == j ? 1.5f : 0.f) - 0.5f * acc[a][b];
       }
     __syncthreads();
 #pragma unroll
     for (int a = 0; a < TI; ++a)
 #pragma unroll
       for (int b = 0; b < TJ; ++b) acc[a][b] = 0.f;
-    for (int r = 0; r < D; ++r) {  // V (3 I - W) / 2, rows ti + 32 a of V
+    for (int r = 0; r < D; ++r) {  // V (3 I - V^T V) / 2, rows ti + 32 a of V
       float va[TI], wb[TJ];
 #pragma unroll
       for (int a = 0; a < TI; ++a) va[a] = V[(ti + 32 * a) * LD + r];
 #pragma unroll
-      for (int b = 0; b < TJ; ++b) wb[b] = A[r * LD + tj + 16 * b];
+      for (int b = 0; b < TJ; ++b) wb[b] = W[r * LD + tj + 16 * b];
 #pragma unroll
       for (int a = 0; a < TI; ++a)
 #pragma unroll
@@ -418,7 +457,6 @@ __global__ void __launch_bounds__(kEigThreads, 1) calib_eig_kernel(const float* 
     for (int a = 0; a < TI; ++a)
 #pragma unroll
       for (int b = 0; b < TJ; ++b) V[(ti + 32 * a) * LD + tj + 16 * b] = acc[a][b];
-    __syncthreads();
   }
   if (tid < D) {
     const float l = lam[tid];
@@ -429,7 +467,8 @@ __global__ void __launch_bounds__(kEigThreads, 1) calib_eig_kernel(const float* 
     }
     rank[tid] = rk;
   }
-  for (int j = warp; j < D; j += kEigThreads / 32) {
+  __syncthreads();
+  for (int j = warp; j < D; j += kFinThreads / 32) {
     float best = -1.f;
     int bi = 0;
     for (int i = lane; i < D; i += 32) {
@@ -450,16 +489,14 @@ __global__ void __launch_bounds__(kEigThreads, 1) calib_eig_kernel(const float* 
     }
     if (lane == 0) sgn[j] = V[bi * LD + j] < 0.f ? -1.f : 1.f;
   }
-  __syncthreads();
   if (tid < D) inv[rank[tid]] = tid;
   __syncthreads();
   float* R = io.R[kv] + static_cast<size_t>(h) * D * D;
-  for (int e = tid; e < D * D; e += kEigThreads) {
+  for (int e = tid; e < D * D; e += kFinThreads) {
     const int i = e / D, col = e % D, j = inv[col];
     R[e] = sgn[j] * V[i * LD + j];
   }
   if (io.eig[kv] && tid < D) io.eig[kv][static_cast<size_t>(h) * D + rank[tid]] = lam[tid];
-  if (io.sweeps[kv] && tid == 0) io.sweeps[kv][h] = sweep < kMaxSweeps ? sweep + 1 : kMaxSweeps;
 }
 
 // ---- |x . R| per sample and channel --------------------------------------------------------
@@ -731,7 +768,7 @@ int64_t moment_chunks(int H, int64_t N) {
 }
 
 struct WsLayout {
-  size_t part_m, part_s, y, total;
+  size_t part_m, part_s, y, v, lam, total;
   int64_t per, n_pad;
 };
 
@@ -743,7 +780,9 @@ WsLayout ws_layout(int H, int D, int64_t N) {
   w.part_m = 0;
   w.part_s = align_up(w.part_m + mats * w.per * D * D * 4, 256);
   w.y = align_up(w.part_s + mats * w.per * D * 4, 256);
-  w.total = align_up(w.y + mats * D * static_cast<size_t>(w.n_pad) * 4, 256);
+  w.v = align_up(w.y + mats * D * static_cast<size_t>(w.n_pad) * 4, 256);
+  w.lam = align_up(w.v + mats * D * D * 4, 256);
+  w.total = align_up(w.lam + mats * D * 4, 256);
   return w;
 }
 
@@ -765,10 +804,16 @@ cudaError_t run_calibration(int H, int64_t N, const void* k, const void* v, int 
       mk, mv, N, H, kv_base, part_m, part_s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
+  float* v_ws = reinterpret_cast<float*>(ws + w.v);
+  float* lam_ws = reinterpret_cast<float*>(ws + w.lam);
   e = set_smem_limit_once(reinterpret_cast<const void*>(calib_eig_kernel<D>), eig_smem<D>());
   if (e != cudaSuccess) return e;
-  calib_eig_kernel<D><<<dim3(H, nkv), kEigThreads, eig_smem<D>(), stream>>>(part_m, part_s, static_cast<int>(w.per),
-                                                                            N, centered, H, kv_base, io);
+  calib_eig_kernel<D><<<dim3(H, nkv, kSlices), kEigThreads, eig_smem<D>(), stream>>>(
+      part_m, part_s, static_cast<int>(w.per), N, centered, H, kv_base, io, v_ws, lam_ws);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = set_smem_limit_once(reinterpret_cast<const void*>(calib_finalize_kernel<D>), fin_smem<D>());
+  if (e != cudaSuccess) return e;
+  calib_finalize_kernel<D><<<dim3(H, nkv), kFinThreads, fin_smem<D>(), stream>>>(v_ws, lam_ws, H, kv_base, io);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   const int64_t ntiles = (N + kTok - 1) / kTok;
