@@ -167,7 +167,8 @@ size_t oscar_decode_workspace_bytes(const oscar_dims_t* dims, int32_t batch, int
  * Arguments
  *   max_seq_len   host bound on every seq_lens[b] (<= max_pages_per_seq * P);
  *                 larger device values are clamped and flagged
- *   pages_per_split  0 = chosen from the grid size; else >= 1
+ *   pages_per_split  0 = chosen from the grid size; else >= 1 (at most 65535 splits
+ *                    per sequence, and batch <= 65535: grid dimensions)
  *   q             device bf16 [batch][Hq][D]
  *   R_k, R_v      device fp32 [Hkv][D][D] (the rotations used at append time)
  *   int2_pages, scale_zero_pages   the pools written by oscar_append

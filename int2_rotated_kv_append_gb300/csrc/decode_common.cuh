@@ -149,6 +149,7 @@ bool make_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req, int S
   p->n_paged = max_pages == 0 ? 0 : (max_pages + pps - 1) / pps;
   p->ns = p->n_paged + p->n_dense;
   if (p->ns == 0) p->ns = 1;
+  if (p->ns > 65535 || B > 65535) return false;  // split index and sequence are grid y/z dimensions
   const size_t bh = static_cast<size_t>(B) * d->num_q_heads;
   size_t off = 0;
   p->off_qrot = off;

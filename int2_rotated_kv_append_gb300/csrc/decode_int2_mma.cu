@@ -381,7 +381,9 @@ __device__ __forceinline__ void dense_split(const Params& p, int d, int h, int b
 template <int NT, int NG>
 __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_kernel(Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int s = blockIdx.x + p.split_base, h = blockIdx.y, b = blockIdx.z;
+  // Dispatch order: KV head fastest, then sequence, split index slowest, so the
+  // last CTAs to start are the high splits that only long sequences have.
+  const int s = blockIdx.z + p.split_base, h = blockIdx.x, b = blockIdx.y;
   if (s >= p.n_paged) {
     dense_split<NT>(p, s - p.n_paged, h, b, smem);
     return;
@@ -936,7 +938,7 @@ cudaError_t launch_impl(const Params& p, cudaStream_t stream) {
   constexpr size_t smem = Geo<NG>::kSmem;
   cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(int2_mma_split_kernel<NT, NG>), smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(int2_mma_split_kernel<NT, NG>, dim3(p.ns - p.split_base, p.H, p.B), dim3(kWarps * 32), smem,
+  return launch_pdl(int2_mma_split_kernel<NT, NG>, dim3(p.H, p.B, p.ns - p.split_base), dim3(kWarps * 32), smem,
                     stream, p);
 }
 

@@ -196,3 +196,11 @@ def test_calibrate_validation(lib):
     assert cal(ws=ctypes.c_void_p(264)) == E      # misaligned workspace
     assert cal(dims=_dims(head_dim=96, group_size=32)) == ok.OSCAR_ERR_UNSUPPORTED
     assert cal(ws_bytes=need - 1) == ok.OSCAR_ERR_WORKSPACE
+
+
+def test_decode_plan_respects_grid_limits(lib):
+    # the split index is a grid dimension (<= 65535): a plan with more splits is refused
+    d = _dims(max_pages_per_seq=70000)
+    assert lib.oscar_decode_workspace_bytes(ctypes.byref(d), 1, 70000 * 16, 1, 64, 128) == 0
+    assert lib.oscar_decode_workspace_bytes(ctypes.byref(d), 1, 70000 * 16, 2, 64, 128) > 0
+    assert _decode(lib, d, batch=1, msl=70000 * 16, pps=1, S=64, W=128) == ok.OSCAR_ERR_INVALID_ARG
