@@ -180,8 +180,8 @@ def workload_config(args, w, batch, seq_len, pps, l2_policy):
 # launch (q-rotation + split + merge kernels) on the batch-1 32K and batch-64
 # workloads, from one ncu capture of the three kernels each (cold caches: the
 # split partials are re-read from DRAM there, from L2 in the timed loop).
-MEASURED_DECODE_TRAFFIC = {1: 554240 + 21765888 + 2091008,
-                           2: 1070848 + (424401152 + 5219584) + 8040960}
+MEASURED_DECODE_TRAFFIC = {1: 554240 + 21766656 + 2083840,
+                           2: 440659115}  # mean over three launches: 1.07 MB + 431.6 MB + 8.04 MB
 
 
 def dist_setup():
