@@ -333,7 +333,7 @@ oscar_status_t oscar_bf16_decode(const oscar_dims_t* dims, int32_t batch, int32_
  * eigenvalues coincide (or nearly, relative to fp32 rounding) the basis of their
  * eigenspace is not unique and the columns there may differ from another solver's.
  * Arguments
- *   num_samples   N, 1 .. 2^31 - 257
+ *   num_samples   N, 1 .. 2^31 - 256
  *   k, v          device bf16 [N][Hkv][D] (the layout oscar_append takes), 16-byte
  *                 aligned; either may be NULL (then its out_* must be NULL too)
  *   centered      1: covariance about the sample mean; 0: second moment

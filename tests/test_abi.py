@@ -182,6 +182,7 @@ def test_calibrate_validation(lib):
     assert cal(N=0) == E
     assert cal(N=-5) == E
     assert cal(N=1 << 31) == E
+    assert cal(N=(1 << 31) - 255) == E          # the largest accepted is 2^31 - 256
     assert cal(k=None) == E                       # k missing but out_k given
     assert cal(ov=None) == E                      # v given but out_v missing
     assert cal(k=None, v=None, ok_=None, ov=None) == E  # nothing to calibrate
