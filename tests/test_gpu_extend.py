@@ -153,3 +153,26 @@ def test_extend_varlen_rows_beyond_the_tokens_are_flagged():
     assert ok.oscar_device_errors(reset=True) & ok.OSCAR_DEVERR_POSITION
     assert torch.all(out[:2] == 0)            # positions -2 and -1: nothing attended
     assert torch.all(torch.isfinite(out))
+
+
+def test_extend_varlen_full_workload_sampled():
+    # the extend workload the benchmark times: 32 sequences x 8192 cached tokens, the
+    # last 16 of each as query rows (tiles of 16 rows), sampled (row, query head) pairs
+    B, L, chunk = 32, 8192, 16
+    w = synth.make_workload(num_q_heads=32, num_kv_heads=8, head_dim=128, group_size=64, sink_len=64,
+                            window_len=128, seq_lens=[L] * B, seed=11, device="cuda")
+    cache = Int2Cache(w)
+    cache.prefill()
+    q_start = torch.arange(0, B * chunk + 1, chunk, dtype=torch.int32, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(3)
+    q = torch.randn((B * chunk, 32, 128), generator=g, device="cuda").to(torch.bfloat16)
+    ok.oscar_device_errors(reset=True)
+    out = cache.extend_varlen(q, q_start, chunk)
+    torch.cuda.synchronize()
+    assert ok.oscar_device_errors(reset=True) == 0
+    rs = np.repeat(np.arange(B, dtype=np.int32), chunk)
+    rp = np.tile(np.arange(L - chunk, L, dtype=np.int32), B)
+    rng = np.random.default_rng(5)
+    rows = sorted(set([0, chunk - 1, B * chunk - 1] + rng.choice(B * chunk, 21, replace=False).tolist()))
+    pairs = [(r, int(h)) for r in rows for h in rng.choice(32, 2, replace=False)]
+    compare_decode(out, oracle_extend_on_gpu_cache(w, cache, q, rs, rp, pairs=pairs), pairs=pairs)
