@@ -184,6 +184,22 @@ MEASURED_DECODE_TRAFFIC = {1: 554240 + 21766656 + 2083840,
                            2: 440659115}  # mean over three launches: 1.07 MB + 431.6 MB + 8.04 MB
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over all ranks (the slowest rank's time is the job's time)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(world: int, bytes_per_rank_step: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank moves bytes_per_rank_step per step (weak scaling)."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -405,11 +421,7 @@ def run_ours(args, world, rank, local):
         t1 = time.perf_counter()
         torch.cuda.synchronize()
         barrier()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            tt = torch.tensor([ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms = float(tt.item())
+        ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
         return ms, (t0, t1)
 
     log("caches built; timing")
@@ -433,7 +445,7 @@ def run_ours(args, world, rank, local):
     step_bytes_app = algorithmic_bytes_append(w, B, bf16_rows=True)
     step_bytes = step_bytes_dec + step_bytes_app
     ms_step = ms / K
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbps(world, step_bytes, ms_step)
     dec_us = ms_dec / K * 1e3
     achieved = step_bytes_dec / (dec_us * 1e-6) / 1e9
     peak, peak_kind = measured_peak_hbm()
@@ -487,11 +499,7 @@ def run_ours(args, world, rank, local):
     te = time.perf_counter()
     e2e_run(E)
     te = time.perf_counter() - te
-    e2e_ms = te / E * 1e3
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(te / E * 1e3, world, dev)
     h2d = per_stage  # q, k, v and slots of the step in one copy (256-byte aligned parts)
     d2h = B * Hq * D * 4
 
@@ -525,7 +533,7 @@ def run_ours(args, world, rank, local):
                          "kernel": "oscar_decode (q-rotate + split + merge) per launch",
                          "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_launch": step_bytes_dec},
             "cpu_baseline": cpu,
-            "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "e2e": {"value": whole_job_gbps(world, step_bytes, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "mode": "one CUDA graph per step (H2D inputs, append, decode, D2H output); two steps in flight, "
                              "the host waits for step i-2's output before launching step i"},
