@@ -439,6 +439,24 @@ def run_ours(args, world, rank, local):
     log(f"bf16 decode: {ms_bf / K * 1e3:.2f} us")
     ms_app, _ = timed(lambda i: append_r(i % NR), K, Wm)
     log(f"append: {ms_app / K * 1e3:.2f} us")
+    # Warm L2: replica 0 decoded again and again (its cache stays in L2 when it fits).
+    Kw = min(K, 2000)
+    ms_warm, _ = timed(lambda i: decode_r(0), Kw, Wm)
+    # Single launch: one decode issued on its own (no graph), L2 flushed before it.
+    flush_buf = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    single = []
+    for j in range(25):
+        flush_buf.zero_()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        decode_r(j % NR)
+        e1.record()
+        e1.synchronize()
+        single.append(e0.elapsed_time(e1) * 1e3)
+    del flush_buf
+    single_us = statistics.median(single[5:])
+    log(f"decode warm L2: {ms_warm / Kw * 1e3:.2f} us, single launch: {single_us:.2f} us")
     sampler.stop()
 
     step_bytes_dec = algorithmic_bytes_decode(w, lens_all[:B])
@@ -526,6 +544,12 @@ def run_ours(args, world, rank, local):
             "tokens_per_s": world * B / (ms_step * 1e-3),
             "us_per_step": ms_step * 1e3,
             "decode_us": dec_us, "append_us": ms_app / K * 1e3, "bf16_decode_us": bf_us,
+            "decode_warm_l2_us": ms_warm / Kw * 1e3,
+            "decode_warm_l2_note": "one replica decoded repeatedly in a CUDA graph: its cache "
+                                   + ("fits" if step_bytes_dec <= l2 else "does not fit") + " in L2",
+            "decode_single_launch_us": single_us,
+            "decode_single_launch_note": "one decode call (three kernels) launched on its own, L2 flushed "
+                                         "before it, CUDA events around it; median of 20",
             "speedup_vs_bf16": bf_us / dec_us,
             "bf16_decode_GBps": algorithmic_bytes_bf16(w, lens_all[:B]) / (bf_us * 1e-6) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
