@@ -45,6 +45,13 @@ struct CalibIO {
   int32_t* sweeps[2];
 };
 
+// Entry kv (0: keys, 1: values) of a pair of output pointers, chosen without
+// indexing the kernel parameter at run time (which would copy it to local memory).
+template <typename T>
+__device__ __forceinline__ T* pick(T* const (&a)[2], int kv) {
+  return kv ? a[1] : a[0];
+}
+
 // ---- second moments --------------------------------------------------------------------
 //
 // For one (KV head, K|V) and every per-th tile of 128 samples: D[m][n] += sum_t
@@ -270,7 +277,7 @@ __global__ void __launch_bounds__(kEigThreads, 1) calib_eig_kernel(const float* 
     V[i * LD + j] = (slice * RS + i == j) ? 1.f : 0.f;
   }
   __syncthreads();
-  float* cov = (io.cov[kv] && slice == 0) ? io.cov[kv] + static_cast<size_t>(h) * D * D : nullptr;
+  float* cov = (pick(io.cov, kv) && slice == 0) ? pick(io.cov, kv) + static_cast<size_t>(h) * D * D : nullptr;
   float cij[(D * D + kEigThreads - 1) / kEigThreads];
 #pragma unroll
   for (int u = 0; u < (D * D + kEigThreads - 1) / kEigThreads; ++u) {
@@ -375,7 +382,7 @@ __global__ void __launch_bounds__(kEigThreads, 1) calib_eig_kernel(const float* 
   for (int e = tid; e < RS * D; e += kEigThreads) vw[static_cast<size_t>(slice * RS + e / D) * D + e % D] = V[(e / D) * LD + e % D];
   if (slice == 0) {
     if (tid < D) lam_ws[static_cast<size_t>(mat) * D + tid] = A[tid * LD + tid];
-    if (io.sweeps[kv] && tid == 0) io.sweeps[kv][h] = sweep < kMaxSweeps ? sweep + 1 : kMaxSweeps;
+    if (pick(io.sweeps, kv) && tid == 0) pick(io.sweeps, kv)[h] = sweep < kMaxSweeps ? sweep + 1 : kMaxSweeps;
   }
 }
 
@@ -491,12 +498,12 @@ __global__ void __launch_bounds__(kFinThreads, 1) calib_finalize_kernel(const fl
   }
   if (tid < D) inv[rank[tid]] = tid;
   __syncthreads();
-  float* R = io.R[kv] + static_cast<size_t>(h) * D * D;
+  float* R = pick(io.R, kv) + static_cast<size_t>(h) * D * D;
   for (int e = tid; e < D * D; e += kFinThreads) {
     const int i = e / D, col = e % D, j = inv[col];
     R[e] = sgn[j] * V[i * LD + j];
   }
-  if (io.eig[kv] && tid < D) io.eig[kv][static_cast<size_t>(h) * D + rank[tid]] = lam[tid];
+  if (pick(io.eig, kv) && tid < D) pick(io.eig, kv)[static_cast<size_t>(h) * D + rank[tid]] = lam[tid];
 }
 
 // ---- |x . R| per sample and channel --------------------------------------------------------
@@ -546,7 +553,7 @@ __global__ void __launch_bounds__(kRoThreads, 1) calib_rotate_kernel(
   const int64_t ntiles = (num_samples + kTok - 1) / kTok;
   const int per = gridDim.x, j0 = blockIdx.x;
   const int n_my = static_cast<int>((ntiles - j0 + per - 1) / per);
-  const float* R = io.R[kv] + static_cast<size_t>(h) * D * D;
+  const float* R = pick(io.R, kv) + static_cast<size_t>(h) * D * D;
   const CUtensorMap* map = kv ? &map_v : &map_k;
 
   if (tid == 0) {
@@ -740,7 +747,7 @@ __global__ void __launch_bounds__(kSelThreads) calib_select_kernel(const uint32_
     rank -= sel[1];
     __syncthreads();
   }
-  if (tid == 0) io.clip[kv][static_cast<size_t>(h) * D + j] = __uint_as_float(prefix);
+  if (tid == 0) pick(io.clip, kv)[static_cast<size_t>(h) * D + j] = __uint_as_float(prefix);
 }
 
 // ---- host ---------------------------------------------------------------------------------------
