@@ -325,10 +325,11 @@ oscar_status_t oscar_bf16_decode(const oscar_dims_t* dims, int32_t batch, int32_
  * Arithmetic: the sums of x x^T and x are taken on the tensor cores from the bf16
  * samples with fp32 accumulation (products exact; each chunk of samples is one
  * accumulation chain of 8 MMAs per 128 samples, so its relative error grows with the
- * chunk's length, about N / (16 x number of SMs / (2 Hkv)) units of 2^-23), partial
- * sums per chunk are added in a fixed order and centred in fp64; the eigenvectors come
- * from cyclic Jacobi in fp32 (a pair is left alone once |a_pq| <= 2^-21
- * sqrt(|a_pp a_qq|); at most 40 sweeps); |x . R| is formed on the tensor cores
+ * chunk's length, about N / (16 x number of SMs / (2 Hkv)) units of 2^-23); the chunk
+ * partials are added in fp32 in a fixed order, then symmetrised and centred in fp64;
+ * the eigenvectors come from cyclic Jacobi in fp32 (a pair is left alone once
+ * |a_pq| <= 2^-21 sqrt(|a_pp a_qq|); at most 40 sweeps) followed by one Newton-Schulz
+ * step that restores orthogonality to fp32 rounding; |x . R| is formed on the tensor cores
  * with R split into three bf16 terms (about 24 bits) and fp32 accumulation, and the
  * k-th smallest of those fp32 values is selected exactly.  The centred covariance
  * loses relative accuracy in proportion to |mu|^2 / variance (fp32 sums).  Where

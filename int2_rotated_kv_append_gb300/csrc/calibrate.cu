@@ -211,8 +211,8 @@ __global__ void __launch_bounds__(kMoThreads, 1) calib_moments_kernel(
 // ---- eigendecomposition ------------------------------------------------------------------
 //
 // Cyclic Jacobi in fp32 over (KV head, K|V) matrices.  kSlices CTAs serve one
-// matrix: each sums the chunk partials in a fixed order, symmetrises and (if asked)
-// centres them in fp64, and runs the same sweeps on A (so all of them hold the
+// matrix: each sums the chunk partials in fp32 in a fixed order, symmetrises and (if
+// asked) centres them in fp64, and runs the same sweeps on A (so all of them hold the
 // same A, bit for bit), while accumulating only its own D / kSlices rows of
 // V = J_1 J_2 ...; the rotations need no exchange between the CTAs.
 //   * A is kept as its upper triangle (element (i, j) at min/max), in shared memory;
