@@ -184,6 +184,20 @@ MEASURED_DECODE_TRAFFIC = {1: 554240 + 21766656 + 2083840,
                            2: 440659115}  # mean over three launches: 1.07 MB + 431.6 MB + 8.04 MB
 
 
+def cpu_model() -> str:
+    """The host CPU's model name as /proc/cpuinfo or the platform reports it ("unknown" if neither does)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "hardware", "cpu model"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine() or "unknown"
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     """The largest x over all ranks (the slowest rank's time is the job's time)."""
     if world <= 1:
@@ -271,7 +285,7 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(args, w, w.batch, int(lens.max()), 0, "host memory (fp64 CPU oracle)"),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": gqa, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": gqa, "kind": "oracle", "cpu_model": cpu_model(),
                          "sample": f"per step: the {gqa} query heads of one KV head of sequence 0 over its first "
                                    f"{L} of {L_full} tokens (fp64 oracle, one thread per query head)"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -772,6 +786,7 @@ def cpu_baseline(w, cache, B, step_bytes):
         if el > 10.0 or n >= 20:
             break
     return {"value": step_bytes * n / el / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "cpu_model": cpu_model(), "host_cores": os.cpu_count(),
             "sample": f"{n} full step(s) of one replica (append of {B} token(s) + decode of {len(pairs)} "
                       f"(sequence, query head) pairs), fp64 oracle, {threads} threads",
             "s_per_step": el / n}
