@@ -295,6 +295,200 @@ def run_reference(args, world, rank):
 
 # --------------------------------------------------------------------------- our arm
 
+def capture_graph(fn, n, dev):
+    """CUDA graph of a chunk of calls fn(0..per-1), replayed n // per times (per | n, per <= 1000)."""
+    import torch
+    per = n if n <= 1000 else next(d for d in range(1000, 0, -1) if n % d == 0)
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(min(3, n)):
+            fn(i)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(per):
+            fn(i)
+    return g, n // per
+
+
+def timed_graph(fn, n, warm, dev, world, barrier):
+    """n calls of fn captured in CUDA graphs, after `warm` untimed calls; CUDA events
+    on the replaying stream, a synchronize and a barrier on both sides; the slowest
+    rank's milliseconds and the host clock around the timed region."""
+    import torch
+    g, reps = capture_graph(fn, n, dev)
+    if warm > 0:
+        gw, rw = capture_graph(fn, warm, dev)
+        for _ in range(rw):
+            gw.replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    e1.synchronize()
+    t1 = time.perf_counter()
+    torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    return ms, (t0, t1)
+
+
+class DecodeSetup:
+    """One decode workload on the device: enough cache replicas (disjoint pages of
+    one pool) that they exceed 3x L2, the INT2 and BF16 caches built by the
+    library's appends, per-replica inputs in one staging block (q, k, v, slots of
+    the current token), and the calls of a step (append, decode, BF16 decode)."""
+
+    def __init__(self, cfg, dev, l2, replicas=0, pps=-1):
+        import numpy as np
+        import torch
+
+        import int2_rotated_kv_append_gb300 as ok
+        from int2_rotated_kv_append_gb300 import synth
+        from int2_rotated_kv_append_gb300.cache import Bf16Cache, Int2Cache
+
+        self.cfg = cfg
+        base_lens = synth.config_seq_lens(cfg)
+        B = len(base_lens)
+        one = types.SimpleNamespace(num_q_heads=64 if cfg == 3 else 32, num_kv_heads=8, head_dim=128,
+                                    group_size=64, sink_len=64, window_len=256 if cfg == 3 else 128)
+        w0_bytes = algorithmic_bytes_decode(one, base_lens)
+        NR = max(1, math.ceil(3 * l2 / w0_bytes)) if replicas <= 0 else replicas
+        log(f"generating workload: config {cfg}, {NR} replicas")
+        w = synth.make_config(cfg, device=dev, replicas=NR)
+        log("building INT2 and BF16 caches")
+        cache = Int2Cache(w, device=dev, pages_per_split=None if pps < 0 else pps)
+        cache.prefill()
+        bf = Bf16Cache(w, device=dev, pages_per_split=None if pps < 0 else pps)
+        bf.prefill()
+        torch.cuda.synchronize()
+        self.w, self.cache, self.bf, self.NR, self.B, self.l2 = w, cache, bf, NR, B, l2
+        H, Hq, D = w.num_kv_heads, w.num_q_heads, w.head_dim
+        lens_all = w.seq_lens.tolist()
+        self.lens_all = lens_all
+        # Current token (position L-1) of every sequence: the K/V appended by each step.
+        starts = np.cumsum([0] + lens_all)[:-1]
+        cur = torch.as_tensor(starts + np.array(lens_all) - 1, dtype=torch.long)
+        k_cur = w.k[cur.to(dev)].contiguous()
+        v_cur = w.v[cur.to(dev)].contiguous()
+        s_cur = w.slot_mapping[cur].to(dev).contiguous()
+        p_cur = w.tok_pos[cur].to(dev).contiguous()                  # position L - 1 of the current token
+        i_cur = torch.arange(B, dtype=torch.int32, device=dev)      # sequence index inside a replica
+        q = w.q.contiguous()
+        out = torch.empty((w.batch, Hq, D), dtype=torch.float32, device=dev)
+        out_bf = torch.empty_like(out)
+        ws = cache.workspace(max(lens_all))
+        ws_bf = bf.workspace()
+        # A step's inputs (q, k, v, slots) sit in one staging block per replica, so the
+        # end-to-end loop moves them host -> device with a single copy.
+        in_sizes = [B * Hq * D * 2, B * H * D * 2, B * H * D * 2, B * 8]
+        in_offs = [0]
+        for sz_ in in_sizes[:-1]:
+            in_offs.append((in_offs[-1] + sz_ + 255) // 256 * 256)
+        per_stage = (in_offs[-1] + in_sizes[-1] + 255) // 256 * 256
+        stage = torch.empty(NR * per_stage, dtype=torch.uint8, device=dev)
+
+        def stage_view(r, idx, dtype, shape):
+            base = r * per_stage + in_offs[idx]
+            return stage[base:base + in_sizes[idx]].view(dtype).view(shape)
+
+        def views(r):
+            sl = slice(r * B, (r + 1) * B)
+            x = dict(q=stage_view(r, 0, torch.bfloat16, (B, Hq, D)), k=stage_view(r, 1, torch.bfloat16, (B, H, D)),
+                     v=stage_view(r, 2, torch.bfloat16, (B, H, D)), slots=stage_view(r, 3, torch.int64, (B,)))
+            x["q"].copy_(q[sl])
+            x["k"].copy_(k_cur[sl])
+            x["v"].copy_(v_cur[sl])
+            x["slots"].copy_(s_cur[sl])
+            x.update(pos=p_cur[sl], pt=cache.page_table[sl], lens=cache.seq_lens[sl], sink=cache.sink[sl],
+                     win=cache.window[sl], out=out[sl], out_bf=out_bf[sl], bpt=bf.page_table[sl],
+                     blens=bf.seq_lens[sl])
+            return x
+        V = [views(r) for r in range(NR)]
+        msl_r = [max(lens_all[r * B:(r + 1) * B]) for r in range(NR)]
+        self.V, self.stage, self.per_stage, self.out = V, stage, per_stage, out
+
+        def append_r(r):
+            # the current token into the INT2 pool and its BF16 row into the window ring
+            x = V[r]
+            ok.oscar_append_mixed(w.dims, x["k"], x["v"], cache.R_k, cache.R_v, cache.clip_k, cache.clip_v,
+                                  x["pt"], x["slots"], i_cur, x["pos"], x["lens"], w.sink_len, w.window_len,
+                                  cache.int2_pages, cache.scale_zero, x["sink"], x["win"])
+
+        def decode_r(r):
+            x = V[r]
+            ok.oscar_decode(w.dims, B, msl_r[r], cache.pps, x["q"], cache.R_k, cache.R_v, cache.int2_pages,
+                            cache.scale_zero, x["sink"], x["win"], x["pt"], x["lens"], w.sink_len, w.window_len,
+                            0.0, x["out"], ws)
+
+        def bf16_r(r):
+            x = V[r]
+            ok.oscar_bf16_decode(w.dims, B, msl_r[r], bf.pps, x["q"], bf.pages, x["bpt"], x["blens"], 0.0,
+                                 x["out_bf"], ws_bf)
+
+        def step(i):
+            r = i % NR
+            append_r(r)
+            decode_r(r)
+
+        self.append_r, self.decode_r, self.bf16_r, self.step = append_r, decode_r, bf16_r, step
+
+    def bytes_decode(self):
+        return algorithmic_bytes_decode(self.w, self.lens_all[:self.B])
+
+    def bytes_step(self):
+        return self.bytes_decode() + algorithmic_bytes_append(self.w, self.B, bf16_rows=True)
+
+
+def extra_config_line(cfg, dev, l2, K, Wm, world, barrier) -> dict:
+    """The decode step, the decode alone and the BF16 reference decode of another
+    workload, timed as the main one (CUDA graphs over cache replicas larger than
+    L2, CUDA events, W warm-up calls), with its own roofline."""
+    import torch
+
+    from int2_rotated_kv_append_gb300 import synth
+    S = DecodeSetup(cfg, dev, l2)
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.1)
+    ms_step, (t0, t1) = timed_graph(S.step, K, Wm, dev, world, barrier)
+    clocks = sampler.summary(t0, t1)
+    sampler.stop()
+    ms_dec, _ = timed_graph(lambda i: S.decode_r(i % S.NR), K, Wm, dev, world, barrier)
+    ms_bf, _ = timed_graph(lambda i: S.bf16_r(i % S.NR), K, Wm, dev, world, barrier)
+    w, B = S.w, S.B
+    dec_us, bf_us, step_us = ms_dec / K * 1e3, ms_bf / K * 1e3, ms_step / K * 1e3
+    peak, peak_kind = measured_peak_hbm()
+    nbytes = S.bytes_decode()
+    achieved = nbytes / (dec_us * 1e-6) / 1e9
+    lens = S.lens_all[:B]
+    line = {"workload": synth.CONFIG_NAMES[cfg], "batch": B, "seq_len_min": min(lens), "seq_len_max": max(lens),
+            "seq_len_mean": sum(lens) / B, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "sink": w.sink_len, "window": w.window_len, "group": w.group_size,
+            "pages_per_split": "auto" if S.cache.pps == 0 else S.cache.pps,
+            "l2_policy": f"inputs larger than L2: {S.NR} cache replica(s) in disjoint pages, "
+                         f"{S.NR * nbytes / 1e6:.0f} MB cycled (L2 {l2 / 1e6:.0f} MB)",
+            "us_per_step": step_us, "value": whole_job_gbps(world, S.bytes_step(), ms_step / K), "unit": "GB/s",
+            "tokens_per_s": world * B / (step_us * 1e-6),
+            "decode_us": dec_us, "bf16_decode_us": bf_us, "speedup_vs_bf16": bf_us / dec_us,
+            "bf16_decode_GBps": algorithmic_bytes_bf16(w, lens) / (bf_us * 1e-6) / 1e9,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": MEASURED_DECODE_TRAFFIC.get(cfg), "kernel": "oscar_decode per launch",
+                         "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_launch": nbytes},
+            "clocks": clocks}
+    log(f"config {cfg}: step {step_us:.2f} us, decode {dec_us:.2f} us ({achieved / peak:.3f} of HBM), "
+        f"bf16 {bf_us:.2f} us ({bf_us / dec_us:.2f}x)")
+    del S
+    torch.cuda.empty_cache()
+    return line
+
+
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
@@ -302,8 +496,6 @@ def run_ours(args, world, rank, local):
 
     import int2_rotated_kv_append_gb300 as ok
     from int2_rotated_kv_append_gb300 import build as okbuild
-    from int2_rotated_kv_append_gb300 import synth
-    from int2_rotated_kv_append_gb300.cache import Bf16Cache, Int2Cache
 
     okbuild.build()
     ok.load_library()
@@ -318,125 +510,16 @@ def run_ours(args, world, rank, local):
 
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
-    base_lens = synth.config_seq_lens(args.config)
-    B = len(base_lens)
-    # Number of replicas so that the cycled caches exceed 3x L2 (shape of one replica from a tiny draw).
-    one = types.SimpleNamespace(num_q_heads=64 if args.config == 3 else 32, num_kv_heads=8, head_dim=128,
-                                group_size=64, sink_len=64, window_len=256 if args.config == 3 else 128)
-    w0_bytes = algorithmic_bytes_decode(one, base_lens)
-    NR = max(1, math.ceil(3 * l2 / w0_bytes)) if args.replicas <= 0 else args.replicas
-    log(f"generating workload: config {args.config}, {NR} replicas")
-    w = synth.make_config(args.config, device=dev, replicas=NR)
-    log("building INT2 and BF16 caches")
-    cache = Int2Cache(w, device=dev, pages_per_split=None if args.pps < 0 else args.pps)
-    cache.prefill()
-    bf = Bf16Cache(w, device=dev, pages_per_split=None if args.pps < 0 else args.pps)
-    bf.prefill()
-    torch.cuda.synchronize()
-
+    S = DecodeSetup(args.config, dev, l2, args.replicas, args.pps)
+    w, cache, bf, NR, B, V = S.w, S.cache, S.bf, S.NR, S.B, S.V
     H, Hq, D = w.num_kv_heads, w.num_q_heads, w.head_dim
-    lens_all = w.seq_lens.tolist()
+    lens_all = S.lens_all
     msl = max(lens_all)
-    # Current token (position L-1) of every sequence: the K/V appended by each step.
-    starts = np.cumsum([0] + lens_all)[:-1]
-    cur = torch.as_tensor(starts + np.array(lens_all) - 1, dtype=torch.long)
-    k_cur = w.k[cur.to(dev)].contiguous()
-    v_cur = w.v[cur.to(dev)].contiguous()
-    s_cur = w.slot_mapping[cur].to(dev).contiguous()
-    p_cur = w.tok_pos[cur].to(dev).contiguous()                  # position L - 1 of the current token
-    i_cur = torch.arange(B, dtype=torch.int32, device=dev)      # sequence index inside a replica
-    q = w.q.contiguous()
-    out = torch.empty((w.batch, Hq, D), dtype=torch.float32, device=dev)
-    out_bf = torch.empty_like(out)
-    ws = cache.workspace(msl)
-    ws_bf = bf.workspace()
-
-    # A step's inputs (q, k, v, slots) sit in one staging block per replica, so the
-    # end-to-end loop moves them host -> device with a single copy.
-    in_sizes = [B * Hq * D * 2, B * H * D * 2, B * H * D * 2, B * 8]
-    in_offs = [0]
-    for sz_ in in_sizes[:-1]:
-        in_offs.append((in_offs[-1] + sz_ + 255) // 256 * 256)
-    per_stage = (in_offs[-1] + in_sizes[-1] + 255) // 256 * 256
-    stage = torch.empty(NR * per_stage, dtype=torch.uint8, device=dev)
-
-    def stage_view(r, idx, dtype, shape):
-        base = r * per_stage + in_offs[idx]
-        return stage[base:base + in_sizes[idx]].view(dtype).view(shape)
-
-    def views(r):
-        sl = slice(r * B, (r + 1) * B)
-        x = dict(q=stage_view(r, 0, torch.bfloat16, (B, Hq, D)), k=stage_view(r, 1, torch.bfloat16, (B, H, D)),
-                 v=stage_view(r, 2, torch.bfloat16, (B, H, D)), slots=stage_view(r, 3, torch.int64, (B,)))
-        x["q"].copy_(q[sl])
-        x["k"].copy_(k_cur[sl])
-        x["v"].copy_(v_cur[sl])
-        x["slots"].copy_(s_cur[sl])
-        x.update(pos=p_cur[sl], pt=cache.page_table[sl], lens=cache.seq_lens[sl], sink=cache.sink[sl],
-                 win=cache.window[sl], out=out[sl], out_bf=out_bf[sl], bpt=bf.page_table[sl], blens=bf.seq_lens[sl])
-        return x
-    V = [views(r) for r in range(NR)]
-    msl_r = [max(lens_all[r * B:(r + 1) * B]) for r in range(NR)]
-
-    def append_r(r):
-        # the current token into the INT2 pool and its BF16 row into the window ring
-        x = V[r]
-        ok.oscar_append_mixed(w.dims, x["k"], x["v"], cache.R_k, cache.R_v, cache.clip_k, cache.clip_v, x["pt"],
-                              x["slots"], i_cur, x["pos"], x["lens"], w.sink_len, w.window_len, cache.int2_pages,
-                              cache.scale_zero, x["sink"], x["win"])
-
-    def decode_r(r):
-        x = V[r]
-        ok.oscar_decode(w.dims, B, msl_r[r], cache.pps, x["q"], cache.R_k, cache.R_v, cache.int2_pages,
-                        cache.scale_zero, x["sink"], x["win"], x["pt"], x["lens"], w.sink_len, w.window_len, 0.0,
-                        x["out"], ws)
-
-    def bf16_r(r):
-        x = V[r]
-        ok.oscar_bf16_decode(w.dims, B, msl_r[r], bf.pps, x["q"], bf.pages, x["bpt"], x["blens"], 0.0, x["out_bf"],
-                             ws_bf)
-
-    def step(i):
-        r = i % NR
-        append_r(r)
-        decode_r(r)
-
-    def capture(fn, n):
-        """CUDA graph of a chunk of calls fn(0..per-1), replayed n // per times (per | n, per <= 1000)."""
-        per = n if n <= 1000 else next(d for d in range(1000, 0, -1) if n % d == 0)
-        s = torch.cuda.Stream(device=dev)
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            for i in range(min(3, n)):
-                fn(i)
-        torch.cuda.current_stream().wait_stream(s)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for i in range(per):
-                fn(i)
-        return g, n // per
+    stage, per_stage, out = S.stage, S.per_stage, S.out
+    append_r, decode_r, bf16_r, step = S.append_r, S.decode_r, S.bf16_r, S.step
 
     def timed(fn, n, warm):
-        g, reps = capture(fn, n)
-        if warm > 0:
-            gw, rw = capture(fn, warm)
-            for _ in range(rw):
-                gw.replay()
-        torch.cuda.synchronize()
-        barrier()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0 = time.perf_counter()
-        e0.record()
-        for _ in range(reps):
-            g.replay()
-        e1.record()
-        e1.synchronize()
-        t1 = time.perf_counter()
-        torch.cuda.synchronize()
-        barrier()
-        ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-        return ms, (t0, t1)
+        return timed_graph(fn, n, warm, dev, world, barrier)
 
     log("caches built; timing")
     sampler = ClockSampler(local)
@@ -536,6 +619,10 @@ def run_ours(args, world, rank, local):
     d2h = B * Hq * D * 4
 
     log(f"e2e: {e2e_ms * 1e3:.2f} us/step")
+    extra = {}
+    for cfg in args.extra_configs:
+        if cfg != args.config:
+            extra[f"config{cfg}"] = extra_config_line(cfg, dev, l2, K, Wm, world, barrier)
     append_line = append_workload(dev) if rank == 0 and not args.no_append else None
     extend_line = extend_workload(dev) if rank == 0 and not args.no_extend else None
     calib_line = calibrate_workload(dev) if rank == 0 and not args.no_calibrate else None
@@ -576,6 +663,7 @@ def run_ours(args, world, rank, local):
                     "mode": "one CUDA graph per step (H2D inputs, append, decode, D2H output); two steps in flight, "
                              "the host waits for step i-2's output before launching step i"},
             "gpu_launches": K * 4,
+            **extra,
             "append_workload": append_line,
             "extend_workload": extend_line,
             "calibrate_workload": calib_line,
@@ -824,11 +912,17 @@ def main():
                     help="workload: 1 batch-1 32K (default), 2 batch-64 mixed lengths, 3 batch-4 131K")
     ap.add_argument("--replicas", type=int, default=0, help="cache replicas (0: enough to exceed 3x L2)")
     ap.add_argument("--pps", type=int, default=-1, help="pages per split for both decodes (-1: the workload's, 0: auto)")
+    ap.add_argument("--extra-configs", default="2,3",
+                    help="comma-separated workloads (2, 3) measured after the main one and reported under "
+                         "config2 / config3 of the same line ('' for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-append", action="store_true", help="skip the append throughput workload")
     ap.add_argument("--no-extend", action="store_true", help="skip the extend (chunked prefill) workload")
     ap.add_argument("--no-calibrate", action="store_true", help="skip the offline calibration workload")
     args = ap.parse_args()
+    args.extra_configs = [int(c) for c in args.extra_configs.split(",") if c.strip()]
+    if any(c not in (1, 2, 3) for c in args.extra_configs):
+        ap.error("--extra-configs takes workloads 1, 2, 3")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()

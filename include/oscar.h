@@ -264,7 +264,10 @@ oscar_status_t oscar_extend_varlen(const oscar_dims_t* dims, int32_t batch, int3
  * that loads the library holds until the process exits.
  *   - The first call on a device looks up that array's device address (a host
  *     call made once per device, with that device current); make this first call
- *     before any stream capture.
+ *     before any stream capture.  The address is remembered together with the
+ *     context it belongs to: after the device's context is destroyed and created
+ *     again (cudaDeviceReset), the next call looks it up anew, so that first call
+ *     too must come before any stream capture.
  *   - A call whose plan (see oscar_decode_workspace_bytes) needs more than
  *     OSCAR_NOALLOC_SCRATCH_BYTES returns OSCAR_ERR_WORKSPACE and launches nothing.
  *   - Every call shares the one array and it keeps the last call's contents.

@@ -417,19 +417,57 @@ extern "C" oscar_status_t oscar_bf16_decode(const oscar_dims_t* dims, int32_t ba
 // device that loads this library until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[OSCAR_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch on the current device.  The host-side name
-// is only a stand-in, so the address is looked up with cudaGetSymbolAddress once
-// per device (with that device current) and cached.
+// Identity of the calling thread's current CUDA context: cuCtxGetId of
+// cuCtxGetCurrent, reached through the runtime's driver entry points (no link
+// against the driver library).  Unlike a context handle, the id is never reused
+// within a process, so a context destroyed (cudaDeviceReset) and created again
+// gets a new one.  False when the driver offers neither call or no context is
+// current.
+static bool current_context_id(unsigned long long* id) {
+  using GetCurrentFn = int (*)(void**);
+  using GetIdFn = int (*)(void*, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(f);
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  void* ctx = nullptr;
+  if (get_current(&ctx) != 0 || ctx == nullptr) return false;
+  return get_id(ctx, id) == 0;
+}
+
+// Device address of g_noalloc_scratch in the current context.  The host-side
+// name is only a stand-in, so the address is looked up with cudaGetSymbolAddress
+// (with the device current) and cached per device together with the id of the
+// context it belongs to.  A call from another context of that device (the
+// primary context reset and created again, which may load the library's module
+// at a new address) looks it up again instead of using a stale address.
 static oscar_status_t noalloc_scratch(void** out) {
   static std::mutex mu;
   static void* cached[64] = {};
+  static unsigned long long cached_ctx[64] = {};
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return OSCAR_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
-  if (cached[dev] == nullptr) {
+  unsigned long long ctx = 0;
+  const bool have_ctx = current_context_id(&ctx);
+  if (cached[dev] == nullptr || !have_ctx || ctx != cached_ctx[dev]) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return OSCAR_ERR_CUDA;
+    // the lookup makes the device's primary context current if none was
+    if (!current_context_id(&ctx)) ctx = 0;
     cached[dev] = ptr;
+    cached_ctx[dev] = ctx;
   }
   *out = cached[dev];
   return OSCAR_OK;

@@ -113,14 +113,33 @@ def check_append(w: Workload, codes_gpu: np.ndarray, sz_gpu: np.ndarray, k: torc
     return stats
 
 
+def _threads() -> int:
+    try:
+        return max(1, min(32, len(os.sched_getaffinity(0))))
+    except AttributeError:
+        return max(1, min(32, os.cpu_count() or 1))
+
+
 def oracle_decode_on_gpu_cache(w: Workload, cache, pairs=None, q=None, seq_lens=None, sm_scale=0.0) -> np.ndarray:
+    """The oracle's decode of the GPU's cache; a list of (sequence, query head)
+    pairs is spread over host threads (the oracle call releases the GIL)."""
     codes, sz = pools_to_host(cache)
     sink = bits16(cache.sink) if cache.sink is not None else None
     win = bits16(cache.window) if cache.window is not None else None
     qb = bits16(w.q if q is None else q)
     sl = (w.seq_lens if seq_lens is None else seq_lens).cpu().numpy()
-    return O.decode(w.dims, w.batch, qb, w.R_k.cpu().numpy(), w.R_v.cpu().numpy(), codes, sz, sink, win,
-                    w.page_table.numpy(), sl, w.sink_len, w.window_len, sm_scale, pairs=pairs)
+    Rk, Rv, pt = w.R_k.cpu().numpy(), w.R_v.cpu().numpy(), w.page_table.numpy()
+
+    def run(pr):
+        return O.decode(w.dims, w.batch, qb, Rk, Rv, codes, sz, sink, win, pt, sl, w.sink_len, w.window_len,
+                        sm_scale, pairs=pr)
+    if pairs is None or len(pairs) < 2:
+        return run(pairs)
+    import concurrent.futures
+    chunks = [list(c) for c in np.array_split(np.arange(len(pairs)), min(_threads(), len(pairs))) if len(c)]
+    with concurrent.futures.ThreadPoolExecutor(len(chunks)) as ex:
+        parts = list(ex.map(lambda ix: run([pairs[i] for i in ix]), chunks))
+    return np.concatenate(parts, axis=0)
 
 
 def oracle_extend_on_gpu_cache(w: Workload, cache, q: torch.Tensor, row_seq: np.ndarray, row_pos: np.ndarray,

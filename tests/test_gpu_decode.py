@@ -38,8 +38,10 @@ def test_decode_batch64_config_sampled():
     cache = _built(w)
     out = cache.decode(w.q)
     lens = w.seq_lens.numpy()
-    bs = [int(np.argmin(lens)), int(np.argmax(lens)), 7, 33]
-    pairs = [(b, h) for b in bs for h in (0, 13, 31)]
+    # 16 sequences (the shortest, the longest and 14 drawn) x 3 query heads of different KV heads
+    rest = [int(b) for b in np.random.default_rng(2).permutation(len(lens)) if b not in (np.argmin(lens), np.argmax(lens))]
+    bs = [int(np.argmin(lens)), int(np.argmax(lens))] + rest[:14]
+    pairs = [(b, (5 * b + 11 * j) % 32) for b in bs for j in range(3)]
     compare_decode(out, oracle_decode_on_gpu_cache(w, cache, pairs=pairs), pairs=pairs)
 
 
@@ -47,7 +49,8 @@ def test_decode_131k_gqa8_config_sampled():
     w = synth.make_config(3, device="cuda")
     cache = _built(w)
     out = cache.decode(w.q)
-    pairs = [(0, 0), (1, 9), (2, 40), (3, 63)]
+    # every (sequence, KV head) once, a different query head of the GQA group each time, plus the group ends
+    pairs = [(b, 8 * h + (3 * b + h) % 8) for b in range(4) for h in range(8)] + [(0, 0), (1, 7), (2, 56), (3, 63)]
     compare_decode(out, oracle_decode_on_gpu_cache(w, cache, pairs=pairs), pairs=pairs)
 
 
