@@ -146,6 +146,25 @@ size_t oscar_decode_workspace_bytes(const oscar_dims_t* dims, int32_t batch, int
                                     int32_t pages_per_split, int32_t sink_len, int32_t window_len);
 
 /*
+ * oscar_decode_plan -- how oscar_decode (and oscar_decode_noalloc) runs a decode
+ * of these sizes; the arguments are those of oscar_decode_workspace_bytes.  No
+ * page defines this call: it reports the library's own schedule.
+ *   *fused            1: the single-wave form (head_dim 128, group 64 or 128, when
+ *                     every (sequence, KV head) gets its own CTAs in one wave of
+ *                     one CTA per SM): INT2 split CTAs that rotate the query
+ *                     themselves and un-rotate their own output, one BF16
+ *                     sink/window CTA per (sequence, KV head), then a log-sum-exp
+ *                     merge -- two kernels;
+ *                     0: the general form -- q-rotation, split and merge kernels
+ *   *splits           INT2 splits per (sequence, KV head)
+ *   *pages_per_split_used  pages per INT2 split
+ * Any output pointer may be NULL.  Invalid sizes return OSCAR_ERR_INVALID_ARG.
+ */
+oscar_status_t oscar_decode_plan(const oscar_dims_t* dims, int32_t batch, int32_t max_seq_len,
+                                 int32_t pages_per_split, int32_t sink_len, int32_t window_len, int32_t* fused,
+                                 int32_t* splits, int32_t* pages_per_split_used);
+
+/*
  * oscar_decode -- one decode step of mixed-precision paged GQA attention.
  *
  * Defined by: project card "How it works" (a BF16 sink of initial tokens and a

@@ -58,6 +58,8 @@ def _load():
         "oscar_append": (I32, [D, I64, P, P, P, P, P, P, P, P, P, P, P]),
         "oscar_append_mixed": (I32, [D, I64, P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, P, P, P, P, P]),
         "oscar_decode_workspace_bytes": (SZ, [D, I32, I32, I32, I32, I32]),
+        "oscar_decode_plan": (I32, [D, I32, I32, I32, I32, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
+                                    ctypes.POINTER(I32)]),
         "oscar_decode": (I32, [D, I32, I32, I32, P, P, P, P, P, P, P, P, P, I32, I32, F32, P, P, SZ, P]),
         "oscar_decode_noalloc": (I32, [D, I32, I32, I32, P, P, P, P, P, P, P, P, P, I32, I32, F32, P, P]),
         "oscar_extend_workspace_bytes": (SZ, [D, I32, I32, I32, I32, I32]),
@@ -160,6 +162,16 @@ def oscar_append_mixed(dims, k, v, R_k, R_v, clip_k, clip_v, page_table, slot_ma
 def oscar_decode_workspace_bytes(dims, batch, max_seq_len, pages_per_split, sink_len, window_len) -> int:
     return int(lib.oscar_decode_workspace_bytes(ctypes.byref(_dims(dims)), int(batch), int(max_seq_len),
                                                 int(pages_per_split), int(sink_len), int(window_len)))
+
+
+def oscar_decode_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len) -> dict:
+    """The decode's schedule for these sizes: {"fused": 0|1, "splits": INT2 splits per
+    (sequence, KV head), "pages_per_split": pages per INT2 split}."""
+    f, s, pps = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib.oscar_decode_plan(ctypes.byref(_dims(dims)), int(batch), int(max_seq_len), int(pages_per_split),
+                                 int(sink_len), int(window_len), ctypes.byref(f), ctypes.byref(s), ctypes.byref(pps)),
+           "oscar_decode_plan")
+    return {"fused": f.value, "splits": s.value, "pages_per_split": pps.value}
 
 
 def oscar_decode(dims, batch, max_seq_len, pages_per_split, q, R_k, R_v, int2_pages, scale_zero_pages, bf16_sink,

@@ -93,5 +93,6 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __
 oscar_status_t oscar_internal_append_errors(uint32_t* flags, int reset);
 oscar_status_t oscar_internal_decode_errors(uint32_t* flags, int reset);
 oscar_status_t oscar_internal_decode_mma_errors(uint32_t* flags, int reset);
+oscar_status_t oscar_internal_decode_fused_errors(uint32_t* flags, int reset);
 oscar_status_t oscar_internal_decode_bf16_errors(uint32_t* flags, int reset);
 oscar_status_t oscar_internal_calib_errors(uint32_t* flags, int reset);

@@ -149,6 +149,8 @@ Params base_params(const oscar_dims_t* d, int B, int max_seq_len, const Plan& pl
     p.qrot_spc = static_cast<int>(spc);
   }
   p.mma = plan.mma;
+  p.fused = plan.fused;
+  p.bulk_lo = plan.bulk_lo;
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(d->head_dim));
   p.scale_log2 = scale * 1.4426950408889634f;
   char* w = static_cast<char*>(ws);
@@ -165,9 +167,39 @@ extern "C" size_t oscar_decode_workspace_bytes(const oscar_dims_t* dims, int32_t
                                                int32_t pages_per_split, int32_t sink_len, int32_t window_len) {
   if (check_dims(dims) != OSCAR_OK) return 0;
   Plan plan;
-  if (!make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, split_ctas_per_sm(dims, kMixed), &plan)) return 0;
+  if (!make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed,
+                 split_ctas_per_sm(dims, kMixed), &plan, /*allow_fused=*/true))
+    return 0;
   return plan.total;
 }
+
+extern "C" oscar_status_t oscar_decode_plan(const oscar_dims_t* dims, int32_t batch, int32_t max_seq_len,
+                                            int32_t pages_per_split, int32_t sink_len, int32_t window_len,
+                                            int32_t* fused, int32_t* splits, int32_t* pages_per_split_used) {
+  const oscar_status_t st = check_dims(dims);
+  if (st != OSCAR_OK) return st;
+  Plan plan;
+  if (!make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed,
+                 split_ctas_per_sm(dims, kMixed), &plan, /*allow_fused=*/true))
+    return OSCAR_ERR_INVALID_ARG;
+  if (fused) *fused = plan.fused;
+  if (splits) *splits = plan.n_paged;
+  if (pages_per_split_used) *pages_per_split_used = plan.pps;
+  return OSCAR_OK;
+}
+
+namespace {
+// Workspace of the row-wise attention of the extend entry points (never the fused plan).
+size_t extend_plan_bytes(const oscar_dims_t* dims, int32_t rows, int32_t max_seq_len, int32_t pages_per_split,
+                         int32_t sink_len, int32_t window_len) {
+  if (check_dims(dims) != OSCAR_OK) return 0;
+  Plan plan;
+  if (!make_plan(dims, rows, max_seq_len, pages_per_split, sink_len, window_len, kMixed,
+                 split_ctas_per_sm(dims, kMixed), &plan))
+    return 0;
+  return plan.total;
+}
+}  // namespace
 
 namespace {
 
@@ -194,7 +226,8 @@ oscar_status_t mixed_attention(const oscar_dims_t* dims, int32_t rows, int32_t n
       misaligned16(scale_zero_pages) || misaligned16(bf16_sink) || misaligned16(bf16_window))
     return OSCAR_ERR_INVALID_ARG;
   Plan plan;
-  if (!make_plan(dims, rows, max_seq_len, pages_per_split, sink_len, window_len, kMixed, split_ctas_per_sm(dims, kMixed), &plan))
+  if (!make_plan(dims, rows, max_seq_len, pages_per_split, sink_len, window_len, kMixed,
+                 split_ctas_per_sm(dims, kMixed), &plan, /*allow_fused=*/row_seq == nullptr))
     return OSCAR_ERR_INVALID_ARG;
   if (workspace_bytes < plan.total) return OSCAR_ERR_WORKSPACE;
   if (merge_smem(dims->head_dim, plan.ns, 1, 0, kMergeThreadsSmall) > kMergeSmemLimit) return OSCAR_ERR_UNSUPPORTED;
@@ -215,6 +248,12 @@ oscar_status_t mixed_attention(const oscar_dims_t* dims, int32_t rows, int32_t n
   p.row_pos = row_pos;
   p.num_seqs = num_seqs;
   p.out = out;
+  if (p.fused) {
+    p.qfrag = nullptr;
+    p.q_rot = nullptr;
+    p.n_dense_pages = (sink_len + kPageSize - 1) / kPageSize + (window_len + kPageSize - 1) / kPageSize;
+    return int2_fused_decode(p, as_stream(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+  }
   if (!int2_mma_supported(p)) p.qfrag = nullptr;
   return run(p, kMixed, stream);
 }
@@ -287,7 +326,7 @@ cudaError_t launch_extend_tiles(Params p, int batch, cudaStream_t stream) {
 extern "C" size_t oscar_extend_varlen_workspace_bytes(const oscar_dims_t* dims, int32_t num_rows,
                                                       int32_t max_seq_len, int32_t pages_per_split,
                                                       int32_t sink_len, int32_t window_len) {
-  const size_t base = oscar_decode_workspace_bytes(dims, num_rows, max_seq_len, pages_per_split, sink_len, window_len);
+  const size_t base = extend_plan_bytes(dims, num_rows, max_seq_len, pages_per_split, sink_len, window_len);
   if (base == 0) return 0;
   return base + 2 * align_up(static_cast<size_t>(num_rows) * 4, 256);
 }
@@ -361,7 +400,7 @@ extern "C" oscar_status_t oscar_extend_varlen(const oscar_dims_t* dims, int32_t 
 
 extern "C" size_t oscar_extend_workspace_bytes(const oscar_dims_t* dims, int32_t num_rows, int32_t max_seq_len,
                                                int32_t pages_per_split, int32_t sink_len, int32_t window_len) {
-  return oscar_decode_workspace_bytes(dims, num_rows, max_seq_len, pages_per_split, sink_len, window_len);
+  return extend_plan_bytes(dims, num_rows, max_seq_len, pages_per_split, sink_len, window_len);
 }
 
 extern "C" oscar_status_t oscar_extend(const oscar_dims_t* dims, int32_t batch, int32_t num_rows,
@@ -484,7 +523,8 @@ extern "C" oscar_status_t oscar_decode_noalloc(const oscar_dims_t* dims, int32_t
   if (check_dims(dims) == OSCAR_OK && batch > 0 && max_seq_len >= 0 && pages_per_split >= 0 && sink_len >= 0 &&
       window_len >= 0) {
     Plan plan;
-    if (make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed, split_ctas_per_sm(dims, kMixed), &plan) &&
+    if (make_plan(dims, batch, max_seq_len, pages_per_split, sink_len, window_len, kMixed,
+                  split_ctas_per_sm(dims, kMixed), &plan, /*allow_fused=*/true) &&
         plan.total > OSCAR_NOALLOC_SCRATCH_BYTES)
       return OSCAR_ERR_WORKSPACE;
   }

@@ -35,6 +35,8 @@ struct Plan {
   int ns = 0;          // n_paged + n_dense
   int ml_ns = 0;       // row stride (splits) of the (m, l) partials: ns rounded up to even (16-byte rows)
   int mma = 0;         // 1: the tensor-core split kernel runs (dense splits of kDenseMmaPages pages)
+  int fused = 0;       // 1: the single-wave fused decode (decode_fused.cu) runs
+  int bulk_lo = 0;     // fused: first page of INT2 split 0 (splits cover the bulk pages only)
   size_t off_qrot = 0, off_qfrag = 0, off_po = 0, off_pml = 0, total = 0;
 };
 
@@ -47,6 +49,9 @@ struct Params {
   int qrot_spc;     // sequences per q-rotation CTA (qrot_spc * gqa <= kQrotMaxQ)
   int merge_stage;  // merge kernel: kStageRv (R_v staged before the wait) | kStagePartials
   int mma;          // 1: tensor-core split kernel (INT2 mode: head_dim 128, group 64 or 128)
+  // Fused single-wave decode (decode_fused.cu): n_paged INT2 split CTAs per unit starting
+  // at page bulk_lo, then n_dense (0 or 1) BF16 CTAs covering n_dense_pages 16-row pages.
+  int fused, bulk_lo, n_dense_pages;
   const __nv_bfloat16* q;
   const float* R_k;
   const float* R_v;
@@ -85,6 +90,11 @@ bool int2_tile_supported(const Params& p);
 cudaError_t int2_tile_split(const Params& p, cudaStream_t stream);
 bool bf16_mma_supported(const Params& p);
 cudaError_t bf16_mma_split(const Params& p, cudaStream_t stream);
+// Fused single-wave decode (decode_fused.cu).
+bool int2_fused_shape(int D, int G, int gqa);
+int int2_fused_max_pps();
+int int2_fused_ctas_per_sm(int gqa, int G);
+cudaError_t int2_fused_decode(const Params& p, cudaStream_t stream);
 
 // Launches `kernel` with programmatic stream serialisation: it may overlap the
 // tail of the preceding kernel in the stream and must call grid_dep_wait()
@@ -125,10 +135,49 @@ int dense_splits(int S, int W, int max_seq_len, bool mma) {
 // (ctas_per_sm x SMs, the sink/window splits counted), 4..128 pages per split.
 // The tensor-core split kernels cover head_dim 128 (INT2: group 64 or 128) and
 // splits of at most kMmaMaxPps pages.
+// Fused single-wave plan of a decode (no extend rows): unit (sequence, KV head) u
+// gets n_s INT2 split CTAs over its bulk pages [S/16, ceil(max(S, max_seq_len - W)/16))
+// and one BF16 CTA when S + W > 0; used when every unit's CTAs fit one wave of the
+// fused kernel (about one CTA per SM) and a split's page ids fit its table.
+bool make_fused_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req, int S, int W, Plan* p) {
+  const int gqa = d->num_q_heads / d->num_kv_heads;
+  if (B <= 0 || !int2_fused_shape(d->head_dim, d->group_size, gqa)) return false;
+  const long long units = static_cast<long long>(B) * d->num_kv_heads;
+  const long long slots = static_cast<long long>(int2_fused_ctas_per_sm(gqa, d->group_size)) * num_sms();
+  const int n_d = S + W > 0 ? 1 : 0;
+  const int bulk_lo = S / kPageSize;
+  const int bulk_hi = ((S > max_seq_len - W ? S : max_seq_len - W) + kPageSize - 1) / kPageSize;
+  const int nb = bulk_hi > bulk_lo ? bulk_hi - bulk_lo : 0;
+  int pps = pps_req;
+  if (pps == 0) {
+    long long n_s = slots / units - n_d;
+    if (n_s < 1) return false;
+    pps = static_cast<int>((nb + n_s - 1) / n_s);
+    if (pps < 1) pps = 1;
+  }
+  const int n_s = nb > 0 ? (nb + pps - 1) / pps : 1;
+  if (pps > int2_fused_max_pps() || units * (n_s + n_d) > slots) return false;
+  p->fused = 1;
+  p->mma = 1;
+  p->bulk_lo = bulk_lo;
+  p->pps = pps;
+  p->n_paged = n_s;
+  p->n_dense = n_d;
+  p->ns = n_s + n_d;
+  p->ml_ns = (p->ns + 1) & ~1;
+  const size_t bh = static_cast<size_t>(B) * d->num_q_heads;
+  p->off_qrot = p->off_qfrag = p->off_po = 0;
+  p->off_pml = align_up(bh * p->ns * d->head_dim * sizeof(float), 256);
+  p->total = p->off_pml + align_up(bh * p->ml_ns * 2 * sizeof(float), 256);
+  return true;
+}
+
 bool make_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req, int S, int W, Mode mode, int ctas_per_sm,
-               Plan* p) {
+               Plan* p, bool allow_fused = false) {
   if (B < 0 || max_seq_len < 0 || pps_req < 0 || S < 0 || W < 0) return false;
   if (max_seq_len > d->max_pages_per_seq * kPageSize) return false;
+  *p = Plan{};
+  if (allow_fused && mode == kMixed && make_fused_plan(d, B, max_seq_len, pps_req, S, W, p)) return true;
   const int max_pages = (max_seq_len + kPageSize - 1) / kPageSize;
   const bool shape_mma = d->head_dim == 128 && (mode == kBf16Paged || d->group_size == 64 || d->group_size == 128);
   p->n_dense = mode == kMixed ? dense_splits(S, W, max_seq_len, shape_mma) : 0;
