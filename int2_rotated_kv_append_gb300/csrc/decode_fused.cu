@@ -281,20 +281,20 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
   };
   for (int i0 = 0; i0 < min(n_my, kStages); i0 += 16) issue(i0, min(min(n_my, kStages), i0 + 16));
 
-  float m_run[NT], l_run[NT], zacc[NT][NG], O[NT][8][4];
+  float m_run[NT], O[NT][8][4];
+  float2 l2[NT], z2[NT][NG];  // per token slot (g, g + 8) of the page body
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     m_run[nt] = -INFINITY;
-    l_run[nt] = 0.f;
+    l2[nt] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = 0.f;
+    for (int gg = 0; gg < NG; ++gg) z2[nt][gg] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int mi = 0; mi < 8; ++mi)
 #pragma unroll
       for (int c = 0; c < 4; ++c) O[nt][mi][c] = 0.f;
   }
   const uint32_t vsel = (2 * (g & 1)) | ((2 * (g & 1) + 1) << 4) | ((4 + 2 * (g & 1)) << 8) | ((5 + 2 * (g & 1)) << 12);
-  const int src1 = 4 * t + (g >> 1), src2 = src1 + 16;
   auto wait_page = [&](int k) {
     return mbar_wait_bounded(smem_u32(&my_bars[k % kStages]), (k / kStages) & 1);
   };
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
       bool t2[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) t2[nt][0] = t2[nt][1] = true;
-      int2_pages<NT, NG, 2, true>(st2, g, t, t2, t2, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
+      int2_pages<NT, NG, 2, true>(st2, g, t, t2, t2, vsel, bq, F, qs, m_run, l2, z2, O);
     } else {
       const bool b00 = token_ok(i, g), b01 = token_ok(i + 1, g), b10 = token_ok(i, g + 8), b11 = token_ok(i + 1, g + 8);
       bool a0[NT][2], a1[NT][2];
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
         a1[nt][0] = b10;
         a1[nt][1] = b11;
       }
-      int2_pages<NT, NG, 2, false>(st2, g, t, a0, a1, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
+      int2_pages<NT, NG, 2, false>(st2, g, t, a0, a1, vsel, bq, F, qs, m_run, l2, z2, O);
     }
     if (i + kStages < n_my) {  // refill the two stages just consumed
       __syncwarp();
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
         a0[nt][0] = b0;
         a1[nt][0] = b1;
       }
-      int2_pages<NT, NG, 1, false>(st1, g, t, a0, a1, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
+      int2_pages<NT, NG, 1, false>(st1, g, t, a0, a1, vsel, bq, F, qs, m_run, l2, z2, O);
       ++i;
     }
   }
@@ -364,9 +364,9 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       m_run[nt] = -INFINITY;
-      l_run[nt] = 0.f;
+      l2[nt] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = 0.f;
+      for (int gg = 0; gg < NG; ++gg) z2[nt][gg] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int mi = 0; mi < 8; ++mi)
 #pragma unroll
@@ -375,8 +375,12 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
   }
 
   // ---- warp totals, then a log-sum-exp merge of the NW warps ----
+  float l_run[NT], zacc[NT][NG];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
+    l_run[nt] = l2[nt].x + l2[nt].y;
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = z2[nt][gg].x + z2[nt][gg].y;
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], off);

@@ -202,20 +202,20 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
     }
   }
   // ---- main loop over this warp's pages ----
-  float m_run[NT], l_run[NT], zacc[NT][NG], O[NT][8][4];
+  float m_run[NT], O[NT][8][4];
+  float2 l2[NT], z2[NT][NG];  // per token slot (g, g + 8) of the page body
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     m_run[nt] = -INFINITY;
-    l_run[nt] = 0.f;
+    l2[nt] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = 0.f;
+    for (int gg = 0; gg < NG; ++gg) z2[nt][gg] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int mi = 0; mi < 8; ++mi)
 #pragma unroll
       for (int c = 0; c < 4; ++c) O[nt][mi][c] = 0.f;
   }
   const uint32_t vsel = (2 * (g & 1)) | ((2 * (g & 1) + 1) << 4) | ((4 + 2 * (g & 1)) << 8) | ((5 + 2 * (g & 1)) << 12);
-  const int src1 = 4 * t + (g >> 1), src2 = src1 + 16;
   int i = 0;
   // Stage of local page k: k % kStages (kStages even: a pair never wraps).
   auto wait_page = [&](int k) {
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
       bool t2[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) t2[nt][0] = t2[nt][1] = true;
-      int2_pages<NT, NG, 2, true>(st2, g, t, t2, t2, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
+      int2_pages<NT, NG, 2, true>(st2, g, t, t2, t2, vsel, bq, F, qs, m_run, l2, z2, O);
     } else {
       const bool b00 = token_ok(i, g), b01 = token_ok(i + 1, g), b10 = token_ok(i, g + 8), b11 = token_ok(i + 1, g + 8);
       bool a0[NT][2], a1[NT][2];
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
         a1[nt][0] = b10;
         a1[nt][1] = b11;
       }
-      int2_pages<NT, NG, 2, false>(st2, g, t, a0, a1, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
+      int2_pages<NT, NG, 2, false>(st2, g, t, a0, a1, vsel, bq, F, qs, m_run, l2, z2, O);
     }
     __syncwarp();
     issue(min(n_my, i + kStages), min(n_my, i + 2 + kStages));
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
         a0[nt][0] = b0;
         a1[nt][0] = b1;
       }
-      int2_pages<NT, NG, 1, false>(st1, g, t, a0, a1, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
+      int2_pages<NT, NG, 1, false>(st1, g, t, a0, a1, vsel, bq, F, qs, m_run, l2, z2, O);
       ++i;
     }
   }
@@ -283,9 +283,9 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       m_run[nt] = -INFINITY;
-      l_run[nt] = 0.f;
+      l2[nt] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = 0.f;
+      for (int gg = 0; gg < NG; ++gg) z2[nt][gg] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int mi = 0; mi < 8; ++mi)
 #pragma unroll
@@ -294,8 +294,12 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   }
 
   // ---- warp totals, then a log-sum-exp merge of the 4 warps ----
+  float l_run[NT], zacc[NT][NG];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
+    l_run[nt] = l2[nt].x + l2[nt].y;
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = z2[nt][gg].x + z2[nt][gg].y;
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], off);
@@ -469,20 +473,20 @@ __global__ void __launch_bounds__(kTileWarps * 32, 1) int2_tile_split_kernel(Par
       qs[nt][0] = (c[0] + c[1]) + (c[2] + c[3]);
     }
   }
-  float m_run[NT], l_run[NT], zacc[NT][NG], O[NT][8][4];
+  float m_run[NT], O[NT][8][4];
+  float2 l2[NT], z2[NT][NG];  // per token slot (g, g + 8) of the page body
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     m_run[nt] = -INFINITY;
-    l_run[nt] = 0.f;
+    l2[nt] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = 0.f;
+    for (int gg = 0; gg < NG; ++gg) z2[nt][gg] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int mi = 0; mi < 8; ++mi)
 #pragma unroll
       for (int c = 0; c < 4; ++c) O[nt][mi][c] = 0.f;
   }
   const uint32_t vsel = (2 * (g & 1)) | ((2 * (g & 1) + 1) << 4) | ((4 + 2 * (g & 1)) << 8) | ((5 + 2 * (g & 1)) << 12);
-  const int src1 = 4 * t + (g >> 1), src2 = src1 + 16;
   // the smallest bound over the warp's valid columns: pages below it need no masks
   int r1_min = r1_tile;
 #pragma unroll
@@ -522,7 +526,7 @@ __global__ void __launch_bounds__(kTileWarps * 32, 1) int2_tile_split_kernel(Par
       bool t2[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) t2[nt][0] = t2[nt][1] = true;
-      int2_pages<NT, NG, 2, true>(st2, g, t, t2, t2, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
+      int2_pages<NT, NG, 2, true>(st2, g, t, t2, t2, vsel, bq, F, qs, m_run, l2, z2, O);
     } else {
       bool a0[NT][2], a1[NT][2];
 #pragma unroll
@@ -534,7 +538,7 @@ __global__ void __launch_bounds__(kTileWarps * 32, 1) int2_tile_split_kernel(Par
           a0[nt][pg] = ok && valid[nt] && pos0 >= r0 && pos0 < r1[nt];
           a1[nt][pg] = ok && valid[nt] && pos1 >= r0 && pos1 < r1[nt];
         }
-      int2_pages<NT, NG, 2, false>(st2, g, t, a0, a1, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
+      int2_pages<NT, NG, 2, false>(st2, g, t, a0, a1, vsel, bq, F, qs, m_run, l2, z2, O);
     }
     release(i);
     release(i + 1);
@@ -552,7 +556,7 @@ __global__ void __launch_bounds__(kTileWarps * 32, 1) int2_tile_split_kernel(Par
         a0[nt][0] = ok && valid[nt] && base + g >= r0 && base + g < r1[nt];
         a1[nt][0] = ok && valid[nt] && base + g + 8 >= r0 && base + g + 8 < r1[nt];
       }
-      int2_pages<NT, NG, 1, false>(st1, g, t, a0, a1, vsel, src1, src2, bq, F, qs, m_run, l_run, zacc, O);
+      int2_pages<NT, NG, 1, false>(st1, g, t, a0, a1, vsel, bq, F, qs, m_run, l2, z2, O);
       release(i);
       ++i;
     }
@@ -562,9 +566,9 @@ __global__ void __launch_bounds__(kTileWarps * 32, 1) int2_tile_split_kernel(Par
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       m_run[nt] = -INFINITY;
-      l_run[nt] = 0.f;
+      l2[nt] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = 0.f;
+      for (int gg = 0; gg < NG; ++gg) z2[nt][gg] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int mi = 0; mi < 8; ++mi)
 #pragma unroll
@@ -573,8 +577,12 @@ __global__ void __launch_bounds__(kTileWarps * 32, 1) int2_tile_split_kernel(Par
   }
   // ---- this warp's partials, one per column (no merge across warps: each warp
   // owns its columns)
+  float l_run[NT], zacc[NT][NG];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
+    l_run[nt] = l2[nt].x + l2[nt].y;
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = z2[nt][gg].x + z2[nt][gg].y;
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], off);

@@ -69,16 +69,22 @@ __device__ __forceinline__ float2 lds_h2f(uint32_t addr) {
 // memory.  FULL: every token of the pages is in range (no per-token masking);
 // otherwise v0[k] / v1[k] say whether this thread's tokens g and g + 8 of page k
 // are.
+// A lane's softmax values come in pairs (token g, token g + 8) and are computed as
+// packed fp32 pairs.  The PV B operand P' = p * scale of a lane's column (query
+// g/2, fp16 part g%2) and tokens 2t, 2t+1 / 2t+8, 2t+9 is the transpose of the
+// (token, hi|lo) values the lane holds for query t: one movmatrix per 8 tokens.
+// The running sums l_run and the zero terms zacc are kept per token slot of the
+// pair and added by the caller at the end.
 template <int NT, int NG, int NP, bool FULL>
 __device__ __forceinline__ void int2_pages(const uint32_t (&st)[NP], int g, int t, const bool (&v0)[NT][NP],
-                                           const bool (&v1)[NT][NP], uint32_t vsel, int src1, int src2,
-                                           const uint32_t (&bq)[NT][8][2], const float (&F)[NT],
-                                           const float (&qs)[NT][NG], float (&m_run)[NT], float (&l_run)[NT],
-                                           float (&zacc)[NT][NG], float (&O)[NT][8][4]) {
+                                           const bool (&v1)[NT][NP], uint32_t vsel, const uint32_t (&bq)[NT][8][2],
+                                           const float (&F)[NT], const float (&qs)[NT][NG], float (&m_run)[NT],
+                                           float2 (&l_run)[NT], float2 (&zacc)[NT][NG], float (&O)[NT][8][4]) {
   // K words t and t + 4 of tokens g and g + 8; V words g/2 and 4 + g/2 of tokens
-  // t, t + 8 (xa) and t + 4, t + 12 (xb); (scale, zero) of K and V for tokens g, g + 8
+  // 2t, 2t + 1 (xa) and 2t + 8, 2t + 9 (xb); (scale, zero) pairs of K and V for
+  // tokens (g, g + 8) per group
   uint32_t kw[NP][4], xa[NP][2], xb[NP][2];
-  float2 k0[NP][NG], k1[NP][NG], w0[NP][NG], w1[NP][NG];
+  float2 sk[NP][NG], zk[NP][NG], sv[NP][NG], zv[NP][NG];
 #pragma unroll
   for (int pg = 0; pg < NP; ++pg) {
     const uint32_t kp = st[pg] + g * 32 + 4 * t;
@@ -86,18 +92,20 @@ __device__ __forceinline__ void int2_pages(const uint32_t (&st)[NP], int g, int 
     kw[pg][1] = lds32(kp + 16);
     kw[pg][2] = lds32(kp + 256);
     kw[pg][3] = lds32(kp + 272);
-    const uint32_t vp = st[pg] + 512 + t * 32 + 4 * (g >> 1);
-    xa[pg][0] = __byte_perm(lds32(vp), lds32(vp + 256), vsel);
-    xa[pg][1] = __byte_perm(lds32(vp + 16), lds32(vp + 272), vsel);
-    xb[pg][0] = __byte_perm(lds32(vp + 128), lds32(vp + 384), vsel);
-    xb[pg][1] = __byte_perm(lds32(vp + 144), lds32(vp + 400), vsel);
+    const uint32_t vp = st[pg] + 512 + t * 64 + 4 * (g >> 1);
+    xa[pg][0] = __byte_perm(lds32(vp), lds32(vp + 32), vsel);
+    xa[pg][1] = __byte_perm(lds32(vp + 16), lds32(vp + 48), vsel);
+    xb[pg][0] = __byte_perm(lds32(vp + 256), lds32(vp + 288), vsel);
+    xb[pg][1] = __byte_perm(lds32(vp + 272), lds32(vp + 304), vsel);
     const uint32_t sp = st[pg] + kCodeBytes + g * NG * 4;
 #pragma unroll
     for (int gg = 0; gg < NG; ++gg) {
-      k0[pg][gg] = lds_h2f(sp + 4 * gg);
-      k1[pg][gg] = lds_h2f(sp + 32 * NG + 4 * gg);
-      w0[pg][gg] = lds_h2f(sp + 64 * NG + 4 * gg);
-      w1[pg][gg] = lds_h2f(sp + 96 * NG + 4 * gg);
+      const float2 kg = lds_h2f(sp + 4 * gg), kh = lds_h2f(sp + 32 * NG + 4 * gg);
+      const float2 vg = lds_h2f(sp + 64 * NG + 4 * gg), vh = lds_h2f(sp + 96 * NG + 4 * gg);
+      sk[pg][gg] = make_float2(kg.x, kh.x);
+      zk[pg][gg] = make_float2(kg.y, kh.y);
+      sv[pg][gg] = make_float2(vg.x, vh.x);
+      zv[pg][gg] = make_float2(vg.y, vh.y);
     }
   }
 
@@ -132,33 +140,38 @@ __device__ __forceinline__ void int2_pages(const uint32_t (&st)[NP], int g, int 
 
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    float sc0[NP], sc1[NP];
-    float mx = -INFINITY;
+    // logits of tokens (g, g + 8): F * sum_g scale_g * acc_g + sum_g zero_g * qsum_g
+    float2 sc[NP];
 #pragma unroll
     for (int pg = 0; pg < NP; ++pg) {
-      float a0 = 0.f, a1 = 0.f;
+      float2 A[NG];
 #pragma unroll
-      for (int gg = 0; gg < NG; ++gg) {
-        a0 = fmaf(k0[pg][gg].x * F[nt], acc[pg][nt][gg][0] + acc[pg][nt][gg][1], fmaf(k0[pg][gg].y, qs[nt][gg], a0));
-        a1 = fmaf(k1[pg][gg].x * F[nt], acc[pg][nt][gg][2] + acc[pg][nt][gg][3], fmaf(k1[pg][gg].y, qs[nt][gg], a1));
+      for (int gg = 0; gg < NG; ++gg)
+        A[gg] = make_float2(acc[pg][nt][gg][0] + acc[pg][nt][gg][1], acc[pg][nt][gg][2] + acc[pg][nt][gg][3]);
+      float2 X = f2mul(sk[pg][0], A[0]);
+      float2 Z = f2mul(zk[pg][0], make_float2(qs[nt][0], qs[nt][0]));
+      if (NG == 2) {
+        X = f2fma(sk[pg][NG - 1], A[NG - 1], X);
+        Z = f2fma(zk[pg][NG - 1], make_float2(qs[nt][NG - 1], qs[nt][NG - 1]), Z);
       }
+      float2 a = f2fma(make_float2(F[nt], F[nt]), X, Z);
       if (!FULL) {
-        a0 = v0[nt][pg] ? a0 : -INFINITY;
-        a1 = v1[nt][pg] ? a1 : -INFINITY;
+        a.x = v0[nt][pg] ? a.x : -INFINITY;
+        a.y = v1[nt][pg] ? a.y : -INFINITY;
       }
-      sc0[pg] = a0;
-      sc1[pg] = a1;
-      mx = fmaxf(mx, fmaxf(a0, a1));
+      sc[pg] = a;
     }
+    float mx = NP == 2 ? fmaxf(fmax3(sc[0].x, sc[0].y, sc[NP - 1].x), sc[NP - 1].y) : fmaxf(sc[0].x, sc[0].y);
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
     const float m_new = fmaxf(m_run[nt], mx);
     if (__any_sync(0xffffffffu, m_new > m_run[nt])) {
       const float alpha = m_run[nt] == -INFINITY ? 0.f : fast_exp2(m_run[nt] - m_new);
-      l_run[nt] *= alpha;
+      const float2 al = make_float2(alpha, alpha);
+      l_run[nt] = f2mul(l_run[nt], al);
 #pragma unroll
-      for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] *= alpha;
+      for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = f2mul(zacc[nt][gg], al);
 #pragma unroll
       for (int mi = 0; mi < 8; ++mi)
 #pragma unroll
@@ -167,31 +180,33 @@ __device__ __forceinline__ void int2_pages(const uint32_t (&st)[NP], int g, int 
     }
 #pragma unroll
     for (int pg = 0; pg < NP; ++pg) {
-      float p0 = fast_exp2(sc0[pg] - m_new), p1 = fast_exp2(sc1[pg] - m_new);
+      float2 pr = f2sub(sc[pg], make_float2(m_new, m_new));
+      pr.x = fast_exp2(pr.x);
+      pr.y = fast_exp2(pr.y);
       if (!FULL) {
-        p0 = v0[nt][pg] ? p0 : 0.f;
-        p1 = v1[nt][pg] ? p1 : 0.f;
+        pr.x = v0[nt][pg] ? pr.x : 0.f;
+        pr.y = v1[nt][pg] ? pr.y : 0.f;
       }
-      l_run[nt] += p0 + p1;
+      l_run[nt] = f2add(l_run[nt], pr);
       uint32_t bp[NG][2];
 #pragma unroll
       for (int gg = 0; gg < NG; ++gg) {
-        float q0 = p0 * w0[pg][gg].x, q1 = p1 * w1[pg][gg].x;
-        float z0 = p0 * w0[pg][gg].y, z1 = p1 * w1[pg][gg].y;
-        if (!FULL) {  // masked tokens may hold any bits: never multiply them in
-          q0 = v0[nt][pg] ? q0 : 0.f;
-          q1 = v1[nt][pg] ? q1 : 0.f;
-          z0 = v0[nt][pg] ? z0 : 0.f;
-          z1 = v1[nt][pg] ? z1 : 0.f;
+        float2 q = f2mul(pr, sv[pg][gg]);
+        if (FULL) {
+          zacc[nt][gg] = f2fma(pr, zv[pg][gg], zacc[nt][gg]);
+        } else {  // masked tokens may hold any bits: never multiply them in
+          float2 z = f2mul(pr, zv[pg][gg]);
+          q.x = v0[nt][pg] ? q.x : 0.f;
+          q.y = v1[nt][pg] ? q.y : 0.f;
+          z.x = v0[nt][pg] ? z.x : 0.f;
+          z.y = v1[nt][pg] ? z.y : 0.f;
+          zacc[nt][gg] = f2add(zacc[nt][gg], z);
         }
-        zacc[nt][gg] += z0 + z1;
-        const __half2 hi = __floats2half2_rn(q0, q1);
-        const float2 hf = __half22float2(hi);
-        const uint32_t xhi = h2_bits(hi), xlo = h2_bits(__floats2half2_rn(q0 - hf.x, q1 - hf.y));
-        const uint32_t h_1 = __shfl_sync(0xffffffffu, xhi, src1), l_1 = __shfl_sync(0xffffffffu, xlo, src1);
-        const uint32_t h_2 = __shfl_sync(0xffffffffu, xhi, src2), l_2 = __shfl_sync(0xffffffffu, xlo, src2);
-        bp[gg][0] = (g & 1) ? l_1 : h_1;
-        bp[gg][1] = (g & 1) ? l_2 : h_2;
+        // fp16 hi + lo of each weight, (hi, lo) of a token in one register
+        const float2 hf = __half22float2(__floats2half2_rn(q.x, q.y));
+        const float2 d = f2sub(q, hf);
+        bp[gg][0] = movmatrix_trans(h2_bits(__floats2half2_rn(hf.x, d.x)));
+        bp[gg][1] = movmatrix_trans(h2_bits(__floats2half2_rn(hf.y, d.y)));
       }
       // PV: m-tile mi covers channels 16*word + 8*(g&1) + 2*(mi&3) + {0 (row g), 1 (row g+8)},
       // word = g/2 for mi < 4 and 4 + g/2 for mi >= 4.

@@ -53,18 +53,27 @@ def test_extend_matches_oracle(D, G, Hq, H, lens, S, W, chunk):
 
 
 def test_extend_last_rows_equal_decode():
-    # one row per sequence at position L - 1 with the decode's queries: the same
-    # plan and kernels, so the same outputs bit for bit
+    # one row per sequence at position L - 1 with the decode's queries.  With one-page
+    # splits the decode takes the general form, the extend's plan and kernels: the same
+    # outputs bit for bit.  With the automatic split the decode runs the single-wave
+    # form (another summation order): equal within the split-size invariance bound.
     w = synth.make_workload(num_q_heads=8, num_kv_heads=2, head_dim=128, group_size=64, sink_len=8, window_len=24,
                             seq_lens=[70, 300, 45, 1200], seed=5)
-    cache = Int2Cache(w)
-    cache.prefill()
-    dec = cache.decode(w.q.cuda())
     rs = torch.arange(w.batch, dtype=torch.int32).cuda()
     rp = (w.seq_lens - 1).to(torch.int32).cuda()
+    cache = Int2Cache(w, pages_per_split=1)
+    cache.prefill()
+    assert ok.oscar_decode_plan(w.dims, w.batch, w.max_seq_len, 1, w.sink_len, w.window_len)["fused"] == 0
+    dec = cache.decode(w.q.cuda())
     ext = cache.extend(w.q.cuda(), rs, rp)
     torch.cuda.synchronize()
     assert torch.equal(dec, ext)
+    auto = Int2Cache(w, pages_per_split=0)
+    auto.int2_pages, auto.scale_zero, auto.sink, auto.window = cache.int2_pages, cache.scale_zero, cache.sink, cache.window
+    assert ok.oscar_decode_plan(w.dims, w.batch, w.max_seq_len, 0, w.sink_len, w.window_len)["fused"] == 1
+    dec_fused = auto.decode(w.q.cuda())
+    torch.cuda.synchronize()
+    assert torch.max(torch.abs(dec_fused - ext)).item() <= 1e-4
 
 
 def test_extend_bad_rows_attend_nothing_and_are_flagged():
