@@ -249,7 +249,6 @@ oscar_status_t mixed_attention(const oscar_dims_t* dims, int32_t rows, int32_t n
   p.num_seqs = num_seqs;
   p.out = out;
   if (p.fused) {
-    p.qfrag = nullptr;
     p.q_rot = nullptr;
     p.n_dense_pages = (sink_len + kPageSize - 1) / kPageSize + (window_len + kPageSize - 1) / kPageSize;
     return int2_fused_decode(p, as_stream(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;

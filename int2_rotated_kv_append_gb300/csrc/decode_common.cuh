@@ -166,8 +166,10 @@ bool make_fused_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req,
   p->ns = n_s + n_d;
   p->ml_ns = (p->ns + 1) & ~1;
   const size_t bh = static_cast<size_t>(B) * d->num_q_heads;
-  p->off_qrot = p->off_qfrag = p->off_po = 0;
-  p->off_pml = align_up(bh * p->ns * d->head_dim * sizeof(float), 256);
+  p->off_qrot = 0;
+  p->off_qfrag = 0;  // the q-rotation's QK operand blocks, kQfragBytes per (sequence, KV head)
+  p->off_po = align_up(static_cast<size_t>(B) * d->num_kv_heads * kQfragBytes, 256);
+  p->off_pml = p->off_po + align_up(bh * p->ns * d->head_dim * sizeof(float), 256);
   p->total = p->off_pml + align_up(bh * p->ml_ns * 2 * sizeof(float), 256);
   return true;
 }
@@ -373,7 +375,8 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(Params p) {
     const int qq = idx / 32, c = idx % 32;
     const float tot = ((part[0][qq][c] + part[1][qq][c]) + part[2][qq][c]) + part[3][qq][c];
     const int j = qq / gqa, qi = qq % gqa;
-    p.q_rot[((static_cast<size_t>(b0 + j) * p.Hq + static_cast<size_t>(h) * gqa + qi)) * D + 32 * cb + c] = tot;
+    if (p.q_rot != nullptr)  // the fp32 rotated queries are kept only for the CUDA-core split body
+      p.q_rot[((static_cast<size_t>(b0 + j) * p.Hq + static_cast<size_t>(h) * gqa + qi)) * D + 32 * cb + c] = tot;
     qrb[qq][c] = tot;
   }
   if (p.qfrag == nullptr) {

@@ -45,23 +45,18 @@ struct FusedGeo {
   static constexpr int kStages = fused_stages<NG, NW>();
   static constexpr int kStageBytes = PageGeo<NG>::kStageBytes;
   static constexpr int kSzBytes = PageGeo<NG>::kSzBytes;
-  // Area 0, reused in turn: (a) the prologue's R_k, q, q_rot, operand words and
-  // q-rotation partial sums; (b) the page ring; (c) the warps' states after the loop;
-  // (d) for the BF16 CTA, one 16-row stage per warp and its barriers.
-  static constexpr size_t kPrRk = 0;
-  static constexpr size_t kPrQ = kPrRk + kRBytes;                        // q fp32 [8][D]
-  static constexpr size_t kPrQrot = kPrQ + kMaxGqa * kD * 4;             // q . R_k fp32 [8][D]
-  static constexpr size_t kPrFrag = kPrQrot + kMaxGqa * kD * 4;          // [32 lanes][kFragWords]
-  static constexpr size_t kPrPart = kPrFrag + 32 * kFragWords * 4;       // [RG][8][D]
-  static constexpr size_t kPrologue = kPrPart + static_cast<size_t>(kThreads / kD) * kMaxGqa * kD * 4;
+  // Area 0, reused in turn: (a) the page ring; (b) the warps' states after the loop;
+  // (c) for the BF16 CTA, one 16-row stage per warp and its barriers.
   static constexpr size_t kRing = static_cast<size_t>(NW) * kStages * kStageBytes;
   static constexpr size_t kWarpState = static_cast<size_t>(NW) * kMaxGqa * (2 + kOwPitch) * 4 + 4 * NT * kD * 4;
   static constexpr size_t kDense = static_cast<size_t>(NW) * bf16pg::kStageBytes + NW * 8;
-  static constexpr size_t kArea0 = cmax(cmax(kPrologue, kRing), cmax(kWarpState, kDense));
-  static constexpr size_t kOffMisc = (kArea0 + 127) / 128 * 128;  // exponents, group sums, (M, l)
+  static constexpr size_t kArea0 = cmax(kRing, cmax(kWarpState, kDense));
+  // The q-rotation's QK operand block of the unit (kQfragBytes), in use while the ring fills.
+  static constexpr size_t kOffFrag = (kArea0 + 127) / 128 * 128;
+  static constexpr size_t kOffMisc = kOffFrag + kQfragBytes;
   static constexpr size_t kOffPid = kOffMisc + 64 * 4;              // page ids [kFMaxPps]
-  static constexpr size_t kOffBars = kOffPid + kFMaxPps * 4;        // NW * kStages ring barriers + R barrier
-  static constexpr size_t kSmem = kOffBars + (NW * kStages + 2) * 8;
+  static constexpr size_t kOffBars = kOffPid + kFMaxPps * 4;        // NW * kStages ring barriers
+  static constexpr size_t kSmem = kOffBars + (NW * kStages + 1) * 8;  // + the operand block's barrier
 };
 
 // INT2 split CTA s < n_paged of unit (b, h), or the unit's BF16 CTA (s == n_paged).
@@ -81,19 +76,13 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int gqa = p.gqa;
-  float* Rs = reinterpret_cast<float*>(smem + Geo::kPrRk);
-  float* qf = reinterpret_cast<float*>(smem + Geo::kPrQ);
-  float* qr = reinterpret_cast<float*>(smem + Geo::kPrQrot);
-  uint32_t* frag = reinterpret_cast<uint32_t*>(smem + Geo::kPrFrag);
-  float* part = reinterpret_cast<float*>(smem + Geo::kPrPart);
+  const uint32_t* frag = reinterpret_cast<const uint32_t*>(smem + Geo::kOffFrag);
   float* misc = reinterpret_cast<float*>(smem + Geo::kOffMisc);
-  int* Ei = reinterpret_cast<int*>(misc);  // [8] fp16 exponents of the QK operands
-  float* qsum = misc + 8;                  // [8][2] group sums of q_rot (log2 units)
-  float* Ms = misc + 24;                   // [8] CTA maximum per query
-  float* Ls = misc + 32;                   // [8] CTA sum per query
+  float* Ms = misc + 24;  // [8] CTA maximum per query
+  float* Ls = misc + 32;  // [8] CTA sum per query
   int* pids = reinterpret_cast<int*>(smem + Geo::kOffPid);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo::kOffBars);
-  const uint32_t rbar = smem_u32(&bars[NW * kStages]);
+  const uint32_t fbar = smem_u32(&bars[NW * kStages]);
   const size_t bh0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(h) * gqa;
 
   if (tid == 0) {
@@ -101,134 +90,14 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
     mbar_init_fence();
   }
   __syncthreads();
-
-  // ---- prologue: q . R_k[h] and the QK operands (reads q and R_k only) ----
-  if (tid == 0) {
-    mbar_arrive_expect_tx(rbar, kRBytes);
-    const char* src = reinterpret_cast<const char*>(p.R_k + static_cast<size_t>(h) * kD * kD);
-    for (int c = 0; c < 4; ++c) bulk_g2s(smem_u32(Rs) + c * (kRBytes / 4), src + c * (kRBytes / 4), kRBytes / 4, rbar);
-  }
-  for (int i = tid; i < gqa * kD / 8; i += T) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.q + bh0 * kD) + i);
-    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      qf[8 * i + 2 * e] = __uint_as_float(wv[e] << 16);
-      qf[8 * i + 2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
-    }
-  }
-  const bool rk_ok = __syncthreads_and(mbar_wait_bounded(rbar, 0));
-  if (!rk_ok) {  // R_k never arrived: record it, let the copy land (bounded), contribute nothing
-    if (tid == 0) {
-      record_error(OSCAR_DEVERR_TIMEOUT);
-      mbar_wait_bounded(rbar, 0);
-    }
-    grid_dep_launch_dependents();
-    grid_dep_wait();
-    if (tid < gqa) {
-      p.part_ml[((bh0 + tid) * p.ml_ns + s) * 2 + 0] = -INFINITY;
-      p.part_ml[((bh0 + tid) * p.ml_ns + s) * 2 + 1] = 0.f;
-    }
-    return;
-  }
-  {
-    // thread (column c, row group rg) sums rows [rg * D / RG, (rg + 1) * D / RG) for every query
-    constexpr int RG = T / kD, kRows = kD / RG;
-    const int c = tid % kD, rg = tid / kD;
-    float acc[kQ];
-#pragma unroll
-    for (int qi = 0; qi < kQ; ++qi) acc[qi] = 0.f;
-#pragma unroll 1
-    for (int i = rg * kRows; i < (rg + 1) * kRows; i += 4) {
-      const float r0 = Rs[i * kD + c], r1 = Rs[(i + 1) * kD + c], r2 = Rs[(i + 2) * kD + c], r3 = Rs[(i + 3) * kD + c];
-#pragma unroll
-      for (int qi = 0; qi < kQ; ++qi) {
-        const float4 qv = *reinterpret_cast<const float4*>(&qf[qi * kD + i]);
-        acc[qi] = fmaf(qv.w, r3, fmaf(qv.z, r2, fmaf(qv.y, r1, fmaf(qv.x, r0, acc[qi]))));
-      }
-    }
-#pragma unroll
-    for (int qi = 0; qi < kQ; ++qi) part[(rg * kMaxGqa + qi) * kD + c] = acc[qi];
-  }
-  if (warp < gqa) {  // ||q|| bounds every |q_rot[ch]| (R orthogonal): the operands' fp16 exponent
-    const float4 v = reinterpret_cast<const float4*>(qf + warp * kD)[lane];
-    float ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, v.w * v.w)));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    if (lane == 0) Ei[warp] = qk_exponent(sqrtf(ss), p.scale_log2);
-  }
-  __syncthreads();
-  for (int idx = tid; idx < gqa * kD; idx += T) {  // the row groups added in order
-    const int qi = idx / kD, cc = idx % kD;
-    float sum = 0.f;
-#pragma unroll
-    for (int r = 0; r < T / kD; ++r) sum += part[(r * kMaxGqa + qi) * kD + cc];
-    qr[idx] = sum;
-  }
-  __syncthreads();
-  if (warp < gqa) {  // group sums of q_rot in log2 units (lane: 4 channels)
-    const float4 v = reinterpret_cast<const float4*>(qr + warp * kD)[lane];
-    float s4 = (v.x + v.y) + (v.z + v.w);
-#pragma unroll
-    for (int off = 1; off < 16; off <<= 1) s4 += __shfl_xor_sync(0xffffffffu, s4, off);
-    if (NG == 1) s4 += __shfl_xor_sync(0xffffffffu, s4, 16);
-    if (lane == 0) qsum[warp * 2] = s4 * p.scale_log2;
-    if (NG == 2 && lane == 16) qsum[warp * 2 + 1] = s4 * p.scale_log2;
-  }
-  __syncthreads();
-  // Operand words of lane L = 4g + t: word nt*16 + 2ks + c2 is the QK B register c2 of
-  // k-step ks for n-tile nt (query 4nt + g/2, fp16 hi part for even g, remainder for
-  // odd g; channels 16w + 2(ks&3) + c2 and +8 of word w = t + 4(ks>>2)); words 32 + nt:
-  // 2^(24 - E) of query 4nt + t; words 34 + 2nt + gg: its group sums.
-  for (int idx = tid; idx < 32 * 38; idx += T) {
-    const int L = idx / 38, wi = idx % 38;
-    const int lg = L >> 2, lt = L & 3;
-    uint32_t word = 0u;
-    if (wi < 32) {
-      const int nt = wi >> 4, ks = (wi >> 1) & 7, c2 = wi & 1;
-      const int qb = 4 * nt + (lg >> 1);
-      const int ch_lo = 16 * (lt + 4 * (ks >> 2)) + 2 * (ks & 3) + c2;
-      if (nt < NT && qb < gqa)
-        word = qk_word(qr[qb * kD + ch_lo], qr[qb * kD + ch_lo + 8], p.scale_log2, Ei[qb], ch_lo, (lg & 1) != 0);
-    } else if (wi < 34) {
-      const int qi = 4 * (wi - 32) + lt;
-      word = __float_as_uint(qi < gqa ? pow2i(24 - Ei[qi]) : 0.f);
-    } else {
-      const int nt = (wi - 34) >> 1, gg = (wi - 34) & 1;
-      const int qi = 4 * nt + lt;
-      word = __float_as_uint(qi < gqa && gg < NG ? qsum[qi * 2 + gg] : 0.f);
-    }
-    frag[L * kFragWords + wi] = word;
-  }
-  __syncthreads();
-  uint32_t bq[NT][8][2];
-  float F[NT], qs[NT][NG];
-  {
-    const uint4* fw4 = reinterpret_cast<const uint4*>(frag + lane * kFragWords);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 v = fw4[4 * nt + k];
-        bq[nt][2 * k][0] = v.x;
-        bq[nt][2 * k][1] = v.y;
-        bq[nt][2 * k + 1][0] = v.z;
-        bq[nt][2 * k + 1][1] = v.w;
-      }
-    const uint4 f0 = fw4[8], f1 = fw4[9];
-    const float fw[8] = {__uint_as_float(f0.x), __uint_as_float(f0.y), __uint_as_float(f0.z), __uint_as_float(f0.w),
-                         __uint_as_float(f1.x), __uint_as_float(f1.y), __uint_as_float(f1.z), __uint_as_float(f1.w)};
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      F[nt] = fw[nt];
-#pragma unroll
-      for (int gg = 0; gg < NG; ++gg) qs[nt][gg] = fw[2 + 2 * nt + gg];
-    }
-  }
-
   grid_dep_launch_dependents();
-  // ---- pages, lengths and page ids may come from the preceding kernel ----
+  // ---- the q-rotation's operands, lengths, page ids and pages may come from the
+  // preceding kernels (the q-rotation, and an append before it) ----
   grid_dep_wait();
+  if (tid == 0) {  // the unit's operand block (5.6 KB) by one bulk copy
+    mbar_arrive_expect_tx(fbar, kQfragBytes);
+    bulk_g2s(smem_u32(frag), p.qfrag + (static_cast<size_t>(b) * p.H + h) * (32 * kQfragWords), kQfragBytes, fbar);
+  }
   const RowView rv = row_view(p, b);
   const int win_begin = max(p.S, rv.L - p.W);
   const int lo_pos = (p.bulk_lo + s * p.pps) * kPageSize;
@@ -237,15 +106,13 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
   const int npg = r1 > r0 ? (r1 - 1) / kPageSize + 1 - pg0 : 0;
   for (int k = tid; k < npg; k += T)
     pids[k] = __ldg(p.page_table + static_cast<size_t>(rv.seq) * p.max_pages + pg0 + k);
-  // the prologue's buffers were written and read by generic accesses; bulk copies
-  // overwrite them next
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
   if (npg == 0) {  // nothing of the bulk in this split: an empty partial (the merge skips it)
     if (tid < gqa) {
       p.part_ml[((bh0 + tid) * p.ml_ns + s) * 2 + 0] = -INFINITY;
       p.part_ml[((bh0 + tid) * p.ml_ns + s) * 2 + 1] = 0.f;
     }
+    if (tid == 0) mbar_wait_bounded(fbar, 0);  // the operand copy lands before the CTA exits
     return;
   }
 
@@ -281,6 +148,46 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
   };
   for (int i0 = 0; i0 < min(n_my, kStages); i0 += 16) issue(i0, min(min(n_my, kStages), i0 + 16));
 
+  // ---- this lane's QK B-fragments and per-query factors from the operand block
+  // (kQfragWords words per lane, written by the q-rotation: per n-tile nt the lane's
+  // C columns belong to query 4*nt + t and its B column to query 4*nt + (g >> 1),
+  // part g & 1) ----
+  const bool frag_ok = __any_sync(0xffffffffu, !mbar_wait_bounded(fbar, 0)) == 0;
+  uint32_t bq[NT][8][2];
+  float F[NT], qs[NT][NG];
+  {
+    const uint4* qw4 = reinterpret_cast<const uint4*>(frag + lane * kQfragWords);
+    uint4 v[4 * NT], f[3];
+#pragma unroll
+    for (int k = 0; k < 4 * NT; ++k) v[k] = qw4[k];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) f[k] = qw4[8 + k];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        bq[nt][2 * k][0] = v[4 * nt + k].x;
+        bq[nt][2 * k][1] = v[4 * nt + k].y;
+        bq[nt][2 * k + 1][0] = v[4 * nt + k].z;
+        bq[nt][2 * k + 1][1] = v[4 * nt + k].w;
+      }
+    const uint32_t fw[12] = {f[0].x, f[0].y, f[0].z, f[0].w, f[1].x, f[1].y,
+                             f[1].z, f[1].w, f[2].x, f[2].y, f[2].z, f[2].w};
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      F[nt] = __uint_as_float(fw[5 * nt]);
+      // group sums from the four 32-column block sums
+      const float c0 = __uint_as_float(fw[5 * nt + 1]), c1 = __uint_as_float(fw[5 * nt + 2]);
+      const float c2 = __uint_as_float(fw[5 * nt + 3]), c3 = __uint_as_float(fw[5 * nt + 4]);
+      if (NG == 2) {
+        qs[nt][0] = c0 + c1;
+        qs[nt][NG - 1] = c2 + c3;
+      } else {
+        qs[nt][0] = (c0 + c1) + (c2 + c3);
+      }
+    }
+  }
+
   float m_run[NT], O[NT][8][4];
   float2 l2[NT], z2[NT][NG];  // per token slot (g, g + 8) of the page body
 #pragma unroll
@@ -310,9 +217,9 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
     const int pos = (pg0 + jpage) * kPageSize + tok;
     return pid >= 0 && pid < p.num_pages && pos >= r0 && pos < r1;
   };
-  bool aborted = false;
+  bool aborted = !frag_ok;
   int i = 0;
-  for (; i + 1 < n_my; i += 2) {
+  for (; !aborted && i + 1 < n_my; i += 2) {
     if (__any_sync(0xffffffffu, !wait_page(i) || !wait_page(i + 1))) {
       aborted = true;
       break;
@@ -411,23 +318,30 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
       }
     }
   }
+  // this warp's rows of R_v for the un-rotation (lane l: columns 4l .. 4l+3), loaded
+  // while the other warps finish
+  constexpr int kRowsPerWarp = kD / NW;  // 8 (16 warps) or 16 (8 warps)
+  float4 rvr[kRowsPerWarp];
+  {
+    const float4* Rv4 = reinterpret_cast<const float4*>(p.R_v + static_cast<size_t>(h) * kD * kD);
+#pragma unroll
+    for (int u = 0; u < kRowsPerWarp; ++u) rvr[u] = __ldg(Rv4 + (warp * kRowsPerWarp + u) * (kD / 4) + lane);
+  }
   __syncthreads();
-  if (tid < gqa) {  // CTA maximum and sum; mw becomes the warps' weights
-    float M = -INFINITY;
+  if (warp < gqa) {  // CTA maximum and sum of query `warp`, lane w for warp w's state; mw becomes the weights
+    const float mwq = lane < NW ? mw[lane * kMaxGqa + warp] : -INFINITY;
+    float M = mwq;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, mw[w * kMaxGqa + tid]);
-    float l = 0.f;
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float wt = (M == -INFINITY || mwq == -INFINITY) ? 0.f : fast_exp2(mwq - M);
+    float l = lane < NW ? wt * lw[lane * kMaxGqa + warp] : 0.f;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float mwq = mw[w * kMaxGqa + tid];
-      const float wt = (M == -INFINITY || mwq == -INFINITY) ? 0.f : fast_exp2(mwq - M);
-      l = fmaf(wt, lw[w * kMaxGqa + tid], l);
-      mw[w * kMaxGqa + tid] = wt;
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    if (lane < NW) mw[lane * kMaxGqa + warp] = wt;
+    if (lane == 0) {
+      Ms[warp] = M;
+      Ls[warp] = l;
     }
-    const bool okq = !aborted;
-    Ms[tid] = M;
-    Ls[tid] = l;
-    (void)okq;
   }
   const bool ok = __syncthreads_and(!aborted);
   // the CTA's output in rotated space (unnormalised), behind the warps' states
@@ -448,18 +362,13 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
     reinterpret_cast<float4*>(orot)[idx] = o;
   }
   __syncthreads();
-  // ---- un-rotation, out[c] = sum_j o_rot[j] R_v[h][c][j]: warp w takes rows
-  // c0 .. c0 + kRowsPerWarp - 1 of R_v straight from L2 (lane l: columns 4l .. 4l+3, a
-  // coalesced 512-byte row per load), forms every (row, query) partial dot product of
-  // its columns, then a reduce-scatter across the lanes leaves one total per lane ----
+  // ---- un-rotation, out[c] = sum_j o_rot[j] R_v[h][c][j]: warp w holds rows
+  // c0 .. c0 + kRowsPerWarp - 1 of R_v (read from L2 above), forms every (row, query)
+  // partial dot product of its lane's columns, then a reduce-scatter across the lanes
+  // leaves one total per lane ----
   {
-    constexpr int kRowsPerWarp = kD / NW;          // 8 (16 warps) or 16 (8 warps)
     constexpr int kVals = kRowsPerWarp * kQ;       // 32 or 128 partial sums per lane
     const int c0 = warp * kRowsPerWarp;
-    const float4* Rv4 = reinterpret_cast<const float4*>(p.R_v + static_cast<size_t>(h) * kD * kD);
-    float4 rv[kRowsPerWarp];
-#pragma unroll
-    for (int u = 0; u < kRowsPerWarp; ++u) rv[u] = __ldg(Rv4 + (c0 + u) * (kD / 4) + lane);
     float4 oq[kQ];
 #pragma unroll
     for (int qi = 0; qi < kQ; ++qi) oq[qi] = reinterpret_cast<const float4*>(orot + qi * kD)[lane];
@@ -470,7 +379,7 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
 #pragma unroll
       for (int v = 0; v < 32; ++v) {
         const int idx = 32 * half + v, u = idx / kQ, qi = idx % kQ;
-        val[v] = fmaf(rv[u].x, oq[qi].x, fmaf(rv[u].y, oq[qi].y, fmaf(rv[u].z, oq[qi].z, rv[u].w * oq[qi].w)));
+        val[v] = fmaf(rvr[u].x, oq[qi].x, fmaf(rvr[u].y, oq[qi].y, fmaf(rvr[u].z, oq[qi].z, rvr[u].w * oq[qi].w)));
       }
       // reduce-scatter: after the round with offset o, a lane keeps the half of its
       // values selected by its bit o; at the end lane l holds the total of value l
@@ -577,6 +486,10 @@ template <int NT, int NG, int NW>
 cudaError_t launch_fused_impl(const Params& p, cudaStream_t stream) {
   constexpr size_t smem = FusedGeo<NT, NG, NW>::kSmem;
   cudaError_t e = set_smem_limit_once(fused_kernel_ptr<NT, NG, NW>(), smem);
+  if (e != cudaSuccess) return e;
+  // the query rotation and its QK operand blocks, once per (sequence, KV head)
+  const int chunks = (p.B + p.qrot_spc - 1) / p.qrot_spc;
+  e = launch_pdl(qrot_kernel<kD>, dim3(chunks * p.H, kD / 32), dim3(kQrotThreads), 0, stream, p);
   if (e != cudaSuccess) return e;
   e = launch_pdl(int2_fused_kernel<NT, NG, NW>, dim3(p.ns, p.H, p.B), dim3(NW * 32), smem, stream, p);
   if (e != cudaSuccess) return e;
