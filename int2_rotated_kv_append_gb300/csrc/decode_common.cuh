@@ -92,7 +92,7 @@ bool bf16_mma_supported(const Params& p);
 cudaError_t bf16_mma_split(const Params& p, cudaStream_t stream);
 // Fused single-wave decode (decode_fused.cu).
 bool int2_fused_shape(int D, int G, int gqa);
-int int2_fused_max_pps();
+int int2_fused_max_pps(int gqa);
 int int2_fused_ctas_per_sm(int gqa, int G);
 cudaError_t int2_fused_decode(const Params& p, cudaStream_t stream);
 
@@ -156,7 +156,7 @@ bool make_fused_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req,
     if (pps < 1) pps = 1;
   }
   const int n_s = nb > 0 ? (nb + pps - 1) / pps : 1;
-  if (pps > int2_fused_max_pps() || units * (n_s + n_d) > slots) return false;
+  if (pps > int2_fused_max_pps(gqa) || units * (n_s + n_d) > slots) return false;
   p->fused = 1;
   p->mma = 1;
   p->bulk_lo = bulk_lo;

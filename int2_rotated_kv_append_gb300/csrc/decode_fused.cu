@@ -28,7 +28,9 @@ namespace oscar_dec {
 namespace {
 
 constexpr int kRBytes = kD * kD * 4;
-constexpr int kFMaxPps = 4096;      // page ids of one split staged in shared memory
+// page ids of one split staged in shared memory (the 8-warp form has room for more)
+template <int NW>
+constexpr int fused_max_pps() { return NW >= 16 ? 2048 : 4096; }
 constexpr int kFragWords = 44;      // per-lane QK operand words in shared memory (44: conflict-free rows)
 constexpr int kOwPitch = kD + 4;    // padded row of a warp's output in the merge area
 
@@ -54,14 +56,16 @@ struct FusedGeo {
   // The q-rotation's QK operand block of the unit (kQfragBytes), in use while the ring fills.
   static constexpr size_t kOffFrag = (kArea0 + 127) / 128 * 128;
   static constexpr size_t kOffMisc = kOffFrag + kQfragBytes;
-  static constexpr size_t kOffPid = kOffMisc + 64 * 4;              // page ids [kFMaxPps]
-  static constexpr size_t kOffBars = kOffPid + kFMaxPps * 4;        // NW * kStages ring barriers
+  static constexpr size_t kOffPid = kOffMisc + 64 * 4;              // page ids [fused_max_pps]
+  static constexpr size_t kOffBars = kOffPid + fused_max_pps<NW>() * 4;  // NW * kStages ring barriers
   static constexpr size_t kSmem = kOffBars + (NW * kStages + 1) * 8;  // + the operand block's barrier
 };
 
 // INT2 split CTA s < n_paged of unit (b, h), or the unit's BF16 CTA (s == n_paged).
+// The 16-warp form is held to 96 registers (the bound of a 20-warp CTA), so that the
+// small q-rotation and merge CTAs of neighbouring calls fit on an SM beside it.
 template <int NT, int NG, int NW>
-__global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
+__global__ void __launch_bounds__(NT == 1 ? 640 : NW * 32, 1) int2_fused_kernel(Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   using Geo = FusedGeo<NT, NG, NW>;
   constexpr int T = NW * 32;
@@ -91,6 +95,32 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
   }
   __syncthreads();
   grid_dep_launch_dependents();
+  {
+    // Before the dependency wait (the preceding kernels may still run): the split's
+    // pages as the current length and page table give them are prefetched into L2.
+    // This reads the length and the page table early but only as a hint: every value
+    // used below is read again after the wait, and a prefetched line is still updated
+    // by any later write, so a page an earlier kernel changes is read correctly.
+    int L = __ldg(p.seq_lens + b);
+    L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
+    const int wb = max(p.S, L - p.W);
+    const int lo = (p.bulk_lo + s * p.pps) * kPageSize;
+    const int q0 = max(lo, p.S), q1 = min(lo + p.pps * kPageSize, wb);
+    const int pf0 = q0 / kPageSize, npf = q1 > q0 ? (q1 - 1) / kPageSize + 1 - pf0 : 0;
+    // (line by line through the load/store path: bulk prefetches would queue in the
+    // bulk-copy unit ahead of the split's own copies)
+    constexpr int kLines = (kCodeBytes + kSzBytes) / 128;  // 10 (group 64) or 9 (group 128)
+    for (int k = tid; k < npf * kLines; k += T) {
+      const int pg = k / kLines, ln = k % kLines;
+      const int pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pf0 + pg);
+      if (pid >= 0 && pid < p.num_pages) {
+        const size_t ph = static_cast<size_t>(pid) * p.H + h;
+        prefetch_l2_line(ln < kCodeBytes / 128 ? p.codes + ph * kCodeBytes + ln * 128
+                                               : reinterpret_cast<const uint8_t*>(p.sz) + ph * kSzBytes +
+                                                     (ln - kCodeBytes / 128) * 128);
+      }
+    }
+  }
   // ---- the q-rotation's operands, lengths, page ids and pages may come from the
   // preceding kernels (the q-rotation, and an append before it) ----
   grid_dep_wait();
@@ -320,9 +350,10 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
   }
   // this warp's rows of R_v for the un-rotation (lane l: columns 4l .. 4l+3), loaded
   // while the other warps finish
-  constexpr int kRowsPerWarp = kD / NW;  // 8 (16 warps) or 16 (8 warps)
+  constexpr int kUnrotWarps = NW >= 16 ? 16 : NW;  // warps that take rows of R_v
+  constexpr int kRowsPerWarp = kD / kUnrotWarps;    // 8 or 16
   float4 rvr[kRowsPerWarp];
-  {
+  if (warp < kUnrotWarps) {
     const float4* Rv4 = reinterpret_cast<const float4*>(p.R_v + static_cast<size_t>(h) * kD * kD);
 #pragma unroll
     for (int u = 0; u < kRowsPerWarp; ++u) rvr[u] = __ldg(Rv4 + (warp * kRowsPerWarp + u) * (kD / 4) + lane);
@@ -362,11 +393,11 @@ __global__ void __launch_bounds__(NW * 32, 1) int2_fused_kernel(Params p) {
     reinterpret_cast<float4*>(orot)[idx] = o;
   }
   __syncthreads();
-  // ---- un-rotation, out[c] = sum_j o_rot[j] R_v[h][c][j]: warp w holds rows
-  // c0 .. c0 + kRowsPerWarp - 1 of R_v (read from L2 above), forms every (row, query)
-  // partial dot product of its lane's columns, then a reduce-scatter across the lanes
-  // leaves one total per lane ----
-  {
+  // ---- un-rotation, out[c] = sum_j o_rot[j] R_v[h][c][j]: warp w < kUnrotWarps holds
+  // rows c0 .. c0 + kRowsPerWarp - 1 of R_v (read from L2 above), forms every (row,
+  // query) partial dot product of its lane's columns, then a reduce-scatter across the
+  // lanes leaves one total per lane ----
+  if (warp < kUnrotWarps) {
     constexpr int kVals = kRowsPerWarp * kQ;       // 32 or 128 partial sums per lane
     const int c0 = warp * kRowsPerWarp;
     float4 oq[kQ];
@@ -496,8 +527,8 @@ cudaError_t launch_fused_impl(const Params& p, cudaStream_t stream) {
   return launch_pdl(fused_merge_kernel, dim3(p.B * p.Hq), dim3(kLseWarps * 32), 0, stream, p);
 }
 
-// Warps per CTA: 16 for up to 4 query heads per KV head (96 registers), 8 for more
-// (the 8-query page body holds about 220 registers).
+// Warps per CTA: 16 for up to 4 query heads per KV head, 8 for more (the 8-query page
+// body holds about 220 registers).
 constexpr int kFusedWarpsNarrow = 16;
 constexpr int kFusedWarpsWide = 8;
 
@@ -507,7 +538,9 @@ bool int2_fused_shape(int D, int G, int gqa) {
   return D == kD && (G == 64 || G == 128) && gqa >= 1 && gqa <= kMaxGqa;
 }
 
-int int2_fused_max_pps() { return kFMaxPps; }
+int int2_fused_max_pps(int gqa) {
+  return gqa > 4 ? fused_max_pps<kFusedWarpsWide>() : fused_max_pps<kFusedWarpsNarrow>();
+}
 
 
 

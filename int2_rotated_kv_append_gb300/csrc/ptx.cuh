@@ -79,6 +79,19 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uin
       : "memory");
 }
 
+// Best-effort prefetch of `bytes` (multiple of 16, 16-byte aligned) into L2: a hint
+// only, with no ordering against later writes (a line the hint brought in is still
+// updated by any write to it).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Best-effort prefetch of the 128-byte line holding `addr` into L2 through the
+// load/store path (a hint, as above).
+__device__ __forceinline__ void prefetch_l2_line(const void* addr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+}
+
 // Programmatic dependent launch: grid_dep_wait() blocks until the preceding
 // kernel has completed and its writes are visible (a no-op without a
 // programmatic dependency); grid_dep_launch_dependents() lets the following
