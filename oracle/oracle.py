@@ -60,10 +60,12 @@ def load(path: str | None = None):
         "orc_clip": (None, [ctypes.c_int32, _P, _P]),
         "orc_group_params": (None, [ctypes.c_int32, _P, _P, _P]),
         "orc_quantize": (ctypes.c_int32, [ctypes.c_double, ctypes.c_uint16, ctypes.c_uint16, _P]),
-        "orc_append_prequant": (ctypes.c_int32, [_P, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P]),
+        "orc_offset_key": (None, [ctypes.c_int32, _P, _P, _P]),
+        "orc_f32_to_bf16": (ctypes.c_uint16, [ctypes.c_float]),
+        "orc_append_prequant": (ctypes.c_int32, [_P, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P]),
         "orc_codes_given_params": (None, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]),
-        "orc_append": (ctypes.c_int32, [_P, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
-        "orc_append_mixed": (ctypes.c_int32, [_P, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+        "orc_append": (ctypes.c_int32, [_P, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+        "orc_append_mixed": (ctypes.c_int32, [_P, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]),
         "orc_attend_mixed": (None, [ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P,
                                     ctypes.c_double, _P, _P]),
@@ -133,6 +135,26 @@ def rotate(x_bf16_bits: np.ndarray, R: np.ndarray, lib=None) -> np.ndarray:
     return out
 
 
+def offset_key(k_bf16_bits: np.ndarray, c: np.ndarray, lib=None) -> np.ndarray:
+    """fp32(k - c) of one key (bf16 bits [D]) and its offset (fp32 [D]), as fp64."""
+    lib = lib or load()
+    k = _c(k_bf16_bits, np.uint16)
+    cc = _c(c, np.float32)
+    out = np.empty(k.shape[0], np.float64)
+    lib.orc_offset_key(k.shape[0], _ptr(k), _ptr(cc), _ptr(out))
+    return out
+
+
+def f32_to_bf16(vals, lib=None) -> np.ndarray:
+    lib = lib or load()
+    v = np.asarray(vals, dtype=np.float32)
+    return np.array([lib.orc_f32_to_bf16(float(x)) for x in v.ravel()], dtype=np.uint16).reshape(v.shape)
+
+
+def _offset(offset_k):
+    return None if offset_k is None else _c(offset_k, np.float32)
+
+
 def clip(x: np.ndarray, c: np.ndarray, lib=None) -> np.ndarray:
     lib = lib or load()
     y = _c(x, np.float64).copy()
@@ -171,8 +193,9 @@ def codes_given_params(x: np.ndarray, sz_bits: np.ndarray, group_size: int, lib=
     return codes, u
 
 
-def append_prequant(dims, k_bits, v_bits, R_k, R_v, clip_k, clip_v, lib=None) -> np.ndarray:
-    """Rotated+clipped fp64 values [T][Hkv][2][D] of every (token, head, K|V)."""
+def append_prequant(dims, k_bits, v_bits, R_k, R_v, clip_k, clip_v, offset_k=None, lib=None) -> np.ndarray:
+    """Rotated+clipped fp64 values [T][Hkv][2][D] of every (token, head, K|V);
+    ``offset_k`` (fp32 [Hkv][D] or None) is subtracted from every key first."""
     lib = lib or load()
     d = _dims(dims)
     k = _c(k_bits, np.uint16)
@@ -180,12 +203,13 @@ def append_prequant(dims, k_bits, v_bits, R_k, R_v, clip_k, clip_v, lib=None) ->
     T = k.shape[0]
     out = np.empty((T, d.num_kv_heads, 2, d.head_dim), np.float64)
     args = [_c(a, np.float32) for a in (R_k, R_v, clip_k, clip_v)]
-    lib.orc_append_prequant(ctypes.byref(d), T, _ptr(k), _ptr(v), *[_ptr(a) for a in args], _ptr(out))
+    off = _offset(offset_k)
+    lib.orc_append_prequant(ctypes.byref(d), T, _ptr(k), _ptr(v), *[_ptr(a) for a in args], _ptr(off), _ptr(out))
     return out
 
 
 def append(dims, k_bits, v_bits, R_k, R_v, clip_k, clip_v, slot_mapping, int2_pages, scale_zero_pages,
-           lib=None) -> int:
+           offset_k=None, lib=None) -> int:
     """Append into the given host pools in place (uint8 codes, uint16 fp16-bits scale/zero)."""
     lib = lib or load()
     d = _dims(dims)
@@ -195,12 +219,14 @@ def append(dims, k_bits, v_bits, R_k, R_v, clip_k, clip_v, slot_mapping, int2_pa
     assert int2_pages.dtype == np.uint8 and int2_pages.flags.c_contiguous
     assert scale_zero_pages.dtype == np.uint16 and scale_zero_pages.flags.c_contiguous
     args = [_c(a, np.float32) for a in (R_k, R_v, clip_k, clip_v)]
-    return lib.orc_append(ctypes.byref(d), k.shape[0], _ptr(k), _ptr(v), *[_ptr(a) for a in args],
+    off = _offset(offset_k)
+    return lib.orc_append(ctypes.byref(d), k.shape[0], _ptr(k), _ptr(v), *[_ptr(a) for a in args], _ptr(off),
                           _ptr(slots), _ptr(int2_pages), _ptr(scale_zero_pages))
 
 
 def append_mixed(dims, k_bits, v_bits, R_k, R_v, clip_k, clip_v, slot_mapping, seq_ids, positions, seq_lens,
-                 sink_len, window_len, int2_pages, scale_zero_pages, sink_bits, window_bits, lib=None) -> int:
+                 sink_len, window_len, int2_pages, scale_zero_pages, sink_bits, window_bits, offset_k=None,
+                 lib=None) -> int:
     """Append into the host INT2 pools and the BF16 sink/window (uint16 bf16 bits,
     [B][2][Hkv][S|W][D]) in place."""
     lib = lib or load()
@@ -213,8 +239,9 @@ def append_mixed(dims, k_bits, v_bits, R_k, R_v, clip_k, clip_v, slot_mapping, s
                  (window_bits, np.uint16)):
         assert a.dtype == t and a.flags.c_contiguous
     args = [_c(a, np.float32) for a in (R_k, R_v, clip_k, clip_v)]
+    off = _offset(offset_k)
     return lib.orc_append_mixed(ctypes.byref(d), k.shape[0], _ptr(k), _ptr(v), *[_ptr(a) for a in args],
-                                _ptr(slots), _ptr(sid), _ptr(pos), _ptr(lens), lens.shape[0], int(sink_len),
+                                _ptr(off), _ptr(slots), _ptr(sid), _ptr(pos), _ptr(lens), lens.shape[0], int(sink_len),
                                 int(window_len), _ptr(int2_pages), _ptr(scale_zero_pages), _ptr(sink_bits),
                                 _ptr(window_bits))
 

@@ -17,6 +17,10 @@
 //               Cache Quantization", abstract: fixed rotations and clipping
 //               thresholds, INT2 attention kernel compatible with paged KV-cache
 //               serving.
+//   [OptR]      the OptR abstract on that same paper page (a follow-up on
+//               output-aware rotations): an attention-equivalent key
+//               reparameterisation that removes large per-channel key offsets
+//               without changing the softmax distribution, paged format kept.
 // The pages give no formulas; the arithmetic below is the plainest reading of
 // the words (rotate, clip, per-group asymmetric INT2 with fp16 scale/zero,
 // paged storage, softmax attention).  Each such reading carries a tag (R#) and
@@ -103,14 +107,52 @@ uint16_t orc_f64_to_f16(double v) {
 // ---------------------------------------------------------------------------
 
 // Step A2 (rotation, reading R7): row vector convention, x_rot = x . R, with
-// x_rot[j] = sum_i x[i] * R[i][j].  R is row-major fp32 [D][D].
-void orc_rotate(int32_t D, const uint16_t* x_bf16, const float* R, double* x_rot) {
+// x_rot[j] = sum_i x[i] * R[i][j].  R is row-major fp32 [D][D]; x is given in fp64.
+static void rotate_f64(int32_t D, const double* x, const float* R, double* x_rot) {
   for (int j = 0; j < D; ++j) {
     double acc = 0.0;
-    for (int i = 0; i < D; ++i) {
-      acc += orc_bf16_to_f64(x_bf16[i]) * static_cast<double>(R[static_cast<size_t>(i) * D + j]);
-    }
+    for (int i = 0; i < D; ++i) acc += x[i] * static_cast<double>(R[static_cast<size_t>(i) * D + j]);
     x_rot[j] = acc;
+  }
+}
+
+// Step A2 for a bf16 vector.
+void orc_rotate(int32_t D, const uint16_t* x_bf16, const float* R, double* x_rot) {
+  std::vector<double> x(D);
+  for (int i = 0; i < D; ++i) x[i] = orc_bf16_to_f64(x_bf16[i]);
+  rotate_f64(D, x.data(), R, x_rot);
+}
+
+// Key offset removal ([OptR]: an attention-equivalent reparameterisation of the
+// keys; the subtraction and its precision are reading R26): every key k is replaced by k' = k - c with a fixed per-(KV head,
+// channel) fp32 offset c, the difference taken in fp32 (round to nearest even).
+// Softmax is unchanged, since q . c is the same for all keys of a query.  Values
+// are not offset.  out[i] = fp32(bf16(k_i) - c_i) as an exact double.
+void orc_offset_key(int32_t D, const uint16_t* k_bf16, const float* c, double* out) {
+  for (int i = 0; i < D; ++i) {
+    // the fp64 difference of a bf16 and an fp32 value is exact when their exponents
+    // differ by at most 28; otherwise the smaller operand is below a sixteenth of an
+    // fp32 ulp of the larger and both roundings give the larger operand's fp32 value
+    out[i] = static_cast<double>(static_cast<float>(orc_bf16_to_f64(k_bf16[i]) - static_cast<double>(c[i])));
+  }
+}
+
+// fp32 -> bf16 bit pattern, round to nearest even (finite inputs).
+uint16_t orc_f32_to_bf16(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  const uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7fffu + lsb;
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// The vector that is rotated for token row x of KV head h (K when kv == 0): the key
+// minus its offset when an offset is given (reading R26), else the bf16 values.
+static void pre_rotation(int32_t D, const uint16_t* x, int kv, const float* offset_k, int h, double* out) {
+  if (kv == 0 && offset_k != nullptr) {
+    orc_offset_key(D, x, offset_k + static_cast<size_t>(h) * D, out);
+  } else {
+    for (int i = 0; i < D; ++i) out[i] = orc_bf16_to_f64(x[i]);
   }
 }
 
@@ -189,8 +231,9 @@ static size_t sz_row(const orc_dims_t* d, int64_t page, int h, int kv, int off) 
 // [T][Hkv][2][D]; tokens whose slot is negative are still computed.
 int32_t orc_append_prequant(const orc_dims_t* d, int64_t T, const uint16_t* k, const uint16_t* v,
                             const float* R_k, const float* R_v, const float* clip_k,
-                            const float* clip_v, double* out) {
+                            const float* clip_v, const float* offset_k, double* out) {
   const int H = d->num_kv_heads, D = d->head_dim;
+  std::vector<double> x0(D);
   for (int64_t t = 0; t < T; ++t) {
     for (int h = 0; h < H; ++h) {
       for (int kv = 0; kv < 2; ++kv) {
@@ -198,7 +241,8 @@ int32_t orc_append_prequant(const orc_dims_t* d, int64_t T, const uint16_t* k, c
         const float* R = (kv ? R_v : R_k) + static_cast<size_t>(h) * D * D;
         const float* clip = (kv ? clip_v : clip_k) + static_cast<size_t>(h) * D;
         double* y = out + ((static_cast<size_t>(t) * H + h) * 2 + kv) * D;
-        orc_rotate(D, x, R, y);
+        pre_rotation(D, x, kv, offset_k, h, x0.data());
+        rotate_f64(D, x0.data(), R, y);
         orc_clip(D, y, clip);
       }
     }
@@ -214,9 +258,10 @@ int32_t orc_append_prequant(const orc_dims_t* d, int64_t T, const uint16_t* k, c
 // pool (nothing is written for that token).
 int32_t orc_append(const orc_dims_t* d, int64_t T, const uint16_t* k, const uint16_t* v,
                    const float* R_k, const float* R_v, const float* clip_k, const float* clip_v,
-                   const int64_t* slot_mapping, uint8_t* int2_pages, uint16_t* scale_zero_pages) {
+                   const float* offset_k, const int64_t* slot_mapping, uint8_t* int2_pages,
+                   uint16_t* scale_zero_pages) {
   const int H = d->num_kv_heads, D = d->head_dim, P = d->page_size, G = d->group_size;
-  std::vector<double> y(D);
+  std::vector<double> y(D), x0(D);
   int32_t status = 0;
   for (int64_t t = 0; t < T; ++t) {
     const int64_t slot = slot_mapping[t];
@@ -232,7 +277,8 @@ int32_t orc_append(const orc_dims_t* d, int64_t T, const uint16_t* k, const uint
         const uint16_t* x = (kv ? v : k) + (static_cast<size_t>(t) * H + h) * D;
         const float* R = (kv ? R_v : R_k) + static_cast<size_t>(h) * D * D;
         const float* clip = (kv ? clip_v : clip_k) + static_cast<size_t>(h) * D;
-        orc_rotate(D, x, R, y.data());
+        pre_rotation(D, x, kv, offset_k, h, x0.data());
+        rotate_f64(D, x0.data(), R, y.data());
         orc_clip(D, y.data(), clip);
         uint8_t* row = int2_pages + code_row(d, page, h, kv, off);
         uint16_t* sz = scale_zero_pages + sz_row(d, page, h, kv, off);
@@ -258,7 +304,8 @@ int32_t orc_append(const orc_dims_t* d, int64_t T, const uint16_t* k, const uint
 // tokens and a BF16 window of the most recent ones next to the INT2 bulk).  Every
 // token t with slot_mapping[t] >= 0 is appended to the INT2 pool exactly as
 // orc_append does ("dual write", reading R13).  Its original bf16 K and V rows are
-// also stored, unrotated (reading R12), for sequence b = seq_ids[t] at position
+// also stored, unrotated (reading R12; with a key offset the K row is the offset
+// key, reading R26), for sequence b = seq_ids[t] at position
 // p = positions[t], with L = seq_lens[b] the sequence length after this append
 // (reading R18):
 //   p < S                  -> sink[b][K|V][h][p][:]
@@ -270,11 +317,13 @@ int32_t orc_append(const orc_dims_t* d, int64_t T, const uint16_t* k, const uint
 // of range (its BF16 rows are not written).
 int32_t orc_append_mixed(const orc_dims_t* d, int64_t T, const uint16_t* k, const uint16_t* v,
                          const float* R_k, const float* R_v, const float* clip_k, const float* clip_v,
-                         const int64_t* slot_mapping, const int32_t* seq_ids, const int32_t* positions,
-                         const int32_t* seq_lens, int32_t B, int32_t S, int32_t W, uint8_t* int2_pages,
-                         uint16_t* scale_zero_pages, uint16_t* sink, uint16_t* window) {
-  int32_t status = orc_append(d, T, k, v, R_k, R_v, clip_k, clip_v, slot_mapping, int2_pages, scale_zero_pages);
+                         const float* offset_k, const int64_t* slot_mapping, const int32_t* seq_ids,
+                         const int32_t* positions, const int32_t* seq_lens, int32_t B, int32_t S, int32_t W,
+                         uint8_t* int2_pages, uint16_t* scale_zero_pages, uint16_t* sink, uint16_t* window) {
+  int32_t status = orc_append(d, T, k, v, R_k, R_v, clip_k, clip_v, offset_k, slot_mapping, int2_pages,
+                              scale_zero_pages);
   const int H = d->num_kv_heads, D = d->head_dim;
+  std::vector<double> x0(D);
   for (int64_t t = 0; t < T; ++t) {
     if (slot_mapping[t] < 0) continue;
     const int32_t b = seq_ids[t], p = positions[t];
@@ -293,7 +342,13 @@ int32_t orc_append_mixed(const orc_dims_t* d, int64_t T, const uint16_t* k, cons
         } else if (W > 0 && p >= win_begin) {
           dst = window + (((static_cast<size_t>(b) * 2 + kv) * H + h) * W + p % W) * D;
         }
-        if (dst != nullptr) std::memcpy(dst, x, static_cast<size_t>(D) * sizeof(uint16_t));
+        if (dst == nullptr) continue;
+        if (kv == 0 && offset_k != nullptr) {  // the stored key is the offset key, rounded to bf16
+          orc_offset_key(D, x, offset_k + static_cast<size_t>(h) * D, x0.data());
+          for (int i = 0; i < D; ++i) dst[i] = orc_f32_to_bf16(static_cast<float>(x0[i]));
+        } else {
+          std::memcpy(dst, x, static_cast<size_t>(D) * sizeof(uint16_t));
+        }
       }
     }
   }

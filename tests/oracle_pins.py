@@ -729,6 +729,123 @@ def pin_append_mixed_bf16_rows_and_int2(lib):
                 assert np.all(win[b, :, :, r] == 0xFFFF)
 
 
+# --- key offset removal (OptR abstract on the OSCAR paper page) ------------------
+
+def _golden_offset():
+    with open(os.path.join(GOLDEN, "key_offset.json")) as f:
+        return json.load(f)
+
+
+def pin_key_offset_golden_differences(lib):
+    """fp32(k - c) and its bf16 rounding for hand-derived keys and offsets
+    (tests/golden/key_offset.json): both round to nearest even."""
+    for case in _golden_offset()["differences"]:
+        k = np.array([case["k_bits"]], np.uint16)
+        c = np.array([float.fromhex(case["c"])], np.float32)
+        got = float(O.offset_key(k, c, lib=lib)[0])
+        assert got == float.fromhex(case["diff"]), case["name"]
+        assert int(O.f32_to_bf16(np.float32(got), lib=lib)) == case["bf16_bits"], case["name"]
+
+
+def pin_key_offset_golden_append(lib):
+    """One token appended with a key offset (R = I, infinite clip, sink of one
+    row): the INT2 codes, scale and zero are those of k - c, V is untouched, the
+    BF16 sink rows hold bf16(k - c) and v (tests/golden/key_offset.json)."""
+    g = _golden_offset()["append"]
+    dims = g["dims"]
+    D, P, G = dims["head_dim"], dims["page_size"], dims["group_size"]
+    kb = bf16_bits(np.array(g["k"]).reshape(1, 1, D))
+    vb = bf16_bits(np.array(g["v"]).reshape(1, 1, D))
+    R = np.eye(D, dtype=np.float32)[None]
+    ck = np.full((1, D), np.inf, np.float32)
+    off = np.array(g["offset_k"], np.float32).reshape(1, D)
+    pre = O.append_prequant(dims, kb, vb, R, R, ck, ck, offset_k=off, lib=lib)
+    assert np.array_equal(pre[0, 0, 0], g["k_shifted"]) and np.array_equal(pre[0, 0, 1], g["v"])
+    pool = np.full(P * 2 * (D // 4), 0xA5, np.uint8)
+    sz = np.full(P * 2 * (D // G) * 2, 0xA5A5, np.uint16)
+    sink = np.full((1, 2, 1, 1, D), 0xFFFF, np.uint16)
+    win = np.full((1, 2, 1, 1, D), 0xFFFF, np.uint16)
+    one = np.array([1], np.int32)
+    zero = np.array([0], np.int32)
+    rc = O.append_mixed(dims, kb, vb, R, R, ck, ck, np.array([g["slot"]], np.int64), zero, zero, one, 1, 0, pool,
+                        sz, sink, win, offset_k=off, lib=lib)
+    assert rc == 0
+    szv = sz.reshape(2, P, D // G, 2)
+    assert pool[0] == g["k_code_byte"] and pool[P] == g["v_code_byte"]
+    assert tuple(szv[0, 0, 0]) == (g["k_scale_bits"], g["k_zero_bits"])
+    assert tuple(szv[1, 0, 0]) == (g["v_scale_bits"], g["v_zero_bits"])
+    assert list(sink[0, 0, 0, 0]) == g["k_row_bf16_bits"] and list(sink[0, 1, 0, 0]) == g["v_row_bf16_bits"]
+    assert np.all(pool[1:P] == 0xA5) and np.all(pool[P + 1:] == 0xA5)
+
+
+def _offset_case(seed):
+    """Keys and per-(head, channel) offsets on a 1/16 grid, so that k - c has at
+    most 7 significant bits and is exact in bf16; finite clips."""
+    rng = np.random.default_rng(seed)
+    c = _mixed_inputs(seed=seed, lens=(6, 30, 45), S=4, W=12)
+    H, D = c["H"], c["D"]
+    k = rng.integers(-64, 65, size=c["kb"].shape) / 16.0
+    off = (rng.integers(-32, 33, size=(H, D)) / 16.0).astype(np.float32)
+    c["kb"] = bf16_bits(k)
+    c["shifted"] = bf16_bits(k - off[None].astype(np.float64))
+    assert np.array_equal(bf16_vals(c["shifted"]), k - off[None])
+    c["ck"] = rng.uniform(1.0, 3.0, (H, D)).astype(np.float32)
+    c["cv"] = rng.uniform(1.0, 3.0, (H, D)).astype(np.float32)
+    return c, off
+
+
+def _mixed_with(lib, c, keys, offset):
+    bufs = _mixed_buffers(c)
+    n = len(c["seq"])
+    rc = O.append_mixed(c["dims"], keys, c["vb"], c["Rk"], c["Rv"], c["ck"], c["cv"], c["slots"], c["seq"],
+                        c["pos"], c["lens"], c["S"], c["W"], *bufs, offset_k=offset, lib=lib)
+    assert rc == 0 and n == keys.shape[0]
+    return bufs
+
+
+def pin_key_offset_equals_shifted_input(lib):
+    """With k - c exact in bf16, appending k with the offset c leaves the same
+    INT2 pool, scale/zero and BF16 sink/window as appending k - c with no offset
+    (values untouched, each KV head with its own offset); a zero offset is no
+    offset."""
+    c, off = _offset_case(61)
+    with_off = _mixed_with(lib, c, c["kb"], off)
+    shifted = _mixed_with(lib, c, c["shifted"], None)
+    for a, b in zip(with_off, shifted):
+        assert np.array_equal(a, b)
+    zero = _mixed_with(lib, c, c["kb"], np.zeros_like(off))
+    none = _mixed_with(lib, c, c["kb"], None)
+    for a, b in zip(zero, none):
+        assert np.array_equal(a, b)
+    assert not np.array_equal(with_off[0], none[0])     # the offset did change the INT2 keys
+
+
+def pin_key_offset_softmax_invariance(lib):
+    """Every key in the BF16 sink/window (S + W >= L) and k - c exact in bf16:
+    the decode of the cache appended with an offset equals textbook attention
+    over the ORIGINAL keys, since q . c is the same for every key of a query."""
+    c, off = _offset_case(62)
+    d = c["dims"]
+    H, D, P = c["H"], c["D"], c["P"]
+    c["W"] = 64                                          # S + W >= every length
+    pool, sz, sink, win = _mixed_with(lib, c, c["kb"], off)
+    rng = np.random.default_rng(63)
+    B = len(c["lens"])
+    qb = bf16_bits(rng.standard_normal((B, d["num_q_heads"], D)))
+    pt = np.zeros((B, d["max_pages_per_seq"]), np.int32)   # no INT2 page is read
+    out = O.decode(d, B, qb, c["Rk"], c["Rv"], pool, sz, sink, win, pt, c["lens"], c["S"], c["W"], 0.0, lib=lib)
+    out = out.reshape(B, d["num_q_heads"], D)
+    start = np.concatenate([[0], np.cumsum(c["lens"])[:-1]])
+    gqa = d["num_q_heads"] // H
+    for b, L in enumerate(c["lens"]):
+        rows = slice(start[b], start[b] + L)
+        for hq in range(d["num_q_heads"]):
+            h = hq // gqa
+            want = dense_attention(bf16_vals(qb[b, hq]), bf16_vals(c["kb"][rows, h]), bf16_vals(c["vb"][rows, h]),
+                                   1 / math.sqrt(D))
+            assert np.allclose(out[b, hq], want, rtol=0, atol=1e-11), (b, hq)
+
+
 def _extend_rows(lib, c, rows_pos, seed=41, row_seq=None):
     """Extend output [rows][Hq][D] over the single-sequence cache of case ``c`` for query rows
     at the given positions (fresh queries)."""

@@ -23,8 +23,8 @@ CALIB_SRC = os.path.join(os.path.dirname(SRC), "calibration.py")
 # (name, text in the oracle, replacement, expected number of occurrences)
 MUTANTS = [
     ("rotation_transposed",
-     "orc_bf16_to_f64(x_bf16[i]) * static_cast<double>(R[static_cast<size_t>(i) * D + j])",
-     "orc_bf16_to_f64(x_bf16[i]) * static_cast<double>(R[static_cast<size_t>(j) * D + i])", 1),
+     "x[i] * static_cast<double>(R[static_cast<size_t>(i) * D + j])",
+     "x[i] * static_cast<double>(R[static_cast<size_t>(j) * D + i])", 1),
     ("clip_lower_bound_dropped", "    if (x[j] < -c) x[j] = -c;\n", "", 1),
     ("scale_divisor_4", "(mx - mn) / 3.0", "(mx - mn) / 4.0", 1),
     ("zero_is_max", "const float z32 = static_cast<float>(mn);", "const float z32 = static_cast<float>(mx);", 1),
@@ -56,6 +56,18 @@ MUTANTS = [
     ("extend_excludes_own_position", "hq, b, L, pos + 1, R_k", "hq, b, L, pos, R_k", 1),
     ("extend_window_of_prefix_length", "const int win_begin = (L - W > S) ? L - W : S;\n  for (int p = 0; p < A; ++p)",
      "const int win_begin = (A - W > S) ? A - W : S;\n  for (int p = 0; p < A; ++p)", 1),
+    ("key_offset_added", "orc_bf16_to_f64(k_bf16[i]) - static_cast<double>(c[i])",
+     "orc_bf16_to_f64(k_bf16[i]) + static_cast<double>(c[i])", 1),
+    ("key_offset_not_rounded_to_f32",
+     "out[i] = static_cast<double>(static_cast<float>(orc_bf16_to_f64(k_bf16[i]) - static_cast<double>(c[i])));",
+     "out[i] = orc_bf16_to_f64(k_bf16[i]) - static_cast<double>(c[i]);", 1),
+    ("key_offset_on_values_too", "if (kv == 0 && offset_k != nullptr) {\n    orc_offset_key",
+     "if (offset_k != nullptr) {\n    orc_offset_key", 1),
+    ("key_offset_of_head0_for_all", "orc_offset_key(D, x, offset_k + static_cast<size_t>(h) * D, out);",
+     "orc_offset_key(D, x, offset_k, out);", 1),
+    ("mixed_key_row_not_offset", "if (kv == 0 && offset_k != nullptr) {  // the stored key",
+     "if (false) {  // the stored key", 1),
+    ("bf16_rounding_truncates", "u += 0x7fffu + lsb;", "u += 0u * lsb;", 1),
     ("extend_row_as_sequence", "const int b = row_seq[r];", "const int b = r < batch ? r : row_seq[r];", 1),
 ]
 
