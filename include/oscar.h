@@ -90,6 +90,16 @@ typedef struct {
  *   k, v          device bf16 [num_tokens][Hkv][D]
  *   R_k, R_v      device fp32 [Hkv][D][D]
  *   clip_k/_v     device fp32 [Hkv][D]
+ *   offset_k      device fp32 [Hkv][D], finite, 16-byte aligned, or NULL (no
+ *                 offset).  Key offset removal (the OptR abstract on the OSCAR
+ *                 paper page: an attention-equivalent key reparameterisation
+ *                 that removes per-channel key offsets without changing the
+ *                 softmax distribution): every key is taken as
+ *                 x = fp32(k - offset_k[h]) (round to nearest even) before the
+ *                 rotation; values are never offset.  Softmax is unchanged since
+ *                 q . offset_k[h] is the same for every key of a query, so the
+ *                 decode needs no change; the caller keeps the offset fixed for
+ *                 the life of the cache.
  *   page_table    unused (may be NULL): placement is by slot_mapping only
  *   slot_mapping  device int64 [num_tokens]; page * P + offset; < 0 skips the token
  *   int2_pages    device uint8 [num_pages][Hkv][2 = K,V][P][D/4]; channel j of a
@@ -101,11 +111,12 @@ typedef struct {
  * multiply on tensor cores with R split into three
  * bf16 terms (about 24 significant bits), so y may differ from a sequential fp32
  * sum by rounding, and a value within rounding of a code boundary may take the
- * neighbouring code.
+ * neighbouring code.  With an offset that path forms (x . R) - (offset . R), equal
+ * to (k - offset) . R up to rounding.
  */
 oscar_status_t oscar_append(const oscar_dims_t* dims, int64_t num_tokens, const void* k, const void* v,
                             const float* R_k, const float* R_v, const float* clip_k, const float* clip_v,
-                            const int32_t* page_table, const int64_t* slot_mapping, uint8_t* int2_pages,
+                            const float* offset_k, const int32_t* page_table, const int64_t* slot_mapping, uint8_t* int2_pages,
                             void* scale_zero_pages, void* stream);
 
 /*
@@ -113,7 +124,8 @@ oscar_status_t oscar_append(const oscar_dims_t* dims, int64_t num_tokens, const 
  * recent window (project card "How it works": a BF16 sink of the first tokens
  * and a BF16 window of the most recent ones), in the same pass over K/V.
  * Every token with slot_mapping >= 0 is appended to the INT2 pool exactly as by
- * oscar_append.  Its original (unrotated) bf16 K and V rows are also written,
+ * oscar_append.  Its original (unrotated) bf16 K and V rows are also written
+ * (with offset_k, the K row is bf16(fp32(k - offset_k[h])), round to nearest even),
  * for sequence b = seq_ids[t] at position p = positions[t], with
  * L = seq_lens[b] the sequence's length after this append:
  *   p < sink_len                      -> bf16_sink[b][K|V][h][p][:]
@@ -132,7 +144,7 @@ oscar_status_t oscar_append(const oscar_dims_t* dims, int64_t num_tokens, const 
  */
 oscar_status_t oscar_append_mixed(const oscar_dims_t* dims, int64_t num_tokens, const void* k, const void* v,
                                   const float* R_k, const float* R_v, const float* clip_k, const float* clip_v,
-                                  const int32_t* page_table, const int64_t* slot_mapping, const int32_t* seq_ids,
+                                  const float* offset_k, const int32_t* page_table, const int64_t* slot_mapping, const int32_t* seq_ids,
                                   const int32_t* positions, const int32_t* seq_lens, int32_t batch,
                                   int32_t sink_len, int32_t window_len, uint8_t* int2_pages, void* scale_zero_pages,
                                   void* bf16_sink, void* bf16_window, void* stream);

@@ -55,8 +55,8 @@ def _load():
     P, I32, I64, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     D = ctypes.POINTER(oscar_dims_t)
     sigs = {
-        "oscar_append": (I32, [D, I64, P, P, P, P, P, P, P, P, P, P, P]),
-        "oscar_append_mixed": (I32, [D, I64, P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, P, P, P, P, P]),
+        "oscar_append": (I32, [D, I64, P, P, P, P, P, P, P, P, P, P, P, P]),
+        "oscar_append_mixed": (I32, [D, I64, P, P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, P, P, P, P, P]),
         "oscar_decode_workspace_bytes": (SZ, [D, I32, I32, I32, I32, I32]),
         "oscar_decode_plan": (I32, [D, I32, I32, I32, I32, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
                                     ctypes.POINTER(I32)]),
@@ -140,20 +140,23 @@ def _check(status: int, where: str):
 
 
 def oscar_append(dims, k, v, R_k, R_v, clip_k, clip_v, page_table, slot_mapping, int2_pages, scale_zero_pages,
-                 stream=None):
-    """Rotate, clip, INT2-quantise and store k/v (bf16 [T][Hkv][D]) at slot_mapping."""
+                 stream=None, offset_k=None):
+    """Rotate, clip, INT2-quantise and store k/v (bf16 [T][Hkv][D]) at slot_mapping;
+    ``offset_k`` (fp32 [Hkv][D] or None) is subtracted from every key first."""
     _check(lib.oscar_append(ctypes.byref(_dims(dims)), int(k.shape[0]), _ptr(k), _ptr(v), _ptr(R_k), _ptr(R_v),
-                            _ptr(clip_k), _ptr(clip_v), _ptr(page_table), _ptr(slot_mapping), _ptr(int2_pages),
-                            _ptr(scale_zero_pages), _stream(stream)), "oscar_append")
+                            _ptr(clip_k), _ptr(clip_v), _ptr(offset_k), _ptr(page_table), _ptr(slot_mapping),
+                            _ptr(int2_pages), _ptr(scale_zero_pages), _stream(stream)), "oscar_append")
 
 
 def oscar_append_mixed(dims, k, v, R_k, R_v, clip_k, clip_v, page_table, slot_mapping, seq_ids, positions,
                        seq_lens, sink_len, window_len, int2_pages, scale_zero_pages, bf16_sink, bf16_window,
-                       stream=None):
+                       stream=None, offset_k=None):
     """oscar_append plus the tokens' bf16 rows in the sink (position < sink_len) and
-    the window ring (positions of the window after this append)."""
+    the window ring (positions of the window after this append); with ``offset_k``
+    the K rows are the offset keys."""
     _check(lib.oscar_append_mixed(ctypes.byref(_dims(dims)), int(k.shape[0]), _ptr(k), _ptr(v), _ptr(R_k),
-                                  _ptr(R_v), _ptr(clip_k), _ptr(clip_v), _ptr(page_table), _ptr(slot_mapping),
+                                  _ptr(R_v), _ptr(clip_k), _ptr(clip_v), _ptr(offset_k), _ptr(page_table),
+                                  _ptr(slot_mapping),
                                   _ptr(seq_ids), _ptr(positions), _ptr(seq_lens), int(seq_lens.shape[0]),
                                   int(sink_len), int(window_len), _ptr(int2_pages), _ptr(scale_zero_pages),
                                   _ptr(bf16_sink), _ptr(bf16_window), _stream(stream)), "oscar_append_mixed")

@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (make_dims, oscar_append, oscar_bf16_append, oscar_bf16_decode, oscar_bf16_decode_workspace_bytes,
+from . import (make_dims, oscar_append, oscar_append_mixed, oscar_bf16_append, oscar_bf16_decode, oscar_bf16_decode_workspace_bytes,
                oscar_calibrate, oscar_calibrate_workspace_bytes, oscar_decode, oscar_decode_workspace_bytes,
                oscar_extend, oscar_extend_varlen, oscar_extend_varlen_workspace_bytes, oscar_extend_workspace_bytes)
 from .synth import Workload
@@ -34,6 +34,7 @@ class Int2Cache:
         self.seq_lens = w.seq_lens.to(self.device)
         self.R_k, self.R_v = w.R_k.to(self.device), w.R_v.to(self.device)
         self.clip_k, self.clip_v = w.clip_k.to(self.device), w.clip_v.to(self.device)
+        self.offset_k = None if w.offset_k is None else w.offset_k.to(self.device).contiguous()
         self.pps = w.pages_per_split if pages_per_split is None else pages_per_split
         self.sink = None
         self.window = None
@@ -41,11 +42,23 @@ class Int2Cache:
 
     def append(self, k, v, slot_mapping, stream=None):
         oscar_append(self.dims, k, v, self.R_k, self.R_v, self.clip_k, self.clip_v, self.page_table, slot_mapping,
-                     self.int2_pages, self.scale_zero, stream)
+                     self.int2_pages, self.scale_zero, stream, offset_k=self.offset_k)
 
     def prefill(self, stream=None):
-        """Append every token of the workload and fill the BF16 sink/window buffers."""
+        """Append every token of the workload and fill the BF16 sink/window buffers
+        (with a key offset, both in one oscar_append_mixed call, which stores the
+        offset keys in the BF16 rows)."""
         w = self.w
+        if self.offset_k is not None:
+            B, H, D = w.batch, w.num_kv_heads, w.head_dim
+            self.sink = torch.zeros((B, 2, H, max(w.sink_len, 1), D), dtype=torch.bfloat16, device=self.device)
+            self.window = torch.zeros((B, 2, H, max(w.window_len, 1), D), dtype=torch.bfloat16, device=self.device)
+            d = self.device
+            oscar_append_mixed(self.dims, w.k.to(d), w.v.to(d), self.R_k, self.R_v, self.clip_k, self.clip_v,
+                               self.page_table, w.slot_mapping.to(d), w.tok_seq.to(d), w.tok_pos.to(d), self.seq_lens,
+                               w.sink_len, w.window_len, self.int2_pages, self.scale_zero, self.sink, self.window,
+                               stream, offset_k=self.offset_k)
+            return
         self.append(w.k.to(self.device), w.v.to(self.device), w.slot_mapping.to(self.device), stream)
         sink, win = w.sink_window()
         self.sink, self.window = sink.to(self.device), win.to(self.device)

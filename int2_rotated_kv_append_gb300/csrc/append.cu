@@ -5,6 +5,11 @@
 // "Practical Summary" -- fixed rotations and clipping thresholds, 2-bit KV
 // cache; abstract -- paged KV cache).
 //
+// With a key offset c (fp32 [Hkv][D]; the OptR abstract on the same paper page:
+// an attention-equivalent key reparameterisation that removes per-channel key
+// offsets without changing softmax), every key is rotated as k - c, and the BF16
+// sink/window key rows hold bf16(k - c); values are never offset.
+//
 // One CTA owns a tile of 32 tokens of one (KV head, K|V) pair, so R (fp32,
 // 64 KB at D = 128) is staged once in shared memory and reused by all tokens of
 // the tile.  Each warp rotates 4 tokens; lane l owns channels [l*D/32,
@@ -119,12 +124,40 @@ __device__ __forceinline__ void quantize_store(const float (&acc)[D / 32], const
   }
 }
 
+// Stages the bf16 rows of tokens [t0, t0 + ntok) of head h into xs (fp32 [ntok][D]),
+// subtracting the key offset off (nullptr: none) in fp32, and writes each token's
+// BF16 row (the offset key rounded to bf16) to its sink/window row when it has one.
+template <int D>
+__device__ __forceinline__ void stage_rows(const __nv_bfloat16* __restrict__ x, const float* __restrict__ off,
+                                           int64_t t0, int ntok, int64_t num_tokens, int H, int h,
+                                           const MixedDst& md, const int64_t* dst_row, const int* dst_buf,
+                                           float* xs) {
+  for (int i = threadIdx.x; i < ntok * D / 2; i += blockDim.x) {
+    const int tt = i / (D / 2), c2 = i % (D / 2);
+    const int64_t t = t0 + tt;
+    float2 val = make_float2(0.f, 0.f);
+    if (t < num_tokens) {
+      __nv_bfloat162 raw = reinterpret_cast<const __nv_bfloat162*>(x + (static_cast<size_t>(t) * H + h) * D)[c2];
+      val = __bfloat1622float2(raw);
+      if (off != nullptr) {
+        const float2 c = __ldg(reinterpret_cast<const float2*>(off) + c2);
+        val = make_float2(__fsub_rn(val.x, c.x), __fsub_rn(val.y, c.y));
+        raw = __floats2bfloat162_rn(val.x, val.y);
+      }
+      if (md.active() && dst_row[tt] >= 0)
+        reinterpret_cast<__nv_bfloat162*>((dst_buf[tt] ? md.win : md.sink) + dst_row[tt])[c2] = raw;
+    }
+    xs[tt * D + 2 * c2] = val.x;
+    xs[tt * D + 2 * c2 + 1] = val.y;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) append_kernel(
     int64_t num_tokens, int H, int G, int num_pages, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ R_k, const float* __restrict__ R_v,
-    const float* __restrict__ clip_k, const float* __restrict__ clip_v, const int64_t* __restrict__ slots,
-    uint8_t* __restrict__ codes, __half* __restrict__ sz, MixedDst md) {
+    const float* __restrict__ clip_k, const float* __restrict__ clip_v, const float* __restrict__ offset_k,
+    const int64_t* __restrict__ slots, uint8_t* __restrict__ codes, __half* __restrict__ sz, MixedDst md) {
   grid_dep_launch_dependents();  // a following q-rotation (reads neither output) may start
   constexpr int CPL = D / 32;  // channels per lane
   extern __shared__ __align__(16) float smem[];
@@ -147,19 +180,8 @@ __global__ void __launch_bounds__(kThreads) append_kernel(
     dst_buf[threadIdx.x] = which;
   }
   if (md.active()) __syncthreads();
-  for (int i = threadIdx.x; i < kTokTile * D / 2; i += kThreads) {
-    const int tt = i / (D / 2), c2 = i % (D / 2);
-    const int64_t t = t0 + tt;
-    float2 val = make_float2(0.f, 0.f);
-    if (t < num_tokens) {
-      const __nv_bfloat162 raw = reinterpret_cast<const __nv_bfloat162*>(x + (static_cast<size_t>(t) * H + h) * D)[c2];
-      val = __bfloat1622float2(raw);
-      if (md.active() && dst_row[tt] >= 0)
-        reinterpret_cast<__nv_bfloat162*>((dst_buf[tt] ? md.win : md.sink) + dst_row[tt])[c2] = raw;
-    }
-    xs[tt * D + 2 * c2] = val.x;
-    xs[tt * D + 2 * c2 + 1] = val.y;
-  }
+  const float* off = (kv == 0 && offset_k != nullptr) ? offset_k + static_cast<size_t>(h) * D : nullptr;
+  stage_rows<D>(x, off, t0, kTokTile, num_tokens, H, h, md, dst_row, dst_buf, xs);
   __syncthreads();
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -236,8 +258,15 @@ constexpr uint32_t kUmTmemCols = 128 * kUmGroups; // one 128-column fp32 accumul
 static_assert(kUmTmemCols == 512 || kUmTmemCols == 256, "TMEM allocation must be a power of two");
 // barriers: x_full, x_empty per stage; acc_full, acc_empty per group
 constexpr int kUmBars = 2 * kUmStages + 2 * kUmGroups;
-// R^T terms | x stages | clip | mbarriers | TMEM address, counters; +1 KB to align to 1024
-constexpr size_t kUmSmem = 1024 + 3 * kUmRPart + kUmStages * kUmXBytes + 128 * 4 + kUmBars * 8 + 16;
+// R^T terms | x stages | clip | c . R | partial c . R (4 x 128) | mbarriers | TMEM address,
+// counters; +1 KB to align to 1024
+constexpr size_t kUmSmem = 1024 + 3 * kUmRPart + kUmStages * kUmXBytes + 6 * 128 * 4 + kUmBars * 8 + 16;
+
+// Two bf16 keys (one 32-bit word) minus their offsets in fp32, rounded back to bf16.
+__device__ __forceinline__ uint32_t offset_pair(uint32_t w, float c0, float c1) {
+  const float a = __uint_as_float(w << 16), b = __uint_as_float(w & 0xffff0000u);
+  return bf16_pair(__float2bfloat16_rn(__fsub_rn(a, c0)), __float2bfloat16_rn(__fsub_rn(b, c1)));
+}
 
 // Exact code of one value (the quotient path of the append's rule).
 __device__ __forceinline__ uint32_t exact_code(float y, float z, float s) {
@@ -249,8 +278,8 @@ __global__ void __launch_bounds__(kUmThreads, 1) append_umma_kernel(
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v, int64_t num_tokens, int H,
     int num_pages, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
     const float* __restrict__ R_k, const float* __restrict__ R_v, const float* __restrict__ clip_k,
-    const float* __restrict__ clip_v, const int64_t* __restrict__ slots, uint8_t* __restrict__ codes,
-    __half* __restrict__ sz, MixedDst md) {
+    const float* __restrict__ clip_v, const float* __restrict__ offset_k, const int64_t* __restrict__ slots,
+    uint8_t* __restrict__ codes, __half* __restrict__ sz, MixedDst md) {
   grid_dep_launch_dependents();  // a following q-rotation (reads neither output) may start
   constexpr int D = 128, NGRP = D / G;
   extern __shared__ uint8_t usm_raw[];
@@ -258,7 +287,9 @@ __global__ void __launch_bounds__(kUmThreads, 1) append_umma_kernel(
   const uint32_t r_s = smem_u32(usm);       // 3 terms of R^T, K-major, swizzled
   const uint32_t x_s = r_s + 3 * kUmRPart;  // x stages
   float* clip_s = reinterpret_cast<float*>(usm + 3 * kUmRPart + kUmStages * kUmXBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(clip_s + 128);
+  float* cr_s = clip_s + 128;    // c . R of the key offset (K with an offset only)
+  float* cr_part = cr_s + 128;   // its four partial sums over 32 rows of R each
+  uint64_t* bars = reinterpret_cast<uint64_t*>(cr_part + 4 * 128);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kUmBars);
   uint32_t* flags = tmem_slot + 1;  // [0]: x tiles requested, [1]: x tiles consumed, [2]: MMA chains committed
   auto x_full = [&](int st) { return smem_u32(&bars[st]); };
@@ -272,6 +303,8 @@ __global__ void __launch_bounds__(kUmThreads, 1) append_umma_kernel(
   const int n_my = static_cast<int>((ntiles - j0 + per - 1) / per);  // tiles j0, j0 + per, ...
   const float* R = (kv ? R_v : R_k) + static_cast<size_t>(h) * D * D;
   const CUtensorMap* map = kv ? &map_v : &map_k;
+  // With a key offset c the K accumulator x . R is reduced by c . R (= (x - c) . R).
+  const float* key_off = (kv == 0 && offset_k != nullptr) ? offset_k + static_cast<size_t>(h) * D : nullptr;
 
   if (tid == 0) {
     for (int i = 0; i < kUmStages; ++i) {
@@ -336,11 +369,22 @@ __global__ void __launch_bounds__(kUmThreads, 1) append_umma_kernel(
     }
   }
   if (tid < D) clip_s[tid] = __ldg((kv ? clip_v : clip_k) + static_cast<size_t>(h) * D + tid);
+  if (key_off != nullptr && tid < 4 * D) {  // partial (c . R)_j over rows 32 qq .. 32 qq + 31
+    const int j = tid & (D - 1), qq = tid / D;
+    float a = 0.f;
+#pragma unroll 8
+    for (int i = 32 * qq; i < 32 * qq + 32; ++i) a = fmaf(__ldg(key_off + i), __ldg(R + static_cast<size_t>(i) * D + j), a);
+    cr_part[tid] = a;
+  }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // R^T visible to the tensor cores
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  if (key_off != nullptr) {  // CTA-uniform
+    if (tid < D) cr_s[tid] = (cr_part[tid] + cr_part[D + tid]) + (cr_part[2 * D + tid] + cr_part[3 * D + tid]);
+    __syncthreads();
+  }
 
   if (warp == 0) {
     // ---- TMA producer ----
@@ -410,6 +454,16 @@ __global__ void __launch_bounds__(kUmThreads, 1) append_umma_kernel(
         uint32_t vb[32];
         umma::tmem_ld32(ta + 32 * c, vb);
         umma::tmem_ld_wait();
+        if (key_off != nullptr) {
+          const float4* cr4 = reinterpret_cast<const float4*>(cr_s) + 8 * c;
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 o = cr4[i4];
+            const float ov[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) vb[4 * i4 + r] = __float_as_uint(__uint_as_float(vb[4 * i4 + r]) - ov[r]);
+          }
+        }
         float lo[4] = {INFINITY, INFINITY, INFINITY, INFINITY}, hi[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
@@ -518,8 +572,19 @@ __global__ void __launch_bounds__(kUmThreads, 1) append_umma_kernel(
         if (dst >= 0) {
           const uint4* src = reinterpret_cast<const uint4*>((kv ? v : k) + (static_cast<size_t>(t) * H + h) * D);
           uint4* out = reinterpret_cast<uint4*>((which ? md.win : md.sink) + dst);
+          if (key_off != nullptr) {  // the offset key, rounded to bf16
+            const float4* c4 = reinterpret_cast<const float4*>(key_off);
 #pragma unroll 4
-          for (int c = 0; c < D / 8; ++c) out[c] = __ldg(src + c);
+            for (int c = 0; c < D / 8; ++c) {
+              const uint4 w = __ldg(src + c);
+              const float4 ca = __ldg(c4 + 2 * c), cb = __ldg(c4 + 2 * c + 1);
+              out[c] = make_uint4(offset_pair(w.x, ca.x, ca.y), offset_pair(w.y, ca.z, ca.w),
+                                  offset_pair(w.z, cb.x, cb.y), offset_pair(w.w, cb.z, cb.w));
+            }
+          } else {
+#pragma unroll 4
+            for (int c = 0; c < D / 8; ++c) out[c] = __ldg(src + c);
+          }
         }
       }
       if (slot >= static_cast<int64_t>(num_pages) * kPageSize) {
@@ -573,8 +638,9 @@ bool x_tensor_map(CUtensorMap* m, const void* x, int64_t T, int H) {
 
 template <int G>
 cudaError_t launch_append_umma(int64_t T, const oscar_dims_t* d, const void* k, const void* v, const float* R_k,
-                               const float* R_v, const float* clip_k, const float* clip_v, const int64_t* slots,
-                               uint8_t* codes, void* sz, const MixedDst& md, cudaStream_t stream) {
+                               const float* R_v, const float* clip_k, const float* clip_v, const float* offset_k,
+                               const int64_t* slots, uint8_t* codes, void* sz, const MixedDst& md,
+                               cudaStream_t stream) {
   CUtensorMap mk, mv;
   if (!x_tensor_map(&mk, k, T, d->num_kv_heads) || !x_tensor_map(&mv, v, T, d->num_kv_heads))
     return cudaErrorInvalidValue;
@@ -590,7 +656,8 @@ cudaError_t launch_append_umma(int64_t T, const oscar_dims_t* d, const void* k, 
   const dim3 grid(static_cast<unsigned>(per), d->num_kv_heads, 2);
   append_umma_kernel<G><<<grid, kUmThreads, kUmSmem, stream>>>(
       mk, mv, T, d->num_kv_heads, d->num_pages, static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz), md);
+      static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, offset_k, slots, codes,
+      static_cast<__half*>(sz), md);
   return cudaGetLastError();
 }
 
@@ -598,8 +665,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads) append_small_kernel(
     int64_t num_tokens, int H, int G, int num_pages, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ R_k, const float* __restrict__ R_v,
-    const float* __restrict__ clip_k, const float* __restrict__ clip_v, const int64_t* __restrict__ slots,
-    uint8_t* __restrict__ codes, __half* __restrict__ sz, MixedDst md) {
+    const float* __restrict__ clip_k, const float* __restrict__ clip_v, const float* __restrict__ offset_k,
+    const int64_t* __restrict__ slots, uint8_t* __restrict__ codes, __half* __restrict__ sz, MixedDst md) {
   grid_dep_launch_dependents();  // a following q-rotation (reads neither output) may start
   constexpr int CPL = D / 32;
   constexpr int kWarpsA = kThreads / 32;
@@ -641,19 +708,8 @@ __global__ void __launch_bounds__(kThreads) append_small_kernel(
     dst_buf[threadIdx.x] = which;
   }
   if (md.active()) __syncthreads();
-  for (int i = threadIdx.x; i < kSmallTok * D / 2; i += kThreads) {
-    const int tt = i / (D / 2), c2 = i % (D / 2);
-    const int64_t t = t0 + tt;
-    float2 val = make_float2(0.f, 0.f);
-    if (t < num_tokens) {
-      const __nv_bfloat162 raw = reinterpret_cast<const __nv_bfloat162*>(x + (static_cast<size_t>(t) * H + h) * D)[c2];
-      val = __bfloat1622float2(raw);
-      if (md.active() && dst_row[tt] >= 0)
-        reinterpret_cast<__nv_bfloat162*>((dst_buf[tt] ? md.win : md.sink) + dst_row[tt])[c2] = raw;
-    }
-    xs[tt * D + 2 * c2] = val.x;
-    xs[tt * D + 2 * c2 + 1] = val.y;
-  }
+  const float* off = (kv == 0 && offset_k != nullptr) ? offset_k + static_cast<size_t>(h) * D : nullptr;
+  stage_rows<D>(x, off, t0, kSmallTok, num_tokens, H, h, md, dst_row, dst_buf, xs);
   __syncthreads();
   float acc[kSmallTok][CPL];
 #pragma unroll
@@ -719,21 +775,26 @@ __global__ void bf16_append_kernel(int64_t num_tokens, int H, int D, int num_pag
 
 template <int D>
 cudaError_t launch_append(int64_t T, const oscar_dims_t* d, const void* k, const void* v, const float* R_k,
-                          const float* R_v, const float* clip_k, const float* clip_v, const int64_t* slots,
-                          uint8_t* codes, void* sz, const MixedDst& md, cudaStream_t stream) {
+                          const float* R_v, const float* clip_k, const float* clip_v, const float* offset_k,
+                          const int64_t* slots, uint8_t* codes, void* sz, const MixedDst& md,
+                          cudaStream_t stream) {
   // Few tokens per (head, K|V): spread R's rows over warps instead of staging all of R.
   if (T <= kSmallTokenLimit) {
     const dim3 grid(static_cast<unsigned>((T + kSmallTok - 1) / kSmallTok), d->num_kv_heads, 2);
     append_small_kernel<D><<<grid, kThreads, 0, stream>>>(
         T, d->num_kv_heads, d->group_size, d->num_pages, static_cast<const __nv_bfloat16*>(k),
-        static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz), md);
+        static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, offset_k, slots, codes,
+        static_cast<__half*>(sz), md);
     return cudaGetLastError();
   }
   if (D == 128 && T < 0x7fffffffLL - kUmTok) {  // the rotation on tcgen05 tensor cores
     switch (d->group_size) {
-      case 32: return launch_append_umma<32>(T, d, k, v, R_k, R_v, clip_k, clip_v, slots, codes, sz, md, stream);
-      case 64: return launch_append_umma<64>(T, d, k, v, R_k, R_v, clip_k, clip_v, slots, codes, sz, md, stream);
-      default: return launch_append_umma<128>(T, d, k, v, R_k, R_v, clip_k, clip_v, slots, codes, sz, md, stream);
+      case 32: return launch_append_umma<32>(T, d, k, v, R_k, R_v, clip_k, clip_v, offset_k, slots, codes, sz, md,
+                                               stream);
+      case 64: return launch_append_umma<64>(T, d, k, v, R_k, R_v, clip_k, clip_v, offset_k, slots, codes, sz, md,
+                                               stream);
+      default: return launch_append_umma<128>(T, d, k, v, R_k, R_v, clip_k, clip_v, offset_k, slots, codes, sz, md,
+                                               stream);
     }
   }
   const size_t smem = (static_cast<size_t>(D) * D + kTokTile * D) * sizeof(float);
@@ -742,7 +803,8 @@ cudaError_t launch_append(int64_t T, const oscar_dims_t* d, const void* k, const
   const dim3 grid(static_cast<unsigned>((T + kTokTile - 1) / kTokTile), d->num_kv_heads, 2);
   append_kernel<D><<<grid, kThreads, smem, stream>>>(
       T, d->num_kv_heads, d->group_size, d->num_pages, static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, slots, codes, static_cast<__half*>(sz), md);
+      static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, offset_k, slots, codes,
+      static_cast<__half*>(sz), md);
   return cudaGetLastError();
 }
 
@@ -752,8 +814,8 @@ namespace {
 
 oscar_status_t run_append(const oscar_dims_t* dims, int64_t num_tokens, const void* k, const void* v,
                           const float* R_k, const float* R_v, const float* clip_k, const float* clip_v,
-                          const int64_t* slot_mapping, uint8_t* int2_pages, void* scale_zero_pages,
-                          const MixedDst& md, void* stream) {
+                          const float* offset_k, const int64_t* slot_mapping, uint8_t* int2_pages,
+                          void* scale_zero_pages, const MixedDst& md, void* stream) {
   oscar_status_t st = check_dims(dims);
   if (st != OSCAR_OK) return st;
   if (num_tokens < 0) return OSCAR_ERR_INVALID_ARG;
@@ -761,14 +823,14 @@ oscar_status_t run_append(const oscar_dims_t* dims, int64_t num_tokens, const vo
   if (!k || !v || !R_k || !R_v || !clip_k || !clip_v || !slot_mapping || !int2_pages || !scale_zero_pages)
     return OSCAR_ERR_INVALID_ARG;
   if (misaligned16(k) || misaligned16(v) || misaligned16(R_k) || misaligned16(R_v) || misaligned16(int2_pages) ||
-      misaligned16(scale_zero_pages) || misaligned16(md.sink) || misaligned16(md.win))
+      misaligned16(scale_zero_pages) || misaligned16(md.sink) || misaligned16(md.win) || misaligned16(offset_k))
     return OSCAR_ERR_INVALID_ARG;
   if ((num_tokens + kTokTile - 1) / kTokTile > 0x7fffffffLL) return OSCAR_ERR_UNSUPPORTED;
   cudaError_t e = dims->head_dim == 128
-                      ? launch_append<128>(num_tokens, dims, k, v, R_k, R_v, clip_k, clip_v, slot_mapping,
-                                           int2_pages, scale_zero_pages, md, as_stream(stream))
-                      : launch_append<64>(num_tokens, dims, k, v, R_k, R_v, clip_k, clip_v, slot_mapping,
-                                          int2_pages, scale_zero_pages, md, as_stream(stream));
+                      ? launch_append<128>(num_tokens, dims, k, v, R_k, R_v, clip_k, clip_v, offset_k,
+                                           slot_mapping, int2_pages, scale_zero_pages, md, as_stream(stream))
+                      : launch_append<64>(num_tokens, dims, k, v, R_k, R_v, clip_k, clip_v, offset_k,
+                                          slot_mapping, int2_pages, scale_zero_pages, md, as_stream(stream));
   return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
@@ -776,17 +838,18 @@ oscar_status_t run_append(const oscar_dims_t* dims, int64_t num_tokens, const vo
 
 extern "C" oscar_status_t oscar_append(const oscar_dims_t* dims, int64_t num_tokens, const void* k, const void* v,
                                        const float* R_k, const float* R_v, const float* clip_k,
-                                       const float* clip_v, const int32_t* page_table,
+                                       const float* clip_v, const float* offset_k, const int32_t* page_table,
                                        const int64_t* slot_mapping, uint8_t* int2_pages, void* scale_zero_pages,
                                        void* stream) {
   (void)page_table;
-  return run_append(dims, num_tokens, k, v, R_k, R_v, clip_k, clip_v, slot_mapping, int2_pages, scale_zero_pages,
-                    MixedDst{}, stream);
+  return run_append(dims, num_tokens, k, v, R_k, R_v, clip_k, clip_v, offset_k, slot_mapping, int2_pages,
+                    scale_zero_pages, MixedDst{}, stream);
 }
 
 extern "C" oscar_status_t oscar_append_mixed(const oscar_dims_t* dims, int64_t num_tokens, const void* k,
                                              const void* v, const float* R_k, const float* R_v,
-                                             const float* clip_k, const float* clip_v, const int32_t* page_table,
+                                             const float* clip_k, const float* clip_v, const float* offset_k,
+                                             const int32_t* page_table,
                                              const int64_t* slot_mapping, const int32_t* seq_ids,
                                              const int32_t* positions, const int32_t* seq_lens, int32_t batch,
                                              int32_t sink_len, int32_t window_len, uint8_t* int2_pages,
@@ -805,8 +868,8 @@ extern "C" oscar_status_t oscar_append_mixed(const oscar_dims_t* dims, int64_t n
   md.W = window_len;
   md.sink = sink_len > 0 ? static_cast<__nv_bfloat16*>(bf16_sink) : nullptr;
   md.win = window_len > 0 ? static_cast<__nv_bfloat16*>(bf16_window) : nullptr;
-  return run_append(dims, num_tokens, k, v, R_k, R_v, clip_k, clip_v, slot_mapping, int2_pages, scale_zero_pages,
-                    md, stream);
+  return run_append(dims, num_tokens, k, v, R_k, R_v, clip_k, clip_v, offset_k, slot_mapping, int2_pages,
+                    scale_zero_pages, md, stream);
 }
 
 extern "C" oscar_status_t oscar_bf16_append(const oscar_dims_t* dims, int64_t num_tokens, const void* k,

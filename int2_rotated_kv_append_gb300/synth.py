@@ -64,6 +64,7 @@ class Workload:
     clip_k: torch.Tensor            # fp32 [Hkv][D]
     clip_v: torch.Tensor            # fp32 [Hkv][D]
     seed: int = 0
+    offset_k: torch.Tensor | None = None  # fp32 [Hkv][D] key offset (None: keys are not offset)
 
     @property
     def dims(self) -> dict:
@@ -82,7 +83,10 @@ class Workload:
     def sink_window(self) -> tuple[torch.Tensor, torch.Tensor]:
         """BF16 sink [B][2][Hkv][S][D] and window ring [B][2][Hkv][W][D] holding the
         original (unrotated) K/V of positions p < S and of p in [max(S, L-W), L)
-        at ring slot p % W.  Slots that hold no token are zero."""
+        at ring slot p % W.  Slots that hold no token are zero.  Workloads with a key
+        offset have no such buffers here: the library's mixed append writes them."""
+        if self.offset_k is not None:
+            raise ValueError("sink/window of a workload with a key offset come from oscar_append_mixed")
         B, H, D, S, W = self.batch, self.num_kv_heads, self.head_dim, self.sink_len, self.window_len
         dev = self.k.device
         sink = torch.zeros((B, 2, H, max(S, 1), D), dtype=torch.bfloat16, device=dev)
@@ -155,9 +159,11 @@ def make_workload(*, num_q_heads: int, num_kv_heads: int, head_dim: int, group_s
                   window_len: int, seq_lens, seed: int, device="cpu", k_kind: str = "qwen",
                   page_size: int = PAGE_SIZE, pages_per_split: int = 0, spare_pages: int = 0,
                   shuffle_pages: bool = True, name: str = "custom", same_rotation: bool = False,
-                  clip_frac: float | None = 0.9) -> Workload:
+                  clip_frac: float | None = 0.9, key_offset: bool = False) -> Workload:
     """Build a workload with the given shape.  Every sequence's tokens are drawn
-    and given slots in a shared page pool (random page order when shuffled)."""
+    and given slots in a shared page pool (random page order when shuffled).
+    ``key_offset``: the workload carries a key offset, the per-(KV head, channel)
+    mean of its keys in fp32, and K's clipping thresholds are taken on k - offset."""
     device = torch.device(device)
     gen_cpu = torch.Generator(device="cpu").manual_seed(seed)
     gen_dev = torch.Generator(device=device).manual_seed(seed + 1_000_003)
@@ -186,18 +192,20 @@ def make_workload(*, num_q_heads: int, num_kv_heads: int, head_dim: int, group_s
         torch.zeros(0, dtype=torch.int32)
     pages = page_table.to(torch.int64)[tok_seq.to(torch.int64), (tok_pos // P).to(torch.int64)]
     slot_mapping = pages * P + (tok_pos % P).to(torch.int64)
+    offset_k = k.to(torch.float32).mean(dim=0).contiguous() if key_offset and T else None
     if clip_frac is None:
         clip_k = torch.full((H, D), float("inf"), dtype=torch.float32)
         clip_v = clip_k.clone()
     else:
-        clip_k = clip_thresholds(k, R_k, clip_frac)
+        clip_k = clip_thresholds(k if offset_k is None else k.to(torch.float32) - offset_k, R_k, clip_frac)
         clip_v = clip_thresholds(v, R_v, clip_frac)
     return Workload(name=name, num_q_heads=Hq, num_kv_heads=H, head_dim=D, page_size=P, group_size=group_size,
                     sink_len=sink_len, window_len=window_len, batch=B, num_pages=num_pages,
                     max_pages_per_seq=max_pages, pages_per_split=pages_per_split,
                     seq_lens=torch.tensor(seq_lens, dtype=torch.int32), page_table=page_table, k=k, v=v,
                     tok_seq=tok_seq, tok_pos=tok_pos, slot_mapping=slot_mapping, q=q, R_k=R_k.to(device),
-                    R_v=R_v.to(device), clip_k=clip_k.to(device), clip_v=clip_v.to(device), seed=seed)
+                    R_v=R_v.to(device), clip_k=clip_k.to(device), clip_v=clip_v.to(device), seed=seed,
+                    offset_k=offset_k)
 
 
 # The five workloads: sizes and distributions as their descriptions state.

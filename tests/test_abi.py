@@ -46,9 +46,9 @@ def _dims(**kw):
 P = ctypes.c_void_p(16)  # never dereferenced: validation fails before any launch
 
 
-def _append(lib, dims, T=4, ptr=P):
+def _append(lib, dims, T=4, ptr=P, offset=None):
     return lib.oscar_append(ctypes.byref(dims) if dims is not None else None, T, ptr, ptr, ptr, ptr, ptr, ptr,
-                            None, ptr, ptr, ptr, None)
+                            offset, None, ptr, ptr, ptr, None)
 
 
 def test_append_validation(lib):
@@ -64,6 +64,7 @@ def test_append_validation(lib):
     assert _append(lib, _dims(), T=0) == ok.OSCAR_OK  # no-op
     assert _append(lib, _dims(), ptr=None) == ok.OSCAR_ERR_INVALID_ARG
     assert _append(lib, _dims(), ptr=ctypes.c_void_p(18)) == ok.OSCAR_ERR_INVALID_ARG  # misaligned
+    assert _append(lib, _dims(), offset=ctypes.c_void_p(24)) == ok.OSCAR_ERR_INVALID_ARG  # misaligned key offset
 
 
 def test_append_rejects_each_misaligned_buffer(lib):
@@ -72,17 +73,17 @@ def test_append_rejects_each_misaligned_buffer(lib):
     for i in (0, 1, 2, 3, 7, 8):
         a = [P] * 9
         a[i] = bad
-        rc = lib.oscar_append(ctypes.byref(_dims()), 4, a[0], a[1], a[2], a[3], a[4], a[5], None, a[6], a[7], a[8],
-                              None)
+        rc = lib.oscar_append(ctypes.byref(_dims()), 4, a[0], a[1], a[2], a[3], a[4], a[5], None, None, a[6], a[7],
+                              a[8], None)
         assert rc == ok.OSCAR_ERR_INVALID_ARG, i
     d = _dims(); bd = ok.OSCAR_ERR_INVALID_ARG
     assert lib.oscar_bf16_append(ctypes.byref(d), 4, bad, P, P, P, None) == bd
     assert lib.oscar_bf16_append(ctypes.byref(d), 4, P, P, P, bad, None) == bd
 
 
-def _append_mixed(lib, dims, T=4, ptr=P, batch=2, S=4, W=8, sink=P, win=P, ids=P):
-    return lib.oscar_append_mixed(ctypes.byref(dims), T, ptr, ptr, ptr, ptr, ptr, ptr, None, ptr, ids, ids, ids,
-                                  batch, S, W, ptr, ptr, sink, win, None)
+def _append_mixed(lib, dims, T=4, ptr=P, batch=2, S=4, W=8, sink=P, win=P, ids=P, offset=None):
+    return lib.oscar_append_mixed(ctypes.byref(dims), T, ptr, ptr, ptr, ptr, ptr, ptr, offset, None, ptr, ids, ids,
+                                  ids, batch, S, W, ptr, ptr, sink, win, None)
 
 
 def test_append_mixed_validation(lib):
@@ -98,6 +99,7 @@ def test_append_mixed_validation(lib):
     assert _append_mixed(lib, _dims(), ptr=None) == ok.OSCAR_ERR_INVALID_ARG
     assert _append_mixed(lib, _dims(), sink=ctypes.c_void_p(20)) == ok.OSCAR_ERR_INVALID_ARG  # misaligned
     assert _append_mixed(lib, _dims(), win=ctypes.c_void_p(24)) == ok.OSCAR_ERR_INVALID_ARG
+    assert _append_mixed(lib, _dims(), offset=ctypes.c_void_p(40)) == ok.OSCAR_ERR_INVALID_ARG
 
 
 def test_extend_validation(lib):
