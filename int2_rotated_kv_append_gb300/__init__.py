@@ -75,6 +75,7 @@ def _load():
                                   ctypes.POINTER(oscar_calib_out_t), P, SZ, P]),
         "oscar_status_string": (ctypes.c_char_p, [I32]),
         "oscar_device_errors": (I32, [ctypes.POINTER(ctypes.c_uint32), I32]),
+        "oscar_test_stall_page_waits": (I32, [I64]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -275,6 +276,12 @@ def oscar_calibrate(dims, num_samples, k, v, centered, clip_quantile, out_k, out
     _check(lib.oscar_calibrate(ctypes.byref(_dims(dims)), int(num_samples), _ptr(k), _ptr(v), int(centered),
                                float(clip_quantile), _calib_out(out_k), _calib_out(out_v), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream)), "oscar_calibrate")
+
+
+def oscar_test_stall_page_waits(cycles: int) -> None:
+    """Test hook: INT2 split warps of later decodes give up their first page wait
+    after ``cycles`` clock cycles (0 = normal operation)."""
+    _check(lib.oscar_test_stall_page_waits(int(cycles)), "oscar_test_stall_page_waits")
 
 
 def oscar_device_errors(reset: bool = False) -> int:

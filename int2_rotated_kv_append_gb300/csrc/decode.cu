@@ -11,6 +11,7 @@
 //   merge  one CTA per (sequence, query head): log-sum-exp merge of the splits,
 //          one un-rotation of the INT2 part by R_v^T, normalisation.
 // Logits are kept in log2 units (scale * log2 e folded into the query side).
+#include <atomic>
 #include <mutex>
 
 #include "decode_common.cuh"
@@ -120,6 +121,10 @@ int split_ctas_per_sm(const oscar_dims_t* d, Mode mode) {
   return 4;
 }
 
+// Cycles after which an INT2 split warp's first page wait gives up, for the timeout
+// test (0: no stall).
+std::atomic<long long> g_stall_cycles{0};
+
 Params base_params(const oscar_dims_t* d, int B, int max_seq_len, const Plan& plan, Mode mode, float sm_scale,
                    void* ws) {
   Params p{};
@@ -158,6 +163,7 @@ Params base_params(const oscar_dims_t* d, int B, int max_seq_len, const Plan& pl
   p.qfrag = reinterpret_cast<uint32_t*>(w + plan.off_qfrag);
   p.part_o = reinterpret_cast<float*>(w + plan.off_po);
   p.part_ml = reinterpret_cast<float*>(w + plan.off_pml);
+  p.stall_cycles = g_stall_cycles.load(std::memory_order_relaxed);
   return p;
 }
 
@@ -541,4 +547,10 @@ extern "C" oscar_status_t oscar_decode_noalloc(const oscar_dims_t* dims, int32_t
 
 oscar_status_t oscar_internal_decode_errors(uint32_t* flags, int reset) {
   return read_unit_errors(flags, reset) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+extern "C" oscar_status_t oscar_test_stall_page_waits(int64_t cycles) {
+  if (cycles < 0) return OSCAR_ERR_INVALID_ARG;
+  g_stall_cycles.store(cycles, std::memory_order_relaxed);
+  return OSCAR_OK;
 }

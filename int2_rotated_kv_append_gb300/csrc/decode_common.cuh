@@ -52,6 +52,10 @@ struct Params {
   // Fused single-wave decode (decode_fused.cu): n_paged INT2 split CTAs per unit starting
   // at page bulk_lo, then n_dense (0 or 1) BF16 CTAs covering n_dense_pages 16-row pages.
   int fused, bulk_lo, n_dense_pages;
+  // > 0 only under oscar_test_stall_page_waits: each INT2 split warp waits for its
+  // first page on a barrier phase that never completes and gives up after this many
+  // cycles, taking the kernels' timeout path.
+  long long stall_cycles;
   const __nv_bfloat16* q;
   const float* R_k;
   const float* R_v;

@@ -232,7 +232,10 @@ __global__ void __launch_bounds__(NT == 1 ? 640 : NW * 32, 1) int2_fused_kernel(
       for (int c = 0; c < 4; ++c) O[nt][mi][c] = 0.f;
   }
   const uint32_t vsel = (2 * (g & 1)) | ((2 * (g & 1) + 1) << 4) | ((4 + 2 * (g & 1)) << 8) | ((5 + 2 * (g & 1)) << 12);
+  // Under the stall test the first page is awaited on the operand barrier's second
+  // phase, which nothing completes (its first phase has completed: frag_ok).
   auto wait_page = [&](int k) {
+    if (p.stall_cycles > 0 && k == 0) return mbar_wait_bounded(fbar, 1, p.stall_cycles);
     return mbar_wait_bounded(smem_u32(&my_bars[k % kStages]), (k / kStages) & 1);
   };
   auto page_full = [&](int k) {
@@ -295,7 +298,9 @@ __global__ void __launch_bounds__(NT == 1 ? 640 : NW * 32, 1) int2_fused_kernel(
   }
   if (aborted) {
     if (lane == 0) record_error(OSCAR_DEVERR_TIMEOUT);
-    // let the copies already requested land (bounded) before the shared memory is reused
+    // let the copies already requested land (bounded) before the shared memory is reused:
+    // the operand block if its wait gave up, and the pages
+    if (!frag_ok && lane == 0) mbar_wait_bounded(fbar, 0);
     const int issued = min(n_my, i + kStages);
     for (int k = i; k < issued; ++k) mbar_wait_bounded(smem_u32(&my_bars[k % kStages]), (k / kStages) & 1);
 #pragma unroll

@@ -167,7 +167,8 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
     bulk_g2s(smem_u32(qbuf), p.qfrag + (static_cast<size_t>(b) * p.H + h) * (32 * kQfragWords), kQfragBytes,
              smem_u32(qbar));
   }
-  aborted = __any_sync(0xffffffffu, !mbar_wait_bounded(smem_u32(qbar), 0));
+  const bool q_ok = __any_sync(0xffffffffu, !mbar_wait_bounded(smem_u32(qbar), 0)) == 0;
+  aborted = !q_ok;
   issue(min(n_my, kFirstIssue), min(n_my, kStages));
   const uint4* qw4 = reinterpret_cast<const uint4*>(qbuf + lane * kQfragWords);
   {
@@ -217,8 +218,11 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   }
   const uint32_t vsel = (2 * (g & 1)) | ((2 * (g & 1) + 1) << 4) | ((4 + 2 * (g & 1)) << 8) | ((5 + 2 * (g & 1)) << 12);
   int i = 0;
-  // Stage of local page k: k % kStages (kStages even: a pair never wraps).
+  // Stage of local page k: k % kStages (kStages even: a pair never wraps).  Under the
+  // stall test the first page is awaited on the operand barrier's second phase, which
+  // nothing completes (its first phase has completed: q_ok).
   auto wait_page = [&](int k) {
+    if (p.stall_cycles > 0 && k == 0) return mbar_wait_bounded(smem_u32(qbar), 1, p.stall_cycles);
     return mbar_wait_bounded(smem_u32(&my_bars[k % kStages]), (k / kStages) & 1);
   };
   auto page_full = [&](int k) {
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
     const int pos = (pg0 + jpage) * kPageSize + tok;
     return pid >= 0 && pid < p.num_pages && pos >= r0 && pos < r1;
   };
-  for (; i + 1 < n_my; i += 2) {
+  for (; !aborted && i + 1 < n_my; i += 2) {
     if (__any_sync(0xffffffffu, !wait_page(i) || !wait_page(i + 1))) {
       aborted = true;
       break;
@@ -277,8 +281,10 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   }
   if (aborted) {
     if (lane == 0) record_error(OSCAR_DEVERR_TIMEOUT);
-    // Let the copies already issued land (bounded) before the shared memory is reused.
-    const int issued = min(n_my, i + kStages);  // pages requested so far
+    // Let the copies already issued land (bounded) before the shared memory is reused:
+    // the operand block if its wait gave up, and the pages requested so far.
+    if (!q_ok && lane == 0) mbar_wait_bounded(smem_u32(qbar), 0);
+    const int issued = min(n_my, i + kStages);
     for (int k = i; k < issued; ++k) mbar_wait_bounded(smem_u32(&my_bars[k % kStages]), (k / kStages) & 1);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
