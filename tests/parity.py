@@ -68,8 +68,8 @@ def check_append(w: Workload, codes_gpu: np.ndarray, sz_gpu: np.ndarray, k: torc
     ks, vs = bits16(k[torch.as_tensor(idx, device=k.device)]), bits16(v[torch.as_tensor(idx, device=v.device)])
     Rk, Rv = w.R_k.cpu().numpy(), w.R_v.cpu().numpy()
     ck, cv = w.clip_k.cpu().numpy(), w.clip_v.cpu().numpy()
-    off = None if w.offset_k is None else w.offset_k.cpu().numpy()
-    pre = O.append_prequant(w.dims, ks, vs, Rk, Rv, ck, cv, offset_k=off)   # [n][H][2][D]
+    offset_k = None if w.offset_k is None else w.offset_k.cpu().numpy()
+    pre = O.append_prequant(w.dims, ks, vs, Rk, Rv, ck, cv, offset_k=offset_k)   # [n][H][2][D]
     page, off = slots[idx] // P, slots[idx] % P
     g_codes = unpack_codes(rows[page, :, :, off], D)                  # [n][H][2][D]
     g_sz = szr[page, :, :, off]                                       # [n][H][2][D/G][2]
@@ -89,7 +89,7 @@ def check_append(w: Workload, codes_gpu: np.ndarray, sz_gpu: np.ndarray, k: torc
     # Scale/zero against the oracle's own append of the same tokens.
     o_codes = np.full(codes_gpu.shape, fill, np.uint8)
     o_sz = np.full(sz_gpu.shape, fill * 0x101, np.uint16)
-    rc = O.append(w.dims, ks, vs, Rk, Rv, ck, cv, slots[idx], o_codes, o_sz, offset_k=off)
+    rc = O.append(w.dims, ks, vs, Rk, Rv, ck, cv, slots[idx], o_codes, o_sz, offset_k=offset_k)
     assert rc == 0
     o_szr = o_sz.reshape(NP, H, 2, P, D // G, 2)[page, :, :, off].view(np.float16).astype(np.float64)
     gs = g_sz.view(np.float16).astype(np.float64)
