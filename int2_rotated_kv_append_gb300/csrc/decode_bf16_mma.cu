@@ -6,9 +6,11 @@
 // Shape covered: head_dim 128, GQA 1..8.  One CTA of 4 warps owns one split of
 // one (sequence, KV head); each warp takes every 4th page of the split.
 // Per warp and page (16 tokens, K and V rows of 256 bytes):
-//   * the 32 rows arrive by 32 bulk async copies (one per lane) into a padded
-//     shared-memory stage (272-byte rows, so ldmatrix is bank-conflict free),
-//     a ring of kStages pages per warp guarded by mbarriers with bounded waits;
+//   * the 8 KB of the page arrive by 16-byte asynchronous copies, 16 per lane (each
+//     instruction moves two whole rows, coalesced), into a padded shared-memory
+//     stage (272-byte rows, so ldmatrix is bank-conflict free); every lane's copies
+//     complete an arrival on the stage's mbarrier, a ring of kStages pages per warp
+//     with bounded waits;
 //   * QK:  S^T[token][query] = K[token][ch] . Q[ch][query], A from ldmatrix,
 //     B = q * scale * log2(e) split into bf16 hi + lo (16 significant bits);
 //   * online softmax per query with warp shuffles;
@@ -61,25 +63,36 @@ __global__ void __launch_bounds__(kWarps * 32) bf16_mma_split_kernel(Params p) {
     pid_s[i] = pid;
   }
   if (lane == 0)
-    for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp * kStages + i]), 1);
+    for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp * kStages + i]), 32);  // one arrival per lane
   mbar_init_fence();
   __syncthreads();
 
   const int n_my = npg > warp ? (npg - warp + kWarps - 1) / kWarps : 0;
   uint8_t* my_stages = smem + warp * kStages * kStageBytes;
   uint64_t* my_bars = bars + warp * kStages;
-  auto issue = [&](int i) {  // whole warp: lane r copies row r of the (page, head): K rows 0..15, V rows 16..31
+  // Whole warp: copy k moves rows 2k, 2k + 1 of the (page, head) block (K rows 0..15,
+  // V rows 16..31): lane l takes 16-byte chunk l % 16 of row 2k + l / 16.  A page with
+  // an invalid id is zeroed instead (its tokens are masked; zero V rows keep p * v finite).
+  const int c16 = lane & 15, rsel = lane >> 4;
+  auto issue = [&](int i) {
     const int pid = pid_s[warp + i * kWarps];
-    const uint32_t bar = smem_u32(&my_bars[i % kStages]);
-    if (pid < 0) {
-      if (lane == 0) mbar_arrive(bar);
-      return;
+    const uint32_t st = smem_u32(my_stages + (i % kStages) * kStageBytes);
+    if (pid >= 0) {
+      const __nv_bfloat16* src = p.pages + (static_cast<size_t>(pid) * p.H + h) * 2 * kPageSize * kD + c16 * 8;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int r = 2 * k + rsel;
+        cp_async16(st + bf16pg::stage_row(r) * kRowPitch + c16 * 16, src + r * kD);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int r = 2 * k + rsel;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(st + bf16pg::stage_row(r) * kRowPitch + c16 * 16),
+                     "r"(0u) : "memory");
+      }
     }
-    if (lane == 0) mbar_arrive_expect_tx(bar, 32 * kRowBytes);
-    __syncwarp();
-    uint8_t* st = my_stages + (i % kStages) * kStageBytes;
-    const size_t row0 = (static_cast<size_t>(pid) * p.H + h) * 2 * kPageSize;  // K row 0 of (page, head)
-    bulk_g2s(smem_u32(st + bf16pg::stage_row(lane) * kRowPitch), p.pages + (row0 + lane) * kD, kRowBytes, bar);
+    cp_async_arrive(smem_u32(&my_bars[i % kStages]));
   };
   for (int i = 0; i < n_my && i < kStages; ++i) issue(i);
 

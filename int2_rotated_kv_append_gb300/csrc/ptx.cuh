@@ -86,6 +86,18 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared memory by the executing thread (both
+// addresses 16-byte aligned), read through L2 only.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on mbarrier `bar` once every cp.async this thread has issued so far has
+// landed (the arrival is not pre-counted: the barrier's count includes it).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Best-effort prefetch of the 128-byte line holding `addr` into L2 through the
 // load/store path (a hint, as above).
 __device__ __forceinline__ void prefetch_l2_line(const void* addr) {
