@@ -115,6 +115,11 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   uint8_t* my_stages = stages + warp * kStages * kStageBytes;
   uint64_t* my_bars = bars + warp * kStages;
   const uint32_t stage_base = smem_u32(my_stages);
+  // Pages are read once: for GQA 8 they are marked evict-first in L2, so that the
+  // stream of pages does not push out what is read again soon (the split partials
+  // the merge reads, R_k and R_v, page tables).  Measured: 3% faster at 131K tokens
+  // with 64-page splits (GQA 8), 1% slower at batch 64 (GQA 4), where it is off.
+  const uint64_t stream_policy = l2_evict_first_policy();
   // Whole warp: bring local pages [i0, i1) of this warp (at most 16) into their
   // stages.  Lane 2j handles page i0 + j's codes, lane 2j + 1 its scale/zero, so the
   // whole batch is requested by one bulk-copy instruction: the issue of a bulk
@@ -138,7 +143,9 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
     if (active && !bad) {
       const size_t ph = static_cast<size_t>(pid) * p.H + h;
       const uint8_t* src = part ? reinterpret_cast<const uint8_t*>(p.sz) + ph * kSzBytes : p.codes + ph * kCodeBytes;
-      bulk_g2s(stage_base + (i % kStages) * kStageBytes + (part ? kCodeBytes : 0), src, part ? kSzBytes : kCodeBytes, bar);
+      const uint32_t dst = stage_base + (i % kStages) * kStageBytes + (part ? kCodeBytes : 0);
+      if (NT == 2) bulk_g2s_hint(dst, src, part ? kSzBytes : kCodeBytes, bar, stream_policy);
+      else bulk_g2s(dst, src, part ? kSzBytes : kCodeBytes, bar);
     }
   };
   grid_dep_launch_dependents();
