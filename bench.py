@@ -177,11 +177,12 @@ def workload_config(args, w, batch, seq_len, pps, l2_policy):
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one oscar_decode
-# launch (q-rotation + split + merge kernels) on the batch-1 32K and batch-64
-# workloads, from one ncu capture of the three kernels each (cold caches: the
+# launch (q-rotation + split + merge kernels) on the batch-1 32K, batch-64 and
+# batch-4 131K workloads, from one ncu capture of the three kernels each (cold caches: the
 # split partials are re-read from DRAM there, from L2 in the timed loop).
 MEASURED_DECODE_TRAFFIC = {1: 557056 + 22292224 + 324608,
-                           2: 1073152 + 427723520 + 3890176 + 8043264}
+                           2: 1073152 + 427723520 + 3890176 + 8043264,
+                           3: 614656 + 340504064 + 5701632 + 18010880}
 
 
 def cpu_model() -> str:
