@@ -61,7 +61,7 @@ struct Geo {
 // ---- the kernel --------------------------------------------------------------
 
 template <int NT, int NG>
-__global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_kernel(Params p) {
+__global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 3) int2_mma_split_kernel(Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   // Dispatch order: KV head fastest, then sequence, split index slowest, so the
   // last CTAs to start are the high splits that only long sequences have.
@@ -178,20 +178,28 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
   aborted = !q_ok;
   issue(min(n_my, kFirstIssue), min(n_my, kStages));
   const uint4* qw4 = reinterpret_cast<const uint4*>(qbuf + lane * kQfragWords);
+  // GQA 8 (two n-tiles): the page body reads the QK B-fragments from the operand
+  // block in shared memory, which keeps the kernel at 168 registers, 3 CTAs per SM
+  // instead of 2 (131K decode 194.5 -> 190.9 us; with one page per iteration
+  // instead of two it was 200.5 us)
+  constexpr bool kBqs = NT == 2;
+  const uint32_t bqs = smem_u32(qbuf + lane * kQfragWords);
   {
     uint4 v[4 * NT], f[3];
+    if (!kBqs) {
 #pragma unroll
-    for (int k = 0; k < 4 * NT; ++k) v[k] = qw4[k];
+      for (int k = 0; k < 4 * NT; ++k) v[k] = qw4[k];
+    }
 #pragma unroll
     for (int k = 0; k < 3; ++k) f[k] = qw4[8 + k];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        bq[nt][2 * k][0] = v[4 * nt + k].x;
-        bq[nt][2 * k][1] = v[4 * nt + k].y;
-        bq[nt][2 * k + 1][0] = v[4 * nt + k].z;
-        bq[nt][2 * k + 1][1] = v[4 * nt + k].w;
+        bq[nt][2 * k][0] = kBqs ? 0u : v[4 * nt + k].x;
+        bq[nt][2 * k][1] = kBqs ? 0u : v[4 * nt + k].y;
+        bq[nt][2 * k + 1][0] = kBqs ? 0u : v[4 * nt + k].z;
+        bq[nt][2 * k + 1][1] = kBqs ? 0u : v[4 * nt + k].w;
       }
     const uint32_t fw[12] = {f[0].x, f[0].y, f[0].z, f[0].w, f[1].x, f[1].y,
                              f[1].z, f[1].w, f[2].x, f[2].y, f[2].z, f[2].w};
@@ -254,7 +262,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
       bool t2[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) t2[nt][0] = t2[nt][1] = true;
-      int2_pages<NT, NG, 2, true>(st2, g, t, t2, t2, vsel, bq, F, qs, m_run, l2, z2, O);
+      int2_pages<NT, NG, 2, true, kBqs>(st2, g, t, t2, t2, vsel, bq, F, qs, m_run, l2, z2, O, bqs);
     } else {
       const bool b00 = token_ok(i, g), b01 = token_ok(i + 1, g), b10 = token_ok(i, g + 8), b11 = token_ok(i + 1, g + 8);
       bool a0[NT][2], a1[NT][2];
@@ -265,7 +273,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
         a1[nt][0] = b10;
         a1[nt][1] = b11;
       }
-      int2_pages<NT, NG, 2, false>(st2, g, t, a0, a1, vsel, bq, F, qs, m_run, l2, z2, O);
+      int2_pages<NT, NG, 2, false, kBqs>(st2, g, t, a0, a1, vsel, bq, F, qs, m_run, l2, z2, O, bqs);
     }
     __syncwarp();
     issue(min(n_my, i + kStages), min(n_my, i + 2 + kStages));
@@ -282,7 +290,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 1) int2_mma_split_k
         a0[nt][0] = b0;
         a1[nt][0] = b1;
       }
-      int2_pages<NT, NG, 1, false>(st1, g, t, a0, a1, vsel, bq, F, qs, m_run, l2, z2, O);
+      int2_pages<NT, NG, 1, false, kBqs>(st1, g, t, a0, a1, vsel, bq, F, qs, m_run, l2, z2, O, bqs);
       ++i;
     }
   }

@@ -75,11 +75,15 @@ __device__ __forceinline__ float2 lds_h2f(uint32_t addr) {
 // (token, hi|lo) values the lane holds for query t: one movmatrix per 8 tokens.
 // The running sums l_run and the zero terms zacc are kept per token slot of the
 // pair and added by the caller at the end.
-template <int NT, int NG, int NP, bool FULL>
+// BQS: the QK B-fragments are read from shared memory at bqs (this lane's operand
+// words: n-tile nt, k-step ks at word nt * 16 + ks * 2) instead of the registers bq,
+// which frees 16 registers per n-tile.
+template <int NT, int NG, int NP, bool FULL, bool BQS = false>
 __device__ __forceinline__ void int2_pages(const uint32_t (&st)[NP], int g, int t, const bool (&v0)[NT][NP],
                                            const bool (&v1)[NT][NP], uint32_t vsel, const uint32_t (&bq)[NT][8][2],
                                            const float (&F)[NT], const float (&qs)[NT][NG], float (&m_run)[NT],
-                                           float2 (&l_run)[NT], float2 (&zacc)[NT][NG], float (&O)[NT][8][4]) {
+                                           float2 (&l_run)[NT], float2 (&zacc)[NT][NG], float (&O)[NT][8][4],
+                                           uint32_t bqs = 0) {
   // K words t and t + 4 of tokens g and g + 8; V words g/2 and 4 + g/2 of tokens
   // 2t, 2t + 1 (xa) and 2t + 8, 2t + 9 (xb); (scale, zero) pairs of K and V for
   // tokens (g, g + 8) per group
@@ -130,8 +134,14 @@ __device__ __forceinline__ void int2_pages(const uint32_t (&st)[NP], int g, int 
     const uint32_t wb = (KS) < 4 ? kw2 : kw3, wbs = (KS) < 4 ? kw2s : kw3s;                       \
     const uint32_t a0 = extract_pair<j>(wa, was), a1 = extract_pair<j>(wb, wbs);                  \
     const uint32_t a2 = extract_pair<j + 1>(wa, was), a3 = extract_pair<j + 1>(wb, wbs);          \
-    _Pragma("unroll") for (int nt = 0; nt < NT; ++nt)                                             \
-        mma16816(acc[pg][nt][gg], a0, a1, a2, a3, bq[nt][KS][0], bq[nt][KS][1]);                  \
+    _Pragma("unroll") for (int nt = 0; nt < NT; ++nt) {                                           \
+      uint32_t b0 = bq[nt][KS][0], b1 = bq[nt][KS][1];                                            \
+      if (BQS) {                                                                                  \
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"                                           \
+                     : "=r"(b0), "=r"(b1) : "r"(bqs + (nt * 16 + (KS) * 2) * 4));                 \
+      }                                                                                           \
+      mma16816(acc[pg][nt][gg], a0, a1, a2, a3, b0, b1);                                          \
+    }                                                                                             \
   }
     OSCAR_QK_STEP(0) OSCAR_QK_STEP(1) OSCAR_QK_STEP(2) OSCAR_QK_STEP(3)
     OSCAR_QK_STEP(4) OSCAR_QK_STEP(5) OSCAR_QK_STEP(6) OSCAR_QK_STEP(7)
