@@ -261,8 +261,8 @@ oscar_status_t oscar_extend(const oscar_dims_t* dims, int32_t batch, int32_t num
  * last n_b = q_start[b+1] - q_start[b] positions of that sequence (the tokens just
  * appended), in order.  Same result as oscar_extend with those rows.  For head_dim
  * 128, group 64 or 128 and GQA 4 or 8, the INT2 part runs in tiles of 64 / GQA rows
- * of one sequence: every page is fetched and its codes turned into tensor-core
- * operands once per tile instead of once per row.
+ * of one sequence on tcgen05: every page is fetched and its codes turned into
+ * tensor-core operands once per tile instead of once per row.
  * Arguments (beyond oscar_extend's)
  *   num_rows          q_start[batch]; q and out have num_rows rows
  *   max_rows_per_seq  host bound on every n_b (sizes the grid)

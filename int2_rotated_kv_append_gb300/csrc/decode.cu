@@ -317,10 +317,13 @@ cudaError_t launch_extend_tiles(Params p, int batch, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   const int chunks = (p.B + p.qrot_spc - 1) / p.qrot_spc;
-  e = launch_pdl(qrot_kernel<D>, dim3(chunks * p.H, D / 32), dim3(kQrotThreads), 0, stream, p);
+  // the tcgen05 tile kernel reads the fp32 rotated queries only: no mma.sync operand blocks
+  Params pq = p;
+  pq.qfrag = nullptr;
+  e = launch_pdl(qrot_kernel<D>, dim3(chunks * p.H, D / 32), dim3(kQrotThreads), 0, stream, pq);
   if (e != cudaSuccess) return e;
   if (p.n_paged > 0) {
-    e = int2_tile_split(p, stream);
+    e = int2_umma_tile_split(p, stream);
     if (e != cudaSuccess) return e;
   }
   return ::merge<D, kMixed>(p, stream);
@@ -386,7 +389,8 @@ extern "C" oscar_status_t oscar_extend_varlen(const oscar_dims_t* dims, int32_t 
   p.row_seq = reinterpret_cast<const int32_t*>(w + plan.total);
   p.row_pos = reinterpret_cast<const int32_t*>(w + plan.total + align_up(static_cast<size_t>(num_rows) * 4, 256));
   if (!int2_mma_supported(p)) p.qfrag = nullptr;
-  const bool tiles = p.qfrag != nullptr && int2_tile_supported(p);
+  // tiles: the sink/window splits run the tensor-core split kernel, the INT2 bulk the tcgen05 tile kernel
+  const bool tiles = p.qfrag != nullptr && int2_umma_tile_supported(p);
   if (tiles) {
     const int rpt = 64 / p.gqa;
     const long long t = (static_cast<long long>(max_rows_per_seq) + rpt - 1) / rpt;

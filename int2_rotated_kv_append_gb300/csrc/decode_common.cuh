@@ -72,7 +72,7 @@ struct Params {
   const int32_t* row_pos;
   int num_seqs;
   int split_base;             // first split index of the launch (the grid's x covers splits split_base ..)
-  // Extend in tiles (int2_tile_split): the rows of sequence b are q_start[b] .. q_start[b + 1) - 1,
+  // Extend in tiles (int2_umma_tile_split): the rows of sequence b are q_start[b] .. q_start[b + 1) - 1,
   // in tiles of 64 / gqa rows, `tiles` per sequence.
   const int32_t* q_start;
   int tiles;
@@ -89,9 +89,9 @@ bool int2_mma_supported(const Params& p);
 int int2_mma_ctas_per_sm(int gqa, int G);  // resident CTAs per SM of the INT2 kernel
 int bf16_mma_ctas_per_sm(int gqa);         // resident CTAs per SM of the BF16 kernel
 cudaError_t int2_mma_split(const Params& p, cudaStream_t stream);
-// Extend in tiles of query rows (decode_int2_mma.cu): the INT2 splits only.
-bool int2_tile_supported(const Params& p);
-cudaError_t int2_tile_split(const Params& p, cudaStream_t stream);
+// Extend in tiles of query rows on tcgen05 (decode_int2_umma.cu): the INT2 splits only.
+bool int2_umma_tile_supported(const Params& p);
+cudaError_t int2_umma_tile_split(const Params& p, cudaStream_t stream);
 bool bf16_mma_supported(const Params& p);
 cudaError_t bf16_mma_split(const Params& p, cudaStream_t stream);
 // Fused single-wave decode (decode_fused.cu).

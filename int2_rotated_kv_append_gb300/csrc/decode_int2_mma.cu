@@ -358,292 +358,6 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 3) int2_mma_split_k
   merge_warps_store<kWarps, kD, kWarps * 32>(p, mw, lw, ow, s, bh0, tid);
 }
 
-// ---- extend: the query rows of a sequence in tiles, every page staged once per CTA ----
-//
-// One CTA per (INT2 split, KV head, sequence x tile of rows).  A tile holds 64 query
-// columns: 16 rows of GQA 4 or 8 rows of GQA 8.  Each of the 8 warps owns 8 columns
-// (n-tile nt: row 2w + nt of GQA 4, or heads 4nt .. 4nt + 3 of row w of GQA 8) and
-// runs every page of the split through the decode's page body with per-column causal
-// masks, so a page is fetched and its codes are turned into tensor-core operands once
-// for 8 query columns per warp instead of once per row.  The pages sit in a CTA-wide
-// ring: warp 0 requests page i + kTileStages once all warps have released page i.
-constexpr int kTileWarps = 8;
-constexpr int kTileStages = 6;
-constexpr int kTileCols = 8 * kTileWarps;  // query columns per tile
-
-template <int NG>
-struct TileGeo {
-  static constexpr int kStageBytes = Geo<NG>::kStageBytes;
-  // page stages | full and empty mbarriers | page ids
-  static constexpr size_t kSmem = static_cast<size_t>(kTileStages) * kStageBytes + 2 * kTileStages * 8 + kMaxPps * 4;
-};
-
-template <int NG>
-__global__ void __launch_bounds__(kTileWarps * 32, 1) int2_tile_split_kernel(Params p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int NT = 2;
-  constexpr int kStageBytes = TileGeo<NG>::kStageBytes;
-  constexpr int kSzBytes = Geo<NG>::kSzBytes;
-  const int s = blockIdx.x, h = blockIdx.y;
-  const int b = blockIdx.z / p.tiles, tile = blockIdx.z % p.tiles;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-  const int gqa = p.gqa;  // 4 or 8
-  const int rpt = kTileCols / gqa;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTileStages * kStageBytes);
-  uint64_t* empty = full + kTileStages;
-  int* pid_all = reinterpret_cast<int*>(empty + kTileStages);
-  grid_dep_launch_dependents();
-  // the q operands come from the q-rotation; pages from appends before it
-  grid_dep_wait();
-  const int q0 = __ldg(p.q_start + b), q1 = __ldg(p.q_start + b + 1);
-  const int r_begin = q0 + tile * rpt;
-  if (r_begin >= q1) return;  // no rows in this tile
-  const int n_rows = min(rpt, q1 - r_begin);
-  const int L = clamp_len(p, b);
-  const int win_begin = max(p.S, L - p.W);
-  const int lo_pos = s * p.pps * kPageSize;
-  const int r0 = max(lo_pos, p.S);
-  // this warp's columns: row and first query head of each n-tile, attended bound
-  int row[NT], hq0[NT], r1[NT];
-  bool valid[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int rl = gqa == 4 ? 2 * warp + nt : warp;
-    valid[nt] = rl < n_rows;
-    row[nt] = r_begin + (valid[nt] ? rl : 0);
-    hq0[nt] = h * gqa + (gqa == 4 ? 0 : 4 * nt);
-    int A = 0;
-    if (valid[nt]) {
-      const int pos = __ldg(p.row_pos + row[nt]);
-      A = (pos >= 0 && pos < L) ? pos + 1 : 0;
-    }
-    r1[nt] = min(lo_pos + p.pps * kPageSize, min(win_begin, A));
-  }
-  // the tile's range: its last row has the largest position
-  int A_last = 0;
-  {
-    const int pos = __ldg(p.row_pos + r_begin + n_rows - 1);
-    A_last = (pos >= 0 && pos < L) ? pos + 1 : 0;
-  }
-  const int r1_tile = min(lo_pos + p.pps * kPageSize, min(win_begin, A_last));
-  auto write_partial = [&](int nt, float m, float l) {
-    const size_t bh = static_cast<size_t>(row[nt]) * p.Hq + hq0[nt] + t;
-    p.part_ml[(bh * p.ml_ns + s) * 2 + 0] = m;
-    p.part_ml[(bh * p.ml_ns + s) * 2 + 1] = l;
-  };
-  if (r1_tile <= r0) {  // nothing of the bulk: empty partials for every column of the tile
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-      if (valid[nt] && g == 0) write_partial(nt, -INFINITY, 0.f);
-    return;
-  }
-  const int pg0 = r0 / kPageSize;
-  const int npg = (r1_tile - 1) / kPageSize + 1 - pg0;
-  for (int k = tid; k < npg; k += kTileWarps * 32)
-    pid_all[k] = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg0 + k);
-  if (tid == 0) {
-    for (int i = 0; i < kTileStages; ++i) {
-      mbar_init(smem_u32(&full[i]), 1);
-      mbar_init(smem_u32(&empty[i]), kTileWarps);
-    }
-  }
-  mbar_init_fence();
-  __syncthreads();
-  const uint32_t stage_base = smem_u32(smem);
-  // one thread requests page j into stage j % kTileStages
-  auto issue = [&](int j) {
-    const int pid = pid_all[j];
-    const uint32_t bar = smem_u32(&full[j % kTileStages]);
-    if (pid < 0 || pid >= p.num_pages) {
-      record_error(OSCAR_DEVERR_PAGE_ID);
-      mbar_arrive(bar);
-      return;
-    }
-    const size_t ph = static_cast<size_t>(pid) * p.H + h;
-    const uint32_t dst = stage_base + (j % kTileStages) * kStageBytes;
-    mbar_arrive_expect_tx(bar, kStageBytes);
-    bulk_g2s(dst, p.codes + ph * kCodeBytes, kCodeBytes, bar);
-    bulk_g2s(dst + kCodeBytes, reinterpret_cast<const uint8_t*>(p.sz) + ph * kSzBytes, kSzBytes, bar);
-  };
-  if (tid == 0)
-    for (int j = 0; j < min(npg, kTileStages); ++j) issue(j);
-  int issued = min(npg, kTileStages);
-
-  // ---- query side: the B-fragments and factors of this warp's two n-tiles, from the
-  // q-rotation's operand blocks (n-tile 0 of each row for GQA 4, n-tiles 0 and 1 of
-  // the row for GQA 8)
-  uint32_t bq[NT][8][2];
-  float F[NT], qs[NT][NG];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int src_nt = gqa == 4 ? 0 : nt;
-    const uint32_t* qw = p.qfrag + (static_cast<size_t>(row[nt]) * p.H + h) * (32 * kQfragWords) + lane * kQfragWords;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      bq[nt][ks][0] = valid[nt] ? __ldg(qw + src_nt * 16 + ks * 2) : 0u;
-      bq[nt][ks][1] = valid[nt] ? __ldg(qw + src_nt * 16 + ks * 2 + 1) : 0u;
-    }
-    F[nt] = valid[nt] ? __uint_as_float(__ldg(qw + 32 + 5 * src_nt)) : 0.f;
-    float c[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) c[k] = valid[nt] ? __uint_as_float(__ldg(qw + 32 + 5 * src_nt + 1 + k)) : 0.f;
-    if (NG == 2) {
-      qs[nt][0] = c[0] + c[1];
-      qs[nt][NG - 1] = c[2] + c[3];
-    } else {
-      qs[nt][0] = (c[0] + c[1]) + (c[2] + c[3]);
-    }
-  }
-  float m_run[NT], O[NT][8][4];
-  float2 l2[NT], z2[NT][NG];  // per token slot (g, g + 8) of the page body
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m_run[nt] = -INFINITY;
-    l2[nt] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int gg = 0; gg < NG; ++gg) z2[nt][gg] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int mi = 0; mi < 8; ++mi)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) O[nt][mi][c] = 0.f;
-  }
-  const uint32_t vsel = (2 * (g & 1)) | ((2 * (g & 1) + 1) << 4) | ((4 + 2 * (g & 1)) << 8) | ((5 + 2 * (g & 1)) << 12);
-  // the smallest bound over the warp's valid columns: pages below it need no masks
-  int r1_min = r1_tile;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-    if (valid[nt]) r1_min = min(r1_min, r1[nt]);
-  auto pid_ok = [&](int k) {
-    const int pid = pid_all[k];
-    return pid >= 0 && pid < p.num_pages;
-  };
-  auto wait_page = [&](int k) {
-    return mbar_wait_bounded(smem_u32(&full[k % kTileStages]), (k / kTileStages) & 1);
-  };
-  // page k released by this warp; thread 0 refills the ring once every warp has
-  auto release = [&](int k) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty[k % kTileStages]));
-    if (tid == 0 && k + kTileStages < npg) {
-      if (mbar_wait_bounded(smem_u32(&empty[k % kTileStages]), (k / kTileStages) & 1)) {
-        issue(k + kTileStages);
-        ++issued;
-      } else {
-        record_error(OSCAR_DEVERR_TIMEOUT);
-      }
-    }
-  };
-  bool aborted = false;
-  int i = 0;
-  for (; i + 1 < npg; i += 2) {
-    if (__any_sync(0xffffffffu, !wait_page(i) || !wait_page(i + 1))) {
-      aborted = true;
-      break;
-    }
-    const uint32_t st2[2] = {stage_base + (i % kTileStages) * kStageBytes,
-                             stage_base + ((i + 1) % kTileStages) * kStageBytes};
-    const int base = (pg0 + i) * kPageSize;
-    if (pid_ok(i) && pid_ok(i + 1) && base >= r0 && base + 2 * kPageSize <= r1_min) {
-      bool t2[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) t2[nt][0] = t2[nt][1] = true;
-      int2_pages<NT, NG, 2, true>(st2, g, t, t2, t2, vsel, bq, F, qs, m_run, l2, z2, O);
-    } else {
-      bool a0[NT][2], a1[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int pg = 0; pg < 2; ++pg) {
-          const bool ok = pid_ok(i + pg);
-          const int pos0 = base + pg * kPageSize + g, pos1 = pos0 + 8;
-          a0[nt][pg] = ok && valid[nt] && pos0 >= r0 && pos0 < r1[nt];
-          a1[nt][pg] = ok && valid[nt] && pos1 >= r0 && pos1 < r1[nt];
-        }
-      int2_pages<NT, NG, 2, false>(st2, g, t, a0, a1, vsel, bq, F, qs, m_run, l2, z2, O);
-    }
-    release(i);
-    release(i + 1);
-  }
-  if (!aborted && i < npg) {  // odd last page
-    if (__any_sync(0xffffffffu, !wait_page(i))) {
-      aborted = true;
-    } else {
-      const uint32_t st1[1] = {stage_base + (i % kTileStages) * kStageBytes};
-      const int base = (pg0 + i) * kPageSize;
-      bool a0[NT][1], a1[NT][1];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const bool ok = pid_ok(i);
-        a0[nt][0] = ok && valid[nt] && base + g >= r0 && base + g < r1[nt];
-        a1[nt][0] = ok && valid[nt] && base + g + 8 >= r0 && base + g + 8 < r1[nt];
-      }
-      int2_pages<NT, NG, 1, false>(st1, g, t, a0, a1, vsel, bq, F, qs, m_run, l2, z2, O);
-      release(i);
-      ++i;
-    }
-  }
-  if (aborted) {
-    if (lane == 0) record_error(OSCAR_DEVERR_TIMEOUT);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      m_run[nt] = -INFINITY;
-      l2[nt] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int gg = 0; gg < NG; ++gg) z2[nt][gg] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int mi = 0; mi < 8; ++mi)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) O[nt][mi][c] = 0.f;
-    }
-  }
-  // ---- this warp's partials, one per column (no merge across warps: each warp
-  // owns its columns)
-  float l_run[NT], zacc[NT][NG];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    l_run[nt] = l2[nt].x + l2[nt].y;
-#pragma unroll
-    for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] = z2[nt][gg].x + z2[nt][gg].y;
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], off);
-#pragma unroll
-      for (int gg = 0; gg < NG; ++gg) zacc[nt][gg] += __shfl_xor_sync(0xffffffffu, zacc[nt][gg], off);
-    }
-  }
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    if (!valid[nt]) continue;
-    const size_t bh = static_cast<size_t>(row[nt]) * p.Hq + hq0[nt] + t;
-    if (g == 0) write_partial(nt, m_run[nt], l_run[nt]);
-    float* po = p.part_o + (bh * p.ns + s) * kD;
-#pragma unroll
-    for (int mi = 0; mi < 8; ++mi) {
-      const int gg = mi * NG / 8;
-      const int word = (mi < 4 ? 0 : 4) + (g >> 1);
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int e = 2 * (mi & 3) + r;
-        const int ch = 16 * word + 8 * (g & 1) + e;
-        po[ch] = (O[nt][mi][2 * r] + O[nt][mi][2 * r + 1]) * pow2i(24 - kpos(e)) + zacc[nt][gg];
-      }
-    }
-  }
-  // copies requested but not consumed (after a timeout) land before the CTA exits
-  __syncthreads();
-  if (tid == 0)
-    for (int k = i; k < issued; ++k) mbar_wait_bounded(smem_u32(&full[k % kTileStages]), (k / kTileStages) & 1);
-}
-
-template <int NG>
-cudaError_t launch_tile(const Params& p, cudaStream_t stream) {
-  constexpr size_t smem = TileGeo<NG>::kSmem;
-  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(int2_tile_split_kernel<NG>), smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(int2_tile_split_kernel<NG>, dim3(p.n_paged, p.H, p.num_seqs * p.tiles), dim3(kTileWarps * 32),
-                    smem, stream, p);
-}
-
 template <int NT, int NG>
 cudaError_t launch_impl(const Params& p, cudaStream_t stream) {
   constexpr size_t smem = Geo<NG>::kSmem;
@@ -680,14 +394,6 @@ int int2_mma_ctas_per_sm(int gqa, int G) {
 
 bool int2_mma_supported(const Params& p) {
   return p.mma != 0 && p.D == kD && (p.G == 64 || p.G == 128) && p.gqa >= 1 && p.gqa <= 8 && p.pps <= kMaxPps;
-}
-
-bool int2_tile_supported(const Params& p) {
-  return p.D == kD && (p.G == 64 || p.G == 128) && (p.gqa == 4 || p.gqa == 8) && p.pps <= kMaxPps;
-}
-
-cudaError_t int2_tile_split(const Params& p, cudaStream_t stream) {
-  return p.G == 64 ? launch_tile<2>(p, stream) : launch_tile<1>(p, stream);
 }
 
 cudaError_t int2_mma_split(const Params& p, cudaStream_t stream) {
