@@ -56,6 +56,8 @@ constexpr int kUtRing = 2 * kUtPages;         // staged pages: two chunks
 constexpr int kUtCols = 64;                   // query columns per tile
 constexpr int kUtMaxPps = 256;                // page ids of one split staged in shared memory
 constexpr uint32_t kUtBlock = 128 * 128;      // one operand block: 128 rows of 128 bytes (16 KB)
+constexpr float kLazy = 12.f;                 // a running maximum is kept while logits stay below it + kLazy
+constexpr float kLazyScale = 15.f;            // ... and V scales at most this: 2^kLazy * 15 < 65504 (fp16)
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 template <int NG>
@@ -466,9 +468,10 @@ __global__ void __launch_bounds__(kUtThreads, 1) int2_umma_tile_kernel(Params p)
       if (ci + 1 < nchunks) ok2 = k_side(ci + 1);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       // Lazy maxima: the chunk keeps the running maxima unless one of its logits exceeds
-      // them by more than 8 (weights up to 2^8) or a V scale exceeds 255 (P' would leave
-      // the fp16 range); then the maxima are taken exactly and O is rescaled.  The
-      // partials carry the maxima used, so either way they are exact.
+      // them by more than kLazy (weights up to 2^kLazy) or a V scale exceeds kLazyScale
+      // (P' = p * scale would leave the fp16 range); then the maxima are taken exactly
+      // and O is rescaled.  The partials carry the maxima used, so either way they are
+      // exact.
       const __half2* tv2 = reinterpret_cast<const __half2*>(tokV) + ((ci & 1) * kUtTok + tr) * NG;
       bool over = false;
       {
@@ -476,11 +479,11 @@ __global__ void __launch_bounds__(kUtThreads, 1) int2_umma_tile_kernel(Params p)
 #pragma unroll
         for (int j4 = 0; j4 < 4; ++j4) {
           const float4 mr = mr4[j4];
-          over |= (sv[4 * j4] > mr.x + 8.f) | (sv[4 * j4 + 1] > mr.y + 8.f) | (sv[4 * j4 + 2] > mr.z + 8.f) |
-                  (sv[4 * j4 + 3] > mr.w + 8.f);
+          over |= (sv[4 * j4] > mr.x + kLazy) | (sv[4 * j4 + 1] > mr.y + kLazy) |
+                  (sv[4 * j4 + 2] > mr.z + kLazy) | (sv[4 * j4 + 3] > mr.w + kLazy);
         }
 #pragma unroll
-        for (int g = 0; g < NG; ++g) over |= tok_ok && !(__low2float(tv2[g]) <= 255.f);
+        for (int g = 0; g < NG; ++g) over |= tok_ok && !(__low2float(tv2[g]) <= kLazyScale);
       }
       if (!ok1 || !ok2) *abort_flag = 1;
       const bool slow = __syncthreads_or(over) != 0;
