@@ -415,10 +415,11 @@ oscar_status_t oscar_device_errors(uint32_t* flags, int32_t reset);
 
 /*
  * Test hook for the bounded waits (not for production use).  With cycles > 0,
- * every oscar_decode / oscar_decode_noalloc call launched afterwards makes each
- * warp of its INT2 split kernel (single-wave fused form or general form) wait for
- * its first page on an mbarrier phase that nothing completes; the wait gives up
- * after `cycles` SM clock cycles.  The kernels then take their timeout path: OSCAR_DEVERR_TIMEOUT
+ * every oscar_decode / oscar_decode_noalloc / oscar_extend / oscar_extend_varlen
+ * call launched afterwards makes each warp of its INT2 split kernel (single-wave
+ * fused form, general form, or the extend's tcgen05 tile kernel) wait for its
+ * first page on an mbarrier phase that nothing completes; the wait gives up after
+ * `cycles` SM clock cycles.  The kernels then take their timeout path: OSCAR_DEVERR_TIMEOUT
  * is recorded, the copies already issued are awaited, and the split's work is
  * dropped (its partial attends nothing).  cycles == 0 restores normal operation.
  * The setting is process-wide and read at launch time (a captured CUDA graph keeps

@@ -21,6 +21,7 @@ extern "C" oscar_status_t oscar_device_errors(uint32_t* flags, int32_t reset) {
   if (st == OSCAR_OK) st = oscar_internal_decode_mma_errors(flags, reset);
   if (st == OSCAR_OK) st = oscar_internal_decode_fused_errors(flags, reset);
   if (st == OSCAR_OK) st = oscar_internal_decode_bf16_errors(flags, reset);
+  if (st == OSCAR_OK) st = oscar_internal_decode_umma_errors(flags, reset);
   if (st == OSCAR_OK) st = oscar_internal_calib_errors(flags, reset);
   return st;
 }

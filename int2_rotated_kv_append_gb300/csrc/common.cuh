@@ -95,4 +95,5 @@ oscar_status_t oscar_internal_decode_errors(uint32_t* flags, int reset);
 oscar_status_t oscar_internal_decode_mma_errors(uint32_t* flags, int reset);
 oscar_status_t oscar_internal_decode_fused_errors(uint32_t* flags, int reset);
 oscar_status_t oscar_internal_decode_bf16_errors(uint32_t* flags, int reset);
+oscar_status_t oscar_internal_decode_umma_errors(uint32_t* flags, int reset);
 oscar_status_t oscar_internal_calib_errors(uint32_t* flags, int reset);

@@ -730,3 +730,7 @@ cudaError_t int2_umma_tile_split(const Params& p, cudaStream_t stream) {
 }
 
 }  // namespace oscar_dec
+
+oscar_status_t oscar_internal_decode_umma_errors(uint32_t* flags, int reset) {
+  return oscar::read_unit_errors(flags, reset) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}

@@ -185,3 +185,59 @@ def test_extend_varlen_full_workload_sampled():
     rows = sorted(set([0, chunk - 1, B * chunk - 1] + rng.choice(B * chunk, 21, replace=False).tolist()))
     pairs = [(r, int(h)) for r in rows for h in rng.choice(32, 2, replace=False)]
     compare_decode(out, oracle_extend_on_gpu_cache(w, cache, q, rs, rp, pairs=pairs), pairs=pairs)
+
+
+@pytest.mark.parametrize("G,Hq,H", [(64, 8, 2), (128, 16, 2)])
+def test_extend_tiles_exact_maxima_paths(G, Hq, H):
+    # The tcgen05 tile kernel keeps a column's running maximum while logits stay within
+    # 2^12 of it and V scales within 15.  Values x 64 (no clipping) put every chunk on the
+    # exact-maximum path; one key x 16 in the middle of each sequence raises the running
+    # maxima far past the margin, so the output accumulator is rescaled mid-split.
+    # Scaling the values by 64 scales every output, and its fp32 rounding, by 64: both
+    # sides are divided by 64 before the decode bounds are applied.
+    lens, chunks = [1500, 700], [16, 9]
+    w = synth.make_workload(num_q_heads=Hq, num_kv_heads=H, head_dim=128, group_size=G, sink_len=16, window_len=32,
+                            seq_lens=lens, seed=41 + G, clip_frac=None)
+    w.v = (w.v.float() * 64).to(torch.bfloat16)
+    pos, seq = w.tok_pos.numpy(), w.tok_seq.numpy()
+    spike = np.nonzero(((seq == 0) & (pos == 900)) | ((seq == 1) & (pos == 400)))[0]
+    k = w.k.float()
+    k[torch.as_tensor(spike)] *= 16
+    w.k = k.to(torch.bfloat16)
+    cache = Int2Cache(w)
+    cache.prefill()
+    q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    rs = np.repeat(np.arange(len(lens), dtype=np.int32), chunks)
+    rp = np.concatenate([np.arange(L - n, L, dtype=np.int32) for L, n in zip(lens, chunks)])
+    g = torch.Generator().manual_seed(10)
+    q = torch.randn((len(rs), Hq, 128), generator=g).to(torch.bfloat16).cuda()
+    ok.oscar_device_errors(reset=True)
+    out = cache.extend_varlen(q, torch.as_tensor(q_start).cuda(), max(chunks))
+    torch.cuda.synchronize()
+    assert ok.oscar_device_errors(reset=True) == 0
+    compare_decode(out / 64, oracle_extend_on_gpu_cache(w, cache, q, rs, rp) / 64)
+
+
+def test_extend_tiles_page_wait_timeout_is_reported_and_recovers():
+    # the test hook stalls the tile kernel's first page wait: the INT2 part is dropped
+    # (no sink or window here, so the output is zero), flagged, and the next call matches
+    lens, chunk = [900, 400], 16
+    w = synth.make_workload(num_q_heads=8, num_kv_heads=2, head_dim=128, group_size=64, sink_len=0, window_len=0,
+                            seq_lens=lens, seed=43)
+    cache = Int2Cache(w)
+    cache.prefill()
+    q_start = torch.tensor([0, chunk, 2 * chunk], dtype=torch.int32).cuda()
+    q = torch.randn((2 * chunk, 8, 128), generator=torch.Generator().manual_seed(11)).to(torch.bfloat16).cuda()
+    before = cache.extend_varlen(q, q_start, chunk).clone()
+    assert torch.count_nonzero(before) > 0 and ok.oscar_device_errors(reset=True) == 0
+    ok.oscar_test_stall_page_waits(1_000_000)
+    try:
+        stalled = cache.extend_varlen(q, q_start, chunk).clone()
+        torch.cuda.synchronize()
+    finally:
+        ok.oscar_test_stall_page_waits(0)
+    assert ok.oscar_device_errors(reset=True) & ok.OSCAR_DEVERR_TIMEOUT
+    assert torch.count_nonzero(stalled) == 0 and torch.isfinite(stalled).all()
+    after = cache.extend_varlen(q, q_start, chunk).clone()
+    assert ok.oscar_device_errors(reset=True) == 0
+    assert torch.equal(after, before)
