@@ -303,7 +303,7 @@ __global__ void extend_rows_kernel(const int32_t* q_start, const int32_t* seq_le
 }
 
 // Extend in tiles: the rows' (sequence, position), the BF16 sink/window splits per
-// row, the q-rotation, the INT2 splits in tiles of rows, the merge per row.
+// row, the q-rotation, the INT2 splits in tiles of rows, the merge per tile.
 template <int D>
 cudaError_t launch_extend_tiles(Params p, int batch, cudaStream_t stream) {
   extend_rows_kernel<<<batch, 128, 0, stream>>>(p.q_start, p.seq_lens, p.B, p.max_seq_len,
@@ -326,7 +326,7 @@ cudaError_t launch_extend_tiles(Params p, int batch, cudaStream_t stream) {
     e = int2_umma_tile_split(p, stream);
     if (e != cudaSuccess) return e;
   }
-  return ::merge<D, kMixed>(p, stream);
+  return extend_tile_merge_supported(p) ? extend_tile_merge(p, stream) : ::merge<D, kMixed>(p, stream);
 }
 
 }  // namespace oscar_extend_rows

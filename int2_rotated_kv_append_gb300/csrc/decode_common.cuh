@@ -92,6 +92,10 @@ cudaError_t int2_mma_split(const Params& p, cudaStream_t stream);
 // Extend in tiles of query rows on tcgen05 (decode_int2_umma.cu): the INT2 splits only.
 bool int2_umma_tile_supported(const Params& p);
 cudaError_t int2_umma_tile_split(const Params& p, cudaStream_t stream);
+// The merge of those tiles' rows: one CTA per (sequence x tile, KV head), R_v staged once;
+// for up to 64 splits per row.
+bool extend_tile_merge_supported(const Params& p);
+cudaError_t extend_tile_merge(const Params& p, cudaStream_t stream);
 bool bf16_mma_supported(const Params& p);
 cudaError_t bf16_mma_split(const Params& p, cudaStream_t stream);
 // Fused single-wave decode (decode_fused.cu).

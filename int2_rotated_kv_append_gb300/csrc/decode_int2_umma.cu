@@ -718,6 +718,152 @@ cudaError_t launch_umma_tile(const Params& p, cudaStream_t stream) {
                     stream, p);
 }
 
+// ---- the extend tiles' merge: the partials of a tile's 64 columns, un-rotated once ----
+//
+// One CTA of 16 warps per (sequence x tile of rows, KV head):
+//   phase A  warp w, columns 4w .. 4w + 3, lane = split: the largest split maximum M,
+//            the weights 2^(m_s - M) (0 for splits that attended nothing) and the
+//            denominator sum_s 2^(m_s - M) l_s;
+//   phase B  thread (warp w, lane): columns 4w + r, channels lane + 32 k: the weighted
+//            sums of the rotated (INT2 splits) and plain (BF16 sink/window splits)
+//            partial outputs, every split's loads issued together; the rotated sums go
+//            to shared memory;
+//   phase C  the same thread: out[c][i] = (plain[c][i] + sum_j rot[c][j] R_v[i][j]) / den[c]
+//            (the single un-rotation by R_v^T), R_v staged in shared memory in rows of
+//            129 floats so that the 32 lanes' rows fall in 32 different banks.
+constexpr int kEmThreads = 512;
+constexpr int kEmRow = kD + 1;
+constexpr int kEmMaxNs = 64;  // splits per row the tile merge takes (weights staged in shared memory)
+constexpr size_t kEmSmem = (static_cast<size_t>(kD) * kEmRow + 64 * kD + 64 + 64 * kEmMaxNs) * 4;
+
+__global__ void __launch_bounds__(kEmThreads, 2) extend_merge_kernel(Params p) {
+  extern __shared__ __align__(16) float em[];
+  float* Rs = em;                  // [128][129]
+  float* rot = Rs + kD * kEmRow;   // [64][128]: rotated sums
+  float* den_s = rot + 64 * kD;    // [64]
+  float* wts = den_s + 64;         // [64][kEmMaxNs]: split weights 2^(m_s - M)
+  const int h = blockIdx.y;
+  const int b = blockIdx.x / p.tiles, tile = blockIdx.x % p.tiles;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {  // R_v[h] is an input of the call, not an output of the kernels before: read before the wait
+    const float4* R4 = reinterpret_cast<const float4*>(p.R_v + static_cast<size_t>(h) * kD * kD);
+    for (int idx = tid; idx < kD * kD / 4; idx += kEmThreads) {
+      const float4 v = __ldg(R4 + idx);
+      float* dst = Rs + (idx >> 5) * kEmRow + (idx & 31) * 4;
+      dst[0] = v.x, dst[1] = v.y, dst[2] = v.z, dst[3] = v.w;
+    }
+  }
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // the partials come from the split kernels before
+  const int gqa = p.gqa, rpt = kUtCols / gqa;
+  const int q0 = __ldg(p.q_start + b), q1 = __ldg(p.q_start + b + 1);
+  const int r_begin = q0 + tile * rpt;
+  if (r_begin >= q1) return;  // no rows in this tile
+  const int n_rows = min(rpt, q1 - r_begin);
+  auto col_valid = [&](int c) { return c / gqa < n_rows; };
+  auto col_bh = [&](int c) { return static_cast<size_t>(r_begin + c / gqa) * p.Hq + h * gqa + c % gqa; };
+  const int ns = p.ns, np = p.n_paged;  // ns <= kEmMaxNs (checked at launch)
+  // phase A: lane = split (and split + 32), the warp's 4 columns at once
+  {
+    float2 v[4][2];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int c = 4 * warp + r;
+      const float2* ml = reinterpret_cast<const float2*>(p.part_ml + col_bh(col_valid(c) ? c : 0) * p.ml_ns * 2);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int sp = lane + 32 * u;
+        v[r][u] = (col_valid(c) && sp < ns) ? ml[sp] : make_float2(-INFINITY, 0.f);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int c = 4 * warp + r;
+      float M = fmaxf(v[r][0].x, v[r][1].x);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float den = 0.f;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        // splits that attended nothing get weight 0 (and their outputs are not used)
+        const float w = (v[r][u].x == -INFINITY) ? 0.f : fast_exp2(v[r][u].x - M);
+        den = fmaf(w, v[r][u].y, den);
+        const int sp = lane + 32 * u;
+        if (sp < kEmMaxNs) wts[c * kEmMaxNs + sp] = w;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      if (lane == 0) den_s[c] = den;
+    }
+  }
+  __syncwarp();  // phase B reads the weights of the warp's own columns
+  // phase B: every split's partial of the 4 columns requested together
+  float acc[4][4];  // [column r][channel k]: the plain sums, then the outputs
+  {
+    float ar[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ar[r][k] = acc[r][k] = 0.f;
+    // the warp's 4 columns are 4 consecutive query heads of one row (GQA 4 or 8): their
+    // partials are ns * 128 floats apart
+    const float* po = p.part_o + col_bh(col_valid(4 * warp) ? 4 * warp : 0) * ns * kD + lane;
+    for (int sp = 0; sp < ns; ++sp) {
+      float o[4][4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[r][k] = po[(static_cast<size_t>(r) * ns + sp) * kD + 32 * k];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float w = wts[(4 * warp + r) * kEmMaxNs + sp];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float t = w != 0.f ? w * o[r][k] : 0.f;  // a skipped split's output is never used
+          if (sp < np)
+            ar[r][k] += t;
+          else
+            acc[r][k] += t;
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) rot[(4 * warp + r) * kD + lane + 32 * k] = ar[r][k];
+  }
+  __syncthreads();
+  // phase C
+  const float* Rrow = Rs + lane * kEmRow;  // rows lane + 32 k are Rrow + 32 k * kEmRow
+#pragma unroll 2
+  for (int j = 0; j < kD; j += 4) {
+    float4 o[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) o[r] = *reinterpret_cast<const float4*>(rot + (4 * warp + r) * kD + j);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      float rv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) rv[k] = Rrow[32 * k * kEmRow + j + jj];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float ov = jj == 0 ? o[r].x : jj == 1 ? o[r].y : jj == 2 ? o[r].z : o[r].w;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[r][k] = fmaf(ov, rv[k], acc[r][k]);
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int c = 4 * warp + r;
+    if (!col_valid(c)) continue;
+    const float den = den_s[c];
+    float* out = p.out + col_bh(c) * kD + lane;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) out[32 * k] = den > 0.f ? acc[r][k] / den : 0.f;
+  }
+}
+
 }  // namespace
 
 bool int2_umma_tile_supported(const Params& p) {
@@ -727,6 +873,14 @@ bool int2_umma_tile_supported(const Params& p) {
 
 cudaError_t int2_umma_tile_split(const Params& p, cudaStream_t stream) {
   return p.G == 64 ? launch_umma_tile<2>(p, stream) : launch_umma_tile<1>(p, stream);
+}
+
+bool extend_tile_merge_supported(const Params& p) { return p.ns <= kEmMaxNs; }
+
+cudaError_t extend_tile_merge(const Params& p, cudaStream_t stream) {
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(extend_merge_kernel), kEmSmem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(extend_merge_kernel, dim3(p.num_seqs * p.tiles, p.H), dim3(kEmThreads), kEmSmem, stream, p);
 }
 
 }  // namespace oscar_dec
