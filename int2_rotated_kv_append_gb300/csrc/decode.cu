@@ -302,18 +302,16 @@ __global__ void extend_rows_kernel(const int32_t* q_start, const int32_t* seq_le
   }
 }
 
-// Extend in tiles: the rows' (sequence, position), the BF16 sink/window splits per
-// row, the q-rotation, the INT2 splits in tiles of rows, the merge per tile.
+// Extend in tiles: the rows' (sequence, position), the BF16 sink/window splits and the
+// INT2 splits in tiles of rows (the q-rotation between them), the merge per tile.
 template <int D>
 cudaError_t launch_extend_tiles(Params p, int batch, cudaStream_t stream) {
   extend_rows_kernel<<<batch, 128, 0, stream>>>(p.q_start, p.seq_lens, p.B, p.max_seq_len,
                                                 const_cast<int32_t*>(p.row_seq), const_cast<int32_t*>(p.row_pos));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (p.n_dense > 0) {
-    Params pd = p;
-    pd.split_base = p.n_paged;
-    e = int2_mma_split(pd, stream);
+  if (p.n_dense > 0) {  // the sink/window rows once per tile of rows, on tcgen05
+    e = bf16_dense_tile(p, stream);
     if (e != cudaSuccess) return e;
   }
   const int chunks = (p.B + p.qrot_spc - 1) / p.qrot_spc;

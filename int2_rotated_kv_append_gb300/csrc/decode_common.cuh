@@ -95,6 +95,9 @@ cudaError_t int2_umma_tile_split(const Params& p, cudaStream_t stream);
 // The merge of those tiles' rows: one CTA per (sequence x tile, KV head), R_v staged once;
 // for up to 64 splits per row.
 bool extend_tile_merge_supported(const Params& p);
+// The BF16 sink/window splits of those tiles on tcgen05: one CTA per (sequence x tile,
+// KV head, dense split of kDenseMmaPages pages).
+cudaError_t bf16_dense_tile(const Params& p, cudaStream_t stream);
 cudaError_t extend_tile_merge(const Params& p, cudaStream_t stream);
 bool bf16_mma_supported(const Params& p);
 cudaError_t bf16_mma_split(const Params& p, cudaStream_t stream);

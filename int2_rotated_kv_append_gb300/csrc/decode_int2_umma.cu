@@ -183,6 +183,10 @@ __global__ void __launch_bounds__(kUtThreads, 1) int2_umma_tile_kernel(Params p)
   auto col_bh = [&](int c) { return static_cast<size_t>(r_begin + c / gqa) * p.Hq + h * gqa + c % gqa; };
   // the tile's range: its last row has the largest position
   const int r1_tile = attend_end(r_begin + n_rows - 1);
+  if (tid < n_rows) {  // a row outside its sequence attends nothing and is flagged
+    const int pos = __ldg(p.row_pos + r_begin + tid);
+    if (pos < 0 || pos >= L) record_error(OSCAR_DEVERR_POSITION);
+  }
   if (r1_tile <= r0) {  // nothing of the bulk: empty partials for every column of the tile
     if (tid < kUtCols && col_valid(tid)) {
       const size_t bh = col_bh(tid);
@@ -718,6 +722,237 @@ cudaError_t launch_umma_tile(const Params& p, cudaStream_t stream) {
                     stream, p);
 }
 
+// ---- the extend tiles' BF16 sink/window part on tcgen05 ----
+//
+// One CTA of 16 warps per (sequence x tile of rows, KV head, dense split); a dense split
+// is 8 pages of 16 rows of the sink buffer, then of the window ring (the decode's
+// enumeration), 128 tokens: one chunk, so no running maximum is needed.  The K and V
+// rows (bf16) are the A operands as they are (K-major for QK, the same bytes MN-major
+// for PV), the unrotated bf16 queries the QK B operand (exact products, fp32 sums);
+// the weights p <= 1 are split into bf16 high and low parts (16 significant bits) as
+// the PV B operand, written over the K operand once QK has read it.  The partial of
+// each column is unrotated, in the decode's format.
+constexpr int kDtThreads = 512;
+constexpr uint32_t kDtAK = 0, kDtAV = 2 * kUtBlock, kDtBq = 4 * kUtBlock;      // Bq: 2 K blocks of 64 rows
+constexpr uint32_t kDtCol = kDtBq + kUtBlock;                                     // per-token / per-column values
+constexpr size_t kDtSmem = 1024 + kDtCol + (128 + 64 + 4 * 64 + 4 * 64 + 2 * 64) * 4 + 4 * 8 + 16;
+
+__global__ void __launch_bounds__(kDtThreads, 2) bf16_dense_tile_kernel(Params p) {
+  extern __shared__ uint8_t dt_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dt_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  int* tokpos = reinterpret_cast<int*>(sm + kDtCol);  // [128]: position of the token, -1 when not in the cache
+  int* colA = tokpos + 128;                            // [64]: attended positions [0, A) of the column
+  float* red = reinterpret_cast<float*>(colA + 64);    // [4][64]: per-warp column maxima
+  float* red2 = red + 4 * 64;                          // [4][64]: per-warp column sums
+  float* mcol = red2 + 4 * 64;                         // [64]: column maximum (log2 units)
+  float* mused = mcol + 64;                            // [64]: the maximum the weights use
+  uint64_t* bars = reinterpret_cast<uint64_t*>(mused + 64);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 4);  // TMEM address
+  const uint32_t bar_s = smem_u32(&bars[0]), bar_o = smem_u32(&bars[1]);
+  const int h = blockIdx.y, ds = blockIdx.z;
+  const int b = blockIdx.x / p.tiles, tile = blockIdx.x % p.tiles;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gqa = p.gqa, rpt = kUtCols / gqa;
+  const int sidx = p.n_paged + ds;  // this split's partial index
+  grid_dep_launch_dependents();
+  // the rows' positions come from the row kernel, the sink/window rows from appends before
+  grid_dep_wait();
+  const int q0 = __ldg(p.q_start + b), q1 = __ldg(p.q_start + b + 1);
+  const int r_begin = q0 + tile * rpt;
+  if (r_begin >= q1) return;  // no rows in this tile
+  const int n_rows = min(rpt, q1 - r_begin);
+  const int L = clamp_len(p, b);
+  auto col_valid = [&](int c) { return c / gqa < n_rows; };
+  auto col_bh = [&](int c) { return static_cast<size_t>(r_begin + c / gqa) * p.Hq + h * gqa + c % gqa; };
+  const int nsp = (p.S + kPageSize - 1) / kPageSize, nwp = (p.W + kPageSize - 1) / kPageSize;
+  const int first = ds * kDenseMmaPages;
+  if (first >= nsp + nwp) {  // no pages in this split: empty partials
+    if (tid < kUtCols && col_valid(tid)) {
+      const size_t bh = col_bh(tid);
+      p.part_ml[(bh * p.ml_ns + sidx) * 2 + 0] = -INFINITY;
+      p.part_ml[(bh * p.ml_ns + sidx) * 2 + 1] = 0.f;
+    }
+    return;
+  }
+  if (tid == 0) {
+    mbar_init(bar_s, 1);
+    mbar_init(bar_o, 1);
+    mbar_init_fence();
+  }
+  if (warp == 0) umma::tmem_alloc(smem_u32(misc), 128);  // S^T (64 columns), then O (64)
+  if (tid < kUtCols) {
+    int A = 0;
+    if (col_valid(tid)) {
+      const int pos = __ldg(p.row_pos + r_begin + tid / gqa);
+      A = (pos >= 0 && pos < L) ? pos + 1 : 0;  // a row outside its sequence attends nothing
+    }
+    colA[tid] = A;
+  }
+  // token t of the split: K row half (part 0, 1) or V row half (part 2, 3), 128 bytes
+  {
+    const int t = tid & 127, part = tid >> 7, kv = part >> 1, half = part & 1;
+    const int k = first + (t >> 4), r = t & 15;
+    const __nv_bfloat16* src = nullptr;
+    int pos = -1;
+    if (k < nsp) {
+      const int sp = k * kPageSize + r;
+      if (sp < min(p.S, L)) {
+        pos = sp;
+        src = p.sink + (((static_cast<size_t>(b) * 2 + kv) * p.H + h) * p.S + sp) * kD;
+      }
+    } else if (k < nsp + nwp) {
+      const int slot = (k - nsp) * kPageSize + r;
+      if (slot < p.W && L > 0) {
+        int back = (L - 1 - slot) % p.W;
+        if (back < 0) back += p.W;
+        const int wpos = L - 1 - back;  // the position the ring slot holds
+        if (wpos >= p.S) {
+          pos = wpos;
+          src = p.win + (((static_cast<size_t>(b) * 2 + kv) * p.H + h) * p.W + slot) * kD;
+        }
+      }
+    }
+    if (part == 0) tokpos[t] = pos;
+    const uint32_t blk = sb + (kv ? kDtAV : kDtAK) + half * kUtBlock;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (src != nullptr) v = __ldg(reinterpret_cast<const uint4*>(src + 64 * half) + q);
+      st_shared_v4(blk + t * 128 + ((q ^ (t & 7)) << 4), v.x, v.y, v.z, v.w);
+    }
+  }
+  {  // the queries (unrotated bf16): column c, 16 channels e
+    const int c = tid >> 3, e = tid & 7;
+    uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+    if (col_valid(c)) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + col_bh(c) * kD + 16 * e);
+      v0 = __ldg(src);
+      v1 = __ldg(src + 1);
+    }
+    const uint32_t blk = sb + kDtBq + (e >> 2) * (64 * 128);
+    const int q = 2 * (e & 3);
+    st_shared_v4(blk + c * 128 + ((q ^ (c & 7)) << 4), v0.x, v0.y, v0.z, v0.w);
+    st_shared_v4(blk + c * 128 + (((q + 1) ^ (c & 7)) << 4), v1.x, v1.y, v1.z, v1.w);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = *misc;
+  if (tid == 0) {  // QK: S^T[token][column], M = 128, N = 64
+    constexpr uint32_t idesc = umma::idesc_bf16_f32(128, 64);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      umma::mma_bf16(tmem, umma::desc_k_sw128(sb + kDtAK + (ks >> 2) * kUtBlock + (ks & 3) * 32),
+                     umma::desc_k_sw128(sb + kDtBq + (ks >> 2) * (64 * 128) + (ks & 3) * 32), idesc, ks != 0);
+    umma::commit(bar_s);
+  }
+  const int q4 = warp & 3, hq = warp >> 2, tr = 32 * q4 + lane;
+  const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+  const bool ok1 = mbar_wait_bounded(bar_s, 0);
+  umma::fence_after_sync();
+  float sv[16];
+  {
+    uint32_t a[16];
+    umma::tmem_ld16(t_lane + 16 * hq, a);
+    umma::tmem_ld_wait();
+    const int pos = tokpos[tr];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      sv[j] = (pos >= 0 && pos < colA[16 * hq + j]) ? __uint_as_float(a[j]) * p.scale_log2 : -INFINITY;
+  }
+  {
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = sv[j];
+    const float m = warp_cols16<true>(v, lane);
+    if (lane < 16) red[q4 * 64 + 16 * hq + lane] = m;
+  }
+  const bool ok_a = __syncthreads_and(ok1);
+  if (tid < kUtCols) {
+    const float m = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+    mcol[tid] = m;
+    mused[tid] = m == -INFINITY ? 0.f : m;
+  }
+  __syncthreads();
+  {  // weights, their column sums, and p as bf16 high and low parts over the K operand
+    const float4* mu4 = reinterpret_cast<const float4*>(mused + 16 * hq);
+#pragma unroll
+    for (int j4 = 0; j4 < 4; ++j4) {
+      const float4 mu = mu4[j4];
+      sv[4 * j4] = fast_exp2(sv[4 * j4] - mu.x);
+      sv[4 * j4 + 1] = fast_exp2(sv[4 * j4 + 1] - mu.y);
+      sv[4 * j4 + 2] = fast_exp2(sv[4 * j4 + 2] - mu.z);
+      sv[4 * j4 + 3] = fast_exp2(sv[4 * j4 + 3] - mu.w);
+    }
+    const uint32_t row_off = (tr >> 3) * 1024 + (tr & 7) * 128;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x0 = sv[8 * q + 2 * e], x1 = sv[8 * q + 2 * e + 1];
+        const __nv_bfloat162 hh = __floats2bfloat162_rn(x0, x1);
+        const float2 hf = __bfloat1622float2(hh);
+        const __nv_bfloat162 ll = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+        hw[e] = *reinterpret_cast<const uint32_t*>(&hh);
+        lw[e] = *reinterpret_cast<const uint32_t*>(&ll);
+      }
+      const uint32_t off = row_off + (((2 * hq + q) ^ (tr & 7)) << 4);
+      st_shared_v4(sb + kDtAK + off, hw[0], hw[1], hw[2], hw[3]);
+      st_shared_v4(sb + kDtAK + kUtBlock + off, lw[0], lw[1], lw[2], lw[3]);
+    }
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = sv[j];
+    const float l = warp_cols16<false>(v, lane);
+    if (lane < 16) red2[q4 * 64 + 16 * hq + lane] = l;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  umma::fence_before_sync();
+  __syncthreads();
+  if (tid == 0 && ok_a) {  // PV: O^T[channel][column], M = 128, N = 64, high then low parts
+    umma::fence_after_sync();
+    constexpr uint32_t idesc = umma::idesc_bf16_f32_mn(128, 64);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+        umma::mma_bf16(tmem + 64, umma::desc_mn_sw128(sb + kDtAV + ks * 2048, kUtBlock),
+                       umma::desc_mn_sw128(sb + kDtAK + part * kUtBlock + ks * 2048, kUtBlock), idesc,
+                       (ks | part) != 0);
+    umma::commit(bar_o);
+  }
+  const bool ok2 = ok_a && mbar_wait_bounded(bar_o, 0);
+  const bool ok_b = __syncthreads_and(ok2);
+  umma::fence_after_sync();
+  if (ok_b) {
+    uint32_t o[16];
+    umma::tmem_ld16(t_lane + 64 + 16 * hq, o);
+    umma::tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int c = 16 * hq + j;
+      if (col_valid(c) && mcol[c] != -INFINITY)
+        p.part_o[(col_bh(c) * p.ns + sidx) * kD + tr] = __uint_as_float(o[j]);
+    }
+  }
+  if (tid < kUtCols && col_valid(tid)) {
+    const size_t bh = col_bh(tid);
+    const float l = (red2[tid] + red2[64 + tid]) + (red2[128 + tid] + red2[192 + tid]);
+    p.part_ml[(bh * p.ml_ns + sidx) * 2 + 0] = ok_b ? mcol[tid] : -INFINITY;
+    p.part_ml[(bh * p.ml_ns + sidx) * 2 + 1] = ok_b ? l : 0.f;
+  }
+  if (!ok_b && tid == 0) record_error(OSCAR_DEVERR_TIMEOUT);
+  umma::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    umma::fence_after_sync();
+    umma::tmem_dealloc(tmem, 128);
+  }
+}
+
 // ---- the extend tiles' merge: the partials of a tile's 64 columns, un-rotated once ----
 //
 // One CTA of 16 warps per (sequence x tile of rows, KV head):
@@ -876,6 +1111,13 @@ cudaError_t int2_umma_tile_split(const Params& p, cudaStream_t stream) {
 }
 
 bool extend_tile_merge_supported(const Params& p) { return p.ns <= kEmMaxNs; }
+
+cudaError_t bf16_dense_tile(const Params& p, cudaStream_t stream) {
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(bf16_dense_tile_kernel), kDtSmem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(bf16_dense_tile_kernel, dim3(p.num_seqs * p.tiles, p.H, p.n_dense), dim3(kDtThreads), kDtSmem,
+                    stream, p);
+}
 
 cudaError_t extend_tile_merge(const Params& p, cudaStream_t stream) {
   cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(extend_merge_kernel), kEmSmem);
