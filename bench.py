@@ -724,8 +724,8 @@ def extend_workload(dev):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "bytes_per_launch": nbytes,
                          "peak_source": f"{peak_kind} hbm_gbs"},
-            "note": "oscar_extend_varlen: the INT2 pages are read once per tile of 16 query rows (GQA 4) of a "
-                    "sequence; the BF16 sink/window once per row"}
+            "note": "oscar_extend_varlen: the INT2 pages and the BF16 sink/window rows are read once per tile of "
+                    "16 query rows (GQA 4) of a sequence, on tcgen05"}
 
 
 def calibrate_workload(dev):
