@@ -709,6 +709,10 @@ __global__ void __launch_bounds__(kThreads) append_small_kernel(
   }
   if (md.active()) __syncthreads();
   const float* off = (kv == 0 && offset_k != nullptr) ? offset_k + static_cast<size_t>(h) * D : nullptr;
+  // Launched as a programmatic dependent: R, the thresholds and the slots above were
+  // read while the kernel before may still run; the token rows are read, and every
+  // output written, only after it has completed.
+  grid_dep_wait();
   stage_rows<D>(x, off, t0, kSmallTok, num_tokens, H, h, md, dst_row, dst_buf, xs);
   __syncthreads();
   float acc[kSmallTok][CPL];
@@ -780,12 +784,21 @@ cudaError_t launch_append(int64_t T, const oscar_dims_t* d, const void* k, const
                           cudaStream_t stream) {
   // Few tokens per (head, K|V): spread R's rows over warps instead of staging all of R.
   if (T <= kSmallTokenLimit) {
-    const dim3 grid(static_cast<unsigned>((T + kSmallTok - 1) / kSmallTok), d->num_kv_heads, 2);
-    append_small_kernel<D><<<grid, kThreads, 0, stream>>>(
-        T, d->num_kv_heads, d->group_size, d->num_pages, static_cast<const __nv_bfloat16*>(k),
-        static_cast<const __nv_bfloat16*>(v), R_k, R_v, clip_k, clip_v, offset_k, slots, codes,
-        static_cast<__half*>(sz), md);
-    return cudaGetLastError();
+    // programmatic stream serialisation: the kernel may start while the one before ends
+    // (it waits for it before reading the token rows or writing anything)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((T + kSmallTok - 1) / kSmallTok), d->num_kv_heads, 2);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, append_small_kernel<D>, T, d->num_kv_heads, d->group_size, d->num_pages,
+                              static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), R_k, R_v,
+                              clip_k, clip_v, offset_k, slots, codes, static_cast<__half*>(sz), md);
   }
   if (D == 128 && T < 0x7fffffffLL - kUmTok) {  // the rotation on tcgen05 tensor cores
     switch (d->group_size) {
