@@ -2,9 +2,9 @@
 """Benchmark of the OSCAR decode step (INT2 rotated KV append + mixed-precision
 paged decode) on one GB300, printing one JSON line.
 
-A step is one decode step of a batch: oscar_append_mixed of each sequence's
-current token (INT2 pool and its BF16 window row), then oscar_decode over the
-whole cache.  The default workload is the
+A step is one decode step of a batch: oscar_append_decode, which appends each
+sequence's current token (INT2 pool and its BF16 window row, as
+oscar_append_mixed) and decodes over the whole cache (as oscar_decode).  The default workload is the
 batch-1 long decode (32 query / 8 KV heads, head_dim 128, context 32768, sink
 64 + window 128 in BF16, group 64, shuffled pages).  Its cache (21.7 MB) fits
 in L2, so the benchmark builds enough independent cache replicas (disjoint
@@ -433,12 +433,19 @@ class DecodeSetup:
             ok.oscar_bf16_decode(w.dims, B, msl_r[r], bf.pps, x["q"], bf.pages, x["bpt"], x["blens"], 0.0,
                                  x["out_bf"], ws_bf)
 
+        def step_r(r):
+            # one call: the current tokens appended (INT2 pool, BF16 window rows), then the decode
+            x = V[r]
+            ok.oscar_append_decode(w.dims, B, msl_r[r], cache.pps, x["q"], x["k"], x["v"], cache.R_k, cache.R_v,
+                                   cache.clip_k, cache.clip_v, x["slots"], cache.int2_pages, cache.scale_zero,
+                                   x["sink"], x["win"], x["pt"], x["lens"], w.sink_len, w.window_len, 0.0, x["out"],
+                                   ws)
+
         def step(i):
-            r = i % NR
-            append_r(r)
-            decode_r(r)
+            step_r(i % NR)
 
         self.append_r, self.decode_r, self.bf16_r, self.step = append_r, decode_r, bf16_r, step
+        self.step_r = step_r
 
     def bytes_decode(self):
         return algorithmic_bytes_decode(self.w, self.lens_all[:self.B])
@@ -517,7 +524,7 @@ def run_ours(args, world, rank, local):
     lens_all = S.lens_all
     msl = max(lens_all)
     stage, per_stage, out = S.stage, S.per_stage, S.out
-    append_r, decode_r, bf16_r, step = S.append_r, S.decode_r, S.bf16_r, S.step
+    append_r, decode_r, bf16_r, step, step_r = S.append_r, S.decode_r, S.bf16_r, S.step, S.step_r
 
     def timed(fn, n, warm):
         return timed_graph(fn, n, warm, dev, world, barrier)
@@ -578,8 +585,7 @@ def run_ours(args, world, rank, local):
         sl = slice(r * B, (r + 1) * B)
         x = V[r]
         stage[r * per_stage:(r + 1) * per_stage].copy_(stage_h[r * per_stage:(r + 1) * per_stage], non_blocking=True)
-        append_r(r)
-        decode_r(r)
+        step_r(r)
         out_h[sl].copy_(x["out"], non_blocking=True)
 
     # One CUDA graph per cache replica holds a whole step: the host->device copies

@@ -220,6 +220,34 @@ oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, int32_t max
                             size_t workspace_bytes, void* stream);
 
 /*
+ * oscar_append_decode -- one decode step in one call: the current token of every
+ * sequence is appended (exactly oscar_append_mixed with token b at position
+ * seq_lens[b] - 1 of sequence b: INT2 codes and scale/zero into the pool at
+ * slot_mapping[b], the BF16 row into the sink or the window ring), then the queries
+ * are decoded (exactly oscar_decode, the appended token included).  The result equals
+ * those two calls.  When the decode takes its single-wave form and window_len >= 1
+ * (the appended position is then in the window, never read from the INT2 pool by
+ * this decode), the append runs inside the decode's sink/window CTAs, beside the
+ * INT2 splits instead of before them; otherwise the two run one after the other.
+ * (OSCAR project card "How it works": the new K/V are rotated, clipped and quantised
+ * as they are appended, and the decode attends a BF16 recent window.)
+ * Arguments: those of oscar_decode, plus
+ *   k, v          bf16 [batch][Hkv][D]: the current token of each sequence (16-byte aligned)
+ *   clip_k, clip_v, offset_k, slot_mapping   as oscar_append_mixed (slot_mapping [batch])
+ *   int2_pages, scale_zero_pages, bf16_sink, bf16_window   written (the append) and read
+ * Workspace: oscar_decode_workspace_bytes.  Errors: those of both calls; nothing is
+ * launched on an argument error.
+ */
+oscar_status_t oscar_append_decode(const oscar_dims_t* dims, int32_t batch, int32_t max_seq_len,
+                                   int32_t pages_per_split, const void* q, const void* k, const void* v,
+                                   const float* R_k, const float* R_v, const float* clip_k, const float* clip_v,
+                                   const float* offset_k, const int64_t* slot_mapping, uint8_t* int2_pages,
+                                   void* scale_zero_pages, void* bf16_sink, void* bf16_window,
+                                   const int32_t* page_table, const int32_t* seq_lens, int32_t sink_len,
+                                   int32_t window_len, float sm_scale, float* out, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/*
  * oscar_extend -- mixed-precision paged attention of many query tokens per
  * sequence (chunked prefill / extend) over the same INT2 + BF16 cache.
  *

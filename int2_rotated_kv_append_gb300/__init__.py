@@ -61,6 +61,8 @@ def _load():
         "oscar_decode_plan": (I32, [D, I32, I32, I32, I32, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
                                     ctypes.POINTER(I32)]),
         "oscar_decode": (I32, [D, I32, I32, I32, P, P, P, P, P, P, P, P, P, I32, I32, F32, P, P, SZ, P]),
+        "oscar_append_decode": (I32, [D, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, I32, I32, F32,
+                                      P, P, SZ, P]),
         "oscar_decode_noalloc": (I32, [D, I32, I32, I32, P, P, P, P, P, P, P, P, P, I32, I32, F32, P, P]),
         "oscar_extend_workspace_bytes": (SZ, [D, I32, I32, I32, I32, I32]),
         "oscar_extend": (I32, [D, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, I32, I32, F32, P, P, SZ, P]),
@@ -186,6 +188,20 @@ def oscar_decode(dims, batch, max_seq_len, pages_per_split, q, R_k, R_v, int2_pa
                             _ptr(bf16_window), _ptr(page_table), _ptr(seq_lens), int(sink_len), int(window_len),
                             float(sm_scale), _ptr(out), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream)), "oscar_decode")
+
+
+def oscar_append_decode(dims, batch, max_seq_len, pages_per_split, q, k, v, R_k, R_v, clip_k, clip_v, slot_mapping,
+                        int2_pages, scale_zero_pages, bf16_sink, bf16_window, page_table, seq_lens, sink_len,
+                        window_len, sm_scale, out, workspace, stream=None, offset_k=None):
+    """One decode step: appends each sequence's current token k, v [B][Hkv][D] (position
+    seq_lens[b] - 1, slot slot_mapping[b]), then decodes q; writes fp32 out [B][Hq][D]."""
+    _check(lib.oscar_append_decode(ctypes.byref(_dims(dims)), int(batch), int(max_seq_len), int(pages_per_split),
+                                   _ptr(q), _ptr(k), _ptr(v), _ptr(R_k), _ptr(R_v), _ptr(clip_k), _ptr(clip_v),
+                                   _ptr(offset_k), _ptr(slot_mapping), _ptr(int2_pages), _ptr(scale_zero_pages),
+                                   _ptr(bf16_sink), _ptr(bf16_window), _ptr(page_table), _ptr(seq_lens),
+                                   int(sink_len), int(window_len), float(sm_scale), _ptr(out), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "oscar_append_decode")
 
 
 def oscar_extend_workspace_bytes(dims, num_rows, max_seq_len, pages_per_split, sink_len, window_len) -> int:

@@ -32,8 +32,8 @@ constexpr int64_t kSmallTokenLimit = 512;  // at most this many tokens use the f
 // first tokens and a BF16 recent window).  Inactive (sink == win == nullptr) for
 // oscar_append.
 struct MixedDst {
-  const int32_t* seq_ids;    // [T]
-  const int32_t* positions;  // [T]
+  const int32_t* seq_ids;    // [T]; null: token t is the current token of sequence t (position seq_lens[t] - 1)
+  const int32_t* positions;  // [T] (null with seq_ids)
   const int32_t* seq_lens;   // [B] lengths after this append
   int B, S, W;
   __nv_bfloat16* sink;       // [B][2][Hkv][S][D]
@@ -51,13 +51,14 @@ __device__ __forceinline__ int64_t mixed_row(const MixedDst& md, int64_t t, int6
                                              int kv, int* which) {
   *which = 0;
   if (slot < 0) return -1;
-  const int b = __ldg(md.seq_ids + t), p = __ldg(md.positions + t);
-  if (b < 0 || b >= md.B || p < 0) {
+  const int b = md.seq_ids != nullptr ? __ldg(md.seq_ids + t) : static_cast<int>(t);
+  if (b < 0 || b >= md.B) {
     record_error(OSCAR_DEVERR_POSITION);
     return -1;
   }
   const int L = __ldg(md.seq_lens + b);
-  if (p >= L) {
+  const int p = md.seq_ids != nullptr ? __ldg(md.positions + t) : L - 1;
+  if (p < 0 || p >= L) {
     record_error(OSCAR_DEVERR_POSITION);
     return -1;
   }
@@ -882,6 +883,30 @@ extern "C" oscar_status_t oscar_append_mixed(const oscar_dims_t* dims, int64_t n
   md.sink = sink_len > 0 ? static_cast<__nv_bfloat16*>(bf16_sink) : nullptr;
   md.win = window_len > 0 ? static_cast<__nv_bfloat16*>(bf16_window) : nullptr;
   return run_append(dims, num_tokens, k, v, R_k, R_v, clip_k, clip_v, offset_k, slot_mapping, int2_pages,
+                    scale_zero_pages, md, stream);
+}
+
+// The current token of every sequence (token b at position seq_lens[b] - 1 of sequence
+// b): oscar_append_mixed with those ids and positions (oscar_append_decode's sequential
+// form).
+oscar_status_t oscar_internal_append_current(const oscar_dims_t* dims, int32_t batch, const void* k, const void* v,
+                                             const float* R_k, const float* R_v, const float* clip_k,
+                                             const float* clip_v, const float* offset_k,
+                                             const int64_t* slot_mapping, const int32_t* seq_lens,
+                                             int32_t sink_len, int32_t window_len, uint8_t* int2_pages,
+                                             void* scale_zero_pages, void* bf16_sink, void* bf16_window,
+                                             void* stream) {
+  if (batch < 0 || sink_len < 0 || window_len < 0) return OSCAR_ERR_INVALID_ARG;
+  if (batch > 0 && !seq_lens) return OSCAR_ERR_INVALID_ARG;
+  if ((sink_len > 0 && !bf16_sink) || (window_len > 0 && !bf16_window)) return OSCAR_ERR_INVALID_ARG;
+  MixedDst md{};
+  md.seq_lens = seq_lens;
+  md.B = batch;
+  md.S = sink_len;
+  md.W = window_len;
+  md.sink = sink_len > 0 ? static_cast<__nv_bfloat16*>(bf16_sink) : nullptr;
+  md.win = window_len > 0 ? static_cast<__nv_bfloat16*>(bf16_window) : nullptr;
+  return run_append(dims, batch, k, v, R_k, R_v, clip_k, clip_v, offset_k, slot_mapping, int2_pages,
                     scale_zero_pages, md, stream);
 }
 

@@ -89,6 +89,15 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __
 
 }  // namespace oscar
 
+// oscar_append_mixed of the current token of every sequence (append.cu).
+oscar_status_t oscar_internal_append_current(const oscar_dims_t* dims, int32_t batch, const void* k, const void* v,
+                                             const float* R_k, const float* R_v, const float* clip_k,
+                                             const float* clip_v, const float* offset_k,
+                                             const int64_t* slot_mapping, const int32_t* seq_lens,
+                                             int32_t sink_len, int32_t window_len, uint8_t* int2_pages,
+                                             void* scale_zero_pages, void* bf16_sink, void* bf16_window,
+                                             void* stream);
+
 // Per-unit error readers (each defined in its own .cu file).
 oscar_status_t oscar_internal_append_errors(uint32_t* flags, int reset);
 oscar_status_t oscar_internal_decode_errors(uint32_t* flags, int reset);

@@ -209,6 +209,20 @@ size_t extend_plan_bytes(const oscar_dims_t* dims, int32_t rows, int32_t max_seq
 
 namespace {
 
+// oscar_append_decode's append: the current token of every sequence.
+struct CurrentAppend {
+  const void* k;
+  const void* v;
+  const float* clip_k;
+  const float* clip_v;
+  const float* offset_k;
+  const int64_t* slot_mapping;
+  uint8_t* int2_pages;
+  void* scale_zero_pages;
+  void* bf16_sink;
+  void* bf16_window;
+};
+
 // The mixed-precision attention of `rows` query rows: a decode (row_seq null,
 // row b is sequence b and attends its whole cache) or an extend (row b attends
 // positions 0 .. row_pos[b] of sequence row_seq[b] < num_seqs).
@@ -218,7 +232,7 @@ oscar_status_t mixed_attention(const oscar_dims_t* dims, int32_t rows, int32_t n
                                const void* scale_zero_pages, const void* bf16_sink, const void* bf16_window,
                                const int32_t* page_table, const int32_t* seq_lens, int32_t sink_len,
                                int32_t window_len, float sm_scale, float* out, void* workspace,
-                               size_t workspace_bytes, void* stream) {
+                               size_t workspace_bytes, void* stream, const CurrentAppend* app = nullptr) {
   oscar_status_t st = check_dims(dims);
   if (st != OSCAR_OK) return st;
   if (rows < 0 || num_seqs < 0 || max_seq_len < 0 || pages_per_split < 0 || sink_len < 0 || window_len < 0)
@@ -254,6 +268,26 @@ oscar_status_t mixed_attention(const oscar_dims_t* dims, int32_t rows, int32_t n
   p.row_pos = row_pos;
   p.num_seqs = num_seqs;
   p.out = out;
+  if (app != nullptr && !(p.fused && window_len >= 1)) {
+    // sequential form: the append, then the decode (one stream)
+    const oscar_status_t sa = oscar_internal_append_current(
+        dims, rows, app->k, app->v, R_k, R_v, app->clip_k, app->clip_v, app->offset_k, app->slot_mapping, seq_lens,
+        sink_len, window_len, app->int2_pages, app->scale_zero_pages, app->bf16_sink, app->bf16_window, stream);
+    if (sa != OSCAR_OK) return sa;
+    app = nullptr;
+  }
+  if (app != nullptr) {  // fused form: the unit's BF16 CTA appends the current token
+    p.app_k = static_cast<const __nv_bfloat16*>(app->k);
+    p.app_v = static_cast<const __nv_bfloat16*>(app->v);
+    p.app_clip_k = app->clip_k;
+    p.app_clip_v = app->clip_v;
+    p.app_offset_k = app->offset_k;
+    p.app_slots = app->slot_mapping;
+    p.app_codes = app->int2_pages;
+    p.app_sz = static_cast<__half*>(app->scale_zero_pages);
+    p.app_sink = static_cast<__nv_bfloat16*>(app->bf16_sink);
+    p.app_win = static_cast<__nv_bfloat16*>(app->bf16_window);
+  }
   if (p.fused) {
     p.q_rot = nullptr;
     p.n_dense_pages = (sink_len + kPageSize - 1) / kPageSize + (window_len + kPageSize - 1) / kPageSize;
@@ -275,6 +309,28 @@ extern "C" oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, 
   return mixed_attention(dims, batch, batch, nullptr, nullptr, max_seq_len, pages_per_split, q, R_k, R_v,
                          int2_pages, scale_zero_pages, bf16_sink, bf16_window, page_table, seq_lens, sink_len,
                          window_len, sm_scale, out, workspace, workspace_bytes, stream);
+}
+
+extern "C" oscar_status_t oscar_append_decode(const oscar_dims_t* dims, int32_t batch, int32_t max_seq_len,
+                                              int32_t pages_per_split, const void* q, const void* k, const void* v,
+                                              const float* R_k, const float* R_v, const float* clip_k,
+                                              const float* clip_v, const float* offset_k,
+                                              const int64_t* slot_mapping, uint8_t* int2_pages,
+                                              void* scale_zero_pages, void* bf16_sink, void* bf16_window,
+                                              const int32_t* page_table, const int32_t* seq_lens, int32_t sink_len,
+                                              int32_t window_len, float sm_scale, float* out, void* workspace,
+                                              size_t workspace_bytes, void* stream) {
+  if (batch < 0) return OSCAR_ERR_INVALID_ARG;
+  if (batch == 0) return check_dims(dims);
+  if (!k || !v || !clip_k || !clip_v || !slot_mapping) return OSCAR_ERR_INVALID_ARG;
+  if (misaligned16(k) || misaligned16(v) || misaligned16(clip_k) || misaligned16(clip_v) ||
+      misaligned16(offset_k))
+    return OSCAR_ERR_INVALID_ARG;
+  const CurrentAppend app{k, v, clip_k, clip_v, offset_k, slot_mapping, int2_pages, scale_zero_pages, bf16_sink,
+                          bf16_window};
+  return mixed_attention(dims, batch, batch, nullptr, nullptr, max_seq_len, pages_per_split, q, R_k, R_v,
+                         int2_pages, scale_zero_pages, bf16_sink, bf16_window, page_table, seq_lens, sink_len,
+                         window_len, sm_scale, out, workspace, workspace_bytes, stream, &app);
 }
 
 namespace oscar_extend_rows {

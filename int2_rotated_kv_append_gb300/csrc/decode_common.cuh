@@ -77,6 +77,18 @@ struct Params {
   const int32_t* q_start;
   int tiles;
   float* out;
+  // oscar_append_decode's fused form: the current token of sequence b (position
+  // seq_lens[b] - 1) is appended by the unit's BF16 CTA (null app_k: no append)
+  const __nv_bfloat16* app_k;  // [B][H][D]
+  const __nv_bfloat16* app_v;
+  const float* app_clip_k;     // [H][D]
+  const float* app_clip_v;
+  const float* app_offset_k;   // [H][D] or null
+  const int64_t* app_slots;    // [B]
+  uint8_t* app_codes;          // the INT2 pool (the same as codes)
+  __half* app_sz;              // the scale/zero pool (the same as sz)
+  __nv_bfloat16* app_sink;     // the sink and window buffers (the same as sink, win)
+  __nv_bfloat16* app_win;
   float* q_rot;
   uint32_t* qfrag;  // kQfragBytes per (sequence, KV head); null when not needed
   float* part_o;

@@ -1,0 +1,118 @@
+"""GPU parity of oscar_append_decode (one decode step: append each sequence's current
+token, then decode).  The cache of every sequence but its last token is built first;
+then two copies take the step, one as oscar_append_mixed + oscar_decode and one as
+oscar_append_decode.  The BF16 rows must be equal, the codes of the appended tokens
+must match the oracle's append (boundary band exempt), and the outputs must be equal
+to the two-call step and match the oracle's decode of the resulting cache."""
+
+import numpy as np
+import pytest
+import torch
+
+import int2_rotated_kv_append_gb300 as ok
+from int2_rotated_kv_append_gb300 import synth
+from int2_rotated_kv_append_gb300.cache import Int2Cache
+from parity import check_append, compare_decode, oracle_decode_on_gpu_cache, pools_to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def _step_pair(w, pps=0):
+    """Cache of all tokens but the last of each sequence, in two copies; the current
+    tokens (one per sequence, in sequence order)."""
+    d = torch.device("cuda")
+    cache = Int2Cache(w, pages_per_split=pps)
+    B, H, D = w.batch, w.num_kv_heads, w.head_dim
+    cache.sink = torch.zeros((B, 2, H, max(w.sink_len, 1), D), dtype=torch.bfloat16, device=d)
+    cache.window = torch.zeros((B, 2, H, max(w.window_len, 1), D), dtype=torch.bfloat16, device=d)
+    lens = w.seq_lens.numpy()
+    pos, seq = w.tok_pos.numpy(), w.tok_seq.numpy()
+    cur = np.array([np.nonzero((seq == b) & (pos == lens[b] - 1))[0][0] for b in range(B)])
+    past = np.setdiff1d(np.arange(len(pos)), cur)
+    ip = torch.as_tensor(past)
+    if len(past):
+        ok.oscar_append_mixed(w.dims, w.k[ip].to(d), w.v[ip].to(d), cache.R_k, cache.R_v, cache.clip_k, cache.clip_v,
+                              None, w.slot_mapping[ip].to(d), w.tok_seq[ip].to(d), w.tok_pos[ip].to(d),
+                              torch.as_tensor(np.maximum(lens - 1, 0), dtype=torch.int32).to(d), w.sink_len,
+                              w.window_len, cache.int2_pages, cache.scale_zero, cache.sink, cache.window,
+                              offset_k=cache.offset_k)
+    other = Int2Cache(w, pages_per_split=pps)
+    other.int2_pages, other.scale_zero = cache.int2_pages.clone(), cache.scale_zero.clone()
+    other.sink, other.window = cache.sink.clone(), cache.window.clone()
+    return cache, other, cur, past
+
+
+def _run_two_calls(w, cache, cur):
+    d = torch.device("cuda")
+    ic = torch.as_tensor(cur)
+    ok.oscar_append_mixed(w.dims, w.k[ic].to(d), w.v[ic].to(d), cache.R_k, cache.R_v, cache.clip_k, cache.clip_v,
+                          None, w.slot_mapping[ic].to(d), torch.arange(w.batch, dtype=torch.int32, device=d),
+                          w.tok_pos[ic].to(d), cache.seq_lens, w.sink_len, w.window_len, cache.int2_pages,
+                          cache.scale_zero, cache.sink, cache.window, offset_k=cache.offset_k)
+    return cache.decode(w.q.cuda())
+
+
+def _run_fused(w, cache, cur):
+    d = torch.device("cuda")
+    ic = torch.as_tensor(cur)
+    out = torch.empty((w.batch, w.num_q_heads, w.head_dim), dtype=torch.float32, device=d)
+    ws = cache.workspace(w.max_seq_len)
+    ok.oscar_append_decode(w.dims, w.batch, w.max_seq_len, cache.pps, w.q.cuda(), w.k[ic].to(d).contiguous(),
+                           w.v[ic].to(d).contiguous(), cache.R_k, cache.R_v, cache.clip_k, cache.clip_v,
+                           w.slot_mapping[ic].to(d).contiguous(), cache.int2_pages, cache.scale_zero, cache.sink,
+                           cache.window, cache.page_table, cache.seq_lens, w.sink_len, w.window_len, 0.0, out, ws,
+                           offset_k=cache.offset_k)
+    return out
+
+
+@pytest.mark.parametrize("name,Hq,H,G,lens,S,W,key_offset,fused", [
+    ("batch1_gqa4", 32, 8, 64, [3000], 64, 128, False, 1),       # single-wave form: the append in the BF16 CTAs
+    ("batch2_gqa4_g128", 8, 2, 128, [900, 1700], 16, 48, False, 1),
+    ("batch1_gqa8", 16, 2, 64, [2500], 32, 64, False, 1),        # the 8-warp single-wave form
+    ("batch1_key_offset", 8, 2, 64, [1200], 16, 32, True, 1),
+    ("current_in_sink", 8, 2, 64, [5, 700], 16, 32, False, 1),    # a current token inside the sink
+    ("no_window", 8, 2, 64, [600, 300], 16, 0, False, 1),         # W = 0: the two calls one after the other
+    ("batch64", 32, 8, 64, [300 + 37 * i for i in range(64)], 16, 64, False, 0),  # general form: sequential
+])
+def test_append_decode_equals_append_then_decode(name, Hq, H, G, lens, S, W, key_offset, fused):
+    w = synth.make_workload(num_q_heads=Hq, num_kv_heads=H, head_dim=128, group_size=G, sink_len=S, window_len=W,
+                            seq_lens=lens, seed=len(lens) * 7 + Hq + G + S + W, key_offset=key_offset)
+    assert ok.oscar_decode_plan(w.dims, w.batch, w.max_seq_len, 0, S, W)["fused"] == fused
+    a, b, cur, past = _step_pair(w)
+    ok.oscar_device_errors(reset=True)
+    out_a = _run_two_calls(w, a, cur)
+    out_b = _run_fused(w, b, cur)
+    torch.cuda.synchronize()
+    assert ok.oscar_device_errors(reset=True) == 0
+    # the BF16 rows are the same bf16 conversions of the same inputs
+    assert torch.equal(a.sink, b.sink) and torch.equal(a.window, b.window)
+    # the appended tokens' codes and scale/zero against the oracle's append
+    ic = torch.as_tensor(cur)
+    codes, sz = pools_to_host(b)
+    check_append(w, codes, sz, w.k[ic], w.v[ic], w.slot_mapping[ic].numpy(), written_slots=w.slot_mapping.numpy())
+    # the decode of this step does not read the appended token's codes (it is in the
+    # window or the sink): equal outputs whenever the BF16 rows are equal
+    if W > 0:
+        assert torch.equal(out_a, out_b)
+    compare_decode(out_b, oracle_decode_on_gpu_cache(w, b))
+
+
+def test_append_decode_slot_out_of_range_is_flagged():
+    w = synth.make_workload(num_q_heads=8, num_kv_heads=2, head_dim=128, group_size=64, sink_len=8, window_len=16,
+                            seq_lens=[400], seed=77)
+    assert ok.oscar_decode_plan(w.dims, w.batch, w.max_seq_len, 0, 8, 16)["fused"] == 1
+    a, b, cur, past = _step_pair(w)
+    d = torch.device("cuda")
+    ic = torch.as_tensor(cur)
+    slots = torch.full((1,), w.num_pages * w.page_size, dtype=torch.int64, device=d)  # one past the pool
+    out = torch.empty((1, 8, 128), dtype=torch.float32, device=d)
+    before = b.int2_pages.clone()
+    ok.oscar_device_errors(reset=True)
+    ok.oscar_append_decode(w.dims, 1, w.max_seq_len, b.pps, w.q.cuda(), w.k[ic].to(d).contiguous(),
+                           w.v[ic].to(d).contiguous(), b.R_k, b.R_v, b.clip_k, b.clip_v, slots, b.int2_pages,
+                           b.scale_zero, b.sink, b.window, b.page_table, b.seq_lens, 8, 16, 0.0, out,
+                           b.workspace(w.max_seq_len))
+    torch.cuda.synchronize()
+    assert ok.oscar_device_errors(reset=True) & ok.OSCAR_DEVERR_SLOT
+    assert torch.equal(b.int2_pages, before)  # no code written
+    assert torch.isfinite(out).all()
