@@ -433,13 +433,15 @@ class DecodeSetup:
             ok.oscar_bf16_decode(w.dims, B, msl_r[r], bf.pps, x["q"], bf.pages, x["bpt"], x["blens"], 0.0,
                                  x["out_bf"], ws_bf)
 
-        def step_r(r):
+        ws_alt = cache.workspace(max(lens_all)).clone()  # a second step in flight on another stream
+
+        def step_r(r, alt=False):
             # one call: the current tokens appended (INT2 pool, BF16 window rows), then the decode
             x = V[r]
             ok.oscar_append_decode(w.dims, B, msl_r[r], cache.pps, x["q"], x["k"], x["v"], cache.R_k, cache.R_v,
                                    cache.clip_k, cache.clip_v, x["slots"], cache.int2_pages, cache.scale_zero,
                                    x["sink"], x["win"], x["pt"], x["lens"], w.sink_len, w.window_len, 0.0, x["out"],
-                                   ws)
+                                   ws_alt if alt else ws)
 
         def step(i):
             step_r(i % NR)
@@ -574,6 +576,11 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peak_hbm()
     bf_us = ms_bf / K * 1e3
 
+    # kernels of one oscar_append_decode: q-rotation, decode, merge (the single-wave
+    # form appends inside the decode), plus the append kernel when it runs on its own
+    plan = ok.oscar_decode_plan(w.dims, B, msl, cache.pps, w.sink_len, w.window_len)
+    step_kernels = 3 if plan["fused"] and w.window_len >= 1 else 4
+
     # End to end through the public API with pinned host buffers.
     E = min(K, 2000)
     log("end-to-end loop")
@@ -585,24 +592,28 @@ def run_ours(args, world, rank, local):
         sl = slice(r * B, (r + 1) * B)
         x = V[r]
         stage[r * per_stage:(r + 1) * per_stage].copy_(stage_h[r * per_stage:(r + 1) * per_stage], non_blocking=True)
-        step_r(r)
+        step_r(r, alt=(r % 2) == 1)
         out_h[sl].copy_(x["out"], non_blocking=True)
 
     # One CUDA graph per cache replica holds a whole step: the host->device copies
     # of its inputs, the append, the decode and the device->host copy of its
-    # output.  Two steps are in flight, as in a serving loop: before launching step
-    # i the host waits until the output of step i - 2 has landed in host memory.
-    side = torch.cuda.Stream()
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
-        for r in range(NR):
+    # output.  Two steps are in flight, as in a serving loop with two independent
+    # batches: replica r's graph runs on stream r % 2 with its own workspace, so one
+    # step's copies and launch overlap the other's kernels, and before launching
+    # step i the host waits until the output of step i - 2 has landed in host memory.
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s_ in streams:
+        s_.wait_stream(stream)
+    for r in range(NR):
+        with torch.cuda.stream(streams[r % 2]):
             e2e_body(r)
-    stream.wait_stream(side)
+    for s_ in streams:
+        stream.wait_stream(s_)
     torch.cuda.synchronize()
     graphs = []
     for r in range(NR):
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
+        with torch.cuda.graph(g, stream=streams[r % 2]):
             e2e_body(r)
         graphs.append(g)
 
@@ -612,9 +623,11 @@ def run_ours(args, world, rank, local):
         for i in range(n):
             if i >= 2:
                 done[i % 2].synchronize()  # step i - 2's output is in host memory
-            graphs[i % NR].replay()
-            done[i % 2].record(stream)
-        stream.synchronize()
+            r = i % NR
+            with torch.cuda.stream(streams[r % 2]):
+                graphs[r].replay()
+                done[i % 2].record(streams[r % 2])
+        torch.cuda.synchronize()
 
     e2e_run(min(50, E))
     barrier()
@@ -667,9 +680,10 @@ def run_ours(args, world, rank, local):
             "cpu_baseline": cpu,
             "e2e": {"value": whole_job_gbps(world, step_bytes, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "mode": "one CUDA graph per step (H2D inputs, append, decode, D2H output); two steps in flight, "
-                             "the host waits for step i-2's output before launching step i"},
-            "gpu_launches": K * 4,
+                    "mode": "one CUDA graph per step (H2D inputs, oscar_append_decode, D2H output); two steps in "
+                             "flight on two streams (independent cache replicas, one workspace each), the host waits "
+                             "for step i-2's output before launching step i"},
+            "gpu_launches": K * step_kernels,
             **extra,
             "append_workload": append_line,
             "extend_workload": extend_line,
