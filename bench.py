@@ -576,10 +576,10 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peak_hbm()
     bf_us = ms_bf / K * 1e3
 
-    # kernels of one oscar_append_decode: q-rotation, decode, merge (the single-wave
-    # form appends inside the decode), plus the append kernel when it runs on its own
-    plan = ok.oscar_decode_plan(w.dims, B, msl, cache.pps, w.sink_len, w.window_len)
-    step_kernels = 3 if plan["fused"] and w.window_len >= 1 else 4
+    # kernels of one oscar_append_decode: q-rotation, decode, merge; with a window the
+    # decode's sink/window CTA appends the current token (the tensor-core kernels),
+    # without one the append kernel runs first
+    step_kernels = 3 if w.window_len >= 1 and w.head_dim == 128 else 4
 
     # End to end through the public API with pinned host buffers.
     E = min(K, 2000)

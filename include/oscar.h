@@ -225,10 +225,12 @@ oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, int32_t max
  * seq_lens[b] - 1 of sequence b: INT2 codes and scale/zero into the pool at
  * slot_mapping[b], the BF16 row into the sink or the window ring), then the queries
  * are decoded (exactly oscar_decode, the appended token included).  The result equals
- * those two calls.  When the decode takes its single-wave form and window_len >= 1
- * (the appended position is then in the window, never read from the INT2 pool by
- * this decode), the append runs inside the decode's sink/window CTAs, beside the
- * INT2 splits instead of before them; otherwise the two run one after the other.
+ * those two calls.  When window_len >= 1 and the decode runs on its tensor-core
+ * kernels (head_dim 128, group 64 or 128, GQA 1..8; the appended position is then in
+ * the sink or the window, never read from the INT2 pool by this decode),
+ * the append runs inside the decode, in the CTA that attends the sink/window rows
+ * holding that position, beside the INT2 splits instead of before them; otherwise
+ * the two run one after the other.
  * (OSCAR project card "How it works": the new K/V are rotated, clipped and quantised
  * as they are appended, and the decode attends a BF16 recent window.)
  * Arguments: those of oscar_decode, plus

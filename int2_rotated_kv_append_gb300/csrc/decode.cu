@@ -268,7 +268,11 @@ oscar_status_t mixed_attention(const oscar_dims_t* dims, int32_t rows, int32_t n
   p.row_pos = row_pos;
   p.num_seqs = num_seqs;
   p.out = out;
-  if (app != nullptr && !(p.fused && window_len >= 1)) {
+  // The current token goes into the sink or the window when W >= 1, and no INT2 split
+  // reads its position: the CTA that attends its sink/window rows appends it (the
+  // fused single-wave kernel's BF16 CTA, or the tensor-core split kernel's dense CTA).
+  // Otherwise (no window, or the CUDA-core split body) the append runs first.
+  if (app != nullptr && !(window_len >= 1 && (p.fused || int2_mma_supported(p)))) {
     // sequential form: the append, then the decode (one stream)
     const oscar_status_t sa = oscar_internal_append_current(
         dims, rows, app->k, app->v, R_k, R_v, app->clip_k, app->clip_v, app->offset_k, app->slot_mapping, seq_lens,
@@ -276,7 +280,7 @@ oscar_status_t mixed_attention(const oscar_dims_t* dims, int32_t rows, int32_t n
     if (sa != OSCAR_OK) return sa;
     app = nullptr;
   }
-  if (app != nullptr) {  // fused form: the unit's BF16 CTA appends the current token
+  if (app != nullptr) {  // fused form
     p.app_k = static_cast<const __nv_bfloat16*>(app->k);
     p.app_v = static_cast<const __nv_bfloat16*>(app->v);
     p.app_clip_k = app->clip_k;

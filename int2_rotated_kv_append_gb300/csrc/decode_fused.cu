@@ -22,6 +22,7 @@
 // Logits are in log2 units (scale * log2 e folded into the query operands).
 #include <mutex>
 
+#include "append_token.cuh"
 #include "int2_page.cuh"
 
 namespace oscar_dec {
@@ -60,115 +61,6 @@ struct FusedGeo {
   static constexpr size_t kOffBars = kOffPid + fused_max_pps<NW>() * 4;  // NW * kStages ring barriers
   static constexpr size_t kSmem = kOffBars + (NW * kStages + 1) * 8;  // + the operand block's barrier
 };
-
-// oscar_append_decode's fused form, in the unit's BF16 CTA: the current token of
-// sequence b (position L - 1, L = seq_lens[b]) for KV head h, appended as
-// oscar_append_mixed appends it: K (minus the key offset, in fp32) and V rotated by
-// R_k[h] and R_v[h] (y_j = sum_i x_i R[i][j]: each warp sums a slice of the rows, the
-// slices are added in order), clipped, quantised per group of G channels (fp16 scale
-// (max - min) / 3 and zero min, codes rint((y - zero) / scale) clamped to 0..3, 0 when
-// the scale is 0) and written to the pool row of slot_mapping[b]; the BF16 rows (the
-// offset key rounded to bf16, and V) written to the sink row or the window slot of
-// position L - 1.  The INT2 splits never read that position (it is in the window), and
-// the BF16 rows are written before this CTA's own sink/window copies read them.
-template <int NW>
-__device__ __forceinline__ void fused_append_token(const Params& p, int b, int h, uint8_t* smem) {
-  constexpr int T = NW * 32;
-  constexpr int kRows = kD / NW;  // rows of R per warp
-  float* xs = reinterpret_cast<float*>(smem);  // [2][kD]: the token's K (offset) and V
-  float* part = xs + 2 * kD;                   // [2][NW][kD]: per-warp partial sums
-  float* cmn = part + 2 * NW * kD;             // [2][4]: min of each 32-channel chunk
-  float* cmx = cmn + 8;                        // [2][4]: max
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  grid_dep_wait();  // the previous step's reads of the window row this token replaces are over
-  const int L = __ldg(p.seq_lens + b);
-  if (L < 1 || L > p.max_seq_len) return;  // nothing to append (the decode flags the length)
-  const int pos = L - 1;
-  const int64_t slot = __ldg(p.app_slots + b);  // a negative slot: the token is skipped entirely
-  if (slot < 0) return;
-  for (int i = tid; i < kD; i += T) {  // (K|V, channel pair)
-    const int kv = i >> 6, c2 = i & 63;
-    const __nv_bfloat16* x = (kv ? p.app_v : p.app_k) + (static_cast<size_t>(b) * p.H + h) * kD;
-    __nv_bfloat162 raw = reinterpret_cast<const __nv_bfloat162*>(x)[c2];
-    float2 val = __bfloat1622float2(raw);
-    if (kv == 0 && p.app_offset_k != nullptr) {
-      const float2 c = __ldg(reinterpret_cast<const float2*>(p.app_offset_k + static_cast<size_t>(h) * kD) + c2);
-      val = make_float2(__fsub_rn(val.x, c.x), __fsub_rn(val.y, c.y));
-      raw = __floats2bfloat162_rn(val.x, val.y);
-    }
-    xs[kv * kD + 2 * c2] = val.x;
-    xs[kv * kD + 2 * c2 + 1] = val.y;
-    __nv_bfloat16* dst = nullptr;
-    if (pos < p.S)
-      dst = p.app_sink + (((static_cast<size_t>(b) * 2 + kv) * p.H + h) * p.S + pos) * kD;
-    else if (p.W > 0 && pos >= max(p.S, L - p.W))
-      dst = p.app_win + (((static_cast<size_t>(b) * 2 + kv) * p.H + h) * p.W + pos % p.W) * kD;
-    if (dst != nullptr) reinterpret_cast<__nv_bfloat162*>(dst)[c2] = raw;
-  }
-  asm volatile("fence.proxy.async.global;" ::: "memory");  // the rows, for this CTA's bulk copies
-  __syncthreads();
-#pragma unroll 1
-  for (int kv = 0; kv < 2; ++kv) {
-    const float* R = (kv ? p.R_v : p.R_k) + static_cast<size_t>(h) * kD * kD +
-                     static_cast<size_t>(warp * kRows) * kD + 4 * lane;
-    float4 rr[kRows];
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) rr[r] = __ldg(reinterpret_cast<const float4*>(R + r * kD));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      const float xv = xs[kv * kD + warp * kRows + r];
-      acc.x = fmaf(xv, rr[r].x, acc.x);
-      acc.y = fmaf(xv, rr[r].y, acc.y);
-      acc.z = fmaf(xv, rr[r].z, acc.z);
-      acc.w = fmaf(xv, rr[r].w, acc.w);
-    }
-    *reinterpret_cast<float4*>(part + (kv * NW + warp) * kD + 4 * lane) = acc;
-  }
-  __syncthreads();
-  const int kv = tid >> 7, j = tid & (kD - 1);  // threads 0 .. 255: (K|V, channel)
-  float y = 0.f;
-  if (tid < 2 * kD) {
-    for (int w = 0; w < NW; ++w) y += part[(kv * NW + w) * kD + j];
-    const float cl = __ldg((kv ? p.app_clip_v : p.app_clip_k) + static_cast<size_t>(h) * kD + j);
-    y = fminf(fmaxf(y, -cl), cl);
-    float mn = y, mx = y;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    if (lane == 0) {
-      cmn[kv * 4 + (j >> 5)] = mn;
-      cmx[kv * 4 + (j >> 5)] = mx;
-    }
-  }
-  __syncthreads();
-  if (tid < 2 * kD) {
-    const int G = p.G, ng = kD / G, g = j / G;
-    float mn = INFINITY, mx = -INFINITY;
-    for (int c = g * G / 32; c < (g + 1) * G / 32; ++c) {
-      mn = fminf(mn, cmn[kv * 4 + c]);
-      mx = fmaxf(mx, cmx[kv * 4 + c]);
-    }
-    const __half sh = __float2half_rn((mx - mn) / 3.0f), zh = __float2half_rn(mn);
-    const float sc = __half2float(sh), z = __half2float(zh);
-    uint32_t code = 0;
-    if (sc != 0.f) code = static_cast<uint32_t>(fminf(fmaxf(rintf((y - z) / sc), 0.f), 3.f));
-    uint32_t wv = code << (2 * (j & 15));  // 16 channels per 32-bit word, channel j at bits 2 (j % 16)
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) wv |= __shfl_xor_sync(0xffffffffu, wv, o);
-    if (slot < static_cast<int64_t>(p.num_pages) * kPageSize) {
-      const size_t row =
-          ((static_cast<size_t>(slot / kPageSize) * p.H + h) * 2 + kv) * kPageSize + static_cast<size_t>(slot % kPageSize);
-      if ((j & 15) == 0) reinterpret_cast<uint32_t*>(p.app_codes + row * (kD / 4))[j >> 4] = wv;
-      if (j % G == 0) reinterpret_cast<__half2*>(p.app_sz + row * ng * 2)[g] = __halves2half2(sh, zh);
-    } else if (tid == 0) {
-      record_error(OSCAR_DEVERR_SLOT);
-    }
-  }
-  __syncthreads();  // the shared memory holds the sink/window stages next
-}
 
 // INT2 split CTA s < n_paged of unit (b, h), or the unit's BF16 CTA (s == n_paged).
 // The 16-warp form is held to 96 registers (the bound of a 20-warp CTA), so that the

@@ -32,6 +32,7 @@
 // CTA writes one (max, sum, output) partial per query head.
 #include <mutex>
 
+#include "append_token.cuh"
 #include "int2_page.cuh"
 
 namespace oscar_dec {
@@ -66,7 +67,9 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 5 : 3) int2_mma_split_k
   // Dispatch order: KV head fastest, then sequence, split index slowest, so the
   // last CTAs to start are the high splits that only long sequences have.
   const int s = blockIdx.z + p.split_base, h = blockIdx.x, b = blockIdx.y;
-  if (s >= p.n_paged) {
+  if (s >= p.n_paged) {  // BF16 sink/window pages (and, in oscar_append_decode, the current token's append)
+    if (p.app_k != nullptr && s - p.n_paged == current_token_dense_cta(p, b, kDensePagesPerCta))
+      fused_append_token<kWarps>(p, b, h, smem);
     dense_part<NT, kWarps>(p, (s - p.n_paged) * kDensePagesPerCta, kDensePagesPerCta, s, h, b, smem);
     return;
   }

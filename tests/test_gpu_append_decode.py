@@ -72,12 +72,22 @@ def _run_fused(w, cache, cur):
     ("batch1_key_offset", 8, 2, 64, [1200], 16, 32, True, 1),
     ("current_in_sink", 8, 2, 64, [5, 700], 16, 32, False, 1),    # a current token inside the sink
     ("no_window", 8, 2, 64, [600, 300], 16, 0, False, 1),         # W = 0: the two calls one after the other
-    ("batch64", 32, 8, 64, [300 + 37 * i for i in range(64)], 16, 64, False, 0),  # general form: sequential
+    # general split form: the append in the dense CTA that holds the current row
+    ("batch64", 32, 8, 64, [300 + 37 * i for i in range(64)], 16, 64, False, 0),
+    # 5 dense CTAs per unit (4 sink + 32 window pages): the current rows spread over all of them
+    ("batch48_many_dense_ctas", 32, 8, 64, [700 + 29 * i for i in range(48)], 64, 512, False, 0),
+    ("batch40_gqa8_g128", 32, 4, 128, [900 + 53 * i for i in range(40)], 32, 96, True, 0),
+    ("batch48_some_in_sink", 16, 4, 64, [3 + 40 * i for i in range(48)], 64, 32, False, 0),
+    ("batch64_no_window", 32, 8, 64, [300 + 37 * i for i in range(64)], 16, 0, False, 0),  # sequential
 ])
 def test_append_decode_equals_append_then_decode(name, Hq, H, G, lens, S, W, key_offset, fused):
     w = synth.make_workload(num_q_heads=Hq, num_kv_heads=H, head_dim=128, group_size=G, sink_len=S, window_len=W,
                             seq_lens=lens, seed=len(lens) * 7 + Hq + G + S + W, key_offset=key_offset)
     assert ok.oscar_decode_plan(w.dims, w.batch, w.max_seq_len, 0, S, W)["fused"] == fused
+    if name == "batch48_many_dense_ctas":  # the current rows fall in every dense CTA (8 pages each)
+        nsp = S // 16
+        ctas = {((L - 1) // 16 if L - 1 < S else nsp + ((L - 1) % W) // 16) // 8 for L in lens}
+        assert ctas == set(range((nsp + W // 16 + 7) // 8))
     a, b, cur, past = _step_pair(w)
     ok.oscar_device_errors(reset=True)
     out_a = _run_two_calls(w, a, cur)
