@@ -37,3 +37,14 @@ def test_bf16_decode_batch1_32k_config():
     out = cache.decode(w.q)
     pairs = [(0, h) for h in range(32)]
     compare_decode(out, _oracle(w, cache, pairs), pairs=pairs)
+
+
+@pytest.mark.parametrize("Hq,H,lens", [(64, 8, [6000, 2500]), (16, 4, [7000, 4001, 15, 0])])
+def test_bf16_decode_small_batch_ragged(Hq, H, lens):
+    # GQA 8 and 4, a sequence shorter than one split, an empty one.
+    w = synth.make_workload(num_q_heads=Hq, num_kv_heads=H, head_dim=128, group_size=64, sink_len=0, window_len=0,
+                            seq_lens=lens, seed=Hq + len(lens))
+    cache = Bf16Cache(w)
+    cache.prefill()
+    out = cache.decode(w.q.cuda())
+    compare_decode(out, _oracle(w, cache))

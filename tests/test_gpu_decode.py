@@ -106,6 +106,28 @@ def test_decode_split_size_invariance():
         assert torch.max(torch.abs(o - outs[0])).item() <= 1e-4
 
 
+@pytest.mark.parametrize("Hq,H,pps", [(8, 2, 4), (16, 2, 0), (4, 4, 1)])
+def test_decode_batch_permutation_bit_identical(Hq, H, pps):
+    # Variable lengths give the INT2 splits of a decode different page counts and the
+    # CTAs of a sequence different places in the grid; a permuted batch must give every
+    # sequence bit-identical outputs, and both match the oracle.  Empty splits (short
+    # sequences) and sequences inside the sink included.
+    g = np.random.default_rng(Hq + pps)
+    lens = [3, 9, 40] + g.integers(41, 1500, 37).tolist()
+    w = synth.make_workload(num_q_heads=Hq, num_kv_heads=H, head_dim=128, group_size=64, sink_len=16, window_len=32,
+                            seq_lens=lens, seed=Hq * 3 + pps, device="cuda")
+    cache = _built(w, pps=pps)
+    out = cache.decode(w.q)
+    compare_decode(out, oracle_decode_on_gpu_cache(w, cache))
+    perm = torch.as_tensor(g.permutation(len(lens)), device="cuda")
+    out_p = torch.empty_like(out)
+    ok.oscar_decode(cache.dims, w.batch, w.max_seq_len, cache.pps, w.q[perm].contiguous(), cache.R_k, cache.R_v,
+                    cache.int2_pages, cache.scale_zero, cache.sink[perm].contiguous(), cache.window[perm].contiguous(),
+                    cache.page_table[perm].contiguous(), cache.seq_lens[perm].contiguous(), w.sink_len, w.window_len,
+                    0.0, out_p, cache.workspace(w.max_seq_len))
+    assert torch.equal(out_p, out[perm])
+
+
 def test_decode_page_shuffle_bit_identical():
     w = synth.make_workload(num_q_heads=4, num_kv_heads=1, head_dim=128, group_size=64, sink_len=8, window_len=16,
                             seq_lens=[900], seed=12, spare_pages=10)
