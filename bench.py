@@ -24,6 +24,7 @@ same computation), on the same workload and metric.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -38,6 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "oscar_decode HBM GB/s (% of peak) & tokens/s; INT2 vs BF16 decode speedup"
+E2E_IN_FLIGHT = 4  # steps of independent batches in flight in the end-to-end loop
 
 
 # --------------------------------------------------------------------------- helpers
@@ -140,6 +142,29 @@ class ClockSampler:
 
 
 _T0 = time.perf_counter()
+
+
+def cuda_runtime():
+    """The CUDA runtime library the OSCAR library links (already loaded in this
+    process), for the end-to-end loop's graph launches and events."""
+    ok = sys.modules["int2_rotated_kv_append_gb300"]
+    ok.load_library()
+    rt = None
+    for name in ("libcudart.so.13", "libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+            break
+        except OSError:
+            continue
+    if rt is None:
+        raise RuntimeError("libcudart not found")
+    P = ctypes.c_void_p
+    rt.cudaGraphLaunch.argtypes = [P, P]
+    rt.cudaEventRecord.argtypes = [P, P]
+    rt.cudaEventSynchronize.argtypes = [P]
+    rt.cudaEventDestroy.argtypes = [P]
+    rt.cudaEventCreateWithFlags.argtypes = [ctypes.POINTER(P), ctypes.c_uint]
+    return rt
 
 
 def log(msg: str):
@@ -433,15 +458,17 @@ class DecodeSetup:
             ok.oscar_bf16_decode(w.dims, B, msl_r[r], bf.pps, x["q"], bf.pages, x["bpt"], x["blens"], 0.0,
                                  x["out_bf"], ws_bf)
 
-        ws_alt = cache.workspace(max(lens_all)).clone()  # a second step in flight on another stream
+        # one workspace per step in flight (the end-to-end loop runs up to E2E_IN_FLIGHT
+        # steps of different replicas at once, on as many streams)
+        wss = [ws] + [cache.workspace(max(lens_all)).clone() for _ in range(min(E2E_IN_FLIGHT, NR) - 1)]
 
-        def step_r(r, alt=False):
+        def step_r(r, slot=0):
             # one call: the current tokens appended (INT2 pool, BF16 window rows), then the decode
             x = V[r]
             ok.oscar_append_decode(w.dims, B, msl_r[r], cache.pps, x["q"], x["k"], x["v"], cache.R_k, cache.R_v,
                                    cache.clip_k, cache.clip_v, x["slots"], cache.int2_pages, cache.scale_zero,
                                    x["sink"], x["win"], x["pt"], x["lens"], w.sink_len, w.window_len, 0.0, x["out"],
-                                   ws_alt if alt else ws)
+                                   wss[slot])
 
         def step(i):
             step_r(i % NR)
@@ -588,24 +615,29 @@ def run_ours(args, world, rank, local):
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     stream = torch.cuda.current_stream()
 
+    # One CUDA graph per cache replica holds a whole step: the host->device copy of
+    # its inputs, the oscar_append_decode call and the device->host copy of its
+    # output.  NF steps are in flight, as in a serving loop with NF independent
+    # batches: replica r's graph runs on stream r % NF with its own workspace, so the
+    # copies, launches and kernel ramps of one step overlap the others' kernels, and
+    # before launching step i the host waits until the output of step i - NF has
+    # landed in host memory.  The loop launches the graphs and records and waits on
+    # the events through the CUDA runtime (about 4 us of host time per launch,
+    # against 12 us through torch's graph replay with a stream switch).
+    NF = min(E2E_IN_FLIGHT, NR)
+
     def e2e_body(r):
         sl = slice(r * B, (r + 1) * B)
         x = V[r]
         stage[r * per_stage:(r + 1) * per_stage].copy_(stage_h[r * per_stage:(r + 1) * per_stage], non_blocking=True)
-        step_r(r, alt=(r % 2) == 1)
+        step_r(r, slot=r % NF)
         out_h[sl].copy_(x["out"], non_blocking=True)
 
-    # One CUDA graph per cache replica holds a whole step: the host->device copies
-    # of its inputs, the append, the decode and the device->host copy of its
-    # output.  Two steps are in flight, as in a serving loop with two independent
-    # batches: replica r's graph runs on stream r % 2 with its own workspace, so one
-    # step's copies and launch overlap the other's kernels, and before launching
-    # step i the host waits until the output of step i - 2 has landed in host memory.
-    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    streams = [torch.cuda.Stream() for _ in range(NF)]
     for s_ in streams:
         s_.wait_stream(stream)
     for r in range(NR):
-        with torch.cuda.stream(streams[r % 2]):
+        with torch.cuda.stream(streams[r % NF]):
             e2e_body(r)
     for s_ in streams:
         stream.wait_stream(s_)
@@ -613,20 +645,27 @@ def run_ours(args, world, rank, local):
     graphs = []
     for r in range(NR):
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=streams[r % 2]):
+        with torch.cuda.graph(g, stream=streams[r % NF]):
             e2e_body(r)
         graphs.append(g)
-
-    done = [torch.cuda.Event(), torch.cuda.Event()]
+    rt = cuda_runtime()
+    gexec = [ctypes.c_void_p(g.raw_cuda_graph_exec()) for g in graphs]
+    sptr = [ctypes.c_void_p(s_.cuda_stream) for s_ in streams]
+    done = []
+    for _ in range(NF):
+        ev = ctypes.c_void_p()
+        if rt.cudaEventCreateWithFlags(ctypes.byref(ev), 2) != 0:  # cudaEventDisableTiming
+            raise RuntimeError("cudaEventCreateWithFlags failed")
+        done.append(ev)
 
     def e2e_run(n):
         for i in range(n):
-            if i >= 2:
-                done[i % 2].synchronize()  # step i - 2's output is in host memory
+            k = i % NF
+            if i >= NF and rt.cudaEventSynchronize(done[k]) != 0:  # step i - NF's output is in host memory
+                raise RuntimeError("cudaEventSynchronize failed")
             r = i % NR
-            with torch.cuda.stream(streams[r % 2]):
-                graphs[r].replay()
-                done[i % 2].record(streams[r % 2])
+            if rt.cudaGraphLaunch(gexec[r], sptr[r % NF]) != 0 or rt.cudaEventRecord(done[k], sptr[r % NF]) != 0:
+                raise RuntimeError("cudaGraphLaunch / cudaEventRecord failed")
         torch.cuda.synchronize()
 
     e2e_run(min(50, E))
@@ -638,7 +677,9 @@ def run_ours(args, world, rank, local):
     h2d = per_stage  # q, k, v and slots of the step in one copy (256-byte aligned parts)
     d2h = B * Hq * D * 4
 
-    log(f"e2e: {e2e_ms * 1e3:.2f} us/step")
+    for ev in done:
+        rt.cudaEventDestroy(ev)
+    log(f"e2e: {e2e_ms * 1e3:.2f} us/step ({NF} steps in flight)")
     extra = {}
     for cfg in args.extra_configs:
         if cfg != args.config:
@@ -680,9 +721,11 @@ def run_ours(args, world, rank, local):
             "cpu_baseline": cpu,
             "e2e": {"value": whole_job_gbps(world, step_bytes, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "mode": "one CUDA graph per step (H2D inputs, oscar_append_decode, D2H output); two steps in "
-                             "flight on two streams (independent cache replicas, one workspace each), the host waits "
-                             "for step i-2's output before launching step i"},
+                    "in_flight": NF,
+                    "mode": f"one CUDA graph per step (H2D inputs, oscar_append_decode, D2H output) launched by "
+                            f"cudaGraphLaunch; {NF} steps in flight on {NF} streams (independent cache replicas, one "
+                            f"workspace each), the host waits for step i-{NF}'s output (cudaEventSynchronize) before "
+                            f"launching step i"},
             "gpu_launches": K * step_kernels,
             **extra,
             "append_workload": append_line,
