@@ -371,7 +371,7 @@ class DecodeSetup:
     library's appends, per-replica inputs in one staging block (q, k, v, slots of
     the current token), and the calls of a step (append, decode, BF16 decode)."""
 
-    def __init__(self, cfg, dev, l2, replicas=0, pps=-1):
+    def __init__(self, cfg, dev, l2, replicas=0, pps=-1, in_flight=1):
         import numpy as np
         import torch
 
@@ -458,9 +458,9 @@ class DecodeSetup:
             ok.oscar_bf16_decode(w.dims, B, msl_r[r], bf.pps, x["q"], bf.pages, x["bpt"], x["blens"], 0.0,
                                  x["out_bf"], ws_bf)
 
-        # one workspace per step in flight (the end-to-end loop runs up to E2E_IN_FLIGHT
+        # one workspace per step in flight (the end-to-end loop runs up to in_flight
         # steps of different replicas at once, on as many streams)
-        wss = [ws] + [cache.workspace(max(lens_all)).clone() for _ in range(min(E2E_IN_FLIGHT, NR) - 1)]
+        wss = [ws] + [cache.workspace(max(lens_all)).clone() for _ in range(min(in_flight, NR) - 1)]
 
         def step_r(r, slot=0):
             # one call: the current tokens appended (INT2 pool, BF16 window rows), then the decode
@@ -547,7 +547,7 @@ def run_ours(args, world, rank, local):
 
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
-    S = DecodeSetup(args.config, dev, l2, args.replicas, args.pps)
+    S = DecodeSetup(args.config, dev, l2, args.replicas, args.pps, in_flight=args.e2e_in_flight)
     w, cache, bf, NR, B, V = S.w, S.cache, S.bf, S.NR, S.B, S.V
     H, Hq, D = w.num_kv_heads, w.num_q_heads, w.head_dim
     lens_all = S.lens_all
@@ -624,7 +624,7 @@ def run_ours(args, world, rank, local):
     # landed in host memory.  The loop launches the graphs and records and waits on
     # the events through the CUDA runtime (about 4 us of host time per launch,
     # against 12 us through torch's graph replay with a stream switch).
-    NF = min(E2E_IN_FLIGHT, NR)
+    NF = min(args.e2e_in_flight, NR)
 
     def e2e_body(r):
         sl = slice(r * B, (r + 1) * B)
@@ -1019,12 +1019,16 @@ def main():
     ap.add_argument("--no-append", action="store_true", help="skip the append throughput workload")
     ap.add_argument("--no-extend", action="store_true", help="skip the extend (chunked prefill) workload")
     ap.add_argument("--no-calibrate", action="store_true", help="skip the offline calibration workload")
+    ap.add_argument("--e2e-in-flight", type=int, default=E2E_IN_FLIGHT,
+                    help="independent steps in flight in the end-to-end loop (one stream and workspace each)")
     args = ap.parse_args()
     args.extra_configs = [int(c) for c in args.extra_configs.split(",") if c.strip()]
     if any(c not in (1, 2, 3) for c in args.extra_configs):
         ap.error("--extra-configs takes workloads 1, 2, 3")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.e2e_in_flight < 1:
+        ap.error("--e2e-in-flight must be >= 1")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
