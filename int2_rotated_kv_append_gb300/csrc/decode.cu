@@ -29,8 +29,9 @@ cudaError_t merge(const Params& p, cudaStream_t stream) {
     auto k = merge_kernel<D, MODE, kMergeThreadsBatch, kMergeQBatch>;
     cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(k), kMergeSmemLimit);
     if (e != cudaSuccess) return e;
-    k<<<grid, kMergeThreadsBatch, smem, stream>>>(p);
-    return cudaGetLastError();
+    // launched as a programmatic dependent: its CTAs take the SMs the last split
+    // CTAs leave and stage R_v before their dependency wait
+    return launch_pdl(k, dim3(grid), dim3(kMergeThreadsBatch), smem, stream, p);
   }
   const int grid = p.B * p.H * (p.gqa / p.merge_qpc);
   // A grid of at most one CTA per SM (one query head per CTA) is launched early
