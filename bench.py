@@ -205,9 +205,9 @@ def workload_config(args, w, batch, seq_len, pps, l2_policy):
 # launch (q-rotation + split + merge kernels) on the batch-1 32K, batch-64 and
 # batch-4 131K workloads, from one ncu capture of the three kernels each (cold caches: the
 # split partials are re-read from DRAM there, from L2 in the timed loop).
-MEASURED_DECODE_TRAFFIC = {1: 557056 + 22292224 + 324608,
-                           2: 1073152 + 427723520 + 3890176 + 8043264,
-                           3: 614656 + 340504064 + 5701632 + 18010880}
+MEASURED_DECODE_TRAFFIC = {1: 556800 + 22836480 + 324864,
+                           2: 1073152 + 428750848 + 4023552 + 8043520,
+                           3: 616704 + 341499648 + 5570560 + 18014976}
 
 
 def cpu_model() -> str:
