@@ -10,15 +10,15 @@ namespace {
 
 // oscar_append_decode's fused form, in the CTA that attends the sink/window rows
 // holding the current token of sequence b (position L - 1, L = seq_lens[b]), for KV
-// head h: the token appended as
-// oscar_append_mixed appends it: K (minus the key offset, in fp32) and V rotated by
-// R_k[h] and R_v[h] (y_j = sum_i x_i R[i][j]: each warp sums a slice of the rows, the
-// slices are added in order), clipped, quantised per group of G channels (fp16 scale
-// (max - min) / 3 and zero min, codes rint((y - zero) / scale) clamped to 0..3, 0 when
-// the scale is 0) and written to the pool row of slot_mapping[b]; the BF16 rows (the
-// offset key rounded to bf16, and V) written to the sink row or the window slot of
-// position L - 1.  The INT2 splits never read that position (it is in the window), and
-// the BF16 rows are written before this CTA's own sink/window copies read them.
+// head h.  The token is appended as oscar_append_mixed appends it: K (minus the key
+// offset, in fp32) and V rotated by R_k[h] and R_v[h] (y_j = sum_i x_i R[i][j]: each
+// warp sums a slice of the rows, the slices are added in order), clipped, quantised
+// per group of G channels (fp16 scale (max - min) / 3 and zero min, codes
+// rint((y - zero) / scale) clamped to 0..3, 0 when the scale is 0) and written to the
+// pool row of slot_mapping[b]; the BF16 rows (the offset key rounded to bf16, and V)
+// go to the sink row or the window slot of position L - 1.  No INT2 split reads that
+// position (with a window it lies in the sink or the window), and the BF16 rows are
+// written before this CTA's own sink/window copies read them.
 template <int NW>
 __device__ __forceinline__ void fused_append_token(const Params& p, int b, int h, uint8_t* smem) {
   constexpr int T = NW * 32;      // 128 .. 512 threads
