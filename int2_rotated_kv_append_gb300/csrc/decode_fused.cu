@@ -28,11 +28,9 @@
 namespace oscar_dec {
 namespace {
 
-constexpr int kRBytes = kD * kD * 4;
 // page ids of one split staged in shared memory (the 8-warp form has room for more)
 template <int NW>
 constexpr int fused_max_pps() { return NW >= 16 ? 2048 : 4096; }
-constexpr int kFragWords = 44;      // per-lane QK operand words in shared memory (44: conflict-free rows)
 constexpr int kOwPitch = kD + 4;    // padded row of a warp's output in the merge area
 
 constexpr size_t cmax(size_t a, size_t b) { return a > b ? a : b; }
@@ -44,7 +42,6 @@ constexpr int fused_stages() { return (164 * 1024) / (NW * PageGeo<NG>::kStageBy
 
 template <int NT, int NG, int NW>
 struct FusedGeo {
-  static constexpr int kThreads = NW * 32;
   static constexpr int kStages = fused_stages<NG, NW>();
   static constexpr int kStageBytes = PageGeo<NG>::kStageBytes;
   static constexpr int kSzBytes = PageGeo<NG>::kSzBytes;
