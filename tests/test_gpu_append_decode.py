@@ -126,3 +126,58 @@ def test_append_decode_slot_out_of_range_is_flagged():
     assert ok.oscar_device_errors(reset=True) & ok.OSCAR_DEVERR_SLOT
     assert torch.equal(b.int2_pages, before)  # no code written
     assert torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("lens,W", [([900 + 37 * i for i in range(40)], 64), ([700], 128)])
+def test_append_decode_negative_slots_skip_the_token(lens, W):
+    # A negative slot skips the token entirely (no codes, no BF16 row), as in
+    # oscar_append_mixed: the general form (40 sequences) and the single-wave form.
+    w = synth.make_workload(num_q_heads=32, num_kv_heads=8, head_dim=128, group_size=64, sink_len=16, window_len=W,
+                            seq_lens=lens, seed=len(lens) + W)
+    a, b, cur, past = _step_pair(w)
+    d = torch.device("cuda")
+    ic = torch.as_tensor(cur)
+    slots = w.slot_mapping[ic].clone()
+    slots[::3] = -1
+    slots = slots.to(d)
+    ok.oscar_device_errors(reset=True)
+    ok.oscar_append_mixed(w.dims, w.k[ic].to(d), w.v[ic].to(d), a.R_k, a.R_v, a.clip_k, a.clip_v, None, slots,
+                          torch.arange(w.batch, dtype=torch.int32, device=d), w.tok_pos[ic].to(d), a.seq_lens,
+                          w.sink_len, w.window_len, a.int2_pages, a.scale_zero, a.sink, a.window, offset_k=a.offset_k)
+    out_a = a.decode(w.q.cuda())
+    out_b = torch.empty_like(out_a)
+    ok.oscar_append_decode(w.dims, w.batch, w.max_seq_len, b.pps, w.q.cuda(), w.k[ic].to(d).contiguous(),
+                           w.v[ic].to(d).contiguous(), b.R_k, b.R_v, b.clip_k, b.clip_v, slots, b.int2_pages,
+                           b.scale_zero, b.sink, b.window, b.page_table, b.seq_lens, w.sink_len, w.window_len, 0.0,
+                           out_b, b.workspace(w.max_seq_len), offset_k=b.offset_k)
+    torch.cuda.synchronize()
+    assert ok.oscar_device_errors(reset=True) == 0
+    assert torch.equal(a.sink, b.sink) and torch.equal(a.window, b.window)
+    assert torch.equal(a.int2_pages, b.int2_pages) and torch.equal(a.scale_zero, b.scale_zero)
+    assert torch.equal(out_a, out_b)
+
+
+def test_append_decode_general_form_slot_out_of_range_is_flagged():
+    lens = [600 + 31 * i for i in range(40)]
+    w = synth.make_workload(num_q_heads=32, num_kv_heads=8, head_dim=128, group_size=64, sink_len=16, window_len=64,
+                            seq_lens=lens, seed=91)
+    assert ok.oscar_decode_plan(w.dims, w.batch, w.max_seq_len, 0, 16, 64)["fused"] == 0
+    a, b, cur, past = _step_pair(w)
+    d = torch.device("cuda")
+    ic = torch.as_tensor(cur)
+    slots = w.slot_mapping[ic].clone()
+    slots[7] = w.num_pages * w.page_size  # one past the pool
+    before = b.int2_pages.clone()
+    out = torch.empty((w.batch, 32, 128), dtype=torch.float32, device=d)
+    ok.oscar_device_errors(reset=True)
+    ok.oscar_append_decode(w.dims, w.batch, w.max_seq_len, b.pps, w.q.cuda(), w.k[ic].to(d).contiguous(),
+                           w.v[ic].to(d).contiguous(), b.R_k, b.R_v, b.clip_k, b.clip_v, slots.to(d), b.int2_pages,
+                           b.scale_zero, b.sink, b.window, b.page_table, b.seq_lens, 16, 64, 0.0, out,
+                           b.workspace(w.max_seq_len))
+    torch.cuda.synchronize()
+    assert ok.oscar_device_errors(reset=True) & ok.OSCAR_DEVERR_SLOT
+    assert torch.isfinite(out).all()
+    # only pages holding the other tokens' slots change: the flagged token writes no code
+    changed = (b.int2_pages != before).view(w.num_pages, -1).any(dim=1).nonzero().flatten().cpu().numpy()
+    written = {int(s) // w.page_size for j, s in enumerate(slots.numpy()) if j != 7}
+    assert set(changed.tolist()) <= written
