@@ -230,7 +230,12 @@ oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, int32_t max
  * the sink or the window, never read from the INT2 pool by this decode),
  * the append runs inside the decode, in the CTA that attends the sink/window rows
  * holding that position, beside the INT2 splits instead of before them; otherwise
- * the two run one after the other.
+ * the two run one after the other.  Lengths are taken as given, as oscar_append_mixed
+ * takes positions: a sequence with seq_lens[b] < 1 has no sink/window row for its
+ * token (flagged OSCAR_DEVERR_POSITION; its codes are still written at the slot, and
+ * in the fused form that write is not ordered before this decode's reads of the same
+ * page), and one longer than max_seq_len is appended at position seq_lens[b] - 1
+ * while the decode flags the length.  A negative slot skips the token entirely.
  * (OSCAR project card "How it works": the new K/V are rotated, clipped and quantised
  * as they are appended, and the decode attends a BF16 recent window.)
  * Arguments: those of oscar_decode, plus

@@ -31,11 +31,13 @@ __device__ __forceinline__ void fused_append_token(const Params& p, int b, int h
   float* ys = cmx + 8;                         // [2][kD]: the clipped rotated values
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   grid_dep_wait();  // the previous step's reads of the window row this token replaces are over
-  const int L = __ldg(p.seq_lens + b);
-  if (L < 1 || L > p.max_seq_len) return;  // nothing to append (the decode flags the length)
-  const int pos = L - 1;
   const int64_t slot = __ldg(p.app_slots + b);  // a negative slot: the token is skipped entirely
   if (slot < 0) return;
+  const int L = __ldg(p.seq_lens + b);
+  const int pos = L - 1;
+  // as oscar_append_mixed at position L - 1: a sequence of length < 1 has no row for
+  // the token (flagged; its codes are still written at the slot)
+  if (pos < 0 && tid == 0) record_error(OSCAR_DEVERR_POSITION);
   for (int i = tid; i < kD; i += T) {  // (K|V, channel pair)
     const int kv = i >> 6, c2 = i & 63;
     const __nv_bfloat16* x = (kv ? p.app_v : p.app_k) + (static_cast<size_t>(b) * p.H + h) * kD;
@@ -49,7 +51,9 @@ __device__ __forceinline__ void fused_append_token(const Params& p, int b, int h
     xs[kv * kD + 2 * c2] = val.x;
     xs[kv * kD + 2 * c2 + 1] = val.y;
     __nv_bfloat16* dst = nullptr;
-    if (pos < p.S)
+    if (pos < 0)
+      dst = nullptr;
+    else if (pos < p.S)
       dst = p.app_sink + (((static_cast<size_t>(b) * 2 + kv) * p.H + h) * p.S + pos) * kD;
     else if (p.W > 0 && pos >= max(p.S, L - p.W))
       dst = p.app_win + (((static_cast<size_t>(b) * 2 + kv) * p.H + h) * p.W + pos % p.W) * kD;
@@ -131,14 +135,15 @@ __device__ __forceinline__ void fused_append_token(const Params& p, int b, int h
 
 // The index of the dense CTA (of `per` 16-row sink/window pages each, in the order
 // dense_part takes them: sink pages, then window pages) whose pages hold position
-// L - 1 of sequence b, or -1 when the sequence has no such row (L outside
-// 1 .. max_seq_len, or the position past the sink with no window).  Waits for the
+// L - 1 of sequence b (L = seq_lens[b] as given, as oscar_append_mixed takes it);
+// CTA 0 when L < 1 (the token has no row: that CTA writes its codes and flags it);
+// -1 when the position is past the sink and there is no window.  Waits for the
 // preceding kernel first (the lengths are read after it, as everywhere).
 __device__ __forceinline__ int current_token_dense_cta(const Params& p, int b, int per) {
   grid_dep_launch_dependents();
   grid_dep_wait();
   const int L = __ldg(p.seq_lens + b);
-  if (L < 1 || L > p.max_seq_len) return -1;
+  if (L < 1) return 0;
   const int pos = L - 1;
   if (pos < p.S) return (pos / kPageSize) / per;
   if (p.W < 1) return -1;

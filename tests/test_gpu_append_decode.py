@@ -181,3 +181,59 @@ def test_append_decode_general_form_slot_out_of_range_is_flagged():
     changed = (b.int2_pages != before).view(w.num_pages, -1).any(dim=1).nonzero().flatten().cpu().numpy()
     written = {int(s) // w.page_size for j, s in enumerate(slots.numpy()) if j != 7}
     assert set(changed.tolist()) <= written
+
+
+@pytest.mark.parametrize("lens,Hq,H", [([700 + 37 * i for i in range(39)] + [0], 32, 8), ([0, 900], 8, 2)])
+def test_append_decode_lengths_out_of_range_follow_append_mixed(lens, Hq, H):
+    # Lengths are taken as oscar_append_mixed takes positions: a sequence of length 0
+    # gets no sink/window row (flagged) but its codes at the slot (here in the page
+    # that sequence owns and no decode reads), and with max_seq_len below the longest
+    # sequence that one is appended at its length - 1 while the decode flags the length.
+    # The general form (40 sequences) and the single-wave form, each against the two calls.
+    w = synth.make_workload(num_q_heads=Hq, num_kv_heads=H, head_dim=128, group_size=64, sink_len=16, window_len=48,
+                            seq_lens=lens, seed=len(lens) + 5)
+    d = torch.device("cuda")
+    B = w.batch
+    lens_np = w.seq_lens.numpy()
+    pos, seq = w.tok_pos.numpy(), w.tok_seq.numpy()
+    zb = int(np.argmin(lens_np))
+    cur_idx = {b: int(np.nonzero((seq == b) & (pos == lens_np[b] - 1))[0][0]) for b in range(B) if lens_np[b] > 0}
+    past = np.setdiff1d(np.arange(len(pos)), list(cur_idx.values()))
+    k_cur = torch.stack([w.k[cur_idx.get(b, 0)] for b in range(B)]).to(d).contiguous()
+    v_cur = torch.stack([w.v[cur_idx.get(b, 0)] for b in range(B)]).to(d).contiguous()
+    slots = torch.tensor([int(w.slot_mapping[cur_idx[b]]) if b in cur_idx else int(w.page_table[zb, 0]) * w.page_size
+                          for b in range(B)], dtype=torch.int64, device=d)
+    positions = torch.tensor([int(lens_np[b]) - 1 for b in range(B)], dtype=torch.int32, device=d)
+    msl = int(lens_np.max()) - 5
+    caches = []
+    for _ in range(2):
+        c = Int2Cache(w)
+        c.sink = torch.zeros((B, 2, H, 16, 128), dtype=torch.bfloat16, device=d)
+        c.window = torch.zeros((B, 2, H, 48, 128), dtype=torch.bfloat16, device=d)
+        ip = torch.as_tensor(past)
+        ok.oscar_append_mixed(w.dims, w.k[ip].to(d), w.v[ip].to(d), c.R_k, c.R_v, c.clip_k, c.clip_v, None,
+                              w.slot_mapping[ip].to(d), w.tok_seq[ip].to(d), w.tok_pos[ip].to(d),
+                              torch.as_tensor(np.maximum(lens_np - 1, 0), dtype=torch.int32).to(d), 16, 48,
+                              c.int2_pages, c.scale_zero, c.sink, c.window)
+        caches.append(c)
+    a, b = caches
+    assert ok.oscar_decode_plan(w.dims, B, msl, 0, 16, 48)["fused"] == (1 if B == 2 else 0)
+    torch.cuda.synchronize()
+    ok.oscar_device_errors(reset=True)
+    ok.oscar_append_mixed(w.dims, k_cur, v_cur, a.R_k, a.R_v, a.clip_k, a.clip_v, None, slots,
+                          torch.arange(B, dtype=torch.int32, device=d), positions, a.seq_lens, 16, 48, a.int2_pages,
+                          a.scale_zero, a.sink, a.window)
+    out_a = a.decode(w.q.cuda(), max_seq_len=msl)
+    torch.cuda.synchronize()
+    flags_a = ok.oscar_device_errors(reset=True)
+    out_b = torch.empty_like(out_a)
+    ok.oscar_append_decode(w.dims, B, msl, b.pps, w.q.cuda(), k_cur, v_cur, b.R_k, b.R_v, b.clip_k, b.clip_v, slots,
+                           b.int2_pages, b.scale_zero, b.sink, b.window, b.page_table, b.seq_lens, 16, 48, 0.0, out_b,
+                           b.workspace(msl))
+    torch.cuda.synchronize()
+    flags_b = ok.oscar_device_errors(reset=True)
+    assert flags_a & ok.OSCAR_DEVERR_POSITION and flags_a & ok.OSCAR_DEVERR_SEQ_LEN
+    assert flags_b == flags_a
+    assert torch.equal(a.sink, b.sink) and torch.equal(a.window, b.window)
+    assert torch.equal(a.int2_pages, b.int2_pages) and torch.equal(a.scale_zero, b.scale_zero)
+    assert torch.equal(out_a, out_b)
