@@ -225,7 +225,10 @@ oscar_status_t oscar_decode(const oscar_dims_t* dims, int32_t batch, int32_t max
  * seq_lens[b] - 1 of sequence b: INT2 codes and scale/zero into the pool at
  * slot_mapping[b], the BF16 row into the sink or the window ring), then the queries
  * are decoded (exactly oscar_decode, the appended token included).  The result equals
- * those two calls.  When window_len >= 1 and the decode runs on its tensor-core
+ * those two calls, bit for bit for up to 512 sequences (the append forms x.R with
+ * the FP32 operations of oscar_append_mixed's few-token kernel; for more tokens that
+ * call forms x.R on tensor cores, so a code can differ where x.R lies within
+ * rounding error of a code boundary).  When window_len >= 1 and the decode runs on its tensor-core
  * kernels (head_dim 128, group 64 or 128, GQA 1..8; the appended position is then in
  * the sink or the window, never read from the INT2 pool by this decode),
  * the append runs inside the decode, in the CTA that attends the sink/window rows

@@ -11,8 +11,8 @@ namespace {
 // oscar_append_decode's fused form, in the CTA that attends the sink/window rows
 // holding the current token of sequence b (position L - 1, L = seq_lens[b]), for KV
 // head h.  The token is appended as oscar_append_mixed appends it: K (minus the key
-// offset, in fp32) and V rotated by R_k[h] and R_v[h] (y_j = sum_i x_i R[i][j]: each
-// warp sums a slice of the rows, the slices are added in order), clipped, quantised
+// offset, in fp32) and V rotated by R_k[h] and R_v[h] (y_j = sum_i x_i R[i][j], in
+// the few-token append kernel's order of operations), clipped, quantised
 // per group of G channels (fp16 scale (max - min) / 3 and zero min, codes
 // rint((y - zero) / scale) clamped to 0..3, 0 when the scale is 0) and written to the
 // pool row of slot_mapping[b]; the BF16 rows (the offset key rounded to bf16, and V)
@@ -21,12 +21,15 @@ namespace {
 // written before this CTA's own sink/window copies read them.
 template <int NW>
 __device__ __forceinline__ void fused_append_token(const Params& p, int b, int h, uint8_t* smem) {
-  constexpr int T = NW * 32;      // 128 .. 512 threads
-  constexpr int kRows = kD / NW;  // rows of R per warp
-  constexpr int kChunk = kRows < 16 ? kRows : 16;
+  constexpr int T = NW * 32;  // 128 .. 512 threads
+  // x . R summed as the few-token append kernel sums it, so that the codes equal
+  // those of oscar_append_mixed on the same token bit for bit: 8 slices of 16 rows,
+  // each an fma chain in row order from 0 (lane l: channels 4l .. 4l + 3), the
+  // slices then added in order.  Warp w takes the (K|V, slice) tasks w, w + NW, ...
+  constexpr int kSlices = 8, kSliceRows = kD / kSlices, kChunk = 8;
   float* xs = reinterpret_cast<float*>(smem);  // [2][kD]: the token's K (offset) and V
-  float* part = xs + 2 * kD;                   // [2][NW][kD]: per-warp partial sums
-  float* cmn = part + 2 * NW * kD;             // [2][4]: min of each 32-channel chunk
+  float* part = xs + 2 * kD;                   // [2][kSlices][kD]: per-slice partial sums
+  float* cmn = part + 2 * kSlices * kD;        // [2][4]: min of each 32-channel chunk
   float* cmx = cmn + 8;                        // [2][4]: max
   float* ys = cmx + 8;                         // [2][kD]: the clipped rotated values
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -62,25 +65,26 @@ __device__ __forceinline__ void fused_append_token(const Params& p, int b, int h
   asm volatile("fence.proxy.async.global;" ::: "memory");  // the rows, for this CTA's bulk copies
   __syncthreads();
 #pragma unroll 1
-  for (int kv = 0; kv < 2; ++kv) {
+  for (int task = warp; task < 2 * kSlices; task += NW) {
+    const int kv = task / kSlices, sl = task % kSlices;
     const float* R = (kv ? p.R_v : p.R_k) + static_cast<size_t>(h) * kD * kD +
-                     static_cast<size_t>(warp * kRows) * kD + 4 * lane;
+                     static_cast<size_t>(sl * kSliceRows) * kD + 4 * lane;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-    for (int r0 = 0; r0 < kRows; r0 += kChunk) {  // rows in chunks of at most 16 (registers)
+    for (int r0 = 0; r0 < kSliceRows; r0 += kChunk) {  // the rows' loads in two rounds (registers)
       float4 rr[kChunk];
 #pragma unroll
       for (int r = 0; r < kChunk; ++r) rr[r] = __ldg(reinterpret_cast<const float4*>(R + (r0 + r) * kD));
 #pragma unroll
       for (int r = 0; r < kChunk; ++r) {
-        const float xv = xs[kv * kD + warp * kRows + r0 + r];
+        const float xv = xs[kv * kD + sl * kSliceRows + r0 + r];
         acc.x = fmaf(xv, rr[r].x, acc.x);
         acc.y = fmaf(xv, rr[r].y, acc.y);
         acc.z = fmaf(xv, rr[r].z, acc.z);
         acc.w = fmaf(xv, rr[r].w, acc.w);
       }
     }
-    *reinterpret_cast<float4*>(part + (kv * NW + warp) * kD + 4 * lane) = acc;
+    *reinterpret_cast<float4*>(part + (kv * kSlices + sl) * kD + 4 * lane) = acc;
   }
   __syncthreads();
   // items (K|V, channel) 0 .. 255 in blocks of T threads; a warp holds 32 consecutive channels
@@ -88,7 +92,8 @@ __device__ __forceinline__ void fused_append_token(const Params& p, int b, int h
   for (int it = tid; it < 2 * kD; it += T) {
     const int kv = it >> 7, j = it & (kD - 1);
     float y = 0.f;
-    for (int w = 0; w < NW; ++w) y += part[(kv * NW + w) * kD + j];
+#pragma unroll
+    for (int sl = 0; sl < kSlices; ++sl) y += part[(kv * kSlices + sl) * kD + j];
     const float cl = __ldg((kv ? p.app_clip_v : p.app_clip_k) + static_cast<size_t>(h) * kD + j);
     y = fminf(fmaxf(y, -cl), cl);
     ys[it] = y;

@@ -237,3 +237,74 @@ def test_append_decode_lengths_out_of_range_follow_append_mixed(lens, Hq, H):
     assert torch.equal(a.sink, b.sink) and torch.equal(a.window, b.window)
     assert torch.equal(a.int2_pages, b.int2_pages) and torch.equal(a.scale_zero, b.scale_zero)
     assert torch.equal(out_a, out_b)
+
+
+@pytest.mark.parametrize("lens0,fused", [([3000], 1), ([500 + 41 * i for i in range(40)], 0)])
+def test_append_decode_loop_of_steps(lens0, fused):
+    # 40 consecutive decode steps per sequence with a 32-row window: tokens pass
+    # through the window ring and leave it for the INT2 bulk, which each step reads
+    # from codes written by earlier steps.  Every step equals the two calls; at the
+    # end every code matches the oracle's append, the sink and window hold the
+    # expected bf16 rows, and the last step's output matches the oracle's decode.
+    N, S, W = 40, 16, 32
+    lens = [L + N for L in lens0]
+    w = synth.make_workload(num_q_heads=32, num_kv_heads=8, head_dim=128, group_size=64, sink_len=S, window_len=W,
+                            seq_lens=lens, seed=len(lens0) + 123)
+    d = torch.device("cuda")
+    B = w.batch
+    L0 = np.array(lens0)
+    pos, seq = w.tok_pos.numpy(), w.tok_seq.numpy()
+    past = np.nonzero(pos < L0[seq])[0]
+    caches = []
+    for _ in range(2):
+        c = Int2Cache(w)
+        c.sink = torch.zeros((B, 2, 8, S, 128), dtype=torch.bfloat16, device=d)
+        c.window = torch.zeros((B, 2, 8, W, 128), dtype=torch.bfloat16, device=d)
+        ip = torch.as_tensor(past)
+        ok.oscar_append_mixed(w.dims, w.k[ip].to(d), w.v[ip].to(d), c.R_k, c.R_v, c.clip_k, c.clip_v, None,
+                              w.slot_mapping[ip].to(d), w.tok_seq[ip].to(d), w.tok_pos[ip].to(d),
+                              torch.as_tensor(L0, dtype=torch.int32).to(d), S, W, c.int2_pages, c.scale_zero,
+                              c.sink, c.window)
+        caches.append(c)
+    a, b = caches
+    msl = w.max_seq_len
+    assert ok.oscar_decode_plan(w.dims, B, msl, 0, S, W)["fused"] == fused
+    q = w.q.cuda()
+    ok.oscar_device_errors(reset=True)
+    for n in range(N):
+        cur = torch.as_tensor([int(np.nonzero((seq == bb) & (pos == L0[bb] + n))[0][0]) for bb in range(B)])
+        sl = torch.as_tensor(L0 + n + 1, dtype=torch.int32).to(d)
+        k_cur, v_cur, s_cur = w.k[cur].to(d).contiguous(), w.v[cur].to(d).contiguous(), w.slot_mapping[cur].to(d)
+        ok.oscar_append_mixed(w.dims, k_cur, v_cur, a.R_k, a.R_v, a.clip_k, a.clip_v, None, s_cur,
+                              torch.arange(B, dtype=torch.int32, device=d), w.tok_pos[cur].to(d), sl, S, W,
+                              a.int2_pages, a.scale_zero, a.sink, a.window)
+        out_a = a.decode(q, seq_lens=sl)
+        out_b = torch.empty_like(out_a)
+        ok.oscar_append_decode(w.dims, B, msl, b.pps, q, k_cur, v_cur, b.R_k, b.R_v, b.clip_k, b.clip_v, s_cur,
+                               b.int2_pages, b.scale_zero, b.sink, b.window, b.page_table, sl, S, W, 0.0, out_b,
+                               b.workspace(msl))
+        torch.cuda.synchronize()
+        assert torch.equal(out_a, out_b), f"step {n}"
+    assert ok.oscar_device_errors(reset=True) == 0
+    assert torch.equal(a.sink, b.sink) and torch.equal(a.window, b.window)
+    # the codes of every token appended by the steps and of 3000 earlier tokens
+    # against the oracle's append (every slot was written)
+    codes, sz = pools_to_host(b)
+    loop_tok = np.nonzero(pos >= L0[seq])[0]
+    sample = np.concatenate([loop_tok, np.random.default_rng(5).choice(past, min(3000, len(past)), replace=False)])
+    check_append(w, codes, sz, w.k, w.v, w.slot_mapping.numpy(), sample=sample,
+                 written_slots=w.slot_mapping.numpy())
+    # sink rows: positions 0 .. S-1; window slot r: the latest position p = r (mod W)
+    kb, vb = w.k.view(torch.int16).numpy(), w.v.view(torch.int16).numpy()
+    sink_h, win_h = b.sink.view(torch.int16).cpu().numpy(), b.window.view(torch.int16).cpu().numpy()
+    for bb in range(B):
+        L = lens[bb]
+        idx = {int(p): i for i, p in zip(np.nonzero(seq == bb)[0], pos[seq == bb])}
+        for p in range(S):
+            assert np.array_equal(sink_h[bb, 0, :, p], kb[idx[p]]) and np.array_equal(sink_h[bb, 1, :, p], vb[idx[p]])
+        for r in range(W):
+            p = L - 1 - ((L - 1 - r) % W)
+            assert np.array_equal(win_h[bb, 0, :, r], kb[idx[p]]) and np.array_equal(win_h[bb, 1, :, r], vb[idx[p]])
+    # the last step's output against the oracle's decode of the final cache
+    pairs = None if B == 1 else [(bb, (7 * bb + 3) % 32) for bb in range(0, B, 2)]
+    compare_decode(out_b, oracle_decode_on_gpu_cache(w, b, pairs=pairs), pairs=pairs)
