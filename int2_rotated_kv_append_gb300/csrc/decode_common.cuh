@@ -27,6 +27,7 @@ enum Mode { kMixed = 0, kBf16Paged = 1 };
 
 constexpr int kDenseMmaPages = 8;  // 16-row sink/window pages per dense split of the tensor-core kernel
 constexpr int kMmaMaxPps = 256;    // largest split the tensor-core kernels stage page ids for
+constexpr int kMinFusedSplits = 8; // fewest INT2 split CTAs per unit for the automatic fused plan
 
 struct Plan {
   int pps = 0;         // pages per INT2 (or BF16-paged) split
@@ -162,7 +163,8 @@ int dense_splits(int S, int W, int max_seq_len, bool mma) {
 // Fused single-wave plan of a decode (no extend rows): unit (sequence, KV head) u
 // gets n_s INT2 split CTAs over its bulk pages [S/16, ceil(max(S, max_seq_len - W)/16))
 // and one BF16 CTA when S + W > 0; used when every unit's CTAs fit one wave of the
-// fused kernel (about one CTA per SM) and a split's page ids fit its table.
+// fused kernel (about one CTA per SM), a split's page ids fit its table and, with
+// the split size chosen here, a unit gets at least kMinFusedSplits split CTAs.
 bool make_fused_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req, int S, int W, Plan* p) {
   const int gqa = d->num_q_heads / d->num_kv_heads;
   if (B <= 0 || !int2_fused_shape(d->head_dim, d->group_size, gqa)) return false;
@@ -175,7 +177,12 @@ bool make_fused_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req,
   int pps = pps_req;
   if (pps == 0) {
     long long n_s = slots / units - n_d;
-    if (n_s < 1) return false;
+    // With fewer than kMinFusedSplits split CTAs per unit the general split grid
+    // (several CTAs per SM) is faster.  Measured at 32K tokens, GQA 4, fused against
+    // general: batch 2 (8 splits) 22.1 / 24.0 us, batch 3 (5) 32.9 / 31.0 us, batch 4
+    // (3) 48.0 / 38.0 us, batch 8 (1) 142.9 / 68.1 us; batch 1 at 131K (18 splits,
+    // 455 pages each) 54.5 / 63.6 us at GQA 8 and 35.2 / 36.8 us at GQA 4.
+    if (n_s < kMinFusedSplits) return false;
     pps = static_cast<int>((nb + n_s - 1) / n_s);
     if (pps < 1) pps = 1;
   }

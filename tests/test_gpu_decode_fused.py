@@ -32,9 +32,12 @@ def test_plan_fused_for_small_batches_only():
         dims = ok.make_dims(Hq, 8, 128, 16, 64, B * (L // 16 + 1), L // 16 + 1)
         return ok.oscar_decode_plan(dims, B, L, pps, 64, W)
     assert plan(32, 1, 32768, 128)["fused"] == 1           # batch 1, 32K
+    assert plan(32, 2, 32768, 128)["fused"] == 1           # batch 2, 32K: 8 splits of 255 pages
+    assert plan(32, 3, 32768, 128)["fused"] == 0           # batch 3: 5 splits per unit, the general grid
     assert plan(32, 64, 16384, 128)["fused"] == 0          # 512 (sequence, KV head) units: more than one wave
-    p3 = plan(64, 4, 131072, 256)                          # batch 4, 131K, GQA 8
-    assert p3["fused"] == 1 and p3["splits"] >= 2
+    assert plan(64, 4, 131072, 256)["fused"] == 0          # batch 4, 131K, GQA 8: 3 splits per unit
+    assert plan(64, 1, 131072, 256)["fused"] == 1          # batch 1, 131K, GQA 8: 18 splits of 455 pages
+    assert plan(64, 4, 131072, 256, pps=2800)["fused"] == 1  # the same with the split size given
     assert plan(32, 1, 32768, 128, pps=1)["fused"] == 0    # 2036 splits of one page: more than one wave
 
 
@@ -53,9 +56,11 @@ def test_fused_split_counts(pps):
                                     (7, 1, 64)])
 def test_fused_gqa_shapes_and_edge_lengths(Hq, H, G):
     S, W = 5, 19
-    lens = [0, 1, S - 1, S + W + 1, 16 * 9 + 3, 3000]
+    # as many sequences as keep 8 split CTAs per (sequence, KV head) unit (the
+    # automatic fused plan): the edge lengths with 4 KV heads or fewer
+    lens = [3000, S + W + 1, 0, 1, S - 1, 16 * 9 + 3]
     w = synth.make_workload(num_q_heads=Hq, num_kv_heads=H, head_dim=128, group_size=G, sink_len=S, window_len=W,
-                            seq_lens=lens[:max(1, 152 // (2 * H))], seed=Hq + H + G, spare_pages=3)
+                            seq_lens=lens[:max(1, 152 // (9 * H))], seed=Hq + H + G, spare_pages=3)
     assert _plan(w, 0)["fused"] == 1
     cache = _built(w)
     out = cache.decode(w.q.cuda())
