@@ -28,6 +28,8 @@ enum Mode { kMixed = 0, kBf16Paged = 1 };
 constexpr int kDenseMmaPages = 8;  // 16-row sink/window pages per dense split of the tensor-core kernel
 constexpr int kMmaMaxPps = 256;    // largest split the tensor-core kernels stage page ids for
 constexpr int kMinFusedSplits = 8; // fewest INT2 split CTAs per unit for the automatic fused plan
+constexpr int kFusedMaxPps = 960;      // most pages per split CTA for that plan (16 warps, GQA <= 4)
+constexpr int kFusedMaxPpsGqa8 = 512;  // the same for GQA 8 (8 warps)
 
 struct Plan {
   int pps = 0;         // pages per INT2 (or BF16-paged) split
@@ -164,7 +166,8 @@ int dense_splits(int S, int W, int max_seq_len, bool mma) {
 // gets n_s INT2 split CTAs over its bulk pages [S/16, ceil(max(S, max_seq_len - W)/16))
 // and one BF16 CTA when S + W > 0; used when every unit's CTAs fit one wave of the
 // fused kernel (about one CTA per SM), a split's page ids fit its table and, with
-// the split size chosen here, a unit gets at least kMinFusedSplits split CTAs.
+// the split size chosen here, a unit gets at least kMinFusedSplits split CTAs of at
+// most kFusedMaxPps (GQA 8: kFusedMaxPpsGqa8) pages.
 bool make_fused_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req, int S, int W, Plan* p) {
   const int gqa = d->num_q_heads / d->num_kv_heads;
   if (B <= 0 || !int2_fused_shape(d->head_dim, d->group_size, gqa)) return false;
@@ -185,6 +188,12 @@ bool make_fused_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req,
     if (n_s < kMinFusedSplits) return false;
     pps = static_cast<int>((nb + n_s - 1) / n_s);
     if (pps < 1) pps = 1;
+    // ... and with more than about 60 pages per warp of a split CTA (16 warps at GQA
+    // <= 4, 8 at GQA 8): fused against general, batch 2 at 131K 71.3 / 63.4 us (GQA 4,
+    // 1023 pages per split) and 117.7 / 98.0 us (GQA 8, 1022), batch 1 at 262K, GQA 8
+    // (910) 105.4 / 96.8 us; the fused form led with batch 1 at 262K, GQA 4 (910
+    // pages: 63.8 / 64.9 us) and batch 2 at 64K, GQA 8 (510 pages: 58.1 / 63.4 us)
+    if (pps > (gqa > 4 ? kFusedMaxPpsGqa8 : kFusedMaxPps)) return false;
   }
   const int n_s = nb > 0 ? (nb + pps - 1) / pps : 1;
   if (pps > int2_fused_max_pps(gqa) || units * (n_s + n_d) > slots) return false;
