@@ -159,7 +159,7 @@ int dense_splits(int S, int W, int max_seq_len, bool mma) {
 // Split plan.  With pages_per_split == 0 the split size is chosen so that the
 // paged splits of the whole batch fill about one wave of resident CTAs
 // (ctas_per_sm x SMs, the sink/window splits counted; 5/3 x SMs for the BF16
-// reference), 4..128 pages per split.
+// reference), 4..128 pages per split; at the 128-page cap, whole waves.
 // The tensor-core split kernels cover head_dim 128 (INT2: group 64 or 128) and
 // splits of at most kMmaMaxPps pages.
 // Fused single-wave plan of a decode (no extend rows): unit (sequence, KV head) u
@@ -231,11 +231,27 @@ bool make_plan(const oscar_dims_t* d, int B, int max_seq_len, int pps_req, int S
     // that fit (B=1, 32K tokens: 31 splits instead of 57, 28.6 against 30.0 us for
     // the call; fewer partials to merge, each CTA streaming longer)
     if (mode == kBf16Paged) slots = static_cast<long long>(num_sms()) * 5 / 3;
+    const long long total = mode == kBf16Paged ? slots : slots + units * p->n_dense;  // CTA slots of a wave
+    const long long dense = units * p->n_dense;
     if (slots < units) slots = units;
     const long long splits = (slots + units - 1) / units;
     long long want = (max_pages + splits - 1) / splits;
     if (want < 4) want = 4;
-    if (want > 128) want = 128;
+    const bool capped = want >= 128;
+    if (capped) want = 128;
+    // At the 128-page cap and more than one wave: fill k whole waves instead of
+    // spilling a few CTAs into one more (32K tokens, batch 8: 68.3 -> 65.9 us; 8K
+    // tokens, batch 16: 56.5 -> 47.9 us; 131K, batch 2, GQA 8: 98.1 -> 93.9 us).
+    // Below the cap one wave that a few sink/window CTAs overflow measured best.
+    const long long n_at = (max_pages + want - 1) / want;
+    if (capped && units * n_at + dense > total) {
+      const long long k = (units * n_at + dense + total - 1) / total;
+      const long long sk = (k * total - dense) / units;
+      if (sk > n_at) {
+        want = (max_pages + sk - 1) / sk;
+        if (want < 4) want = 4;
+      }
+    }
     pps = static_cast<int>(want);
   }
   p->mma = shape_mma && pps <= kMmaMaxPps ? 1 : 0;
