@@ -206,9 +206,9 @@ def workload_config(args, w, batch, seq_len, pps, l2_policy):
 # launch (q-rotation + split + merge kernels) on the batch-1 32K, batch-64 and
 # batch-4 131K workloads, from one ncu capture of the three kernels each (cold caches: the
 # split partials are re-read from DRAM there, from L2 in the timed loop).
-MEASURED_DECODE_TRAFFIC = {1: 556800 + 22836480 + 324864,
-                           2: 1073152 + 428750848 + 4023552 + 8043520,
-                           3: 616704 + 341499648 + 5570560 + 18014976}
+MEASURED_DECODE_TRAFFIC = {1: 556288 + 22832896 + 324864,
+                           2: 1072640 + 428843264 + 4089088 + 8044544,
+                           3: 613888 + 341584384 + 5817856 + 18014464}
 
 
 def cpu_model() -> str:
