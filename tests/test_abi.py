@@ -207,3 +207,19 @@ def test_decode_plan_respects_grid_limits(lib):
     assert lib.oscar_decode_workspace_bytes(ctypes.byref(d), 1, 70000 * 16, 1, 64, 128) == 0
     assert lib.oscar_decode_workspace_bytes(ctypes.byref(d), 1, 70000 * 16, 2, 64, 128) > 0
     assert _decode(lib, d, batch=1, msl=70000 * 16, pps=1, S=64, W=128) == ok.OSCAR_ERR_INVALID_ARG
+
+
+def test_decode_plan_fused_form_rules(lib):
+    # Host logic only (no kernel runs): the automatic split size takes the fused
+    # single-wave form only with at least 8 split CTAs per (sequence, KV head) of at
+    # most 960 pages (512 at GQA 8); a split size given by the caller is kept.
+    def plan(Hq, B, L, W, pps=0):
+        dims = ok.make_dims(Hq, 8, 128, 16, 64, B * (L // 16 + 1), L // 16 + 1)
+        return ok.oscar_decode_plan(dims, B, L, pps, 64, W)
+    p1 = plan(32, 1, 32768, 128)
+    assert p1["fused"] == 1 and p1["splits"] >= 8 and p1["pages_per_split"] <= 960
+    assert plan(32, 3, 32768, 128)["fused"] == 0      # about 5 splits per unit
+    assert plan(32, 2, 131072, 128)["fused"] == 0     # about 1023 pages per split
+    assert plan(64, 2, 131072, 256)["fused"] == 0     # GQA 8: more than 512 pages per split
+    assert plan(64, 1, 131072, 256)["fused"] == 1     # GQA 8: about 455 pages per split
+    assert plan(64, 4, 131072, 256, pps=2800)["fused"] == 1

@@ -106,6 +106,18 @@ def test_decode_split_size_invariance():
         assert torch.max(torch.abs(o - outs[0])).item() <= 1e-4
 
 
+def test_plan_fills_whole_waves_at_the_split_cap():
+    # batch 16 at 8K: one wave at the 128-page cap would be 512 split CTAs and 256
+    # sink/window CTAs, a few more than one wave; the plan takes smaller splits that
+    # fill two waves instead
+    dims = ok.make_dims(32, 8, 128, 16, 64, 16 * 513, 513)
+    plan = ok.oscar_decode_plan(dims, 16, 8192, 0, 64, 128)
+    assert plan["fused"] == 0 and plan["pages_per_split"] < 128, plan
+    # batch 64 with 16K sequences keeps splits near the cap
+    dims = ok.make_dims(32, 8, 128, 16, 64, 64 * 1025, 1025)
+    assert ok.oscar_decode_plan(dims, 64, 16384, 0, 64, 128)["pages_per_split"] >= 120
+
+
 @pytest.mark.parametrize("Hq,H,pps", [(8, 2, 4), (16, 2, 0), (4, 4, 1)])
 def test_decode_batch_permutation_bit_identical(Hq, H, pps):
     # Variable lengths give the INT2 splits of a decode different page counts and the
